@@ -1,0 +1,292 @@
+/*
+ * zero.h -- C ABI of the GB300 ZeRO-1/2 gradient-and-optimizer step.
+ *
+ * One process, one GPU. W data-parallel ranks are simulated: each rank's full
+ * low-precision gradient set is a separate buffer in HBM. One step
+ *   reduce-scatters those W buffers (each rank's shard of every bucket is the
+ *   sum over the W ranks), checks the reduced values for inf/NaN, forms the
+ *   global gradient norm and clip coefficient, advances the loss-scale state
+ *   machine, applies AdamW to each rank's fp32 master/m/v shard and casts the
+ *   updated parameters back into one flat low-precision buffer (the
+ *   all-gather).
+ *
+ * Sources (page title, section):
+ *   [DO]  leetllm "Deep dive: Megatron", "Distributed optimizer: trade
+ *         replicated state for collectives" -- reduce-scatter, local fp32
+ *         update, all-gather; equal contiguous shards; contiguous bucketed
+ *         buffers; reduction scaled to the loss normalisation; byte ledger.
+ *   [ND]  "nano-deepspeed (Teaching Edition)", "2. Current Feature Range" --
+ *         ZeRO stages 1/2, AdamW only, FP16 dynamic loss scaling and the bf16
+ *         path, stage 2 as packed all-reduce plus local scatter-back;
+ *         "9. Experimental Results" -- communication_data_type, runs checked
+ *         for non-finite values.
+ *   [MD]  "3.7 Megatron-LM, DeepSpeed & Parallelism in Practice",
+ *         "ZeRO-Offload and ZeRO-Infinity" -- fp16 loss_scale 0 (dynamic),
+ *         loss_scale_window, gradient_clipping, bucket sizes;
+ *         "Initializing a DeepSpeed Engine" -- backward()/step() with
+ *         torch.optim.AdamW; "DeepSpeed config for this run" -- 500 MB buckets.
+ *   [NM]  "nanoMegatron", "Comparison with production frameworks" and
+ *         "Benchmarks" -- flat-buffer bucketed reduction versus per-parameter
+ *         hooks.
+ *
+ * Conventions for every call:
+ *   - Return value: ZERO_OK (0) or a zero_status code. No C++ exception
+ *     crosses this boundary. zero_last_error() gives a message for the last
+ *     failing call on the calling thread.
+ *   - "device pointer": memory on the current CUDA device, owned by the
+ *     caller (for instance a torch tensor's data_ptr()). The library never
+ *     frees caller memory. All device pointers must be 16-byte aligned.
+ *   - "stream": a cudaStream_t passed as void*; NULL is the legacy default
+ *     stream. Calls that take a stream only enqueue work on it and return
+ *     without waiting, unless stated otherwise.
+ *   - A layout is used from one host thread and one stream at a time.
+ *   - Arguments are validated on the host before anything is enqueued; an
+ *     invalid call changes no state.
+ */
+#ifndef ZERO_GB300_H
+#define ZERO_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define ZERO_ABI_VERSION 1
+#define ZERO_MAX_WORLD 64
+
+typedef enum {
+  ZERO_OK = 0,
+  ZERO_ERR_INVALID = 1, /* bad argument: null, size, alignment, dtype, stage, world */
+  ZERO_ERR_CUDA = 2,    /* a CUDA runtime call failed; the message names it */
+  ZERO_ERR_OOM = 3,     /* the library's own small device allocation failed */
+  ZERO_ERR_TIMEOUT = 4, /* reserved: a bounded device wait gave up */
+  ZERO_ERR_STATE = 5    /* call out of order (e.g. step before bind/init) */
+} zero_status;
+
+typedef enum { ZERO_F32 = 0, ZERO_F16 = 1, ZERO_BF16 = 2 } zero_dtype;
+
+typedef struct zero_layout zero_layout_t; /* opaque, host-owned */
+
+/* Layout configuration. [ND] stages 1/2; [MD] bucket sizes in bytes.
+ *   world        W simulated data-parallel ranks, 1..ZERO_MAX_WORLD.
+ *   stage        1: every rank receives the whole reduced gradient (all-reduce)
+ *                   and updates only its optimizer shard (ZeRO-1);
+ *                2: every rank receives only its reduced shard (ZeRO-2).
+ *   bucket_bytes bucket capacity in bytes of gradient dtype (> 0).
+ *   grad_dtype   dtype of the W input gradient buffers.
+ *   param_dtype  dtype of the cast-out parameters (ZERO_F16 or ZERO_BF16).
+ *   comm_dtype   dtype the reduced gradient is rounded to once after the fp32
+ *                sum ([ND] communication_data_type); -1 = grad_dtype. */
+typedef struct {
+  int32_t world;
+  int32_t stage;
+  int64_t bucket_bytes;
+  int32_t grad_dtype;
+  int32_t param_dtype;
+  int32_t comm_dtype;
+  int32_t reserved;
+} zero_config;
+
+/* What zero_layout_query reports. Element counts unless noted. */
+typedef struct {
+  int64_t n_params;
+  int64_t n_real;          /* N: sum of the parameters' element counts */
+  int64_t n_padded;        /* Np: length of the flat layout */
+  int64_t shard_elems;     /* Np / W: one rank's shard (all buckets) */
+  int64_t n_buckets;
+  int64_t n_tiles;         /* work units the kernels iterate over */
+  int64_t grad_bytes;      /* bytes of ONE rank's flat gradient buffer (Np * size(grad)) */
+  int64_t state_bytes;     /* bytes of ONE of master/m/v (Np * 4, all ranks' shards) */
+  int64_t params_bytes;    /* bytes of the flat parameter buffer (Np * size(param)) */
+  int64_t scratch_bytes;   /* stage 2: reduced shards (Np * size(comm)); stage 1: 0 */
+  int64_t allreduce_bytes; /* stage 1: bytes of ONE rank's all-reduce output; stage 2: 0 */
+  int64_t device_bytes_owned; /* device bytes the library allocates at bind */
+  double ledger_bytes_per_param; /* [DO] per-rank persistent bytes per parameter:
+                                    stage 1: P + G + 12/W; stage 2: P + G/W + 12/W
+                                    (P, G = param and grad dtype sizes) */
+  double step_bytes_per_elem;    /* roofline bytes per real element of one step:
+                                    2W grad reads + 24 master/m/v + P param write */
+} zero_layout_info;
+
+/* Loss-scaler configuration. [MD] fp16 loss_scale 0 = dynamic with
+ * loss_scale_window N; [ND] the bf16 path uses no loss scaling.
+ *   init_scale       starting S (> 0).
+ *   dynamic          1: halve on overflow, grow after growth_interval clean
+ *                    steps; 0: S stays init_scale (overflow still skips).
+ *   growth_interval  N (> 0).
+ *   growth_factor    > 1 (2.0); backoff_factor in (0,1) (0.5); min_scale > 0 (1.0). */
+typedef struct {
+  double init_scale;
+  int32_t dynamic;
+  int32_t reserved;
+  int64_t growth_interval;
+  double growth_factor;
+  double backoff_factor;
+  double min_scale;
+} zero_scaler_cfg;
+
+/* Per-step hyper-parameters ([ND] AdamW; [MD] gradient_clipping).
+ *   max_grad_norm <= 0 turns clipping off.
+ *   grad_divisor  D in g = r * clip / (S * D); <= 0 means W (replica mean,
+ *                 [DO] sharded-SGD example); 1 is the plain sum. Weighting by
+ *                 token counts is the caller's job ([DO] failure case). */
+typedef struct {
+  double lr;
+  double beta1;
+  double beta2;
+  double eps;
+  double weight_decay;
+  double max_grad_norm;
+  double grad_divisor;
+} zero_hparams;
+
+/* Scaler state and the last step's report, read back by zero_loss_scale_state. */
+typedef struct {
+  double scale;        /* S for the next step */
+  int64_t counter;     /* clean steps since the last overflow or growth */
+  int64_t t;           /* Adam step count: applied steps only */
+  int32_t overflow;    /* last step saw a non-finite reduced gradient */
+  int32_t skipped;     /* last step was skipped (== overflow) */
+  double grad_norm;    /* last step: norm of the unscaled, divided gradient */
+  double clip_coef;    /* last step: clip coefficient (0 if skipped) */
+  double norm_sq_raw;  /* last step: sum of squares of the reduced (scaled) values */
+  int64_t steps;       /* zero_step calls since zero_state_init */
+} zero_scaler_state;
+
+/* ------------------------------------------------------------------------ */
+/* Layout ([DO] contiguous bucketed buffers, equal contiguous shards).        */
+/* ------------------------------------------------------------------------ */
+
+/* Build the flat bucketed layout of n_params parameters.
+ *   shapes[p]  host array of ndims[p] dimensions (each >= 0); ndims[p] in
+ *              0..8 (0 = scalar, one element).
+ * Rules: parameters keep their order; each starts at a multiple of 64
+ * elements; a new bucket opens when the next parameter would take the
+ * bucket's span past bucket_bytes / size(grad) elements and the bucket
+ * already holds a parameter (a parameter is never split); each bucket is
+ * padded to a multiple of W*128 elements; rank r owns
+ * [start + r*len/W, start + (r+1)*len/W) of every bucket.
+ * *out receives a host object freed by zero_layout_destroy. Host only. */
+int zero_layout_create(const int64_t* const* shapes, const int* ndims, int n_params,
+                       const zero_config* cfg, zero_layout_t** out);
+
+/* Free a layout and the device memory it allocated (synchronises the device
+ * memory free). NULL is accepted. */
+int zero_layout_destroy(zero_layout_t* layout);
+
+int zero_layout_query(const zero_layout_t* layout, zero_layout_info* out);
+
+/* Element offset of parameter `param` in the flat layout (host only). */
+int zero_param_offset(const zero_layout_t* layout, int param, int64_t* elem_offset);
+
+/* Bucket `bucket`: flat start and padded length (host only). */
+int zero_bucket_range(const zero_layout_t* layout, int bucket, int64_t* start, int64_t* len);
+
+/* Rank `rank`'s slice of bucket `bucket`: flat begin, its offset inside the
+ * rank-major shard buffers (master/m/v/scratch), and its length. */
+int zero_shard_range(const zero_layout_t* layout, int bucket, int rank, int64_t* flat_begin,
+                     int64_t* shard_offset, int64_t* len);
+
+/* ------------------------------------------------------------------------ */
+/* State                                                                     */
+/* ------------------------------------------------------------------------ */
+
+/* Bind caller-owned device buffers and allocate the library's small device
+ * block (work tables, norm partials, scalars: device_bytes_owned bytes).
+ *   master, m, v  fp32, Np elements each, RANK-MAJOR: rank r's shard is
+ *                 [r*Np/W, (r+1)*Np/W), holding its slice of bucket 0, then
+ *                 bucket 1, ... (zero_shard_range gives each slice).
+ *   params_flat   param_dtype, Np elements, flat layout (the gathered view).
+ *   scratch       stage 2: comm_dtype, Np elements, rank-major (each rank's
+ *                 reduce-scatter output); stage 1: ignored (may be NULL).
+ * Rebinding replaces the pointers (and reuses the device block). Synchronous. */
+int zero_state_bind(zero_layout_t* layout, void* master, void* m, void* v, void* params_flat,
+                    void* scratch);
+
+/* Initialise the bound state: master <- master_init_flat (device fp32, Np,
+ * flat layout; padding ignored), m = v = 0, params_flat <- RNE(master) with
+ * padding zero, scaler <- cfg, t = 0. Enqueued on `stream`. */
+int zero_state_init(zero_layout_t* layout, const float* master_init_flat,
+                    const zero_scaler_cfg* cfg, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* The step ([DO] ownership trace; [MD] backward()/step(); [ND] FP16 dynamic   */
+/* loss scaling).                                                            */
+/* ------------------------------------------------------------------------ */
+
+/* One ZeRO-1/2 step over W flat-layout gradient buffers.
+ *   grads          host array of W device pointers; grads[w] holds rank w's
+ *                  gradients in the flat layout (Np elements of grad_dtype;
+ *                  padding is never read). Read only.
+ *   allreduce_out  stage 1: host array of W device pointers, Np elements of
+ *                  comm_dtype each, flat layout; receives the reduced
+ *                  gradient for every rank (may alias grads when
+ *                  comm_dtype == grad_dtype; padding is not written).
+ *                  stage 2: must be NULL.
+ *   hp             host struct, copied at the call.
+ * Enqueues three kernels on `stream`:
+ *   reduce + overflow/norm partials, finalize (norm, clip, scaler, t),
+ *   fused unscale/clip/AdamW/cast-out (returns at once on a skipped step).
+ * Reduced value r = RNE_comm(g_0 + ... + g_{W-1}) (fp32 adds in rank order);
+ * overflow = any non-finite r over real elements; on overflow the update is
+ * skipped, S is multiplied by backoff (dynamic mode, floored at min_scale)
+ * and the clean counter resets; otherwise t += 1, g = r * clip / (S * D),
+ * decoupled-decay AdamW with bias correction, master/m/v stored fp32,
+ * params_flat <- RNE_param(master), and S grows after N clean steps. */
+int zero_step(zero_layout_t* layout, const void* const* grads, void* const* allreduce_out,
+              const zero_hparams* hp, void* stream);
+
+/* Same step, gradients given per tensor instead of flat ([NM] per-parameter
+ * gradients of the hook-based prior art).
+ *   grad_ptrs  host array of W * n_params device pointers, rank-major
+ *              (grad_ptrs[w * n_params + p]); each points at parameter p's
+ *              numel elements of grad_dtype, 16-byte aligned; NULL means an
+ *              all-zero gradient (not read at all).
+ * Everything else as zero_step. */
+int zero_step_tensors(zero_layout_t* layout, const void* const* grad_ptrs,
+                      void* const* allreduce_out, const zero_hparams* hp, void* stream);
+
+/* Same step from HOST gradients: copies host_grads[w] (Np elements of
+ * grad_dtype each, flat layout; pinned memory gives asynchronous copies) into
+ * the device buffers dev_grads[w] with one cudaMemcpyAsync per rank on
+ * `stream`, then runs zero_step on dev_grads. */
+int zero_step_host(zero_layout_t* layout, const void* const* host_grads, void* const* dev_grads,
+                   void* const* allreduce_out, const zero_hparams* hp, void* stream);
+
+/* Read the scaler state and the last step's report. Enqueues a device-to-host
+ * copy on `stream` and WAITS for it (synchronises the stream). */
+int zero_loss_scale_state(zero_layout_t* layout, void* stream, zero_scaler_state* out);
+
+/* Copy the flat parameters out to per-tensor storage ([DO] the all-gather
+ * rebuilds the parameter buffer for the next forward).
+ *   dst  host array of n_replicas * n_params device pointers
+ *        (dst[k * n_params + p]: replica k's parameter p, numel elements of
+ *        param_dtype). Enqueued on `stream`. */
+int zero_gather_params(zero_layout_t* layout, void* const* dst, int n_replicas, void* stream);
+
+/* Copy the rank-major fp32 state out to / in from flat-layout device buffers
+ * (Np elements each; padding of the flat buffers is written as 0 on export
+ * and ignored on import). Any of the three pointers may be NULL to skip it.
+ * Enqueued on `stream`. */
+int zero_state_export(zero_layout_t* layout, float* master_flat, float* m_flat, float* v_flat,
+                      void* stream);
+int zero_state_import(zero_layout_t* layout, const float* master_flat, const float* m_flat,
+                      const float* v_flat, void* stream);
+
+/* Message for the last failing call on this thread ("" if none). The pointer
+ * stays valid until the next failing call on this thread. */
+const char* zero_last_error(void);
+
+/* Replace the allocator used for the library's own device block (default:
+ * cudaMalloc / cudaFree). alloc returns NULL on failure -> ZERO_ERR_OOM. */
+typedef void* (*zero_alloc_fn)(size_t bytes, void* ctx);
+typedef void (*zero_free_fn)(void* ptr, void* ctx);
+int zero_layout_set_allocator(zero_layout_t* layout, zero_alloc_fn alloc, zero_free_fn free_fn,
+                              void* ctx);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* ZERO_GB300_H */

@@ -1,0 +1,16 @@
+"""GB300-native ZeRO-1/2 gradient-and-optimizer step.
+
+The product is the C-ABI library libzero_gb300.so (declared in include/zero.h,
+hand-written CUDA for sm_103a). ``_abi`` binds its entry points one for one;
+``engine.ZeroStep`` owns the device buffers of one layout. No CPU fallback
+exists: without the built library every call raises.
+"""
+from ._abi import (ZERO_BF16, ZERO_F16, ZERO_F32, ZeroError, zero_bucket_range, zero_config,
+                   zero_gather_params, zero_hparams, zero_last_error, zero_layout_create,
+                   zero_layout_destroy, zero_layout_info, zero_layout_query,
+                   zero_layout_set_allocator, zero_loss_scale_state, zero_param_offset,
+                   zero_scaler_cfg, zero_scaler_state, zero_shard_range, zero_state_bind,
+                   zero_state_export, zero_state_import, zero_state_init, zero_step,
+                   zero_step_host, zero_step_tensors, lib)
+
+__all__ = [n for n in dir() if n.startswith("zero_") or n.startswith("ZERO_")] + ["ZeroError", "lib"]

@@ -1,0 +1,212 @@
+"""ctypes binding of the C ABI in include/zero.h, entry point for entry point.
+
+Argument marshalling only: every function here converts Python values to the
+C types, calls the entry point of the same name in libzero_gb300.so, and turns
+a non-zero status into ZeroError. Device pointers and streams are plain ints
+(``tensor.data_ptr()``, ``torch.cuda.current_stream().cuda_stream``).
+
+There is no fallback: if the library is not built, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libzero_gb300.so")
+
+ZERO_OK, ZERO_ERR_INVALID, ZERO_ERR_CUDA, ZERO_ERR_OOM, ZERO_ERR_TIMEOUT, ZERO_ERR_STATE = range(6)
+ZERO_F32, ZERO_F16, ZERO_BF16 = 0, 1, 2
+ZERO_MAX_WORLD = 64
+STATUS_NAME = {0: "ZERO_OK", 1: "ZERO_ERR_INVALID", 2: "ZERO_ERR_CUDA", 3: "ZERO_ERR_OOM",
+               4: "ZERO_ERR_TIMEOUT", 5: "ZERO_ERR_STATE"}
+
+
+class ZeroError(RuntimeError):
+    def __init__(self, code: int, message: str):
+        super().__init__(f"{STATUS_NAME.get(code, code)}: {message}")
+        self.code = code
+
+
+class zero_config(ctypes.Structure):
+    _fields_ = [("world", ctypes.c_int32), ("stage", ctypes.c_int32),
+                ("bucket_bytes", ctypes.c_int64), ("grad_dtype", ctypes.c_int32),
+                ("param_dtype", ctypes.c_int32), ("comm_dtype", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
+
+
+class zero_layout_info(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int64) for n in (
+        "n_params", "n_real", "n_padded", "shard_elems", "n_buckets", "n_tiles", "grad_bytes",
+        "state_bytes", "params_bytes", "scratch_bytes", "allreduce_bytes", "device_bytes_owned")] + \
+        [("ledger_bytes_per_param", ctypes.c_double), ("step_bytes_per_elem", ctypes.c_double)]
+
+
+class zero_scaler_cfg(ctypes.Structure):
+    _fields_ = [("init_scale", ctypes.c_double), ("dynamic", ctypes.c_int32),
+                ("reserved", ctypes.c_int32), ("growth_interval", ctypes.c_int64),
+                ("growth_factor", ctypes.c_double), ("backoff_factor", ctypes.c_double),
+                ("min_scale", ctypes.c_double)]
+
+
+class zero_hparams(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_double) for n in (
+        "lr", "beta1", "beta2", "eps", "weight_decay", "max_grad_norm", "grad_divisor")]
+
+
+class zero_scaler_state(ctypes.Structure):
+    _fields_ = [("scale", ctypes.c_double), ("counter", ctypes.c_int64), ("t", ctypes.c_int64),
+                ("overflow", ctypes.c_int32), ("skipped", ctypes.c_int32),
+                ("grad_norm", ctypes.c_double), ("clip_coef", ctypes.c_double),
+                ("norm_sq_raw", ctypes.c_double), ("steps", ctypes.c_int64)]
+
+
+ALLOC_FN = ctypes.CFUNCTYPE(ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p)
+FREE_FN = ctypes.CFUNCTYPE(None, ctypes.c_void_p, ctypes.c_void_p)
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with __graft_entry__.build() "
+                               "(there is no CPU fallback)")
+        L = ctypes.CDLL(LIB_PATH)
+        P, I, I64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
+        PP = ctypes.POINTER(ctypes.c_void_p)
+        sig = {
+            "zero_layout_create": [ctypes.POINTER(ctypes.POINTER(ctypes.c_int64)),
+                                   ctypes.POINTER(ctypes.c_int), I, ctypes.POINTER(zero_config),
+                                   ctypes.POINTER(P)],
+            "zero_layout_destroy": [P],
+            "zero_layout_query": [P, ctypes.POINTER(zero_layout_info)],
+            "zero_param_offset": [P, I, ctypes.POINTER(I64)],
+            "zero_bucket_range": [P, I, ctypes.POINTER(I64), ctypes.POINTER(I64)],
+            "zero_shard_range": [P, I, I, ctypes.POINTER(I64), ctypes.POINTER(I64),
+                                 ctypes.POINTER(I64)],
+            "zero_state_bind": [P, P, P, P, P, P],
+            "zero_state_init": [P, P, ctypes.POINTER(zero_scaler_cfg), P],
+            "zero_step": [P, PP, PP, ctypes.POINTER(zero_hparams), P],
+            "zero_step_tensors": [P, PP, PP, ctypes.POINTER(zero_hparams), P],
+            "zero_step_host": [P, PP, PP, PP, ctypes.POINTER(zero_hparams), P],
+            "zero_loss_scale_state": [P, P, ctypes.POINTER(zero_scaler_state)],
+            "zero_gather_params": [P, PP, I, P],
+            "zero_state_export": [P, P, P, P, P],
+            "zero_state_import": [P, P, P, P, P],
+            "zero_layout_set_allocator": [P, ALLOC_FN, FREE_FN, P],
+        }
+        for name, args in sig.items():
+            fn = getattr(L, name)
+            fn.argtypes = args
+            fn.restype = ctypes.c_int
+        L.zero_last_error.argtypes = []
+        L.zero_last_error.restype = ctypes.c_char_p
+        _lib = L
+    return _lib
+
+
+def zero_last_error() -> str:
+    return lib().zero_last_error().decode()
+
+
+def _check(rc: int) -> None:
+    if rc != ZERO_OK:
+        raise ZeroError(rc, zero_last_error())
+
+
+def _ptrs(values) -> ctypes.Array:
+    return (ctypes.c_void_p * len(values))(*[int(v) if v else None for v in values])
+
+
+def zero_layout_create(shapes, cfg: zero_config) -> int:
+    n = len(shapes)
+    dims = [(ctypes.c_int64 * max(1, len(s)))(*[int(d) for d in s]) for s in shapes]
+    shape_ptrs = (ctypes.POINTER(ctypes.c_int64) * max(1, n))(
+        *[ctypes.cast(d, ctypes.POINTER(ctypes.c_int64)) for d in dims])
+    ndims = (ctypes.c_int * max(1, n))(*[len(s) for s in shapes])
+    out = ctypes.c_void_p()
+    _check(lib().zero_layout_create(shape_ptrs, ndims, n, ctypes.byref(cfg), ctypes.byref(out)))
+    return out.value
+
+
+def zero_layout_destroy(layout: int) -> None:
+    _check(lib().zero_layout_destroy(layout))
+
+
+def zero_layout_query(layout: int) -> zero_layout_info:
+    info = zero_layout_info()
+    _check(lib().zero_layout_query(layout, ctypes.byref(info)))
+    return info
+
+
+def zero_param_offset(layout: int, param: int) -> int:
+    off = ctypes.c_int64()
+    _check(lib().zero_param_offset(layout, param, ctypes.byref(off)))
+    return off.value
+
+
+def zero_bucket_range(layout: int, bucket: int):
+    a, b = ctypes.c_int64(), ctypes.c_int64()
+    _check(lib().zero_bucket_range(layout, bucket, ctypes.byref(a), ctypes.byref(b)))
+    return a.value, b.value
+
+
+def zero_shard_range(layout: int, bucket: int, rank: int):
+    a, b, c = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int64()
+    _check(lib().zero_shard_range(layout, bucket, rank, ctypes.byref(a), ctypes.byref(b),
+                                  ctypes.byref(c)))
+    return a.value, b.value, c.value
+
+
+def zero_state_bind(layout: int, master: int, m: int, v: int, params_flat: int, scratch: int) -> None:
+    _check(lib().zero_state_bind(layout, master, m, v, params_flat, scratch or None))
+
+
+def zero_state_init(layout: int, master_init_flat: int, cfg: zero_scaler_cfg, stream: int) -> None:
+    _check(lib().zero_state_init(layout, master_init_flat, ctypes.byref(cfg), stream or None))
+
+
+def zero_step(layout: int, grads, allreduce_out, hp: zero_hparams, stream: int) -> None:
+    ar = _ptrs(allreduce_out) if allreduce_out is not None else None
+    _check(lib().zero_step(layout, _ptrs(grads), ar, ctypes.byref(hp), stream or None))
+
+
+def zero_step_tensors(layout: int, grad_ptrs, allreduce_out, hp: zero_hparams, stream: int) -> None:
+    ar = _ptrs(allreduce_out) if allreduce_out is not None else None
+    _check(lib().zero_step_tensors(layout, _ptrs(grad_ptrs), ar, ctypes.byref(hp), stream or None))
+
+
+def zero_step_host(layout: int, host_grads, dev_grads, allreduce_out, hp: zero_hparams,
+                   stream: int) -> None:
+    ar = _ptrs(allreduce_out) if allreduce_out is not None else None
+    _check(lib().zero_step_host(layout, _ptrs(host_grads), _ptrs(dev_grads), ar, ctypes.byref(hp),
+                                stream or None))
+
+
+def zero_loss_scale_state(layout: int, stream: int) -> zero_scaler_state:
+    st = zero_scaler_state()
+    _check(lib().zero_loss_scale_state(layout, stream or None, ctypes.byref(st)))
+    return st
+
+
+def zero_gather_params(layout: int, dst, n_replicas: int, stream: int) -> None:
+    _check(lib().zero_gather_params(layout, _ptrs(dst), n_replicas, stream or None))
+
+
+def zero_state_export(layout: int, master_flat: int, m_flat: int, v_flat: int, stream: int) -> None:
+    _check(lib().zero_state_export(layout, master_flat or None, m_flat or None, v_flat or None,
+                                   stream or None))
+
+
+def zero_state_import(layout: int, master_flat: int, m_flat: int, v_flat: int, stream: int) -> None:
+    _check(lib().zero_state_import(layout, master_flat or None, m_flat or None, v_flat or None,
+                                   stream or None))
+
+
+def zero_layout_set_allocator(layout: int, alloc, free_fn, ctx: int = 0) -> None:
+    """alloc/free_fn: ALLOC_FN / FREE_FN instances (keep them alive), or None for the default."""
+    _check(lib().zero_layout_set_allocator(layout, alloc or ALLOC_FN(), free_fn or FREE_FN(),
+                                           ctx or None))

@@ -1,0 +1,599 @@
+// Host side of the C ABI declared in include/zero.h: layout construction,
+// argument validation, the library's small device block, and the launch
+// sequence of one step. No compute happens here; every step of the path runs
+// in the kernels (k_reduce*.cu, k_update.cu, k_copy.cu).
+#include "zero.h"
+
+#include <algorithm>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <string>
+#include <vector>
+
+#include <cuda_runtime.h>
+
+#include "internal.h"
+
+using namespace zg;
+
+namespace {
+
+thread_local std::string g_last_error;
+
+int fail(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return code;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  return fail(ZERO_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+#define ZERO_CUDA(call)                              \
+  do {                                               \
+    cudaError_t e_ = (call);                         \
+    if (e_ != cudaSuccess) return cuda_fail(e_, #call); \
+  } while (0)
+
+int64_t align_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+int dtype_bytes(int d) { return d == ZERO_F32 ? 4 : 2; }
+bool valid_dtype(int d) { return d == ZERO_F32 || d == ZERO_F16 || d == ZERO_BF16; }
+
+constexpr int kMaxPartials = 4096;  // upper bound on the reduce grid (SMs x blocks/SM)
+
+void* default_alloc(size_t n, void*) {
+  void* p = nullptr;
+  return cudaMalloc(&p, n) == cudaSuccess ? p : nullptr;
+}
+void default_free(void* p, void*) { cudaFree(p); }
+
+}  // namespace
+
+struct zero_layout {
+  zero_config cfg{};
+  int comm_dtype = 0;
+  std::vector<int64_t> numel, offset;
+  std::vector<int> bucket_of;
+  std::vector<int64_t> bstart, blen;
+  int64_t n_real = 0, np = 0;
+  std::vector<Tile> tiles;
+
+  zero_alloc_fn alloc = default_alloc;
+  zero_free_fn free_fn = default_free;
+  void* alloc_ctx = nullptr;
+
+  // bound state (caller-owned buffers)
+  bool bound = false;
+  bool initialized = false;
+  int device = -1;
+  float* master = nullptr;
+  float* m = nullptr;
+  float* v = nullptr;
+  void* params = nullptr;
+  void* scratch = nullptr;
+
+  // library-owned device block
+  void* dblock = nullptr;
+  size_t dblock_bytes = 0;
+  Tile* d_tiles = nullptr;
+  double* d_part = nullptr;
+  unsigned* d_ovf = nullptr;
+  DevState* d_state = nullptr;
+  const void** d_table = nullptr;  // W * n_params grad pointers (table mode)
+  void* d_gather = nullptr;        // replica pointer table for K4 (grown on demand)
+  size_t gather_cap = 0;
+
+  int grid_reduce = 0, grid_update = 0, grid_copy = 0;
+
+  int world() const { return cfg.world; }
+  int n_params() const { return (int)numel.size(); }
+};
+
+namespace {
+
+int check_layout(const zero_layout_t* L) {
+  if (L == nullptr) return fail(ZERO_ERR_INVALID, "layout is NULL");
+  return ZERO_OK;
+}
+
+int check_ready(const zero_layout_t* L, bool need_init) {
+  if (int rc = check_layout(L)) return rc;
+  if (!L->bound) return fail(ZERO_ERR_STATE, "zero_state_bind has not been called");
+  if (need_init && !L->initialized) return fail(ZERO_ERR_STATE, "zero_state_init has not been called");
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev != L->device)
+    return fail(ZERO_ERR_STATE, "current device %d is not the bound device %d", dev, L->device);
+  return ZERO_OK;
+}
+
+// The flat bucketed layout and the tile list (see zero_layout_create).
+void build_layout(zero_layout* L) {
+  const int W = L->cfg.world;
+  const int64_t cap = L->cfg.bucket_bytes / dtype_bytes(L->cfg.grad_dtype);
+  const int64_t unit = (int64_t)W * kShardUnit;
+  const int P = L->n_params();
+  L->offset.assign(P, 0);
+  L->bucket_of.assign(P, 0);
+  int64_t cursor = 0, bucket_begin = 0;
+  int first_in_bucket = 0;
+  auto close_bucket = [&](int64_t end) {
+    L->bstart.push_back(bucket_begin);
+    L->blen.push_back(align_up(end - bucket_begin, unit));
+    bucket_begin += L->blen.back();
+  };
+  for (int p = 0; p < P; ++p) {
+    int64_t at = align_up(cursor, kParamAlign);
+    const bool holds_one = p > first_in_bucket;
+    if (holds_one && at + L->numel[p] - bucket_begin > cap) {
+      close_bucket(cursor);
+      first_in_bucket = p;
+      at = bucket_begin;
+    }
+    L->offset[p] = at;
+    L->bucket_of[p] = (int)L->bstart.size();
+    cursor = at + L->numel[p];
+  }
+  close_bucket(cursor);
+  L->np = bucket_begin;
+
+  // Tiles in flat order: bucket, then rank slice, then parameter runs.
+  const int64_t shard_total = L->np / W;
+  int64_t shard_prefix = 0;  // sum of len/W over the buckets before b
+  int p_lo = 0;
+  for (size_t b = 0; b < L->bstart.size(); ++b) {
+    const int64_t slice = L->blen[b] / W;
+    int p_hi = p_lo;
+    while (p_hi < P && L->bucket_of[p_hi] == (int)b) ++p_hi;
+    for (int r = 0; r < W; ++r) {
+      const int64_t lo = L->bstart[b] + r * slice, hi = lo + slice;
+      const int64_t shard_base = r * shard_total + shard_prefix;
+      for (int p = p_lo; p < p_hi; ++p) {
+        const int64_t a = std::max(lo, L->offset[p]);
+        const int64_t e = std::min(hi, L->offset[p] + L->numel[p]);
+        for (int64_t x = a; x < e; x += kTileElems) {
+          Tile t{};
+          t.flat = x;
+          t.shard = shard_base + (x - lo);
+          t.in_param = x - L->offset[p];
+          t.len = (int32_t)std::min<int64_t>(kTileElems, e - x);
+          t.param = p;
+          t.rank = r;
+          L->tiles.push_back(t);
+        }
+      }
+    }
+    shard_prefix += slice;
+    p_lo = p_hi;
+  }
+}
+
+int launch_step(zero_layout* L, const GradSrc& src, void* const* allreduce_out,
+                const zero_hparams* hp, cudaStream_t s) {
+  const int W = L->world();
+  const int n_tiles = (int)L->tiles.size();
+  ReduceArgs ra{};
+  ra.tiles = L->d_tiles;
+  ra.n_tiles = n_tiles;
+  ra.world = W;
+  ra.stage = L->cfg.stage;
+  ra.grad_dtype = L->cfg.grad_dtype;
+  ra.comm_dtype = L->comm_dtype;
+  ra.src = src;
+  if (L->cfg.stage == 1) {
+    for (int w = 0; w < W; ++w) ra.out.base[w] = allreduce_out[w];
+  } else {
+    ra.out.base[0] = L->scratch;
+  }
+  ra.part_sumsq = L->d_part;
+  ra.part_ovf = L->d_ovf;
+  int n_part = 0;
+  if (n_tiles > 0) {
+    cudaError_t e = launch_reduce(ra, L->grid_reduce, s);
+    if (e != cudaSuccess) return cuda_fail(e, "reduce kernel launch");
+    n_part = L->grid_reduce;
+  }
+  Hparams h{hp->lr, hp->beta1, hp->beta2, hp->eps, hp->weight_decay, hp->max_grad_norm,
+            hp->grad_divisor};
+  cudaError_t e = launch_finalize(L->d_part, L->d_ovf, n_part, W, h, L->d_state, s);
+  if (e != cudaSuccess) return cuda_fail(e, "finalize kernel launch");
+  if (n_tiles > 0) {
+    UpdateArgs ua{};
+    ua.tiles = L->d_tiles;
+    ua.n_tiles = n_tiles;
+    ua.stage = L->cfg.stage;
+    ua.comm_dtype = L->comm_dtype;
+    ua.param_dtype = L->cfg.param_dtype;
+    ua.red = ra.out;
+    ua.master = L->master;
+    ua.m = L->m;
+    ua.v = L->v;
+    ua.params_flat = L->params;
+    ua.state = L->d_state;
+    e = launch_update(ua, L->grid_update, s);
+    if (e != cudaSuccess) return cuda_fail(e, "update kernel launch");
+  }
+  return ZERO_OK;
+}
+
+int check_hparams(const zero_hparams* hp) {
+  if (hp == nullptr) return fail(ZERO_ERR_INVALID, "hparams is NULL");
+  if (!(hp->lr >= 0.0) || !(hp->beta1 >= 0.0 && hp->beta1 < 1.0) ||
+      !(hp->beta2 >= 0.0 && hp->beta2 < 1.0) || !(hp->eps > 0.0) || !(hp->weight_decay >= 0.0))
+    return fail(ZERO_ERR_INVALID, "hparams out of range (lr>=0, 0<=beta<1, eps>0, wd>=0)");
+  if (hp->max_grad_norm != hp->max_grad_norm || hp->grad_divisor != hp->grad_divisor)
+    return fail(ZERO_ERR_INVALID, "hparams contain NaN");
+  return ZERO_OK;
+}
+
+int check_allreduce(const zero_layout* L, void* const* allreduce_out) {
+  if (L->cfg.stage == 2) {
+    if (allreduce_out != nullptr) return fail(ZERO_ERR_INVALID, "stage 2 takes no allreduce_out");
+    return ZERO_OK;
+  }
+  if (allreduce_out == nullptr) return fail(ZERO_ERR_INVALID, "stage 1 needs allreduce_out");
+  for (int w = 0; w < L->world(); ++w) {
+    if (allreduce_out[w] == nullptr || !aligned16(allreduce_out[w]))
+      return fail(ZERO_ERR_INVALID, "allreduce_out[%d] is NULL or not 16-byte aligned", w);
+  }
+  return ZERO_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* zero_last_error(void) { return g_last_error.c_str(); }
+
+int zero_layout_create(const int64_t* const* shapes, const int* ndims, int n_params,
+                       const zero_config* cfg, zero_layout_t** out) {
+  if (out == nullptr || cfg == nullptr) return fail(ZERO_ERR_INVALID, "NULL argument");
+  *out = nullptr;
+  if (n_params <= 0) return fail(ZERO_ERR_INVALID, "n_params must be positive");
+  if (shapes == nullptr || ndims == nullptr) return fail(ZERO_ERR_INVALID, "shapes/ndims NULL");
+  if (cfg->world < 1 || cfg->world > ZERO_MAX_WORLD)
+    return fail(ZERO_ERR_INVALID, "world %d outside 1..%d", cfg->world, ZERO_MAX_WORLD);
+  if (cfg->stage != 1 && cfg->stage != 2) return fail(ZERO_ERR_INVALID, "stage must be 1 or 2");
+  if (cfg->bucket_bytes <= 0) return fail(ZERO_ERR_INVALID, "bucket_bytes must be positive");
+  if (!valid_dtype(cfg->grad_dtype)) return fail(ZERO_ERR_INVALID, "bad grad_dtype");
+  if (cfg->param_dtype != ZERO_F16 && cfg->param_dtype != ZERO_BF16)
+    return fail(ZERO_ERR_INVALID, "param_dtype must be ZERO_F16 or ZERO_BF16");
+  const int comm = cfg->comm_dtype < 0 ? cfg->grad_dtype : cfg->comm_dtype;
+  if (!valid_dtype(comm)) return fail(ZERO_ERR_INVALID, "bad comm_dtype");
+  if (cfg->bucket_bytes / dtype_bytes(cfg->grad_dtype) < 1)
+    return fail(ZERO_ERR_INVALID, "bucket_bytes smaller than one gradient element");
+
+  zero_layout* L = new (std::nothrow) zero_layout();
+  if (L == nullptr) return fail(ZERO_ERR_OOM, "host allocation failed");
+  L->cfg = *cfg;
+  L->comm_dtype = comm;
+  L->numel.resize(n_params);
+  for (int p = 0; p < n_params; ++p) {
+    if (ndims[p] < 0 || ndims[p] > 8 || (ndims[p] > 0 && shapes[p] == nullptr)) {
+      delete L;
+      return fail(ZERO_ERR_INVALID, "parameter %d: bad ndims/shape", p);
+    }
+    int64_t n = 1;
+    for (int d = 0; d < ndims[p]; ++d) {
+      const int64_t k = shapes[p][d];
+      if (k < 0 || (k > 0 && n > (int64_t(1) << 46) / k)) {
+        delete L;
+        return fail(ZERO_ERR_INVALID, "parameter %d: negative or oversized dimension", p);
+      }
+      n *= k;
+    }
+    L->numel[p] = n;
+    L->n_real += n;
+  }
+  build_layout(L);
+  if (L->tiles.size() > (size_t)INT32_MAX) {
+    delete L;
+    return fail(ZERO_ERR_INVALID, "model too large for the tile table");
+  }
+  *out = L;
+  return ZERO_OK;
+}
+
+int zero_layout_destroy(zero_layout_t* L) {
+  if (L == nullptr) return ZERO_OK;
+  if (L->dblock) L->free_fn(L->dblock, L->alloc_ctx);
+  if (L->d_gather) L->free_fn(L->d_gather, L->alloc_ctx);
+  delete L;
+  return ZERO_OK;
+}
+
+int zero_layout_set_allocator(zero_layout_t* L, zero_alloc_fn alloc, zero_free_fn free_fn,
+                              void* ctx) {
+  if (int rc = check_layout(L)) return rc;
+  if ((alloc == nullptr) != (free_fn == nullptr))
+    return fail(ZERO_ERR_INVALID, "alloc and free must both be set or both be NULL");
+  if (L->dblock != nullptr) return fail(ZERO_ERR_STATE, "allocator must be set before bind");
+  L->alloc = alloc ? alloc : default_alloc;
+  L->free_fn = free_fn ? free_fn : default_free;
+  L->alloc_ctx = ctx;
+  return ZERO_OK;
+}
+
+int zero_layout_query(const zero_layout_t* L, zero_layout_info* o) {
+  if (int rc = check_layout(L)) return rc;
+  if (o == nullptr) return fail(ZERO_ERR_INVALID, "out is NULL");
+  const int W = L->world();
+  const double G = dtype_bytes(L->cfg.grad_dtype), P = dtype_bytes(L->cfg.param_dtype);
+  const int C = dtype_bytes(L->comm_dtype);
+  std::memset(o, 0, sizeof(*o));
+  o->n_params = L->n_params();
+  o->n_real = L->n_real;
+  o->n_padded = L->np;
+  o->shard_elems = L->np / W;
+  o->n_buckets = (int64_t)L->bstart.size();
+  o->n_tiles = (int64_t)L->tiles.size();
+  o->grad_bytes = L->np * (int64_t)G;
+  o->state_bytes = L->np * 4;
+  o->params_bytes = L->np * (int64_t)P;
+  o->scratch_bytes = L->cfg.stage == 2 ? L->np * C : 0;
+  o->allreduce_bytes = L->cfg.stage == 1 ? L->np * C : 0;
+  const size_t tiles = align_up((int64_t)L->tiles.size() * sizeof(Tile), 256);
+  o->device_bytes_owned = (int64_t)(tiles + align_up(kMaxPartials * 8, 256) +
+                                    align_up(kMaxPartials * 4, 256) + align_up(sizeof(DevState), 256) +
+                                    align_up((int64_t)W * L->n_params() * 8, 256));
+  o->ledger_bytes_per_param = L->cfg.stage == 1 ? P + G + 12.0 / W : P + G / W + 12.0 / W;
+  o->step_bytes_per_elem = W * G + 24.0 + P;
+  return ZERO_OK;
+}
+
+int zero_param_offset(const zero_layout_t* L, int param, int64_t* off) {
+  if (int rc = check_layout(L)) return rc;
+  if (off == nullptr || param < 0 || param >= L->n_params())
+    return fail(ZERO_ERR_INVALID, "param index out of range");
+  *off = L->offset[param];
+  return ZERO_OK;
+}
+
+int zero_bucket_range(const zero_layout_t* L, int bucket, int64_t* start, int64_t* len) {
+  if (int rc = check_layout(L)) return rc;
+  if (start == nullptr || len == nullptr || bucket < 0 || bucket >= (int)L->bstart.size())
+    return fail(ZERO_ERR_INVALID, "bucket index out of range");
+  *start = L->bstart[bucket];
+  *len = L->blen[bucket];
+  return ZERO_OK;
+}
+
+int zero_shard_range(const zero_layout_t* L, int bucket, int rank, int64_t* flat_begin,
+                     int64_t* shard_offset, int64_t* len) {
+  if (int rc = check_layout(L)) return rc;
+  if (flat_begin == nullptr || shard_offset == nullptr || len == nullptr || bucket < 0 ||
+      bucket >= (int)L->bstart.size() || rank < 0 || rank >= L->world())
+    return fail(ZERO_ERR_INVALID, "bucket or rank out of range");
+  const int W = L->world();
+  int64_t prefix = 0;
+  for (int b = 0; b < bucket; ++b) prefix += L->blen[b] / W;
+  const int64_t slice = L->blen[bucket] / W;
+  *flat_begin = L->bstart[bucket] + rank * slice;
+  *shard_offset = rank * (L->np / W) + prefix;
+  *len = slice;
+  return ZERO_OK;
+}
+
+int zero_state_bind(zero_layout_t* L, void* master, void* m, void* v, void* params_flat,
+                    void* scratch) {
+  if (int rc = check_layout(L)) return rc;
+  if (master == nullptr || m == nullptr || v == nullptr || params_flat == nullptr)
+    return fail(ZERO_ERR_INVALID, "master/m/v/params_flat must not be NULL");
+  if (!aligned16(master) || !aligned16(m) || !aligned16(v) || !aligned16(params_flat))
+    return fail(ZERO_ERR_INVALID, "state buffers must be 16-byte aligned");
+  if (L->cfg.stage == 2 && (scratch == nullptr || !aligned16(scratch)))
+    return fail(ZERO_ERR_INVALID, "stage 2 needs a 16-byte aligned scratch buffer");
+
+  if (L->dblock == nullptr) {
+    const size_t tiles_b = align_up((int64_t)L->tiles.size() * sizeof(Tile), 256);
+    const size_t part_b = align_up(kMaxPartials * sizeof(double), 256);
+    const size_t ovf_b = align_up(kMaxPartials * sizeof(unsigned), 256);
+    const size_t state_b = align_up(sizeof(DevState), 256);
+    const size_t table_b = align_up((int64_t)L->world() * L->n_params() * sizeof(void*), 256);
+    const size_t total = tiles_b + part_b + ovf_b + state_b + table_b;
+    void* blk = L->alloc(total, L->alloc_ctx);
+    if (blk == nullptr) return fail(ZERO_ERR_OOM, "device allocation of %zu bytes failed", total);
+    char* c = static_cast<char*>(blk);
+    L->dblock = blk;
+    L->dblock_bytes = total;
+    L->d_tiles = reinterpret_cast<Tile*>(c);
+    L->d_part = reinterpret_cast<double*>(c + tiles_b);
+    L->d_ovf = reinterpret_cast<unsigned*>(c + tiles_b + part_b);
+    L->d_state = reinterpret_cast<DevState*>(c + tiles_b + part_b + ovf_b);
+    L->d_table = reinterpret_cast<const void**>(c + tiles_b + part_b + ovf_b + state_b);
+    if (!L->tiles.empty()) {
+      cudaError_t e = cudaMemcpy(L->d_tiles, L->tiles.data(), L->tiles.size() * sizeof(Tile),
+                                 cudaMemcpyHostToDevice);
+      if (e != cudaSuccess) return cuda_fail(e, "upload of the tile table");
+    }
+    int dev = 0, sms = 0;
+    ZERO_CUDA(cudaGetDevice(&dev));
+    ZERO_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+    L->device = dev;
+    const int n_tiles = (int)L->tiles.size();
+    const int bps_r = reduce_blocks_per_sm(L->cfg.grad_dtype, L->comm_dtype, L->world(), L->cfg.stage);
+    const int bps_u = update_blocks_per_sm(L->comm_dtype, L->cfg.param_dtype);
+    if (bps_r <= 0 || bps_u <= 0)
+      return fail(ZERO_ERR_CUDA, "kernel occupancy query failed (no sm_103a image for this GPU?)");
+    L->grid_reduce = std::max(1, std::min({n_tiles, sms * bps_r, kMaxPartials}));
+    L->grid_update = std::max(1, std::min(n_tiles, sms * bps_u));
+    L->grid_copy = std::max(1, std::min(n_tiles, sms * 4));
+  }
+  L->master = static_cast<float*>(master);
+  L->m = static_cast<float*>(m);
+  L->v = static_cast<float*>(v);
+  L->params = params_flat;
+  L->scratch = scratch;
+  L->bound = true;
+  L->initialized = false;
+  return ZERO_OK;
+}
+
+int zero_state_init(zero_layout_t* L, const float* master_init_flat, const zero_scaler_cfg* cfg,
+                    void* stream) {
+  if (int rc = check_ready(L, false)) return rc;
+  if (master_init_flat == nullptr || !aligned16(master_init_flat) || cfg == nullptr)
+    return fail(ZERO_ERR_INVALID, "master_init_flat (16-byte aligned) and cfg are required");
+  if (!(cfg->init_scale > 0.0) || cfg->growth_interval <= 0 || !(cfg->growth_factor >= 1.0) ||
+      !(cfg->backoff_factor > 0.0 && cfg->backoff_factor <= 1.0) || !(cfg->min_scale > 0.0))
+    return fail(ZERO_ERR_INVALID, "scaler config out of range");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t nbytes = (size_t)L->np * 4;
+  ZERO_CUDA(cudaMemsetAsync(L->master, 0, nbytes, s));
+  ZERO_CUDA(cudaMemsetAsync(L->m, 0, nbytes, s));
+  ZERO_CUDA(cudaMemsetAsync(L->v, 0, nbytes, s));
+  ZERO_CUDA(cudaMemsetAsync(L->params, 0, (size_t)L->np * dtype_bytes(L->cfg.param_dtype), s));
+  ScalerCfg sc{cfg->init_scale, cfg->dynamic ? 1 : 0, cfg->growth_interval, cfg->growth_factor,
+               cfg->backoff_factor, cfg->min_scale};
+  cudaError_t e = launch_state_init(sc, L->d_state, s);
+  if (e != cudaSuccess) return cuda_fail(e, "state init launch");
+  if (!L->tiles.empty()) {
+    e = launch_init_from_flat(L->d_tiles, (int)L->tiles.size(), master_init_flat, L->master,
+                              L->params, L->cfg.param_dtype, L->grid_copy, s);
+    if (e != cudaSuccess) return cuda_fail(e, "init kernel launch");
+  }
+  L->initialized = true;
+  return ZERO_OK;
+}
+
+int zero_step(zero_layout_t* L, const void* const* grads, void* const* allreduce_out,
+              const zero_hparams* hp, void* stream) {
+  if (int rc = check_ready(L, true)) return rc;
+  if (int rc = check_hparams(hp)) return rc;
+  if (int rc = check_allreduce(L, allreduce_out)) return rc;
+  if (grads == nullptr) return fail(ZERO_ERR_INVALID, "grads is NULL");
+  GradSrc src{};
+  for (int w = 0; w < L->world(); ++w) {
+    if (grads[w] == nullptr || !aligned16(grads[w]))
+      return fail(ZERO_ERR_INVALID, "grads[%d] is NULL or not 16-byte aligned", w);
+    src.base[w] = grads[w];
+  }
+  return launch_step(L, src, allreduce_out, hp, static_cast<cudaStream_t>(stream));
+}
+
+int zero_step_tensors(zero_layout_t* L, const void* const* grad_ptrs, void* const* allreduce_out,
+                      const zero_hparams* hp, void* stream) {
+  if (int rc = check_ready(L, true)) return rc;
+  if (int rc = check_hparams(hp)) return rc;
+  if (int rc = check_allreduce(L, allreduce_out)) return rc;
+  if (grad_ptrs == nullptr) return fail(ZERO_ERR_INVALID, "grad_ptrs is NULL");
+  const int64_t n = (int64_t)L->world() * L->n_params();
+  for (int64_t i = 0; i < n; ++i) {
+    if (grad_ptrs[i] != nullptr && !aligned16(grad_ptrs[i]))
+      return fail(ZERO_ERR_INVALID, "grad_ptrs[%lld] is not 16-byte aligned", (long long)i);
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // The host array is staged by the runtime before this call returns.
+  ZERO_CUDA(cudaMemcpyAsync(L->d_table, grad_ptrs, (size_t)n * sizeof(void*),
+                            cudaMemcpyHostToDevice, s));
+  GradSrc src{};
+  src.table = L->d_table;
+  src.n_params = L->n_params();
+  src.table_mode = 1;
+  return launch_step(L, src, allreduce_out, hp, s);
+}
+
+int zero_step_host(zero_layout_t* L, const void* const* host_grads, void* const* dev_grads,
+                   void* const* allreduce_out, const zero_hparams* hp, void* stream) {
+  if (int rc = check_ready(L, true)) return rc;
+  if (host_grads == nullptr || dev_grads == nullptr)
+    return fail(ZERO_ERR_INVALID, "host_grads/dev_grads is NULL");
+  const size_t bytes = (size_t)L->np * dtype_bytes(L->cfg.grad_dtype);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  for (int w = 0; w < L->world(); ++w) {
+    if (host_grads[w] == nullptr || dev_grads[w] == nullptr || !aligned16(dev_grads[w]))
+      return fail(ZERO_ERR_INVALID, "host_grads[%d]/dev_grads[%d] NULL or misaligned", w, w);
+  }
+  if (int rc = check_hparams(hp)) return rc;
+  if (int rc = check_allreduce(L, allreduce_out)) return rc;
+  for (int w = 0; w < L->world(); ++w)
+    ZERO_CUDA(cudaMemcpyAsync(dev_grads[w], host_grads[w], bytes, cudaMemcpyHostToDevice, s));
+  return zero_step(L, dev_grads, allreduce_out, hp, stream);
+}
+
+int zero_loss_scale_state(zero_layout_t* L, void* stream, zero_scaler_state* out) {
+  if (int rc = check_ready(L, true)) return rc;
+  if (out == nullptr) return fail(ZERO_ERR_INVALID, "out is NULL");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  DevState h{};
+  ZERO_CUDA(cudaMemcpyAsync(&h, L->d_state, sizeof(DevState), cudaMemcpyDeviceToHost, s));
+  ZERO_CUDA(cudaStreamSynchronize(s));
+  out->scale = h.scale;
+  out->counter = h.counter;
+  out->t = h.t;
+  out->overflow = h.overflow;
+  out->skipped = h.skipped;
+  out->grad_norm = h.grad_norm;
+  out->clip_coef = h.clip_coef;
+  out->norm_sq_raw = h.norm_sq_raw;
+  out->steps = h.steps;
+  return ZERO_OK;
+}
+
+int zero_gather_params(zero_layout_t* L, void* const* dst, int n_replicas, void* stream) {
+  if (int rc = check_ready(L, true)) return rc;
+  if (dst == nullptr || n_replicas < 1) return fail(ZERO_ERR_INVALID, "dst NULL or n_replicas < 1");
+  const int64_t n = (int64_t)n_replicas * L->n_params();
+  for (int64_t i = 0; i < n; ++i) {
+    if (dst[i] == nullptr && L->numel[i % L->n_params()] > 0)
+      return fail(ZERO_ERR_INVALID, "dst[%lld] is NULL", (long long)i);
+    if ((reinterpret_cast<uintptr_t>(dst[i]) & 1u) != 0)
+      return fail(ZERO_ERR_INVALID, "dst[%lld] is not 2-byte aligned", (long long)i);
+  }
+  const size_t need = (size_t)n * sizeof(void*);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (need > L->gather_cap) {
+    ZERO_CUDA(cudaStreamSynchronize(s));  // the old table may still be read
+    if (L->d_gather) L->free_fn(L->d_gather, L->alloc_ctx);
+    L->d_gather = L->alloc(need, L->alloc_ctx);
+    L->gather_cap = L->d_gather ? need : 0;
+    if (L->d_gather == nullptr) return fail(ZERO_ERR_OOM, "device allocation for the dst table");
+  }
+  ZERO_CUDA(cudaMemcpyAsync(L->d_gather, dst, need, cudaMemcpyHostToDevice, s));
+  if (L->tiles.empty()) return ZERO_OK;
+  cudaError_t e = launch_gather(L->d_tiles, (int)L->tiles.size(), L->params,
+                                static_cast<void* const*>(L->d_gather), L->n_params(), n_replicas,
+                                dtype_bytes(L->cfg.param_dtype), L->grid_copy, s);
+  if (e != cudaSuccess) return cuda_fail(e, "gather kernel launch");
+  return ZERO_OK;
+}
+
+static int state_copy(zero_layout_t* L, float* a, float* b, float* c, int dir, void* stream) {
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  float* flat[3] = {a, b, c};
+  float* shard[3] = {L->master, L->m, L->v};
+  for (int k = 0; k < 3; ++k) {
+    if (flat[k] == nullptr) continue;
+    if (!aligned16(flat[k])) return fail(ZERO_ERR_INVALID, "state buffer not 16-byte aligned");
+    if (dir == 0) ZERO_CUDA(cudaMemsetAsync(flat[k], 0, (size_t)L->np * 4, s));
+    if (L->tiles.empty()) continue;
+    cudaError_t e = launch_state_copy(L->d_tiles, (int)L->tiles.size(), shard[k], flat[k], dir,
+                                      L->grid_copy, s);
+    if (e != cudaSuccess) return cuda_fail(e, "state copy launch");
+  }
+  return ZERO_OK;
+}
+
+int zero_state_export(zero_layout_t* L, float* master_flat, float* m_flat, float* v_flat,
+                      void* stream) {
+  if (int rc = check_ready(L, true)) return rc;
+  return state_copy(L, master_flat, m_flat, v_flat, 0, stream);
+}
+
+int zero_state_import(zero_layout_t* L, const float* master_flat, const float* m_flat,
+                      const float* v_flat, void* stream) {
+  if (int rc = check_ready(L, true)) return rc;
+  return state_copy(L, const_cast<float*>(master_flat), const_cast<float*>(m_flat),
+                    const_cast<float*>(v_flat), 1, stream);
+}
+
+}  // extern "C"

@@ -1,0 +1,126 @@
+// Internal interface between the host side (api.cpp) and the kernels (*.cu).
+// Not part of the public ABI (include/zero.h is).
+#pragma once
+
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+namespace zg {
+
+constexpr int kMaxWorld = 64;         // == ZERO_MAX_WORLD
+constexpr int64_t kParamAlign = 64;   // every parameter starts on a multiple of this
+constexpr int64_t kShardUnit = 128;   // buckets are padded to a multiple of W * this
+constexpr int kTileElems = 8192;      // longest work unit (multiple of kParamAlign)
+constexpr int kThreads = 256;         // threads per block of the streaming kernels
+constexpr int kMaxBlocksPerSm = 8;    // 2048 threads / kThreads
+constexpr int kFinalizeThreads = 256;
+
+enum Dtype : int { kF32 = 0, kF16 = 1, kBF16 = 2 };
+
+// One work unit: a run of REAL elements (never padding) of one parameter
+// inside one rank's slice of one bucket, at most kTileElems long. Its start
+// is a multiple of 64 elements in both coordinate systems, so every 16-byte
+// vector access inside it is aligned when the buffers are.
+struct Tile {
+  int64_t flat;      // offset in the flat layout (grads, params, all-reduce outputs)
+  int64_t shard;     // offset in the rank-major shard buffers (master, m, v, scratch)
+  int64_t in_param;  // offset inside its parameter (per-tensor pointers)
+  int32_t len;       // elements, 1..kTileElems
+  int32_t param;     // parameter index
+  int32_t rank;      // owning rank
+  int32_t reserved;
+};
+
+// Device-resident scalars: the loss-scale state machine, the last step's
+// report, and the per-step values the update kernel reads.
+struct DevState {
+  double scale;
+  long long counter;
+  long long t;
+  long long steps;
+  long long growth_interval;
+  double growth_factor, backoff_factor, min_scale;
+  int dynamic;
+  int overflow;
+  int skipped;
+  int skip;  // read by the update kernel: 1 = leave everything untouched
+  double grad_norm, clip_coef, norm_sq_raw;
+  // per-step values for the update kernel (fp32, derived in fp64)
+  float gscale;        // clip / (S * D)
+  float decay;         // 1 - lr * wd
+  float step_size;     // lr / (1 - beta1^t)
+  float inv_sqrt_bc2;  // 1 / sqrt(1 - beta2^t)
+  float beta1, one_minus_beta1, beta2, one_minus_beta2, eps;
+  float reserved_;
+};
+
+struct Hparams {  // mirror of zero_hparams
+  double lr, beta1, beta2, eps, weight_decay, max_grad_norm, grad_divisor;
+};
+
+struct ScalerCfg {
+  double init_scale;
+  int dynamic;
+  long long growth_interval;
+  double growth_factor, backoff_factor, min_scale;
+};
+
+// Where the reduce kernel reads rank w's gradient for a tile.
+struct GradSrc {
+  const void* base[kMaxWorld];  // flat mode: rank w's flat buffer
+  const void* const* table;     // table mode: device array [W * n_params] (entries may be null)
+  int n_params;
+  int table_mode;
+};
+
+// Reduced-gradient buffers: stage 2 -> base[0] is the rank-major scratch;
+// stage 1 -> base[w] is rank w's flat all-reduce output.
+struct RedBufs {
+  void* base[kMaxWorld];
+};
+
+struct ReduceArgs {
+  const Tile* tiles;
+  int n_tiles;
+  int world;
+  int stage;
+  int grad_dtype, comm_dtype;
+  GradSrc src;
+  RedBufs out;
+  double* part_sumsq;   // [grid]
+  unsigned* part_ovf;   // [grid]
+};
+
+struct UpdateArgs {
+  const Tile* tiles;
+  int n_tiles;
+  int stage;
+  int comm_dtype, param_dtype;
+  RedBufs red;
+  float* master;
+  float* m;
+  float* v;
+  void* params_flat;
+  const DevState* state;
+};
+
+// Kernel launchers. Each returns the launch's cudaError_t.
+cudaError_t launch_reduce(const ReduceArgs& a, int grid, cudaStream_t s);
+int reduce_blocks_per_sm(int grad_dtype, int comm_dtype, int world, int stage);
+cudaError_t launch_finalize(const double* part_sumsq, const unsigned* part_ovf, int n_part,
+                            int world, const Hparams& hp, DevState* st, cudaStream_t s);
+cudaError_t launch_update(const UpdateArgs& a, int grid, cudaStream_t s);
+int update_blocks_per_sm(int comm_dtype, int param_dtype);
+cudaError_t launch_state_init(const ScalerCfg& cfg, DevState* st, cudaStream_t s);
+cudaError_t launch_init_from_flat(const Tile* tiles, int n_tiles, const float* master_flat,
+                                  float* master, void* params_flat, int param_dtype, int grid,
+                                  cudaStream_t s);
+// dir 0: rank-major -> flat (export); 1: flat -> rank-major (import)
+cudaError_t launch_state_copy(const Tile* tiles, int n_tiles, float* shard_buf, float* flat_buf,
+                              int dir, int grid, cudaStream_t s);
+cudaError_t launch_gather(const Tile* tiles, int n_tiles, const void* params_flat,
+                          void* const* dst_table, int n_params, int n_replicas, int elem_bytes,
+                          int grid, cudaStream_t s);
+
+}  // namespace zg

@@ -1,0 +1,86 @@
+// Layout copies over the real elements of every tile: state initialisation,
+// rank-major <-> flat state export/import, and K4, the gather of the flat
+// parameters into per-tensor storage (leetllm "Deep dive: Megatron",
+// "Distributed optimizer": the all-gather rebuilds the parameter buffer for
+// the next forward).
+#include "vec.cuh"
+
+namespace zg {
+
+// master[shard] <- init[flat]; params_flat[flat] <- RNE(init[flat]).
+template <typename PT>
+__global__ void __launch_bounds__(kThreads)
+    k_init_from_flat(const Tile* __restrict__ tiles, int n_tiles, const float* __restrict__ init,
+                     float* __restrict__ master, PT* __restrict__ params) {
+  for (int t = blockIdx.x; t < n_tiles; t += gridDim.x) {
+    const Tile tl = tiles[t];
+    for (int i = threadIdx.x; i < tl.len; i += kThreads) {
+      const float x = init[tl.flat + i];
+      master[tl.shard + i] = x;
+      params[tl.flat + i] = DT<PT>::from_f32(x);
+    }
+  }
+}
+
+cudaError_t launch_init_from_flat(const Tile* tiles, int n_tiles, const float* master_flat,
+                                  float* master, void* params_flat, int param_dtype, int grid,
+                                  cudaStream_t s) {
+  if (param_dtype == kF16)
+    k_init_from_flat<__half><<<grid, kThreads, 0, s>>>(tiles, n_tiles, master_flat, master,
+                                                       static_cast<__half*>(params_flat));
+  else
+    k_init_from_flat<__nv_bfloat16><<<grid, kThreads, 0, s>>>(
+        tiles, n_tiles, master_flat, master, static_cast<__nv_bfloat16*>(params_flat));
+  return cudaGetLastError();
+}
+
+__global__ void __launch_bounds__(kThreads)
+    k_state_copy(const Tile* __restrict__ tiles, int n_tiles, float* __restrict__ shard_buf,
+                 float* __restrict__ flat_buf, int dir) {
+  for (int t = blockIdx.x; t < n_tiles; t += gridDim.x) {
+    const Tile tl = tiles[t];
+    for (int i = threadIdx.x; i < tl.len; i += kThreads) {
+      if (dir == 0)
+        flat_buf[tl.flat + i] = shard_buf[tl.shard + i];
+      else
+        shard_buf[tl.shard + i] = flat_buf[tl.flat + i];
+    }
+  }
+}
+
+cudaError_t launch_state_copy(const Tile* tiles, int n_tiles, float* shard_buf, float* flat_buf,
+                              int dir, int grid, cudaStream_t s) {
+  k_state_copy<<<grid, kThreads, 0, s>>>(tiles, n_tiles, shard_buf, flat_buf, dir);
+  return cudaGetLastError();
+}
+
+// K4: dst[k * n_params + p][in_param + i] <- params_flat[flat + i] for every
+// replica k. 16-byte vectors where the destination is 16-byte aligned (tile
+// starts are 64-element aligned inside a parameter), element copies otherwise.
+__global__ void __launch_bounds__(kThreads)
+    k_gather(const Tile* __restrict__ tiles, int n_tiles, const uint16_t* __restrict__ src,
+             void* const* __restrict__ dst_table, int n_params, int n_replicas) {
+  for (int t = blockIdx.x; t < n_tiles; t += gridDim.x) {
+    const Tile tl = tiles[t];
+    const uint16_t* s = src + tl.flat;
+    for (int k = 0; k < n_replicas; ++k) {
+      uint16_t* d = static_cast<uint16_t*>(dst_table[(int64_t)k * n_params + tl.param]) + tl.in_param;
+      const bool vec = (reinterpret_cast<uintptr_t>(d) & 15u) == 0;
+      const int nvec = vec ? (tl.len >> 3) : 0;
+      for (int vi = threadIdx.x; vi < nvec; vi += kThreads)
+        st_stream(d + (int64_t)vi * 8, __ldg(reinterpret_cast<const uint4*>(s) + vi));
+      for (int i = nvec * 8 + threadIdx.x; i < tl.len; i += kThreads) d[i] = s[i];
+    }
+  }
+}
+
+cudaError_t launch_gather(const Tile* tiles, int n_tiles, const void* params_flat,
+                          void* const* dst_table, int n_params, int n_replicas, int elem_bytes,
+                          int grid, cudaStream_t s) {
+  if (elem_bytes != 2) return cudaErrorInvalidValue;
+  k_gather<<<grid, kThreads, 0, s>>>(tiles, n_tiles, static_cast<const uint16_t*>(params_flat),
+                                     dst_table, n_params, n_replicas);
+  return cudaGetLastError();
+}
+
+}  // namespace zg

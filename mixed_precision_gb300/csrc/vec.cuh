@@ -1,0 +1,149 @@
+// Device helpers shared by the kernels: 8-element vector loads/stores of
+// fp32 / fp16 / bf16 with streaming cache hints, dtype traits, and
+// deterministic block reductions.
+#pragma once
+
+#include <cstdint>
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "internal.h"
+
+namespace zg {
+
+// ---- streaming 16-byte accesses (each element is touched once per kernel) --
+
+__device__ __forceinline__ uint4 ld_stream(const void* p) {
+  return __ldcs(reinterpret_cast<const uint4*>(p));
+}
+__device__ __forceinline__ void st_stream(void* p, uint4 v) {
+  __stcs(reinterpret_cast<uint4*>(p), v);
+}
+
+// ---- dtype traits -----------------------------------------------------------
+
+template <typename T> struct DT;
+template <> struct DT<float> {
+  static constexpr int kBytes = 4;
+  __device__ static float to_f32(float x) { return x; }
+  __device__ static float from_f32(float x) { return x; }
+  __device__ static bool finite_bits(float x) {
+    return (__float_as_uint(x) & 0x7F800000u) != 0x7F800000u;
+  }
+};
+template <> struct DT<__half> {
+  static constexpr int kBytes = 2;
+  __device__ static float to_f32(__half x) { return __half2float(x); }
+  __device__ static __half from_f32(float x) { return __float2half_rn(x); }
+  __device__ static bool finite_bits(__half x) {
+    return (__half_as_ushort(x) & 0x7C00u) != 0x7C00u;
+  }
+};
+template <> struct DT<__nv_bfloat16> {
+  static constexpr int kBytes = 2;
+  __device__ static float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+  __device__ static __nv_bfloat16 from_f32(float x) { return __float2bfloat16_rn(x); }
+  __device__ static bool finite_bits(__nv_bfloat16 x) {
+    return (__bfloat16_as_ushort(x) & 0x7F80u) != 0x7F80u;
+  }
+};
+
+// 8 consecutive elements of T as fp32 (one 16-byte load for 2-byte types,
+// two for fp32). p must be 16-byte aligned.
+template <typename T>
+__device__ __forceinline__ void load8(const T* p, float (&x)[8]) {
+  if constexpr (sizeof(T) == 4) {
+    uint4 a = ld_stream(p), b = ld_stream(p + 4);
+    x[0] = __uint_as_float(a.x); x[1] = __uint_as_float(a.y);
+    x[2] = __uint_as_float(a.z); x[3] = __uint_as_float(a.w);
+    x[4] = __uint_as_float(b.x); x[5] = __uint_as_float(b.y);
+    x[6] = __uint_as_float(b.z); x[7] = __uint_as_float(b.w);
+  } else {
+    uint4 a = ld_stream(p);
+    const T* h = reinterpret_cast<const T*>(&a);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) x[j] = DT<T>::to_f32(h[j]);
+  }
+}
+
+// 8 raw elements of T (no conversion).
+template <typename T>
+struct Pack8 {
+  T e[8];
+};
+
+template <typename T>
+__device__ __forceinline__ void store8_raw(T* p, const Pack8<T>& v) {
+  if constexpr (sizeof(T) == 4) {
+    const uint4* u = reinterpret_cast<const uint4*>(v.e);
+    st_stream(p, u[0]);
+    st_stream(p + 4, u[1]);
+  } else {
+    st_stream(p, *reinterpret_cast<const uint4*>(v.e));
+  }
+}
+
+template <typename T>
+__device__ __forceinline__ Pack8<T> load8_raw(const T* p) {
+  Pack8<T> v;
+  if constexpr (sizeof(T) == 4) {
+    uint4* u = reinterpret_cast<uint4*>(v.e);
+    u[0] = ld_stream(p);
+    u[1] = ld_stream(p + 4);
+  } else {
+    *reinterpret_cast<uint4*>(v.e) = ld_stream(p);
+  }
+  return v;
+}
+
+__device__ __forceinline__ void load8_f32(const float* p, float (&x)[8]) {
+  uint4 a = ld_stream(p), b = ld_stream(p + 4);
+  x[0] = __uint_as_float(a.x); x[1] = __uint_as_float(a.y);
+  x[2] = __uint_as_float(a.z); x[3] = __uint_as_float(a.w);
+  x[4] = __uint_as_float(b.x); x[5] = __uint_as_float(b.y);
+  x[6] = __uint_as_float(b.z); x[7] = __uint_as_float(b.w);
+}
+
+__device__ __forceinline__ void store8_f32(float* p, const float (&x)[8]) {
+  st_stream(p, make_uint4(__float_as_uint(x[0]), __float_as_uint(x[1]), __float_as_uint(x[2]),
+                          __float_as_uint(x[3])));
+  st_stream(p + 4, make_uint4(__float_as_uint(x[4]), __float_as_uint(x[5]), __float_as_uint(x[6]),
+                              __float_as_uint(x[7])));
+}
+
+// ---- deterministic block reductions (fixed shuffle tree, fixed warp order) --
+
+template <int kBlock>
+__device__ __forceinline__ double block_sum(double x, double* smem /* kBlock/32 */) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x += __shfl_down_sync(0xffffffffu, x, o);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) smem[warp] = x;
+  __syncthreads();
+  double r = 0.0;
+  if (warp == 0) {
+    r = lane < kBlock / 32 ? smem[lane] : 0.0;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) r += __shfl_down_sync(0xffffffffu, r, o);
+  }
+  __syncthreads();
+  return r;  // valid in thread 0
+}
+
+template <int kBlock>
+__device__ __forceinline__ unsigned block_or(unsigned x, unsigned* smem) {
+  x = __any_sync(0xffffffffu, x != 0u) ? 1u : 0u;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) smem[warp] = x;
+  __syncthreads();
+  unsigned r = 0u;
+  if (warp == 0) {
+    r = lane < kBlock / 32 ? smem[lane] : 0u;
+    r = __any_sync(0xffffffffu, r != 0u) ? 1u : 0u;
+  }
+  __syncthreads();
+  return r;
+}
+
+}  // namespace zg

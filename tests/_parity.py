@@ -1,0 +1,144 @@
+"""Run the CUDA step and the oracle step side by side on the same seeded inputs.
+
+The CUDA side goes through the C ABI (mixed_precision_gb300); the oracle side
+through its own ctypes wrapper. The two share only the seeded input generators
+(workloads). The oracle's state evolves from its own results; nothing measured
+on the GPU is ever fed back into it.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+import workloads as wl
+from _util import rel_err, ulp_diff16
+from mixed_precision_gb300.engine import Hparams, ZeroStep
+
+INF_BITS = {wl.BF16: 0x7F80, wl.F16: 0x7C00}
+
+
+def to_np(t: torch.Tensor) -> np.ndarray:
+    t = t.detach().cpu().contiguous()
+    if t.dtype == torch.float32:
+        return t.numpy()
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+def same_bits_or_both_nan(a: np.ndarray, b: np.ndarray, dtype: int) -> bool:
+    if np.array_equal(a, b):
+        return True
+    fa, fb = oracle.decode(a, dtype), oracle.decode(b, dtype)
+    diff = a != b
+    return bool(np.all(np.isnan(fa[diff]) & np.isnan(fb[diff])))
+
+
+class Pair:
+    def __init__(self, shapes, world, stage, bucket_bytes, grad_dtype, param_dtype, comm_dtype=-1,
+                 init_scale=1.0, dynamic=False, growth_interval=1000, index=9, master_sigma=0.02):
+        self.shapes = shapes
+        self.numel = wl.numels(shapes)
+        self.W, self.stage, self.bucket = world, stage, bucket_bytes
+        self.gdt, self.pdt = grad_dtype, param_dtype
+        self.cdt = grad_dtype if comm_dtype < 0 else comm_dtype
+        self.index = index
+        self.z = ZeroStep(shapes, world, stage, bucket_bytes, grad_dtype, param_dtype, comm_dtype)
+        self.z.allocate()
+        self.L = oracle.layout(self.numel, world, bucket_bytes, wl.ELEM_BYTES[grad_dtype])
+        assert self.z.np == self.L.np_total
+        self.np = self.L.np_total
+        master0 = wl.master_init(self.z.offsets, self.numel, self.np, master_sigma,
+                                 wl.master_seed(index))
+        m0 = master0.cuda() if self.np else torch.zeros(8, device="cuda")
+        self.z.init(m0, init_scale=init_scale, dynamic=dynamic,
+                    growth_interval=growth_interval)
+        self.perm = self.L.flat_of_shard()
+        self.mask_flat = self.L.real_mask().astype(bool)
+        self.mask_shard = self.mask_flat[self.perm]
+        self.o_master = master0.numpy()[self.perm].copy()
+        self.o_m = np.zeros(self.np, np.float32)
+        self.o_v = np.zeros(self.np, np.float32)
+        self.o_params = oracle.encode(master0.numpy(), param_dtype)
+        self.o_params[~self.mask_flat] = 0
+        self.o_scaler = oracle.Scaler(scale=init_scale, dynamic=dynamic,
+                                      growth_interval=growth_interval)
+        self.o_out = None
+        if stage == 1:
+            self.o_out = [np.zeros(self.np, oracle.storage_dtype(self.cdt)) for _ in range(world)]
+
+    def grads(self, step: int, sigma: float, zero_params=(), inject=None):
+        """Seeded flat gradients (CPU) for this step; inject = [(rank, flat_index, bits)]."""
+        out = []
+        for r in range(self.W):
+            g = wl.flat_grads(self.z.offsets, self.numel, self.np, sigma,
+                              wl.grad_seed(self.index, r, step), self.gdt,
+                              zero_params=zero_params)
+            out.append(g)
+        for rank, idx, bits in (inject or []):
+            out[rank].view(torch.int16)[idx] = int(np.array(bits, np.uint16).view(np.int16))
+        return out
+
+    def step(self, grads_cpu, hp: Hparams, mode: str = "flat"):
+        dev = [g.cuda() if g.numel() else torch.empty(8, dtype=g.dtype, device="cuda")
+               for g in grads_cpu]
+        if mode == "flat":
+            self.z.step(dev, hp)
+        elif mode == "tensors":
+            per = []
+            for r in range(self.W):
+                row = []
+                for p, (off, n) in enumerate(zip(self.z.offsets, self.numel)):
+                    t = grads_cpu[r][off:off + n]
+                    row.append(None if (n == 0 or not t.any()) else t.clone().cuda())
+                per.append(row)
+            self.z.step_tensors(per, hp)
+        elif mode == "host":
+            pinned = [(g if g.numel() else torch.empty(8, dtype=g.dtype)).pin_memory()
+                      for g in grads_cpu]
+            self.z.step_host(pinned, dev, hp)
+        else:
+            raise ValueError(mode)
+        torch.cuda.synchronize()
+        gpu_state = self.z.scaler_state()
+        o_hp = oracle.Hparams(hp.lr, hp.beta1, hp.beta2, hp.eps, hp.weight_decay, hp.max_grad_norm,
+                              hp.grad_divisor)
+        info = oracle.zero_step(self.numel, self.W, self.stage, self.bucket, self.gdt, self.cdt,
+                                self.pdt, [to_np(g) for g in grads_cpu], self.o_master, self.o_m,
+                                self.o_v, self.o_params, o_hp, self.o_scaler,
+                                allreduce_out=self.o_out)
+        return gpu_state, info, grads_cpu
+
+    def check(self, gpu_state, info, grads_cpu, rtol=1e-5):
+        """Every acceptance check of one step; returns the worst relative error."""
+        sc = self.o_scaler
+        assert gpu_state["overflow"] == info.overflow
+        assert gpu_state["skipped"] == info.skipped
+        assert gpu_state["scale"] == sc.scale
+        assert gpu_state["counter"] == sc.counter
+        assert gpu_state["t"] == sc.t
+        if np.isfinite(info.grad_norm):
+            assert abs(gpu_state["grad_norm"] - info.grad_norm) <= 1e-6 * max(info.grad_norm, 1e-300)
+        if not info.skipped:
+            assert abs(gpu_state["clip_coef"] - info.clip_coef) <= 1e-6 * info.clip_coef
+        # reduced values: bit-exact
+        if self.stage == 2:
+            got = to_np(self.z.scratch)[:self.np]
+            exp = np.zeros(self.np, oracle.storage_dtype(self.cdt))
+            gn = [to_np(g) for g in grads_cpu]
+            for _, _, f0, s0, ln in self.L.shard_ranges():
+                exp[s0:s0 + ln] = oracle.reduce(gn, self.gdt, self.cdt, f0, f0 + ln, self.L.real_mask())
+            assert same_bits_or_both_nan(got[self.mask_shard], exp[self.mask_shard], self.cdt)
+        else:
+            for w in range(self.W):
+                got = to_np(self.z.allreduce_out[w])[:self.np]
+                assert same_bits_or_both_nan(got[self.mask_flat], self.o_out[w][self.mask_flat],
+                                             self.cdt)
+        worst = 0.0
+        for gpu_t, ref in ((self.z.master, self.o_master), (self.z.m, self.o_m), (self.z.v, self.o_v)):
+            got = to_np(gpu_t)[:self.np][self.mask_shard]
+            e = rel_err(got, ref[self.mask_shard])
+            worst = max(worst, float(e.max()) if e.size else 0.0)
+        assert worst <= rtol, worst
+        p = to_np(self.z.params_flat)[:self.np]
+        assert ulp_diff16(p[self.mask_flat], self.o_params[self.mask_flat]).max(initial=0) <= 1
+        return worst

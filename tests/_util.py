@@ -1,0 +1,21 @@
+"""Comparison helpers for the parity tests (no step arithmetic)."""
+import numpy as np
+
+
+def ordered16(bits: np.ndarray) -> np.ndarray:
+    """Map 16-bit sign-magnitude float patterns to integers ordered like the values."""
+    b = bits.astype(np.int32)
+    mag = b & 0x7FFF
+    return np.where(b & 0x8000, -mag, mag)
+
+
+def ulp_diff16(a: np.ndarray, b: np.ndarray) -> np.ndarray:
+    return np.abs(ordered16(a) - ordered16(b))
+
+
+def rel_err(got: np.ndarray, ref: np.ndarray, tiny: float = 1e-30) -> np.ndarray:
+    """|got - ref| / |ref|, or the absolute difference where |ref| < tiny."""
+    got = got.astype(np.float64)
+    ref = ref.astype(np.float64)
+    d = np.abs(got - ref)
+    return np.where(np.abs(ref) < tiny, d, d / np.maximum(np.abs(ref), tiny))

@@ -1,0 +1,243 @@
+"""CUDA path versus the oracle, element by element, through the C ABI.
+
+Acceptance: reduced (communication-dtype) values, the overflow flag and the
+loss-scale/step-count trajectory bit-exact; fp32 master/m/v within 1e-5
+relative error (absolute below 1e-30); cast-out parameters within 1 ulp.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as wl
+from _parity import INF_BITS, Pair, to_np
+from mixed_precision_gb300 import ZeroError
+from mixed_precision_gb300.engine import Hparams
+
+pytestmark = pytest.mark.gpu
+
+
+def small_qwen_shapes():
+    return wl.qwen3_0_6b_shapes(vocab=1000, hidden=128, layers=2, q_dim=256, kv_dim=128, ffn=384,
+                                head_dim=32)
+
+
+def test_tiny_four_steps_with_inf():
+    """The tiny fp16 workload: W=2, ZeRO-2, S0 = 2^16, +inf in step 3."""
+    w = wl.workload("tiny")
+    pr = Pair(w.shapes, w.world, w.stage, w.bucket_bytes, w.grad_dtype, w.param_dtype,
+              init_scale=w.init_scale, dynamic=True, index=w.index)
+    hp = Hparams(lr=w.lr, weight_decay=w.weight_decay, max_grad_norm=w.max_grad_norm)
+    rank, idx = wl.inject_position(pr.numel, pr.z.offsets, w.world, seed=1234)
+    scales, ts = [], []
+    for step in range(1, 5):
+        inj = [(rank, idx, INF_BITS[wl.F16])] if step == 3 else None
+        g = pr.grads(step, w.grad_sigma, inject=inj)
+        st, info, gc = pr.step(g, hp)
+        pr.check(st, info, gc)
+        scales.append(st["scale"])
+        ts.append(st["t"])
+        assert st["overflow"] == (1 if step == 3 else 0)
+    assert ts == [1, 2, 2, 3]
+    assert scales == [2.0 ** 16, 2.0 ** 16, 2.0 ** 15, 2.0 ** 15]
+
+
+@pytest.mark.parametrize("W,stage,gdt,cdt,pdt,bucket", [
+    (2, 2, wl.BF16, -1, wl.BF16, 64_000),
+    (2, 1, wl.BF16, -1, wl.BF16, 64_000),
+    (4, 2, wl.F16, wl.F32, wl.F16, 200_000),
+    (8, 2, wl.BF16, -1, wl.BF16, 500_000_000),
+    (3, 2, wl.BF16, -1, wl.F16, 30_000),
+    (5, 1, wl.F32, wl.BF16, wl.BF16, 100_000),
+    (1, 2, wl.F16, -1, wl.F16, 50_000),
+])
+def test_small_qwen_shaped(W, stage, gdt, cdt, pdt, bucket):
+    pr = Pair(small_qwen_shapes(), W, stage, bucket, gdt, pdt, cdt, init_scale=8.0, index=20 + W)
+    for step, hp in enumerate([Hparams(), Hparams(max_grad_norm=0.0, grad_divisor=1.0),
+                               Hparams(lr=3e-4, weight_decay=0.1, max_grad_norm=1e-3)]):
+        st, info, gc = pr.step(pr.grads(step, 1e-3), hp)
+        pr.check(st, info, gc)
+        assert st["t"] == step + 1
+
+
+def test_stage1_equals_stage2_bitwise():
+    shapes = small_qwen_shapes()
+    res = []
+    for stage in (1, 2):
+        pr = Pair(shapes, 8, stage, 100_000, wl.F16, wl.F16, init_scale=2.0 ** 16, dynamic=True,
+                  index=31)
+        for step in range(3):
+            st, info, gc = pr.step(pr.grads(step, 1e-4), Hparams())
+            pr.check(st, info, gc)
+        res.append([to_np(t) for t in (pr.z.master, pr.z.m, pr.z.v, pr.z.params_flat)] + [st])
+    for a, b in zip(res[0][:4], res[1][:4]):
+        assert np.array_equal(a, b)
+    assert res[0][4] == res[1][4]
+
+
+@pytest.mark.parametrize("W", [3, 16, 64])
+def test_generic_world_and_ragged(W):
+    """Odd and large W (the runtime-W kernel path), 1-element, empty and ragged
+    parameters that straddle bucket and shard boundaries."""
+    rng = np.random.default_rng(W)
+    sizes = [1, 0, 7, 63, 64, 65, 129, 8191, 8193, 20000, 3, 1]
+    sizes += [int(x) for x in rng.integers(1, 3000, size=10)]
+    shapes = [(s,) for s in sizes]
+    pr = Pair(shapes, W, 2, 4096 * 2, wl.BF16, wl.BF16, index=40 + W)
+    for step in range(2):
+        st, info, gc = pr.step(pr.grads(step, 1e-2), Hparams(max_grad_norm=0.5))
+        pr.check(st, info, gc)
+
+
+def test_pointer_table_mode_matches_flat():
+    """Per-tensor gradient pointers (NULL = all-zero) give the same bits as the
+    flat buffers with those parameters zeroed."""
+    shapes = small_qwen_shapes()
+    zero = (1, 4, 7)
+    outs = []
+    for mode in ("flat", "tensors"):
+        pr = Pair(shapes, 4, 2, 80_000, wl.BF16, wl.BF16, index=50)
+        for step in range(2):
+            g = pr.grads(step, 1e-3, zero_params=zero)
+            st, info, gc = pr.step(g, Hparams(), mode=mode)
+            pr.check(st, info, gc)
+        outs.append([to_np(t) for t in (pr.z.master, pr.z.m, pr.z.v, pr.z.params_flat)])
+    for a, b in zip(*outs):
+        assert np.array_equal(a, b)
+
+
+def test_host_entry_point_matches_device():
+    shapes = small_qwen_shapes()
+    outs = []
+    for mode in ("flat", "host"):
+        pr = Pair(shapes, 2, 2, 500_000_000, wl.BF16, wl.BF16, index=60)
+        st, info, gc = pr.step(pr.grads(0, 1e-3), Hparams(), mode=mode)
+        pr.check(st, info, gc)
+        outs.append([to_np(t) for t in (pr.z.master, pr.z.params_flat)])
+    for a, b in zip(*outs):
+        assert np.array_equal(a, b)
+
+
+def test_overflow_at_shard_edges_skips():
+    """+inf / -inf / NaN at the first or last real element of shards in the
+    first and last rank: flag set, step skipped, state untouched, scale halved."""
+    shapes = [(300,), (64,), (513,), (1000,)]
+    pr = Pair(shapes, 3, 2, 1024, wl.F16, wl.F16, init_scale=1024.0, dynamic=True, index=70)
+    st, info, gc = pr.step(pr.grads(0, 1e-2), Hparams())
+    pr.check(st, info, gc)
+    positions = []
+    for _, _, f0, _, ln in pr.L.shard_ranges():
+        real = np.nonzero(pr.mask_flat[f0:f0 + ln])[0]
+        if len(real):
+            positions += [f0 + int(real[0]), f0 + int(real[-1])]
+    bad_bits = [0x7C00, 0xFC00, 0x7E00]
+    for k, pos in enumerate(positions[:8]):
+        before = [to_np(t).copy() for t in (pr.z.master, pr.z.m, pr.z.v, pr.z.params_flat)]
+        rank = 0 if k % 2 == 0 else pr.W - 1
+        g = pr.grads(k + 1, 1e-2, inject=[(rank, pos, bad_bits[k % 3])])
+        st, info, gc = pr.step(g, Hparams())
+        assert st["overflow"] == 1 and st["skipped"] == 1
+        pr.check(st, info, gc)
+        after = [to_np(t) for t in (pr.z.master, pr.z.m, pr.z.v, pr.z.params_flat)]
+        for a, b in zip(before, after):
+            assert np.array_equal(a, b)
+
+
+def test_fp16_overflow_only_after_reduction():
+    """Finite fp16 inputs whose fp32 sum rounds past 65504 overflow in fp16
+    communication but not in fp32 communication."""
+    shapes = [(4096,), (100,)]
+    for cdt, expect in ((wl.F16, 1), (wl.F32, 0)):
+        pr = Pair(shapes, 2, 2, 1 << 20, wl.F16, wl.F16, cdt, init_scale=4.0, dynamic=True, index=80)
+        g = pr.grads(0, 1e-2)
+        for r in range(2):
+            g[r][17] = 40000.0
+        st, info, gc = pr.step(g, Hparams())
+        assert st["overflow"] == expect
+        pr.check(st, info, gc)
+
+
+def test_padding_garbage_is_ignored():
+    """The gradient buffers' padding holds NaN (the generator's default) and the
+    step still matches the oracle, which never reads padding."""
+    pr = Pair([(100,), (30,), (200,)], 2, 2, 512, wl.BF16, wl.BF16, index=90)
+    st, info, gc = pr.step(pr.grads(0, 1e-2), Hparams())
+    assert np.isnan(gc[0][100].float().item())
+    assert st["overflow"] == 0
+    pr.check(st, info, gc)
+
+
+def test_scaler_growth_and_long_trajectory():
+    """fp16, W=8, dynamic scaling with growth after N=10 clean steps and an
+    +inf every 7th step: 40 steps, scale/counter/t bit-exact every step."""
+    shapes = [(1000,), (129,), (4000,)]
+    pr = Pair(shapes, 8, 2, 4096, wl.F16, wl.F16, init_scale=2.0 ** 10, dynamic=True,
+              growth_interval=10, index=95)
+    rank, idx = wl.inject_position(pr.numel, pr.z.offsets, 8, seed=5)
+    seen_growth = False
+    prev = 2.0 ** 10
+    for step in range(1, 41):
+        inj = [(rank, idx, INF_BITS[wl.F16])] if step % 7 == 0 else None
+        st, info, gc = pr.step(pr.grads(step, 1e-3, inject=inj), Hparams())
+        pr.check(st, info, gc)
+        seen_growth |= st["scale"] > prev
+        prev = st["scale"]
+    assert seen_growth
+
+
+def test_empty_model():
+    """All parameters empty: no element work, the step still advances t."""
+    pr = Pair([(0,), (0, 5)], 2, 2, 1024, wl.BF16, wl.BF16, index=99)
+    st, info, gc = pr.step(pr.grads(0, 1e-3), Hparams())
+    assert st["t"] == 1 and info.grad_norm == 0.0
+
+
+def test_gather_export_import():
+    shapes = small_qwen_shapes()
+    pr = Pair(shapes, 4, 2, 100_000, wl.BF16, wl.BF16, index=101)
+    st, info, gc = pr.step(pr.grads(0, 1e-3), Hparams())
+    pr.check(st, info, gc)
+    z = pr.z
+    # K4: two replicas of per-tensor storage, one of them deliberately offset by
+    # one element (2-byte aligned only) to take the unaligned path
+    backing = torch.empty(z.np + 64, dtype=torch.bfloat16, device="cuda")
+    rep0 = [torch.empty(s, dtype=torch.bfloat16, device="cuda") for s in shapes]
+    rep1, at = [], 1
+    for s, n in zip(shapes, pr.numel):
+        rep1.append(backing[at:at + n].view(s))
+        at += n + 1
+    z.gather([rep0, rep1])
+    torch.cuda.synchronize()
+    for p in range(len(shapes)):
+        ref = z.param_view(z.params_flat, p)
+        assert torch.equal(rep0[p].view(torch.int16), ref.view(torch.int16))
+        assert torch.equal(rep1[p].view(torch.int16), ref.view(torch.int16))
+    # export to flat order and back
+    master_f, m_f, v_f = z.export_state()
+    exp_master = np.zeros(z.np, np.float32)
+    exp_master[pr.perm] = pr.o_master
+    got = to_np(master_f)
+    assert np.allclose(got[pr.mask_flat], exp_master[pr.mask_flat], rtol=1e-5, atol=0)
+    assert np.all(got[~pr.mask_flat] == 0)
+    saved = [to_np(t).copy() for t in (z.master, z.m, z.v)]
+    z.master.zero_(), z.m.zero_(), z.v.zero_()
+    z.import_state(master_f, m_f, v_f)
+    torch.cuda.synchronize()
+    for t, s in zip((z.master, z.m, z.v), saved):
+        assert np.array_equal(to_np(t)[pr.mask_shard], s[pr.mask_shard])
+
+
+def test_invalid_device_arguments():
+    pr = Pair([(100,)], 2, 2, 1024, wl.BF16, wl.BF16, index=102)
+    g = [x.cuda() for x in pr.grads(0, 1e-3)]
+    hp = Hparams()
+    with pytest.raises(ZeroError) as e:
+        pr.z.step([g[0], g[1][1:]], hp)  # 2-byte offset: not 16-byte aligned
+    assert e.value.code == 1
+    with pytest.raises(ZeroError) as e:
+        pr.z.step(g, Hparams(beta1=1.0))
+    assert e.value.code == 1
+    # nothing was enqueued: a valid step afterwards is the first one
+    pr.z.step(g, hp)
+    torch.cuda.synchronize()
+    assert pr.z.scaler_state()["t"] == 1
