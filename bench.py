@@ -1,0 +1,462 @@
+"""Benchmark of the ZeRO-1/2 gradient-and-optimizer step on GB300.
+
+One "step" is one pass of the whole hot path over one batch of synthetic
+gradients: the W-way reduce with overflow/norm partials, the finalize kernel
+(norm, clip, loss-scale state machine) and the fused unscale/clip/AdamW/
+cast-out kernel. Default workload: the Qwen3-0.6B-shaped parameter list
+(596,049,920 elements, 310 tensors), W = 2 simulated ranks, ZeRO-2, bf16
+gradients N(0, 1e-4), bucket 500 MB, clip 1.0. Inputs (2.4 GB of gradients,
+7.2 GB of fp32 state) are larger than the 129 MB L2, so no flush is needed.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+N > 1 (torchrun, one rank per GPU) runs N independent replicas of the same
+workload (weak scaling: the simulated ranks already live inside each GPU).
+Rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "ZeRO step params updated/s and achieved HBM GB/s (% of GB300 step roofline)"
+DEFAULT_WORKLOAD = "qwen3_0.6b_bf16_w2"
+L2_BYTES = 129 * 1000 * 1000
+# Bytes the library copies back per zero_loss_scale_state call (its device
+# scalar block: 8 eight-byte fields, 4 ints, 3 doubles, 10 floats).
+STATE_READ_BYTES = 144
+# DRAM bytes per real element of the update kernel from one ncu capture
+# (dram__bytes_read.sum + dram__bytes_write.sum / elements), with the capture
+# it comes from; None until a capture of the current kernel exists.
+NCU_TRAFFIC_PER_ELEM = {
+    # profiles/k_adamw_cast_qwen3_layers8.md: (1.763 + 1.703) GB / 125,847,552 elements
+    "k_adamw_cast": 27.54,
+    # profiles/k_reduce_norm_qwen3_layers8.md: (504.1 + 211.7) MB / 125,847,552 elements
+    "k_reduce_norm": 5.69,
+}
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="target CPU time of the oracle sample")
+    return ap.parse_args(argv)
+
+
+# ---------------------------------------------------------------------------
+# Distributed plumbing (timing only: no collective touches the data path)
+# ---------------------------------------------------------------------------
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def init_dist(world: int, backend: str):
+    if world <= 1:
+        return None
+    import torch.distributed as dist
+    if not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+    return dist
+
+
+def barrier(dist, device=None):
+    if dist is not None:
+        if device is not None and dist.get_backend() == "nccl":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+def max_over_ranks(dist, value: float, device=None) -> float:
+    """Largest value over all ranks (the slowest rank sets the job's time)."""
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device if device is not None else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(units_per_rank: float, n_ranks: int, seconds: float) -> float:
+    """Whole-job throughput: the units every rank processed over the slowest time."""
+    return units_per_rank * n_ranks / seconds
+
+
+# ---------------------------------------------------------------------------
+# Clock sampling during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons every 200 ms while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self._thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return self
+        self._thread = threading.Thread(target=self._read, daemon=True)
+        self._thread.start()
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self._thread is not None:
+            self._thread.join(timeout=2)
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for name, flag in zip(names, parts[5:9]):
+                if flag.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "power_w_max": max(power), "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------------------
+# Shared helpers
+# ---------------------------------------------------------------------------
+
+def hbm_peak():
+    """(GB/s, source): the measured copy bandwidth, else the fallback."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+def config_of(w, scaling_note=None) -> dict:
+    import workloads as wl
+    cfg = {"workload": w.name, "n_params": w.n_real, "tensors": len(w.shapes),
+           "world_simulated": w.world, "zero_stage": w.stage,
+           "grad_dtype": wl.DTYPE_NAME[w.grad_dtype], "param_dtype": wl.DTYPE_NAME[w.param_dtype],
+           "comm_dtype": wl.DTYPE_NAME[w.comm_dtype], "bucket_bytes": w.bucket_bytes,
+           "clip": w.max_grad_norm, "grad_sigma": w.grad_sigma,
+           "l2": "inputs larger than L2 (no flush)", "parallelism": "replicas"}
+    if scaling_note:
+        cfg["note"] = scaling_note
+    return cfg
+
+
+def sample_shapes(shapes, target_elems: int):
+    """A bounded sample of a workload: its tensors in order, skipping any tensor
+    larger than the target, until the target element count is reached."""
+    import workloads as wl
+    out, total = [], 0
+    for s in shapes:
+        n = wl.numels([s])[0]
+        if n > target_elems:
+            continue
+        out.append(s)
+        total += n
+        if total >= target_elems:
+            break
+    return out, total
+
+
+def time_oracle(w, target_elems: int, seconds: float, min_steps: int = 1, warmup: int = 0,
+                steps: int | None = None):
+    """Run the host oracle's ZeRO step on a sample of the workload.
+
+    Returns (params per second, steps timed, sample elements, sample description).
+    Single-threaded: the oracle is plain sequential host code.
+    """
+    import numpy as np
+    import torch
+
+    import oracle
+    import workloads as wl
+
+    shapes, n_sample = sample_shapes(w.shapes, target_elems)
+    numel = wl.numels(shapes)
+    L = oracle.layout(numel, w.world, w.bucket_bytes, wl.ELEM_BYTES[w.grad_dtype])
+
+    def bits(t):
+        return t.numpy() if t.dtype == torch.float32 else t.view(torch.int16).numpy().view(np.uint16)
+
+    grads = [bits(wl.flat_grads(L.param_offset, numel, L.np_total, w.grad_sigma,
+                                wl.grad_seed(w.index, r), w.grad_dtype)) for r in range(w.world)]
+    ms = bits(wl.master_init(L.param_offset, numel, L.np_total, w.master_sigma,
+                             wl.master_seed(w.index)))[L.flat_of_shard()].copy()
+    m, v = np.zeros_like(ms), np.zeros_like(ms)
+    params = np.zeros(L.np_total, oracle.storage_dtype(w.param_dtype))
+    outs = ([np.zeros(L.np_total, oracle.storage_dtype(w.comm_dtype)) for _ in range(w.world)]
+            if w.stage == 1 else None)
+    hp = oracle.Hparams(w.lr, w.beta1, w.beta2, w.eps, w.weight_decay, w.max_grad_norm, 0.0)
+    sc = oracle.Scaler(scale=w.init_scale, dynamic=w.dynamic, growth_interval=w.growth_interval)
+
+    def one():
+        oracle.zero_step(numel, w.world, w.stage, w.bucket_bytes, w.grad_dtype, w.comm_dtype,
+                         w.param_dtype, grads, ms, m, v, params, hp, sc, allreduce_out=outs)
+
+    for _ in range(warmup):
+        one()
+    t0 = time.perf_counter()
+    done = 0
+    while True:
+        one()
+        done += 1
+        el = time.perf_counter() - t0
+        if steps is not None:
+            if done >= steps:
+                break
+        elif done >= min_steps and el >= seconds:
+            break
+    el = time.perf_counter() - t0
+    desc = (f"{len(shapes)} of the workload's {len(w.shapes)} tensors ({n_sample} elements, "
+            f"tensors larger than {target_elems} skipped), W={w.world}, ZeRO-{w.stage}, "
+            f"{done} full oracle steps")
+    return n_sample * done / el, done, n_sample, desc
+
+
+# ---------------------------------------------------------------------------
+# Our arm: the CUDA library through its C ABI
+# ---------------------------------------------------------------------------
+
+def run_ours(args) -> dict | None:
+    import torch
+
+    import workloads as wl
+    from mixed_precision_gb300 import _abi as abi
+    from mixed_precision_gb300.engine import Hparams, ZeroStep
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    dist = init_dist(world, "nccl")
+    w = wl.workload(args.workload)
+    K, W = args.steps, args.warmup
+    if W < 3:
+        raise SystemExit("--warmup must be at least 3")
+
+    z = ZeroStep(w.shapes, w.world, w.stage, w.bucket_bytes, w.grad_dtype, w.param_dtype,
+                 w.comm_dtype)
+    z.allocate()
+    info = z.info
+    numel = wl.numels(w.shapes)
+    master0 = wl.master_init(z.offsets, numel, z.np, w.master_sigma, wl.master_seed(w.index),
+                             device=device)
+    z.init(master0, init_scale=w.init_scale, dynamic=w.dynamic, growth_interval=w.growth_interval)
+    torch.cuda.synchronize()
+    del master0
+    grads = [wl.flat_grads(z.offsets, numel, z.np, w.grad_sigma,
+                           wl.grad_seed(w.index, r + 1000 * rank), w.grad_dtype, device=device)
+             for r in range(w.world)]
+    hp = Hparams(lr=w.lr, beta1=w.beta1, beta2=w.beta2, eps=w.eps, weight_decay=w.weight_decay,
+                 max_grad_norm=w.max_grad_norm)
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    for row in ev:  # events are created on first record
+        for e in row:
+            e.record()
+    for _ in range(W):
+        z.step(grads, hp)
+    torch.cuda.synchronize()
+    barrier(dist, device)
+
+    sampler = ClockSampler(local).start()
+    time.sleep(0.3)
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    t_start.record()
+    for k in range(K):
+        abi.zero_set_step_events(z.handle, [e.cuda_event for e in ev[k]])
+        z.step(grads, hp)
+    t_end.record()
+    torch.cuda.synchronize()
+    abi.zero_set_step_events(z.handle, None)
+    clocks = sampler.stop()
+    barrier(dist, device)
+    local_ms = t_start.elapsed_time(t_end)
+    total_ms = max_over_ranks(dist, local_ms, device)
+    st = z.scaler_state()
+    assert st["overflow"] == 0 and st["steps"] == K + W, st
+
+    k1 = [ev[k][0].elapsed_time(ev[k][1]) for k in range(K)]
+    k2 = [ev[k][1].elapsed_time(ev[k][2]) for k in range(K)]
+    k3 = [ev[k][2].elapsed_time(ev[k][3]) for k in range(K)]
+
+    # A skipped step: +inf in one element, the update kernel returns at once.
+    saved = grads[0][z.offsets[0]].clone()
+    grads[0][z.offsets[0]] = float("inf")
+    torch.cuda.synchronize()
+    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s0.record()
+    for _ in range(3):
+        z.step(grads, hp)
+    s1.record()
+    torch.cuda.synchronize()
+    skip_ms = s0.elapsed_time(s1) / 3
+    assert z.scaler_state()["skipped"] == 1
+    grads[0][z.offsets[0]] = saved
+    torch.cuda.synchronize()
+
+    # End to end through the host-buffer entry point: pinned host gradients are
+    # copied in every step and the step's scaler state is read back.
+    E = max(1, args.e2e_steps)
+    host = [g.cpu().pin_memory() for g in grads]
+    z.step_host(host, grads, hp)
+    z.scaler_state()
+    torch.cuda.synchronize()
+    barrier(dist, device)
+    t0 = time.perf_counter()
+    for _ in range(E):
+        z.step_host(host, grads, hp)
+        z.scaler_state()  # device-to-host read of the step's result; synchronises
+    e2e_s = max_over_ranks(dist, time.perf_counter() - t0, device)
+    del host
+
+    N = info.n_real
+    peak, peak_src = hbm_peak()
+    step_s = total_ms / 1e3 / K
+    G = wl.ELEM_BYTES[w.grad_dtype]
+    C = wl.ELEM_BYTES[w.comm_dtype]
+    P = wl.ELEM_BYTES[w.param_dtype]
+    k1_bytes = N * (w.world * G + (w.world * C if w.stage == 1 else C))
+    k3_bytes = N * (C + 24 + P)
+    k1_ms, k2_ms, k3_ms = statistics.mean(k1), statistics.mean(k2), statistics.mean(k3)
+    dom = ("k_adamw_cast", k3_bytes, k3_ms) if k3_ms >= k1_ms else ("k_reduce_norm", k1_bytes, k1_ms)
+    achieved = dom[1] / (dom[2] / 1e3) / 1e9
+    tr = NCU_TRAFFIC_PER_ELEM.get(dom[0])
+    step_gbs = info.step_bytes_per_elem * N / step_s / 1e9
+    out = {
+        "metric": METRIC,
+        "value": job_value(N, world, step_s),
+        "unit": "params/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": W,
+        "ms_per_step": total_ms / K,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic",
+        "config": config_of(w),
+        "hbm_gbs_step": step_gbs,
+        "step_roofline": {"bytes_per_param": info.step_bytes_per_elem, "peak_gbs": peak,
+                          "frac": step_gbs / peak, "peak_source": peak_src},
+        "roofline": {"bound": "hbm", "kernel": dom[0], "achieved": achieved, "peak": peak,
+                     "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": (tr * N if tr is not None else None),
+                     "algorithmic_bytes_per_launch": dom[1], "peak_source": peak_src},
+        "kernels_ms": {"k_reduce_norm": k1_ms, "k_finalize": k2_ms, "k_adamw_cast": k3_ms,
+                       "k_reduce_norm_gbs": k1_bytes / (k1_ms / 1e3) / 1e9,
+                       "k_adamw_cast_gbs": k3_bytes / (k3_ms / 1e3) / 1e9},
+        "skip_step_ms": skip_ms,
+        "e2e": {"value": job_value(N, world, e2e_s / E), "unit": "params/s",
+                "h2d_bytes_per_step": w.world * z.np * G, "d2h_bytes_per_step": STATE_READ_BYTES},
+        "gpu_launches": 3 * K,
+        "clocks": clocks,
+    }
+    z.close()
+    if dist is not None:
+        dist.destroy_process_group()
+    return out if rank == 0 else None
+
+
+# ---------------------------------------------------------------------------
+# Reference arm: the host oracle (a deliberately slow program)
+# ---------------------------------------------------------------------------
+
+def cpu_baseline(w, seconds: float) -> dict:
+    rate, done, n, desc = time_oracle(w, 20_000_000, seconds)
+    return {"value": rate, "unit": "params/s", "cores": 1, "kind": "oracle", "sample": desc}
+
+
+def run_reference(args) -> dict | None:
+    import workloads as wl
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return None
+    w = wl.workload(args.workload)
+    # size each step's sample so the whole run stays within about two minutes
+    rate0, _, _, _ = time_oracle(w, 1_000_000, 0.0, min_steps=1)
+    per_step = max(1_000_000, int(rate0 * 120.0 / max(1, args.steps + args.warmup)))
+    per_step = min(per_step, 20_000_000)
+    rate, done, n, desc = time_oracle(w, per_step, 0.0, warmup=args.warmup, steps=args.steps)
+    cpu = {"value": rate, "unit": "params/s", "cores": 1, "kind": "oracle", "sample": desc}
+    return {"impl": "reference", "metric": METRIC, "value": rate, "unit": "params/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": n / rate * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": config_of(w),
+            "cpu_baseline": cpu,
+            "e2e": {"value": rate, "unit": "params/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        out = run_reference(args)
+    else:
+        out = run_ours(args)
+        rank, world, _ = dist_env()
+        if out is not None and world == 1 and not args.no_cpu_baseline:
+            import workloads as wl
+            out["cpu_baseline"] = cpu_baseline(wl.workload(args.workload), args.cpu_seconds)
+    if out is not None:
+        print(json.dumps(out), flush=True)
+
+
+if __name__ == "__main__":
+    main()

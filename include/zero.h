@@ -275,6 +275,14 @@ int zero_state_export(zero_layout_t* layout, float* master_flat, float* m_flat, 
 int zero_state_import(zero_layout_t* layout, const float* master_flat, const float* m_flat,
                       const float* v_flat, void* stream);
 
+/* Optional timing hook. events: host array of 4 cudaEvent_t (as void*),
+ * created by the caller; every later step records events[0] before the
+ * reduce kernel, events[1] after it, events[2] after the finalize kernel and
+ * events[3] after the update kernel, on the step's stream. NULL turns the
+ * hook off. The events must outlive their use. No counterpart on the pages:
+ * it exists so a benchmark can time each kernel with CUDA events. */
+int zero_set_step_events(zero_layout_t* layout, void* const* events);
+
 /* Message for the last failing call on this thread ("" if none). The pointer
  * stays valid until the next failing call on this thread. */
 const char* zero_last_error(void);

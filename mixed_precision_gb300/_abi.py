@@ -97,6 +97,7 @@ def lib() -> ctypes.CDLL:
             "zero_state_export": [P, P, P, P, P],
             "zero_state_import": [P, P, P, P, P],
             "zero_layout_set_allocator": [P, ALLOC_FN, FREE_FN, P],
+            "zero_set_step_events": [P, PP],
         }
         for name, args in sig.items():
             fn = getattr(L, name)
@@ -204,6 +205,11 @@ def zero_state_export(layout: int, master_flat: int, m_flat: int, v_flat: int, s
 def zero_state_import(layout: int, master_flat: int, m_flat: int, v_flat: int, stream: int) -> None:
     _check(lib().zero_state_import(layout, master_flat or None, m_flat or None, v_flat or None,
                                    stream or None))
+
+
+def zero_set_step_events(layout: int, events) -> None:
+    """events: four cudaEvent_t handles (ints), or None to turn the hook off."""
+    _check(lib().zero_set_step_events(layout, _ptrs(events) if events is not None else None))
 
 
 def zero_layout_set_allocator(layout: int, alloc, free_fn, ctx: int = 0) -> None:

@@ -92,6 +92,8 @@ struct zero_layout {
   size_t gather_cap = 0;
 
   int grid_reduce = 0, grid_update = 0, grid_copy = 0;
+  cudaEvent_t events[4] = {nullptr, nullptr, nullptr, nullptr};
+  bool timing = false;
 
   int world() const { return cfg.world; }
   int n_params() const { return (int)numel.size(); }
@@ -197,15 +199,18 @@ int launch_step(zero_layout* L, const GradSrc& src, void* const* allreduce_out,
   ra.part_sumsq = L->d_part;
   ra.part_ovf = L->d_ovf;
   int n_part = 0;
+  if (L->timing) ZERO_CUDA(cudaEventRecord(L->events[0], s));
   if (n_tiles > 0) {
     cudaError_t e = launch_reduce(ra, L->grid_reduce, s);
     if (e != cudaSuccess) return cuda_fail(e, "reduce kernel launch");
     n_part = L->grid_reduce;
   }
+  if (L->timing) ZERO_CUDA(cudaEventRecord(L->events[1], s));
   Hparams h{hp->lr, hp->beta1, hp->beta2, hp->eps, hp->weight_decay, hp->max_grad_norm,
             hp->grad_divisor};
   cudaError_t e = launch_finalize(L->d_part, L->d_ovf, n_part, W, h, L->d_state, s);
   if (e != cudaSuccess) return cuda_fail(e, "finalize kernel launch");
+  if (L->timing) ZERO_CUDA(cudaEventRecord(L->events[2], s));
   if (n_tiles > 0) {
     UpdateArgs ua{};
     ua.tiles = L->d_tiles;
@@ -222,6 +227,7 @@ int launch_step(zero_layout* L, const GradSrc& src, void* const* allreduce_out,
     e = launch_update(ua, L->grid_update, s);
     if (e != cudaSuccess) return cuda_fail(e, "update kernel launch");
   }
+  if (L->timing) ZERO_CUDA(cudaEventRecord(L->events[3], s));
   return ZERO_OK;
 }
 
@@ -253,6 +259,20 @@ int check_allreduce(const zero_layout* L, void* const* allreduce_out) {
 extern "C" {
 
 const char* zero_last_error(void) { return g_last_error.c_str(); }
+
+int zero_set_step_events(zero_layout_t* L, void* const* events) {
+  if (int rc = check_layout(L)) return rc;
+  if (events == nullptr) {
+    L->timing = false;
+    return ZERO_OK;
+  }
+  for (int k = 0; k < 4; ++k) {
+    if (events[k] == nullptr) return fail(ZERO_ERR_INVALID, "events[%d] is NULL", k);
+  }
+  for (int k = 0; k < 4; ++k) L->events[k] = static_cast<cudaEvent_t>(events[k]);
+  L->timing = true;
+  return ZERO_OK;
+}
 
 int zero_layout_create(const int64_t* const* shapes, const int* ndims, int n_params,
                        const zero_config* cfg, zero_layout_t** out) {

@@ -13,8 +13,8 @@
 // rank-major scratch at the tile's shard offset (rank `tile.rank`'s
 // reduce-scatter output). Stage 1 writes r into all W flat outputs (the
 // all-reduce). Every thread accumulates sum(r^2) (fp32 over 8 elements, then
-// fp64) and an "any non-finite r" flag; each block writes one fp64 partial and
-// one flag. The grid is persistent (a multiple of the SM count) and walks the
+// a compensated fp32 running sum, fp64 for huge groups) and an "any non-finite
+// r" flag; each block writes one fp64 partial and one flag. The grid is persistent (a multiple of the SM count) and walks the
 // tile list with a fixed stride, so the partials are deterministic.
 #pragma once
 
@@ -50,50 +50,66 @@ __device__ __forceinline__ float load1(const GT* p, int64_t i) {
   return p == nullptr ? 0.0f : DT<GT>::to_f32(p[i]);
 }
 
+// Rank w's gradient pointer for a tile (flat buffers, or the per-tensor table
+// where NULL stands for an all-zero gradient).
+template <typename GT>
+__device__ __forceinline__ const GT* grad_ptr(const ReduceArgs& a, const Tile& tl, int w) {
+  if (a.src.table_mode) {
+    const void* q = a.src.table[(int64_t)w * a.src.n_params + tl.param];
+    return q ? static_cast<const GT*>(q) + tl.in_param : nullptr;
+  }
+  return static_cast<const GT*>(a.src.base[w]) + tl.flat;
+}
+
+// Squares of one group of 8 reduced values, added to a compensated fp32
+// running sum (hi, lo). A group whose fp32 sum is not below 2^100 (or not
+// finite) goes to an fp64 accumulator instead, so the fp32 sum cannot
+// overflow. GB300's fp64 pipe is narrow, so fp64 is kept off the common path.
+__device__ __forceinline__ void add_group(float ss, float& hi, float& lo, double& big,
+                                          const float (&rf)[8]) {
+  if (ss < 0x1p100f) {  // false for +inf and NaN as well
+    const float y = ss - lo;
+    const float t = hi + y;
+    lo = (t - hi) - y;
+    hi = t;
+  } else {
+    double d = 0.0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) d += (double)rf[j] * (double)rf[j];
+    big += d;
+  }
+}
+
 template <typename GT, typename CT, int WT, bool STAGE1>
-__global__ void __launch_bounds__(kThreads) k_reduce_norm(const __grid_constant__ ReduceArgs a) {
-  // Vectors in flight per thread: keep about eight 16-byte gradient loads
-  // outstanding whatever W is.
-  constexpr int U = (WT == 0 || WT >= 8) ? 1 : 8 / WT;
-  __shared__ const GT* s_ptr[kMaxWorld];
-  __shared__ CT* s_out[STAGE1 ? kMaxWorld : 1];
+__global__ void __launch_bounds__(kThreads, 4) k_reduce_norm(const __grid_constant__ ReduceArgs a) {
+  // Vectors in flight per thread: keep up to eight 16-byte gradient loads
+  // outstanding (at most four vectors, to stay within 64 registers).
+  constexpr int U = (WT == 0 || WT >= 8) ? 1 : (8 / WT > 4 ? 4 : 8 / WT);
   __shared__ double s_red[kThreads / 32];
   __shared__ unsigned s_or[kThreads / 32];
 
   const int W = WT ? WT : a.world;
-  double acc = 0.0;
+  float hi = 0.0f, lo = 0.0f;
+  double big = 0.0;
   unsigned bad = 0u;
 
   for (int t = blockIdx.x; t < a.n_tiles; t += gridDim.x) {
     const Tile tl = a.tiles[t];
-    __syncthreads();  // everyone is done with the previous tile's pointers
-    for (int w = threadIdx.x; w < W; w += kThreads) {
-      const GT* p;
-      if (a.src.table_mode) {
-        const void* q = a.src.table[(int64_t)w * a.src.n_params + tl.param];
-        p = q ? static_cast<const GT*>(q) + tl.in_param : nullptr;
-      } else {
-        p = static_cast<const GT*>(a.src.base[w]) + tl.flat;
-      }
-      s_ptr[w] = p;
-      if constexpr (STAGE1) s_out[w] = static_cast<CT*>(a.out.base[w]) + tl.flat;
-    }
-    __syncthreads();
-
     CT* out_shard = static_cast<CT*>(a.out.base[0]) + tl.shard;
     const int nvec = tl.len >> 3;
     for (int v0 = threadIdx.x; v0 < nvec; v0 += kThreads * U) {
       float s[U][8];
+      {
+        const GT* p0 = grad_ptr<GT>(a, tl, 0);
 #pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int v = v0 + u * kThreads;
-        if (v < nvec) {
-          const GT* p0 = s_ptr[0];
-          first8(p0 ? p0 + (int64_t)v * 8 : nullptr, s[u]);
+        for (int u = 0; u < U; ++u) {
+          const int v = v0 + u * kThreads;
+          if (v < nvec) first8(p0 ? p0 + (int64_t)v * 8 : nullptr, s[u]);
         }
       }
+#pragma unroll(WT ? WT : 1)
       for (int w = 1; w < W; ++w) {
-        const GT* pw = s_ptr[w];
+        const GT* pw = grad_ptr<GT>(a, tl, w);
 #pragma unroll
         for (int u = 0; u < U; ++u) {
           const int v = v0 + u * kThreads;
@@ -105,29 +121,21 @@ __global__ void __launch_bounds__(kThreads) k_reduce_norm(const __grid_constant_
         const int v = v0 + u * kThreads;
         if (v < nvec) {
           Pack8<CT> rc;
+          float rf[8];
           float ss = 0.0f;
           bool fin = true;
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
             rc.e[j] = DT<CT>::from_f32(s[u][j]);
-            const float rf = DT<CT>::to_f32(rc.e[j]);
+            rf[j] = DT<CT>::to_f32(rc.e[j]);
             fin = fin && DT<CT>::finite_bits(rc.e[j]);
-            ss = __fmaf_rn(rf, rf, ss);
+            ss = __fmaf_rn(rf[j], rf[j], ss);
           }
           if (!fin) bad = 1u;
-          if (isfinite(ss)) {
-            acc += (double)ss;
-          } else {  // finite values whose squares overflow fp32 (or a non-finite r)
-            double d = 0.0;
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              const double rf = (double)DT<CT>::to_f32(rc.e[j]);
-              d += rf * rf;
-            }
-            acc += d;
-          }
+          add_group(ss, hi, lo, big, rf);
           if constexpr (STAGE1) {
-            for (int w = 0; w < W; ++w) store8_raw(s_out[w] + (int64_t)v * 8, rc);
+            for (int w = 0; w < W; ++w)
+              store8_raw(static_cast<CT*>(a.out.base[w]) + tl.flat + (int64_t)v * 8, rc);
           } else {
             store8_raw(out_shard + (int64_t)v * 8, rc);
           }
@@ -138,21 +146,21 @@ __global__ void __launch_bounds__(kThreads) k_reduce_norm(const __grid_constant_
     const int rem = tl.len & 7;
     if (threadIdx.x < rem) {
       const int64_t i = (int64_t)nvec * 8 + threadIdx.x;
-      float sum = load1(s_ptr[0], i);
-      for (int w = 1; w < W; ++w) sum = __fadd_rn(sum, load1(s_ptr[w], i));
+      float sum = load1(grad_ptr<GT>(a, tl, 0), i);
+      for (int w = 1; w < W; ++w) sum = __fadd_rn(sum, load1(grad_ptr<GT>(a, tl, w), i));
       const CT rc = DT<CT>::from_f32(sum);
       const double rf = (double)DT<CT>::to_f32(rc);
       if (!DT<CT>::finite_bits(rc)) bad = 1u;
-      acc += rf * rf;
+      big += rf * rf;
       if constexpr (STAGE1) {
-        for (int w = 0; w < W; ++w) s_out[w][i] = rc;
+        for (int w = 0; w < W; ++w) static_cast<CT*>(a.out.base[w])[tl.flat + i] = rc;
       } else {
         out_shard[i] = rc;
       }
     }
   }
 
-  const double total = block_sum<kThreads>(acc, s_red);
+  const double total = block_sum<kThreads>((double)hi + (double)lo + big, s_red);
   const unsigned any_bad = block_or<kThreads>(bad, s_or);
   if (threadIdx.x == 0) {
     a.part_sumsq[blockIdx.x] = total;

@@ -19,3 +19,13 @@ def rel_err(got: np.ndarray, ref: np.ndarray, tiny: float = 1e-30) -> np.ndarray
     ref = ref.astype(np.float64)
     d = np.abs(got - ref)
     return np.where(np.abs(ref) < tiny, d, d / np.maximum(np.abs(ref), tiny))
+
+
+def scaled_err(got: np.ndarray, ref: np.ndarray, prev: np.ndarray, tiny: float = 1e-30) -> np.ndarray:
+    """|got - ref| / max(|ref|, |prev|): the error relative to the larger of the
+    result and the value it was computed from (the operands' scale)."""
+    got = got.astype(np.float64)
+    ref = ref.astype(np.float64)
+    scale = np.maximum(np.maximum(np.abs(ref), np.abs(prev.astype(np.float64))), tiny)
+    d = np.abs(got - ref)
+    return np.where(scale <= tiny, d, d / scale)

@@ -127,6 +127,11 @@ def workload(name: str, **over) -> Workload:
     elif name == "qwen3_0.6b_fp16_w8":
         w = Workload(name, qwen3_0_6b_shapes(), 8, 2, F16, F16, F16, 500 * MB, 1e-4,
                      init_scale=2.0 ** 16, dynamic=True, index=3)
+    elif name == "qwen3_layers8_bf16_w2":
+        # 8 Qwen3-0.6B decoder layers, no embedding: 125.8M elements, about
+        # 2.5 GB on the device; a profiling-sized case of the same kernels.
+        w = Workload(name, qwen3_0_6b_shapes(layers=8)[1:-1], 2, 2, BF16, BF16, BF16, 500 * MB,
+                     1e-4, index=6)
     elif name == "moe_3.9b_bf16_w4":
         w = Workload(name, moe_3_9b_shapes()[0], 4, 2, BF16, BF16, BF16, 500 * MB, 1e-4, index=4)
     elif name == "ragged_2000":
