@@ -7,6 +7,7 @@
 #include <algorithm>
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <new>
 #include <string>
@@ -92,6 +93,8 @@ struct zero_layout {
   size_t gather_cap = 0;
 
   int grid_reduce = 0, grid_update = 0, grid_copy = 0;
+  // 1: shared-memory pipelines fed by cp.async.bulk; 0: register-staged loads
+  int reduce_variant = 1, update_variant = 1;
   cudaEvent_t events[4] = {nullptr, nullptr, nullptr, nullptr};
   bool timing = false;
 
@@ -198,10 +201,12 @@ int launch_step(zero_layout* L, const GradSrc& src, void* const* allreduce_out,
   }
   ra.part_sumsq = L->d_part;
   ra.part_ovf = L->d_ovf;
+  ra.chunk = reduce_chunk(W, L->cfg.grad_dtype);
+  ra.error = &L->d_state->error;
   int n_part = 0;
   if (L->timing) ZERO_CUDA(cudaEventRecord(L->events[0], s));
   if (n_tiles > 0) {
-    cudaError_t e = launch_reduce(ra, L->grid_reduce, s);
+    cudaError_t e = launch_reduce(ra, L->grid_reduce, L->reduce_variant, s);
     if (e != cudaSuccess) return cuda_fail(e, "reduce kernel launch");
     n_part = L->grid_reduce;
   }
@@ -224,7 +229,8 @@ int launch_step(zero_layout* L, const GradSrc& src, void* const* allreduce_out,
     ua.v = L->v;
     ua.params_flat = L->params;
     ua.state = L->d_state;
-    e = launch_update(ua, L->grid_update, s);
+    ua.error = &L->d_state->error;
+    e = launch_update(ua, L->grid_update, L->update_variant, s);
     if (e != cudaSuccess) return cuda_fail(e, "update kernel launch");
   }
   if (L->timing) ZERO_CUDA(cudaEventRecord(L->events[3], s));
@@ -440,8 +446,11 @@ int zero_state_bind(zero_layout_t* L, void* master, void* m, void* v, void* para
     ZERO_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
     L->device = dev;
     const int n_tiles = (int)L->tiles.size();
-    const int bps_r = reduce_blocks_per_sm(L->cfg.grad_dtype, L->comm_dtype, L->world(), L->cfg.stage);
-    const int bps_u = update_blocks_per_sm(L->comm_dtype, L->cfg.param_dtype);
+    if (const char* v = std::getenv("ZERO_REDUCE_VARIANT")) L->reduce_variant = std::atoi(v) == 0 ? 0 : 1;
+    if (const char* v = std::getenv("ZERO_UPDATE_VARIANT")) L->update_variant = std::atoi(v) == 0 ? 0 : 1;
+    const int bps_r = reduce_blocks_per_sm(L->cfg.grad_dtype, L->comm_dtype, L->world(), L->cfg.stage,
+                                           L->reduce_variant);
+    const int bps_u = update_blocks_per_sm(L->comm_dtype, L->cfg.param_dtype, L->update_variant);
     if (bps_r <= 0 || bps_u <= 0)
       return fail(ZERO_ERR_CUDA, "kernel occupancy query failed (no sm_103a image for this GPU?)");
     L->grid_reduce = std::max(1, std::min({n_tiles, sms * bps_r, kMaxPartials}));
@@ -556,6 +565,8 @@ int zero_loss_scale_state(zero_layout_t* L, void* stream, zero_scaler_state* out
   out->clip_coef = h.clip_coef;
   out->norm_sq_raw = h.norm_sq_raw;
   out->steps = h.steps;
+  if (h.error != 0)
+    return fail(ZERO_ERR_TIMEOUT, "a kernel's bounded wait gave up (device error word %u)", h.error);
   return ZERO_OK;
 }
 

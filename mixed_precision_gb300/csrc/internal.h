@@ -52,7 +52,7 @@ struct DevState {
   float step_size;     // lr / (1 - beta1^t)
   float inv_sqrt_bc2;  // 1 / sqrt(1 - beta2^t)
   float beta1, one_minus_beta1, beta2, one_minus_beta2, eps;
-  float reserved_;
+  unsigned error;  // bit 0: a kernel's bounded wait gave up (reported as ZERO_ERR_TIMEOUT)
 };
 
 struct Hparams {  // mirror of zero_hparams
@@ -90,6 +90,8 @@ struct ReduceArgs {
   RedBufs out;
   double* part_sumsq;   // [grid]
   unsigned* part_ovf;   // [grid]
+  int chunk;            // shared-memory pipeline: elements per stage
+  unsigned* error;      // DevState::error
 };
 
 struct UpdateArgs {
@@ -103,15 +105,21 @@ struct UpdateArgs {
   float* v;
   void* params_flat;
   const DevState* state;
+  unsigned* error;  // &state->error
 };
 
 // Kernel launchers. Each returns the launch's cudaError_t.
-cudaError_t launch_reduce(const ReduceArgs& a, int grid, cudaStream_t s);
-int reduce_blocks_per_sm(int grad_dtype, int comm_dtype, int world, int stage);
+// Kernel variants: 0 = register-staged loads; 1 = shared-memory stages filled
+// by cp.async.bulk.
+constexpr int kRedStages = 3;
+constexpr int kRedStageBytes = 32768;
+int reduce_chunk(int world, int grad_dtype);  // elements per stage of the pipelined variant
+cudaError_t launch_reduce(const ReduceArgs& a, int grid, int variant, cudaStream_t s);
+int reduce_blocks_per_sm(int grad_dtype, int comm_dtype, int world, int stage, int variant);
 cudaError_t launch_finalize(const double* part_sumsq, const unsigned* part_ovf, int n_part,
                             int world, const Hparams& hp, DevState* st, cudaStream_t s);
-cudaError_t launch_update(const UpdateArgs& a, int grid, cudaStream_t s);
-int update_blocks_per_sm(int comm_dtype, int param_dtype);
+cudaError_t launch_update(const UpdateArgs& a, int grid, int variant, cudaStream_t s);
+int update_blocks_per_sm(int comm_dtype, int param_dtype, int variant);
 cudaError_t launch_state_init(const ScalerCfg& cfg, DevState* st, cudaStream_t s);
 cudaError_t launch_init_from_flat(const Tile* tiles, int n_tiles, const float* master_flat,
                                   float* master, void* params_flat, int param_dtype, int grid,

@@ -18,6 +18,7 @@
 // tile list with a fixed stride, so the partials are deterministic.
 #pragma once
 
+#include "bulk.cuh"
 #include "vec.cuh"
 
 namespace zg {
@@ -168,29 +169,190 @@ __global__ void __launch_bounds__(kThreads, 4) k_reduce_norm(const __grid_consta
   }
 }
 
+// ---------------------------------------------------------------------------
+// K1, shared-memory pipeline. Same arithmetic and outputs as k_reduce_norm.
+// Each stage holds one chunk (a.chunk elements) of all W ranks' gradients,
+// copied in by cp.async.bulk (one request per rank, issued by one thread,
+// completed on the stage's mbarrier); kRedStages stages in flight. A NULL
+// per-tensor gradient is not copied and reads as zeros. The chunk's last
+// (len mod 8) elements come from global memory directly. Bounded waits; on
+// timeout the block records kErrWaitTimeout, waits for its copies in flight
+// and returns without a partial (the host reports ZERO_ERR_TIMEOUT).
+// ---------------------------------------------------------------------------
+template <typename GT, typename CT, int WT, bool STAGE1>
+__global__ void __launch_bounds__(kThreads) k_reduce_norm_bulk(const __grid_constant__ ReduceArgs a) {
+  constexpr int S = kRedStages;
+  extern __shared__ __align__(128) unsigned char smem[];
+  __shared__ __align__(8) uint64_t full[S];
+  __shared__ double s_red[kThreads / 32];
+  __shared__ unsigned s_or[kThreads / 32];
+  const int W = WT ? WT : a.world;
+  const int C = a.chunk;
+  const int kStage = W * C * (int)sizeof(GT);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) mbar_init(&full[s], 1);
+    mbar_init_fence();
+  }
+  __syncthreads();
+
+  int pt = blockIdx.x, pc = 0;
+  unsigned issued = 0;
+  auto issue = [&](int s) {
+    if (pt >= a.n_tiles) return;
+    const Tile tl = a.tiles[pt];
+    const int clen = min(C, tl.len - pc);
+    const int nb = clen & ~7;
+    GT* base = reinterpret_cast<GT*>(smem + s * kStage);
+    uint32_t bytes = 0;
+    for (int w = 0; w < W; ++w)
+      if (nb > 0 && grad_ptr<GT>(a, tl, w) != nullptr) bytes += nb * (uint32_t)sizeof(GT);
+    if (bytes > 0) {
+      mbar_arrive_expect_tx(&full[s], bytes);
+      for (int w = 0; w < W; ++w) {
+        const GT* g = grad_ptr<GT>(a, tl, w);
+        if (g != nullptr) bulk_g2s(base + w * C, g + pc, nb * (int)sizeof(GT), &full[s]);
+      }
+    } else {
+      mbar_arrive(&full[s]);
+    }
+    ++issued;
+    pc += C;
+    if (pc >= tl.len) {
+      pc = 0;
+      pt += gridDim.x;
+    }
+  };
+  if (threadIdx.x == 0)
+    for (int s = 0; s < S; ++s) issue(s);
+
+  float hi = 0.0f, lo = 0.0f;
+  double big = 0.0;
+  unsigned bad = 0u;
+  int ct = blockIdx.x, cc = 0;
+  unsigned k = 0;
+  bool ok = true;
+  while (ct < a.n_tiles) {
+    const int s = (int)(k % S);
+    const uint32_t parity = (k / S) & 1u;
+    const Tile tl = a.tiles[ct];
+    const int clen = min(C, tl.len - cc);
+    const int nb = clen & ~7;
+    const bool mine = mbar_wait(&full[s], parity);
+    if (!__syncthreads_and(mine)) {
+      ok = false;
+      break;
+    }
+    const GT* base = reinterpret_cast<const GT*>(smem + s * kStage);
+    for (int e = 8 * threadIdx.x; e < nb; e += 8 * kThreads) {
+      float acc[8];
+      if (grad_ptr<GT>(a, tl, 0) != nullptr) {
+        load8_smem(base + e, acc);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
+      }
+#pragma unroll(WT ? WT : 1)
+      for (int w = 1; w < W; ++w) {
+        float x[8];
+        if (grad_ptr<GT>(a, tl, w) != nullptr) {
+          load8_smem(base + w * C + e, x);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) x[j] = 0.0f;
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[j] = __fadd_rn(acc[j], x[j]);
+      }
+      Pack8<CT> rc;
+      float rf[8];
+      float ss = 0.0f;
+      bool fin = true;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        rc.e[j] = DT<CT>::from_f32(acc[j]);
+        rf[j] = DT<CT>::to_f32(rc.e[j]);
+        fin = fin && DT<CT>::finite_bits(rc.e[j]);
+        ss = __fmaf_rn(rf[j], rf[j], ss);
+      }
+      if (!fin) bad = 1u;
+      add_group(ss, hi, lo, big, rf);
+      if constexpr (STAGE1) {
+        for (int w = 0; w < W; ++w)
+          store8_raw(static_cast<CT*>(a.out.base[w]) + tl.flat + cc + e, rc);
+      } else {
+        store8_raw(static_cast<CT*>(a.out.base[0]) + tl.shard + cc + e, rc);
+      }
+    }
+    const int tail = clen - nb;
+    if (threadIdx.x < tail) {
+      const int64_t i = (int64_t)cc + nb + threadIdx.x;
+      float sum = load1(grad_ptr<GT>(a, tl, 0), i);
+      for (int w = 1; w < W; ++w) sum = __fadd_rn(sum, load1(grad_ptr<GT>(a, tl, w), i));
+      const CT rc = DT<CT>::from_f32(sum);
+      const double rf = (double)DT<CT>::to_f32(rc);
+      if (!DT<CT>::finite_bits(rc)) bad = 1u;
+      big += rf * rf;
+      if constexpr (STAGE1) {
+        for (int w = 0; w < W; ++w) static_cast<CT*>(a.out.base[w])[tl.flat + i] = rc;
+      } else {
+        static_cast<CT*>(a.out.base[0])[tl.shard + i] = rc;
+      }
+    }
+    __syncthreads();  // stage s is free again
+    if (threadIdx.x == 0) issue(s);
+    ++k;
+    cc += C;
+    if (cc >= tl.len) {
+      cc = 0;
+      ct += gridDim.x;
+    }
+  }
+  if (!ok) {
+    if (threadIdx.x == 0) {
+      atomicOr(a.error, kErrWaitTimeout);
+      for (unsigned j = k; j < issued; ++j) mbar_wait(&full[j % S], (j / S) & 1u);
+    }
+    return;
+  }
+  const double total = block_sum<kThreads>((double)hi + (double)lo + big, s_red);
+  const unsigned any_bad = block_or<kThreads>(bad, s_or);
+  if (threadIdx.x == 0) {
+    a.part_sumsq[blockIdx.x] = total;
+    a.part_ovf[blockIdx.x] = any_bad;
+  }
+}
+
+template <typename GT, typename CT, int WT, bool S1>
+const void* reduce_kernel_v(int variant) {
+  if (variant == 1) return reinterpret_cast<const void*>(&k_reduce_norm_bulk<GT, CT, WT, S1>);
+  return reinterpret_cast<const void*>(&k_reduce_norm<GT, CT, WT, S1>);
+}
+
 template <typename GT, typename CT, bool S1>
-const void* reduce_kernel_w(int world) {
+const void* reduce_kernel_w(int world, int variant) {
   switch (world) {
-    case 1: return reinterpret_cast<const void*>(&k_reduce_norm<GT, CT, 1, S1>);
-    case 2: return reinterpret_cast<const void*>(&k_reduce_norm<GT, CT, 2, S1>);
-    case 4: return reinterpret_cast<const void*>(&k_reduce_norm<GT, CT, 4, S1>);
-    case 8: return reinterpret_cast<const void*>(&k_reduce_norm<GT, CT, 8, S1>);
-    default: return reinterpret_cast<const void*>(&k_reduce_norm<GT, CT, 0, S1>);
+    case 1: return reduce_kernel_v<GT, CT, 1, S1>(variant);
+    case 2: return reduce_kernel_v<GT, CT, 2, S1>(variant);
+    case 4: return reduce_kernel_v<GT, CT, 4, S1>(variant);
+    case 8: return reduce_kernel_v<GT, CT, 8, S1>(variant);
+    default: return reduce_kernel_v<GT, CT, 0, S1>(variant);
   }
 }
 
 template <typename GT, typename CT>
-const void* reduce_kernel_s(int world, int stage) {
-  return stage == 1 ? reduce_kernel_w<GT, CT, true>(world) : reduce_kernel_w<GT, CT, false>(world);
+const void* reduce_kernel_s(int world, int stage, int variant) {
+  return stage == 1 ? reduce_kernel_w<GT, CT, true>(world, variant)
+                    : reduce_kernel_w<GT, CT, false>(world, variant);
 }
 
-// The kernel instance for (grad dtype GT, comm dtype, world, stage).
+// The kernel instance for (grad dtype GT, comm dtype, world, stage, variant).
 template <typename GT>
-const void* reduce_kernel_for(int comm_dtype, int world, int stage) {
+const void* reduce_kernel_for(int comm_dtype, int world, int stage, int variant) {
   switch (comm_dtype) {
-    case kF32: return reduce_kernel_s<GT, float>(world, stage);
-    case kF16: return reduce_kernel_s<GT, __half>(world, stage);
-    case kBF16: return reduce_kernel_s<GT, __nv_bfloat16>(world, stage);
+    case kF32: return reduce_kernel_s<GT, float>(world, stage, variant);
+    case kF16: return reduce_kernel_s<GT, __half>(world, stage, variant);
+    case kBF16: return reduce_kernel_s<GT, __nv_bfloat16>(world, stage, variant);
     default: return nullptr;
   }
 }

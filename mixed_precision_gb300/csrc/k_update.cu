@@ -1,34 +1,55 @@
 // K2 (finalize) and K3 (fused unscale / clip / AdamW / cast-out), plus the
 // launch dispatch of K1.
+#include "bulk.cuh"
 #include "vec.cuh"
 
 namespace zg {
 
-const void* reduce_kernel_f32(int comm_dtype, int world, int stage);
-const void* reduce_kernel_f16(int comm_dtype, int world, int stage);
-const void* reduce_kernel_bf16(int comm_dtype, int world, int stage);
+const void* reduce_kernel_f32(int comm_dtype, int world, int stage, int variant);
+const void* reduce_kernel_f16(int comm_dtype, int world, int stage, int variant);
+const void* reduce_kernel_bf16(int comm_dtype, int world, int stage, int variant);
 
-static const void* reduce_kernel(int grad_dtype, int comm_dtype, int world, int stage) {
+static const void* reduce_kernel(int grad_dtype, int comm_dtype, int world, int stage, int variant) {
   switch (grad_dtype) {
-    case kF32: return reduce_kernel_f32(comm_dtype, world, stage);
-    case kF16: return reduce_kernel_f16(comm_dtype, world, stage);
-    case kBF16: return reduce_kernel_bf16(comm_dtype, world, stage);
+    case kF32: return reduce_kernel_f32(comm_dtype, world, stage, variant);
+    case kF16: return reduce_kernel_f16(comm_dtype, world, stage, variant);
+    case kBF16: return reduce_kernel_bf16(comm_dtype, world, stage, variant);
     default: return nullptr;
   }
 }
 
-cudaError_t launch_reduce(const ReduceArgs& a, int grid, cudaStream_t s) {
-  const void* f = reduce_kernel(a.grad_dtype, a.comm_dtype, a.world, a.stage);
-  if (f == nullptr) return cudaErrorInvalidValue;
-  void* args[] = {const_cast<ReduceArgs*>(&a)};
-  return cudaLaunchKernel(f, dim3(grid), dim3(kThreads), args, 0, s);
+// Elements per stage of the pipelined reduce: the W ranks' slices of one chunk
+// fill about kRedStageBytes; a multiple of 128 elements, at least 128.
+int reduce_chunk(int world, int grad_dtype) {
+  const int g = grad_dtype == kF32 ? 4 : 2;
+  int c = kRedStageBytes / (world * g);
+  c &= ~127;
+  return c < 128 ? 128 : c;
 }
 
-int reduce_blocks_per_sm(int grad_dtype, int comm_dtype, int world, int stage) {
-  const void* f = reduce_kernel(grad_dtype, comm_dtype, world, stage);
-  int n = 0;
-  if (f == nullptr || cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, f, kThreads, 0) != cudaSuccess)
+static int reduce_smem(int world, int grad_dtype, int variant) {
+  if (variant != 1) return 0;
+  const int g = grad_dtype == kF32 ? 4 : 2;
+  return kRedStages * world * reduce_chunk(world, grad_dtype) * g;
+}
+
+cudaError_t launch_reduce(const ReduceArgs& a, int grid, int variant, cudaStream_t s) {
+  const void* f = reduce_kernel(a.grad_dtype, a.comm_dtype, a.world, a.stage, variant);
+  if (f == nullptr) return cudaErrorInvalidValue;
+  void* args[] = {const_cast<ReduceArgs*>(&a)};
+  return cudaLaunchKernel(f, dim3(grid), dim3(kThreads), args,
+                          reduce_smem(a.world, a.grad_dtype, variant), s);
+}
+
+int reduce_blocks_per_sm(int grad_dtype, int comm_dtype, int world, int stage, int variant) {
+  const void* f = reduce_kernel(grad_dtype, comm_dtype, world, stage, variant);
+  if (f == nullptr) return 0;
+  const int smem = reduce_smem(world, grad_dtype, variant);
+  if (smem > 0 && cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+                      cudaSuccess)
     return 0;
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, f, kThreads, smem) != cudaSuccess) return 0;
   return n;
 }
 
@@ -198,36 +219,200 @@ __global__ void __launch_bounds__(kThreads) k_adamw_cast(const __grid_constant__
   }
 }
 
+// ---------------------------------------------------------------------------
+// K3, shared-memory pipeline. The same arithmetic as k_adamw_cast; the four
+// input streams (master, m, v, reduced gradient) of each chunk of C elements
+// arrive in a shared-memory stage by cp.async.bulk, issued by one thread and
+// completed on the stage's mbarrier, S stages deep. The threads read the
+// stage, update, and write master/m/v/params straight to global memory. One
+// thread moving 14 bytes per element in four bulk requests replaces seven
+// 16-byte loads per thread, which kept the load/store queues full.
+// A chunk's last (len mod 8) elements are not bulk-copied (16-byte rule) and
+// are handled from global memory directly. Every wait is bounded; on timeout
+// the block records kErrWaitTimeout, waits (bounded) for its copies in flight
+// and returns.
+// ---------------------------------------------------------------------------
 template <typename CT>
-static const void* update_kernel_c(int param_dtype) {
+struct UpdStage {
+  __host__ __device__ static constexpr int bytes(int C) { return C * (12 + (int)sizeof(CT)); }
+};
+
+template <typename CT, typename PT, int C, int S>
+__global__ void __launch_bounds__(kThreads) k_adamw_cast_bulk(const __grid_constant__ UpdateArgs a) {
+  static_assert(C % (4 * kThreads) == 0, "chunk must be whole 4-element groups per thread");
+  extern __shared__ __align__(128) unsigned char smem[];
+  __shared__ __align__(8) uint64_t full[S];
+  constexpr int kStage = UpdStage<CT>::bytes(C);
+
+  const DevState* st = a.state;
+  if (st->skip) return;
+  const float gs = st->gscale, decay = st->decay, step = st->step_size;
+  const float isb2 = st->inv_sqrt_bc2, eps = st->eps;
+  const float b1 = st->beta1, omb1 = st->one_minus_beta1;
+  const float b2 = st->beta2, omb2 = st->one_minus_beta2;
+  auto adam = [&](float r, float& p, float& m, float& v) {
+    const float g = r * gs;
+    p = p * decay;
+    m = b1 * m + omb1 * g;
+    v = b2 * v + omb2 * (g * g);
+    const float denom = sqrtf(v) * isb2 + eps;
+    p = p - step * (m / denom);
+  };
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) mbar_init(&full[s], 1);
+    mbar_init_fence();
+  }
+  __syncthreads();
+
+  auto red_ptr = [&](const Tile& tl) -> const CT* {
+    return a.stage == 1 ? static_cast<const CT*>(a.red.base[tl.rank]) + tl.flat
+                        : static_cast<const CT*>(a.red.base[0]) + tl.shard;
+  };
+
+  // Producer (thread 0): walks this block's chunk sequence S items ahead.
+  int pt = blockIdx.x, pc = 0;
+  unsigned issued = 0;
+  auto issue = [&](int s) {
+    if (pt >= a.n_tiles) return;
+    const Tile tl = a.tiles[pt];
+    const int clen = min(C, tl.len - pc);
+    const int nb = clen & ~7;
+    unsigned char* base = smem + s * kStage;
+    if (nb > 0) {
+      mbar_arrive_expect_tx(&full[s], (uint32_t)nb * (12u + (uint32_t)sizeof(CT)));
+      const int64_t so = tl.shard + pc;
+      bulk_g2s(base, a.master + so, nb * 4, &full[s]);
+      bulk_g2s(base + C * 4, a.m + so, nb * 4, &full[s]);
+      bulk_g2s(base + C * 8, a.v + so, nb * 4, &full[s]);
+      bulk_g2s(base + C * 12, red_ptr(tl) + pc, nb * (int)sizeof(CT), &full[s]);
+    } else {
+      mbar_arrive(&full[s]);
+    }
+    ++issued;
+    pc += C;
+    if (pc >= tl.len) {
+      pc = 0;
+      pt += gridDim.x;
+    }
+  };
+  if (threadIdx.x == 0)
+    for (int s = 0; s < S; ++s) issue(s);
+
+  // Consumers: every thread walks the same sequence.
+  int ct = blockIdx.x, cc = 0;
+  unsigned k = 0;
+  bool ok = true;
+  while (ct < a.n_tiles) {
+    const int s = (int)(k % S);
+    const uint32_t parity = (k / S) & 1u;
+    const Tile tl = a.tiles[ct];
+    const int clen = min(C, tl.len - cc);
+    const int nb = clen & ~7;
+    const bool mine = mbar_wait(&full[s], parity);
+    if (!__syncthreads_and(mine)) {
+      ok = false;
+      break;
+    }
+    const unsigned char* base = smem + s * kStage;
+    const float* sp = reinterpret_cast<const float*>(base);
+    const float* sm = reinterpret_cast<const float*>(base + C * 4);
+    const float* sv = reinterpret_cast<const float*>(base + C * 8);
+    const CT* sr = reinterpret_cast<const CT*>(base + C * 12);
+    const int64_t so = tl.shard + cc, fo = tl.flat + cc;
+    PT* pp = static_cast<PT*>(a.params_flat) + fo;
+    for (int e = 4 * threadIdx.x; e < nb; e += 4 * kThreads) {
+      float4 p = *reinterpret_cast<const float4*>(sp + e);
+      float4 m = *reinterpret_cast<const float4*>(sm + e);
+      float4 v = *reinterpret_cast<const float4*>(sv + e);
+      float r[4];
+      load4_smem(sr + e, r);
+      adam(r[0], p.x, m.x, v.x);
+      adam(r[1], p.y, m.y, v.y);
+      adam(r[2], p.z, m.z, v.z);
+      adam(r[3], p.w, m.w, v.w);
+      __stcs(reinterpret_cast<float4*>(a.master + so + e), p);
+      __stcs(reinterpret_cast<float4*>(a.m + so + e), m);
+      __stcs(reinterpret_cast<float4*>(a.v + so + e), v);
+      PT q[4] = {DT<PT>::from_f32(p.x), DT<PT>::from_f32(p.y), DT<PT>::from_f32(p.z),
+                 DT<PT>::from_f32(p.w)};
+      __stcs(reinterpret_cast<uint2*>(pp + e), *reinterpret_cast<const uint2*>(q));
+    }
+    const int tail = clen - nb;
+    if (threadIdx.x < tail) {
+      const int e = nb + threadIdx.x;
+      float p = a.master[so + e], m = a.m[so + e], v = a.v[so + e];
+      adam(DT<CT>::to_f32(red_ptr(tl)[cc + e]), p, m, v);
+      a.master[so + e] = p;
+      a.m[so + e] = m;
+      a.v[so + e] = v;
+      pp[e] = DT<PT>::from_f32(p);
+    }
+    __syncthreads();  // stage s is free again
+    if (threadIdx.x == 0) issue(s);
+    ++k;
+    cc += C;
+    if (cc >= tl.len) {
+      cc = 0;
+      ct += gridDim.x;
+    }
+  }
+  if (!ok && threadIdx.x == 0) {
+    atomicOr(a.error, kErrWaitTimeout);
+    for (unsigned j = k; j < issued; ++j) mbar_wait(&full[j % S], (j / S) & 1u);
+  }
+}
+
+constexpr int kUpdChunk = 2048;
+constexpr int kUpdStages = 3;
+
+template <typename CT, typename PT>
+static const void* update_kernel_cp(int variant) {
+  if (variant == 1)
+    return reinterpret_cast<const void*>(&k_adamw_cast_bulk<CT, PT, kUpdChunk, kUpdStages>);
+  return reinterpret_cast<const void*>(&k_adamw_cast<CT, PT>);
+}
+
+template <typename CT>
+static const void* update_kernel_c(int param_dtype, int variant) {
   switch (param_dtype) {
-    case kF16: return reinterpret_cast<const void*>(&k_adamw_cast<CT, __half>);
-    case kBF16: return reinterpret_cast<const void*>(&k_adamw_cast<CT, __nv_bfloat16>);
+    case kF16: return update_kernel_cp<CT, __half>(variant);
+    case kBF16: return update_kernel_cp<CT, __nv_bfloat16>(variant);
     default: return nullptr;
   }
 }
 
-static const void* update_kernel(int comm_dtype, int param_dtype) {
+static const void* update_kernel(int comm_dtype, int param_dtype, int variant) {
   switch (comm_dtype) {
-    case kF32: return update_kernel_c<float>(param_dtype);
-    case kF16: return update_kernel_c<__half>(param_dtype);
-    case kBF16: return update_kernel_c<__nv_bfloat16>(param_dtype);
+    case kF32: return update_kernel_c<float>(param_dtype, variant);
+    case kF16: return update_kernel_c<__half>(param_dtype, variant);
+    case kBF16: return update_kernel_c<__nv_bfloat16>(param_dtype, variant);
     default: return nullptr;
   }
 }
 
-cudaError_t launch_update(const UpdateArgs& a, int grid, cudaStream_t s) {
-  const void* f = update_kernel(a.comm_dtype, a.param_dtype);
+static int update_smem(int comm_dtype, int variant) {
+  if (variant != 1) return 0;
+  const int cb = comm_dtype == kF32 ? 4 : 2;
+  return kUpdStages * kUpdChunk * (12 + cb);
+}
+
+cudaError_t launch_update(const UpdateArgs& a, int grid, int variant, cudaStream_t s) {
+  const void* f = update_kernel(a.comm_dtype, a.param_dtype, variant);
   if (f == nullptr) return cudaErrorInvalidValue;
   void* args[] = {const_cast<UpdateArgs*>(&a)};
-  return cudaLaunchKernel(f, dim3(grid), dim3(kThreads), args, 0, s);
+  return cudaLaunchKernel(f, dim3(grid), dim3(kThreads), args, update_smem(a.comm_dtype, variant), s);
 }
 
-int update_blocks_per_sm(int comm_dtype, int param_dtype) {
-  const void* f = update_kernel(comm_dtype, param_dtype);
-  int n = 0;
-  if (f == nullptr || cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, f, kThreads, 0) != cudaSuccess)
+int update_blocks_per_sm(int comm_dtype, int param_dtype, int variant) {
+  const void* f = update_kernel(comm_dtype, param_dtype, variant);
+  if (f == nullptr) return 0;
+  const int smem = update_smem(comm_dtype, variant);
+  if (smem > 0 && cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+                      cudaSuccess)
     return 0;
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, f, kThreads, smem) != cudaSuccess) return 0;
   return n;
 }
 

@@ -67,6 +67,35 @@ __device__ __forceinline__ void load8(const T* p, float (&x)[8]) {
   }
 }
 
+// 8 consecutive elements of T from shared memory as fp32 (16-byte aligned).
+template <typename T>
+__device__ __forceinline__ void load8_smem(const T* p, float (&x)[8]) {
+  if constexpr (sizeof(T) == 4) {
+    const float4 a = reinterpret_cast<const float4*>(p)[0], b = reinterpret_cast<const float4*>(p)[1];
+    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+    x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+  } else {
+    const uint4 a = *reinterpret_cast<const uint4*>(p);
+    const T* h = reinterpret_cast<const T*>(&a);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) x[j] = DT<T>::to_f32(h[j]);
+  }
+}
+
+// 4 consecutive elements of T from shared memory as fp32 (8 or 16 bytes, aligned).
+template <typename T>
+__device__ __forceinline__ void load4_smem(const T* p, float (&r)[4]) {
+  if constexpr (sizeof(T) == 4) {
+    const float4 x = *reinterpret_cast<const float4*>(p);
+    r[0] = x.x; r[1] = x.y; r[2] = x.z; r[3] = x.w;
+  } else {
+    const uint2 x = *reinterpret_cast<const uint2*>(p);
+    const T* h = reinterpret_cast<const T*>(&x);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) r[j] = DT<T>::to_f32(h[j]);
+  }
+}
+
 // 8 raw elements of T (no conversion).
 template <typename T>
 struct Pack8 {
