@@ -283,6 +283,34 @@ int zero_state_import(zero_layout_t* layout, const float* master_flat, const flo
  * it exists so a benchmark can time each kernel with CUDA events. */
 int zero_set_step_events(zero_layout_t* layout, void* const* events);
 
+/* Reduce + overflow check + squared norm of W flat gradient buffers, using no
+ * device memory of its own. The pages have no counterpart: this exists for
+ * callers that cannot allocate -- code that must not call cudaMalloc while a
+ * graph is being captured elsewhere in the process, embeddings whose device
+ * memory is all handed out at start-up, hosts that forbid a library from
+ * growing its footprint later. It computes what the step's first kernel
+ * computes over the plain range [0, n) (no layout, no padding mask):
+ *   r[i] = RNE_comm(g_0[i] + ... + g_{W-1}[i])  (fp32 adds in rank order),
+ *   *norm_sq_out = sum of r[i]^2 (fp64 result), *overflow_out = any r non-finite.
+ *   grads         host array of `world` device pointers (1..64), n elements of
+ *                 grad_dtype each, 16-byte aligned. Read only.
+ *   comm_dtype    dtype of r; -1 = grad_dtype.
+ *   reduced_out   device, n elements of comm_dtype (16-byte aligned), or NULL
+ *                 to skip writing r.
+ *   norm_sq_out   device double; overflow_out: device int32.
+ * Scratch: a fixed array inside the library (about 768 KB on every GPU that
+ * loads it, held until the process exits) for one partial per 65,536
+ * elements; n above 2^32 is rejected with ZERO_ERR_INVALID. The first call
+ * made with a device current looks up that array's device address for the
+ * device (cudaGetSymbolAddress); make that first call before any stream
+ * capture. Every call shares the one array: calls whose work overlaps on the
+ * GPU (different streams, no ordering between them) race and give wrong
+ * results. Allocates nothing: no cudaMalloc, cudaFree or allocating library
+ * call. Enqueued on `stream`. */
+int zero_reduce_norm_noalloc(const void* const* grads, int world, int64_t n, int grad_dtype,
+                             int comm_dtype, void* reduced_out, double* norm_sq_out,
+                             int32_t* overflow_out, void* stream);
+
 /* Message for the last failing call on this thread ("" if none). The pointer
  * stays valid until the next failing call on this thread. */
 const char* zero_last_error(void);

@@ -98,6 +98,7 @@ def lib() -> ctypes.CDLL:
             "zero_state_import": [P, P, P, P, P],
             "zero_layout_set_allocator": [P, ALLOC_FN, FREE_FN, P],
             "zero_set_step_events": [P, PP],
+            "zero_reduce_norm_noalloc": [PP, I, I64, I, I, P, P, P, P],
         }
         for name, args in sig.items():
             fn = getattr(L, name)
@@ -216,3 +217,11 @@ def zero_layout_set_allocator(layout: int, alloc, free_fn, ctx: int = 0) -> None
     """alloc/free_fn: ALLOC_FN / FREE_FN instances (keep them alive), or None for the default."""
     _check(lib().zero_layout_set_allocator(layout, alloc or ALLOC_FN(), free_fn or FREE_FN(),
                                            ctx or None))
+
+
+def zero_reduce_norm_noalloc(grads, n: int, grad_dtype: int, comm_dtype: int, reduced_out: int,
+                             norm_sq_out: int, overflow_out: int, stream: int) -> None:
+    """grads: W device pointers; outputs are device pointers (reduced_out may be 0)."""
+    _check(lib().zero_reduce_norm_noalloc(_ptrs(grads), len(grads), n, grad_dtype, comm_dtype,
+                                          reduced_out or None, norm_sq_out, overflow_out,
+                                          stream or None))

@@ -58,6 +58,8 @@ void default_free(void* p, void*) { cudaFree(p); }
 
 }  // namespace
 
+int zg::zero_internal_fail(int code, const char* msg) { return fail(code, "%s", msg); }
+
 struct zero_layout {
   zero_config cfg{};
   int comm_dtype = 0;

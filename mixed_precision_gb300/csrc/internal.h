@@ -127,6 +127,10 @@ cudaError_t launch_init_from_flat(const Tile* tiles, int n_tiles, const float* m
 // dir 0: rank-major -> flat (export); 1: flat -> rank-major (import)
 cudaError_t launch_state_copy(const Tile* tiles, int n_tiles, float* shard_buf, float* flat_buf,
                               int dir, int grid, cudaStream_t s);
+// Record a failure message for zero_last_error() and return `code` (for entry
+// points defined outside api.cpp).
+int zero_internal_fail(int code, const char* msg);
+
 cudaError_t launch_gather(const Tile* tiles, int n_tiles, const void* params_flat,
                           void* const* dst_table, int n_params, int n_replicas, int elem_bytes,
                           int grid, cudaStream_t s);
