@@ -40,10 +40,10 @@ STATE_READ_BYTES = 144
 # (dram__bytes_read.sum + dram__bytes_write.sum / elements), with the capture
 # it comes from; None until a capture of the current kernel exists.
 NCU_TRAFFIC_PER_ELEM = {
-    # profiles/k_adamw_cast_qwen3_layers8.md: (1.763 + 1.703) GB / 125,847,552 elements
-    "k_adamw_cast": 27.54,
-    # profiles/k_reduce_norm_qwen3_layers8.md: (504.1 + 211.7) MB / 125,847,552 elements
-    "k_reduce_norm": 5.69,
+    # profiles/k_adamw_cast_bulk_qwen3_layers8.md: (1.7627 + 1.7008) GB / 125,847,552 elements
+    "k_adamw_cast": 27.52,
+    # profiles/k_reduce_norm_bulk_qwen3_layers8.md: (504.0 + 212.6) MB / 125,847,552 elements
+    "k_reduce_norm": 5.694,
 }
 
 
@@ -58,6 +58,8 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="target CPU time of the oracle sample")
+    ap.add_argument("--tensors", action="store_true",
+                    help="step from per-tensor gradient pointers (NULL for all-zero gradients)")
     return ap.parse_args(argv)
 
 
@@ -298,8 +300,22 @@ def run_ours(args) -> dict | None:
     torch.cuda.synchronize()
     del master0
     grads = [wl.flat_grads(z.offsets, numel, z.np, w.grad_sigma,
-                           wl.grad_seed(w.index, r + 1000 * rank), w.grad_dtype, device=device)
+                           wl.grad_seed(w.index, r + 1000 * rank), w.grad_dtype, device=device,
+                           zero_params=wl.zero_params(w, r))
              for r in range(w.world)]
+    per_tensor = None
+    if args.tensors:
+        per_tensor = []
+        for r in range(w.world):
+            zero = set(wl.zero_params(w, r))
+            per_tensor.append([None if p in zero else grads[r][off:off + n]
+                               for p, (off, n) in enumerate(zip(z.offsets, numel))])
+
+    def do_step():
+        if per_tensor is not None:
+            z.step_tensors(per_tensor, hp)
+        else:
+            z.step(grads, hp)
     hp = Hparams(lr=w.lr, beta1=w.beta1, beta2=w.beta2, eps=w.eps, weight_decay=w.weight_decay,
                  max_grad_norm=w.max_grad_norm)
 
@@ -308,7 +324,7 @@ def run_ours(args) -> dict | None:
         for e in row:
             e.record()
     for _ in range(W):
-        z.step(grads, hp)
+        do_step()
     torch.cuda.synchronize()
     barrier(dist, device)
 
@@ -320,7 +336,7 @@ def run_ours(args) -> dict | None:
     t_start.record()
     for k in range(K):
         abi.zero_set_step_events(z.handle, [e.cuda_event for e in ev[k]])
-        z.step(grads, hp)
+        do_step()
     t_end.record()
     torch.cuda.synchronize()
     abi.zero_set_step_events(z.handle, None)
@@ -342,7 +358,7 @@ def run_ours(args) -> dict | None:
     s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     s0.record()
     for _ in range(3):
-        z.step(grads, hp)
+        do_step()
     s1.record()
     torch.cuda.synchronize()
     skip_ms = s0.elapsed_time(s1) / 3
@@ -391,7 +407,8 @@ def run_ours(args) -> dict | None:
         "vs_baseline": None,
         "dtype": "f32",
         "data": "synthetic",
-        "config": config_of(w),
+        "config": config_of(w, "per-tensor gradient pointers, NULL for all-zero gradients"
+                            if args.tensors else None),
         "hbm_gbs_step": step_gbs,
         "step_roofline": {"bytes_per_param": info.step_bytes_per_elem, "peak_gbs": peak,
                           "frac": step_gbs / peak, "peak_source": peak_src},

@@ -1,0 +1,139 @@
+"""Full-size parity of the named workloads, in the launch configuration the
+benchmark times, on sampled outputs (see _fullsize.py).
+
+- Qwen3-0.6B-shaped, W=2, ZeRO-2, bf16 (the benchmark's workload): two steps.
+- Qwen3-0.6B-shaped, W=8, fp16 dynamic loss scaling, ZeRO-1 and ZeRO-2:
+  the two stages bit-identical; sampled parity; 200 steps with +inf at steps
+  50/100/150/200 and the scale/counter/t trajectory bit-exact.
+- MoE ~3.9B, W=4, bf16, 14 of 16 experts' gradients zero per rank and layer:
+  sampled parity, and the per-tensor entry point (NULL for the zero experts)
+  bit-identical to the flat one.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as wl
+from _fullsize import SampledOracle, sample_indices
+from _parity import INF_BITS, to_np
+from mixed_precision_gb300.engine import Hparams, ZeroStep
+
+pytestmark = pytest.mark.gpu
+
+
+def _setup(w, stage=None):
+    stage = w.stage if stage is None else stage
+    z = ZeroStep(w.shapes, w.world, stage, w.bucket_bytes, w.grad_dtype, w.param_dtype, w.comm_dtype)
+    z.allocate()
+    numel = wl.numels(w.shapes)
+    master0 = wl.master_init(z.offsets, numel, z.np, w.master_sigma, wl.master_seed(w.index),
+                             device="cuda")
+    z.init(master0, init_scale=w.init_scale, dynamic=w.dynamic, growth_interval=w.growth_interval)
+    return z, numel, master0
+
+
+def _grads(z, w, numel, step):
+    return [wl.flat_grads(z.offsets, numel, z.np, w.grad_sigma, wl.grad_seed(w.index, r, step),
+                          w.grad_dtype, device="cuda", zero_params=wl.zero_params(w, r))
+            for r in range(w.world)]
+
+
+def _hp(w):
+    return Hparams(lr=w.lr, beta1=w.beta1, beta2=w.beta2, eps=w.eps, weight_decay=w.weight_decay,
+                   max_grad_norm=w.max_grad_norm)
+
+
+def test_fullsize_qwen3_bf16_w2():
+    w = wl.workload("qwen3_0.6b_bf16_w2")
+    z, numel, master0 = _setup(w)
+    so = SampledOracle(z, numel, master0, sample_indices(z, numel, 200_000, 1), w.init_scale,
+                       w.dynamic, w.growth_interval)
+    del master0
+    for step in range(2):
+        g = _grads(z, w, numel, step)
+        z.step(g, _hp(w))
+        torch.cuda.synchronize()
+        st = z.scaler_state()
+        info, red_at = so.step(g, _hp(w))
+        so.check(st, info, red_at)
+        del g
+    z.close()
+
+
+def test_fullsize_qwen3_fp16_w8_stages_and_trajectory():
+    w = wl.workload("qwen3_0.6b_fp16_w8")
+    z2, numel, master0 = _setup(w, stage=2)
+    z1, _, _ = _setup(w, stage=1)
+    so = SampledOracle(z2, numel, master0, sample_indices(z2, numel, 100_000, 2), w.init_scale,
+                       w.dynamic, w.growth_interval)
+    del master0
+    g = _grads(z2, w, numel, 0)
+    hp = _hp(w)
+    # step 1: sampled parity, and ZeRO-1 == ZeRO-2 bit for bit
+    z2.step(g, hp)
+    z1.step(g, hp)
+    torch.cuda.synchronize()
+    st = z2.scaler_state()
+    assert st == z1.scaler_state()
+    info, red_at = so.step(g, hp)
+    so.check(st, info, red_at)
+    for a, b in ((z1.master, z2.master), (z1.m, z2.m), (z1.v, z2.v), (z1.params_flat, z2.params_flat)):
+        assert torch.equal(a.view(torch.int32 if a.dtype == torch.float32 else torch.int16),
+                           b.view(torch.int32 if b.dtype == torch.float32 else torch.int16))
+    z1.close()
+    # 199 more steps on the same gradients, +inf at 1-indexed steps 50/100/150/200
+    rank, idx = wl.inject_position(numel, z2.offsets, w.world, seed=3)
+    clean_ovf = info.overflow
+    bits = INF_BITS[wl.F16]
+    vals = [to_np(g[r][idx:idx + 1]) for r in range(w.world)]
+    vals[rank] = np.array([bits], np.uint16)
+    inj_ovf, _ = oracle.overflow_sumsq(oracle.reduce(vals, wl.F16, wl.F16), wl.F16)
+    saved = g[rank][idx].clone()
+    for step in range(2, 201):
+        inject = step % 50 == 0
+        if inject:
+            g[rank].view(torch.int16)[idx] = int(np.array(bits, np.uint16).view(np.int16))
+        z2.step(g, hp)
+        st = z2.scaler_state()
+        if inject:
+            g[rank][idx] = saved
+        # the oracle's scaler on the oracle's flags (norm irrelevant to the trajectory)
+        o_info = oracle.finalize(1.0, inj_ovf if inject else clean_ovf, w.world,
+                                 oracle.Hparams(), so.scaler)
+        assert (st["overflow"], st["skipped"]) == (o_info.overflow, o_info.skipped)
+        assert (st["scale"], st["counter"], st["t"]) == (so.scaler.scale, so.scaler.counter,
+                                                         so.scaler.t)
+    assert so.scaler.scale == 2.0 ** 12 and so.scaler.t == 196
+    z2.close()
+
+
+def test_fullsize_moe_w4_flat_and_tensors():
+    w = wl.workload("moe_3.9b_bf16_w4")
+    z, numel, master0 = _setup(w)
+    so = SampledOracle(z, numel, master0, sample_indices(z, numel, 100_000, 3), w.init_scale,
+                       w.dynamic, w.growth_interval)
+    del master0
+    g = _grads(z, w, numel, 0)
+    hp = _hp(w)
+    z.step(g, hp)
+    torch.cuda.synchronize()
+    st = z.scaler_state()
+    info, red_at = so.step(g, hp)
+    so.check(st, info, red_at)
+    # the same step from per-tensor pointers, the zero experts passed as NULL
+    zt, _, master0 = _setup(w)
+    del master0
+    per = []
+    for r in range(w.world):
+        zero = set(wl.zero_params(w, r))
+        per.append([None if p in zero else g[r][off:off + n]
+                    for p, (off, n) in enumerate(zip(zt.offsets, numel))])
+    zt.step_tensors(per, hp)
+    torch.cuda.synchronize()
+    assert zt.scaler_state() == st
+    for a, b in ((z.master, zt.master), (z.m, zt.m), (z.v, zt.v)):
+        assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+    assert torch.equal(z.params_flat.view(torch.int16), zt.params_flat.view(torch.int16))
+    zt.close()
+    z.close()

@@ -212,3 +212,13 @@ def inject_position(numel, param_offset, world: int, seed: int):
         p = (p + 1) % len(numel)
     k = int(rng.integers(0, int(numel[p])))
     return rank, int(param_offset[p]) + k
+
+
+def zero_params(w: Workload, rank: int):
+    """Parameters whose gradients are all zero on this rank: for the MoE
+    workload, the experts that rank's tokens did not route to (14 of 16 per
+    layer); none otherwise."""
+    if w.name.startswith("moe_"):
+        _, tags = moe_3_9b_shapes()
+        return moe_zero_experts(tags, rank, grad_seed(w.index, 0))
+    return []
