@@ -40,10 +40,10 @@ STATE_READ_BYTES = 144
 # (dram__bytes_read.sum + dram__bytes_write.sum / elements), with the capture
 # it comes from; None until a capture of the current kernel exists.
 NCU_TRAFFIC_PER_ELEM = {
-    # profiles/k_adamw_cast_bulk_qwen3_layers8.md: (1.7627 + 1.7008) GB / 125,847,552 elements
+    # profiles/k_adamw_cast_ws_qwen3_layers8.md: (1.7628 + 1.7007) GB / 125,847,552 elements
     "k_adamw_cast": 27.52,
-    # profiles/k_reduce_norm_bulk_qwen3_layers8.md: (504.0 + 212.6) MB / 125,847,552 elements
-    "k_reduce_norm": 5.694,
+    # the producer-warp reduce kernel has not been captured yet
+    "k_reduce_norm": None,
 }
 
 
@@ -54,10 +54,15 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
-    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--e2e-steps", type=int, default=5,
+                    help="end-to-end steps through the host-buffer entry point (0: skip)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="target CPU time of the oracle sample")
+    ap.add_argument("--world", type=int, default=None, help="override the simulated world size")
+    ap.add_argument("--bucket-bytes", type=int, default=None, help="override the bucket size")
+    ap.add_argument("--per-tensor-launch", action="store_true",
+                    help="launch the step tensor by tensor (the hook-style baseline)")
     ap.add_argument("--tensors", action="store_true",
                     help="step from per-tensor gradient pointers (NULL for all-zero gradients)")
     return ap.parse_args(argv)
@@ -185,6 +190,17 @@ def hbm_peak():
         return 6800.0, "fallback"
 
 
+def workload_of(args):
+    """The named workload with the command line's overrides."""
+    import workloads as wl
+    over = {}
+    if getattr(args, "world", None):
+        over["world"] = args.world
+    if getattr(args, "bucket_bytes", None):
+        over["bucket_bytes"] = args.bucket_bytes
+    return wl.workload(args.workload, **over)
+
+
 def config_of(w, scaling_note=None) -> dict:
     import workloads as wl
     cfg = {"workload": w.name, "n_params": w.n_real, "tensors": len(w.shapes),
@@ -284,7 +300,7 @@ def run_ours(args) -> dict | None:
     torch.cuda.set_device(local)
     device = torch.device("cuda", local)
     dist = init_dist(world, "nccl")
-    w = wl.workload(args.workload)
+    w = workload_of(args)
     K, W = args.steps, args.warmup
     if W < 3:
         raise SystemExit("--warmup must be at least 3")
@@ -314,6 +330,8 @@ def run_ours(args) -> dict | None:
     def do_step():
         if per_tensor is not None:
             z.step_tensors(per_tensor, hp)
+        elif args.per_tensor_launch:
+            z.step_per_tensor_launch(grads, hp)
         else:
             z.step(grads, hp)
     hp = Hparams(lr=w.lr, beta1=w.beta1, beta2=w.beta2, eps=w.eps, weight_decay=w.weight_decay,
@@ -368,18 +386,23 @@ def run_ours(args) -> dict | None:
 
     # End to end through the host-buffer entry point: pinned host gradients are
     # copied in every step and the step's scaler state is read back.
-    E = max(1, args.e2e_steps)
-    host = [g.cpu().pin_memory() for g in grads]
-    z.step_host(host, grads, hp)
-    z.scaler_state()
-    torch.cuda.synchronize()
-    barrier(dist, device)
-    t0 = time.perf_counter()
-    for _ in range(E):
+    E = args.e2e_steps
+    e2e = None
+    if E > 0:
+        host = [g.cpu().pin_memory() for g in grads]
         z.step_host(host, grads, hp)
-        z.scaler_state()  # device-to-host read of the step's result; synchronises
-    e2e_s = max_over_ranks(dist, time.perf_counter() - t0, device)
-    del host
+        z.scaler_state()
+        torch.cuda.synchronize()
+        barrier(dist, device)
+        t0 = time.perf_counter()
+        for _ in range(E):
+            z.step_host(host, grads, hp)
+            z.scaler_state()  # device-to-host read of the step's result; synchronises
+        e2e_s = max_over_ranks(dist, time.perf_counter() - t0, device)
+        del host
+        e2e = {"value": job_value(info.n_real, world, e2e_s / E), "unit": "params/s",
+               "h2d_bytes_per_step": w.world * z.np * wl.ELEM_BYTES[w.grad_dtype],
+               "d2h_bytes_per_step": STATE_READ_BYTES}
 
     N = info.n_real
     peak, peak_src = hbm_peak()
@@ -408,7 +431,8 @@ def run_ours(args) -> dict | None:
         "dtype": "f32",
         "data": "synthetic",
         "config": config_of(w, "per-tensor gradient pointers, NULL for all-zero gradients"
-                            if args.tensors else None),
+                            if args.tensors else ("one reduce and one update launch per tensor"
+                                                  if args.per_tensor_launch else None)),
         "hbm_gbs_step": step_gbs,
         "step_roofline": {"bytes_per_param": info.step_bytes_per_elem, "peak_gbs": peak,
                           "frac": step_gbs / peak, "peak_source": peak_src},
@@ -420,9 +444,8 @@ def run_ours(args) -> dict | None:
                        "k_reduce_norm_gbs": k1_bytes / (k1_ms / 1e3) / 1e9,
                        "k_adamw_cast_gbs": k3_bytes / (k3_ms / 1e3) / 1e9},
         "skip_step_ms": skip_ms,
-        "e2e": {"value": job_value(N, world, e2e_s / E), "unit": "params/s",
-                "h2d_bytes_per_step": w.world * z.np * G, "d2h_bytes_per_step": STATE_READ_BYTES},
-        "gpu_launches": 3 * K,
+        "e2e": e2e,
+        "gpu_launches": K * ((2 * sum(1 for n in numel if n > 0) + 1) if args.per_tensor_launch else 3),
         "clocks": clocks,
     }
     z.close()
@@ -445,7 +468,7 @@ def run_reference(args) -> dict | None:
     rank, world, _ = dist_env()
     if rank != 0:
         return None
-    w = wl.workload(args.workload)
+    w = workload_of(args)
     # size each step's sample so the whole run stays within about two minutes
     rate0, _, _, _ = time_oracle(w, 1_000_000, 0.0, min_steps=1)
     per_step = max(1_000_000, int(rate0 * 120.0 / max(1, args.steps + args.warmup)))
@@ -470,7 +493,7 @@ def main(argv=None):
         rank, world, _ = dist_env()
         if out is not None and world == 1 and not args.no_cpu_baseline:
             import workloads as wl
-            out["cpu_baseline"] = cpu_baseline(wl.workload(args.workload), args.cpu_seconds)
+            out["cpu_baseline"] = cpu_baseline(workload_of(args), args.cpu_seconds)
     if out is not None:
         print(json.dumps(out), flush=True)
 

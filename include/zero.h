@@ -248,6 +248,16 @@ int zero_step(zero_layout_t* layout, const void* const* grads, void* const* allr
 int zero_step_tensors(zero_layout_t* layout, const void* const* grad_ptrs,
                       void* const* allreduce_out, const zero_hparams* hp, void* stream);
 
+/* The same step launched tensor by tensor: one reduce launch per parameter,
+ * the finalize, then one update launch per parameter (2P + 1 launches). This
+ * is the per-parameter, hook-driven form of the prior art ([NM] "Benchmarks":
+ * about 2k collective calls per backward, bound by launch cost), kept as the
+ * baseline the flat three-launch step is measured against. Arguments,
+ * arithmetic and results are those of zero_step; only the norm's summation
+ * order differs. */
+int zero_step_per_tensor_launch(zero_layout_t* layout, const void* const* grads,
+                                void* const* allreduce_out, const zero_hparams* hp, void* stream);
+
 /* Same step from HOST gradients: copies host_grads[w] (Np elements of
  * grad_dtype each, flat layout; pinned memory gives asynchronous copies) into
  * the device buffers dev_grads[w] with one cudaMemcpyAsync per rank on

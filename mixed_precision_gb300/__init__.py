@@ -11,6 +11,6 @@ from ._abi import (ZERO_BF16, ZERO_F16, ZERO_F32, ZeroError, zero_bucket_range, 
                    zero_layout_set_allocator, zero_loss_scale_state, zero_param_offset,
                    zero_scaler_cfg, zero_scaler_state, zero_set_step_events, zero_shard_range, zero_state_bind,
                    zero_state_export, zero_state_import, zero_state_init, zero_step,
-                   zero_step_host, zero_step_tensors, lib)
+                   zero_step_host, zero_step_per_tensor_launch, zero_step_tensors, lib)
 
 __all__ = [n for n in dir() if n.startswith("zero_") or n.startswith("ZERO_")] + ["ZeroError", "lib"]

@@ -91,6 +91,7 @@ def lib() -> ctypes.CDLL:
             "zero_state_init": [P, P, ctypes.POINTER(zero_scaler_cfg), P],
             "zero_step": [P, PP, PP, ctypes.POINTER(zero_hparams), P],
             "zero_step_tensors": [P, PP, PP, ctypes.POINTER(zero_hparams), P],
+            "zero_step_per_tensor_launch": [P, PP, PP, ctypes.POINTER(zero_hparams), P],
             "zero_step_host": [P, PP, PP, PP, ctypes.POINTER(zero_hparams), P],
             "zero_loss_scale_state": [P, P, ctypes.POINTER(zero_scaler_state)],
             "zero_gather_params": [P, PP, I, P],
@@ -174,6 +175,13 @@ def zero_state_init(layout: int, master_init_flat: int, cfg: zero_scaler_cfg, st
 def zero_step(layout: int, grads, allreduce_out, hp: zero_hparams, stream: int) -> None:
     ar = _ptrs(allreduce_out) if allreduce_out is not None else None
     _check(lib().zero_step(layout, _ptrs(grads), ar, ctypes.byref(hp), stream or None))
+
+
+def zero_step_per_tensor_launch(layout: int, grads, allreduce_out, hp: zero_hparams,
+                                stream: int) -> None:
+    ar = _ptrs(allreduce_out) if allreduce_out is not None else None
+    _check(lib().zero_step_per_tensor_launch(layout, _ptrs(grads), ar, ctypes.byref(hp),
+                                             stream or None))
 
 
 def zero_step_tensors(layout: int, grad_ptrs, allreduce_out, hp: zero_hparams, stream: int) -> None:

@@ -49,6 +49,7 @@ int dtype_bytes(int d) { return d == ZERO_F32 ? 4 : 2; }
 bool valid_dtype(int d) { return d == ZERO_F32 || d == ZERO_F16 || d == ZERO_BF16; }
 
 constexpr int kMaxPartials = 4096;  // upper bound on the reduce grid (SMs x blocks/SM)
+constexpr int kMaxPerTensorGrid = 1024;  // per-tensor launches: blocks per launch at most
 
 void* default_alloc(size_t n, void*) {
   void* p = nullptr;
@@ -68,6 +69,11 @@ struct zero_layout {
   std::vector<int64_t> bstart, blen;
   int64_t n_real = 0, np = 0;
   std::vector<Tile> tiles;
+  // the same tiles grouped by parameter (per-tensor launches): parameter p's
+  // tiles are tiles_pt[pt_begin[p] .. pt_begin[p+1])
+  std::vector<Tile> tiles_pt;
+  std::vector<int> pt_begin;
+  int64_t pt_partials = 0;  // sum over parameters of min(tiles, kMaxPerTensorGrid)
 
   zero_alloc_fn alloc = default_alloc;
   zero_free_fn free_fn = default_free;
@@ -91,11 +97,16 @@ struct zero_layout {
   unsigned* d_ovf = nullptr;
   DevState* d_state = nullptr;
   const void** d_table = nullptr;  // W * n_params grad pointers (table mode)
+  Tile* d_tiles_pt = nullptr;
+  double* d_part_pt = nullptr;
+  unsigned* d_ovf_pt = nullptr;
   void* d_gather = nullptr;        // replica pointer table for K4 (grown on demand)
   size_t gather_cap = 0;
 
   int grid_reduce = 0, grid_update = 0, grid_copy = 0;
-  // 1: shared-memory pipelines fed by cp.async.bulk; 0: register-staged loads
+  // 1 (default): shared-memory pipelines fed by cp.async.bulk; 0: the
+  // register-staged kernels, kept as the comparison baseline (environment
+  // ZERO_REDUCE_VARIANT / ZERO_UPDATE_VARIANT = 0 at bind selects them)
   int reduce_variant = 1, update_variant = 1;
   cudaEvent_t events[4] = {nullptr, nullptr, nullptr, nullptr};
   bool timing = false;
@@ -182,6 +193,35 @@ void build_layout(zero_layout* L) {
     shard_prefix += slice;
     p_lo = p_hi;
   }
+
+  L->tiles_pt = L->tiles;
+  std::stable_sort(L->tiles_pt.begin(), L->tiles_pt.end(),
+                   [](const Tile& a, const Tile& b) { return a.param < b.param; });
+  L->pt_begin.assign(P + 1, 0);
+  for (const Tile& t : L->tiles_pt) L->pt_begin[t.param + 1] += 1;
+  for (int p = 0; p < P; ++p) L->pt_begin[p + 1] += L->pt_begin[p];
+  L->pt_partials = 0;
+  for (int p = 0; p < P; ++p)
+    L->pt_partials += std::min(L->pt_begin[p + 1] - L->pt_begin[p], kMaxPerTensorGrid);
+}
+
+// Sizes of the library's device block, in allocation order.
+struct BlockPlan {
+  size_t tiles, part, ovf, state, table, tiles_pt, part_pt, ovf_pt, total;
+};
+
+BlockPlan plan_block(const zero_layout* L) {
+  BlockPlan b{};
+  b.tiles = align_up((int64_t)L->tiles.size() * sizeof(Tile), 256);
+  b.part = align_up(kMaxPartials * sizeof(double), 256);
+  b.ovf = align_up(kMaxPartials * sizeof(unsigned), 256);
+  b.state = align_up(sizeof(DevState), 256);
+  b.table = align_up((int64_t)L->cfg.world * (int64_t)L->numel.size() * sizeof(void*), 256);
+  b.tiles_pt = b.tiles;
+  b.part_pt = align_up(std::max<int64_t>(1, L->pt_partials) * sizeof(double), 256);
+  b.ovf_pt = align_up(std::max<int64_t>(1, L->pt_partials) * sizeof(unsigned), 256);
+  b.total = b.tiles + b.part + b.ovf + b.state + b.table + b.tiles_pt + b.part_pt + b.ovf_pt;
+  return b;
 }
 
 int launch_step(zero_layout* L, const GradSrc& src, void* const* allreduce_out,
@@ -233,6 +273,69 @@ int launch_step(zero_layout* L, const GradSrc& src, void* const* allreduce_out,
     ua.state = L->d_state;
     ua.error = &L->d_state->error;
     e = launch_update(ua, L->grid_update, L->update_variant, s);
+    if (e != cudaSuccess) return cuda_fail(e, "update kernel launch");
+  }
+  if (L->timing) ZERO_CUDA(cudaEventRecord(L->events[3], s));
+  return ZERO_OK;
+}
+
+// The step launched tensor by tensor (the hook-style baseline): per
+// parameter, the reduce kernel over that parameter's tiles with its own slice
+// of the partials; the finalize over all of them; per parameter, the update.
+int launch_step_per_tensor(zero_layout* L, const GradSrc& src, void* const* allreduce_out,
+                           const zero_hparams* hp, cudaStream_t s) {
+  const int W = L->world();
+  const int P = L->n_params();
+  ReduceArgs ra{};
+  ra.world = W;
+  ra.stage = L->cfg.stage;
+  ra.grad_dtype = L->cfg.grad_dtype;
+  ra.comm_dtype = L->comm_dtype;
+  ra.src = src;
+  if (L->cfg.stage == 1) {
+    for (int w = 0; w < W; ++w) ra.out.base[w] = allreduce_out[w];
+  } else {
+    ra.out.base[0] = L->scratch;
+  }
+  ra.chunk = reduce_chunk(W, L->cfg.grad_dtype);
+  ra.error = &L->d_state->error;
+  if (L->timing) ZERO_CUDA(cudaEventRecord(L->events[0], s));
+  int64_t part_at = 0;
+  for (int p = 0; p < P; ++p) {
+    const int n = L->pt_begin[p + 1] - L->pt_begin[p];
+    if (n == 0) continue;
+    const int grid = std::min({n, kMaxPerTensorGrid, L->grid_reduce});
+    ra.tiles = L->d_tiles_pt + L->pt_begin[p];
+    ra.n_tiles = n;
+    ra.part_sumsq = L->d_part_pt + part_at;
+    ra.part_ovf = L->d_ovf_pt + part_at;
+    cudaError_t e = launch_reduce(ra, grid, L->reduce_variant, s);
+    if (e != cudaSuccess) return cuda_fail(e, "reduce kernel launch");
+    part_at += grid;
+  }
+  if (L->timing) ZERO_CUDA(cudaEventRecord(L->events[1], s));
+  Hparams h{hp->lr, hp->beta1, hp->beta2, hp->eps, hp->weight_decay, hp->max_grad_norm,
+            hp->grad_divisor};
+  cudaError_t e = launch_finalize(L->d_part_pt, L->d_ovf_pt, (int)part_at, W, h, L->d_state, s);
+  if (e != cudaSuccess) return cuda_fail(e, "finalize kernel launch");
+  if (L->timing) ZERO_CUDA(cudaEventRecord(L->events[2], s));
+  UpdateArgs ua{};
+  ua.stage = L->cfg.stage;
+  ua.comm_dtype = L->comm_dtype;
+  ua.param_dtype = L->cfg.param_dtype;
+  ua.red = ra.out;
+  ua.master = L->master;
+  ua.m = L->m;
+  ua.v = L->v;
+  ua.params_flat = L->params;
+  ua.state = L->d_state;
+  ua.error = &L->d_state->error;
+  for (int p = 0; p < P; ++p) {
+    const int n = L->pt_begin[p + 1] - L->pt_begin[p];
+    if (n == 0) continue;
+    ua.tiles = L->d_tiles_pt + L->pt_begin[p];
+    ua.n_tiles = n;
+    e = launch_update(ua, std::min(n, L->grid_update), L->update_variant, s);
     if (e != cudaSuccess) return cuda_fail(e, "update kernel launch");
   }
   if (L->timing) ZERO_CUDA(cudaEventRecord(L->events[3], s));
@@ -369,10 +472,7 @@ int zero_layout_query(const zero_layout_t* L, zero_layout_info* o) {
   o->params_bytes = L->np * (int64_t)P;
   o->scratch_bytes = L->cfg.stage == 2 ? L->np * C : 0;
   o->allreduce_bytes = L->cfg.stage == 1 ? L->np * C : 0;
-  const size_t tiles = align_up((int64_t)L->tiles.size() * sizeof(Tile), 256);
-  o->device_bytes_owned = (int64_t)(tiles + align_up(kMaxPartials * 8, 256) +
-                                    align_up(kMaxPartials * 4, 256) + align_up(sizeof(DevState), 256) +
-                                    align_up((int64_t)W * L->n_params() * 8, 256));
+  o->device_bytes_owned = (int64_t)plan_block(L).total;
   o->ledger_bytes_per_param = L->cfg.stage == 1 ? P + G + 12.0 / W : P + G / W + 12.0 / W;
   o->step_bytes_per_elem = W * G + 24.0 + P;
   return ZERO_OK;
@@ -422,26 +522,34 @@ int zero_state_bind(zero_layout_t* L, void* master, void* m, void* v, void* para
     return fail(ZERO_ERR_INVALID, "stage 2 needs a 16-byte aligned scratch buffer");
 
   if (L->dblock == nullptr) {
-    const size_t tiles_b = align_up((int64_t)L->tiles.size() * sizeof(Tile), 256);
-    const size_t part_b = align_up(kMaxPartials * sizeof(double), 256);
-    const size_t ovf_b = align_up(kMaxPartials * sizeof(unsigned), 256);
-    const size_t state_b = align_up(sizeof(DevState), 256);
-    const size_t table_b = align_up((int64_t)L->world() * L->n_params() * sizeof(void*), 256);
-    const size_t total = tiles_b + part_b + ovf_b + state_b + table_b;
-    void* blk = L->alloc(total, L->alloc_ctx);
-    if (blk == nullptr) return fail(ZERO_ERR_OOM, "device allocation of %zu bytes failed", total);
+    const BlockPlan b = plan_block(L);
+    void* blk = L->alloc(b.total, L->alloc_ctx);
+    if (blk == nullptr) return fail(ZERO_ERR_OOM, "device allocation of %zu bytes failed", b.total);
     char* c = static_cast<char*>(blk);
     L->dblock = blk;
-    L->dblock_bytes = total;
+    L->dblock_bytes = b.total;
     L->d_tiles = reinterpret_cast<Tile*>(c);
-    L->d_part = reinterpret_cast<double*>(c + tiles_b);
-    L->d_ovf = reinterpret_cast<unsigned*>(c + tiles_b + part_b);
-    L->d_state = reinterpret_cast<DevState*>(c + tiles_b + part_b + ovf_b);
-    L->d_table = reinterpret_cast<const void**>(c + tiles_b + part_b + ovf_b + state_b);
+    c += b.tiles;
+    L->d_part = reinterpret_cast<double*>(c);
+    c += b.part;
+    L->d_ovf = reinterpret_cast<unsigned*>(c);
+    c += b.ovf;
+    L->d_state = reinterpret_cast<DevState*>(c);
+    c += b.state;
+    L->d_table = reinterpret_cast<const void**>(c);
+    c += b.table;
+    L->d_tiles_pt = reinterpret_cast<Tile*>(c);
+    c += b.tiles_pt;
+    L->d_part_pt = reinterpret_cast<double*>(c);
+    c += b.part_pt;
+    L->d_ovf_pt = reinterpret_cast<unsigned*>(c);
     if (!L->tiles.empty()) {
       cudaError_t e = cudaMemcpy(L->d_tiles, L->tiles.data(), L->tiles.size() * sizeof(Tile),
                                  cudaMemcpyHostToDevice);
-      if (e != cudaSuccess) return cuda_fail(e, "upload of the tile table");
+      if (e == cudaSuccess)
+        e = cudaMemcpy(L->d_tiles_pt, L->tiles_pt.data(), L->tiles_pt.size() * sizeof(Tile),
+                       cudaMemcpyHostToDevice);
+      if (e != cudaSuccess) return cuda_fail(e, "upload of the tile tables");
     }
     int dev = 0, sms = 0;
     ZERO_CUDA(cudaGetDevice(&dev));
@@ -509,6 +617,21 @@ int zero_step(zero_layout_t* L, const void* const* grads, void* const* allreduce
     src.base[w] = grads[w];
   }
   return launch_step(L, src, allreduce_out, hp, static_cast<cudaStream_t>(stream));
+}
+
+int zero_step_per_tensor_launch(zero_layout_t* L, const void* const* grads,
+                                void* const* allreduce_out, const zero_hparams* hp, void* stream) {
+  if (int rc = check_ready(L, true)) return rc;
+  if (int rc = check_hparams(hp)) return rc;
+  if (int rc = check_allreduce(L, allreduce_out)) return rc;
+  if (grads == nullptr) return fail(ZERO_ERR_INVALID, "grads is NULL");
+  GradSrc src{};
+  for (int w = 0; w < L->world(); ++w) {
+    if (grads[w] == nullptr || !aligned16(grads[w]))
+      return fail(ZERO_ERR_INVALID, "grads[%d] is NULL or not 16-byte aligned", w);
+    src.base[w] = grads[w];
+  }
+  return launch_step_per_tensor(L, src, allreduce_out, hp, static_cast<cudaStream_t>(stream));
 }
 
 int zero_step_tensors(zero_layout_t* L, const void* const* grad_ptrs, void* const* allreduce_out,

@@ -110,9 +110,10 @@ struct UpdateArgs {
 
 // Kernel launchers. Each returns the launch's cudaError_t.
 // Kernel variants: 0 = register-staged loads; 1 = shared-memory stages filled
-// by cp.async.bulk.
+// by cp.async.bulk from a producer warp, consumed by 8 consumer warps.
 constexpr int kRedStages = 3;
 constexpr int kRedStageBytes = 32768;
+constexpr int kRedConsumers = 8;  // consumer warps of the warp-specialised reduce
 int reduce_chunk(int world, int grad_dtype);  // elements per stage of the pipelined variant
 cudaError_t launch_reduce(const ReduceArgs& a, int grid, int variant, cudaStream_t s);
 int reduce_blocks_per_sm(int grad_dtype, int comm_dtype, int world, int stage, int variant);

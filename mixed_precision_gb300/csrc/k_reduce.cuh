@@ -170,81 +170,105 @@ __global__ void __launch_bounds__(kThreads, 4) k_reduce_norm(const __grid_consta
 }
 
 // ---------------------------------------------------------------------------
-// K1, shared-memory pipeline. Same arithmetic and outputs as k_reduce_norm.
-// Each stage holds one chunk (a.chunk elements) of all W ranks' gradients,
-// copied in by cp.async.bulk (one request per rank, issued by one thread,
-// completed on the stage's mbarrier); kRedStages stages in flight. A NULL
-// per-tensor gradient is not copied and reads as zeros. The chunk's last
-// (len mod 8) elements come from global memory directly. Bounded waits; on
-// timeout the block records kErrWaitTimeout, waits for its copies in flight
-// and returns without a partial (the host reports ZERO_ERR_TIMEOUT).
+// K1, shared-memory pipeline (the default). Same arithmetic and outputs as
+// k_reduce_norm. Each stage holds one chunk (a.chunk elements) of all W
+// ranks' gradients (kRedStageBytes), copied in by cp.async.bulk, kRedStages
+// stages deep; a NULL per-tensor gradient is not copied and reads as zeros;
+// a chunk's last (len mod 8) elements come from global memory directly. One
+// producer warp (lane 0) fills the stages with one
+// cp.async.bulk per rank and chunk; NC consumer warps each reduce a fixed
+// slice of every chunk and release the stage on its "empty" mbarrier. The
+// block's norm partial is assembled without a block barrier: each consumer
+// warp leaves its partial in a shared slot and the last warp to finish (a
+// shared-memory counter) adds the slots in warp order, so the result is the
+// same on every run. A warp whose bounded wait gives up records
+// kErrWaitTimeout and leaves; the block then writes no partial.
 // ---------------------------------------------------------------------------
-template <typename GT, typename CT, int WT, bool STAGE1>
-__global__ void __launch_bounds__(kThreads) k_reduce_norm_bulk(const __grid_constant__ ReduceArgs a) {
+template <typename GT, typename CT, int WT, bool STAGE1, int NC>
+__global__ void __launch_bounds__((NC + 1) * 32)
+    k_reduce_norm_ws(const __grid_constant__ ReduceArgs a) {
   constexpr int S = kRedStages;
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ __align__(8) uint64_t full[S];
-  __shared__ double s_red[kThreads / 32];
-  __shared__ unsigned s_or[kThreads / 32];
+  __shared__ __align__(8) uint64_t empty[S];
+  __shared__ double s_part[NC];
+  __shared__ unsigned s_flag[NC];
+  __shared__ unsigned s_done;
   const int W = WT ? WT : a.world;
   const int C = a.chunk;
   const int kStage = W * C * (int)sizeof(GT);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < S; ++s) mbar_init(&full[s], 1);
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], NC);
+    }
+    s_done = 0u;
     mbar_init_fence();
   }
   __syncthreads();
 
-  int pt = blockIdx.x, pc = 0;
-  unsigned issued = 0;
-  auto issue = [&](int s) {
-    if (pt >= a.n_tiles) return;
-    const Tile tl = a.tiles[pt];
-    const int clen = min(C, tl.len - pc);
-    const int nb = clen & ~7;
-    GT* base = reinterpret_cast<GT*>(smem + s * kStage);
-    uint32_t bytes = 0;
-    for (int w = 0; w < W; ++w)
-      if (nb > 0 && grad_ptr<GT>(a, tl, w) != nullptr) bytes += nb * (uint32_t)sizeof(GT);
-    if (bytes > 0) {
-      mbar_arrive_expect_tx(&full[s], bytes);
-      for (int w = 0; w < W; ++w) {
-        const GT* g = grad_ptr<GT>(a, tl, w);
-        if (g != nullptr) bulk_g2s(base + w * C, g + pc, nb * (int)sizeof(GT), &full[s]);
+  if (warp == NC) {  // producer
+    if (lane != 0) return;
+    int pt = blockIdx.x, pc = 0;
+    unsigned k = 0;
+    bool ok = true;
+    while (pt < a.n_tiles) {
+      const int s = (int)(k % S);
+      if (k >= (unsigned)S && !mbar_wait(&empty[s], ((k / S) - 1) & 1u)) {
+        ok = false;
+        break;
       }
-    } else {
-      mbar_arrive(&full[s]);
+      const Tile tl = a.tiles[pt];
+      const int clen = min(C, tl.len - pc);
+      const int nb = clen & ~7;
+      GT* base = reinterpret_cast<GT*>(smem + s * kStage);
+      uint32_t bytes = 0;
+      for (int w = 0; w < W; ++w)
+        if (nb > 0 && grad_ptr<GT>(a, tl, w) != nullptr) bytes += nb * (uint32_t)sizeof(GT);
+      if (bytes > 0) {
+        mbar_arrive_expect_tx(&full[s], bytes);
+        for (int w = 0; w < W; ++w) {
+          const GT* g = grad_ptr<GT>(a, tl, w);
+          if (g != nullptr) bulk_g2s(base + w * C, g + pc, nb * (int)sizeof(GT), &full[s]);
+        }
+      } else {
+        mbar_arrive(&full[s]);
+      }
+      ++k;
+      pc += C;
+      if (pc >= tl.len) {
+        pc = 0;
+        pt += gridDim.x;
+      }
     }
-    ++issued;
-    pc += C;
-    if (pc >= tl.len) {
-      pc = 0;
-      pt += gridDim.x;
+    if (!ok) {
+      atomicOr(a.error, kErrWaitTimeout);
+      for (unsigned j = k > (unsigned)S ? k - S : 0u; j < k; ++j) mbar_wait(&full[j % S], (j / S) & 1u);
     }
-  };
-  if (threadIdx.x == 0)
-    for (int s = 0; s < S; ++s) issue(s);
+    return;
+  }
 
+  // consumers: warp `warp` owns elements [warp*per, (warp+1)*per) of every chunk
+  const int per = ((C / NC) + 7) & ~7;
   float hi = 0.0f, lo = 0.0f;
   double big = 0.0;
   unsigned bad = 0u;
   int ct = blockIdx.x, cc = 0;
   unsigned k = 0;
-  bool ok = true;
   while (ct < a.n_tiles) {
     const int s = (int)(k % S);
-    const uint32_t parity = (k / S) & 1u;
     const Tile tl = a.tiles[ct];
     const int clen = min(C, tl.len - cc);
     const int nb = clen & ~7;
-    const bool mine = mbar_wait(&full[s], parity);
-    if (!__syncthreads_and(mine)) {
-      ok = false;
-      break;
+    if (!__all_sync(0xffffffffu, mbar_wait(&full[s], (k / S) & 1u))) {
+      if (lane == 0) atomicOr(a.error, kErrWaitTimeout);
+      return;
     }
     const GT* base = reinterpret_cast<const GT*>(smem + s * kStage);
-    for (int e = 8 * threadIdx.x; e < nb; e += 8 * kThreads) {
+    const int e_end = min(nb, (warp + 1) * per);
+    for (int e = warp * per + 8 * lane; e < e_end; e += 256) {
       float acc[8];
       if (grad_ptr<GT>(a, tl, 0) != nullptr) {
         load8_smem(base + e, acc);
@@ -284,9 +308,8 @@ __global__ void __launch_bounds__(kThreads) k_reduce_norm_bulk(const __grid_cons
         store8_raw(static_cast<CT*>(a.out.base[0]) + tl.shard + cc + e, rc);
       }
     }
-    const int tail = clen - nb;
-    if (threadIdx.x < tail) {
-      const int64_t i = (int64_t)cc + nb + threadIdx.x;
+    if (warp == 0 && lane < clen - nb) {
+      const int64_t i = (int64_t)cc + nb + lane;
       float sum = load1(grad_ptr<GT>(a, tl, 0), i);
       for (int w = 1; w < W; ++w) sum = __fadd_rn(sum, load1(grad_ptr<GT>(a, tl, w), i));
       const CT rc = DT<CT>::from_f32(sum);
@@ -299,8 +322,8 @@ __global__ void __launch_bounds__(kThreads) k_reduce_norm_bulk(const __grid_cons
         static_cast<CT*>(a.out.base[0])[tl.shard + i] = rc;
       }
     }
-    __syncthreads();  // stage s is free again
-    if (threadIdx.x == 0) issue(s);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);
     ++k;
     cc += C;
     if (cc >= tl.len) {
@@ -308,24 +331,33 @@ __global__ void __launch_bounds__(kThreads) k_reduce_norm_bulk(const __grid_cons
       ct += gridDim.x;
     }
   }
-  if (!ok) {
-    if (threadIdx.x == 0) {
-      atomicOr(a.error, kErrWaitTimeout);
-      for (unsigned j = k; j < issued; ++j) mbar_wait(&full[j % S], (j / S) & 1u);
+  // warp partial (fixed shuffle tree), then the last warp adds the slots in order
+  double x = (double)hi + (double)lo + big;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x += __shfl_down_sync(0xffffffffu, x, o);
+  const unsigned any = __any_sync(0xffffffffu, bad != 0u) ? 1u : 0u;
+  if (lane == 0) {
+    s_part[warp] = x;
+    s_flag[warp] = any;
+    __threadfence_block();
+    if (atomicAdd(&s_done, 1u) == NC - 1) {
+      __threadfence_block();
+      double total = 0.0;
+      unsigned f = 0u;
+      for (int w = 0; w < NC; ++w) {
+        total += *reinterpret_cast<volatile double*>(&s_part[w]);
+        f |= *reinterpret_cast<volatile unsigned*>(&s_flag[w]);
+      }
+      a.part_sumsq[blockIdx.x] = total;
+      a.part_ovf[blockIdx.x] = f;
     }
-    return;
-  }
-  const double total = block_sum<kThreads>((double)hi + (double)lo + big, s_red);
-  const unsigned any_bad = block_or<kThreads>(bad, s_or);
-  if (threadIdx.x == 0) {
-    a.part_sumsq[blockIdx.x] = total;
-    a.part_ovf[blockIdx.x] = any_bad;
   }
 }
 
 template <typename GT, typename CT, int WT, bool S1>
 const void* reduce_kernel_v(int variant) {
-  if (variant == 1) return reinterpret_cast<const void*>(&k_reduce_norm_bulk<GT, CT, WT, S1>);
+  if (variant == 1)
+    return reinterpret_cast<const void*>(&k_reduce_norm_ws<GT, CT, WT, S1, kRedConsumers>);
   return reinterpret_cast<const void*>(&k_reduce_norm<GT, CT, WT, S1>);
 }
 

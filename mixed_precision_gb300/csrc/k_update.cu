@@ -27,8 +27,10 @@ int reduce_chunk(int world, int grad_dtype) {
   return c < 128 ? 128 : c;
 }
 
+static int reduce_threads(int variant) { return variant == 1 ? (kRedConsumers + 1) * 32 : kThreads; }
+
 static int reduce_smem(int world, int grad_dtype, int variant) {
-  if (variant != 1) return 0;
+  if (variant == 0) return 0;
   const int g = grad_dtype == kF32 ? 4 : 2;
   return kRedStages * world * reduce_chunk(world, grad_dtype) * g;
 }
@@ -37,7 +39,7 @@ cudaError_t launch_reduce(const ReduceArgs& a, int grid, int variant, cudaStream
   const void* f = reduce_kernel(a.grad_dtype, a.comm_dtype, a.world, a.stage, variant);
   if (f == nullptr) return cudaErrorInvalidValue;
   void* args[] = {const_cast<ReduceArgs*>(&a)};
-  return cudaLaunchKernel(f, dim3(grid), dim3(kThreads), args,
+  return cudaLaunchKernel(f, dim3(grid), dim3(reduce_threads(variant)), args,
                           reduce_smem(a.world, a.grad_dtype, variant), s);
 }
 
@@ -49,7 +51,9 @@ int reduce_blocks_per_sm(int grad_dtype, int comm_dtype, int world, int stage, i
                       cudaSuccess)
     return 0;
   int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, f, kThreads, smem) != cudaSuccess) return 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, f, reduce_threads(variant), smem) !=
+      cudaSuccess)
+    return 0;
   return n;
 }
 
@@ -219,33 +223,94 @@ __global__ void __launch_bounds__(kThreads) k_adamw_cast(const __grid_constant__
   }
 }
 
-// ---------------------------------------------------------------------------
-// K3, shared-memory pipeline. The same arithmetic as k_adamw_cast; the four
-// input streams (master, m, v, reduced gradient) of each chunk of C elements
-// arrive in a shared-memory stage by cp.async.bulk, issued by one thread and
-// completed on the stage's mbarrier, S stages deep. The threads read the
-// stage, update, and write master/m/v/params straight to global memory. One
-// thread moving 14 bytes per element in four bulk requests replaces seven
-// 16-byte loads per thread, which kept the load/store queues full.
-// A chunk's last (len mod 8) elements are not bulk-copied (16-byte rule) and
-// are handled from global memory directly. Every wait is bounded; on timeout
-// the block records kErrWaitTimeout, waits (bounded) for its copies in flight
-// and returns.
-// ---------------------------------------------------------------------------
 template <typename CT>
 struct UpdStage {
   __host__ __device__ static constexpr int bytes(int C) { return C * (12 + (int)sizeof(CT)); }
 };
 
-template <typename CT, typename PT, int C, int S>
-__global__ void __launch_bounds__(kThreads) k_adamw_cast_bulk(const __grid_constant__ UpdateArgs a) {
-  static_assert(C % (4 * kThreads) == 0, "chunk must be whole 4-element groups per thread");
+// ---------------------------------------------------------------------------
+// K3, shared-memory pipeline (the default). The same arithmetic as
+// k_adamw_cast; the four input streams of each chunk of C elements (master,
+// m, v, reduced gradient: 14 bytes per element) arrive in a shared-memory
+// stage by cp.async.bulk, S stages deep, completed on the stage's "full"
+// mbarrier. One thread moving them in four bulk requests replaces seven
+// 16-byte loads per thread, which kept the load/store queues full; a chunk's
+// last (len mod 8) elements are not bulk-copied (16-byte rule) and come from
+// global memory directly. One producer warp (its lane 0) issues the
+// bulk copies of each chunk into the next free stage; NC consumer warps each
+// update a fixed slice of every chunk and release the stage by arriving on
+// its "empty" mbarrier. No block-wide barrier in the loop: consumer warps
+// never wait for one another, only for data. Bounded, warp-uniform waits: a
+// consumer warp that times out records kErrWaitTimeout and leaves; the
+// producer then times out on the stage that warp never releases, records
+// the error, waits (bounded) for its copies in flight and leaves.
+// ---------------------------------------------------------------------------
+template <typename CT, typename PT, int C, int S, int NC>
+__global__ void __launch_bounds__((NC + 1) * 32)
+    k_adamw_cast_ws(const __grid_constant__ UpdateArgs a) {
+  constexpr int kPerWarp = C / NC;
+  static_assert(kPerWarp % 128 == 0, "a warp's slice must be whole 4-element groups per lane");
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ __align__(8) uint64_t full[S];
+  __shared__ __align__(8) uint64_t empty[S];
   constexpr int kStage = UpdStage<CT>::bytes(C);
 
   const DevState* st = a.state;
   if (st->skip) return;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], NC);
+    }
+    mbar_init_fence();
+  }
+  __syncthreads();
+
+  auto red_ptr = [&](const Tile& tl) -> const CT* {
+    return a.stage == 1 ? static_cast<const CT*>(a.red.base[tl.rank]) + tl.flat
+                        : static_cast<const CT*>(a.red.base[0]) + tl.shard;
+  };
+
+  if (warp == NC) {  // producer
+    if (lane != 0) return;
+    int pt = blockIdx.x, pc = 0;
+    unsigned k = 0;
+    bool ok = true;
+    while (pt < a.n_tiles) {
+      const int s = (int)(k % S);
+      if (k >= (unsigned)S && !mbar_wait(&empty[s], ((k / S) - 1) & 1u)) {
+        ok = false;
+        break;
+      }
+      const Tile tl = a.tiles[pt];
+      const int clen = min(C, tl.len - pc);
+      const int nb = clen & ~7;
+      unsigned char* base = smem + s * kStage;
+      if (nb > 0) {
+        mbar_arrive_expect_tx(&full[s], (uint32_t)nb * (12u + (uint32_t)sizeof(CT)));
+        const int64_t so = tl.shard + pc;
+        bulk_g2s(base, a.master + so, nb * 4, &full[s]);
+        bulk_g2s(base + C * 4, a.m + so, nb * 4, &full[s]);
+        bulk_g2s(base + C * 8, a.v + so, nb * 4, &full[s]);
+        bulk_g2s(base + C * 12, red_ptr(tl) + pc, nb * (int)sizeof(CT), &full[s]);
+      } else {
+        mbar_arrive(&full[s]);
+      }
+      ++k;
+      pc += C;
+      if (pc >= tl.len) {
+        pc = 0;
+        pt += gridDim.x;
+      }
+    }
+    if (!ok) {
+      atomicOr(a.error, kErrWaitTimeout);
+      for (unsigned j = k > (unsigned)S ? k - S : 0u; j < k; ++j) mbar_wait(&full[j % S], (j / S) & 1u);
+    }
+    return;
+  }
+
   const float gs = st->gscale, decay = st->decay, step = st->step_size;
   const float isb2 = st->inv_sqrt_bc2, eps = st->eps;
   const float b1 = st->beta1, omb1 = st->one_minus_beta1;
@@ -259,60 +324,16 @@ __global__ void __launch_bounds__(kThreads) k_adamw_cast_bulk(const __grid_const
     p = p - step * (m / denom);
   };
 
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < S; ++s) mbar_init(&full[s], 1);
-    mbar_init_fence();
-  }
-  __syncthreads();
-
-  auto red_ptr = [&](const Tile& tl) -> const CT* {
-    return a.stage == 1 ? static_cast<const CT*>(a.red.base[tl.rank]) + tl.flat
-                        : static_cast<const CT*>(a.red.base[0]) + tl.shard;
-  };
-
-  // Producer (thread 0): walks this block's chunk sequence S items ahead.
-  int pt = blockIdx.x, pc = 0;
-  unsigned issued = 0;
-  auto issue = [&](int s) {
-    if (pt >= a.n_tiles) return;
-    const Tile tl = a.tiles[pt];
-    const int clen = min(C, tl.len - pc);
-    const int nb = clen & ~7;
-    unsigned char* base = smem + s * kStage;
-    if (nb > 0) {
-      mbar_arrive_expect_tx(&full[s], (uint32_t)nb * (12u + (uint32_t)sizeof(CT)));
-      const int64_t so = tl.shard + pc;
-      bulk_g2s(base, a.master + so, nb * 4, &full[s]);
-      bulk_g2s(base + C * 4, a.m + so, nb * 4, &full[s]);
-      bulk_g2s(base + C * 8, a.v + so, nb * 4, &full[s]);
-      bulk_g2s(base + C * 12, red_ptr(tl) + pc, nb * (int)sizeof(CT), &full[s]);
-    } else {
-      mbar_arrive(&full[s]);
-    }
-    ++issued;
-    pc += C;
-    if (pc >= tl.len) {
-      pc = 0;
-      pt += gridDim.x;
-    }
-  };
-  if (threadIdx.x == 0)
-    for (int s = 0; s < S; ++s) issue(s);
-
-  // Consumers: every thread walks the same sequence.
   int ct = blockIdx.x, cc = 0;
   unsigned k = 0;
-  bool ok = true;
   while (ct < a.n_tiles) {
     const int s = (int)(k % S);
-    const uint32_t parity = (k / S) & 1u;
     const Tile tl = a.tiles[ct];
     const int clen = min(C, tl.len - cc);
     const int nb = clen & ~7;
-    const bool mine = mbar_wait(&full[s], parity);
-    if (!__syncthreads_and(mine)) {
-      ok = false;
-      break;
+    if (!__all_sync(0xffffffffu, mbar_wait(&full[s], (k / S) & 1u))) {
+      if (lane == 0) atomicOr(a.error, kErrWaitTimeout);
+      return;
     }
     const unsigned char* base = smem + s * kStage;
     const float* sp = reinterpret_cast<const float*>(base);
@@ -321,7 +342,9 @@ __global__ void __launch_bounds__(kThreads) k_adamw_cast_bulk(const __grid_const
     const CT* sr = reinterpret_cast<const CT*>(base + C * 12);
     const int64_t so = tl.shard + cc, fo = tl.flat + cc;
     PT* pp = static_cast<PT*>(a.params_flat) + fo;
-    for (int e = 4 * threadIdx.x; e < nb; e += 4 * kThreads) {
+    const int e_end = min(nb, (warp + 1) * kPerWarp);
+#pragma unroll 2
+    for (int e = warp * kPerWarp + 4 * lane; e < e_end; e += 128) {
       float4 p = *reinterpret_cast<const float4*>(sp + e);
       float4 m = *reinterpret_cast<const float4*>(sm + e);
       float4 v = *reinterpret_cast<const float4*>(sv + e);
@@ -338,9 +361,8 @@ __global__ void __launch_bounds__(kThreads) k_adamw_cast_bulk(const __grid_const
                  DT<PT>::from_f32(p.w)};
       __stcs(reinterpret_cast<uint2*>(pp + e), *reinterpret_cast<const uint2*>(q));
     }
-    const int tail = clen - nb;
-    if (threadIdx.x < tail) {
-      const int e = nb + threadIdx.x;
+    if (warp == 0 && lane < clen - nb) {
+      const int e = nb + lane;
       float p = a.master[so + e], m = a.m[so + e], v = a.v[so + e];
       adam(DT<CT>::to_f32(red_ptr(tl)[cc + e]), p, m, v);
       a.master[so + e] = p;
@@ -348,8 +370,8 @@ __global__ void __launch_bounds__(kThreads) k_adamw_cast_bulk(const __grid_const
       a.v[so + e] = v;
       pp[e] = DT<PT>::from_f32(p);
     }
-    __syncthreads();  // stage s is free again
-    if (threadIdx.x == 0) issue(s);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);
     ++k;
     cc += C;
     if (cc >= tl.len) {
@@ -357,19 +379,17 @@ __global__ void __launch_bounds__(kThreads) k_adamw_cast_bulk(const __grid_const
       ct += gridDim.x;
     }
   }
-  if (!ok && threadIdx.x == 0) {
-    atomicOr(a.error, kErrWaitTimeout);
-    for (unsigned j = k; j < issued; ++j) mbar_wait(&full[j % S], (j / S) & 1u);
-  }
 }
 
-constexpr int kUpdChunk = 2048;
-constexpr int kUpdStages = 3;
+constexpr int kWsChunk = 2048;
+constexpr int kWsStages = 4;
+constexpr int kWsConsumers = 8;
 
 template <typename CT, typename PT>
 static const void* update_kernel_cp(int variant) {
   if (variant == 1)
-    return reinterpret_cast<const void*>(&k_adamw_cast_bulk<CT, PT, kUpdChunk, kUpdStages>);
+    return reinterpret_cast<const void*>(
+        &k_adamw_cast_ws<CT, PT, kWsChunk, kWsStages, kWsConsumers>);
   return reinterpret_cast<const void*>(&k_adamw_cast<CT, PT>);
 }
 
@@ -392,16 +412,18 @@ static const void* update_kernel(int comm_dtype, int param_dtype, int variant) {
 }
 
 static int update_smem(int comm_dtype, int variant) {
-  if (variant != 1) return 0;
   const int cb = comm_dtype == kF32 ? 4 : 2;
-  return kUpdStages * kUpdChunk * (12 + cb);
+  return variant == 1 ? kWsStages * kWsChunk * (12 + cb) : 0;
 }
+
+static int update_threads(int variant) { return variant == 1 ? (kWsConsumers + 1) * 32 : kThreads; }
 
 cudaError_t launch_update(const UpdateArgs& a, int grid, int variant, cudaStream_t s) {
   const void* f = update_kernel(a.comm_dtype, a.param_dtype, variant);
   if (f == nullptr) return cudaErrorInvalidValue;
   void* args[] = {const_cast<UpdateArgs*>(&a)};
-  return cudaLaunchKernel(f, dim3(grid), dim3(kThreads), args, update_smem(a.comm_dtype, variant), s);
+  return cudaLaunchKernel(f, dim3(grid), dim3(update_threads(variant)), args,
+                          update_smem(a.comm_dtype, variant), s);
 }
 
 int update_blocks_per_sm(int comm_dtype, int param_dtype, int variant) {
@@ -412,7 +434,9 @@ int update_blocks_per_sm(int comm_dtype, int param_dtype, int variant) {
                       cudaSuccess)
     return 0;
   int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, f, kThreads, smem) != cudaSuccess) return 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, f, update_threads(variant), smem) !=
+      cudaSuccess)
+    return 0;
   return n;
 }
 

@@ -111,6 +111,12 @@ class ZeroStep:
             ar = [t.data_ptr() for t in outs]
         abi.zero_step(self.handle, [g.data_ptr() for g in grads], ar, hp.c(), _stream_handle(stream))
 
+    def step_per_tensor_launch(self, grads, hp: Hparams, stream=None) -> None:
+        """The same step launched tensor by tensor (the hook-style baseline)."""
+        ar = [t.data_ptr() for t in self.allreduce_out] if self.stage == 1 else None
+        abi.zero_step_per_tensor_launch(self.handle, [g.data_ptr() for g in grads], ar, hp.c(),
+                                        _stream_handle(stream))
+
     def step_tensors(self, grads_per_rank, hp: Hparams, stream=None) -> None:
         """grads_per_rank[w][p]: a tensor or None (all-zero gradient)."""
         ptrs = [(g.data_ptr() if g is not None else 0) for row in grads_per_rank for g in row]

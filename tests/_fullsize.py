@@ -18,7 +18,7 @@ import torch
 import oracle
 import workloads as wl
 from _parity import to_np
-from _util import rel_err, scaled_err, ulp_diff16
+from _util import params_close, rel_err, scaled_err
 from mixed_precision_gb300 import _abi as abi
 
 
@@ -155,5 +155,7 @@ class SampledOracle:
         assert worst <= rtol, worst
         p = to_np(z.params_flat[fl])
         exp = oracle.encode(self.master, z.param_dtype)
-        assert ulp_diff16(p, exp).max() <= 1
+        ok = params_close(p, exp, oracle.decode(exp, z.param_dtype), oracle.decode(p, z.param_dtype),
+                          rtol * self.hist[0].astype(np.float64), z.param_dtype == wl.BF16)
+        assert ok.all(), int((~ok).sum())
         return worst

@@ -29,3 +29,21 @@ def scaled_err(got: np.ndarray, ref: np.ndarray, prev: np.ndarray, tiny: float =
     scale = np.maximum(np.maximum(np.abs(ref), np.abs(prev.astype(np.float64))), tiny)
     d = np.abs(got - ref)
     return np.where(scale <= tiny, d, d / scale)
+
+
+def ulp16_at(bits: np.ndarray, dtype_is_bf16: bool) -> np.ndarray:
+    """Spacing of the 16-bit format at each value's magnitude (subnormal floor)."""
+    b = bits.astype(np.int64) & 0x7FFF
+    if dtype_is_bf16:
+        e = b >> 7
+        return np.ldexp(1.0, np.maximum(e, 1) - 127 - 7)
+    e = b >> 10
+    return np.ldexp(1.0, np.maximum(e, 1) - 15 - 10)
+
+
+def params_close(got_bits, ref_bits, ref_vals, got_vals, master_err_bound, dtype_is_bf16):
+    """Cast-out params agree within 1 ulp, or -- where the master itself sits
+    at a cancellation -- within 1 ulp plus the master's allowed error."""
+    ulp = ulp16_at(ref_bits, dtype_is_bf16)
+    diff = np.abs(got_vals.astype(np.float64) - ref_vals.astype(np.float64))
+    return (ulp_diff16(got_bits, ref_bits) <= 1) | (diff <= ulp + master_err_bound)

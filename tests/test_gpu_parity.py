@@ -106,6 +106,19 @@ def test_pointer_table_mode_matches_flat():
         assert np.array_equal(a, b)
 
 
+@pytest.mark.parametrize("stage", [1, 2])
+def test_per_tensor_launch_matches_oracle(stage):
+    """The tensor-by-tensor launch sequence (the hook-style baseline) computes
+    the same step: ragged tensors across several buckets and rank slices."""
+    rng = np.random.default_rng(stage)
+    shapes = [(int(x),) for x in rng.integers(1, 30000, size=25)] + [(0,), (70000,)]
+    pr = Pair(shapes, 4, stage, 100_000, wl.BF16, wl.BF16, init_scale=4.0, dynamic=True, index=110)
+    for step in range(3):
+        inj = [(0, pr.z.offsets[3], INF_BITS[wl.BF16])] if step == 1 else None
+        st, info, gc = pr.step(pr.grads(step, 1e-3, inject=inj), Hparams(), mode="per_tensor_launch")
+        pr.check(st, info, gc)
+
+
 def test_host_entry_point_matches_device():
     shapes = small_qwen_shapes()
     outs = []
