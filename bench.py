@@ -42,8 +42,8 @@ STATE_READ_BYTES = 144
 NCU_TRAFFIC_PER_ELEM = {
     # profiles/k_adamw_cast_ws_qwen3_layers8.md: (1.7628 + 1.7007) GB / 125,847,552 elements
     "k_adamw_cast": 27.52,
-    # the producer-warp reduce kernel has not been captured yet
-    "k_reduce_norm": None,
+    # profiles/k_reduce_norm_ws_qwen3_layers8.md: (504.0 + 205.4) MB / 125,847,552 elements
+    "k_reduce_norm": 5.637,
 }
 
 

@@ -321,6 +321,32 @@ int zero_reduce_norm_noalloc(const void* const* grads, int world, int64_t n, int
                              int comm_dtype, void* reduced_out, double* norm_sq_out,
                              int32_t* overflow_out, void* stream);
 
+/* Self-test of the bounded-wait path every pipelined kernel relies on. One
+ * block arms an mbarrier for 16 bytes that never arrive, waits on it with at
+ * most `spin_limit` retries (1..2^22), records the timeout in a device error
+ * word as the kernels do, and returns. Returns ZERO_ERR_TIMEOUT when the wait
+ * gave up (the expected outcome), ZERO_OK if it did not, ZERO_ERR_CUDA on a
+ * CUDA failure. Synchronises `stream`; the context stays usable. No
+ * counterpart on the pages: it tests failure detection without a GPU fault. */
+int zero_selftest_wait_timeout(uint32_t spin_limit, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Gradient accumulation into fp32 main-gradient buffers ([DO] "BF16 model   */
+/* parameters and FP32 main gradients"; [MD] "Initializing a DeepSpeed       */
+/* Engine": backward/step fire the reduction only on boundary micro-steps).  */
+/* ------------------------------------------------------------------------ */
+
+/* main[w][i] = (first ? 0 : main[w][i]) + fp32(micro[w][i]) for every real
+ * element i of the layout (padding untouched), for w = 0..W-1.
+ *   micro  host array of W device pointers, flat layout, layout's grad_dtype
+ *          or any ZERO_* dtype given by micro_dtype; read only.
+ *   main   host array of W device pointers, flat layout, fp32.
+ *   first  nonzero on the first micro-step of an accumulation window.
+ * The boundary step then runs zero_step on a layout whose grad_dtype is
+ * ZERO_F32 over `main`. Enqueued on `stream`. */
+int zero_accumulate(zero_layout_t* layout, const void* const* micro, int micro_dtype,
+                    float* const* main, int first, void* stream);
+
 /* Message for the last failing call on this thread ("" if none). The pointer
  * stays valid until the next failing call on this thread. */
 const char* zero_last_error(void);

@@ -100,6 +100,8 @@ def lib() -> ctypes.CDLL:
             "zero_layout_set_allocator": [P, ALLOC_FN, FREE_FN, P],
             "zero_set_step_events": [P, PP],
             "zero_reduce_norm_noalloc": [PP, I, I64, I, I, P, P, P, P],
+            "zero_selftest_wait_timeout": [ctypes.c_uint32, P],
+            "zero_accumulate": [P, PP, I, PP, I, P],
         }
         for name, args in sig.items():
             fn = getattr(L, name)
@@ -233,3 +235,12 @@ def zero_reduce_norm_noalloc(grads, n: int, grad_dtype: int, comm_dtype: int, re
     _check(lib().zero_reduce_norm_noalloc(_ptrs(grads), len(grads), n, grad_dtype, comm_dtype,
                                           reduced_out or None, norm_sq_out, overflow_out,
                                           stream or None))
+
+
+def zero_selftest_wait_timeout(spin_limit: int, stream: int) -> None:
+    _check(lib().zero_selftest_wait_timeout(spin_limit, stream or None))
+
+
+def zero_accumulate(layout: int, micro, micro_dtype: int, main, first: bool, stream: int) -> None:
+    _check(lib().zero_accumulate(layout, _ptrs(micro), micro_dtype, _ptrs(main), int(first),
+                                 stream or None))

@@ -674,6 +674,29 @@ int zero_step_host(zero_layout_t* L, const void* const* host_grads, void* const*
   return zero_step(L, dev_grads, allreduce_out, hp, stream);
 }
 
+int zero_accumulate(zero_layout_t* L, const void* const* micro, int micro_dtype, float* const* main,
+                    int first, void* stream) {
+  if (int rc = check_ready(L, false)) return rc;
+  if (micro == nullptr || main == nullptr) return fail(ZERO_ERR_INVALID, "micro/main is NULL");
+  if (!valid_dtype(micro_dtype)) return fail(ZERO_ERR_INVALID, "bad micro_dtype");
+  AccArgs a{};
+  for (int w = 0; w < L->world(); ++w) {
+    if (micro[w] == nullptr || main[w] == nullptr || !aligned16(micro[w]) || !aligned16(main[w]))
+      return fail(ZERO_ERR_INVALID, "micro[%d]/main[%d] NULL or not 16-byte aligned", w, w);
+    a.micro[w] = micro[w];
+    a.main[w] = main[w];
+  }
+  a.world = L->world();
+  a.micro_dtype = micro_dtype;
+  a.first = first ? 1 : 0;
+  a.tiles = L->d_tiles;
+  a.n_tiles = (int)L->tiles.size();
+  if (a.n_tiles == 0) return ZERO_OK;
+  cudaError_t e = launch_accumulate(a, L->grid_copy, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "accumulate kernel launch");
+  return ZERO_OK;
+}
+
 int zero_loss_scale_state(zero_layout_t* L, void* stream, zero_scaler_state* out) {
   if (int rc = check_ready(L, true)) return rc;
   if (out == nullptr) return fail(ZERO_ERR_INVALID, "out is NULL");

@@ -128,6 +128,17 @@ cudaError_t launch_init_from_flat(const Tile* tiles, int n_tiles, const float* m
 // dir 0: rank-major -> flat (export); 1: flat -> rank-major (import)
 cudaError_t launch_state_copy(const Tile* tiles, int n_tiles, float* shard_buf, float* flat_buf,
                               int dir, int grid, cudaStream_t s);
+struct AccArgs {
+  const void* micro[kMaxWorld];
+  float* main[kMaxWorld];
+  int world;
+  int micro_dtype;
+  int first;
+  const Tile* tiles;
+  int n_tiles;
+};
+cudaError_t launch_accumulate(const AccArgs& a, int grid, cudaStream_t s);
+
 // Record a failure message for zero_last_error() and return `code` (for entry
 // points defined outside api.cpp).
 int zero_internal_fail(int code, const char* msg);

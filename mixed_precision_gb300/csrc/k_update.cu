@@ -326,9 +326,10 @@ __global__ void __launch_bounds__((NC + 1) * 32)
 
   int ct = blockIdx.x, cc = 0;
   unsigned k = 0;
+  // The current tile's descriptor stays in registers for all its chunks.
+  Tile tl = a.tiles[ct < a.n_tiles ? ct : 0];
   while (ct < a.n_tiles) {
     const int s = (int)(k % S);
-    const Tile tl = a.tiles[ct];
     const int clen = min(C, tl.len - cc);
     const int nb = clen & ~7;
     if (!__all_sync(0xffffffffu, mbar_wait(&full[s], (k / S) & 1u))) {
@@ -377,6 +378,7 @@ __global__ void __launch_bounds__((NC + 1) * 32)
     if (cc >= tl.len) {
       cc = 0;
       ct += gridDim.x;
+      if (ct < a.n_tiles) tl = a.tiles[ct];
     }
   }
 }

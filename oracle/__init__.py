@@ -123,6 +123,7 @@ def lib() -> ctypes.CDLL:
         _lib.orc_overflow_sumsq.argtypes = [P, I32, I64, P, P, P]
         _lib.orc_finalize.argtypes = [D, I32, I32, P, P, P]
         _lib.orc_adamw.argtypes = [P, I32, I64, P, P, P, P, P]
+        _lib.orc_accumulate.argtypes = [P, I32, P, I64, P, I32]
         _lib.orc_ddp_step.argtypes = [I32, I64, I32, I32, I32, P, P, P, P, P, P, P, P]
         _lib.orc_ddp_step.restype = I32
         _lib.orc_zero_step.argtypes = [P, I32, I32, I32, I64, I32, I32, I32, P, P, P, P, P, P,
@@ -259,6 +260,14 @@ def adamw(reduced: np.ndarray, comm_dtype: int, hp: Hparams, info: Info, master:
     c_hp = hp._c()
     lib().orc_adamw(_ptr(reduced), comm_dtype, reduced.size, ctypes.byref(c_hp),
                     ctypes.byref(c_info), _ptr(master), _ptr(m), _ptr(v))
+
+
+def accumulate(micro: np.ndarray, micro_dtype: int, main: np.ndarray, first: bool,
+               real_mask: np.ndarray | None = None) -> None:
+    """In place: main = (first ? 0 : main) + fp32(micro) over real elements."""
+    micro = np.ascontiguousarray(micro)
+    lib().orc_accumulate(_ptr(micro), micro_dtype, _ptr(main), main.size,
+                         _ptr(real_mask) if real_mask is not None else None, int(first))
 
 
 # ---------------------------------------------------------------------------

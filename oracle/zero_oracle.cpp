@@ -299,6 +299,23 @@ void orc_adamw(const void* reduced, int comm_dtype, int64_t n, const orc_hparams
 }
 
 /* ------------------------------------------------------------------------ */
+/* Gradient accumulation into fp32 main gradients.                           */
+/* "Deep dive: Megatron", "Distributed optimizer": BF16 parameters with FP32 */
+/* main gradients (the 18-byte ledger). "3.7 ...", "Initializing a DeepSpeed */
+/* Engine": backward and step are accumulation-aware and reduce only on the  */
+/* boundary micro-step. Reading: main = (first ? +0 : main) + fp32(micro),   */
+/* one fp32 add per micro-step, in micro-step order; padding untouched.      */
+/* ------------------------------------------------------------------------ */
+void orc_accumulate(const void* micro, int micro_dtype, float* main_grad, int64_t n,
+                    const uint8_t* real_mask, int first) {
+  for (int64_t i = 0; i < n; ++i) {
+    if (real_mask != nullptr && !real_mask[i]) continue;
+    const float base = first ? 0.0f : main_grad[i];
+    main_grad[i] = base + load_f32(micro, i, micro_dtype);
+  }
+}
+
+/* ------------------------------------------------------------------------ */
 /* Unpartitioned (DDP) step over the whole model, no padding, no shards.     */
 /* "nanoMegatron", "What's in the box": DDP keeps the full model on every    */
 /* GPU and all-reduces gradients. Every rank then runs the same update, so   */

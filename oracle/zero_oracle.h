@@ -81,6 +81,10 @@ void orc_finalize(double norm_sq_raw, int32_t overflow, int world, const orc_hpa
 void orc_adamw(const void* reduced, int comm_dtype, int64_t n, const orc_hparams* hp,
                const orc_info* info, float* master, float* m, float* v);
 
+/* ---- gradient accumulation into fp32 main gradients ---- */
+void orc_accumulate(const void* micro, int micro_dtype, float* main_grad, int64_t n,
+                    const uint8_t* real_mask, int first);
+
 /* ---- composed steps ---- */
 int orc_ddp_step(int world, int64_t n, int grad_dtype, int comm_dtype, int param_dtype,
                  const void* const* grads, float* master, float* m, float* v, void* params,

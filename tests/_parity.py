@@ -81,9 +81,12 @@ class Pair:
             out[rank].view(torch.int16)[idx] = int(np.array(bits, np.uint16).view(np.int16))
         return out
 
-    def step(self, grads_cpu, hp: Hparams, mode: str = "flat"):
-        dev = [g.cuda() if g.numel() else torch.empty(8, dtype=g.dtype, device="cuda")
-               for g in grads_cpu]
+    def step(self, grads_cpu, hp: Hparams, mode: str = "flat", dev=None):
+        """One step on both sides. `dev`: the GPU side's own device gradients
+        (default: grads_cpu uploaded)."""
+        if dev is None:
+            dev = [g.cuda() if g.numel() else torch.empty(8, dtype=g.dtype, device="cuda")
+                   for g in grads_cpu]
         if mode == "flat":
             self.z.step(dev, hp)
         elif mode == "tensors":

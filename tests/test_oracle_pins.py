@@ -530,3 +530,32 @@ def test_overflow_anywhere_skips_step(orc):
                          np.zeros_like(ms), np.zeros_like(ms), np.zeros(L.np_total, np.uint16),
                          orc.Hparams(), orc.Scaler())
     assert info.overflow == 0
+
+
+# ---------------------------------------------------------------------------
+# Gradient accumulation (the step before the reduce)
+# ---------------------------------------------------------------------------
+
+def test_accumulate_exact_and_ordered(orc):
+    """Integer micro-gradients sum exactly; `first` restarts the window; the
+    fp32 adds run in micro-step order (1 + 2^-24 + 2^-24 stays 1)."""
+    main = np.full(4, 123.0, np.float32)
+    steps = [np.array([1, -2, 3, 2.0 ** -24], np.float32), np.array([4, 5, -6, 2.0 ** -24], np.float32),
+             np.array([-7, 8, 9, 0], np.float32)]
+    orc.accumulate(orc.encode(steps[0], wl.BF16), wl.BF16, main, first=True)
+    orc.accumulate(steps[1], wl.F32, main, first=False)
+    orc.accumulate(steps[2], wl.F32, main, first=False)
+    assert main[:3].tolist() == [-2.0, 11.0, 6.0]
+    assert main[3] == np.float32(2.0 ** -24 + 2.0 ** -24)  # bf16 keeps 2^-24 exactly
+    m2 = np.array([1.0], np.float32)
+    orc.accumulate(np.array([2.0 ** -24], np.float32), wl.F32, m2, first=False)
+    orc.accumulate(np.array([2.0 ** -24], np.float32), wl.F32, m2, first=False)
+    assert m2[0] == 1.0
+
+
+def test_accumulate_first_and_padding(orc):
+    main = np.array([5.0, 7.0, 9.0], np.float32)
+    mask = np.array([1, 0, 1], np.uint8)
+    orc.accumulate(np.array([-0.0, 1.0, 2.0], np.float32), wl.F32, main, first=True, real_mask=mask)
+    assert main.tolist() == [0.0, 7.0, 2.0]
+    assert not np.signbit(main[0])  # +0 + -0 is +0
