@@ -61,6 +61,7 @@ def parse_args(argv=None):
                     help="target CPU time of the oracle sample")
     ap.add_argument("--world", type=int, default=None, help="override the simulated world size")
     ap.add_argument("--bucket-bytes", type=int, default=None, help="override the bucket size")
+    ap.add_argument("--stage", type=int, default=None, help="override the ZeRO stage (1, 2, 3)")
     ap.add_argument("--per-tensor-launch", action="store_true",
                     help="launch the step tensor by tensor (the hook-style baseline)")
     ap.add_argument("--tensors", action="store_true",
@@ -198,6 +199,8 @@ def workload_of(args):
         over["world"] = args.world
     if getattr(args, "bucket_bytes", None):
         over["bucket_bytes"] = args.bucket_bytes
+    if getattr(args, "stage", None):
+        over["stage"] = args.stage
     return wl.workload(args.workload, **over)
 
 

@@ -69,11 +69,15 @@ typedef enum { ZERO_F32 = 0, ZERO_F16 = 1, ZERO_BF16 = 2 } zero_dtype;
 
 typedef struct zero_layout zero_layout_t; /* opaque, host-owned */
 
-/* Layout configuration. [ND] stages 1/2; [MD] bucket sizes in bytes.
+/* Layout configuration. [ND] stages 1/2; [MD] bucket sizes in bytes; [MD]
+ * "ZeRO Stages Recap" and [NM] "What's in the box" for stage 3.
  *   world        W simulated data-parallel ranks, 1..ZERO_MAX_WORLD.
  *   stage        1: every rank receives the whole reduced gradient (all-reduce)
  *                   and updates only its optimizer shard (ZeRO-1);
- *                2: every rank receives only its reduced shard (ZeRO-2).
+ *                2: every rank receives only its reduced shard (ZeRO-2);
+ *                3: as 2, and the low-precision parameters stay sharded too:
+ *                   the bound params buffer is RANK-MAJOR like master/m/v,
+ *                   and zero_gather_bucket all-gathers a bucket before use.
  *   bucket_bytes bucket capacity in bytes of gradient dtype (> 0).
  *   grad_dtype   dtype of the W input gradient buffers.
  *   param_dtype  dtype of the cast-out parameters (ZERO_F16 or ZERO_BF16).
@@ -104,7 +108,8 @@ typedef struct {
   int64_t allreduce_bytes; /* stage 1: bytes of ONE rank's all-reduce output; stage 2: 0 */
   int64_t device_bytes_owned; /* device bytes the library allocates at bind */
   double ledger_bytes_per_param; /* [DO] per-rank persistent bytes per parameter:
-                                    stage 1: P + G + 12/W; stage 2: P + G/W + 12/W
+                                    stage 1: P + G + 12/W; stage 2: P + G/W + 12/W;
+                                    stage 3: (P + G + 12)/W
                                     (P, G = param and grad dtype sizes) */
   double step_bytes_per_elem;    /* roofline bytes per real element of one step:
                                     2W grad reads + 24 master/m/v + P param write */
@@ -198,8 +203,9 @@ int zero_shard_range(const zero_layout_t* layout, int bucket, int rank, int64_t*
  *   master, m, v  fp32, Np elements each, RANK-MAJOR: rank r's shard is
  *                 [r*Np/W, (r+1)*Np/W), holding its slice of bucket 0, then
  *                 bucket 1, ... (zero_shard_range gives each slice).
- *   params_flat   param_dtype, Np elements, flat layout (the gathered view).
- *   scratch       stage 2: comm_dtype, Np elements, rank-major (each rank's
+ *   params_flat   param_dtype, Np elements, flat layout (the gathered view);
+ *                 stage 3: rank-major parameter shards instead.
+ *   scratch       stages 2/3: comm_dtype, Np elements, rank-major (each rank's
  *                 reduce-scatter output); stage 1: ignored (may be NULL).
  * Rebinding replaces the pointers (and reuses the device block). Synchronous. */
 int zero_state_bind(zero_layout_t* layout, void* master, void* m, void* v, void* params_flat,
@@ -276,6 +282,14 @@ int zero_loss_scale_state(zero_layout_t* layout, void* stream, zero_scaler_state
  *        param_dtype). Enqueued on `stream`. */
 int zero_gather_params(zero_layout_t* layout, void* const* dst, int n_replicas, void* stream);
 
+/* Stage 3: all-gather bucket `bucket` of the sharded parameters into `dst`,
+ * a device buffer in the FLAT layout (Np elements of param_dtype, or at least
+ * up to the bucket's end); only that bucket's real elements are written.
+ * Enqueued on `stream` -- issue the next bucket's gather on a second stream
+ * to prefetch it while the current one is in use. ZERO_ERR_STATE for stages
+ * 1/2 (their parameters are always gathered). */
+int zero_gather_bucket(zero_layout_t* layout, int bucket, void* dst, void* stream);
+
 /* Copy the rank-major fp32 state out to / in from flat-layout device buffers
  * (Np elements each; padding of the flat buffers is written as 0 on export
  * and ignored on import). Any of the three pointers may be NULL to skip it.
@@ -346,6 +360,32 @@ int zero_selftest_wait_timeout(uint32_t spin_limit, void* stream);
  * ZERO_F32 over `main`. Enqueued on `stream`. */
 int zero_accumulate(zero_layout_t* layout, const void* const* micro, int micro_dtype,
                     float* const* main, int first, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Checkpoints that survive a change of W or bucket size (leetllm "Deep     */
+/* dive: Megatron", "Checkpoints, resharding, and recovery": optimizer      */
+/* moments and iteration counters are saved; a parameter-shaped             */
+/* representation (fully_reshardable) permits resharding).                  */
+/* ------------------------------------------------------------------------ */
+
+/* fp32 master/m/v in PARAMETER-MAJOR order: parameter 0's elements, then
+ * parameter 1's, ... (n_real elements, no padding), independent of W, stage
+ * and bucket size. Any pointer may be NULL to skip that buffer. Device
+ * pointers, 16-byte aligned. Enqueued on `stream`. */
+int zero_state_export_params(zero_layout_t* layout, float* master_pm, float* m_pm, float* v_pm,
+                             void* stream);
+
+/* The inverse: loads master/m/v from parameter-major buffers into this
+ * layout's rank-major shards (any W, stage or bucket size over the same
+ * parameter list) and recasts the flat parameters from the loaded master. A
+ * NULL m_pm / v_pm leaves that state untouched. Enqueued on `stream`. */
+int zero_state_import_params(zero_layout_t* layout, const float* master_pm, const float* m_pm,
+                             const float* v_pm, void* stream);
+
+/* Restore the scaler's scale, clean-step counter and Adam step t (from a
+ * saved zero_scaler_state); the other fields of `st` are ignored. Enqueued
+ * on `stream`. */
+int zero_scaler_restore(zero_layout_t* layout, const zero_scaler_state* st, void* stream);
 
 /* Message for the last failing call on this thread ("" if none). The pointer
  * stays valid until the next failing call on this thread. */

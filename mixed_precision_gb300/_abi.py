@@ -102,6 +102,10 @@ def lib() -> ctypes.CDLL:
             "zero_reduce_norm_noalloc": [PP, I, I64, I, I, P, P, P, P],
             "zero_selftest_wait_timeout": [ctypes.c_uint32, P],
             "zero_accumulate": [P, PP, I, PP, I, P],
+            "zero_state_export_params": [P, P, P, P, P],
+            "zero_state_import_params": [P, P, P, P, P],
+            "zero_scaler_restore": [P, ctypes.POINTER(zero_scaler_state), P],
+            "zero_gather_bucket": [P, I, P, P],
         }
         for name, args in sig.items():
             fn = getattr(L, name)
@@ -244,3 +248,21 @@ def zero_selftest_wait_timeout(spin_limit: int, stream: int) -> None:
 def zero_accumulate(layout: int, micro, micro_dtype: int, main, first: bool, stream: int) -> None:
     _check(lib().zero_accumulate(layout, _ptrs(micro), micro_dtype, _ptrs(main), int(first),
                                  stream or None))
+
+
+def zero_state_export_params(layout: int, master_pm: int, m_pm: int, v_pm: int, stream: int) -> None:
+    _check(lib().zero_state_export_params(layout, master_pm or None, m_pm or None, v_pm or None,
+                                          stream or None))
+
+
+def zero_state_import_params(layout: int, master_pm: int, m_pm: int, v_pm: int, stream: int) -> None:
+    _check(lib().zero_state_import_params(layout, master_pm or None, m_pm or None, v_pm or None,
+                                          stream or None))
+
+
+def zero_scaler_restore(layout: int, st: zero_scaler_state, stream: int) -> None:
+    _check(lib().zero_scaler_restore(layout, ctypes.byref(st), stream or None))
+
+
+def zero_gather_bucket(layout: int, bucket: int, dst: int, stream: int) -> None:
+    _check(lib().zero_gather_bucket(layout, bucket, dst, stream or None))

@@ -71,6 +71,7 @@ struct zero_layout {
   std::vector<Tile> tiles;
   // the same tiles grouped by parameter (per-tensor launches): parameter p's
   // tiles are tiles_pt[pt_begin[p] .. pt_begin[p+1])
+  std::vector<int> bucket_tile_begin;  // bucket b's tiles: [begin[b], begin[b+1])
   std::vector<Tile> tiles_pt;
   std::vector<int> pt_begin;
   int64_t pt_partials = 0;  // sum over parameters of min(tiles, kMaxPerTensorGrid)
@@ -98,6 +99,7 @@ struct zero_layout {
   DevState* d_state = nullptr;
   const void** d_table = nullptr;  // W * n_params grad pointers (table mode)
   Tile* d_tiles_pt = nullptr;
+  int64_t* d_pm_delta = nullptr;  // per parameter: parameter-major start - flat offset
   double* d_part_pt = nullptr;
   unsigned* d_ovf_pt = nullptr;
   void* d_gather = nullptr;        // replica pointer table for K4 (grown on demand)
@@ -169,6 +171,7 @@ void build_layout(zero_layout* L) {
   int64_t shard_prefix = 0;  // sum of len/W over the buckets before b
   int p_lo = 0;
   for (size_t b = 0; b < L->bstart.size(); ++b) {
+    L->bucket_tile_begin.push_back((int)L->tiles.size());
     const int64_t slice = L->blen[b] / W;
     int p_hi = p_lo;
     while (p_hi < P && L->bucket_of[p_hi] == (int)b) ++p_hi;
@@ -194,6 +197,7 @@ void build_layout(zero_layout* L) {
     p_lo = p_hi;
   }
 
+  L->bucket_tile_begin.push_back((int)L->tiles.size());
   L->tiles_pt = L->tiles;
   std::stable_sort(L->tiles_pt.begin(), L->tiles_pt.end(),
                    [](const Tile& a, const Tile& b) { return a.param < b.param; });
@@ -207,7 +211,7 @@ void build_layout(zero_layout* L) {
 
 // Sizes of the library's device block, in allocation order.
 struct BlockPlan {
-  size_t tiles, part, ovf, state, table, tiles_pt, part_pt, ovf_pt, total;
+  size_t tiles, part, ovf, state, table, tiles_pt, part_pt, ovf_pt, pm_delta, total;
 };
 
 BlockPlan plan_block(const zero_layout* L) {
@@ -220,7 +224,9 @@ BlockPlan plan_block(const zero_layout* L) {
   b.tiles_pt = b.tiles;
   b.part_pt = align_up(std::max<int64_t>(1, L->pt_partials) * sizeof(double), 256);
   b.ovf_pt = align_up(std::max<int64_t>(1, L->pt_partials) * sizeof(unsigned), 256);
-  b.total = b.tiles + b.part + b.ovf + b.state + b.table + b.tiles_pt + b.part_pt + b.ovf_pt;
+  b.pm_delta = align_up((int64_t)L->numel.size() * sizeof(int64_t), 256);
+  b.total = b.tiles + b.part + b.ovf + b.state + b.table + b.tiles_pt + b.part_pt + b.ovf_pt +
+            b.pm_delta;
   return b;
 }
 
@@ -353,8 +359,8 @@ int check_hparams(const zero_hparams* hp) {
 }
 
 int check_allreduce(const zero_layout* L, void* const* allreduce_out) {
-  if (L->cfg.stage == 2) {
-    if (allreduce_out != nullptr) return fail(ZERO_ERR_INVALID, "stage 2 takes no allreduce_out");
+  if (L->cfg.stage != 1) {
+    if (allreduce_out != nullptr) return fail(ZERO_ERR_INVALID, "stages 2/3 take no allreduce_out");
     return ZERO_OK;
   }
   if (allreduce_out == nullptr) return fail(ZERO_ERR_INVALID, "stage 1 needs allreduce_out");
@@ -393,7 +399,7 @@ int zero_layout_create(const int64_t* const* shapes, const int* ndims, int n_par
   if (shapes == nullptr || ndims == nullptr) return fail(ZERO_ERR_INVALID, "shapes/ndims NULL");
   if (cfg->world < 1 || cfg->world > ZERO_MAX_WORLD)
     return fail(ZERO_ERR_INVALID, "world %d outside 1..%d", cfg->world, ZERO_MAX_WORLD);
-  if (cfg->stage != 1 && cfg->stage != 2) return fail(ZERO_ERR_INVALID, "stage must be 1 or 2");
+  if (cfg->stage < 1 || cfg->stage > 3) return fail(ZERO_ERR_INVALID, "stage must be 1, 2 or 3");
   if (cfg->bucket_bytes <= 0) return fail(ZERO_ERR_INVALID, "bucket_bytes must be positive");
   if (!valid_dtype(cfg->grad_dtype)) return fail(ZERO_ERR_INVALID, "bad grad_dtype");
   if (cfg->param_dtype != ZERO_F16 && cfg->param_dtype != ZERO_BF16)
@@ -470,10 +476,12 @@ int zero_layout_query(const zero_layout_t* L, zero_layout_info* o) {
   o->grad_bytes = L->np * (int64_t)G;
   o->state_bytes = L->np * 4;
   o->params_bytes = L->np * (int64_t)P;
-  o->scratch_bytes = L->cfg.stage == 2 ? L->np * C : 0;
+  o->scratch_bytes = L->cfg.stage != 1 ? L->np * C : 0;
   o->allreduce_bytes = L->cfg.stage == 1 ? L->np * C : 0;
   o->device_bytes_owned = (int64_t)plan_block(L).total;
-  o->ledger_bytes_per_param = L->cfg.stage == 1 ? P + G + 12.0 / W : P + G / W + 12.0 / W;
+  o->ledger_bytes_per_param = L->cfg.stage == 1   ? P + G + 12.0 / W
+                              : L->cfg.stage == 2 ? P + G / W + 12.0 / W
+                                                  : (P + G + 12.0) / W;
   o->step_bytes_per_elem = W * G + 24.0 + P;
   return ZERO_OK;
 }
@@ -518,8 +526,8 @@ int zero_state_bind(zero_layout_t* L, void* master, void* m, void* v, void* para
     return fail(ZERO_ERR_INVALID, "master/m/v/params_flat must not be NULL");
   if (!aligned16(master) || !aligned16(m) || !aligned16(v) || !aligned16(params_flat))
     return fail(ZERO_ERR_INVALID, "state buffers must be 16-byte aligned");
-  if (L->cfg.stage == 2 && (scratch == nullptr || !aligned16(scratch)))
-    return fail(ZERO_ERR_INVALID, "stage 2 needs a 16-byte aligned scratch buffer");
+  if (L->cfg.stage != 1 && (scratch == nullptr || !aligned16(scratch)))
+    return fail(ZERO_ERR_INVALID, "stages 2/3 need a 16-byte aligned scratch buffer");
 
   if (L->dblock == nullptr) {
     const BlockPlan b = plan_block(L);
@@ -543,6 +551,19 @@ int zero_state_bind(zero_layout_t* L, void* master, void* m, void* v, void* para
     L->d_part_pt = reinterpret_cast<double*>(c);
     c += b.part_pt;
     L->d_ovf_pt = reinterpret_cast<unsigned*>(c);
+    c += b.ovf_pt;
+    L->d_pm_delta = reinterpret_cast<int64_t*>(c);
+    {
+      std::vector<int64_t> delta(L->n_params());
+      int64_t pm = 0;
+      for (int p = 0; p < L->n_params(); ++p) {
+        delta[p] = pm - L->offset[p];
+        pm += L->numel[p];
+      }
+      cudaError_t e = cudaMemcpy(L->d_pm_delta, delta.data(), delta.size() * sizeof(int64_t),
+                                 cudaMemcpyHostToDevice);
+      if (e != cudaSuccess) return cuda_fail(e, "upload of the parameter-major offsets");
+    }
     if (!L->tiles.empty()) {
       cudaError_t e = cudaMemcpy(L->d_tiles, L->tiles.data(), L->tiles.size() * sizeof(Tile),
                                  cudaMemcpyHostToDevice);
@@ -597,7 +618,7 @@ int zero_state_init(zero_layout_t* L, const float* master_init_flat, const zero_
   if (e != cudaSuccess) return cuda_fail(e, "state init launch");
   if (!L->tiles.empty()) {
     e = launch_init_from_flat(L->d_tiles, (int)L->tiles.size(), master_init_flat, L->master,
-                              L->params, L->cfg.param_dtype, L->grid_copy, s);
+                              L->params, L->cfg.param_dtype, L->cfg.stage == 3, L->grid_copy, s);
     if (e != cudaSuccess) return cuda_fail(e, "init kernel launch");
   }
   L->initialized = true;
@@ -741,8 +762,22 @@ int zero_gather_params(zero_layout_t* L, void* const* dst, int n_replicas, void*
   if (L->tiles.empty()) return ZERO_OK;
   cudaError_t e = launch_gather(L->d_tiles, (int)L->tiles.size(), L->params,
                                 static_cast<void* const*>(L->d_gather), L->n_params(), n_replicas,
-                                dtype_bytes(L->cfg.param_dtype), L->grid_copy, s);
+                                dtype_bytes(L->cfg.param_dtype), L->cfg.stage == 3, L->grid_copy, s);
   if (e != cudaSuccess) return cuda_fail(e, "gather kernel launch");
+  return ZERO_OK;
+}
+
+int zero_gather_bucket(zero_layout_t* L, int bucket, void* dst, void* stream) {
+  if (int rc = check_ready(L, true)) return rc;
+  if (L->cfg.stage != 3)
+    return fail(ZERO_ERR_STATE, "zero_gather_bucket is for stage 3 (parameters sharded)");
+  if (bucket < 0 || bucket >= (int)L->bstart.size()) return fail(ZERO_ERR_INVALID, "bucket out of range");
+  if (dst == nullptr || !aligned16(dst)) return fail(ZERO_ERR_INVALID, "dst NULL or not 16-byte aligned");
+  const int t0 = L->bucket_tile_begin[bucket], t1 = L->bucket_tile_begin[bucket + 1];
+  if (t1 == t0) return ZERO_OK;
+  cudaError_t e = launch_gather_bucket(L->d_tiles + t0, t1 - t0, L->params, dst,
+                                       std::min(t1 - t0, L->grid_copy), static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "bucket gather launch");
   return ZERO_OK;
 }
 
@@ -759,6 +794,51 @@ static int state_copy(zero_layout_t* L, float* a, float* b, float* c, int dir, v
                                       L->grid_copy, s);
     if (e != cudaSuccess) return cuda_fail(e, "state copy launch");
   }
+  return ZERO_OK;
+}
+
+static int state_pm_copy(zero_layout_t* L, float* a, float* b, float* c, int dir, void* stream) {
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  float* pm[3] = {a, b, c};
+  float* shard[3] = {L->master, L->m, L->v};
+  for (int k = 0; k < 3; ++k) {
+    if (pm[k] == nullptr || L->tiles.empty()) continue;
+    if (!aligned16(pm[k])) return fail(ZERO_ERR_INVALID, "state buffer not 16-byte aligned");
+    cudaError_t e = launch_state_pm(L->d_tiles, (int)L->tiles.size(), L->d_pm_delta, shard[k], pm[k],
+                                    dir, L->grid_copy, s);
+    if (e != cudaSuccess) return cuda_fail(e, "state copy launch");
+  }
+  return ZERO_OK;
+}
+
+int zero_state_export_params(zero_layout_t* L, float* master_pm, float* m_pm, float* v_pm,
+                             void* stream) {
+  if (int rc = check_ready(L, true)) return rc;
+  return state_pm_copy(L, master_pm, m_pm, v_pm, 0, stream);
+}
+
+int zero_state_import_params(zero_layout_t* L, const float* master_pm, const float* m_pm,
+                             const float* v_pm, void* stream) {
+  if (int rc = check_ready(L, true)) return rc;
+  if (master_pm == nullptr) return fail(ZERO_ERR_INVALID, "master_pm is required");
+  if (int rc = state_pm_copy(L, const_cast<float*>(master_pm), const_cast<float*>(m_pm),
+                             const_cast<float*>(v_pm), 1, stream))
+    return rc;
+  if (L->tiles.empty()) return ZERO_OK;
+  cudaError_t e = launch_recast(L->d_tiles, (int)L->tiles.size(), L->master, L->params,
+                                L->cfg.param_dtype, L->cfg.stage == 3, L->grid_copy,
+                                static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "recast launch");
+  return ZERO_OK;
+}
+
+int zero_scaler_restore(zero_layout_t* L, const zero_scaler_state* st, void* stream) {
+  if (int rc = check_ready(L, true)) return rc;
+  if (st == nullptr || !(st->scale > 0.0) || st->counter < 0 || st->t < 0)
+    return fail(ZERO_ERR_INVALID, "scaler state NULL or out of range");
+  cudaError_t e = launch_scaler_restore(L->d_state, st->scale, st->counter, st->t,
+                                        static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "scaler restore launch");
   return ZERO_OK;
 }
 

@@ -123,8 +123,8 @@ cudaError_t launch_update(const UpdateArgs& a, int grid, int variant, cudaStream
 int update_blocks_per_sm(int comm_dtype, int param_dtype, int variant);
 cudaError_t launch_state_init(const ScalerCfg& cfg, DevState* st, cudaStream_t s);
 cudaError_t launch_init_from_flat(const Tile* tiles, int n_tiles, const float* master_flat,
-                                  float* master, void* params_flat, int param_dtype, int grid,
-                                  cudaStream_t s);
+                                  float* master, void* params_flat, int param_dtype,
+                                  int params_by_shard, int grid, cudaStream_t s);
 // dir 0: rank-major -> flat (export); 1: flat -> rank-major (import)
 cudaError_t launch_state_copy(const Tile* tiles, int n_tiles, float* shard_buf, float* flat_buf,
                               int dir, int grid, cudaStream_t s);
@@ -143,8 +143,16 @@ cudaError_t launch_accumulate(const AccArgs& a, int grid, cudaStream_t s);
 // points defined outside api.cpp).
 int zero_internal_fail(int code, const char* msg);
 
+cudaError_t launch_state_pm(const Tile* tiles, int n_tiles, const int64_t* pm_delta, float* shard_buf,
+                            float* pm_buf, int dir, int grid, cudaStream_t s);
+cudaError_t launch_recast(const Tile* tiles, int n_tiles, const float* master, void* params,
+                          int param_dtype, int params_by_shard, int grid, cudaStream_t s);
+cudaError_t launch_gather_bucket(const Tile* tiles, int n_tiles, const void* shards, void* dst,
+                                 int grid, cudaStream_t s);
+cudaError_t launch_scaler_restore(DevState* st, double scale, long long counter, long long t,
+                                  cudaStream_t s);
 cudaError_t launch_gather(const Tile* tiles, int n_tiles, const void* params_flat,
                           void* const* dst_table, int n_params, int n_replicas, int elem_bytes,
-                          int grid, cudaStream_t s);
+                          int src_by_shard, int grid, cudaStream_t s);
 
 }  // namespace zg

@@ -11,26 +11,29 @@ namespace zg {
 template <typename PT>
 __global__ void __launch_bounds__(kThreads)
     k_init_from_flat(const Tile* __restrict__ tiles, int n_tiles, const float* __restrict__ init,
-                     float* __restrict__ master, PT* __restrict__ params) {
+                     float* __restrict__ master, PT* __restrict__ params, int params_by_shard) {
   for (int t = blockIdx.x; t < n_tiles; t += gridDim.x) {
     const Tile tl = tiles[t];
+    PT* pp = params + (params_by_shard ? tl.shard : tl.flat);
     for (int i = threadIdx.x; i < tl.len; i += kThreads) {
       const float x = init[tl.flat + i];
       master[tl.shard + i] = x;
-      params[tl.flat + i] = DT<PT>::from_f32(x);
+      pp[i] = DT<PT>::from_f32(x);
     }
   }
 }
 
 cudaError_t launch_init_from_flat(const Tile* tiles, int n_tiles, const float* master_flat,
-                                  float* master, void* params_flat, int param_dtype, int grid,
-                                  cudaStream_t s) {
+                                  float* master, void* params_flat, int param_dtype,
+                                  int params_by_shard, int grid, cudaStream_t s) {
   if (param_dtype == kF16)
     k_init_from_flat<__half><<<grid, kThreads, 0, s>>>(tiles, n_tiles, master_flat, master,
-                                                       static_cast<__half*>(params_flat));
+                                                       static_cast<__half*>(params_flat),
+                                                       params_by_shard);
   else
     k_init_from_flat<__nv_bfloat16><<<grid, kThreads, 0, s>>>(
-        tiles, n_tiles, master_flat, master, static_cast<__nv_bfloat16*>(params_flat));
+        tiles, n_tiles, master_flat, master, static_cast<__nv_bfloat16*>(params_flat),
+        params_by_shard);
   return cudaGetLastError();
 }
 
@@ -59,10 +62,10 @@ cudaError_t launch_state_copy(const Tile* tiles, int n_tiles, float* shard_buf, 
 // starts are 64-element aligned inside a parameter), element copies otherwise.
 __global__ void __launch_bounds__(kThreads)
     k_gather(const Tile* __restrict__ tiles, int n_tiles, const uint16_t* __restrict__ src,
-             void* const* __restrict__ dst_table, int n_params, int n_replicas) {
+             void* const* __restrict__ dst_table, int n_params, int n_replicas, int src_by_shard) {
   for (int t = blockIdx.x; t < n_tiles; t += gridDim.x) {
     const Tile tl = tiles[t];
-    const uint16_t* s = src + tl.flat;
+    const uint16_t* s = src + (src_by_shard ? tl.shard : tl.flat);
     for (int k = 0; k < n_replicas; ++k) {
       uint16_t* d = static_cast<uint16_t*>(dst_table[(int64_t)k * n_params + tl.param]) + tl.in_param;
       const bool vec = (reinterpret_cast<uintptr_t>(d) & 15u) == 0;
@@ -76,10 +79,95 @@ __global__ void __launch_bounds__(kThreads)
 
 cudaError_t launch_gather(const Tile* tiles, int n_tiles, const void* params_flat,
                           void* const* dst_table, int n_params, int n_replicas, int elem_bytes,
-                          int grid, cudaStream_t s) {
+                          int src_by_shard, int grid, cudaStream_t s) {
   if (elem_bytes != 2) return cudaErrorInvalidValue;
   k_gather<<<grid, kThreads, 0, s>>>(tiles, n_tiles, static_cast<const uint16_t*>(params_flat),
-                                     dst_table, n_params, n_replicas);
+                                     dst_table, n_params, n_replicas, src_by_shard);
+  return cudaGetLastError();
+}
+
+}  // namespace zg
+
+namespace zg {
+
+// Rank-major shard state <-> parameter-major buffers: element i of a tile is
+// parameter-major index pm_delta[param] + flat + i (pm_delta = the parameter's
+// parameter-major start minus its flat offset). dir 0: export, 1: import.
+__global__ void __launch_bounds__(kThreads)
+    k_state_pm(const Tile* __restrict__ tiles, int n_tiles, const int64_t* __restrict__ pm_delta,
+               float* __restrict__ shard_buf, float* __restrict__ pm_buf, int dir) {
+  for (int t = blockIdx.x; t < n_tiles; t += gridDim.x) {
+    const Tile tl = tiles[t];
+    const int64_t pm0 = pm_delta[tl.param] + tl.flat;
+    for (int i = threadIdx.x; i < tl.len; i += kThreads) {
+      if (dir == 0)
+        pm_buf[pm0 + i] = shard_buf[tl.shard + i];
+      else
+        shard_buf[tl.shard + i] = pm_buf[pm0 + i];
+    }
+  }
+}
+
+cudaError_t launch_state_pm(const Tile* tiles, int n_tiles, const int64_t* pm_delta, float* shard_buf,
+                            float* pm_buf, int dir, int grid, cudaStream_t s) {
+  k_state_pm<<<grid, kThreads, 0, s>>>(tiles, n_tiles, pm_delta, shard_buf, pm_buf, dir);
+  return cudaGetLastError();
+}
+
+// params_flat[flat + i] = RNE(master[shard + i]) over every tile.
+template <typename PT>
+__global__ void __launch_bounds__(kThreads)
+    k_recast(const Tile* __restrict__ tiles, int n_tiles, const float* __restrict__ master,
+             PT* __restrict__ params, int params_by_shard) {
+  for (int t = blockIdx.x; t < n_tiles; t += gridDim.x) {
+    const Tile tl = tiles[t];
+    PT* pp = params + (params_by_shard ? tl.shard : tl.flat);
+    for (int i = threadIdx.x; i < tl.len; i += kThreads) pp[i] = DT<PT>::from_f32(master[tl.shard + i]);
+  }
+}
+
+cudaError_t launch_recast(const Tile* tiles, int n_tiles, const float* master, void* params,
+                          int param_dtype, int params_by_shard, int grid, cudaStream_t s) {
+  if (param_dtype == kF16)
+    k_recast<__half><<<grid, kThreads, 0, s>>>(tiles, n_tiles, master, static_cast<__half*>(params),
+                                               params_by_shard);
+  else
+    k_recast<__nv_bfloat16><<<grid, kThreads, 0, s>>>(
+        tiles, n_tiles, master, static_cast<__nv_bfloat16*>(params), params_by_shard);
+  return cudaGetLastError();
+}
+
+// ZeRO-3 all-gather of one bucket: dst[flat + i] <- shards[shard + i] over the
+// bucket's tiles (2-byte parameters; 16-byte vectors, then the ragged tail).
+__global__ void __launch_bounds__(kThreads)
+    k_gather_bucket(const Tile* __restrict__ tiles, int n_tiles, const uint16_t* __restrict__ shards,
+                    uint16_t* __restrict__ dst) {
+  for (int t = blockIdx.x; t < n_tiles; t += gridDim.x) {
+    const Tile tl = tiles[t];
+    const int nvec = tl.len >> 3;
+    const uint4* s4 = reinterpret_cast<const uint4*>(shards + tl.shard);
+    uint4* d4 = reinterpret_cast<uint4*>(dst + tl.flat);
+    for (int v = threadIdx.x; v < nvec; v += kThreads) d4[v] = __ldcs(s4 + v);
+    for (int i = nvec * 8 + threadIdx.x; i < tl.len; i += kThreads) dst[tl.flat + i] = shards[tl.shard + i];
+  }
+}
+
+cudaError_t launch_gather_bucket(const Tile* tiles, int n_tiles, const void* shards, void* dst,
+                                 int grid, cudaStream_t s) {
+  k_gather_bucket<<<grid, kThreads, 0, s>>>(tiles, n_tiles, static_cast<const uint16_t*>(shards),
+                                            static_cast<uint16_t*>(dst));
+  return cudaGetLastError();
+}
+
+__global__ void k_scaler_restore(DevState* st, double scale, long long counter, long long t) {
+  st->scale = scale;
+  st->counter = counter;
+  st->t = t;
+}
+
+cudaError_t launch_scaler_restore(DevState* st, double scale, long long counter, long long t,
+                                  cudaStream_t s) {
+  k_scaler_restore<<<1, 1, 0, s>>>(st, scale, counter, t);
   return cudaGetLastError();
 }
 

@@ -190,7 +190,8 @@ __global__ void __launch_bounds__(kThreads) k_adamw_cast(const __grid_constant__
     float* mp = a.master + tl.shard;
     float* m1 = a.m + tl.shard;
     float* v1 = a.v + tl.shard;
-    PT* pp = static_cast<PT*>(a.params_flat) + tl.flat;
+    // stage 3 keeps the parameters sharded (rank-major, like master)
+    PT* pp = static_cast<PT*>(a.params_flat) + (a.stage == 3 ? tl.shard : tl.flat);
     const int nvec = tl.len >> 3;
     for (int vi = threadIdx.x; vi < nvec; vi += kThreads) {
       const int64_t o = (int64_t)vi * 8;
@@ -342,7 +343,7 @@ __global__ void __launch_bounds__((NC + 1) * 32)
     const float* sv = reinterpret_cast<const float*>(base + C * 8);
     const CT* sr = reinterpret_cast<const CT*>(base + C * 12);
     const int64_t so = tl.shard + cc, fo = tl.flat + cc;
-    PT* pp = static_cast<PT*>(a.params_flat) + fo;
+    PT* pp = static_cast<PT*>(a.params_flat) + (a.stage == 3 ? so : fo);
     const int e_end = min(nb, (warp + 1) * kPerWarp);
 #pragma unroll 2
     for (int e = warp * kPerWarp + 4 * lane; e < e_end; e += 128) {

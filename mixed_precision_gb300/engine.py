@@ -70,7 +70,7 @@ class ZeroStep:
         self.params_flat = torch.empty(n, dtype=TORCH_DTYPE[self.param_dtype], device=dev)
         self.scratch = None
         self.allreduce_out = None
-        if self.stage == 2:
+        if self.stage != 1:
             self.scratch = torch.empty(n, dtype=TORCH_DTYPE[self.comm_dtype], device=dev)
         else:
             self.allreduce_out = [torch.empty(n, dtype=TORCH_DTYPE[self.comm_dtype], device=dev)

@@ -107,6 +107,15 @@ def test_ledger_matches_page_table(zlib):
     zlib.zero_layout_destroy(h)
 
 
+def test_ledger_stage3_shards_everything(zlib):
+    """ZeRO-3 shards all 16 bytes of fp16/bf16 mixed-precision state: 16/W per
+    parameter ("3.7 ...", "ZeRO Stages Recap")."""
+    for W in (1, 2, 4, 8):
+        h = zlib.zero_layout_create([(1024,)], _cfg(zlib, W, 3, 1 << 20, wl.BF16, wl.BF16))
+        assert zlib.zero_layout_query(h).ledger_bytes_per_param == pytest.approx(16.0 / W)
+        zlib.zero_layout_destroy(h)
+
+
 def test_step_bytes_formula(zlib):
     for W in (2, 4, 8):
         h = zlib.zero_layout_create([(4096,)], _cfg(zlib, W))
@@ -115,7 +124,7 @@ def test_step_bytes_formula(zlib):
 
 
 def test_invalid_arguments(zlib):
-    bad = [_cfg(zlib, 0), _cfg(zlib, 65), _cfg(zlib, 2, stage=3), _cfg(zlib, 2, bucket=0),
+    bad = [_cfg(zlib, 0), _cfg(zlib, 65), _cfg(zlib, 2, stage=4), _cfg(zlib, 2, bucket=0),
            _cfg(zlib, 2, g=7), _cfg(zlib, 2, p=wl.F32), _cfg(zlib, 2, c=9), _cfg(zlib, 2, bucket=1)]
     for cfg in bad:
         with pytest.raises(zlib.ZeroError) as e:

@@ -52,3 +52,116 @@ def test_accumulate_then_boundary_step(micro_dtype, comm):
         assert np.array_equal(to_np(main_dev[r])[real], main_np[r][real])
     st, info, gc = pr.step([torch.from_numpy(m) for m in main_np], Hparams(), dev=main_dev)
     pr.check(st, info, gc)
+
+
+def _pm_from_shards(L, numel, shards):
+    flat = np.zeros(L.np_total, np.float32)
+    flat[L.flat_of_shard()] = shards
+    return np.concatenate([flat[off:off + n] for off, n in zip(L.param_offset, numel)])
+
+
+def _shards_from_pm(L, numel, pm):
+    flat = np.zeros(L.np_total, np.float32)
+    at = 0
+    for off, n in zip(L.param_offset, numel):
+        flat[off:off + n] = pm[at:at + n]
+        at += n
+    return flat[L.flat_of_shard()].copy()
+
+
+def test_checkpoint_reshard_w4_to_w2():
+    """Train 2 steps with W=4 / ZeRO-2 / 80 KB buckets, export the fp32 state in
+    parameter-major order plus the scaler, import it into W=2 / ZeRO-1 / 1 MB
+    buckets, and continue: the imported state is bit-identical per parameter
+    and the next step matches the oracle continued from its own state."""
+    shapes = wl.qwen3_0_6b_shapes(vocab=1000, hidden=128, layers=2, q_dim=256, kv_dim=128,
+                                  ffn=384, head_dim=32)
+    numel = wl.numels(shapes)
+    n = sum(numel)
+    stream = torch.cuda.current_stream().cuda_stream
+    a = Pair(shapes, 4, 2, 80_000, wl.F16, wl.F16, init_scale=1024.0, dynamic=True,
+             growth_interval=3, index=140)
+    for step in range(2):
+        st, info, gc = a.step(a.grads(step, 1e-3), Hparams())
+        a.check(st, info, gc)
+    pm = [torch.empty(n, dtype=torch.float32, device="cuda") for _ in range(3)]
+    abi.zero_state_export_params(a.z.handle, *[t.data_ptr() for t in pm], stream)
+    saved = abi.zero_loss_scale_state(a.z.handle, stream)
+    # the export is the GPU's own state, reordered
+    for t, shard_t in zip(pm, (a.z.master, a.z.m, a.z.v)):
+        assert np.array_equal(to_np(t), _pm_from_shards(a.L, numel, to_np(shard_t)[:a.np]))
+
+    b = Pair(shapes, 2, 1, 1_000_000, wl.F16, wl.F16, init_scale=1.0, dynamic=True,
+             growth_interval=3, index=141)
+    abi.zero_state_import_params(b.z.handle, *[t.data_ptr() for t in pm], stream)
+    abi.zero_scaler_restore(b.z.handle, saved, stream)
+    torch.cuda.synchronize()
+    pm_b = [torch.empty(n, dtype=torch.float32, device="cuda") for _ in range(3)]
+    abi.zero_state_export_params(b.z.handle, *[t.data_ptr() for t in pm_b], stream)
+    torch.cuda.synchronize()
+    for x, y in zip(pm, pm_b):
+        assert torch.equal(x.view(torch.int32), y.view(torch.int32))
+    for p in range(len(shapes)):
+        assert torch.equal(a.z.param_view(a.z.params_flat, p).view(torch.int16),
+                           b.z.param_view(b.z.params_flat, p).view(torch.int16))
+    st_b = b.z.scaler_state()
+    assert (st_b["scale"], st_b["counter"], st_b["t"]) == (saved.scale, saved.counter, saved.t)
+
+    # the oracle side goes through the same reshard, from the oracle's own state
+    o_pm = [_pm_from_shards(a.L, numel, x) for x in (a.o_master, a.o_m, a.o_v)]
+    b.o_master, b.o_m, b.o_v = [_shards_from_pm(b.L, numel, x) for x in o_pm]
+    b.hist = [_shards_from_pm(b.L, numel, _pm_from_shards(a.L, numel, h)) for h in a.hist]
+    flat_master = np.zeros(b.np, np.float32)
+    flat_master[b.perm] = b.o_master
+    b.o_params = oracle.encode(flat_master, wl.F16)
+    b.o_params[~b.mask_flat] = 0
+    b.o_scaler = oracle.Scaler(scale=a.o_scaler.scale, counter=a.o_scaler.counter, t=a.o_scaler.t,
+                               dynamic=True, growth_interval=3)
+    st, info, gc = b.step(b.grads(5, 1e-3), Hparams())
+    b.check(st, info, gc)
+
+
+def test_zero3_sharded_params_and_bucket_gather_with_prefetch():
+    """Stage 3: the cast-out parameters stay in rank-major shards; all-gathering
+    every bucket (the next one prefetched on a second stream while the
+    current one is "in use") rebuilds exactly the flat parameters the oracle
+    computes, step after step."""
+    shapes = wl.qwen3_0_6b_shapes(vocab=1000, hidden=128, layers=2, q_dim=256, kv_dim=128,
+                                  ffn=384, head_dim=32)
+    pr = Pair(shapes, 4, 3, 120_000, wl.BF16, wl.BF16, index=150)
+    info_q = abi.zero_layout_query(pr.z.handle)
+    assert info_q.ledger_bytes_per_param == pytest.approx(16.0 / 4)
+    main = torch.cuda.current_stream()
+    side = torch.cuda.Stream()
+    gathered = torch.zeros(pr.np, dtype=torch.bfloat16, device="cuda")
+    n_b = info_q.n_buckets
+    assert n_b >= 3
+    for step in range(2):
+        st, info, gc = pr.step(pr.grads(step, 1e-3), Hparams())
+        pr.check(st, info, gc)
+        gathered.zero_()
+        ready = [torch.cuda.Event() for _ in range(n_b)]
+        abi.zero_gather_bucket(pr.z.handle, 0, gathered.data_ptr(), main.cuda_stream)
+        ready[0].record(main)
+        side.wait_stream(main)
+        for b in range(n_b):
+            if b + 1 < n_b:  # prefetch the next bucket on the side stream
+                abi.zero_gather_bucket(pr.z.handle, b + 1, gathered.data_ptr(), side.cuda_stream)
+                ready[b + 1].record(side)
+            main.wait_event(ready[b])
+            # bucket b is in use here (a forward would read it on `main`)
+        torch.cuda.synchronize()
+        got = to_np(gathered)
+        assert _gather_matches_shards(pr, got)  # bit for bit; pr.check compared with the oracle
+        assert np.all(got[~pr.mask_flat] == 0)
+    with pytest.raises(ZeroError) as e:
+        abi.zero_gather_bucket(pr.z.handle, n_b, gathered.data_ptr(), main.cuda_stream)
+    assert e.value.code == abi.ZERO_ERR_INVALID
+
+
+def _gather_matches_shards(pr, got):
+    """The gathered params equal the GPU's own shards put back in flat order
+    (those were checked against the oracle's parameters by pr.check)."""
+    flat = np.zeros(pr.np, np.uint16)
+    flat[pr.perm] = to_np(pr.z.params_flat)[:pr.np]
+    return np.array_equal(got[pr.mask_flat], flat[pr.mask_flat])
