@@ -266,10 +266,27 @@ int zero_step_per_tensor_launch(zero_layout_t* layout, const void* const* grads,
 
 /* Same step from HOST gradients: copies host_grads[w] (Np elements of
  * grad_dtype each, flat layout; pinned memory gives asynchronous copies) into
- * the device buffers dev_grads[w] with one cudaMemcpyAsync per rank on
- * `stream`, then runs zero_step on dev_grads. */
+ * the device buffers dev_grads[w], then runs zero_step on dev_grads.
+ * The copies run as pieces of at most 128 MB on copy streams the layout owns
+ * (created on the first call); `stream` waits for them before the step. They
+ * start after the previous zero_step_host step's reduce kernel has finished
+ * reading dev_grads (stages 2/3) -- so they overlap that step's update
+ * kernel -- or after all work queued on `stream` (stage 1, whose all-reduce
+ * outputs may alias the gradients, and the first call). dev_grads must not be
+ * written by anything else between calls. */
 int zero_step_host(zero_layout_t* layout, const void* const* host_grads, void* const* dev_grads,
                    void* const* allreduce_out, const zero_hparams* hp, void* stream);
+
+/* Asynchronous form of zero_loss_scale_state: enqueues a copy of the
+ * library's device state block (ZERO_STATE_BLOB_BYTES bytes) into `blob` on
+ * `stream` and returns at once. `blob` should be pinned host memory (pageable
+ * memory makes the copy synchronous). After the stream has reached that
+ * point, zero_state_blob_decode turns the blob into a zero_scaler_state. */
+#define ZERO_STATE_BLOB_BYTES 256
+int zero_loss_scale_state_async(zero_layout_t* layout, void* blob, void* stream);
+/* Host only. Returns ZERO_ERR_TIMEOUT if the blob records a kernel whose
+ * bounded wait gave up. */
+int zero_state_blob_decode(const void* blob, zero_scaler_state* out);
 
 /* Read the scaler state and the last step's report. Enqueues a device-to-host
  * copy on `stream` and WAITS for it (synchronises the stream). */

@@ -18,6 +18,7 @@ LIB_PATH = os.path.join(_HERE, "libzero_gb300.so")
 ZERO_OK, ZERO_ERR_INVALID, ZERO_ERR_CUDA, ZERO_ERR_OOM, ZERO_ERR_TIMEOUT, ZERO_ERR_STATE = range(6)
 ZERO_F32, ZERO_F16, ZERO_BF16 = 0, 1, 2
 ZERO_MAX_WORLD = 64
+ZERO_STATE_BLOB_BYTES = 256
 STATUS_NAME = {0: "ZERO_OK", 1: "ZERO_ERR_INVALID", 2: "ZERO_ERR_CUDA", 3: "ZERO_ERR_OOM",
                4: "ZERO_ERR_TIMEOUT", 5: "ZERO_ERR_STATE"}
 
@@ -106,6 +107,8 @@ def lib() -> ctypes.CDLL:
             "zero_state_import_params": [P, P, P, P, P],
             "zero_scaler_restore": [P, ctypes.POINTER(zero_scaler_state), P],
             "zero_gather_bucket": [P, I, P, P],
+            "zero_loss_scale_state_async": [P, P, P],
+            "zero_state_blob_decode": [P, ctypes.POINTER(zero_scaler_state)],
         }
         for name, args in sig.items():
             fn = getattr(L, name)
@@ -266,3 +269,13 @@ def zero_scaler_restore(layout: int, st: zero_scaler_state, stream: int) -> None
 
 def zero_gather_bucket(layout: int, bucket: int, dst: int, stream: int) -> None:
     _check(lib().zero_gather_bucket(layout, bucket, dst, stream or None))
+
+
+def zero_loss_scale_state_async(layout: int, blob: int, stream: int) -> None:
+    _check(lib().zero_loss_scale_state_async(layout, blob, stream or None))
+
+
+def zero_state_blob_decode(blob: int) -> zero_scaler_state:
+    st = zero_scaler_state()
+    _check(lib().zero_state_blob_decode(blob, ctypes.byref(st)))
+    return st

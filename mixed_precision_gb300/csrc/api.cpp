@@ -113,6 +113,16 @@ struct zero_layout {
   cudaEvent_t events[4] = {nullptr, nullptr, nullptr, nullptr};
   bool timing = false;
 
+  // zero_step_host: host-to-device copies split over several copy streams
+  static constexpr int kCopyStreams = 4;
+  int n_copy_streams = kCopyStreams;
+  bool copy_ready = false;
+  cudaStream_t copy_stream[kCopyStreams] = {};
+  cudaEvent_t copy_start = nullptr;
+  cudaEvent_t copy_done[kCopyStreams] = {};
+  cudaEvent_t k1_done = nullptr;  // recorded after each step's reduce kernel once host mode is used
+  bool k1_recorded = false;
+
   int world() const { return cfg.world; }
   int n_params() const { return (int)numel.size(); }
 };
@@ -257,6 +267,10 @@ int launch_step(zero_layout* L, const GradSrc& src, void* const* allreduce_out,
     cudaError_t e = launch_reduce(ra, L->grid_reduce, L->reduce_variant, s);
     if (e != cudaSuccess) return cuda_fail(e, "reduce kernel launch");
     n_part = L->grid_reduce;
+  }
+  if (L->k1_done != nullptr) {
+    ZERO_CUDA(cudaEventRecord(L->k1_done, s));
+    L->k1_recorded = true;
   }
   if (L->timing) ZERO_CUDA(cudaEventRecord(L->events[1], s));
   Hparams h{hp->lr, hp->beta1, hp->beta2, hp->eps, hp->weight_decay, hp->max_grad_norm,
@@ -442,6 +456,14 @@ int zero_layout_create(const int64_t* const* shapes, const int* ndims, int n_par
 
 int zero_layout_destroy(zero_layout_t* L) {
   if (L == nullptr) return ZERO_OK;
+  if (L->copy_ready) {
+    for (int i = 0; i < L->n_copy_streams; ++i) {
+      cudaStreamDestroy(L->copy_stream[i]);
+      cudaEventDestroy(L->copy_done[i]);
+    }
+    cudaEventDestroy(L->copy_start);
+    cudaEventDestroy(L->k1_done);
+  }
   if (L->dblock) L->free_fn(L->dblock, L->alloc_ctx);
   if (L->d_gather) L->free_fn(L->d_gather, L->alloc_ctx);
   delete L;
@@ -690,8 +712,47 @@ int zero_step_host(zero_layout_t* L, const void* const* host_grads, void* const*
   }
   if (int rc = check_hparams(hp)) return rc;
   if (int rc = check_allreduce(L, allreduce_out)) return rc;
-  for (int w = 0; w < L->world(); ++w)
-    ZERO_CUDA(cudaMemcpyAsync(dev_grads[w], host_grads[w], bytes, cudaMemcpyHostToDevice, s));
+  if (!L->copy_ready) {
+    if (const char* v = std::getenv("ZERO_H2D_STREAMS")) {
+      const int n = std::atoi(v);
+      L->n_copy_streams = n >= 1 && n <= zero_layout::kCopyStreams ? n : zero_layout::kCopyStreams;
+    }
+    ZERO_CUDA(cudaEventCreateWithFlags(&L->copy_start, cudaEventDisableTiming));
+    ZERO_CUDA(cudaEventCreateWithFlags(&L->k1_done, cudaEventDisableTiming));
+    for (int i = 0; i < L->n_copy_streams; ++i) {
+      ZERO_CUDA(cudaStreamCreateWithFlags(&L->copy_stream[i], cudaStreamNonBlocking));
+      ZERO_CUDA(cudaEventCreateWithFlags(&L->copy_done[i], cudaEventDisableTiming));
+    }
+    L->copy_ready = true;
+  }
+  // The copies start once nothing can still read dev_grads: after the
+  // previous step's reduce kernel (stages 2/3: the update kernel never reads
+  // the gradients, so the copies overlap it), else after everything already
+  // on `stream`. They run as pieces of at most 128 MB spread over the copy
+  // streams, and `stream` waits for all of them before the step.
+  const size_t piece = size_t(128) << 20;
+  const int n = L->n_copy_streams;
+  cudaEvent_t after = L->copy_start;
+  if (L->cfg.stage != 1 && L->k1_recorded) {
+    after = L->k1_done;
+  } else {
+    ZERO_CUDA(cudaEventRecord(L->copy_start, s));
+  }
+  for (int i = 0; i < n; ++i) ZERO_CUDA(cudaStreamWaitEvent(L->copy_stream[i], after, 0));
+  int next = 0;
+  for (int w = 0; w < L->world(); ++w) {
+    for (size_t off = 0; off < bytes; off += piece) {
+      const size_t len = std::min(piece, bytes - off);
+      ZERO_CUDA(cudaMemcpyAsync(static_cast<char*>(dev_grads[w]) + off,
+                                static_cast<const char*>(host_grads[w]) + off, len,
+                                cudaMemcpyHostToDevice, L->copy_stream[next]));
+      next = (next + 1) % n;
+    }
+  }
+  for (int i = 0; i < n; ++i) {
+    ZERO_CUDA(cudaEventRecord(L->copy_done[i], L->copy_stream[i]));
+    ZERO_CUDA(cudaStreamWaitEvent(s, L->copy_done[i], 0));
+  }
   return zero_step(L, dev_grads, allreduce_out, hp, stream);
 }
 
@@ -715,6 +776,34 @@ int zero_accumulate(zero_layout_t* L, const void* const* micro, int micro_dtype,
   if (a.n_tiles == 0) return ZERO_OK;
   cudaError_t e = launch_accumulate(a, L->grid_copy, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "accumulate kernel launch");
+  return ZERO_OK;
+}
+
+static_assert(sizeof(DevState) <= ZERO_STATE_BLOB_BYTES, "state blob too small");
+
+int zero_loss_scale_state_async(zero_layout_t* L, void* blob, void* stream) {
+  if (int rc = check_ready(L, true)) return rc;
+  if (blob == nullptr) return fail(ZERO_ERR_INVALID, "blob is NULL");
+  ZERO_CUDA(cudaMemcpyAsync(blob, L->d_state, sizeof(DevState), cudaMemcpyDeviceToHost,
+                            static_cast<cudaStream_t>(stream)));
+  return ZERO_OK;
+}
+
+int zero_state_blob_decode(const void* blob, zero_scaler_state* out) {
+  if (blob == nullptr || out == nullptr) return fail(ZERO_ERR_INVALID, "blob/out is NULL");
+  DevState h;
+  std::memcpy(&h, blob, sizeof(h));
+  out->scale = h.scale;
+  out->counter = h.counter;
+  out->t = h.t;
+  out->overflow = h.overflow;
+  out->skipped = h.skipped;
+  out->grad_norm = h.grad_norm;
+  out->clip_coef = h.clip_coef;
+  out->norm_sq_raw = h.norm_sq_raw;
+  out->steps = h.steps;
+  if (h.error != 0)
+    return fail(ZERO_ERR_TIMEOUT, "a kernel's bounded wait gave up (device error word %u)", h.error);
   return ZERO_OK;
 }
 

@@ -131,6 +131,36 @@ def test_host_entry_point_matches_device():
         assert np.array_equal(a, b)
 
 
+@pytest.mark.parametrize("stage", [1, 2])
+def test_host_steps_back_to_back_overlap(stage):
+    """Two zero_step_host calls with different gradients into the same device
+    buffers, no synchronisation between them: the second step's copies may
+    overlap the first step's update kernel (stage 2) but never its reduce.
+    The final state matches two oracle steps."""
+    import oracle as orc
+    from _parity import to_np
+    shapes = small_qwen_shapes()
+    pr = Pair(shapes, 2, stage, 100_000, wl.BF16, wl.BF16, index=160)
+    g0, g1 = pr.grads(0, 1e-3), pr.grads(1, 1e-3)
+    dev = [torch.empty(pr.np, dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+    pin0, pin1 = [x.pin_memory() for x in g0], [x.pin_memory() for x in g1]
+    hp = Hparams()
+    pr.z.step_host(pin0, dev, hp)
+    pr.z.step_host(pin1, dev, hp)
+    torch.cuda.synchronize()
+    st = pr.z.scaler_state()
+    o_hp = orc.Hparams(hp.lr, hp.beta1, hp.beta2, hp.eps, hp.weight_decay, hp.max_grad_norm,
+                       hp.grad_divisor)
+    for g in (g0, g1):
+        info = orc.zero_step(pr.numel, pr.W, stage, pr.bucket, pr.gdt, pr.cdt, pr.pdt,
+                             [to_np(x) for x in g], pr.o_master, pr.o_m, pr.o_v, pr.o_params, o_hp,
+                             pr.o_scaler, allreduce_out=pr.o_out)
+        for h, x in zip(pr.hist, (pr.o_master, pr.o_m, pr.o_v)):
+            np.maximum(h, np.abs(x), out=h)
+    assert st["t"] == 2
+    pr.check(st, info, g1)
+
+
 def test_overflow_at_shard_edges_skips():
     """+inf / -inf / NaN at the first or last real element of shards in the
     first and last rank: flag set, step skipped, state untouched, scale halved."""
