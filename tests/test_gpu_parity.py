@@ -12,6 +12,7 @@ import oracle
 import workloads as wl
 from _parity import INF_BITS, Pair, to_np
 from mixed_precision_gb300 import ZeroError
+from mixed_precision_gb300 import _abi as abi
 from mixed_precision_gb300.engine import Hparams
 
 pytestmark = pytest.mark.gpu
@@ -289,3 +290,79 @@ def test_invalid_device_arguments():
     pr.z.step(g, hp)
     torch.cuda.synchronize()
     assert pr.z.scaler_state()["t"] == 1
+
+
+def test_deterministic_across_runs():
+    """The reductions run in a fixed order, so two identical runs give
+    identical bits (norm included)."""
+    outs = []
+    for _ in range(2):
+        pr = Pair(small_qwen_shapes(), 4, 2, 80_000, wl.BF16, wl.BF16, index=180)
+        for step in range(2):
+            st, info, gc = pr.step(pr.grads(step, 1e-3), Hparams())
+        outs.append([to_np(t) for t in (pr.z.master, pr.z.m, pr.z.v, pr.z.params_flat)]
+                    + [to_np(pr.z.scratch)[:pr.np][pr.mask_shard]]  # padding is never written
+                    + [st["grad_norm"], st["norm_sq_raw"]])
+    for a, b in zip(outs[0][:5], outs[1][:5]):
+        assert np.array_equal(a, b)
+    assert outs[0][5:] == outs[1][5:]
+
+
+def test_runs_on_the_given_stream():
+    """Work goes to the stream passed in: a side stream, joined afterwards."""
+    pr = Pair(small_qwen_shapes(), 2, 2, 80_000, wl.BF16, wl.BF16, index=181)
+    g = pr.grads(0, 1e-3)
+    dev = [x.cuda() for x in g]
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        pr.z.step(dev, Hparams(), stream=side)
+        st_side = pr.z.scaler_state(stream=side)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    # the oracle side of the same step
+    import oracle as orc
+    o_hp = orc.Hparams()
+    info = orc.zero_step(pr.numel, 2, 2, pr.bucket, pr.gdt, pr.cdt, pr.pdt, [to_np(x) for x in g],
+                         pr.o_master, pr.o_m, pr.o_v, pr.o_params, o_hp, pr.o_scaler)
+    for h, x in zip(pr.hist, (pr.o_master, pr.o_m, pr.o_v)):
+        np.maximum(h, np.abs(x), out=h)
+    pr.check(st_side, info, g)
+
+
+def test_stage1_in_place_allreduce():
+    """ZeRO-1 with the all-reduce outputs aliasing the gradient buffers: each
+    rank's buffer ends up holding the reduced gradient; the step matches a
+    run with separate outputs."""
+    shapes = small_qwen_shapes()
+    a = Pair(shapes, 4, 1, 80_000, wl.F16, wl.F16, index=182)
+    b = Pair(shapes, 4, 1, 80_000, wl.F16, wl.F16, index=182)
+    g = a.grads(0, 1e-3)
+    st_a, info, gc = a.step(g, Hparams())
+    a.check(st_a, info, gc)
+    dev = [x.cuda() for x in g]
+    b.z.step(dev, Hparams(), allreduce_out=dev)
+    torch.cuda.synchronize()
+    for t_a, t_b in ((a.z.master, b.z.master), (a.z.params_flat, b.z.params_flat)):
+        assert np.array_equal(to_np(t_a), to_np(t_b))
+    for w in range(4):
+        assert np.array_equal(to_np(dev[w])[a.mask_flat], to_np(a.z.allreduce_out[w])[a.mask_flat])
+
+
+def test_rebind_state_buffers():
+    """Binding new buffers redirects the step; the library's own block is reused."""
+    pr = Pair([(5000,), (300,)], 2, 2, 1 << 20, wl.BF16, wl.BF16, index=183)
+    z = pr.z
+    owned = abi.zero_layout_query(z.handle).device_bytes_owned
+    old = (z.master, z.m, z.v, z.params_flat, z.scratch)
+    old_bits = [to_np(t).copy() for t in old]
+    copies = [t.clone() for t in old]
+    z.bind(*copies)
+    z.master, z.m, z.v, z.params_flat, z.scratch = copies
+    z.init(torch.zeros(z.np, dtype=torch.float32, device="cuda"))
+    st, info, gc = pr.step(pr.grads(0, 1e-3), Hparams(max_grad_norm=0.0))
+    assert abi.zero_layout_query(z.handle).device_bytes_owned == owned
+    assert st["t"] == 1
+    assert np.count_nonzero(to_np(z.master)[pr.mask_shard]) > 0  # the new buffers were stepped
+    for t, bits in zip(old, old_bits):  # the old ones were not touched
+        assert np.array_equal(to_np(t), bits)
