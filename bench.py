@@ -33,9 +33,6 @@ if ROOT not in sys.path:
 METRIC = "ZeRO step params updated/s and achieved HBM GB/s (% of GB300 step roofline)"
 DEFAULT_WORKLOAD = "qwen3_0.6b_bf16_w2"
 L2_BYTES = 129 * 1000 * 1000
-# Bytes the library copies back per zero_loss_scale_state call (its device
-# scalar block: 8 eight-byte fields, 4 ints, 3 doubles, 10 floats).
-STATE_READ_BYTES = 144
 # DRAM bytes per real element of the update kernel from one ncu capture
 # (dram__bytes_read.sum + dram__bytes_write.sum / elements), with the capture
 # it comes from; None until a capture of the current kernel exists.
@@ -62,6 +59,10 @@ def parse_args(argv=None):
     ap.add_argument("--world", type=int, default=None, help="override the simulated world size")
     ap.add_argument("--bucket-bytes", type=int, default=None, help="override the bucket size")
     ap.add_argument("--stage", type=int, default=None, help="override the ZeRO stage (1, 2, 3)")
+    ap.add_argument("--clip", type=float, default=None,
+                    help="override max_grad_norm (<= 0: no clipping)")
+    ap.add_argument("--speculative", action="store_true",
+                    help="time zero_step_speculative (single pass when clipping stays inactive)")
     ap.add_argument("--per-tensor-launch", action="store_true",
                     help="launch the step tensor by tensor (the hook-style baseline)")
     ap.add_argument("--tensors", action="store_true",
@@ -201,6 +202,8 @@ def workload_of(args):
         over["bucket_bytes"] = args.bucket_bytes
     if getattr(args, "stage", None):
         over["stage"] = args.stage
+    if getattr(args, "clip", None) is not None:
+        over["max_grad_norm"] = args.clip
     return wl.workload(args.workload, **over)
 
 
@@ -310,7 +313,9 @@ def run_ours(args) -> dict | None:
 
     z = ZeroStep(w.shapes, w.world, w.stage, w.bucket_bytes, w.grad_dtype, w.param_dtype,
                  w.comm_dtype)
-    z.allocate()
+    if args.speculative and w.stage == 1:
+        raise SystemExit("--speculative needs stage 2 or 3")
+    z.allocate(speculative=args.speculative)
     info = z.info
     numel = wl.numels(w.shapes)
     master0 = wl.master_init(z.offsets, numel, z.np, w.master_sigma, wl.master_seed(w.index),
@@ -335,6 +340,8 @@ def run_ours(args) -> dict | None:
             z.step_tensors(per_tensor, hp)
         elif args.per_tensor_launch:
             z.step_per_tensor_launch(grads, hp)
+        elif args.speculative:
+            z.step_speculative(grads, hp)
         else:
             z.step(grads, hp)
     hp = Hparams(lr=w.lr, beta1=w.beta1, beta2=w.beta2, eps=w.eps, weight_decay=w.weight_decay,
@@ -367,6 +374,8 @@ def run_ours(args) -> dict | None:
     total_ms = max_over_ranks(dist, local_ms, device)
     st = z.scaler_state()
     assert st["overflow"] == 0 and st["steps"] == K + W, st
+    # the speculative step commits on the fast path unless clipping is active
+    fast_path = st["fast_path"] if args.speculative else None
 
     k1 = [ev[k][0].elapsed_time(ev[k][1]) for k in range(K)]
     k2 = [ev[k][1].elapsed_time(ev[k][2]) for k in range(K)]
@@ -412,7 +421,7 @@ def run_ours(args) -> dict | None:
         del host
         e2e = {"value": job_value(info.n_real, world, e2e_s / E), "unit": "params/s",
                "h2d_bytes_per_step": w.world * z.np * wl.ELEM_BYTES[w.grad_dtype],
-               "d2h_bytes_per_step": STATE_READ_BYTES,
+               "d2h_bytes_per_step": int(info.state_blob_used),
                "note": "next step's host-to-device copy overlaps this step's update kernel; "
                        "the step result is read back asynchronously into pinned memory"}
 
@@ -425,7 +434,18 @@ def run_ours(args) -> dict | None:
     k1_bytes = N * (w.world * G + (w.world * C if w.stage == 1 else C))
     k3_bytes = N * (C + 24 + P)
     k1_ms, k2_ms, k3_ms = statistics.mean(k1), statistics.mean(k2), statistics.mean(k3)
-    dom = ("k_adamw_cast", k3_bytes, k3_ms) if k3_ms >= k1_ms else ("k_reduce_norm", k1_bytes, k1_ms)
+    if args.speculative:
+        # events: [single pass] [its finalize] [guarded fallback kernels + restore]
+        spec_bytes = N * info.step_bytes_per_elem
+        dom = ("k_spec_step", spec_bytes, k1_ms)
+        kernels = {"k_spec_step": k1_ms, "k_finalize_spec": k2_ms, "guarded_fallback": k3_ms,
+                   "k_spec_step_gbs": spec_bytes / (k1_ms / 1e3) / 1e9}
+    else:
+        dom = ("k_adamw_cast", k3_bytes, k3_ms) if k3_ms >= k1_ms else \
+            ("k_reduce_norm", k1_bytes, k1_ms)
+        kernels = {"k_reduce_norm": k1_ms, "k_finalize": k2_ms, "k_adamw_cast": k3_ms,
+                   "k_reduce_norm_gbs": k1_bytes / (k1_ms / 1e3) / 1e9,
+                   "k_adamw_cast_gbs": k3_bytes / (k3_ms / 1e3) / 1e9}
     achieved = dom[1] / (dom[2] / 1e3) / 1e9
     tr = NCU_TRAFFIC_PER_ELEM.get(dom[0])
     step_gbs = info.step_bytes_per_elem * N / step_s / 1e9
@@ -444,7 +464,10 @@ def run_ours(args) -> dict | None:
         "data": "synthetic",
         "config": config_of(w, "per-tensor gradient pointers, NULL for all-zero gradients"
                             if args.tensors else ("one reduce and one update launch per tensor"
-                                                  if args.per_tensor_launch else None)),
+                                                  if args.per_tensor_launch else
+                                                  ("speculative single pass; e2e through the "
+                                                   "two-pass host entry point"
+                                                   if args.speculative else None))),
         "hbm_gbs_step": step_gbs,
         "step_roofline": {"bytes_per_param": info.step_bytes_per_elem, "peak_gbs": peak,
                           "frac": step_gbs / peak, "peak_source": peak_src},
@@ -452,12 +475,12 @@ def run_ours(args) -> dict | None:
                      "unit": "GB/s", "frac": achieved / peak,
                      "traffic": (tr * N if tr is not None else None),
                      "algorithmic_bytes_per_launch": dom[1], "peak_source": peak_src},
-        "kernels_ms": {"k_reduce_norm": k1_ms, "k_finalize": k2_ms, "k_adamw_cast": k3_ms,
-                       "k_reduce_norm_gbs": k1_bytes / (k1_ms / 1e3) / 1e9,
-                       "k_adamw_cast_gbs": k3_bytes / (k3_ms / 1e3) / 1e9},
+        "kernels_ms": kernels,
+        "fast_path": fast_path,
         "skip_step_ms": skip_ms,
         "e2e": e2e,
-        "gpu_launches": K * ((2 * sum(1 for n in numel if n > 0) + 1) if args.per_tensor_launch else 3),
+        "gpu_launches": K * ((2 * sum(1 for n in numel if n > 0) + 1) if args.per_tensor_launch
+                             else (6 if args.speculative else 3)),
         "clocks": clocks,
     }
     z.close()

@@ -113,6 +113,8 @@ typedef struct {
                                     (P, G = param and grad dtype sizes) */
   double step_bytes_per_elem;    /* roofline bytes per real element of one step:
                                     2W grad reads + 24 master/m/v + P param write */
+  int64_t state_blob_used;       /* bytes of the state blob that
+                                    zero_loss_scale_state_async copies (<= ZERO_STATE_BLOB_BYTES) */
 } zero_layout_info;
 
 /* Loss-scaler configuration. [MD] fp16 loss_scale 0 = dynamic with
@@ -158,6 +160,9 @@ typedef struct {
   double clip_coef;    /* last step: clip coefficient (0 if skipped) */
   double norm_sq_raw;  /* last step: sum of squares of the reduced (scaled) values */
   int64_t steps;       /* zero_step calls since zero_state_init */
+  int32_t state_set;   /* which bound state set holds the current master/m/v:
+                          0 = the zero_state_bind buffers, 1 = the alternate set */
+  int32_t fast_path;   /* last step was a committed speculative single pass */
 } zero_scaler_state;
 
 /* ------------------------------------------------------------------------ */
@@ -211,6 +216,17 @@ int zero_shard_range(const zero_layout_t* layout, int bucket, int rank, int64_t*
 int zero_state_bind(zero_layout_t* layout, void* master, void* m, void* v, void* params_flat,
                     void* scratch);
 
+/* Bind a second master/m/v set (fp32, Np elements each, rank-major like the
+ * first, all distinct from the bound buffers) for zero_step_speculative,
+ * which writes its result into whichever set is not current and then makes
+ * that set current. zero_scaler_state.state_set tells which set holds the
+ * current state; every other call (steps, export/import, gathers) follows it.
+ * Stages 2 and 3 only. Call after zero_state_bind and before zero_state_init
+ * (the layout counts as not initialised afterwards; init makes set 0
+ * current). Rebinding with zero_state_bind drops the alternate set.
+ * Synchronous (queries the kernel's occupancy). */
+int zero_state_bind_alternate(zero_layout_t* layout, void* master2, void* m2, void* v2);
+
 /* Initialise the bound state: master <- master_init_flat (device fp32, Np,
  * flat layout; padding ignored), m = v = 0, params_flat <- RNE(master) with
  * padding zero, scaler <- cfg, t = 0. Enqueued on `stream`. */
@@ -263,6 +279,31 @@ int zero_step_tensors(zero_layout_t* layout, const void* const* grad_ptrs,
  * order differs. */
 int zero_step_per_tensor_launch(zero_layout_t* layout, const void* const* grads,
                                 void* const* allreduce_out, const zero_hparams* hp, void* stream);
+
+/* The same step in one pass over memory when it can be: the reduce, the norm
+ * partials and the AdamW update with clip coefficient 1 run in one kernel,
+ * which reads the current state set and writes the other one (and the
+ * parameters) without knowing the global norm yet. Its finalize then
+ *   - commits (no overflow, clip coefficient exactly 1): the other set
+ *     becomes current; results are bit-identical to zero_step;
+ *   - skips (overflow, [ND] FP16 dynamic loss scaling): state unchanged, the
+ *     parameters are recast from the current master (so they are unchanged
+ *     too), scale backs off;
+ *   - falls back (clipping active, [MD] gradient_clipping): the ordinary
+ *     reduce / finalize / update kernels run, results those of zero_step.
+ * The decision is taken on the device; every branch's kernels are enqueued
+ * and those not taken return at once, so the call never synchronises.
+ * While the last finalized step clipped, the single pass is predicted to
+ * fall back and returns at once: the step then costs what zero_step costs
+ * plus two empty launches, and only the step on which clipping switches on
+ * pays for both passes.
+ * A committed step moves W*size(grad) + 24 + size(param) bytes per element,
+ * the whole step's ledger; the reduced gradients are never stored, so the
+ * scratch buffer's contents are unspecified afterwards.
+ *   grads  flat gradients as for zero_step. Stages 2 and 3 only; needs
+ *          zero_state_bind_alternate. Errors as zero_step. */
+int zero_step_speculative(zero_layout_t* layout, const void* const* grads, const zero_hparams* hp,
+                          void* stream);
 
 /* Same step from HOST gradients: copies host_grads[w] (Np elements of
  * grad_dtype each, flat layout; pinned memory gives asynchronous copies) into

@@ -40,7 +40,8 @@ class zero_layout_info(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int64) for n in (
         "n_params", "n_real", "n_padded", "shard_elems", "n_buckets", "n_tiles", "grad_bytes",
         "state_bytes", "params_bytes", "scratch_bytes", "allreduce_bytes", "device_bytes_owned")] + \
-        [("ledger_bytes_per_param", ctypes.c_double), ("step_bytes_per_elem", ctypes.c_double)]
+        [("ledger_bytes_per_param", ctypes.c_double), ("step_bytes_per_elem", ctypes.c_double),
+         ("state_blob_used", ctypes.c_int64)]
 
 
 class zero_scaler_cfg(ctypes.Structure):
@@ -59,7 +60,8 @@ class zero_scaler_state(ctypes.Structure):
     _fields_ = [("scale", ctypes.c_double), ("counter", ctypes.c_int64), ("t", ctypes.c_int64),
                 ("overflow", ctypes.c_int32), ("skipped", ctypes.c_int32),
                 ("grad_norm", ctypes.c_double), ("clip_coef", ctypes.c_double),
-                ("norm_sq_raw", ctypes.c_double), ("steps", ctypes.c_int64)]
+                ("norm_sq_raw", ctypes.c_double), ("steps", ctypes.c_int64),
+                ("state_set", ctypes.c_int32), ("fast_path", ctypes.c_int32)]
 
 
 ALLOC_FN = ctypes.CFUNCTYPE(ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p)
@@ -90,6 +92,8 @@ def lib() -> ctypes.CDLL:
                                  ctypes.POINTER(I64)],
             "zero_state_bind": [P, P, P, P, P, P],
             "zero_state_init": [P, P, ctypes.POINTER(zero_scaler_cfg), P],
+            "zero_state_bind_alternate": [P, P, P, P],
+            "zero_step_speculative": [P, PP, ctypes.POINTER(zero_hparams), P],
             "zero_step": [P, PP, PP, ctypes.POINTER(zero_hparams), P],
             "zero_step_tensors": [P, PP, PP, ctypes.POINTER(zero_hparams), P],
             "zero_step_per_tensor_launch": [P, PP, PP, ctypes.POINTER(zero_hparams), P],
@@ -184,6 +188,14 @@ def zero_state_init(layout: int, master_init_flat: int, cfg: zero_scaler_cfg, st
 def zero_step(layout: int, grads, allreduce_out, hp: zero_hparams, stream: int) -> None:
     ar = _ptrs(allreduce_out) if allreduce_out is not None else None
     _check(lib().zero_step(layout, _ptrs(grads), ar, ctypes.byref(hp), stream or None))
+
+
+def zero_state_bind_alternate(layout: int, master2: int, m2: int, v2: int) -> None:
+    _check(lib().zero_state_bind_alternate(layout, master2, m2, v2))
+
+
+def zero_step_speculative(layout: int, grads, hp: zero_hparams, stream: int) -> None:
+    _check(lib().zero_step_speculative(layout, _ptrs(grads), ctypes.byref(hp), stream or None))
 
 
 def zero_step_per_tensor_launch(layout: int, grads, allreduce_out, hp: zero_hparams,

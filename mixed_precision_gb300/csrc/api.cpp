@@ -87,6 +87,10 @@ struct zero_layout {
   float* master = nullptr;
   float* m = nullptr;
   float* v = nullptr;
+  // optional second state set for the speculative step (DevState::cur picks)
+  float* master2 = nullptr;
+  float* m2 = nullptr;
+  float* v2 = nullptr;
   void* params = nullptr;
   void* scratch = nullptr;
 
@@ -106,6 +110,7 @@ struct zero_layout {
   size_t gather_cap = 0;
 
   int grid_reduce = 0, grid_update = 0, grid_copy = 0;
+  int grid_spec = 0;  // speculative single pass (set by zero_state_bind_alternate)
   // 1 (default): shared-memory pipelines fed by cp.async.bulk; 0: the
   // register-staged kernels, kept as the comparison baseline (environment
   // ZERO_REDUCE_VARIANT / ZERO_UPDATE_VARIANT = 0 at bind selects them)
@@ -144,6 +149,16 @@ int check_ready(const zero_layout_t* L, bool need_init) {
   if (dev != L->device)
     return fail(ZERO_ERR_STATE, "current device %d is not the bound device %d", dev, L->device);
   return ZERO_OK;
+}
+
+// The two state sets the kernels choose from (the second defaults to the first).
+void state_sets(const zero_layout* L, float* master[2], float* m[2], float* v[2]) {
+  master[0] = L->master;
+  m[0] = L->m;
+  v[0] = L->v;
+  master[1] = L->master2 ? L->master2 : L->master;
+  m[1] = L->m2 ? L->m2 : L->m;
+  v[1] = L->v2 ? L->v2 : L->v;
 }
 
 // The flat bucketed layout and the tile list (see zero_layout_create).
@@ -240,8 +255,10 @@ BlockPlan plan_block(const zero_layout* L) {
   return b;
 }
 
+// The two-pass step: reduce, finalize, update. `guarded` (the speculative
+// step's fallback): each kernel runs only if the speculative finalize asked.
 int launch_step(zero_layout* L, const GradSrc& src, void* const* allreduce_out,
-                const zero_hparams* hp, cudaStream_t s) {
+                const zero_hparams* hp, cudaStream_t s, int guarded = 0) {
   const int W = L->world();
   const int n_tiles = (int)L->tiles.size();
   ReduceArgs ra{};
@@ -261,6 +278,8 @@ int launch_step(zero_layout* L, const GradSrc& src, void* const* allreduce_out,
   ra.part_ovf = L->d_ovf;
   ra.chunk = reduce_chunk(W, L->cfg.grad_dtype);
   ra.error = &L->d_state->error;
+  ra.state = L->d_state;
+  ra.guarded = guarded;
   int n_part = 0;
   if (L->timing) ZERO_CUDA(cudaEventRecord(L->events[0], s));
   if (n_tiles > 0) {
@@ -275,7 +294,7 @@ int launch_step(zero_layout* L, const GradSrc& src, void* const* allreduce_out,
   if (L->timing) ZERO_CUDA(cudaEventRecord(L->events[1], s));
   Hparams h{hp->lr, hp->beta1, hp->beta2, hp->eps, hp->weight_decay, hp->max_grad_norm,
             hp->grad_divisor};
-  cudaError_t e = launch_finalize(L->d_part, L->d_ovf, n_part, W, h, L->d_state, s);
+  cudaError_t e = launch_finalize(L->d_part, L->d_ovf, n_part, W, h, L->d_state, guarded, s);
   if (e != cudaSuccess) return cuda_fail(e, "finalize kernel launch");
   if (L->timing) ZERO_CUDA(cudaEventRecord(L->events[2], s));
   if (n_tiles > 0) {
@@ -286,15 +305,56 @@ int launch_step(zero_layout* L, const GradSrc& src, void* const* allreduce_out,
     ua.comm_dtype = L->comm_dtype;
     ua.param_dtype = L->cfg.param_dtype;
     ua.red = ra.out;
-    ua.master = L->master;
-    ua.m = L->m;
-    ua.v = L->v;
+    state_sets(L, ua.master, ua.m, ua.v);
     ua.params_flat = L->params;
     ua.state = L->d_state;
     ua.error = &L->d_state->error;
     e = launch_update(ua, L->grid_update, L->update_variant, s);
     if (e != cudaSuccess) return cuda_fail(e, "update kernel launch");
   }
+  if (L->timing) ZERO_CUDA(cudaEventRecord(L->events[3], s));
+  return ZERO_OK;
+}
+
+// The speculative step: the single pass and its finalize; then the two-pass
+// kernels guarded on DevState::need_fallback (they return at once unless
+// clipping turned out active), the update (skipped unless the fallback
+// finalize cleared DevState::skip) and the parameter restore after an
+// overflow (guarded on DevState::restore_params).
+int launch_step_spec(zero_layout* L, const GradSrc& src, const zero_hparams* hp, cudaStream_t s) {
+  const int n_tiles = (int)L->tiles.size();
+  if (n_tiles == 0) return launch_step(L, src, nullptr, hp, s);
+  SpecArgs sa{};
+  sa.tiles = L->d_tiles;
+  sa.n_tiles = n_tiles;
+  sa.world = L->world();
+  sa.stage = L->cfg.stage;
+  sa.src = src;
+  state_sets(L, sa.master, sa.m, sa.v);
+  sa.params = L->params;
+  sa.state = L->d_state;
+  sa.hp = Hparams{hp->lr, hp->beta1, hp->beta2, hp->eps, hp->weight_decay, hp->max_grad_norm,
+                  hp->grad_divisor};
+  sa.part_sumsq = L->d_part;
+  sa.part_ovf = L->d_ovf;
+  sa.chunk = spec_chunk(L->world(), L->cfg.grad_dtype);
+  sa.error = &L->d_state->error;
+  if (L->timing) ZERO_CUDA(cudaEventRecord(L->events[0], s));
+  cudaError_t e = launch_spec(&sa, L->cfg.grad_dtype, L->comm_dtype, L->cfg.param_dtype, L->world(),
+                              L->grid_spec, s);
+  if (e != cudaSuccess) return cuda_fail(e, "speculative kernel launch");
+  if (L->timing) ZERO_CUDA(cudaEventRecord(L->events[1], s));
+  e = launch_finalize_spec(L->d_part, L->d_ovf, L->grid_spec, L->world(), sa.hp, L->d_state, s);
+  if (e != cudaSuccess) return cuda_fail(e, "speculative finalize launch");
+  if (L->timing) ZERO_CUDA(cudaEventRecord(L->events[2], s));
+  const bool timing = L->timing;
+  L->timing = false;
+  int rc = launch_step(L, src, nullptr, hp, s, /*guarded=*/1);
+  L->timing = timing;
+  if (rc != ZERO_OK) return rc;
+  e = launch_recast(L->d_tiles, n_tiles, sa.master, L->params, L->cfg.param_dtype, L->cfg.stage == 3,
+                    L->d_state, /*guarded=*/1, L->grid_copy, s);
+  if (e != cudaSuccess) return cuda_fail(e, "parameter restore launch");
   if (L->timing) ZERO_CUDA(cudaEventRecord(L->events[3], s));
   return ZERO_OK;
 }
@@ -319,6 +379,8 @@ int launch_step_per_tensor(zero_layout* L, const GradSrc& src, void* const* allr
   }
   ra.chunk = reduce_chunk(W, L->cfg.grad_dtype);
   ra.error = &L->d_state->error;
+  ra.state = L->d_state;
+  ra.guarded = 0;
   if (L->timing) ZERO_CUDA(cudaEventRecord(L->events[0], s));
   int64_t part_at = 0;
   for (int p = 0; p < P; ++p) {
@@ -336,7 +398,7 @@ int launch_step_per_tensor(zero_layout* L, const GradSrc& src, void* const* allr
   if (L->timing) ZERO_CUDA(cudaEventRecord(L->events[1], s));
   Hparams h{hp->lr, hp->beta1, hp->beta2, hp->eps, hp->weight_decay, hp->max_grad_norm,
             hp->grad_divisor};
-  cudaError_t e = launch_finalize(L->d_part_pt, L->d_ovf_pt, (int)part_at, W, h, L->d_state, s);
+  cudaError_t e = launch_finalize(L->d_part_pt, L->d_ovf_pt, (int)part_at, W, h, L->d_state, 0, s);
   if (e != cudaSuccess) return cuda_fail(e, "finalize kernel launch");
   if (L->timing) ZERO_CUDA(cudaEventRecord(L->events[2], s));
   UpdateArgs ua{};
@@ -344,9 +406,7 @@ int launch_step_per_tensor(zero_layout* L, const GradSrc& src, void* const* allr
   ua.comm_dtype = L->comm_dtype;
   ua.param_dtype = L->cfg.param_dtype;
   ua.red = ra.out;
-  ua.master = L->master;
-  ua.m = L->m;
-  ua.v = L->v;
+  state_sets(L, ua.master, ua.m, ua.v);
   ua.params_flat = L->params;
   ua.state = L->d_state;
   ua.error = &L->d_state->error;
@@ -505,6 +565,7 @@ int zero_layout_query(const zero_layout_t* L, zero_layout_info* o) {
                               : L->cfg.stage == 2 ? P + G / W + 12.0 / W
                                                   : (P + G + 12.0) / W;
   o->step_bytes_per_elem = W * G + 24.0 + P;
+  o->state_blob_used = (int64_t)sizeof(DevState);
   return ZERO_OK;
 }
 
@@ -615,7 +676,32 @@ int zero_state_bind(zero_layout_t* L, void* master, void* m, void* v, void* para
   L->v = static_cast<float*>(v);
   L->params = params_flat;
   L->scratch = scratch;
+  L->master2 = L->m2 = L->v2 = nullptr;
+  L->grid_spec = 0;
   L->bound = true;
+  L->initialized = false;
+  return ZERO_OK;
+}
+
+int zero_state_bind_alternate(zero_layout_t* L, void* master2, void* m2, void* v2) {
+  if (int rc = check_ready(L, false)) return rc;
+  if (L->cfg.stage == 1) return fail(ZERO_ERR_INVALID, "the speculative step needs stage 2 or 3");
+  if (master2 == nullptr || m2 == nullptr || v2 == nullptr)
+    return fail(ZERO_ERR_INVALID, "master2/m2/v2 must not be NULL");
+  if (!aligned16(master2) || !aligned16(m2) || !aligned16(v2))
+    return fail(ZERO_ERR_INVALID, "alternate state buffers must be 16-byte aligned");
+  const void* mine[4] = {L->master, L->m, L->v, L->params};
+  for (const void* q : {master2, m2, v2})
+    for (const void* o : mine)
+      if (q == o) return fail(ZERO_ERR_INVALID, "alternate state buffers must differ from the bound ones");
+  const int bps = spec_blocks_per_sm(L->cfg.grad_dtype, L->comm_dtype, L->cfg.param_dtype, L->world());
+  if (bps <= 0) return fail(ZERO_ERR_CUDA, "speculative kernel occupancy query failed");
+  int sms = 0;
+  ZERO_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, L->device));
+  L->grid_spec = std::max(1, std::min({(int)L->tiles.size(), sms * bps, kMaxPartials}));
+  L->master2 = static_cast<float*>(master2);
+  L->m2 = static_cast<float*>(m2);
+  L->v2 = static_cast<float*>(v2);
   L->initialized = false;
   return ZERO_OK;
 }
@@ -660,6 +746,21 @@ int zero_step(zero_layout_t* L, const void* const* grads, void* const* allreduce
     src.base[w] = grads[w];
   }
   return launch_step(L, src, allreduce_out, hp, static_cast<cudaStream_t>(stream));
+}
+
+int zero_step_speculative(zero_layout_t* L, const void* const* grads, const zero_hparams* hp,
+                          void* stream) {
+  if (int rc = check_ready(L, true)) return rc;
+  if (int rc = check_hparams(hp)) return rc;
+  if (L->master2 == nullptr) return fail(ZERO_ERR_STATE, "zero_state_bind_alternate has not been called");
+  if (grads == nullptr) return fail(ZERO_ERR_INVALID, "grads is NULL");
+  GradSrc src{};
+  for (int w = 0; w < L->world(); ++w) {
+    if (grads[w] == nullptr || !aligned16(grads[w]))
+      return fail(ZERO_ERR_INVALID, "grads[%d] is NULL or not 16-byte aligned", w);
+    src.base[w] = grads[w];
+  }
+  return launch_step_spec(L, src, hp, static_cast<cudaStream_t>(stream));
 }
 
 int zero_step_per_tensor_launch(zero_layout_t* L, const void* const* grads,
@@ -802,6 +903,8 @@ int zero_state_blob_decode(const void* blob, zero_scaler_state* out) {
   out->clip_coef = h.clip_coef;
   out->norm_sq_raw = h.norm_sq_raw;
   out->steps = h.steps;
+  out->state_set = h.cur;
+  out->fast_path = h.fast_path;
   if (h.error != 0)
     return fail(ZERO_ERR_TIMEOUT, "a kernel's bounded wait gave up (device error word %u)", h.error);
   return ZERO_OK;
@@ -814,18 +917,7 @@ int zero_loss_scale_state(zero_layout_t* L, void* stream, zero_scaler_state* out
   DevState h{};
   ZERO_CUDA(cudaMemcpyAsync(&h, L->d_state, sizeof(DevState), cudaMemcpyDeviceToHost, s));
   ZERO_CUDA(cudaStreamSynchronize(s));
-  out->scale = h.scale;
-  out->counter = h.counter;
-  out->t = h.t;
-  out->overflow = h.overflow;
-  out->skipped = h.skipped;
-  out->grad_norm = h.grad_norm;
-  out->clip_coef = h.clip_coef;
-  out->norm_sq_raw = h.norm_sq_raw;
-  out->steps = h.steps;
-  if (h.error != 0)
-    return fail(ZERO_ERR_TIMEOUT, "a kernel's bounded wait gave up (device error word %u)", h.error);
-  return ZERO_OK;
+  return zero_state_blob_decode(&h, out);
 }
 
 int zero_gather_params(zero_layout_t* L, void* const* dst, int n_replicas, void* stream) {
@@ -873,14 +965,18 @@ int zero_gather_bucket(zero_layout_t* L, int bucket, void* dst, void* stream) {
 static int state_copy(zero_layout_t* L, float* a, float* b, float* c, int dir, void* stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   float* flat[3] = {a, b, c};
-  float* shard[3] = {L->master, L->m, L->v};
+  float* sm[2];
+  float* sv1[2];
+  float* sv2[2];
+  state_sets(L, sm, sv1, sv2);
+  float* const* shard[3] = {sm, sv1, sv2};
   for (int k = 0; k < 3; ++k) {
     if (flat[k] == nullptr) continue;
     if (!aligned16(flat[k])) return fail(ZERO_ERR_INVALID, "state buffer not 16-byte aligned");
     if (dir == 0) ZERO_CUDA(cudaMemsetAsync(flat[k], 0, (size_t)L->np * 4, s));
     if (L->tiles.empty()) continue;
     cudaError_t e = launch_state_copy(L->d_tiles, (int)L->tiles.size(), shard[k], flat[k], dir,
-                                      L->grid_copy, s);
+                                      L->d_state, L->grid_copy, s);
     if (e != cudaSuccess) return cuda_fail(e, "state copy launch");
   }
   return ZERO_OK;
@@ -889,12 +985,16 @@ static int state_copy(zero_layout_t* L, float* a, float* b, float* c, int dir, v
 static int state_pm_copy(zero_layout_t* L, float* a, float* b, float* c, int dir, void* stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   float* pm[3] = {a, b, c};
-  float* shard[3] = {L->master, L->m, L->v};
+  float* sm[2];
+  float* sv1[2];
+  float* sv2[2];
+  state_sets(L, sm, sv1, sv2);
+  float* const* shard[3] = {sm, sv1, sv2};
   for (int k = 0; k < 3; ++k) {
     if (pm[k] == nullptr || L->tiles.empty()) continue;
     if (!aligned16(pm[k])) return fail(ZERO_ERR_INVALID, "state buffer not 16-byte aligned");
     cudaError_t e = launch_state_pm(L->d_tiles, (int)L->tiles.size(), L->d_pm_delta, shard[k], pm[k],
-                                    dir, L->grid_copy, s);
+                                    dir, L->d_state, L->grid_copy, s);
     if (e != cudaSuccess) return cuda_fail(e, "state copy launch");
   }
   return ZERO_OK;
@@ -914,8 +1014,12 @@ int zero_state_import_params(zero_layout_t* L, const float* master_pm, const flo
                              const_cast<float*>(v_pm), 1, stream))
     return rc;
   if (L->tiles.empty()) return ZERO_OK;
-  cudaError_t e = launch_recast(L->d_tiles, (int)L->tiles.size(), L->master, L->params,
-                                L->cfg.param_dtype, L->cfg.stage == 3, L->grid_copy,
+  float* sm[2];
+  float* sv1[2];
+  float* sv2[2];
+  state_sets(L, sm, sv1, sv2);
+  cudaError_t e = launch_recast(L->d_tiles, (int)L->tiles.size(), sm, L->params,
+                                L->cfg.param_dtype, L->cfg.stage == 3, L->d_state, 0, L->grid_copy,
                                 static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "recast launch");
   return ZERO_OK;

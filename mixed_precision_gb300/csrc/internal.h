@@ -53,6 +53,12 @@ struct DevState {
   float inv_sqrt_bc2;  // 1 / sqrt(1 - beta2^t)
   float beta1, one_minus_beta1, beta2, one_minus_beta2, eps;
   unsigned error;  // bit 0: a kernel's bounded wait gave up (reported as ZERO_ERR_TIMEOUT)
+  int cur;             // which bound state set holds the current master/m/v (0 or 1)
+  int need_fallback;   // speculative step: the two-pass step must run
+  int restore_params;  // speculative step overflowed: recast params from the master
+  int fast_path;       // last step was committed by the speculative single pass
+  int predict_fallback;  // the last finalized step clipped: the next speculative
+                         // step skips its single pass and runs the two-pass kernels
 };
 
 struct Hparams {  // mirror of zero_hparams
@@ -92,6 +98,8 @@ struct ReduceArgs {
   unsigned* part_ovf;   // [grid]
   int chunk;            // shared-memory pipeline: elements per stage
   unsigned* error;      // DevState::error
+  const DevState* state;
+  int guarded;          // 1: run only if state->need_fallback (the speculative step's fallback)
 };
 
 struct UpdateArgs {
@@ -100,9 +108,9 @@ struct UpdateArgs {
   int stage;
   int comm_dtype, param_dtype;
   RedBufs red;
-  float* master;
-  float* m;
-  float* v;
+  float* master[2];  // the two state sets; DevState::cur picks the current one
+  float* m[2];
+  float* v[2];
   void* params_flat;
   const DevState* state;
   unsigned* error;  // &state->error
@@ -118,16 +126,17 @@ int reduce_chunk(int world, int grad_dtype);  // elements per stage of the pipel
 cudaError_t launch_reduce(const ReduceArgs& a, int grid, int variant, cudaStream_t s);
 int reduce_blocks_per_sm(int grad_dtype, int comm_dtype, int world, int stage, int variant);
 cudaError_t launch_finalize(const double* part_sumsq, const unsigned* part_ovf, int n_part,
-                            int world, const Hparams& hp, DevState* st, cudaStream_t s);
+                            int world, const Hparams& hp, DevState* st, int guarded, cudaStream_t s);
 cudaError_t launch_update(const UpdateArgs& a, int grid, int variant, cudaStream_t s);
 int update_blocks_per_sm(int comm_dtype, int param_dtype, int variant);
 cudaError_t launch_state_init(const ScalerCfg& cfg, DevState* st, cudaStream_t s);
 cudaError_t launch_init_from_flat(const Tile* tiles, int n_tiles, const float* master_flat,
                                   float* master, void* params_flat, int param_dtype,
                                   int params_by_shard, int grid, cudaStream_t s);
-// dir 0: rank-major -> flat (export); 1: flat -> rank-major (import)
-cudaError_t launch_state_copy(const Tile* tiles, int n_tiles, float* shard_buf, float* flat_buf,
-                              int dir, int grid, cudaStream_t s);
+// dir 0: rank-major -> flat (export); 1: flat -> rank-major (import).
+// shard_buf: the two state sets' buffers; st->cur picks one.
+cudaError_t launch_state_copy(const Tile* tiles, int n_tiles, float* const* shard_buf, float* flat_buf,
+                              int dir, const DevState* st, int grid, cudaStream_t s);
 struct AccArgs {
   const void* micro[kMaxWorld];
   float* main[kMaxWorld];
@@ -139,14 +148,45 @@ struct AccArgs {
 };
 cudaError_t launch_accumulate(const AccArgs& a, int grid, cudaStream_t s);
 
+// The speculative single-pass step (k_spec.cuh).
+struct SpecArgs {  // arguments of k_spec_step
+  const Tile* tiles;
+  int n_tiles;
+  int world;
+  int stage;  // 2 or 3 (3: parameters sharded)
+  GradSrc src;
+  float* master[2];
+  float* m[2];
+  float* v[2];
+  void* params;
+  const DevState* state;
+  Hparams hp;
+  double* part_sumsq;
+  unsigned* part_ovf;
+  int chunk;
+  unsigned* error;
+};
+
+constexpr int kSpecStagesHost = 3;        // == kSpecStages
+constexpr int kSpecStageBytesHost = 32768;  // == kSpecStageBytes
+int spec_chunk(int world, int grad_dtype);
+cudaError_t launch_spec(const SpecArgs* args, int grad_dtype, int comm_dtype, int param_dtype, int world,
+                        int grid, cudaStream_t s);
+int spec_blocks_per_sm(int grad_dtype, int comm_dtype, int param_dtype, int world);
+cudaError_t launch_finalize_spec(const double* part_sumsq, const unsigned* part_ovf, int n_part,
+                                 int world, const Hparams& hp, DevState* st, cudaStream_t s);
+
 // Record a failure message for zero_last_error() and return `code` (for entry
 // points defined outside api.cpp).
 int zero_internal_fail(int code, const char* msg);
 
-cudaError_t launch_state_pm(const Tile* tiles, int n_tiles, const int64_t* pm_delta, float* shard_buf,
-                            float* pm_buf, int dir, int grid, cudaStream_t s);
-cudaError_t launch_recast(const Tile* tiles, int n_tiles, const float* master, void* params,
-                          int param_dtype, int params_by_shard, int grid, cudaStream_t s);
+cudaError_t launch_state_pm(const Tile* tiles, int n_tiles, const int64_t* pm_delta,
+                            float* const* shard_buf, float* pm_buf, int dir, const DevState* st,
+                            int grid, cudaStream_t s);
+// params <- RNE(current master); with `guarded`, only if st->restore_params.
+cudaError_t launch_recast(const Tile* tiles, int n_tiles, float* const* master, void* params,
+                          int param_dtype, int params_by_shard, const DevState* st, int guarded,
+                          int grid, cudaStream_t s);
 cudaError_t launch_gather_bucket(const Tile* tiles, int n_tiles, const void* shards, void* dst,
                                  int grid, cudaStream_t s);
 cudaError_t launch_scaler_restore(DevState* st, double scale, long long counter, long long t,

@@ -38,8 +38,9 @@ cudaError_t launch_init_from_flat(const Tile* tiles, int n_tiles, const float* m
 }
 
 __global__ void __launch_bounds__(kThreads)
-    k_state_copy(const Tile* __restrict__ tiles, int n_tiles, float* __restrict__ shard_buf,
-                 float* __restrict__ flat_buf, int dir) {
+    k_state_copy(const Tile* __restrict__ tiles, int n_tiles, float* shard0, float* shard1,
+                 float* __restrict__ flat_buf, int dir, const DevState* __restrict__ st) {
+  float* shard_buf = st->cur ? shard1 : shard0;
   for (int t = blockIdx.x; t < n_tiles; t += gridDim.x) {
     const Tile tl = tiles[t];
     for (int i = threadIdx.x; i < tl.len; i += kThreads) {
@@ -51,9 +52,10 @@ __global__ void __launch_bounds__(kThreads)
   }
 }
 
-cudaError_t launch_state_copy(const Tile* tiles, int n_tiles, float* shard_buf, float* flat_buf,
-                              int dir, int grid, cudaStream_t s) {
-  k_state_copy<<<grid, kThreads, 0, s>>>(tiles, n_tiles, shard_buf, flat_buf, dir);
+cudaError_t launch_state_copy(const Tile* tiles, int n_tiles, float* const* shard_buf, float* flat_buf,
+                              int dir, const DevState* st, int grid, cudaStream_t s) {
+  k_state_copy<<<grid, kThreads, 0, s>>>(tiles, n_tiles, shard_buf[0], shard_buf[1], flat_buf, dir,
+                                         st);
   return cudaGetLastError();
 }
 
@@ -95,7 +97,9 @@ namespace zg {
 // parameter-major start minus its flat offset). dir 0: export, 1: import.
 __global__ void __launch_bounds__(kThreads)
     k_state_pm(const Tile* __restrict__ tiles, int n_tiles, const int64_t* __restrict__ pm_delta,
-               float* __restrict__ shard_buf, float* __restrict__ pm_buf, int dir) {
+               float* shard0, float* shard1, float* __restrict__ pm_buf, int dir,
+               const DevState* __restrict__ st) {
+  float* shard_buf = st->cur ? shard1 : shard0;
   for (int t = blockIdx.x; t < n_tiles; t += gridDim.x) {
     const Tile tl = tiles[t];
     const int64_t pm0 = pm_delta[tl.param] + tl.flat;
@@ -108,17 +112,22 @@ __global__ void __launch_bounds__(kThreads)
   }
 }
 
-cudaError_t launch_state_pm(const Tile* tiles, int n_tiles, const int64_t* pm_delta, float* shard_buf,
-                            float* pm_buf, int dir, int grid, cudaStream_t s) {
-  k_state_pm<<<grid, kThreads, 0, s>>>(tiles, n_tiles, pm_delta, shard_buf, pm_buf, dir);
+cudaError_t launch_state_pm(const Tile* tiles, int n_tiles, const int64_t* pm_delta,
+                            float* const* shard_buf, float* pm_buf, int dir, const DevState* st,
+                            int grid, cudaStream_t s) {
+  k_state_pm<<<grid, kThreads, 0, s>>>(tiles, n_tiles, pm_delta, shard_buf[0], shard_buf[1], pm_buf,
+                                       dir, st);
   return cudaGetLastError();
 }
 
 // params_flat[flat + i] = RNE(master[shard + i]) over every tile.
 template <typename PT>
 __global__ void __launch_bounds__(kThreads)
-    k_recast(const Tile* __restrict__ tiles, int n_tiles, const float* __restrict__ master,
-             PT* __restrict__ params, int params_by_shard) {
+    k_recast(const Tile* __restrict__ tiles, int n_tiles, const float* master0,
+             const float* master1, PT* __restrict__ params, int params_by_shard,
+             const DevState* __restrict__ st, int guarded) {
+  if (guarded && !st->restore_params) return;
+  const float* master = st->cur ? master1 : master0;
   for (int t = blockIdx.x; t < n_tiles; t += gridDim.x) {
     const Tile tl = tiles[t];
     PT* pp = params + (params_by_shard ? tl.shard : tl.flat);
@@ -126,14 +135,17 @@ __global__ void __launch_bounds__(kThreads)
   }
 }
 
-cudaError_t launch_recast(const Tile* tiles, int n_tiles, const float* master, void* params,
-                          int param_dtype, int params_by_shard, int grid, cudaStream_t s) {
+cudaError_t launch_recast(const Tile* tiles, int n_tiles, float* const* master, void* params,
+                          int param_dtype, int params_by_shard, const DevState* st, int guarded,
+                          int grid, cudaStream_t s) {
   if (param_dtype == kF16)
-    k_recast<__half><<<grid, kThreads, 0, s>>>(tiles, n_tiles, master, static_cast<__half*>(params),
-                                               params_by_shard);
+    k_recast<__half><<<grid, kThreads, 0, s>>>(tiles, n_tiles, master[0], master[1],
+                                               static_cast<__half*>(params), params_by_shard, st,
+                                               guarded);
   else
     k_recast<__nv_bfloat16><<<grid, kThreads, 0, s>>>(
-        tiles, n_tiles, master, static_cast<__nv_bfloat16*>(params), params_by_shard);
+        tiles, n_tiles, master[0], master[1], static_cast<__nv_bfloat16*>(params), params_by_shard,
+        st, guarded);
   return cudaGetLastError();
 }
 

@@ -1,0 +1,255 @@
+// The speculative single-pass step.
+//
+// The two-pass step reads every gradient twice over (the reduce writes the
+// reduced gradient, the update reads it back) because clipping and the
+// overflow skip need the global norm before any update. When clipping turns
+// out inactive and nothing overflows, the clip coefficient is exactly 1, so
+// the update could have run in the same pass as the reduce. This pass does
+// exactly that, speculatively:
+//   - reduce the W ranks' gradients (same rounding as the reduce kernel),
+//     accumulate the norm partials and the overflow flag;
+//   - apply AdamW with clip 1 to the CURRENT state set and write the result
+//     to the OTHER set (the current one stays intact), and the cast
+//     parameters in place.
+// k_finalize_spec then commits (flips DevState::cur), skips (overflow: the
+// parameters are recast from the untouched master), or asks for the ordinary
+// two-pass step (clipping active), whose kernels run guarded on that flag.
+// A committed step is bit-identical to the two-pass step: same reduced
+// values, same scalars (derive_adam_scalars with clip 1), same update.
+// While the last finalized step clipped, the pass returns at once (the
+// finalize's predictor, k_update.cu) and costs one empty launch.
+// Bytes per element when it commits: 2W (grads) + 24 (state) + 2 (params).
+#pragma once
+
+#include "k_reduce.cuh"
+
+namespace zg {
+
+// Rank w's gradient pointer for a tile (flat buffers or the per-tensor table).
+template <typename GT>
+__device__ __forceinline__ const GT* spec_grad_ptr(const GradSrc& src, const Tile& tl, int w) {
+  if (src.table_mode) {
+    const void* q = src.table[(int64_t)w * src.n_params + tl.param];
+    return q ? static_cast<const GT*>(q) + tl.in_param : nullptr;
+  }
+  return static_cast<const GT*>(src.base[w]) + tl.flat;
+}
+
+constexpr int kSpecStages = kSpecStagesHost;
+constexpr int kSpecStageBytes = kSpecStageBytesHost;
+
+template <typename GT, typename CT, typename PT, int WT, int NC>
+__global__ void __launch_bounds__((NC + 1) * 32) k_spec_step(const __grid_constant__ SpecArgs a) {
+  constexpr int S = kSpecStages;
+  extern __shared__ __align__(128) unsigned char smem[];
+  __shared__ __align__(8) uint64_t full[S];
+  __shared__ __align__(8) uint64_t empty[S];
+  __shared__ double s_part[NC];
+  __shared__ unsigned s_flag[NC];
+  __shared__ unsigned s_done;
+  __shared__ AdamScalars s_sc;
+  const int W = WT ? WT : a.world;
+  const int C = a.chunk;
+  const int kGrad = W * C * (int)sizeof(GT);
+  const int kStage = kGrad + 12 * C;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const DevState* st = a.state;
+  if (st->predict_fallback) return;  // predicted to clip: the two-pass kernels run instead
+  const int cs = st->cur;
+  const float* src_master = a.master[cs];
+  const float* src_m = a.m[cs];
+  const float* src_v = a.v[cs];
+  float* dst_master = a.master[cs ^ 1];
+  float* dst_m = a.m[cs ^ 1];
+  float* dst_v = a.v[cs ^ 1];
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], NC);
+    }
+    s_done = 0u;
+    const double D = a.hp.grad_divisor > 0.0 ? a.hp.grad_divisor : (double)a.world;
+    const double inv = 1.0 / (st->scale * D);
+    s_sc = derive_adam_scalars(a.hp, inv, 1.0, st->t + 1);
+    mbar_init_fence();
+  }
+  __syncthreads();
+
+  if (warp == NC) {  // producer
+    if (lane != 0) return;
+    int pt = blockIdx.x, pc = 0;
+    unsigned k = 0;
+    bool ok = true;
+    while (pt < a.n_tiles) {
+      const int s = (int)(k % S);
+      if (k >= (unsigned)S && !mbar_wait(&empty[s], ((k / S) - 1) & 1u)) {
+        ok = false;
+        break;
+      }
+      const Tile tl = a.tiles[pt];
+      const int clen = min(C, tl.len - pc);
+      const int nb = clen & ~7;
+      unsigned char* base = smem + s * kStage;
+      if (nb > 0) {
+        mbar_arrive_expect_tx(&full[s], (uint32_t)nb * (uint32_t)(W * (int)sizeof(GT) + 12));
+        for (int w = 0; w < W; ++w)
+          bulk_g2s(base + w * C * (int)sizeof(GT), spec_grad_ptr<GT>(a.src, tl, w) + pc,
+                   nb * (int)sizeof(GT), &full[s]);
+        const int64_t so = tl.shard + pc;
+        bulk_g2s(base + kGrad, src_master + so, nb * 4, &full[s]);
+        bulk_g2s(base + kGrad + C * 4, src_m + so, nb * 4, &full[s]);
+        bulk_g2s(base + kGrad + C * 8, src_v + so, nb * 4, &full[s]);
+      } else {
+        mbar_arrive(&full[s]);
+      }
+      ++k;
+      pc += C;
+      if (pc >= tl.len) {
+        pc = 0;
+        pt += gridDim.x;
+      }
+    }
+    if (!ok) {
+      atomicOr(a.error, kErrWaitTimeout);
+      for (unsigned j = k > (unsigned)S ? k - S : 0u; j < k; ++j) mbar_wait(&full[j % S], (j / S) & 1u);
+    }
+    return;
+  }
+
+  const AdamScalars sc = s_sc;
+  const int per = ((C / NC) + 7) & ~7;
+  float hi = 0.0f, lo = 0.0f;
+  double big = 0.0;
+  unsigned bad = 0u;
+  int ct = blockIdx.x, cc = 0;
+  unsigned k = 0;
+  Tile tl = a.tiles[ct < a.n_tiles ? ct : 0];
+  while (ct < a.n_tiles) {
+    const int s = (int)(k % S);
+    const int clen = min(C, tl.len - cc);
+    const int nb = clen & ~7;
+    if (!__all_sync(0xffffffffu, mbar_wait(&full[s], (k / S) & 1u))) {
+      if (lane == 0) atomicOr(a.error, kErrWaitTimeout);
+      return;
+    }
+    const unsigned char* base = smem + s * kStage;
+    const GT* sg = reinterpret_cast<const GT*>(base);
+    const float* sp = reinterpret_cast<const float*>(base + kGrad);
+    const float* sm = reinterpret_cast<const float*>(base + kGrad + C * 4);
+    const float* sv = reinterpret_cast<const float*>(base + kGrad + C * 8);
+    const int64_t so = tl.shard + cc;
+    PT* pp = static_cast<PT*>(a.params) + (a.stage == 3 ? tl.shard : tl.flat) + cc;
+    const int e_end = min(nb, (warp + 1) * per);
+    for (int e = warp * per + 8 * lane; e < e_end; e += 256) {
+      float acc[8];
+      load8_smem(sg + e, acc);
+#pragma unroll(WT ? WT : 1)
+      for (int w = 1; w < W; ++w) {
+        float x[8];
+        load8_smem(sg + w * C + e, x);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[j] = __fadd_rn(acc[j], x[j]);
+      }
+      float rf[8], p[8], m[8], v[8];
+      float ss = 0.0f;
+      bool fin = true;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const CT rc = DT<CT>::from_f32(acc[j]);
+        rf[j] = DT<CT>::to_f32(rc);
+        fin = fin && DT<CT>::finite_bits(rc);
+        ss = __fmaf_rn(rf[j], rf[j], ss);
+      }
+      if (!fin) bad = 1u;
+      add_group(ss, hi, lo, big, rf);
+      load8_smem(sp + e, p);
+      load8_smem(sm + e, m);
+      load8_smem(sv + e, v);
+      Pack8<PT> q;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        sc.apply(rf[j], p[j], m[j], v[j]);
+        q.e[j] = DT<PT>::from_f32(p[j]);
+      }
+      store8_f32(dst_master + so + e, p);
+      store8_f32(dst_m + so + e, m);
+      store8_f32(dst_v + so + e, v);
+      store8_raw(pp + e, q);
+    }
+    if (warp == 0 && lane < clen - nb) {  // ragged tail, from global memory
+      const int e = nb + lane;
+      float sum = load1(spec_grad_ptr<GT>(a.src, tl, 0), (int64_t)cc + e);
+      for (int w = 1; w < W; ++w)
+        sum = __fadd_rn(sum, load1(spec_grad_ptr<GT>(a.src, tl, w), (int64_t)cc + e));
+      const CT rc = DT<CT>::from_f32(sum);
+      const float rf = DT<CT>::to_f32(rc);
+      if (!DT<CT>::finite_bits(rc)) bad = 1u;
+      big += (double)rf * (double)rf;
+      float p = src_master[so + e], m = src_m[so + e], v = src_v[so + e];
+      sc.apply(rf, p, m, v);
+      dst_master[so + e] = p;
+      dst_m[so + e] = m;
+      dst_v[so + e] = v;
+      pp[e] = DT<PT>::from_f32(p);
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);
+    ++k;
+    cc += C;
+    if (cc >= tl.len) {
+      cc = 0;
+      ct += gridDim.x;
+      if (ct < a.n_tiles) tl = a.tiles[ct];
+    }
+  }
+  double x = (double)hi + (double)lo + big;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x += __shfl_down_sync(0xffffffffu, x, o);
+  const unsigned any = __any_sync(0xffffffffu, bad != 0u) ? 1u : 0u;
+  if (lane == 0) {
+    s_part[warp] = x;
+    s_flag[warp] = any;
+    __threadfence_block();
+    if (atomicAdd(&s_done, 1u) == NC - 1) {
+      __threadfence_block();
+      double total = 0.0;
+      unsigned f = 0u;
+      for (int w = 0; w < NC; ++w) {
+        total += *reinterpret_cast<volatile double*>(&s_part[w]);
+        f |= *reinterpret_cast<volatile unsigned*>(&s_flag[w]);
+      }
+      a.part_sumsq[blockIdx.x] = total;
+      a.part_ovf[blockIdx.x] = f;
+    }
+  }
+}
+
+template <typename GT, typename CT, typename PT>
+const void* spec_kernel_w(int world) {
+  switch (world) {
+    case 2: return reinterpret_cast<const void*>(&k_spec_step<GT, CT, PT, 2, kRedConsumers>);
+    case 4: return reinterpret_cast<const void*>(&k_spec_step<GT, CT, PT, 4, kRedConsumers>);
+    case 8: return reinterpret_cast<const void*>(&k_spec_step<GT, CT, PT, 8, kRedConsumers>);
+    default: return reinterpret_cast<const void*>(&k_spec_step<GT, CT, PT, 0, kRedConsumers>);
+  }
+}
+
+template <typename GT, typename CT>
+const void* spec_kernel_p(int param_dtype, int world) {
+  return param_dtype == kF16 ? spec_kernel_w<GT, CT, __half>(world)
+                             : spec_kernel_w<GT, CT, __nv_bfloat16>(world);
+}
+
+// The kernel instance for (grad dtype GT, comm dtype, param dtype, world).
+template <typename GT>
+const void* spec_kernel_for(int comm_dtype, int param_dtype, int world) {
+  switch (comm_dtype) {
+    case kF32: return spec_kernel_p<GT, float>(param_dtype, world);
+    case kF16: return spec_kernel_p<GT, __half>(param_dtype, world);
+    case kBF16: return spec_kernel_p<GT, __nv_bfloat16>(param_dtype, world);
+    default: return nullptr;
+  }
+}
+
+}  // namespace zg

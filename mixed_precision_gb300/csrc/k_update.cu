@@ -72,7 +72,8 @@ int reduce_blocks_per_sm(int grad_dtype, int comm_dtype, int world, int stage, i
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kFinalizeThreads)
     k_finalize(const double* __restrict__ part_sumsq, const unsigned* __restrict__ part_ovf,
-               int n_part, int world, const Hparams hp, DevState* __restrict__ st) {
+               int n_part, int world, const Hparams hp, DevState* __restrict__ st, int guarded) {
+  if (guarded && !st->need_fallback) return;
   __shared__ double s_red[kFinalizeThreads / 32];
   __shared__ unsigned s_or[kFinalizeThreads / 32];
   double acc = 0.0;
@@ -89,6 +90,9 @@ __global__ void __launch_bounds__(kFinalizeThreads)
   const double D = hp.grad_divisor > 0.0 ? hp.grad_divisor : (double)world;
   const double inv = 1.0 / (S * D);
   st->steps += 1;
+  st->need_fallback = 0;
+  st->restore_params = 0;
+  st->fast_path = 0;
   st->norm_sq_raw = sumsq;
   st->grad_norm = inv * sqrt(sumsq);
   st->overflow = any ? 1 : 0;
@@ -111,18 +115,18 @@ __global__ void __launch_bounds__(kFinalizeThreads)
   st->skipped = 0;
   st->skip = 0;
   st->clip_coef = c;
+  st->predict_fallback = c < 1.0 ? 1 : 0;
   st->t += 1;
-  const double bc1 = 1.0 - pow(hp.beta1, (double)st->t);
-  const double bc2 = 1.0 - pow(hp.beta2, (double)st->t);
-  st->gscale = (float)(inv * c);
-  st->decay = (float)(1.0 - hp.lr * hp.weight_decay);
-  st->step_size = (float)(hp.lr / bc1);
-  st->inv_sqrt_bc2 = (float)(1.0 / sqrt(bc2));
-  st->beta1 = (float)hp.beta1;
-  st->one_minus_beta1 = (float)(1.0 - hp.beta1);
-  st->beta2 = (float)hp.beta2;
-  st->one_minus_beta2 = (float)(1.0 - hp.beta2);
-  st->eps = (float)hp.eps;
+  const AdamScalars a = derive_adam_scalars(hp, inv, c, st->t);
+  st->gscale = a.gs;
+  st->decay = a.decay;
+  st->step_size = a.step;
+  st->inv_sqrt_bc2 = a.isb2;
+  st->beta1 = a.b1;
+  st->one_minus_beta1 = a.omb1;
+  st->beta2 = a.b2;
+  st->one_minus_beta2 = a.omb2;
+  st->eps = a.eps;
   st->counter += 1;
   if (st->dynamic && st->counter == st->growth_interval) {
     st->scale = S * st->growth_factor;
@@ -131,8 +135,8 @@ __global__ void __launch_bounds__(kFinalizeThreads)
 }
 
 cudaError_t launch_finalize(const double* part_sumsq, const unsigned* part_ovf, int n_part,
-                            int world, const Hparams& hp, DevState* st, cudaStream_t s) {
-  k_finalize<<<1, kFinalizeThreads, 0, s>>>(part_sumsq, part_ovf, n_part, world, hp, st);
+                            int world, const Hparams& hp, DevState* st, int guarded, cudaStream_t s) {
+  k_finalize<<<1, kFinalizeThreads, 0, s>>>(part_sumsq, part_ovf, n_part, world, hp, st, guarded);
   return cudaGetLastError();
 }
 
@@ -169,27 +173,20 @@ template <typename CT, typename PT>
 __global__ void __launch_bounds__(kThreads) k_adamw_cast(const __grid_constant__ UpdateArgs a) {
   const DevState* st = a.state;
   if (st->skip) return;
-  const float gs = st->gscale, decay = st->decay, step = st->step_size;
-  const float isb2 = st->inv_sqrt_bc2, eps = st->eps;
-  const float b1 = st->beta1, omb1 = st->one_minus_beta1;
-  const float b2 = st->beta2, omb2 = st->one_minus_beta2;
-
-  auto adam = [&](float r, float& p, float& m, float& v) {
-    const float g = r * gs;
-    p = p * decay;
-    m = b1 * m + omb1 * g;
-    v = b2 * v + omb2 * (g * g);
-    const float denom = sqrtf(v) * isb2 + eps;
-    p = p - step * (m / denom);
-  };
+  const AdamScalars sc = AdamScalars::from(st);
+  auto adam = [&](float r, float& p, float& m, float& v) { sc.apply(r, p, m, v); };
+  const int cs = st->cur;
+  float* const s_master = a.master[cs];
+  float* const s_m = a.m[cs];
+  float* const s_v = a.v[cs];
 
   for (int t = blockIdx.x; t < a.n_tiles; t += gridDim.x) {
     const Tile tl = a.tiles[t];
     const CT* red = a.stage == 1 ? static_cast<const CT*>(a.red.base[tl.rank]) + tl.flat
                                  : static_cast<const CT*>(a.red.base[0]) + tl.shard;
-    float* mp = a.master + tl.shard;
-    float* m1 = a.m + tl.shard;
-    float* v1 = a.v + tl.shard;
+    float* mp = s_master + tl.shard;
+    float* m1 = s_m + tl.shard;
+    float* v1 = s_v + tl.shard;
     // stage 3 keeps the parameters sharded (rank-major, like master)
     PT* pp = static_cast<PT*>(a.params_flat) + (a.stage == 3 ? tl.shard : tl.flat);
     const int nvec = tl.len >> 3;
@@ -259,6 +256,10 @@ __global__ void __launch_bounds__((NC + 1) * 32)
   const DevState* st = a.state;
   if (st->skip) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int cs = st->cur;
+  float* const s_master = a.master[cs];
+  float* const s_m = a.m[cs];
+  float* const s_v = a.v[cs];
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
@@ -291,9 +292,9 @@ __global__ void __launch_bounds__((NC + 1) * 32)
       if (nb > 0) {
         mbar_arrive_expect_tx(&full[s], (uint32_t)nb * (12u + (uint32_t)sizeof(CT)));
         const int64_t so = tl.shard + pc;
-        bulk_g2s(base, a.master + so, nb * 4, &full[s]);
-        bulk_g2s(base + C * 4, a.m + so, nb * 4, &full[s]);
-        bulk_g2s(base + C * 8, a.v + so, nb * 4, &full[s]);
+        bulk_g2s(base, s_master + so, nb * 4, &full[s]);
+        bulk_g2s(base + C * 4, s_m + so, nb * 4, &full[s]);
+        bulk_g2s(base + C * 8, s_v + so, nb * 4, &full[s]);
         bulk_g2s(base + C * 12, red_ptr(tl) + pc, nb * (int)sizeof(CT), &full[s]);
       } else {
         mbar_arrive(&full[s]);
@@ -312,18 +313,8 @@ __global__ void __launch_bounds__((NC + 1) * 32)
     return;
   }
 
-  const float gs = st->gscale, decay = st->decay, step = st->step_size;
-  const float isb2 = st->inv_sqrt_bc2, eps = st->eps;
-  const float b1 = st->beta1, omb1 = st->one_minus_beta1;
-  const float b2 = st->beta2, omb2 = st->one_minus_beta2;
-  auto adam = [&](float r, float& p, float& m, float& v) {
-    const float g = r * gs;
-    p = p * decay;
-    m = b1 * m + omb1 * g;
-    v = b2 * v + omb2 * (g * g);
-    const float denom = sqrtf(v) * isb2 + eps;
-    p = p - step * (m / denom);
-  };
+  const AdamScalars sc = AdamScalars::from(st);
+  auto adam = [&](float r, float& p, float& m, float& v) { sc.apply(r, p, m, v); };
 
   int ct = blockIdx.x, cc = 0;
   unsigned k = 0;
@@ -356,20 +347,20 @@ __global__ void __launch_bounds__((NC + 1) * 32)
       adam(r[1], p.y, m.y, v.y);
       adam(r[2], p.z, m.z, v.z);
       adam(r[3], p.w, m.w, v.w);
-      __stcs(reinterpret_cast<float4*>(a.master + so + e), p);
-      __stcs(reinterpret_cast<float4*>(a.m + so + e), m);
-      __stcs(reinterpret_cast<float4*>(a.v + so + e), v);
+      __stcs(reinterpret_cast<float4*>(s_master + so + e), p);
+      __stcs(reinterpret_cast<float4*>(s_m + so + e), m);
+      __stcs(reinterpret_cast<float4*>(s_v + so + e), v);
       PT q[4] = {DT<PT>::from_f32(p.x), DT<PT>::from_f32(p.y), DT<PT>::from_f32(p.z),
                  DT<PT>::from_f32(p.w)};
       __stcs(reinterpret_cast<uint2*>(pp + e), *reinterpret_cast<const uint2*>(q));
     }
     if (warp == 0 && lane < clen - nb) {
       const int e = nb + lane;
-      float p = a.master[so + e], m = a.m[so + e], v = a.v[so + e];
+      float p = s_master[so + e], m = s_m[so + e], v = s_v[so + e];
       adam(DT<CT>::to_f32(red_ptr(tl)[cc + e]), p, m, v);
-      a.master[so + e] = p;
-      a.m[so + e] = m;
-      a.v[so + e] = v;
+      s_master[so + e] = p;
+      s_m[so + e] = m;
+      s_v[so + e] = v;
       pp[e] = DT<PT>::from_f32(p);
     }
     __syncwarp();
@@ -438,6 +429,160 @@ int update_blocks_per_sm(int comm_dtype, int param_dtype, int variant) {
     return 0;
   int n = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, f, update_threads(variant), smem) !=
+      cudaSuccess)
+    return 0;
+  return n;
+}
+
+}  // namespace zg
+
+namespace zg {
+
+// ---------------------------------------------------------------------------
+// The speculative step's finalize and launch (see k_spec.cuh). Same sums and
+// norm as k_finalize; then:
+//   overflow      -> skip (as k_finalize) and recast the params, which the
+//                    speculative pass overwrote, from the untouched master;
+//   clip active   -> ask for the two-pass step (need_fallback), no bookkeeping;
+//   otherwise     -> commit: the other state set becomes current, t += 1, the
+//                    scaler counts a clean step; the update kernel is skipped.
+// A one-bit predictor saves the wasted pass while clipping stays active: every
+// finalize records whether its step clipped (DevState::predict_fallback), and
+// while it is set the single pass returns at once and this kernel goes
+// straight to the two-pass kernels. Only the step on which clipping switches
+// on runs both.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kFinalizeThreads)
+    k_finalize_spec(const double* __restrict__ part_sumsq, const unsigned* __restrict__ part_ovf,
+                    int n_part, int world, const Hparams hp, DevState* __restrict__ st) {
+  if (st->predict_fallback) {  // the single pass did not run: go to the two-pass kernels
+    if (threadIdx.x == 0) {
+      st->need_fallback = 1;
+      st->restore_params = 0;
+      st->fast_path = 0;
+      st->skip = 1;
+    }
+    return;
+  }
+  __shared__ double s_red[kFinalizeThreads / 32];
+  __shared__ unsigned s_or[kFinalizeThreads / 32];
+  double acc = 0.0;
+  unsigned ovf = 0u;
+  for (int i = threadIdx.x; i < n_part; i += kFinalizeThreads) {
+    acc += part_sumsq[i];
+    ovf |= part_ovf[i];
+  }
+  const double sumsq = block_sum<kFinalizeThreads>(acc, s_red);
+  const unsigned any = block_or<kFinalizeThreads>(ovf, s_or);
+  if (threadIdx.x != 0) return;
+
+  const double S = st->scale;
+  const double D = hp.grad_divisor > 0.0 ? hp.grad_divisor : (double)world;
+  const double inv = 1.0 / (S * D);
+  st->need_fallback = 0;
+  st->restore_params = 0;
+  st->fast_path = 0;
+  st->norm_sq_raw = sumsq;
+  st->grad_norm = inv * sqrt(sumsq);
+  st->overflow = any ? 1 : 0;
+  if (any) {
+    st->steps += 1;
+    st->skipped = 1;
+    st->skip = 1;
+    st->clip_coef = 0.0;
+    st->restore_params = 1;
+    if (st->dynamic) {
+      const double s2 = S * st->backoff_factor;
+      st->scale = s2 < st->min_scale ? st->min_scale : s2;
+    }
+    st->counter = 0;
+    return;
+  }
+  double c = 1.0;
+  if (hp.max_grad_norm > 0.0) {
+    c = hp.max_grad_norm / (st->grad_norm + 1e-6);
+    if (c > 1.0) c = 1.0;
+  }
+  if (c < 1.0) {  // clipping active: the guarded two-pass kernels redo the step
+    st->need_fallback = 1;
+    st->skip = 1;
+    st->predict_fallback = 1;
+    return;
+  }
+  st->steps += 1;
+  st->skipped = 0;
+  st->skip = 1;  // the update already happened
+  st->clip_coef = 1.0;
+  st->t += 1;
+  st->cur ^= 1;
+  st->fast_path = 1;
+  const AdamScalars a = derive_adam_scalars(hp, inv, 1.0, st->t);
+  st->gscale = a.gs;
+  st->decay = a.decay;
+  st->step_size = a.step;
+  st->inv_sqrt_bc2 = a.isb2;
+  st->beta1 = a.b1;
+  st->one_minus_beta1 = a.omb1;
+  st->beta2 = a.b2;
+  st->one_minus_beta2 = a.omb2;
+  st->eps = a.eps;
+  st->counter += 1;
+  if (st->dynamic && st->counter == st->growth_interval) {
+    st->scale = S * st->growth_factor;
+    st->counter = 0;
+  }
+}
+
+cudaError_t launch_finalize_spec(const double* part_sumsq, const unsigned* part_ovf, int n_part,
+                                 int world, const Hparams& hp, DevState* st, cudaStream_t s) {
+  k_finalize_spec<<<1, kFinalizeThreads, 0, s>>>(part_sumsq, part_ovf, n_part, world, hp, st);
+  return cudaGetLastError();
+}
+
+const void* spec_kernel_f32(int comm_dtype, int param_dtype, int world);
+const void* spec_kernel_f16(int comm_dtype, int param_dtype, int world);
+const void* spec_kernel_bf16(int comm_dtype, int param_dtype, int world);
+
+static const void* spec_kernel(int grad_dtype, int comm_dtype, int param_dtype, int world) {
+  switch (grad_dtype) {
+    case kF32: return spec_kernel_f32(comm_dtype, param_dtype, world);
+    case kF16: return spec_kernel_f16(comm_dtype, param_dtype, world);
+    case kBF16: return spec_kernel_bf16(comm_dtype, param_dtype, world);
+    default: return nullptr;
+  }
+}
+
+// Elements per stage: the W ranks' gradient slices plus 12 bytes of state per
+// element fill about kSpecStageBytes; a multiple of 128 elements, at least 128.
+int spec_chunk(int world, int grad_dtype) {
+  const int g = grad_dtype == kF32 ? 4 : 2;
+  int c = kSpecStageBytesHost / (world * g + 12);
+  c &= ~127;
+  return c < 128 ? 128 : c;
+}
+
+static int spec_smem(int world, int grad_dtype) {
+  const int g = grad_dtype == kF32 ? 4 : 2;
+  return kSpecStagesHost * spec_chunk(world, grad_dtype) * (world * g + 12);
+}
+
+cudaError_t launch_spec(const SpecArgs* args, int grad_dtype, int comm_dtype, int param_dtype, int world,
+                        int grid, cudaStream_t s) {
+  const void* f = spec_kernel(grad_dtype, comm_dtype, param_dtype, world);
+  if (f == nullptr) return cudaErrorInvalidValue;
+  void* a[] = {const_cast<SpecArgs*>(args)};
+  return cudaLaunchKernel(f, dim3(grid), dim3((kRedConsumers + 1) * 32), a,
+                          spec_smem(world, grad_dtype), s);
+}
+
+int spec_blocks_per_sm(int grad_dtype, int comm_dtype, int param_dtype, int world) {
+  const void* f = spec_kernel(grad_dtype, comm_dtype, param_dtype, world);
+  if (f == nullptr) return 0;
+  const int smem = spec_smem(world, grad_dtype);
+  if (cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+    return 0;
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, f, (kRedConsumers + 1) * 32, smem) !=
       cudaSuccess)
     return 0;
   return n;

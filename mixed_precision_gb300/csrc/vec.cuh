@@ -141,6 +141,51 @@ __device__ __forceinline__ void store8_f32(float* p, const float (&x)[8]) {
                               __float_as_uint(x[7])));
 }
 
+// ---- the element-wise AdamW update ----------------------------------------
+// One fixed sequence of correctly rounded fp32 operations (explicit
+// intrinsics, so no kernel's compiler contracts it differently): every
+// update kernel produces the same bits for the same inputs and scalars.
+//   g = r * gscale;  p *= decay;  m = b1 m + (1-b1) g;  v = b2 v + (1-b2) g^2;
+//   p -= step * m / (sqrt(v) * inv_sqrt_bc2 + eps)
+struct AdamScalars {
+  float gs, decay, step, isb2, eps, b1, omb1, b2, omb2;
+
+  __device__ static AdamScalars from(const DevState* st) {
+    return AdamScalars{st->gscale, st->decay, st->step_size, st->inv_sqrt_bc2, st->eps,
+                       st->beta1, st->one_minus_beta1, st->beta2, st->one_minus_beta2};
+  }
+
+  __device__ __forceinline__ void apply(float r, float& p, float& m, float& v) const {
+    const float g = __fmul_rn(r, gs);
+    p = __fmul_rn(p, decay);
+    m = __fmaf_rn(b1, m, __fmul_rn(omb1, g));
+    v = __fmaf_rn(b2, v, __fmul_rn(omb2, __fmul_rn(g, g)));
+    const float denom = __fmaf_rn(__fsqrt_rn(v), isb2, eps);
+    p = __fmaf_rn(-step, __fdiv_rn(m, denom), p);
+  }
+};
+
+// The per-step fp32 scalars of the update, derived in fp64 from the scale's
+// inverse `inv` = 1/(S*D), the clip coefficient and the step count t of the
+// update. The finalize kernel and the speculative pass both use this, so the
+// two produce identical scalars.
+__device__ __forceinline__ AdamScalars derive_adam_scalars(const Hparams& hp, double inv, double c,
+                                                          long long t) {
+  const double bc1 = 1.0 - pow(hp.beta1, (double)t);
+  const double bc2 = 1.0 - pow(hp.beta2, (double)t);
+  AdamScalars s;
+  s.gs = (float)(inv * c);
+  s.decay = (float)(1.0 - hp.lr * hp.weight_decay);
+  s.step = (float)(hp.lr / bc1);
+  s.isb2 = (float)(1.0 / sqrt(bc2));
+  s.eps = (float)hp.eps;
+  s.b1 = (float)hp.beta1;
+  s.omb1 = (float)(1.0 - hp.beta1);
+  s.b2 = (float)hp.beta2;
+  s.omb2 = (float)(1.0 - hp.beta2);
+  return s;
+}
+
 // ---- deterministic block reductions (fixed shuffle tree, fixed warp order) --
 
 template <int kBlock>

@@ -59,9 +59,10 @@ class ZeroStep:
         self._bound = False
 
     # ---- buffers ------------------------------------------------------------
-    def allocate(self) -> None:
+    def allocate(self, speculative: bool = False) -> None:
         """Allocate master/m/v, the flat params, the stage-2 scratch or the
-        stage-1 all-reduce outputs, and bind them."""
+        stage-1 all-reduce outputs, and bind them; with `speculative`, also a
+        second master/m/v set for step_speculative (stages 2 and 3)."""
         dev = self.device
         n = max(self.np, 8)  # an empty model still gets non-NULL buffers
         self.master = torch.empty(n, dtype=torch.float32, device=dev)
@@ -76,6 +77,19 @@ class ZeroStep:
             self.allreduce_out = [torch.empty(n, dtype=TORCH_DTYPE[self.comm_dtype], device=dev)
                                   for _ in range(self.world)]
         self.bind(self.master, self.m, self.v, self.params_flat, self.scratch)
+        if speculative:
+            self.bind_alternate(*[torch.empty(n, dtype=torch.float32, device=dev) for _ in range(3)])
+
+    def bind_alternate(self, master2, m2, v2) -> None:
+        """Bind the second master/m/v set (before init)."""
+        abi.zero_state_bind_alternate(self.handle, master2.data_ptr(), m2.data_ptr(), v2.data_ptr())
+        self.master2, self.m2, self.v2 = master2, m2, v2
+
+    def current_state(self, stream=None):
+        """(master, m, v) of the state set that holds the current state."""
+        if self.scaler_state(stream)["state_set"] == 1:
+            return self.master2, self.m2, self.v2
+        return self.master, self.m, self.v
 
     def bind(self, master, m, v, params_flat, scratch=None) -> None:
         abi.zero_state_bind(self.handle, master.data_ptr(), m.data_ptr(), v.data_ptr(),
@@ -110,6 +124,12 @@ class ZeroStep:
             outs = allreduce_out if allreduce_out is not None else self.allreduce_out
             ar = [t.data_ptr() for t in outs]
         abi.zero_step(self.handle, [g.data_ptr() for g in grads], ar, hp.c(), _stream_handle(stream))
+
+    def step_speculative(self, grads, hp: Hparams, stream=None) -> None:
+        """The step as one pass when clipping stays inactive and nothing
+        overflows (bit-identical to step); otherwise skip or two-pass fallback."""
+        abi.zero_step_speculative(self.handle, [g.data_ptr() for g in grads], hp.c(),
+                                  _stream_handle(stream))
 
     def step_per_tensor_launch(self, grads, hp: Hparams, stream=None) -> None:
         """The same step launched tensor by tensor (the hook-style baseline)."""

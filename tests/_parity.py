@@ -35,7 +35,8 @@ def same_bits_or_both_nan(a: np.ndarray, b: np.ndarray, dtype: int) -> bool:
 
 class Pair:
     def __init__(self, shapes, world, stage, bucket_bytes, grad_dtype, param_dtype, comm_dtype=-1,
-                 init_scale=1.0, dynamic=False, growth_interval=1000, index=9, master_sigma=0.02):
+                 init_scale=1.0, dynamic=False, growth_interval=1000, index=9, master_sigma=0.02,
+                 speculative=False):
         self.shapes = shapes
         self.numel = wl.numels(shapes)
         self.W, self.stage, self.bucket = world, stage, bucket_bytes
@@ -43,7 +44,8 @@ class Pair:
         self.cdt = grad_dtype if comm_dtype < 0 else comm_dtype
         self.index = index
         self.z = ZeroStep(shapes, world, stage, bucket_bytes, grad_dtype, param_dtype, comm_dtype)
-        self.z.allocate()
+        self.z.allocate(speculative=speculative)
+        self.last_mode = None
         self.L = oracle.layout(self.numel, world, bucket_bytes, wl.ELEM_BYTES[grad_dtype])
         assert self.z.np == self.L.np_total
         self.np = self.L.np_total
@@ -100,12 +102,15 @@ class Pair:
             self.z.step_tensors(per, hp)
         elif mode == "per_tensor_launch":
             self.z.step_per_tensor_launch(dev, hp)
+        elif mode == "speculative":
+            self.z.step_speculative(dev, hp)
         elif mode == "host":
             pinned = [(g if g.numel() else torch.empty(8, dtype=g.dtype)).pin_memory()
                       for g in grads_cpu]
             self.z.step_host(pinned, dev, hp)
         else:
             raise ValueError(mode)
+        self.last_mode = mode
         torch.cuda.synchronize()
         gpu_state = self.z.scaler_state()
         o_hp = oracle.Hparams(hp.lr, hp.beta1, hp.beta2, hp.eps, hp.weight_decay, hp.max_grad_norm,
@@ -138,8 +143,13 @@ class Pair:
             assert abs(gpu_state["grad_norm"] - info.grad_norm) <= 1e-6 * max(info.grad_norm, 1e-300)
         if not info.skipped:
             assert abs(gpu_state["clip_coef"] - info.clip_coef) <= 1e-6 * info.clip_coef
-        # reduced values: bit-exact
-        if self.stage != 1:
+        # reduced values: bit-exact (a committed or skipped speculative step
+        # never stores them; its fallback does)
+        spec_no_reduce = self.last_mode == "speculative" and (gpu_state["fast_path"] or
+                                                             gpu_state["skipped"])
+        if spec_no_reduce:
+            pass
+        elif self.stage != 1:
             got = to_np(self.z.scratch)[:self.np]
             exp = np.zeros(self.np, oracle.storage_dtype(self.cdt))
             gn = [to_np(g) for g in grads_cpu]
@@ -152,7 +162,9 @@ class Pair:
                 assert same_bits_or_both_nan(got[self.mask_flat], self.o_out[w][self.mask_flat],
                                              self.cdt)
         worst = 0.0
-        for name, gpu_t, ref, hist in zip(("master", "m", "v"), (self.z.master, self.z.m, self.z.v),
+        cur = self.z.current_state() if hasattr(self.z, "master2") else (self.z.master, self.z.m,
+                                                                        self.z.v)
+        for name, gpu_t, ref, hist in zip(("master", "m", "v"), cur,
                                           (self.o_master, self.o_m, self.o_v), self.hist):
             got = to_np(gpu_t)[:self.np][self.mask_shard]
             r, h = ref[self.mask_shard], hist[self.mask_shard]

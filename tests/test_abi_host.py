@@ -155,6 +155,13 @@ def test_invalid_arguments(zlib):
     with pytest.raises(zlib.ZeroError) as e:
         zlib.zero_step(h, [16, 32], None, hp, 0)
     assert e.value.code == 5
+    # the speculative step's entry points are out of order before bind too
+    with pytest.raises(zlib.ZeroError) as e:
+        zlib.zero_state_bind_alternate(h, 16, 32, 48)
+    assert e.value.code == 5
+    with pytest.raises(zlib.ZeroError) as e:
+        zlib.zero_step_speculative(h, [16, 32], hp, 0)
+    assert e.value.code == 5
     zlib.zero_layout_destroy(h)
 
 

@@ -1,0 +1,281 @@
+"""The speculative single-pass step against the oracle and against the
+two-pass step.
+
+zero_step_speculative runs reduce + norm + AdamW (clip coefficient 1) in one
+kernel into the state set that is not current, then decides on the device:
+commit (flip the current set), skip (overflow: parameters restored from the
+untouched master) or fall back (clipping active: the two-pass kernels run).
+Checked here:
+  - every branch against the oracle (the Pair harness, same criteria as the
+    two-pass parity tests), with the branch taken asserted from the report;
+  - commits bit-identical to zero_step on the same inputs (master, m, v and
+    parameters; the norm within the parity tolerance, since the single pass
+    sums it in another grouping), interleaved with two-pass steps on the same
+    layout, in stages 2 and 3, every supported world-size path and dtype mix;
+  - export/import and gathers follow the current set;
+  - nothing is written outside the caller's buffers, alternate set included.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import workloads as wl
+from _parity import INF_BITS, Pair, to_np
+from mixed_precision_gb300 import ZeroError
+from mixed_precision_gb300 import _abi as abi
+from mixed_precision_gb300.engine import Hparams, ZeroStep
+
+pytestmark = pytest.mark.gpu
+
+SCALAR_KEYS = ("scale", "counter", "t", "overflow", "skipped", "clip_coef", "steps")
+
+
+def small_qwen_shapes():
+    return wl.qwen3_0_6b_shapes(vocab=1000, hidden=128, layers=2, q_dim=256, kv_dim=128, ffn=384,
+                                head_dim=32)
+
+
+def ragged_shapes(seed):
+    rng = np.random.default_rng(seed)
+    sizes = [1, 0, 7, 63, 64, 65, 129, 8191, 8193, 20000, 3, 1]
+    sizes += [int(x) for x in rng.integers(1, 3000, size=10)]
+    return [(s,) for s in sizes]
+
+
+@pytest.mark.parametrize("W,stage,gdt,cdt,pdt,bucket", [
+    (2, 2, wl.BF16, -1, wl.BF16, 64_000),
+    (2, 3, wl.BF16, -1, wl.BF16, 64_000),
+    (4, 2, wl.F16, wl.F32, wl.F16, 200_000),
+    (8, 3, wl.F16, -1, wl.F16, 500_000_000),
+    (3, 2, wl.BF16, -1, wl.F16, 30_000),
+    (5, 2, wl.F32, wl.BF16, wl.BF16, 100_000),
+    (1, 2, wl.F16, -1, wl.F16, 50_000),
+])
+def test_every_branch_matches_oracle(W, stage, gdt, cdt, pdt, bucket):
+    """Commit, overflow skip, clip fallback, and commits again, against the oracle."""
+    pr = Pair(small_qwen_shapes(), W, stage, bucket, gdt, pdt, cdt, init_scale=8.0, dynamic=True,
+              growth_interval=3, index=300 + W, speculative=True)
+    rank, idx = wl.inject_position(pr.numel, pr.z.offsets, W, seed=W)
+    bits = INF_BITS.get(gdt)
+    # "fallback": clipping switches on (single pass wasted); "predicted": the
+    # last step clipped, so the single pass is not attempted (two-pass kernels)
+    clip = Hparams(lr=3e-4, weight_decay=0.1, max_grad_norm=1e-3)
+    plan = [("commit", Hparams()), ("commit", Hparams(max_grad_norm=0.0, grad_divisor=1.0)),
+            ("skip", Hparams()), ("fallback", clip), ("predicted", clip),
+            ("predicted", Hparams()), ("commit", Hparams(weight_decay=0.0))]
+    sets = []
+    for step, (kind, hp) in enumerate(plan):
+        inj = [(rank, idx, bits)] if kind == "skip" and bits is not None else None
+        g = pr.grads(step, 1e-3, inject=inj)
+        if kind == "skip" and bits is None:  # fp32 gradients: an inf in the f32 buffer
+            g[rank][idx] = float("inf")
+        st, info, gc = pr.step(g, hp, mode="speculative")
+        pr.check(st, info, gc)
+        assert st["fast_path"] == (kind == "commit"), (step, kind, st)
+        assert st["skipped"] == (kind == "skip")
+        if kind == "fallback" or (kind == "predicted" and hp is clip):
+            assert st["clip_coef"] < 1.0
+        sets.append(st["state_set"])
+    # the current set flips on commits only
+    assert sets == [1, 0, 0, 0, 0, 0, 1]
+
+
+def _twin(shapes, W, stage, bucket, gdt, pdt, cdt=-1, init_scale=8.0, seed=5):
+    """Two layouts with identical initial state: one speculative, one two-pass."""
+    zs = []
+    for spec in (True, False):
+        z = ZeroStep(shapes, W, stage, bucket, gdt, pdt, cdt)
+        z.allocate(speculative=spec)
+        master0 = wl.master_init(z.offsets, z.numels, z.np, 0.02, wl.master_seed(seed),
+                                 device="cuda") if z.np else torch.zeros(8, device="cuda")
+        z.init(master0, init_scale=init_scale, dynamic=True, growth_interval=2)
+        zs.append(z)
+    return zs
+
+
+def _real_shard_mask(z):
+    mask = torch.zeros(max(z.np, 8), dtype=torch.bool, device="cuda")
+    for b in range(z.info.n_buckets):
+        for r in range(z.world):
+            f0, s0, ln = abi.zero_shard_range(z.handle, b, r)
+            for off, n in zip(z.offsets, z.numels):
+                a, e = max(off, f0), min(off + n, f0 + ln)
+                if a < e:
+                    mask[s0 + a - f0:s0 + e - f0] = True
+    return mask
+
+
+def _assert_same(a, b, mask):
+    sa, sb = a.scaler_state(), b.scaler_state()
+    for k in SCALAR_KEYS:
+        assert sa[k] == sb[k], (k, sa, sb)
+    if math.isfinite(sb["grad_norm"]):
+        assert abs(sa["grad_norm"] - sb["grad_norm"]) <= 1e-6 * max(sb["grad_norm"], 1e-300)
+    for x, y in zip(a.current_state(), b.current_state()):
+        assert torch.equal(x[mask].view(torch.int32), y[mask].view(torch.int32))
+    assert torch.equal(a.params_flat.view(torch.int16), b.params_flat.view(torch.int16))
+    return sa
+
+
+@pytest.mark.parametrize("W,stage,gdt,pdt,cdt,shapes", [
+    (2, 2, wl.BF16, wl.BF16, -1, "qwen"),
+    (4, 3, wl.BF16, wl.BF16, -1, "qwen"),
+    (8, 2, wl.F16, wl.F16, -1, "qwen"),
+    (3, 3, wl.BF16, wl.F16, -1, "ragged"),
+    (16, 2, wl.BF16, wl.BF16, -1, "ragged"),
+    (4, 2, wl.F32, wl.BF16, wl.BF16, "ragged"),
+])
+def test_bit_identical_to_two_pass(W, stage, gdt, pdt, cdt, shapes):
+    """The same inputs through both entry points, speculative steps
+    interleaved with two-pass ones on the speculative layout."""
+    sh = small_qwen_shapes() if shapes == "qwen" else ragged_shapes(W)
+    a, b = _twin(sh, W, stage, 60_000, gdt, pdt, cdt, seed=W)
+    mask = _real_shard_mask(a)
+    numel = wl.numels(sh)
+    rank, idx = wl.inject_position(numel, a.offsets, W, seed=11)
+    kinds = ["spec", "spec", "two", "spec", "spec-inf", "spec-clip", "spec-clip", "spec", "two",
+             "spec", "spec"]
+    fast = []
+    for step, kind in enumerate(kinds):
+        grads = [wl.flat_grads(a.offsets, numel, a.np, 1e-3, wl.grad_seed(400 + W, r, step), gdt,
+                               device="cuda") for r in range(W)]
+        if kind == "spec-inf":
+            grads[rank][idx] = float("inf")
+        hp = Hparams(max_grad_norm=1e-4) if kind == "spec-clip" else Hparams()
+        if kind.startswith("spec"):
+            a.step_speculative(grads, hp)
+        else:
+            a.step(grads, hp)
+        b.step(grads, hp)
+        torch.cuda.synchronize()
+        st = _assert_same(a, b, mask)
+        fast.append(st["fast_path"])
+    # clip switches on (wasted pass), stays on (predicted), switches off
+    # (predicted once more: the two-pass kernels find no clipping), commits again
+    assert fast == [1, 1, 0, 1, 0, 0, 0, 0, 0, 1, 1]
+    # gathers read the same parameters
+    reps = [[torch.empty(max(n, 8), dtype=a.params_flat.dtype, device="cuda") for n in numel]
+            for _ in range(2)]
+    a.gather([[t[:n] if n else t for t, n in zip(reps[0], numel)]])
+    b.gather([[t[:n] if n else t for t, n in zip(reps[1], numel)]])
+    torch.cuda.synchronize()
+    for x, y, n in zip(*reps, numel):
+        assert torch.equal(x[:n].view(torch.int16), y[:n].view(torch.int16))
+    a.close()
+    b.close()
+
+
+def test_export_import_follow_current_set():
+    """After an odd number of commits the alternate set is current; export
+    reads it, import writes it, and the next steps continue from it."""
+    sh = small_qwen_shapes()
+    a, b = _twin(sh, 4, 2, 80_000, wl.BF16, wl.BF16, seed=9)
+    mask = _real_shard_mask(a)
+    numel = wl.numels(sh)
+
+    def grads(step):
+        return [wl.flat_grads(a.offsets, numel, a.np, 1e-3, wl.grad_seed(500, r, step), wl.BF16,
+                              device="cuda") for r in range(4)]
+
+    g = grads(0)
+    a.step_speculative(g, Hparams())
+    b.step(g, Hparams())
+    torch.cuda.synchronize()
+    assert a.scaler_state()["state_set"] == 1
+    ea, eb = a.export_state(), b.export_state()
+    real = torch.zeros(a.np, dtype=torch.bool, device="cuda")
+    for off, n in zip(a.offsets, numel):
+        real[off:off + n] = True
+    for x, y in zip(ea, eb):
+        assert torch.equal(x[real], y[real])
+    # parameter-major export matches too
+    pm = [[torch.empty(sum(numel), device="cuda") for _ in range(3)] for _ in range(2)]
+    stream = torch.cuda.current_stream().cuda_stream
+    abi.zero_state_export_params(a.handle, *[t.data_ptr() for t in pm[0]], stream)
+    abi.zero_state_export_params(b.handle, *[t.data_ptr() for t in pm[1]], stream)
+    torch.cuda.synchronize()
+    for x, y in zip(*pm):
+        assert torch.equal(x, y)
+    # import perturbed state into both; the next steps agree bit for bit
+    new = [t * 1.5 for t in eb]
+    a.import_state(*new)
+    b.import_state(*new)
+    for step in (1, 2, 3):
+        g = grads(step)
+        a.step_speculative(g, Hparams())
+        b.step(g, Hparams())
+        torch.cuda.synchronize()
+        _assert_same(a, b, mask)
+    a.close()
+    b.close()
+
+
+def test_needs_alternate_set_and_stage():
+    shapes = [(1000,), (77,)]
+    z = ZeroStep(shapes, 2, 2, 1 << 20, wl.BF16, wl.BF16)
+    z.allocate()
+    z.init(torch.zeros(max(z.np, 8), device="cuda"))
+    g = z.new_grad_buffers()
+    with pytest.raises(ZeroError) as e:
+        z.step_speculative(g, Hparams())
+    assert e.value.code == abi.ZERO_ERR_STATE
+    with pytest.raises(ZeroError) as e:  # aliasing the bound set
+        z.bind_alternate(z.master, z.m2 if hasattr(z, "m2") else torch.empty_like(z.m),
+                         torch.empty_like(z.v))
+    assert e.value.code == abi.ZERO_ERR_INVALID
+    z.close()
+    z1 = ZeroStep(shapes, 2, 1, 1 << 20, wl.BF16, wl.BF16)
+    z1.allocate()
+    with pytest.raises(ZeroError) as e:
+        z1.bind_alternate(*[torch.empty(max(z1.np, 8), device="cuda") for _ in range(3)])
+    assert e.value.code == abi.ZERO_ERR_INVALID
+    z1.close()
+
+
+GUARD = 4096
+PATTERN = 0xA5
+
+
+class Guarded:
+    def __init__(self, n, dtype):
+        esz = torch.empty(0, dtype=dtype).element_size()
+        self.raw = torch.full((2 * GUARD + max(n, 8) * esz,), PATTERN, dtype=torch.uint8,
+                              device="cuda")
+        self.t = self.raw[GUARD:GUARD + max(n, 8) * esz].view(dtype)
+        self.nbytes = max(n, 8) * esz
+
+    def intact(self):
+        return bool((self.raw[:GUARD] == PATTERN).all()) and \
+            bool((self.raw[GUARD + self.nbytes:] == PATTERN).all())
+
+
+@pytest.mark.parametrize("stage", [2, 3])
+def test_no_write_outside_buffers(stage):
+    """Guard bands around both state sets, the parameters and the scratch
+    through commits, an overflow skip and a clip fallback."""
+    rng = np.random.default_rng(stage + 10)
+    shapes = [(int(x),) for x in rng.integers(1, 20000, size=12)] + [(3,), (0,), (8191,), (8193,)]
+    W = 3
+    z = ZeroStep(shapes, W, stage, 40_000, wl.BF16, wl.BF16)
+    n = z.np
+    bufs = [Guarded(n, torch.float32) for _ in range(6)] + [Guarded(n, torch.bfloat16)
+                                                            for _ in range(2)]
+    z.bind(bufs[0].t, bufs[1].t, bufs[2].t, bufs[6].t, bufs[7].t)
+    z.bind_alternate(bufs[3].t, bufs[4].t, bufs[5].t)
+    numel = wl.numels(shapes)
+    z.init(wl.master_init(z.offsets, numel, n, 0.02, 3, device="cuda"), init_scale=8.0, dynamic=True)
+    rank, idx = wl.inject_position(numel, z.offsets, W, seed=3)
+    for step, kind in enumerate(["c", "c", "inf", "clip", "c", "c"]):
+        grads = [wl.flat_grads(z.offsets, numel, n, 1e-3, wl.grad_seed(600, r, step), wl.BF16,
+                               device="cuda") for r in range(W)]
+        if kind == "inf":
+            grads[rank][idx] = float("inf")
+        z.step_speculative(grads, Hparams(max_grad_norm=1e-5 if kind == "clip" else 1.0))
+    torch.cuda.synchronize()
+    st = z.scaler_state()
+    assert st["steps"] == 6 and st["t"] == 5 and st["fast_path"] == 1
+    bad = [i for i, g in enumerate(bufs) if not g.intact()]
+    assert not bad, bad
+    z.close()
