@@ -310,11 +310,15 @@ int zero_step_speculative(zero_layout_t* layout, const void* const* grads, const
  * the device buffers dev_grads[w], then runs zero_step on dev_grads.
  * The copies run as pieces of at most 128 MB on copy streams the layout owns
  * (created on the first call); `stream` waits for them before the step. They
- * start after the previous zero_step_host step's reduce kernel has finished
- * reading dev_grads (stages 2/3) -- so they overlap that step's update
- * kernel -- or after all work queued on `stream` (stage 1, whose all-reduce
- * outputs may alias the gradients, and the first call). dev_grads must not be
- * written by anything else between calls. */
+ * start after the last zero_step_host reduce kernel that read the same
+ * dev_grads set has finished (stages 2/3) -- so they overlap that step's
+ * update kernel -- or after all work queued on `stream` (stage 1, whose
+ * all-reduce outputs may alias the gradients, and a set's first call). The
+ * library remembers the last four sets (identified by their W pointers): a
+ * caller that alternates two disjoint sets lets each step's copies overlap the
+ * previous step's reduce as well, so the host link never waits for the GPU.
+ * dev_grads must not be written by anything else between calls, and two sets
+ * must not overlap in memory. */
 int zero_step_host(zero_layout_t* layout, const void* const* host_grads, void* const* dev_grads,
                    void* const* allreduce_out, const zero_hparams* hp, void* stream);
 

@@ -111,6 +111,7 @@ struct zero_layout {
 
   int grid_reduce = 0, grid_update = 0, grid_copy = 0;
   int grid_spec = 0;  // speculative single pass (set by zero_state_bind_alternate)
+  int chunk_spec = 0;  // its elements per pipeline stage
   // 1 (default): shared-memory pipelines fed by cp.async.bulk; 0: the
   // register-staged kernels, kept as the comparison baseline (environment
   // ZERO_REDUCE_VARIANT / ZERO_UPDATE_VARIANT = 0 at bind selects them)
@@ -125,7 +126,20 @@ struct zero_layout {
   cudaStream_t copy_stream[kCopyStreams] = {};
   cudaEvent_t copy_start = nullptr;
   cudaEvent_t copy_done[kCopyStreams] = {};
-  cudaEvent_t k1_done = nullptr;  // recorded after each step's reduce kernel once host mode is used
+  // The device gradient buffer sets zero_step_host has copied into (keyed by
+  // all W pointers), each with an event after the last reduce
+  // kernel that read it: a new copy into a set waits only for that kernel, so
+  // a caller alternating two sets keeps the host link busy.
+  static constexpr int kHostSets = 4;
+  struct HostSet {
+    std::vector<const void*> key;
+    cudaEvent_t k1 = nullptr;
+    bool recorded = false;
+    unsigned long long used = 0;
+  };
+  HostSet host_sets[kHostSets];
+  unsigned long long host_calls = 0;
+  cudaEvent_t k1_done = nullptr;  // set only while zero_step_host runs its step: recorded after K1
   bool k1_recorded = false;
 
   int world() const { return cfg.world; }
@@ -337,7 +351,7 @@ int launch_step_spec(zero_layout* L, const GradSrc& src, const zero_hparams* hp,
                   hp->grad_divisor};
   sa.part_sumsq = L->d_part;
   sa.part_ovf = L->d_ovf;
-  sa.chunk = spec_chunk(L->world(), L->cfg.grad_dtype);
+  sa.chunk = L->chunk_spec;
   sa.error = &L->d_state->error;
   if (L->timing) ZERO_CUDA(cudaEventRecord(L->events[0], s));
   cudaError_t e = launch_spec(&sa, L->cfg.grad_dtype, L->comm_dtype, L->cfg.param_dtype, L->world(),
@@ -522,7 +536,7 @@ int zero_layout_destroy(zero_layout_t* L) {
       cudaEventDestroy(L->copy_done[i]);
     }
     cudaEventDestroy(L->copy_start);
-    cudaEventDestroy(L->k1_done);
+    for (auto& hs : L->host_sets) cudaEventDestroy(hs.k1);
   }
   if (L->dblock) L->free_fn(L->dblock, L->alloc_ctx);
   if (L->d_gather) L->free_fn(L->d_gather, L->alloc_ctx);
@@ -694,8 +708,20 @@ int zero_state_bind_alternate(zero_layout_t* L, void* master2, void* m2, void* v
   for (const void* q : {master2, m2, v2})
     for (const void* o : mine)
       if (q == o) return fail(ZERO_ERR_INVALID, "alternate state buffers must differ from the bound ones");
-  const int bps = spec_blocks_per_sm(L->cfg.grad_dtype, L->comm_dtype, L->cfg.param_dtype, L->world());
+  // Tuning knobs read at bind, like the kernel variants: ZERO_SPEC_STAGE_BYTES
+  // (bytes per pipeline stage, 3 stages) and ZERO_SPEC_BLOCKS_PER_SM (a cap
+  // on resident blocks, below what the occupancy allows).
+  int stage_bytes = kSpecStageBytesHost, bps_cap = 0;
+  if (const char* v = std::getenv("ZERO_SPEC_STAGE_BYTES")) {
+    const int b = std::atoi(v);
+    if (b >= 4096 && b <= 73728) stage_bytes = b;
+  }
+  if (const char* v = std::getenv("ZERO_SPEC_BLOCKS_PER_SM")) bps_cap = std::atoi(v);
+  const int chunk = spec_chunk(L->world(), L->cfg.grad_dtype, stage_bytes);
+  int bps = spec_blocks_per_sm(L->cfg.grad_dtype, L->comm_dtype, L->cfg.param_dtype, L->world(), chunk);
   if (bps <= 0) return fail(ZERO_ERR_CUDA, "speculative kernel occupancy query failed");
+  if (bps_cap > 0) bps = std::min(bps, bps_cap);
+  L->chunk_spec = chunk;
   int sms = 0;
   ZERO_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, L->device));
   L->grid_spec = std::max(1, std::min({(int)L->tiles.size(), sms * bps, kMaxPartials}));
@@ -819,23 +845,36 @@ int zero_step_host(zero_layout_t* L, const void* const* host_grads, void* const*
       L->n_copy_streams = n >= 1 && n <= zero_layout::kCopyStreams ? n : zero_layout::kCopyStreams;
     }
     ZERO_CUDA(cudaEventCreateWithFlags(&L->copy_start, cudaEventDisableTiming));
-    ZERO_CUDA(cudaEventCreateWithFlags(&L->k1_done, cudaEventDisableTiming));
+    for (auto& hs : L->host_sets) ZERO_CUDA(cudaEventCreateWithFlags(&hs.k1, cudaEventDisableTiming));
     for (int i = 0; i < L->n_copy_streams; ++i) {
       ZERO_CUDA(cudaStreamCreateWithFlags(&L->copy_stream[i], cudaStreamNonBlocking));
       ZERO_CUDA(cudaEventCreateWithFlags(&L->copy_done[i], cudaEventDisableTiming));
     }
     L->copy_ready = true;
   }
-  // The copies start once nothing can still read dev_grads: after the
-  // previous step's reduce kernel (stages 2/3: the update kernel never reads
-  // the gradients, so the copies overlap it), else after everything already
-  // on `stream`. They run as pieces of at most 128 MB spread over the copy
-  // streams, and `stream` waits for all of them before the step.
+  // The copies start once nothing can still read this set of dev_grads:
+  // after the last reduce kernel that read it (stages 2/3: the update kernel
+  // never reads the gradients, so the copies overlap it, and with two sets in
+  // turn they overlap the other set's reduce too), else after everything
+  // already on `stream`. They run as pieces of at most 128 MB spread over the
+  // copy streams, and `stream` waits for all of them before the step.
+  const std::vector<const void*> key(dev_grads, dev_grads + L->world());
+  zero_layout::HostSet* hs = nullptr;
+  for (auto& h : L->host_sets)
+    if (h.key == key) hs = &h;
+  if (hs == nullptr) {  // a new set: take a free slot, else the least recently used
+    hs = &L->host_sets[0];
+    for (auto& h : L->host_sets)
+      if (h.used < hs->used) hs = &h;
+    hs->key = key;
+    hs->recorded = false;
+  }
+  hs->used = ++L->host_calls;
   const size_t piece = size_t(128) << 20;
   const int n = L->n_copy_streams;
   cudaEvent_t after = L->copy_start;
-  if (L->cfg.stage != 1 && L->k1_recorded) {
-    after = L->k1_done;
+  if (L->cfg.stage != 1 && hs->recorded) {
+    after = hs->k1;
   } else {
     ZERO_CUDA(cudaEventRecord(L->copy_start, s));
   }
@@ -854,7 +893,12 @@ int zero_step_host(zero_layout_t* L, const void* const* host_grads, void* const*
     ZERO_CUDA(cudaEventRecord(L->copy_done[i], L->copy_stream[i]));
     ZERO_CUDA(cudaStreamWaitEvent(s, L->copy_done[i], 0));
   }
-  return zero_step(L, dev_grads, allreduce_out, hp, stream);
+  L->k1_done = hs->k1;
+  L->k1_recorded = false;
+  const int rc = zero_step(L, dev_grads, allreduce_out, hp, stream);
+  hs->recorded = L->k1_recorded;
+  L->k1_done = nullptr;
+  return rc;
 }
 
 int zero_accumulate(zero_layout_t* L, const void* const* micro, int micro_dtype, float* const* main,

@@ -168,11 +168,11 @@ struct SpecArgs {  // arguments of k_spec_step
 };
 
 constexpr int kSpecStagesHost = 3;        // == kSpecStages
-constexpr int kSpecStageBytesHost = 32768;  // == kSpecStageBytes
-int spec_chunk(int world, int grad_dtype);
+constexpr int kSpecStageBytesHost = 32768;  // default bytes per pipeline stage
+int spec_chunk(int world, int grad_dtype, int stage_bytes);
 cudaError_t launch_spec(const SpecArgs* args, int grad_dtype, int comm_dtype, int param_dtype, int world,
                         int grid, cudaStream_t s);
-int spec_blocks_per_sm(int grad_dtype, int comm_dtype, int param_dtype, int world);
+int spec_blocks_per_sm(int grad_dtype, int comm_dtype, int param_dtype, int world, int chunk);
 cudaError_t launch_finalize_spec(const double* part_sumsq, const unsigned* part_ovf, int n_part,
                                  int world, const Hparams& hp, DevState* st, cudaStream_t s);
 

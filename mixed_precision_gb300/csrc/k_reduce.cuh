@@ -66,8 +66,9 @@ __device__ __forceinline__ const GT* grad_ptr(const ReduceArgs& a, const Tile& t
 // running sum (hi, lo). A group whose fp32 sum is not below 2^100 (or not
 // finite) goes to an fp64 accumulator instead, so the fp32 sum cannot
 // overflow. GB300's fp64 pipe is narrow, so fp64 is kept off the common path.
+template <int N>
 __device__ __forceinline__ void add_group(float ss, float& hi, float& lo, double& big,
-                                          const float (&rf)[8]) {
+                                          const float (&rf)[N]) {
   if (ss < 0x1p100f) {  // false for +inf and NaN as well
     const float y = ss - lo;
     const float t = hi + y;
@@ -76,7 +77,7 @@ __device__ __forceinline__ void add_group(float ss, float& hi, float& lo, double
   } else {
     double d = 0.0;
 #pragma unroll
-    for (int j = 0; j < 8; ++j) d += (double)rf[j] * (double)rf[j];
+    for (int j = 0; j < N; ++j) d += (double)rf[j] * (double)rf[j];
     big += d;
   }
 }

@@ -36,7 +36,6 @@ __device__ __forceinline__ const GT* spec_grad_ptr(const GradSrc& src, const Til
 }
 
 constexpr int kSpecStages = kSpecStagesHost;
-constexpr int kSpecStageBytes = kSpecStageBytesHost;
 
 template <typename GT, typename CT, typename PT, int WT, int NC>
 __global__ void __launch_bounds__((NC + 1) * 32) k_spec_step(const __grid_constant__ SpecArgs a) {
@@ -140,42 +139,51 @@ __global__ void __launch_bounds__((NC + 1) * 32) k_spec_step(const __grid_consta
     const float* sv = reinterpret_cast<const float*>(base + kGrad + C * 8);
     const int64_t so = tl.shard + cc;
     PT* pp = static_cast<PT*>(a.params) + (a.stage == 3 ? tl.shard : tl.flat) + cc;
-    const int e_end = min(nb, (warp + 1) * per);
-    for (int e = warp * per + 8 * lane; e < e_end; e += 256) {
-      float acc[8];
-      load8_smem(sg + e, acc);
+    // Each lane takes two runs of 4 elements per 256-element span of its
+    // warp's slice: [4 lane, 4 lane + 4) and 128 further on. Every shared
+    // load (8 or 16 bytes per lane) and global store then covers contiguous
+    // bytes across the warp: no bank conflicts, fully coalesced stores.
+    const int w1 = min(nb, (warp + 1) * per);
+    for (int base = warp * per; base < w1; base += 256) {
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int e = base + 128 * h + 4 * lane;
+        if (e >= w1) continue;
+        float acc[4];
+        load4_smem(sg + e, acc);
 #pragma unroll(WT ? WT : 1)
-      for (int w = 1; w < W; ++w) {
-        float x[8];
-        load8_smem(sg + w * C + e, x);
+        for (int w = 1; w < W; ++w) {
+          float x[4];
+          load4_smem(sg + w * C + e, x);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) acc[j] = __fadd_rn(acc[j], x[j]);
-      }
-      float rf[8], p[8], m[8], v[8];
-      float ss = 0.0f;
-      bool fin = true;
+          for (int j = 0; j < 4; ++j) acc[j] = __fadd_rn(acc[j], x[j]);
+        }
+        float rf[4], p[4], m[4], v[4];
+        float ss = 0.0f;
+        bool fin = true;
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const CT rc = DT<CT>::from_f32(acc[j]);
-        rf[j] = DT<CT>::to_f32(rc);
-        fin = fin && DT<CT>::finite_bits(rc);
-        ss = __fmaf_rn(rf[j], rf[j], ss);
-      }
-      if (!fin) bad = 1u;
-      add_group(ss, hi, lo, big, rf);
-      load8_smem(sp + e, p);
-      load8_smem(sm + e, m);
-      load8_smem(sv + e, v);
-      Pack8<PT> q;
+        for (int j = 0; j < 4; ++j) {
+          const CT rc = DT<CT>::from_f32(acc[j]);
+          rf[j] = DT<CT>::to_f32(rc);
+          fin = fin && DT<CT>::finite_bits(rc);
+          ss = __fmaf_rn(rf[j], rf[j], ss);
+        }
+        if (!fin) bad = 1u;
+        add_group(ss, hi, lo, big, rf);
+        load4_smem(sp + e, p);
+        load4_smem(sm + e, m);
+        load4_smem(sv + e, v);
+        PT q[4];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        sc.apply(rf[j], p[j], m[j], v[j]);
-        q.e[j] = DT<PT>::from_f32(p[j]);
+        for (int j = 0; j < 4; ++j) {
+          sc.apply(rf[j], p[j], m[j], v[j]);
+          q[j] = DT<PT>::from_f32(p[j]);
+        }
+        store4_f32(dst_master + so + e, p);
+        store4_f32(dst_m + so + e, m);
+        store4_f32(dst_v + so + e, v);
+        store4_raw(pp + e, q);
       }
-      store8_f32(dst_master + so + e, p);
-      store8_f32(dst_m + so + e, m);
-      store8_f32(dst_v + so + e, v);
-      store8_raw(pp + e, q);
     }
     if (warp == 0 && lane < clen - nb) {  // ragged tail, from global memory
       const int e = nb + lane;

@@ -553,17 +553,17 @@ static const void* spec_kernel(int grad_dtype, int comm_dtype, int param_dtype, 
 }
 
 // Elements per stage: the W ranks' gradient slices plus 12 bytes of state per
-// element fill about kSpecStageBytes; a multiple of 128 elements, at least 128.
-int spec_chunk(int world, int grad_dtype) {
+// element fill about `stage_bytes`; a multiple of 128 elements, at least 128.
+int spec_chunk(int world, int grad_dtype, int stage_bytes) {
   const int g = grad_dtype == kF32 ? 4 : 2;
-  int c = kSpecStageBytesHost / (world * g + 12);
+  int c = stage_bytes / (world * g + 12);
   c &= ~127;
   return c < 128 ? 128 : c;
 }
 
-static int spec_smem(int world, int grad_dtype) {
+static int spec_smem(int world, int grad_dtype, int chunk) {
   const int g = grad_dtype == kF32 ? 4 : 2;
-  return kSpecStagesHost * spec_chunk(world, grad_dtype) * (world * g + 12);
+  return kSpecStagesHost * chunk * (world * g + 12);
 }
 
 cudaError_t launch_spec(const SpecArgs* args, int grad_dtype, int comm_dtype, int param_dtype, int world,
@@ -572,13 +572,13 @@ cudaError_t launch_spec(const SpecArgs* args, int grad_dtype, int comm_dtype, in
   if (f == nullptr) return cudaErrorInvalidValue;
   void* a[] = {const_cast<SpecArgs*>(args)};
   return cudaLaunchKernel(f, dim3(grid), dim3((kRedConsumers + 1) * 32), a,
-                          spec_smem(world, grad_dtype), s);
+                          spec_smem(world, grad_dtype, args->chunk), s);
 }
 
-int spec_blocks_per_sm(int grad_dtype, int comm_dtype, int param_dtype, int world) {
+int spec_blocks_per_sm(int grad_dtype, int comm_dtype, int param_dtype, int world, int chunk) {
   const void* f = spec_kernel(grad_dtype, comm_dtype, param_dtype, world);
   if (f == nullptr) return 0;
-  const int smem = spec_smem(world, grad_dtype);
+  const int smem = spec_smem(world, grad_dtype, chunk);
   if (cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
     return 0;
   int n = 0;

@@ -141,6 +141,22 @@ __device__ __forceinline__ void store8_f32(float* p, const float (&x)[8]) {
                               __float_as_uint(x[7])));
 }
 
+__device__ __forceinline__ void store4_f32(float* p, const float (&x)[4]) {
+  st_stream(p, make_uint4(__float_as_uint(x[0]), __float_as_uint(x[1]), __float_as_uint(x[2]),
+                          __float_as_uint(x[3])));
+}
+
+// 4 elements of a 2-byte type as one 8-byte streaming store (8-byte aligned).
+template <typename T>
+__device__ __forceinline__ void store4_raw(T* p, const T (&e)[4]) {
+  static_assert(sizeof(T) == 2, "4 x 2 bytes");
+  uint2 u;
+  T* h = reinterpret_cast<T*>(&u);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) h[j] = e[j];
+  __stcs(reinterpret_cast<uint2*>(p), u);
+}
+
 // ---- the element-wise AdamW update ----------------------------------------
 // One fixed sequence of correctly rounded fp32 operations (explicit
 // intrinsics, so no kernel's compiler contracts it differently): every
@@ -155,13 +171,21 @@ struct AdamScalars {
                        st->beta1, st->one_minus_beta1, st->beta2, st->one_minus_beta2};
   }
 
+  // Zero operands are answered without calling sqrt or divide (sqrt(+0) =
+  // +0; +-0 / denom = +-0, as denom >= eps > 0), which gives the same bits:
+  // parameters whose gradient has been zero on every rank (MoE experts no
+  // token reached) keep m = v = 0, and the correctly rounded sqrt and divide
+  // are much slower on such operands than on ordinary ones.
   __device__ __forceinline__ void apply(float r, float& p, float& m, float& v) const {
     const float g = __fmul_rn(r, gs);
     p = __fmul_rn(p, decay);
     m = __fmaf_rn(b1, m, __fmul_rn(omb1, g));
     v = __fmaf_rn(b2, v, __fmul_rn(omb2, __fmul_rn(g, g)));
-    const float denom = __fmaf_rn(__fsqrt_rn(v), isb2, eps);
-    p = __fmaf_rn(-step, __fdiv_rn(m, denom), p);
+    const bool vz = v == 0.0f, mz = m == 0.0f;  // v >= +0 always
+    const float sv = __fsqrt_rn(vz ? 1.0f : v);
+    const float denom = __fmaf_rn(vz ? 0.0f : sv, isb2, eps);
+    const float q = __fdiv_rn(mz ? 1.0f : m, denom);
+    p = __fmaf_rn(-step, mz ? m : q, p);
   }
 };
 

@@ -162,6 +162,38 @@ def test_host_steps_back_to_back_overlap(stage):
     pr.check(st, info, g1)
 
 
+def test_host_steps_alternating_device_sets():
+    """Three zero_step_host calls alternating two device gradient sets (A, B,
+    A) without synchronising: each copy waits only for the reduce kernel that
+    last read its own set. The final state matches three oracle steps."""
+    import oracle as orc
+    shapes = small_qwen_shapes()
+    pr = Pair(shapes, 3, 2, 100_000, wl.BF16, wl.BF16, index=161)
+    gs = [pr.grads(k, 1e-3) for k in range(3)]
+    sets = [[torch.empty(pr.np, dtype=torch.bfloat16, device="cuda") for _ in range(3)]
+            for _ in range(2)]
+    pins = [[x.pin_memory() for x in g] for g in gs]
+    hp = Hparams()
+    for k in range(3):
+        pr.z.step_host(pins[k], sets[k % 2], hp)
+    torch.cuda.synchronize()
+    st = pr.z.scaler_state()
+    o_hp = orc.Hparams(hp.lr, hp.beta1, hp.beta2, hp.eps, hp.weight_decay, hp.max_grad_norm,
+                       hp.grad_divisor)
+    for g in gs:
+        info = orc.zero_step(pr.numel, pr.W, 2, pr.bucket, pr.gdt, pr.cdt, pr.pdt,
+                             [to_np(x) for x in g], pr.o_master, pr.o_m, pr.o_v, pr.o_params, o_hp,
+                             pr.o_scaler, allreduce_out=pr.o_out)
+        for h, x in zip(pr.hist, (pr.o_master, pr.o_m, pr.o_v)):
+            np.maximum(h, np.abs(x), out=h)
+    assert st["t"] == 3
+    pr.check(st, info, gs[2])
+    # the device sets hold the last gradients copied into each
+    for k in (1, 2):
+        for r in range(3):
+            assert np.array_equal(to_np(sets[k % 2][r]), to_np(gs[k][r]))
+
+
 def test_overflow_at_shard_edges_skips():
     """+inf / -inf / NaN at the first or last real element of shards in the
     first and last rank: flag set, step skipped, state untouched, scale halved."""
