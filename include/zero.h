@@ -42,6 +42,13 @@
  *   - A layout is used from one host thread and one stream at a time.
  *   - Arguments are validated on the host before anything is enqueued; an
  *     invalid call changes no state.
+ *   - zero_step and zero_step_speculative enqueue kernels only (no
+ *     allocation, no host synchronisation, no events unless
+ *     zero_set_step_events is active), and every decision of the step is
+ *     taken on the device, so both can be captured into a CUDA graph and
+ *     replayed on new gradients written into the captured buffers. The
+ *     hyper-parameters are captured by value. zero_step_host is not
+ *     capturable (its copy streams wait on events of earlier calls).
  */
 #ifndef ZERO_GB300_H
 #define ZERO_GB300_H
@@ -297,6 +304,10 @@ int zero_step_per_tensor_launch(zero_layout_t* layout, const void* const* grads,
  * fall back and returns at once: the step then costs what zero_step costs
  * plus two empty launches, and only the step on which clipping switches on
  * pays for both passes.
+ * The commit decision uses the single pass's own norm, summed in another
+ * grouping than zero_step's (both within the parity tolerance of the exact
+ * norm); only a norm within that rounding of the clip threshold could make
+ * the two calls decide differently.
  * A committed step moves W*size(grad) + 24 + size(param) bytes per element,
  * the whole step's ledger; the reduced gradients are never stored, so the
  * scratch buffer's contents are unspecified afterwards.

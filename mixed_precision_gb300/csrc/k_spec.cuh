@@ -25,13 +25,11 @@
 
 namespace zg {
 
-// Rank w's gradient pointer for a tile (flat buffers or the per-tensor table).
+// Rank w's gradient pointer for a tile. The speculative step takes flat
+// gradient buffers only (zero_step_speculative checks every pointer), so
+// there is no per-tensor table and no NULL (all-zero) gradient here.
 template <typename GT>
 __device__ __forceinline__ const GT* spec_grad_ptr(const GradSrc& src, const Tile& tl, int w) {
-  if (src.table_mode) {
-    const void* q = src.table[(int64_t)w * src.n_params + tl.param];
-    return q ? static_cast<const GT*>(q) + tl.in_param : nullptr;
-  }
   return static_cast<const GT*>(src.base[w]) + tl.flat;
 }
 
