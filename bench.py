@@ -238,13 +238,9 @@ def sample_shapes(shapes, target_elems: int):
     return out, total
 
 
-def time_oracle(w, target_elems: int, seconds: float, min_steps: int = 1, warmup: int = 0,
-                steps: int | None = None):
-    """Run the host oracle's ZeRO step on a sample of the workload.
-
-    Returns (params per second, steps timed, sample elements, sample description).
-    Single-threaded: the oracle is plain sequential host code.
-    """
+def _oracle_setup(w, target_elems: int):
+    """Inputs and state for the host oracle's ZeRO step on a sample of the
+    workload; returns (one step as a callable, sample elements, sample text)."""
     import numpy as np
     import torch
 
@@ -273,6 +269,19 @@ def time_oracle(w, target_elems: int, seconds: float, min_steps: int = 1, warmup
         oracle.zero_step(numel, w.world, w.stage, w.bucket_bytes, w.grad_dtype, w.comm_dtype,
                          w.param_dtype, grads, ms, m, v, params, hp, sc, allreduce_out=outs)
 
+    desc = (f"{len(shapes)} of the workload's {len(w.shapes)} tensors ({n_sample} elements, "
+            f"tensors larger than {target_elems} skipped), W={w.world}, ZeRO-{w.stage}")
+    return one, n_sample, desc
+
+
+def time_oracle(w, target_elems: int, seconds: float, min_steps: int = 1, warmup: int = 0,
+                steps: int | None = None):
+    """Run the host oracle's ZeRO step on a sample of the workload.
+
+    Returns (params per second, steps timed, sample elements, sample description).
+    Single-threaded: the oracle is plain sequential host code.
+    """
+    one, n_sample, desc = _oracle_setup(w, target_elems)
     for _ in range(warmup):
         one()
     t0 = time.perf_counter()
@@ -287,10 +296,34 @@ def time_oracle(w, target_elems: int, seconds: float, min_steps: int = 1, warmup
         elif done >= min_steps and el >= seconds:
             break
     el = time.perf_counter() - t0
-    desc = (f"{len(shapes)} of the workload's {len(w.shapes)} tensors ({n_sample} elements, "
-            f"tensors larger than {target_elems} skipped), W={w.world}, ZeRO-{w.stage}, "
-            f"{done} full oracle steps")
-    return n_sample * done / el, done, n_sample, desc
+    return n_sample * done / el, done, n_sample, f"{desc}, {done} full oracle steps"
+
+
+def time_oracle_threads(w, target_elems: int, seconds: float, threads: int):
+    """The same oracle step on all host cores: `threads` host threads each
+    step their own copy of the sample (the oracle itself stays sequential;
+    its ctypes calls release the interpreter lock). Returns (aggregate params
+    per second, sample description)."""
+    import concurrent.futures
+
+    setups = [_oracle_setup(w, target_elems) for _ in range(threads)]
+    n_sample, desc = setups[0][1], setups[0][2]
+    for one, _, _ in setups:  # first touch of every copy's buffers
+        one()
+
+    def loop(one):
+        done, t0 = 0, time.perf_counter()
+        while time.perf_counter() - t0 < seconds or done == 0:
+            one()
+            done += 1
+        return done, time.perf_counter() - t0
+
+    with concurrent.futures.ThreadPoolExecutor(threads) as ex:
+        res = list(ex.map(loop, [s[0] for s in setups]))
+    total = sum(d for d, _ in res)
+    wall = max(t for _, t in res)
+    return n_sample * total / wall, (f"{threads} threads, each stepping its own copy of {desc}; "
+                                     f"{total} full oracle steps in all")
 
 
 # ---------------------------------------------------------------------------
@@ -379,6 +412,7 @@ def run_ours(args) -> dict | None:
     # the speculative step commits on the fast path unless clipping is active
     fast_path = st["fast_path"] if args.speculative else None
 
+    steps_ms = sorted(ev[k][0].elapsed_time(ev[k][3]) for k in range(K))
     k1 = [ev[k][0].elapsed_time(ev[k][1]) for k in range(K)]
     k2 = [ev[k][1].elapsed_time(ev[k][2]) for k in range(K)]
     k3 = [ev[k][2].elapsed_time(ev[k][3]) for k in range(K)]
@@ -464,6 +498,8 @@ def run_ours(args) -> dict | None:
         "steps": K,
         "warmup": W,
         "ms_per_step": total_ms / K,
+        "step_ms_median": steps_ms[K // 2],
+        "step_ms_min": steps_ms[0],
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
@@ -502,7 +538,12 @@ def run_ours(args) -> dict | None:
 
 def cpu_baseline(w, seconds: float) -> dict:
     rate, done, n, desc = time_oracle(w, 20_000_000, seconds)
-    return {"value": rate, "unit": "params/s", "cores": 1, "kind": "oracle", "sample": desc}
+    out = {"value": rate, "unit": "params/s", "cores": 1, "kind": "oracle", "sample": desc}
+    cores = os.cpu_count() or 1
+    if cores > 1:
+        rate_mt, desc_mt = time_oracle_threads(w, 4_000_000, seconds / 2, cores)
+        out["all_cores"] = {"value": rate_mt, "unit": "params/s", "cores": cores, "sample": desc_mt}
+    return out
 
 
 def run_reference(args) -> dict | None:
