@@ -490,6 +490,8 @@ def run_ours(args) -> dict | None:
     achieved = dom[1] / (dom[2] / 1e3) / 1e9
     tr = NCU_TRAFFIC_PER_ELEM.get(dom[0])
     step_gbs = info.step_bytes_per_elem * N / step_s / 1e9
+    impl_bytes = info.step_bytes_per_elem if args.speculative else \
+        info.step_bytes_per_elem + (w.world * C if w.stage == 1 else C) + C
     out = {
         "metric": METRIC,
         "value": job_value(N, world, step_s),
@@ -513,7 +515,11 @@ def run_ours(args) -> dict | None:
                                                    if args.speculative else None))),
         "hbm_gbs_step": step_gbs,
         "step_roofline": {"bytes_per_param": info.step_bytes_per_elem, "peak_gbs": peak,
-                          "frac": step_gbs / peak, "peak_source": peak_src},
+                          "frac": step_gbs / peak, "peak_source": peak_src,
+                          # bytes the kernels must move per param: the ledger, plus
+                          # (two-pass) the reduced gradient written and read back
+                          "impl_bytes_per_param": impl_bytes,
+                          "impl_ceiling": info.step_bytes_per_elem / impl_bytes},
         "roofline": {"bound": "hbm", "kernel": dom[0], "achieved": achieved, "peak": peak,
                      "unit": "GB/s", "frac": achieved / peak,
                      "traffic": (tr * N if tr is not None else None),

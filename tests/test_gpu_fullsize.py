@@ -8,6 +8,10 @@ benchmark times, on sampled outputs (see _fullsize.py).
 - MoE ~3.9B, W=4, bf16, 14 of 16 experts' gradients zero per rank and layer:
   sampled parity, and the per-tensor entry point (NULL for the zero experts)
   bit-identical to the flat one.
+- The speculative step at full size, in the launch configuration
+  `bench.py --speculative` times: fp16 W=8 (clipping inactive) commits, skips
+  on +inf and commits again; Qwen3 bf16 W=2 at clip 1.0 (clipping active)
+  falls back, then is predicted to. Sampled parity on every step.
 """
 import numpy as np
 import pytest
@@ -22,10 +26,10 @@ from mixed_precision_gb300.engine import Hparams, ZeroStep
 pytestmark = pytest.mark.gpu
 
 
-def _setup(w, stage=None):
+def _setup(w, stage=None, speculative=False):
     stage = w.stage if stage is None else stage
     z = ZeroStep(w.shapes, w.world, stage, w.bucket_bytes, w.grad_dtype, w.param_dtype, w.comm_dtype)
-    z.allocate()
+    z.allocate(speculative=speculative)
     numel = wl.numels(w.shapes)
     master0 = wl.master_init(z.offsets, numel, z.np, w.master_sigma, wl.master_seed(w.index),
                              device="cuda")
@@ -136,4 +140,33 @@ def test_fullsize_moe_w4_flat_and_tensors():
         assert torch.equal(a.view(torch.int32), b.view(torch.int32))
     assert torch.equal(z.params_flat.view(torch.int16), zt.params_flat.view(torch.int16))
     zt.close()
+    z.close()
+
+
+@pytest.mark.parametrize("name,plan", [
+    ("qwen3_0.6b_fp16_w8", ["commit", "skip", "commit"]),
+    ("qwen3_0.6b_bf16_w2", ["fallback", "predicted"]),
+])
+def test_fullsize_speculative(name, plan):
+    w = wl.workload(name)
+    z, numel, master0 = _setup(w, speculative=True)
+    so = SampledOracle(z, numel, master0, sample_indices(z, numel, 100_000, 4), w.init_scale,
+                       w.dynamic, w.growth_interval)
+    del master0
+    hp = _hp(w)
+    rank, idx = wl.inject_position(numel, z.offsets, w.world, seed=9)
+    for step, kind in enumerate(plan):
+        g = _grads(z, w, numel, step)
+        if kind == "skip":
+            g[rank][idx] = float("inf")
+        z.step_speculative(g, hp)
+        torch.cuda.synchronize()
+        st = z.scaler_state()
+        assert st["fast_path"] == (kind == "commit")
+        assert st["skipped"] == (kind == "skip")
+        info, red_at = so.step(g, hp)
+        so.check(st, info, red_at, reduced=kind in ("fallback", "predicted"))
+        if kind in ("fallback", "predicted"):
+            assert st["clip_coef"] < 1.0
+        del g
     z.close()
