@@ -432,6 +432,31 @@ def run_ours(args) -> dict | None:
     grads[0][z.offsets[0]] = saved
     torch.cuda.synchronize()
 
+    # ZeRO-3: the per-bucket all-gather of the sharded parameters into a flat
+    # working buffer (what a forward pass would prefetch bucket by bucket).
+    gather = None
+    if w.stage == 3:
+        stream = torch.cuda.current_stream().cuda_stream
+        blen = max(abi.zero_bucket_range(z.handle, b)[1] for b in range(info.n_buckets))
+        work = torch.empty(blen, dtype=z.params_flat.dtype, device=device)
+        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = 20
+        for _ in range(2):
+            for b in range(info.n_buckets):
+                abi.zero_gather_bucket(z.handle, b, work.data_ptr(), stream)
+        g0.record()
+        for _ in range(reps):
+            for b in range(info.n_buckets):
+                abi.zero_gather_bucket(z.handle, b, work.data_ptr(), stream)
+        g1.record()
+        torch.cuda.synchronize()
+        ms = g0.elapsed_time(g1) / reps
+        pbytes = wl.ELEM_BYTES[w.param_dtype]
+        gather = {"buckets": info.n_buckets, "ms_all_buckets": ms,
+                  "gbs": 2 * pbytes * info.n_real / (ms / 1e3) / 1e9,
+                  "bytes_per_param": 2 * pbytes}
+        del work
+
     # End to end through the host-buffer entry point: pinned host gradients are
     # copied in every step and the step's scaler state is read back.
     E = args.e2e_steps
@@ -527,6 +552,7 @@ def run_ours(args) -> dict | None:
         "kernels_ms": kernels,
         "fast_path": fast_path,
         "skip_step_ms": skip_ms,
+        "zero3_gather": gather,
         "e2e": e2e,
         "gpu_launches": K * ((2 * sum(1 for n in numel if n > 0) + 1) if args.per_tensor_launch
                              else (6 if args.speculative else 3)),
