@@ -109,28 +109,57 @@ def _info(c: _Info) -> Info:
 _lib = None
 
 
+def _open(path: str) -> ctypes.CDLL:
+    L = ctypes.CDLL(path)
+    P = ctypes.c_void_p
+    I64, I32, D = ctypes.c_int64, ctypes.c_int, ctypes.c_double
+    L.orc_layout.argtypes = [P, I32, I32, I64, I32, P, P, P, P, P, P]
+    L.orc_encode.argtypes = [P, I64, I32, P]
+    L.orc_decode.argtypes = [P, I64, I32, P]
+    L.orc_reduce.argtypes = [P, I32, I32, I64, I64, P, I32, P]
+    L.orc_overflow_sumsq.argtypes = [P, I32, I64, P, P, P]
+    L.orc_finalize.argtypes = [D, I32, I32, P, P, P]
+    L.orc_adamw.argtypes = [P, I32, I64, P, P, P, P, P]
+    L.orc_accumulate.argtypes = [P, I32, P, I64, P, I32]
+    L.orc_ddp_step.argtypes = [I32, I64, I32, I32, I32, P, P, P, P, P, P, P, P]
+    L.orc_ddp_step.restype = I32
+    L.orc_zero_step.argtypes = [P, I32, I32, I32, I64, I32, I32, I32, P, P, P, P, P, P,
+                                P, P, P]
+    L.orc_zero_step.restype = I32
+    L.orc_layout.restype = I32
+    return L
+
+
 def lib() -> ctypes.CDLL:
     global _lib
     if _lib is None:
         build()
-        _lib = ctypes.CDLL(LIB_PATH)
-        P = ctypes.c_void_p
-        I64, I32, D = ctypes.c_int64, ctypes.c_int, ctypes.c_double
-        _lib.orc_layout.argtypes = [P, I32, I32, I64, I32, P, P, P, P, P, P]
-        _lib.orc_encode.argtypes = [P, I64, I32, P]
-        _lib.orc_decode.argtypes = [P, I64, I32, P]
-        _lib.orc_reduce.argtypes = [P, I32, I32, I64, I64, P, I32, P]
-        _lib.orc_overflow_sumsq.argtypes = [P, I32, I64, P, P, P]
-        _lib.orc_finalize.argtypes = [D, I32, I32, P, P, P]
-        _lib.orc_adamw.argtypes = [P, I32, I64, P, P, P, P, P]
-        _lib.orc_accumulate.argtypes = [P, I32, P, I64, P, I32]
-        _lib.orc_ddp_step.argtypes = [I32, I64, I32, I32, I32, P, P, P, P, P, P, P, P]
-        _lib.orc_ddp_step.restype = I32
-        _lib.orc_zero_step.argtypes = [P, I32, I32, I32, I64, I32, I32, I32, P, P, P, P, P, P,
-                                       P, P, P]
-        _lib.orc_zero_step.restype = I32
-        _lib.orc_layout.restype = I32
+        _lib = _open(LIB_PATH)
     return _lib
+
+
+def build_variant(src: str, out: str) -> str:
+    """Compile another source of the oracle (the planted-mistake variants of
+    the mutation tests) with the same flags."""
+    cmd = ["g++", "-O2", "-std=c++17", "-fPIC", "-shared", "-ffp-contract=off",
+           "-I", _HERE, "-o", out, src]
+    subprocess.run(cmd, check=True, capture_output=True)
+    return out
+
+
+def use_library(path: str | None):
+    """Route every call through the build at `path` (None: the oracle's own
+    build). Returns the library used before, for restoring. A test hook: the
+    mutation tests plant one mistake at a time this way."""
+    global _lib
+    before = _lib
+    _lib = _open(path) if path is not None else None
+    return before
+
+
+def restore_library(before) -> None:
+    global _lib
+    _lib = before
 
 
 def _ptr(a: np.ndarray) -> int:

@@ -156,6 +156,20 @@ def test_layout_known_small_case(orc):
                                       (0, 1, 128, 256, 128), (1, 1, 384, 384, 128)]
 
 
+def test_layout_bucket_boundary_is_strict(orc):
+    """A bucket closes only when the next parameter would take its span past
+    the cap: a parameter ending exactly at the cap stays in the bucket.
+    Cap 256 elements (512 B of bf16), W=2: sizes 128 + 128 end at 256 -> one
+    bucket [0, 256); sizes 128 + 129 would end at 257 -> the second parameter
+    opens bucket 1 at 256 (129 elements padded to 2 * 128)."""
+    L = orc.layout([128, 128], 2, 512, 2)
+    assert L.param_offset.tolist() == [0, 128]
+    assert L.bucket_start.tolist() == [0] and L.bucket_len.tolist() == [256]
+    L = orc.layout([128, 129], 2, 512, 2)
+    assert L.param_offset.tolist() == [0, 256]
+    assert L.bucket_start.tolist() == [0, 256] and L.bucket_len.tolist() == [256, 256]
+
+
 def test_layout_workload_sizes(orc):
     for name, n_real in [("tiny", 327936), ("qwen3_0.6b_bf16_w2", 596049920),
                          ("moe_3.9b_bf16_w4", 3890479104)]:
@@ -283,6 +297,27 @@ def test_scaler_growth_after_n_clean(orc):
     assert traj[10][4] == 0 and traj[11][4] == 1
 
 
+def test_scaler_overflow_resets_clean_count(orc):
+    """Seven clean steps, an overflow, then clean steps with N = 10: the
+    overflow resets the clean count, so growth comes on the 10th clean step
+    after it (not the 3rd, which a kept count of 7 would give)."""
+    seq = [0] * 7 + [1] + [0] * 12
+    traj = _run_scaler(orc, seq, scale=2.0 ** 10, growth_interval=10)
+    after = [t[3] for t in traj]
+    assert after[6] == 2.0 ** 10 and traj[6][4] == 7
+    assert after[7] == 2.0 ** 9 and traj[7][4] == 0
+    assert after[8:17] == [2.0 ** 9] * 9
+    assert after[17] == 2.0 ** 10 and traj[17][4] == 0
+
+
+def test_scaler_static_never_grows(orc):
+    """Static loss scaling: the scale stays put however many clean steps pass."""
+    sc = orc.Scaler(scale=4.0, dynamic=False, growth_interval=2)
+    for _ in range(7):
+        orc.finalize(1.0, 0, 2, orc.Hparams(), sc)
+    assert sc.scale == 4.0 and sc.t == 7
+
+
 def test_scaler_min_scale_and_static(orc):
     traj = _run_scaler(orc, [1, 1, 1], scale=2.0, min_scale=1.0)
     assert [t[3] for t in traj] == [1.0, 1.0, 1.0]
@@ -324,6 +359,47 @@ def test_adamw_first_step_closed_form(orc):
     np.testing.assert_allclose(p, expect2, rtol=1e-6, atol=1e-12)
     np.testing.assert_allclose(m, 0.19 * g64, rtol=4e-7)
     np.testing.assert_allclose(v, 0.001999 * g64 ** 2, rtol=4e-7)
+
+
+def test_adamw_skipped_step_touches_nothing(orc):
+    """A skipped step (overflow) leaves master, m and v bit for bit, even when
+    the update is called with it."""
+    rng = np.random.default_rng(31)
+    g = rng.standard_normal(64).astype(np.float32)
+    p = rng.standard_normal(64).astype(np.float32)
+    m = (0.1 * rng.standard_normal(64)).astype(np.float32)
+    v = (0.01 * rng.random(64)).astype(np.float32)
+    p0, m0, v0 = p.copy(), m.copy(), v.copy()
+    info = orc.Info(1, 1, float("inf"), float("inf"), 0.0, 0.0, 0.0, 0.0)
+    orc.adamw(g, wl.F32, orc.Hparams(), info, p, m, v)
+    assert np.array_equal(p.view(np.uint32), p0.view(np.uint32))
+    assert np.array_equal(m.view(np.uint32), m0.view(np.uint32))
+    assert np.array_equal(v.view(np.uint32), v0.view(np.uint32))
+
+
+def test_adam_constant_gradient_moves_lr_per_step(orc):
+    """Bias-corrected Adam under a constant gradient g: m_t = (1 - b1^t) g and
+    v_t = (1 - b2^t) g^2, so the corrected moments are exactly g and g^2 and
+    every step moves the parameter by lr * g / (|g| + eps) (weight decay off).
+    Runs the composed step (finalize's t and bias corrections, then the update)
+    for six steps; a correction from the wrong beta or the wrong t moves by a
+    different amount."""
+    n = 64
+    g = np.tile(np.array([0.5, -0.25, 1.0, -2.0], np.float32), n // 4)
+    grads = [orc.encode(g, wl.BF16)]
+    p0 = np.linspace(-1.0, 1.0, n).astype(np.float32)
+    master, m, v = p0.copy(), np.zeros(n, np.float32), np.zeros(n, np.float32)
+    params = np.zeros(n, np.uint16)
+    hp = orc.Hparams(lr=1e-3, weight_decay=0.0, max_grad_norm=0.0)
+    sc = orc.Scaler()
+    step = hp.lr * g.astype(np.float64) / (np.abs(g.astype(np.float64)) + hp.eps)
+    for k in range(1, 7):
+        orc.ddp_step(grads, wl.BF16, wl.BF16, wl.BF16, master, m, v, params, hp, sc)
+        expect = p0.astype(np.float64) - k * step
+        # fp32 storage of master/m/v: a few ulps of |p| per step at most
+        tol = k * 4 * np.spacing(np.abs(expect).astype(np.float32)).astype(np.float64)
+        assert np.all(np.abs(master - expect) <= tol), (k, np.abs(master - expect).max())
+    assert sc.t == 6
 
 
 def test_adamw_zero_grad_pure_decay(orc):
