@@ -151,15 +151,26 @@ cudaError_t launch_recast(const Tile* tiles, int n_tiles, float* const* master, 
 
 // ZeRO-3 all-gather of one bucket: dst[flat + i] <- shards[shard + i] over the
 // bucket's tiles (2-byte parameters; 16-byte vectors, then the ragged tail).
+// Each thread issues 4 independent vector loads before its stores, so a block
+// keeps 16 KB in flight (a tile of 8192 elements is exactly one such round).
 __global__ void __launch_bounds__(kThreads)
     k_gather_bucket(const Tile* __restrict__ tiles, int n_tiles, const uint16_t* __restrict__ shards,
                     uint16_t* __restrict__ dst) {
+  constexpr int U = 4;
   for (int t = blockIdx.x; t < n_tiles; t += gridDim.x) {
     const Tile tl = tiles[t];
     const int nvec = tl.len >> 3;
     const uint4* s4 = reinterpret_cast<const uint4*>(shards + tl.shard);
     uint4* d4 = reinterpret_cast<uint4*>(dst + tl.flat);
-    for (int v = threadIdx.x; v < nvec; v += kThreads) d4[v] = __ldcs(s4 + v);
+    for (int v0 = threadIdx.x; v0 < nvec; v0 += U * kThreads) {
+      uint4 x[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+        if (v0 + u * kThreads < nvec) x[u] = __ldcs(s4 + v0 + u * kThreads);
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+        if (v0 + u * kThreads < nvec) __stcs(d4 + v0 + u * kThreads, x[u]);
+    }
     for (int i = nvec * 8 + threadIdx.x; i < tl.len; i += kThreads) dst[tl.flat + i] = shards[tl.shard + i];
   }
 }
