@@ -371,7 +371,9 @@ def run_ours(args) -> dict | None:
                                for p, (off, n) in enumerate(zip(z.offsets, numel))])
 
     def do_step():
-        if per_tensor is not None:
+        if per_tensor is not None and args.speculative:
+            z.step_speculative_tensors(per_tensor, hp)
+        elif per_tensor is not None:
             z.step_tensors(per_tensor, hp)
         elif args.per_tensor_launch:
             z.step_per_tensor_launch(grads, hp)

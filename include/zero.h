@@ -316,6 +316,16 @@ int zero_step_per_tensor_launch(zero_layout_t* layout, const void* const* grads,
 int zero_step_speculative(zero_layout_t* layout, const void* const* grads, const zero_hparams* hp,
                           void* stream);
 
+/* The speculative step with gradients given per tensor, as zero_step_tensors
+ * takes them: grad_ptrs is a host array of W * n_params device pointers
+ * (grad_ptrs[w * n_params + p]), 16-byte aligned, NULL for an all-zero
+ * gradient, which is never read. Results are those of zero_step_speculative
+ * on flat buffers holding zeros there, bit for bit. The table is copied to
+ * the device on `stream` before the call returns, so it is not capturable
+ * into a CUDA graph. Errors as zero_step_tensors. */
+int zero_step_speculative_tensors(zero_layout_t* layout, const void* const* grad_ptrs,
+                                  const zero_hparams* hp, void* stream);
+
 /* Same step from HOST gradients: copies host_grads[w] (Np elements of
  * grad_dtype each, flat layout; pinned memory gives asynchronous copies) into
  * the device buffers dev_grads[w], then runs zero_step on dev_grads.

@@ -12,7 +12,7 @@ from ._abi import (ZERO_BF16, ZERO_STATE_BLOB_BYTES, zero_accumulate, zero_gathe
                    zero_layout_destroy, zero_layout_info, zero_layout_query,
                    zero_layout_set_allocator, zero_loss_scale_state, zero_param_offset,
                    zero_scaler_cfg, zero_scaler_state, zero_set_step_events, zero_shard_range, zero_state_bind,
-                   zero_state_bind_alternate, zero_step_speculative,
+                   zero_state_bind_alternate, zero_step_speculative, zero_step_speculative_tensors,
                    zero_state_export, zero_state_import, zero_state_init, zero_step,
                    zero_step_host, zero_step_per_tensor_launch, zero_step_tensors, lib)
 

@@ -789,6 +789,28 @@ int zero_step_speculative(zero_layout_t* L, const void* const* grads, const zero
   return launch_step_spec(L, src, hp, static_cast<cudaStream_t>(stream));
 }
 
+int zero_step_speculative_tensors(zero_layout_t* L, const void* const* grad_ptrs,
+                                  const zero_hparams* hp, void* stream) {
+  if (int rc = check_ready(L, true)) return rc;
+  if (int rc = check_hparams(hp)) return rc;
+  if (L->master2 == nullptr) return fail(ZERO_ERR_STATE, "zero_state_bind_alternate has not been called");
+  if (grad_ptrs == nullptr) return fail(ZERO_ERR_INVALID, "grad_ptrs is NULL");
+  const int64_t n = (int64_t)L->world() * L->n_params();
+  for (int64_t i = 0; i < n; ++i) {
+    if (grad_ptrs[i] != nullptr && !aligned16(grad_ptrs[i]))
+      return fail(ZERO_ERR_INVALID, "grad_ptrs[%lld] is not 16-byte aligned", (long long)i);
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // The host array is staged by the runtime before this call returns.
+  ZERO_CUDA(cudaMemcpyAsync(L->d_table, grad_ptrs, (size_t)n * sizeof(void*),
+                            cudaMemcpyHostToDevice, s));
+  GradSrc src{};
+  src.table = L->d_table;
+  src.n_params = L->n_params();
+  src.table_mode = 1;
+  return launch_step_spec(L, src, hp, s);
+}
+
 int zero_step_per_tensor_launch(zero_layout_t* L, const void* const* grads,
                                 void* const* allreduce_out, const zero_hparams* hp, void* stream) {
   if (int rc = check_ready(L, true)) return rc;

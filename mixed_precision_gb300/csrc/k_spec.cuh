@@ -25,11 +25,15 @@
 
 namespace zg {
 
-// Rank w's gradient pointer for a tile. The speculative step takes flat
-// gradient buffers only (zero_step_speculative checks every pointer), so
-// there is no per-tensor table and no NULL (all-zero) gradient here.
+// Rank w's gradient pointer for a tile: its flat buffer, or its per-tensor
+// pointer from the table, where NULL stands for an all-zero gradient (never
+// read; its values count as +0, as in the reduce kernel).
 template <typename GT>
 __device__ __forceinline__ const GT* spec_grad_ptr(const GradSrc& src, const Tile& tl, int w) {
+  if (src.table_mode) {
+    const void* q = src.table[(int64_t)w * src.n_params + tl.param];
+    return q ? static_cast<const GT*>(q) + tl.in_param : nullptr;
+  }
   return static_cast<const GT*>(src.base[w]) + tl.flat;
 }
 
@@ -89,10 +93,14 @@ __global__ void __launch_bounds__((NC + 1) * 32) k_spec_step(const __grid_consta
       const int nb = clen & ~7;
       unsigned char* base = smem + s * kStage;
       if (nb > 0) {
-        mbar_arrive_expect_tx(&full[s], (uint32_t)nb * (uint32_t)(W * (int)sizeof(GT) + 12));
-        for (int w = 0; w < W; ++w)
-          bulk_g2s(base + w * C * (int)sizeof(GT), spec_grad_ptr<GT>(a.src, tl, w) + pc,
-                   nb * (int)sizeof(GT), &full[s]);
+        int live = 0;  // ranks with a gradient to copy (table mode: non-NULL)
+        for (int w = 0; w < W; ++w) live += spec_grad_ptr<GT>(a.src, tl, w) != nullptr;
+        mbar_arrive_expect_tx(&full[s], (uint32_t)nb * (uint32_t)(live * (int)sizeof(GT) + 12));
+        for (int w = 0; w < W; ++w) {
+          const GT* g = spec_grad_ptr<GT>(a.src, tl, w);
+          if (g != nullptr)
+            bulk_g2s(base + w * C * (int)sizeof(GT), g + pc, nb * (int)sizeof(GT), &full[s]);
+        }
         const int64_t so = tl.shard + pc;
         bulk_g2s(base + kGrad, src_master + so, nb * 4, &full[s]);
         bulk_g2s(base + kGrad + C * 4, src_m + so, nb * 4, &full[s]);
@@ -122,6 +130,15 @@ __global__ void __launch_bounds__((NC + 1) * 32) k_spec_step(const __grid_consta
   int ct = blockIdx.x, cc = 0;
   unsigned k = 0;
   Tile tl = a.tiles[ct < a.n_tiles ? ct : 0];
+  // Ranks whose gradient for the current tile is NULL (table mode only).
+  auto null_mask = [&](const Tile& t) -> uint64_t {
+    if (!a.src.table_mode) return 0ull;
+    uint64_t mk = 0ull;
+    for (int w = 0; w < W; ++w)
+      if (spec_grad_ptr<GT>(a.src, t, w) == nullptr) mk |= 1ull << w;
+    return mk;
+  };
+  uint64_t nulls = ct < a.n_tiles ? null_mask(tl) : 0ull;
   while (ct < a.n_tiles) {
     const int s = (int)(k % S);
     const int clen = min(C, tl.len - cc);
@@ -148,11 +165,21 @@ __global__ void __launch_bounds__((NC + 1) * 32) k_spec_step(const __grid_consta
         const int e = base + 128 * h + 4 * lane;
         if (e >= w1) continue;
         float acc[4];
-        load4_smem(sg + e, acc);
+        if (nulls & 1ull) {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) acc[j] = 0.0f;
+        } else {
+          load4_smem(sg + e, acc);
+        }
 #pragma unroll(WT ? WT : 1)
         for (int w = 1; w < W; ++w) {
           float x[4];
-          load4_smem(sg + w * C + e, x);
+          if ((nulls >> w) & 1ull) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) x[j] = 0.0f;
+          } else {
+            load4_smem(sg + w * C + e, x);
+          }
 #pragma unroll
           for (int j = 0; j < 4; ++j) acc[j] = __fadd_rn(acc[j], x[j]);
         }
@@ -185,9 +212,12 @@ __global__ void __launch_bounds__((NC + 1) * 32) k_spec_step(const __grid_consta
     }
     if (warp == 0 && lane < clen - nb) {  // ragged tail, from global memory
       const int e = nb + lane;
-      float sum = load1(spec_grad_ptr<GT>(a.src, tl, 0), (int64_t)cc + e);
-      for (int w = 1; w < W; ++w)
-        sum = __fadd_rn(sum, load1(spec_grad_ptr<GT>(a.src, tl, w), (int64_t)cc + e));
+      const GT* g0 = spec_grad_ptr<GT>(a.src, tl, 0);
+      float sum = g0 ? load1(g0, (int64_t)cc + e) : 0.0f;
+      for (int w = 1; w < W; ++w) {
+        const GT* gw = spec_grad_ptr<GT>(a.src, tl, w);
+        sum = __fadd_rn(sum, gw ? load1(gw, (int64_t)cc + e) : 0.0f);
+      }
       const CT rc = DT<CT>::from_f32(sum);
       const float rf = DT<CT>::to_f32(rc);
       if (!DT<CT>::finite_bits(rc)) bad = 1u;
@@ -206,7 +236,10 @@ __global__ void __launch_bounds__((NC + 1) * 32) k_spec_step(const __grid_consta
     if (cc >= tl.len) {
       cc = 0;
       ct += gridDim.x;
-      if (ct < a.n_tiles) tl = a.tiles[ct];
+      if (ct < a.n_tiles) {
+        tl = a.tiles[ct];
+        nulls = null_mask(tl);
+      }
     }
   }
   double x = (double)hi + (double)lo + big;

@@ -131,6 +131,12 @@ class ZeroStep:
         abi.zero_step_speculative(self.handle, [g.data_ptr() for g in grads], hp.c(),
                                   _stream_handle(stream))
 
+    def step_speculative_tensors(self, grads_per_rank, hp: Hparams, stream=None) -> None:
+        """step_speculative from per-tensor gradients: grads_per_rank[w][p] is
+        a tensor or None (all-zero gradient, never read)."""
+        ptrs = [(g.data_ptr() if g is not None else 0) for row in grads_per_rank for g in row]
+        abi.zero_step_speculative_tensors(self.handle, ptrs, hp.c(), _stream_handle(stream))
+
     def step_per_tensor_launch(self, grads, hp: Hparams, stream=None) -> None:
         """The same step launched tensor by tensor (the hook-style baseline)."""
         ar = [t.data_ptr() for t in self.allreduce_out] if self.stage == 1 else None

@@ -104,6 +104,15 @@ class Pair:
             self.z.step_per_tensor_launch(dev, hp)
         elif mode == "speculative":
             self.z.step_speculative(dev, hp)
+        elif mode == "speculative_tensors":
+            per = []
+            for r in range(self.W):
+                row = []
+                for off, n in zip(self.z.offsets, self.numel):
+                    t = grads_cpu[r][off:off + n]
+                    row.append(None if (n == 0 or not t.any()) else t.clone().cuda())
+                per.append(row)
+            self.z.step_speculative_tensors(per, hp)
         elif mode == "host":
             pinned = [(g if g.numel() else torch.empty(8, dtype=g.dtype)).pin_memory()
                       for g in grads_cpu]
@@ -145,8 +154,8 @@ class Pair:
             assert abs(gpu_state["clip_coef"] - info.clip_coef) <= 1e-6 * info.clip_coef
         # reduced values: bit-exact (a committed or skipped speculative step
         # never stores them; its fallback does)
-        spec_no_reduce = self.last_mode == "speculative" and (gpu_state["fast_path"] or
-                                                             gpu_state["skipped"])
+        spec_no_reduce = self.last_mode.startswith("speculative") and (gpu_state["fast_path"] or
+                                                                      gpu_state["skipped"])
         if spec_no_reduce:
             pass
         elif self.stage != 1:

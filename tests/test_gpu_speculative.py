@@ -82,6 +82,80 @@ def test_every_branch_matches_oracle(W, stage, gdt, cdt, pdt, bucket):
     assert sets == [1, 0, 0, 0, 0, 0, 1]
 
 
+@pytest.mark.parametrize("W,stage,gdt", [(3, 2, wl.BF16), (4, 3, wl.F16), (2, 2, wl.F32)])
+def test_per_tensor_pointers_match_oracle(W, stage, gdt):
+    """zero_step_speculative_tensors, all-zero parameters passed as NULL (a
+    different set per rank), through commit, skip and fallback."""
+    shapes = small_qwen_shapes()
+    cdt = wl.BF16 if gdt == wl.F32 else -1
+    pdt = wl.BF16 if gdt == wl.F32 else gdt
+    pr = Pair(shapes, W, stage, 50_000, gdt, pdt, cdt, init_scale=8.0, dynamic=True,
+              index=330 + W, speculative=True)
+    n_params = len(shapes)
+    zero = [tuple(range(r, n_params, W + 1)) for r in range(W)]
+    rank, idx = wl.inject_position(pr.numel, pr.z.offsets, W, seed=13)
+    plan = [("commit", Hparams()), ("skip", Hparams()),
+            ("fallback", Hparams(max_grad_norm=1e-4)), ("commit", Hparams(max_grad_norm=0.0))]
+    for step, (kind, hp) in enumerate(plan):
+        g = pr.grads(step, 1e-3)
+        for r in range(W):  # this rank's zero parameters
+            for p in zero[r]:
+                off, n = pr.z.offsets[p], pr.numel[p]
+                g[r][off:off + n] = 0
+        if kind == "skip":
+            g[rank][idx] = float("inf")
+        st, info, gc = pr.step(g, hp, mode="speculative_tensors")
+        pr.check(st, info, gc)
+        assert st["skipped"] == (kind == "skip")
+        # a commit needs the predictor clear: the fallback step sets it, the
+        # next (clip off) step runs predicted and clears it
+        if kind == "commit" and step == 0:
+            assert st["fast_path"] == 1
+
+
+def test_per_tensor_pointers_bit_identical_to_flat():
+    """The same steps from flat buffers (zeros written out) and from per-tensor
+    pointers with NULL for the zero gradients."""
+    shapes = ragged_shapes(21)
+    W = 4
+    a, b = [ZeroStep(shapes, W, 3, 40_000, wl.BF16, wl.BF16) for _ in range(2)]
+    for z in (a, b):
+        z.allocate(speculative=True)
+        z.init(wl.master_init(z.offsets, z.numels, z.np, 0.02, wl.master_seed(21), device="cuda"),
+               init_scale=8.0, dynamic=True)
+    mask = _real_shard_mask(a)
+    numel = wl.numels(shapes)
+    rank, idx = wl.inject_position(numel, a.offsets, W, seed=22)
+    fast = []
+    for step, kind in enumerate(["c", "c", "inf", "clip", "clip", "c", "c"]):
+        grads = [wl.flat_grads(a.offsets, numel, a.np, 1e-3, wl.grad_seed(450, r, step), wl.BF16,
+                               device="cuda") for r in range(W)]
+        per = []
+        for r in range(W):
+            row = []
+            for p, (off, n) in enumerate(zip(a.offsets, numel)):
+                if n == 0 or (p + r + step) % 3 == 0:
+                    grads[r][off:off + n] = 0
+                    row.append(None)
+                else:
+                    row.append(grads[r][off:off + n])
+            per.append(row)
+        if kind == "inf":
+            grads[rank][idx] = float("inf")
+            p_inf = int(np.searchsorted(np.array(a.offsets), idx, side="right") - 1)
+            per[rank][p_inf] = grads[rank][a.offsets[p_inf]:a.offsets[p_inf] + numel[p_inf]]
+        hp = Hparams(max_grad_norm=1e-4) if kind == "clip" else Hparams()
+        a.step_speculative(grads, hp)
+        b.step_speculative_tensors(per, hp)
+        torch.cuda.synchronize()
+        st = _assert_same(a, b, mask)
+        assert a.scaler_state()["fast_path"] == st["fast_path"]
+        fast.append(st["fast_path"])
+    assert fast == [1, 1, 0, 0, 0, 0, 1]
+    a.close()
+    b.close()
+
+
 def _twin(shapes, W, stage, bucket, gdt, pdt, cdt=-1, init_scale=8.0, seed=5):
     """Two layouts with identical initial state: one speculative, one two-pass."""
     zs = []
