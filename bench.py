@@ -434,6 +434,26 @@ def run_ours(args) -> dict | None:
     grads[0][z.offsets[0]] = saved
     torch.cuda.synchronize()
 
+    # K4: the cast-out parameters copied into per-tensor storage (one replica),
+    # what a framework's parameter tensors would receive after the step.
+    gather_params = None
+    if not args.tensors:
+        pt = [torch.empty(max(n, 8), dtype=z.params_flat.dtype, device=device) for n in numel]
+        views = [[t[:n] if n else t for t, n in zip(pt, numel)]]
+        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        for _ in range(2):
+            z.gather(views)
+        g0.record()
+        for _ in range(10):
+            z.gather(views)
+        g1.record()
+        torch.cuda.synchronize()
+        ms = g0.elapsed_time(g1) / 10
+        pbytes = wl.ELEM_BYTES[w.param_dtype]
+        gather_params = {"replicas": 1, "ms": ms, "gbs": 2 * pbytes * info.n_real / (ms / 1e3) / 1e9,
+                         "bytes_per_param": 2 * pbytes}
+        del pt, views
+
     # ZeRO-3: the per-bucket all-gather of the sharded parameters into a flat
     # working buffer (what a forward pass would prefetch bucket by bucket).
     gather = None
@@ -555,6 +575,7 @@ def run_ours(args) -> dict | None:
         "fast_path": fast_path,
         "skip_step_ms": skip_ms,
         "zero3_gather": gather,
+        "gather_params": gather_params,
         "e2e": e2e,
         "gpu_launches": K * ((2 * sum(1 for n in numel if n > 0) + 1) if args.per_tensor_launch
                              else (6 if args.speculative else 3)),

@@ -65,15 +65,24 @@ cudaError_t launch_state_copy(const Tile* tiles, int n_tiles, float* const* shar
 __global__ void __launch_bounds__(kThreads)
     k_gather(const Tile* __restrict__ tiles, int n_tiles, const uint16_t* __restrict__ src,
              void* const* __restrict__ dst_table, int n_params, int n_replicas, int src_by_shard) {
+  constexpr int U = 4;  // independent vector loads per thread before the stores
   for (int t = blockIdx.x; t < n_tiles; t += gridDim.x) {
     const Tile tl = tiles[t];
     const uint16_t* s = src + (src_by_shard ? tl.shard : tl.flat);
+    const uint4* s4 = reinterpret_cast<const uint4*>(s);
     for (int k = 0; k < n_replicas; ++k) {
       uint16_t* d = static_cast<uint16_t*>(dst_table[(int64_t)k * n_params + tl.param]) + tl.in_param;
       const bool vec = (reinterpret_cast<uintptr_t>(d) & 15u) == 0;
       const int nvec = vec ? (tl.len >> 3) : 0;
-      for (int vi = threadIdx.x; vi < nvec; vi += kThreads)
-        st_stream(d + (int64_t)vi * 8, __ldg(reinterpret_cast<const uint4*>(s) + vi));
+      for (int v0 = threadIdx.x; v0 < nvec; v0 += U * kThreads) {
+        uint4 x[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+          if (v0 + u * kThreads < nvec) x[u] = __ldg(s4 + v0 + u * kThreads);
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+          if (v0 + u * kThreads < nvec) st_stream(d + (int64_t)(v0 + u * kThreads) * 8, x[u]);
+      }
       for (int i = nvec * 8 + threadIdx.x; i < tl.len; i += kThreads) d[i] = s[i];
     }
   }

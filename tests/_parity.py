@@ -154,8 +154,8 @@ class Pair:
             assert abs(gpu_state["clip_coef"] - info.clip_coef) <= 1e-6 * info.clip_coef
         # reduced values: bit-exact (a committed or skipped speculative step
         # never stores them; its fallback does)
-        spec_no_reduce = self.last_mode.startswith("speculative") and (gpu_state["fast_path"] or
-                                                                      gpu_state["skipped"])
+        spec_no_reduce = (self.last_mode or "").startswith("speculative") and (
+            gpu_state["fast_path"] or gpu_state["skipped"])
         if spec_no_reduce:
             pass
         elif self.stage != 1:
