@@ -61,6 +61,8 @@ def parse_args(argv=None):
     ap.add_argument("--world", type=int, default=None, help="override the simulated world size")
     ap.add_argument("--bucket-bytes", type=int, default=None, help="override the bucket size")
     ap.add_argument("--stage", type=int, default=None, help="override the ZeRO stage (1, 2, 3)")
+    ap.add_argument("--graph", action="store_true",
+                    help="also time the step captured into a CUDA graph and replayed (flat modes)")
     ap.add_argument("--clip", type=float, default=None,
                     help="override max_grad_norm (<= 0: no clipping)")
     ap.add_argument("--speculative", action="store_true",
@@ -419,6 +421,31 @@ def run_ours(args) -> dict | None:
     k2 = [ev[k][1].elapsed_time(ev[k][2]) for k in range(K)]
     k3 = [ev[k][2].elapsed_time(ev[k][3]) for k in range(K)]
 
+    # The same step captured once into a CUDA graph and replayed K times.
+    graph = None
+    if args.graph and per_tensor is None and not args.per_tensor_launch:
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(g, stream=side):
+                do_step()
+        torch.cuda.current_stream().wait_stream(side)
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        r0, r1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        r0.record()
+        for _ in range(K):
+            g.replay()
+        r1.record()
+        torch.cuda.synchronize()
+        st_g = z.scaler_state()
+        assert st_g["overflow"] == 0 and st_g["steps"] == K + W + 3 + K, st_g
+        graph = {"ms_per_step": r0.elapsed_time(r1) / K, "steps": K,
+                 "value": job_value(info.n_real, world, r0.elapsed_time(r1) / 1e3 / K)}
+        del g
+
     # A skipped step: +inf in one element, the update kernel returns at once.
     saved = grads[0][z.offsets[0]].clone()
     grads[0][z.offsets[0]] = float("inf")
@@ -574,6 +601,7 @@ def run_ours(args) -> dict | None:
         "kernels_ms": kernels,
         "fast_path": fast_path,
         "skip_step_ms": skip_ms,
+        "graph": graph,
         "zero3_gather": gather,
         "gather_params": gather_params,
         "e2e": e2e,
