@@ -61,6 +61,9 @@ def parse_args(argv=None):
     ap.add_argument("--world", type=int, default=None, help="override the simulated world size")
     ap.add_argument("--bucket-bytes", type=int, default=None, help="override the bucket size")
     ap.add_argument("--stage", type=int, default=None, help="override the ZeRO stage (1, 2, 3)")
+    ap.add_argument("--profile-range", action="store_true",
+                    help="bracket the timed steps with cudaProfilerStart/Stop (for "
+                         "nsys/ncu capture ranges on the CUDA profiler API)")
     ap.add_argument("--graph", action="store_true",
                     help="also time the step captured into a CUDA graph and replayed (flat modes)")
     ap.add_argument("--clip", type=float, default=None,
@@ -400,11 +403,15 @@ def run_ours(args) -> dict | None:
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
+    if args.profile_range:
+        torch.cuda.cudart().cudaProfilerStart()
     t_start.record()
     for k in range(K):
         abi.zero_set_step_events(z.handle, [e.cuda_event for e in ev[k]])
         do_step()
     t_end.record()
+    if args.profile_range:
+        torch.cuda.cudart().cudaProfilerStop()
     torch.cuda.synchronize()
     abi.zero_set_step_events(z.handle, None)
     clocks = sampler.stop()
