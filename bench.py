@@ -560,11 +560,14 @@ def run_ours(args) -> dict | None:
         # events: [single pass] [its finalize] [guarded fallback kernels + restore]
         spec_bytes = N * info.step_bytes_per_elem
         dom = ("k_spec_step", spec_bytes, k1_ms)
-        kernels = {"k_spec_step": k1_ms, "k_finalize_spec": k2_ms, "guarded_fallback": k3_ms,
+        kernels = {"k_spec_step": k1_ms, "between": k2_ms, "guarded_fallback": k3_ms,
                    "k_spec_step_gbs": spec_bytes / (k1_ms / 1e3) / 1e9}
     else:
         dom = ("k_adamw_cast", k3_bytes, k3_ms) if k3_ms >= k1_ms else \
             ("k_reduce_norm", k1_bytes, k1_ms)
+        # "k_finalize": the interval between the reduce and the update (the
+        # finalize runs inside the reduce's last block, or as its own kernel
+        # with the register-staged reduce and per-tensor launches)
         kernels = {"k_reduce_norm": k1_ms, "k_finalize": k2_ms, "k_adamw_cast": k3_ms,
                    "k_reduce_norm_gbs": k1_bytes / (k1_ms / 1e3) / 1e9,
                    "k_adamw_cast_gbs": k3_bytes / (k3_ms / 1e3) / 1e9}
@@ -612,8 +615,10 @@ def run_ours(args) -> dict | None:
         "zero3_gather": gather,
         "gather_params": gather_params,
         "e2e": e2e,
+        # two-pass: reduce (its last block finalizes) + update; speculative:
+        # single pass (finalizes) + guarded reduce + update + guarded restore
         "gpu_launches": K * ((2 * sum(1 for n in numel if n > 0) + 1) if args.per_tensor_launch
-                             else (6 if args.speculative else 3)),
+                             else (4 if args.speculative else 2)),
         "clocks": clocks,
     }
     z.close()

@@ -255,9 +255,11 @@ int zero_state_init(zero_layout_t* layout, const float* master_init_flat,
  *                  comm_dtype == grad_dtype; padding is not written).
  *                  stage 2: must be NULL.
  *   hp             host struct, copied at the call.
- * Enqueues three kernels on `stream`:
- *   reduce + overflow/norm partials, finalize (norm, clip, scaler, t),
- *   fused unscale/clip/AdamW/cast-out (returns at once on a skipped step).
+ * Enqueues two kernels on `stream` (three with the register-staged reduce):
+ *   reduce + overflow/norm partials, whose last block to finish runs the
+ *   finalize (norm, clip, scaler, t); then the fused unscale/clip/AdamW/
+ *   cast-out (returns at once on a skipped step). After ZERO_ERR_TIMEOUT the
+ *   state must be initialised again (zero_state_init).
  * Reduced value r = RNE_comm(g_0 + ... + g_{W-1}) (fp32 adds in rank order);
  * overflow = any non-finite r over real elements; on overflow the update is
  * skipped, S is multiplied by backoff (dynamic mode, floored at min_scale)
@@ -281,7 +283,7 @@ int zero_step_tensors(zero_layout_t* layout, const void* const* grad_ptrs,
  * the finalize, then one update launch per parameter (2P + 1 launches). This
  * is the per-parameter, hook-driven form of the prior art ([NM] "Benchmarks":
  * about 2k collective calls per backward, bound by launch cost), kept as the
- * baseline the flat three-launch step is measured against. Arguments,
+ * baseline the flat two-launch step is measured against. Arguments,
  * arithmetic and results are those of zero_step; only the norm's summation
  * order differs. */
 int zero_step_per_tensor_launch(zero_layout_t* layout, const void* const* grads,

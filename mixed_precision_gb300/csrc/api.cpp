@@ -313,6 +313,15 @@ int launch_step(zero_layout* L, const GradSrc& src, void* const* allreduce_out,
   ra.error = &L->d_state->error;
   ra.state = L->d_state;
   ra.guarded = guarded;
+  Hparams h{hp->lr, hp->beta1, hp->beta2, hp->eps, hp->weight_decay, hp->max_grad_norm,
+            hp->grad_divisor};
+  // The pipelined reduce finishes the step in its last block when one launch
+  // covers every tile; otherwise (register-staged reduce, empty model) the
+  // finalize kernel follows.
+  const bool fused = n_tiles > 0 && L->reduce_variant == 1;
+  ra.fuse_finalize = fused ? 1 : 0;
+  ra.hp = h;
+  ra.state_rw = L->d_state;
   int n_part = 0;
   if (L->timing) ZERO_CUDA(cudaEventRecord(L->events[0], s));
   if (n_tiles > 0) {
@@ -326,10 +335,8 @@ int launch_step(zero_layout* L, const GradSrc& src, void* const* allreduce_out,
     L->k1_recorded = true;
   }
   if (L->timing) ZERO_CUDA(cudaEventRecord(L->events[1], s));
-  Hparams h{hp->lr, hp->beta1, hp->beta2, hp->eps, hp->weight_decay, hp->max_grad_norm,
-            hp->grad_divisor};
-  cudaError_t e;
-  {
+  cudaError_t e = cudaSuccess;
+  if (!fused) {
     Range r(guarded ? "K2 finalize (guarded)" : "K2 finalize");
     e = launch_finalize(L->d_part, L->d_ovf, n_part, W, h, L->d_state, guarded, s);
   }
@@ -377,6 +384,8 @@ int launch_step_spec(zero_layout* L, const GradSrc& src, const zero_hparams* hp,
   sa.part_sumsq = L->d_part;
   sa.part_ovf = L->d_ovf;
   sa.chunk = L->chunk_spec;
+  sa.fuse_finalize = 1;  // the single pass's last block runs the speculative finalize
+  sa.state_rw = L->d_state;
   sa.error = &L->d_state->error;
   if (L->timing) ZERO_CUDA(cudaEventRecord(L->events[0], s));
   Range r_all("speculative step");
@@ -384,8 +393,6 @@ int launch_step_spec(zero_layout* L, const GradSrc& src, const zero_hparams* hp,
                               L->grid_spec, s);
   if (e != cudaSuccess) return cuda_fail(e, "speculative kernel launch");
   if (L->timing) ZERO_CUDA(cudaEventRecord(L->events[1], s));
-  e = launch_finalize_spec(L->d_part, L->d_ovf, L->grid_spec, L->world(), sa.hp, L->d_state, s);
-  if (e != cudaSuccess) return cuda_fail(e, "speculative finalize launch");
   if (L->timing) ZERO_CUDA(cudaEventRecord(L->events[2], s));
   const bool timing = L->timing;
   L->timing = false;

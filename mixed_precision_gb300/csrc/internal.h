@@ -59,6 +59,8 @@ struct DevState {
   int fast_path;       // last step was committed by the speculative single pass
   int predict_fallback;  // the last finalized step clipped: the next speculative
                          // step skips its single pass and runs the two-pass kernels
+  unsigned blocks_done;  // blocks of the running reduce / speculative pass that have
+                         // written their partial (wraps to 0 after the last one)
 };
 
 struct Hparams {  // mirror of zero_hparams
@@ -100,6 +102,10 @@ struct ReduceArgs {
   unsigned* error;      // DevState::error
   const DevState* state;
   int guarded;          // 1: run only if state->need_fallback (the speculative step's fallback)
+  int fuse_finalize;    // 1: the last block to finish runs the finalize (one launch covers
+                        //    every partial); 0: a separate finalize kernel follows
+  Hparams hp;           // for the fused finalize
+  DevState* state_rw;   // the same state, written by the fused finalize
 };
 
 struct UpdateArgs {
@@ -164,6 +170,8 @@ struct SpecArgs {  // arguments of k_spec_step
   double* part_sumsq;
   unsigned* part_ovf;
   int chunk;
+  int fuse_finalize;   // 1: the last block to finish runs the speculative finalize
+  DevState* state_rw;  // the same state, written by it
   unsigned* error;
 };
 
@@ -173,8 +181,6 @@ int spec_chunk(int world, int grad_dtype, int stage_bytes);
 cudaError_t launch_spec(const SpecArgs* args, int grad_dtype, int comm_dtype, int param_dtype, int world,
                         int grid, cudaStream_t s);
 int spec_blocks_per_sm(int grad_dtype, int comm_dtype, int param_dtype, int world, int chunk);
-cudaError_t launch_finalize_spec(const double* part_sumsq, const unsigned* part_ovf, int n_part,
-                                 int world, const Hparams& hp, DevState* st, cudaStream_t s);
 
 // Record a failure message for zero_last_error() and return `code` (for entry
 // points defined outside api.cpp).

@@ -19,6 +19,7 @@
 #pragma once
 
 #include "bulk.cuh"
+#include "finalize.cuh"
 #include "vec.cuh"
 
 namespace zg {
@@ -339,6 +340,7 @@ __global__ void __launch_bounds__((NC + 1) * 32)
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) x += __shfl_down_sync(0xffffffffu, x, o);
   const unsigned any = __any_sync(0xffffffffu, bad != 0u) ? 1u : 0u;
+  unsigned last = 0u;
   if (lane == 0) {
     s_part[warp] = x;
     s_flag[warp] = any;
@@ -353,7 +355,21 @@ __global__ void __launch_bounds__((NC + 1) * 32)
       }
       a.part_sumsq[blockIdx.x] = total;
       a.part_ovf[blockIdx.x] = f;
+      if (a.fuse_finalize) {  // publish the partial, then count this block in
+        __threadfence();
+        last = atomicInc(&a.state_rw->blocks_done, gridDim.x - 1) == gridDim.x - 1 ? 1u : 0u;
+      }
     }
+  }
+  // The last block to finish (every other block has written its partial and
+  // is past its reads of the state) finishes the step: the global sums and
+  // finalize_state, by the warp that counted it in.
+  if (a.fuse_finalize && __shfl_sync(0xffffffffu, last, 0)) {
+    __threadfence();
+    double sumsq;
+    unsigned ovf;
+    warp_sum_partials(a.part_sumsq, a.part_ovf, gridDim.x, sumsq, ovf);
+    if (lane == 0) finalize_state(sumsq, ovf, a.world, a.hp, a.state_rw);
   }
 }
 

@@ -55,7 +55,10 @@ __global__ void __launch_bounds__((NC + 1) * 32) k_spec_step(const __grid_consta
   const int kStage = kGrad + 12 * C;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const DevState* st = a.state;
-  if (st->predict_fallback) return;  // predicted to clip: the two-pass kernels run instead
+  if (st->predict_fallback) {  // predicted to clip: the two-pass kernels run instead
+    if (a.fuse_finalize && blockIdx.x == 0 && threadIdx.x == 0) spec_predicted_state(a.state_rw);
+    return;
+  }
   const int cs = st->cur;
   const float* src_master = a.master[cs];
   const float* src_m = a.m[cs];
@@ -246,6 +249,7 @@ __global__ void __launch_bounds__((NC + 1) * 32) k_spec_step(const __grid_consta
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) x += __shfl_down_sync(0xffffffffu, x, o);
   const unsigned any = __any_sync(0xffffffffu, bad != 0u) ? 1u : 0u;
+  unsigned last = 0u;
   if (lane == 0) {
     s_part[warp] = x;
     s_flag[warp] = any;
@@ -260,7 +264,20 @@ __global__ void __launch_bounds__((NC + 1) * 32) k_spec_step(const __grid_consta
       }
       a.part_sumsq[blockIdx.x] = total;
       a.part_ovf[blockIdx.x] = f;
+      if (a.fuse_finalize) {
+        __threadfence();
+        last = atomicInc(&a.state_rw->blocks_done, gridDim.x - 1) == gridDim.x - 1 ? 1u : 0u;
+      }
     }
+  }
+  // The last block to finish runs the speculative finalize (commit, skip or
+  // fallback); every other block is past its reads of the state by then.
+  if (a.fuse_finalize && __shfl_sync(0xffffffffu, last, 0)) {
+    __threadfence();
+    double sumsq;
+    unsigned ovf;
+    warp_sum_partials(a.part_sumsq, a.part_ovf, gridDim.x, sumsq, ovf);
+    if (lane == 0) finalize_spec_state(sumsq, ovf, a.world, a.hp, a.state_rw);
   }
 }
 

@@ -1,6 +1,7 @@
 // K2 (finalize) and K3 (fused unscale / clip / AdamW / cast-out), plus the
 // launch dispatch of K1.
 #include "bulk.cuh"
+#include "finalize.cuh"
 #include "vec.cuh"
 
 namespace zg {
@@ -58,17 +59,12 @@ int reduce_blocks_per_sm(int grad_dtype, int comm_dtype, int world, int stage, i
 }
 
 // ---------------------------------------------------------------------------
-// K2: finalize. One block.
-// "3.7 Megatron-LM, DeepSpeed & Parallelism in Practice", "ZeRO-Offload and
-// ZeRO-Infinity": gradient_clipping, and fp16 loss_scale 0 (dynamic) with a
-// loss_scale_window. "nano-deepspeed (Teaching Edition)", "2. Current Feature
-// Range": FP16 dynamic loss scaling. The pages print no formula; the reading:
-//   inv = 1 / (S * D), norm = inv * sqrt(sum r^2),
-//   clip = min(1, max_norm / (norm + 1e-6)) (1 when max_norm <= 0);
-//   overflow -> skip, S <- max(S * backoff, min_scale) (dynamic), counter <- 0;
-//   clean    -> t += 1, counter += 1, S <- S * growth when counter == N.
-// The block partials are summed in a fixed order (strided per thread, then a
-// fixed shuffle tree), so the norm is the same on every run.
+// K2: finalize. One block: the global sums, then finalize_state (finalize.cuh,
+// which cites the passages and states the reading). Used where the reduce
+// kernel cannot finish the step itself (per-tensor launches, the
+// register-staged reduce, an empty model); otherwise the reduce kernel's last
+// block does this work. The block partials are summed in a fixed order
+// (strided per thread, then a fixed shuffle tree): the same norm on every run.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kFinalizeThreads)
     k_finalize(const double* __restrict__ part_sumsq, const unsigned* __restrict__ part_ovf,
@@ -86,52 +82,7 @@ __global__ void __launch_bounds__(kFinalizeThreads)
   const unsigned any = block_or<kFinalizeThreads>(ovf, s_or);
   if (threadIdx.x != 0) return;
 
-  const double S = st->scale;
-  const double D = hp.grad_divisor > 0.0 ? hp.grad_divisor : (double)world;
-  const double inv = 1.0 / (S * D);
-  st->steps += 1;
-  st->need_fallback = 0;
-  st->restore_params = 0;
-  st->fast_path = 0;
-  st->norm_sq_raw = sumsq;
-  st->grad_norm = inv * sqrt(sumsq);
-  st->overflow = any ? 1 : 0;
-  if (any) {
-    st->skipped = 1;
-    st->skip = 1;
-    st->clip_coef = 0.0;
-    if (st->dynamic) {
-      const double s2 = S * st->backoff_factor;
-      st->scale = s2 < st->min_scale ? st->min_scale : s2;
-    }
-    st->counter = 0;
-    return;
-  }
-  double c = 1.0;
-  if (hp.max_grad_norm > 0.0) {
-    c = hp.max_grad_norm / (st->grad_norm + 1e-6);
-    if (c > 1.0) c = 1.0;
-  }
-  st->skipped = 0;
-  st->skip = 0;
-  st->clip_coef = c;
-  st->predict_fallback = c < 1.0 ? 1 : 0;
-  st->t += 1;
-  const AdamScalars a = derive_adam_scalars(hp, inv, c, st->t);
-  st->gscale = a.gs;
-  st->decay = a.decay;
-  st->step_size = a.step;
-  st->inv_sqrt_bc2 = a.isb2;
-  st->beta1 = a.b1;
-  st->one_minus_beta1 = a.omb1;
-  st->beta2 = a.b2;
-  st->one_minus_beta2 = a.omb2;
-  st->eps = a.eps;
-  st->counter += 1;
-  if (st->dynamic && st->counter == st->growth_interval) {
-    st->scale = S * st->growth_factor;
-    st->counter = 0;
-  }
+  finalize_state(sumsq, any, world, hp, st);
 }
 
 cudaError_t launch_finalize(const double* part_sumsq, const unsigned* part_ovf, int n_part,
@@ -439,106 +390,9 @@ int update_blocks_per_sm(int comm_dtype, int param_dtype, int variant) {
 namespace zg {
 
 // ---------------------------------------------------------------------------
-// The speculative step's finalize and launch (see k_spec.cuh). Same sums and
-// norm as k_finalize; then:
-//   overflow      -> skip (as k_finalize) and recast the params, which the
-//                    speculative pass overwrote, from the untouched master;
-//   clip active   -> ask for the two-pass step (need_fallback), no bookkeeping;
-//   otherwise     -> commit: the other state set becomes current, t += 1, the
-//                    scaler counts a clean step; the update kernel is skipped.
-// A one-bit predictor saves the wasted pass while clipping stays active: every
-// finalize records whether its step clipped (DevState::predict_fallback), and
-// while it is set the single pass returns at once and this kernel goes
-// straight to the two-pass kernels. Only the step on which clipping switches
-// on runs both.
+// The speculative step's launch (k_spec.cuh). Its last block runs the
+// speculative finalize (finalize_spec_state): commit, skip or fallback.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kFinalizeThreads)
-    k_finalize_spec(const double* __restrict__ part_sumsq, const unsigned* __restrict__ part_ovf,
-                    int n_part, int world, const Hparams hp, DevState* __restrict__ st) {
-  if (st->predict_fallback) {  // the single pass did not run: go to the two-pass kernels
-    if (threadIdx.x == 0) {
-      st->need_fallback = 1;
-      st->restore_params = 0;
-      st->fast_path = 0;
-      st->skip = 1;
-    }
-    return;
-  }
-  __shared__ double s_red[kFinalizeThreads / 32];
-  __shared__ unsigned s_or[kFinalizeThreads / 32];
-  double acc = 0.0;
-  unsigned ovf = 0u;
-  for (int i = threadIdx.x; i < n_part; i += kFinalizeThreads) {
-    acc += part_sumsq[i];
-    ovf |= part_ovf[i];
-  }
-  const double sumsq = block_sum<kFinalizeThreads>(acc, s_red);
-  const unsigned any = block_or<kFinalizeThreads>(ovf, s_or);
-  if (threadIdx.x != 0) return;
-
-  const double S = st->scale;
-  const double D = hp.grad_divisor > 0.0 ? hp.grad_divisor : (double)world;
-  const double inv = 1.0 / (S * D);
-  st->need_fallback = 0;
-  st->restore_params = 0;
-  st->fast_path = 0;
-  st->norm_sq_raw = sumsq;
-  st->grad_norm = inv * sqrt(sumsq);
-  st->overflow = any ? 1 : 0;
-  if (any) {
-    st->steps += 1;
-    st->skipped = 1;
-    st->skip = 1;
-    st->clip_coef = 0.0;
-    st->restore_params = 1;
-    if (st->dynamic) {
-      const double s2 = S * st->backoff_factor;
-      st->scale = s2 < st->min_scale ? st->min_scale : s2;
-    }
-    st->counter = 0;
-    return;
-  }
-  double c = 1.0;
-  if (hp.max_grad_norm > 0.0) {
-    c = hp.max_grad_norm / (st->grad_norm + 1e-6);
-    if (c > 1.0) c = 1.0;
-  }
-  if (c < 1.0) {  // clipping active: the guarded two-pass kernels redo the step
-    st->need_fallback = 1;
-    st->skip = 1;
-    st->predict_fallback = 1;
-    return;
-  }
-  st->steps += 1;
-  st->skipped = 0;
-  st->skip = 1;  // the update already happened
-  st->clip_coef = 1.0;
-  st->t += 1;
-  st->cur ^= 1;
-  st->fast_path = 1;
-  const AdamScalars a = derive_adam_scalars(hp, inv, 1.0, st->t);
-  st->gscale = a.gs;
-  st->decay = a.decay;
-  st->step_size = a.step;
-  st->inv_sqrt_bc2 = a.isb2;
-  st->beta1 = a.b1;
-  st->one_minus_beta1 = a.omb1;
-  st->beta2 = a.b2;
-  st->one_minus_beta2 = a.omb2;
-  st->eps = a.eps;
-  st->counter += 1;
-  if (st->dynamic && st->counter == st->growth_interval) {
-    st->scale = S * st->growth_factor;
-    st->counter = 0;
-  }
-}
-
-cudaError_t launch_finalize_spec(const double* part_sumsq, const unsigned* part_ovf, int n_part,
-                                 int world, const Hparams& hp, DevState* st, cudaStream_t s) {
-  k_finalize_spec<<<1, kFinalizeThreads, 0, s>>>(part_sumsq, part_ovf, n_part, world, hp, st);
-  return cudaGetLastError();
-}
-
 const void* spec_kernel_f32(int comm_dtype, int param_dtype, int world);
 const void* spec_kernel_f16(int comm_dtype, int param_dtype, int world);
 const void* spec_kernel_bf16(int comm_dtype, int param_dtype, int world);
