@@ -39,9 +39,9 @@ L2_BYTES = 129 * 1000 * 1000
 NCU_TRAFFIC_PER_ELEM = {
     # profiles/k_adamw_cast_ws_qwen3_layers8.md: (1.7628 + 1.7006) GB / 125,847,552 elements
     "k_adamw_cast": 27.52,
-    # profiles/k_reduce_norm_ws_qwen3_layers8.md: (504.0 + 205.6) MB / 125,847,552 elements
-    "k_reduce_norm": 5.639,
-    # profiles/k_spec_step_qwen3_layers8.md: (2.0146 + 1.7138) GB / 125,847,552 elements
+    # profiles/k_reduce_norm_ws_qwen3_layers8.md: (504.1 + 204.9) MB / 125,847,552 elements
+    "k_reduce_norm": 5.634,
+    # profiles/k_spec_step_qwen3_layers8.md: (2.0146 + 1.7137) GB / 125,847,552 elements
     "k_spec_step": 29.63,
 }
 
