@@ -48,8 +48,14 @@ __device__ inline void finalize_state(double sumsq, unsigned any, int world, con
   st->skip = 0;
   st->clip_coef = c;
   st->predict_fallback = c < 1.0 ? 1 : 0;
+  double b1t, b2t;
+  bias_powers(hp, st, b1t, b2t);
   st->t += 1;
-  const AdamScalars a = derive_adam_scalars(hp, inv, c, st->t);
+  st->beta1_pow = b1t;
+  st->beta2_pow = b2t;
+  st->beta1_pow_of = hp.beta1;
+  st->beta2_pow_of = hp.beta2;
+  const AdamScalars a = derive_adam_scalars(hp, inv, c, b1t, b2t);
   st->gscale = a.gs;
   st->decay = a.decay;
   st->step_size = a.step;
@@ -108,10 +114,16 @@ __device__ inline void finalize_spec_state(double sumsq, unsigned any, int world
   st->skipped = 0;
   st->skip = 1;  // the update already happened
   st->clip_coef = 1.0;
+  double b1t, b2t;
+  bias_powers(hp, st, b1t, b2t);
   st->t += 1;
+  st->beta1_pow = b1t;
+  st->beta2_pow = b2t;
+  st->beta1_pow_of = hp.beta1;
+  st->beta2_pow_of = hp.beta2;
   st->cur ^= 1;
   st->fast_path = 1;
-  const AdamScalars a = derive_adam_scalars(hp, inv, 1.0, st->t);
+  const AdamScalars a = derive_adam_scalars(hp, inv, 1.0, b1t, b2t);
   st->gscale = a.gs;
   st->decay = a.decay;
   st->step_size = a.step;
@@ -145,9 +157,23 @@ __device__ inline void warp_sum_partials(const double* part, const unsigned* ovf
   const int lane = threadIdx.x & 31;
   double acc = 0.0;
   unsigned o = 0u;
-  for (int i = lane; i < n; i += 32) {
-    acc += __ldcg(part + i);
-    o |= __ldcg(ovf + i);
+  // Eight independent loads in flight per lane, then the adds in index order
+  // (lane, lane + 32, ...): one L2 round trip per eight partials.
+  constexpr int U = 8;
+  for (int base = lane; base < n; base += 32 * U) {
+    double v[U];
+    unsigned f[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int i = base + 32 * u;
+      v[u] = i < n ? __ldcg(part + i) : 0.0;
+      f[u] = i < n ? __ldcg(ovf + i) : 0u;
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      acc += v[u];
+      o |= f[u];
+    }
   }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) {

@@ -61,6 +61,8 @@ struct DevState {
                          // step skips its single pass and runs the two-pass kernels
   unsigned blocks_done;  // blocks of the running reduce / speculative pass that have
                          // written their partial (wraps to 0 after the last one)
+  double beta1_pow, beta2_pow;        // beta1^t and beta2^t as running products ...
+  double beta1_pow_of, beta2_pow_of;  // ... of these betas (NaN: not valid, use pow)
 };
 
 struct Hparams {  // mirror of zero_hparams

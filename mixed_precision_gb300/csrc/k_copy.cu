@@ -195,6 +195,8 @@ __global__ void k_scaler_restore(DevState* st, double scale, long long counter, 
   st->scale = scale;
   st->counter = counter;
   st->t = t;
+  // the running beta powers no longer match t: the next step uses pow
+  st->beta1_pow_of = st->beta2_pow_of = __longlong_as_double(0x7FF8000000000000ll);
 }
 
 cudaError_t launch_scaler_restore(DevState* st, double scale, long long counter, long long t,

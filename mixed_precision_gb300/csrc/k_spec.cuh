@@ -75,7 +75,9 @@ __global__ void __launch_bounds__((NC + 1) * 32) k_spec_step(const __grid_consta
     s_done = 0u;
     const double D = a.hp.grad_divisor > 0.0 ? a.hp.grad_divisor : (double)a.world;
     const double inv = 1.0 / (st->scale * D);
-    s_sc = derive_adam_scalars(a.hp, inv, 1.0, st->t + 1);
+    double b1t, b2t;  // the same powers the finalize will commit with
+    bias_powers(a.hp, st, b1t, b2t);
+    s_sc = derive_adam_scalars(a.hp, inv, 1.0, b1t, b2t);
     mbar_init_fence();
   }
   __syncthreads();

@@ -100,6 +100,8 @@ __global__ void k_state_init(const ScalerCfg cfg, DevState* st) {
   z.backoff_factor = cfg.backoff_factor;
   z.min_scale = cfg.min_scale;
   z.skip = 1;  // nothing to apply before the first finalize
+  z.beta1_pow = z.beta2_pow = 1.0;  // beta^0
+  z.beta1_pow_of = z.beta2_pow_of = __longlong_as_double(0x7FF8000000000000ll);  // NaN: use pow
   *st = z;
 }
 

@@ -193,10 +193,28 @@ struct AdamScalars {
 // inverse `inv` = 1/(S*D), the clip coefficient and the step count t of the
 // update. The finalize kernel and the speculative pass both use this, so the
 // two produce identical scalars.
+// beta1^(t+1) and beta2^(t+1) for the step after the state's t. The state
+// keeps beta^t as a running product, so this is one fp64 multiply each
+// (GB300's fp64 pipe is narrow, and pow on one thread took most of the
+// finalize's ~10 us); pow is used when the products are not valid for these
+// betas (the first step, a restored t, betas changed between steps). The
+// product differs from pow by at most about t rounding errors of 2^-53.
+__device__ __forceinline__ void bias_powers(const Hparams& hp, const DevState* st, double& b1t,
+                                            double& b2t) {
+  if (hp.beta1 == st->beta1_pow_of && hp.beta2 == st->beta2_pow_of) {
+    b1t = st->beta1_pow * hp.beta1;
+    b2t = st->beta2_pow * hp.beta2;
+  } else {
+    b1t = pow(hp.beta1, (double)(st->t + 1));
+    b2t = pow(hp.beta2, (double)(st->t + 1));
+  }
+}
+
+// b1t = beta1^t and b2t = beta2^t for the step's t (bias_powers).
 __device__ __forceinline__ AdamScalars derive_adam_scalars(const Hparams& hp, double inv, double c,
-                                                          long long t) {
-  const double bc1 = 1.0 - pow(hp.beta1, (double)t);
-  const double bc2 = 1.0 - pow(hp.beta2, (double)t);
+                                                          double b1t, double b2t) {
+  const double bc1 = 1.0 - b1t;
+  const double bc2 = 1.0 - b2t;
   AdamScalars s;
   s.gs = (float)(inv * c);
   s.decay = (float)(1.0 - hp.lr * hp.weight_decay);
