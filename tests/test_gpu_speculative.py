@@ -199,6 +199,7 @@ def _assert_same(a, b, mask):
     (8, 2, wl.F16, wl.F16, -1, "qwen"),
     (3, 3, wl.BF16, wl.F16, -1, "ragged"),
     (16, 2, wl.BF16, wl.BF16, -1, "ragged"),
+    (64, 2, wl.BF16, wl.BF16, -1, "ragged"),
     (4, 2, wl.F32, wl.BF16, wl.BF16, "ragged"),
 ])
 def test_bit_identical_to_two_pass(W, stage, gdt, pdt, cdt, shapes):
