@@ -53,7 +53,7 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
-    ap.add_argument("--e2e-steps", type=int, default=5,
+    ap.add_argument("--e2e-steps", type=int, default=10,
                     help="end-to-end steps through the host-buffer entry point (0: skip)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
@@ -488,6 +488,26 @@ def run_ours(args) -> dict | None:
                          "bytes_per_param": 2 * pbytes}
         del pt, views
 
+    # Gradient accumulation (the step before the reduce): every rank's
+    # micro-step gradients added into its fp32 main gradients.
+    accumulate = None
+    if not args.tensors:
+        stream = torch.cuda.current_stream().cuda_stream
+        mains = [torch.empty(z.np, dtype=torch.float32, device=device) for _ in range(w.world)]
+        mptr, gptr = [t.data_ptr() for t in mains], [g.data_ptr() for g in grads]
+        abi.zero_accumulate(z.handle, gptr, w.grad_dtype, mptr, True, stream)
+        abi.zero_accumulate(z.handle, gptr, w.grad_dtype, mptr, False, stream)
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record()
+        for _ in range(10):
+            abi.zero_accumulate(z.handle, gptr, w.grad_dtype, mptr, False, stream)
+        a1.record()
+        torch.cuda.synchronize()
+        ms = a0.elapsed_time(a1) / 10
+        per = w.world * (wl.ELEM_BYTES[w.grad_dtype] + 8)
+        accumulate = {"ms": ms, "gbs": per * info.n_real / (ms / 1e3) / 1e9, "bytes_per_param": per}
+        del mains
+
     # ZeRO-3: the per-bucket all-gather of the sharded parameters into a flat
     # working buffer (what a forward pass would prefetch bucket by bucket).
     gather = None
@@ -614,6 +634,7 @@ def run_ours(args) -> dict | None:
         "graph": graph,
         "zero3_gather": gather,
         "gather_params": gather_params,
+        "accumulate": accumulate,
         "e2e": e2e,
         # two-pass: reduce (its last block finalizes) + update; speculative:
         # single pass (finalizes) + guarded reduce + update + guarded restore
