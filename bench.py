@@ -508,6 +508,33 @@ def run_ours(args) -> dict | None:
         accumulate = {"ms": ms, "gbs": per * info.n_real / (ms / 1e3) / 1e9, "bytes_per_param": per}
         del mains
 
+    # Checkpoint in parameter-major order (independent of W, stage and bucket
+    # size): export master/m/v, then import them back (the import also
+    # recasts the parameters). Only where the three host-side-sized buffers
+    # stay small next to the workload.
+    checkpoint = None
+    if info.n_real * 12 <= 16e9:
+        stream = torch.cuda.current_stream().cuda_stream
+        pm = [torch.empty(info.n_real, dtype=torch.float32, device=device) for _ in range(3)]
+        ptrs = [t.data_ptr() for t in pm]
+        abi.zero_state_export_params(z.handle, *ptrs, stream)
+        abi.zero_state_import_params(z.handle, *ptrs, stream)
+        c0, c1, c2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+        c0.record()
+        for _ in range(5):
+            abi.zero_state_export_params(z.handle, *ptrs, stream)
+        c1.record()
+        for _ in range(5):
+            abi.zero_state_import_params(z.handle, *ptrs, stream)
+        c2.record()
+        torch.cuda.synchronize()
+        ex, im = c0.elapsed_time(c1) / 5, c1.elapsed_time(c2) / 5
+        pbytes = wl.ELEM_BYTES[w.param_dtype]
+        checkpoint = {"export_ms": ex, "export_gbs": 24 * info.n_real / (ex / 1e3) / 1e9,
+                      "import_ms": im,
+                      "import_gbs": (24 + 4 + pbytes) * info.n_real / (im / 1e3) / 1e9}
+        del pm
+
     # ZeRO-3: the per-bucket all-gather of the sharded parameters into a flat
     # working buffer (what a forward pass would prefetch bucket by bucket).
     gather = None
@@ -635,6 +662,7 @@ def run_ours(args) -> dict | None:
         "zero3_gather": gather,
         "gather_params": gather_params,
         "accumulate": accumulate,
+        "checkpoint": checkpoint,
         "e2e": e2e,
         # two-pass: reduce (its last block finalizes) + update; speculative:
         # single pass (finalizes) + guarded reduce + update + guarded restore

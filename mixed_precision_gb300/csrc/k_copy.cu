@@ -7,6 +7,54 @@
 
 namespace zg {
 
+// These copies move several independent accesses per thread before their
+// stores, so a block keeps enough bytes in flight to stream at HBM rate.
+
+// dst[i] = src[i], i < len, fp32, both 16-byte aligned: float4 vectors (four
+// in flight per thread), then the tail.
+__device__ __forceinline__ void copy_f32_aligned(float* __restrict__ dst,
+                                                 const float* __restrict__ src, int len) {
+  constexpr int U = 4;
+  const int nvec = len >> 2;
+  const float4* s4 = reinterpret_cast<const float4*>(src);
+  float4* d4 = reinterpret_cast<float4*>(dst);
+  for (int v0 = threadIdx.x; v0 < nvec; v0 += U * kThreads) {
+    float4 x[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+      if (v0 + u * kThreads < nvec) x[u] = __ldcs(s4 + v0 + u * kThreads);
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+      if (v0 + u * kThreads < nvec) __stcs(d4 + v0 + u * kThreads, x[u]);
+  }
+  for (int i = nvec * 4 + threadIdx.x; i < len; i += kThreads) dst[i] = src[i];
+}
+
+// dst[i] = RNE(src[i]), i < len, fp32 -> 2-byte type, src 16-byte and dst
+// 16-byte aligned: groups of 8 (two groups in flight per thread), then the tail.
+template <typename PT>
+__device__ __forceinline__ void cast_f32_aligned(PT* __restrict__ dst, const float* __restrict__ src,
+                                                 int len) {
+  constexpr int U = 2;
+  const int ng = len >> 3;
+  for (int g0 = threadIdx.x; g0 < ng; g0 += U * kThreads) {
+    float x[U][8];
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+      if (g0 + u * kThreads < ng) load8_f32(src + (int64_t)(g0 + u * kThreads) * 8, x[u]);
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      if (g0 + u * kThreads < ng) {
+        Pack8<PT> q;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) q.e[j] = DT<PT>::from_f32(x[u][j]);
+        store8_raw(dst + (int64_t)(g0 + u * kThreads) * 8, q);
+      }
+    }
+  }
+  for (int i = ng * 8 + threadIdx.x; i < len; i += kThreads) dst[i] = DT<PT>::from_f32(src[i]);
+}
+
 // master[shard] <- init[flat]; params_flat[flat] <- RNE(init[flat]).
 template <typename PT>
 __global__ void __launch_bounds__(kThreads)
@@ -15,11 +63,8 @@ __global__ void __launch_bounds__(kThreads)
   for (int t = blockIdx.x; t < n_tiles; t += gridDim.x) {
     const Tile tl = tiles[t];
     PT* pp = params + (params_by_shard ? tl.shard : tl.flat);
-    for (int i = threadIdx.x; i < tl.len; i += kThreads) {
-      const float x = init[tl.flat + i];
-      master[tl.shard + i] = x;
-      pp[i] = DT<PT>::from_f32(x);
-    }
+    copy_f32_aligned(master + tl.shard, init + tl.flat, tl.len);
+    cast_f32_aligned(pp, init + tl.flat, tl.len);
   }
 }
 
@@ -43,12 +88,10 @@ __global__ void __launch_bounds__(kThreads)
   float* shard_buf = st->cur ? shard1 : shard0;
   for (int t = blockIdx.x; t < n_tiles; t += gridDim.x) {
     const Tile tl = tiles[t];
-    for (int i = threadIdx.x; i < tl.len; i += kThreads) {
-      if (dir == 0)
-        flat_buf[tl.flat + i] = shard_buf[tl.shard + i];
-      else
-        shard_buf[tl.shard + i] = flat_buf[tl.flat + i];
-    }
+    if (dir == 0)
+      copy_f32_aligned(flat_buf + tl.flat, shard_buf + tl.shard, tl.len);
+    else
+      copy_f32_aligned(shard_buf + tl.shard, flat_buf + tl.flat, tl.len);
   }
 }
 
@@ -112,11 +155,19 @@ __global__ void __launch_bounds__(kThreads)
   for (int t = blockIdx.x; t < n_tiles; t += gridDim.x) {
     const Tile tl = tiles[t];
     const int64_t pm0 = pm_delta[tl.param] + tl.flat;
-    for (int i = threadIdx.x; i < tl.len; i += kThreads) {
-      if (dir == 0)
-        pm_buf[pm0 + i] = shard_buf[tl.shard + i];
-      else
-        shard_buf[tl.shard + i] = pm_buf[pm0 + i];
+    // the parameter-major side has any alignment: scalar accesses, eight in
+    // flight per thread
+    constexpr int U = 8;
+    const float* src = dir == 0 ? shard_buf + tl.shard : pm_buf + pm0;
+    float* dst = dir == 0 ? pm_buf + pm0 : shard_buf + tl.shard;
+    for (int i0 = threadIdx.x; i0 < tl.len; i0 += U * kThreads) {
+      float x[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+        if (i0 + u * kThreads < tl.len) x[u] = src[i0 + u * kThreads];
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+        if (i0 + u * kThreads < tl.len) dst[i0 + u * kThreads] = x[u];
     }
   }
 }
@@ -140,7 +191,7 @@ __global__ void __launch_bounds__(kThreads)
   for (int t = blockIdx.x; t < n_tiles; t += gridDim.x) {
     const Tile tl = tiles[t];
     PT* pp = params + (params_by_shard ? tl.shard : tl.flat);
-    for (int i = threadIdx.x; i < tl.len; i += kThreads) pp[i] = DT<PT>::from_f32(master[tl.shard + i]);
+    cast_f32_aligned(pp, master + tl.shard, tl.len);
   }
 }
 
