@@ -287,6 +287,27 @@ def test_export_import_follow_current_set():
     b.close()
 
 
+@pytest.mark.parametrize("mode", ["flat", "speculative"])
+def test_single_tile_grid(mode):
+    """One parameter of 100 elements at W=1: one tile, so the reduce (or the
+    speculative pass) runs one block, which is also the last to finish and
+    runs the finalize; through an overflow, clipping and clean steps."""
+    pr = Pair([(100,)], 1, 2, 1 << 20, wl.BF16, wl.BF16, init_scale=4.0, dynamic=True,
+              growth_interval=2, index=340, speculative=(mode == "speculative"))
+    plan = [("clean", Hparams()), ("inf", Hparams()), ("clip", Hparams(max_grad_norm=1e-6)),
+            ("clean", Hparams()), ("clean", Hparams()), ("clean", Hparams())]
+    for step, (kind, hp) in enumerate(plan):
+        g = pr.grads(step, 1e-3)
+        if kind == "inf":
+            g[0][7] = float("inf")
+        st, info, gc = pr.step(g, hp, mode=mode)
+        pr.check(st, info, gc)
+        assert st["skipped"] == (kind == "inf")
+        if kind == "clip":
+            assert st["clip_coef"] < 1.0
+    assert st["t"] == 5
+
+
 def test_needs_alternate_set_and_stage():
     shapes = [(1000,), (77,)]
     z = ZeroStep(shapes, 2, 2, 1 << 20, wl.BF16, wl.BF16)
