@@ -117,6 +117,21 @@ MUTANTS = [
      "const float base = main_grad[i];"),
     ("accumulate_subtracts", "main_grad[i] = base + load_f32(micro, i, micro_dtype);",
      "main_grad[i] = base - load_f32(micro, i, micro_dtype);"),
+    ("accumulate_writes_padding",
+     "    if (real_mask != nullptr && !real_mask[i]) continue;\n    const float base = first",
+     "    const float base = first"),
+    # more scaler and update mistakes
+    ("growth_applies_backoff", "    sc->scale = sc->scale * sc->growth_factor;",
+     "    sc->scale = sc->scale * sc->backoff_factor;"),
+    ("min_scale_comparison_flipped", "sc->scale = s < sc->min_scale ? sc->min_scale : s;",
+     "sc->scale = s > sc->min_scale ? sc->min_scale : s;"),
+    ("decay_without_lr", "    p = p * (1.0 - hp->lr * hp->weight_decay);",
+     "    p = p * (1.0 - hp->weight_decay);"),
+    ("divisor_ignored",
+     "const double divisor = hp->grad_divisor > 0.0 ? hp->grad_divisor : (double)world;",
+     "const double divisor = (double)world;"),
+    ("encode_zero_shortcut_removed", "  if (n == 0.0) return sign;\n", ""),
+    ("momentum_from_variance", "mi = b1 * mi + (1.0 - b1) * g;", "mi = b1 * vi + (1.0 - b1) * g;"),
     # composed ZeRO step
     ("norm_misses_last_rank", "    orc_overflow_sumsq(shard_grad[r].data(), comm_dtype, shard_total, "
      "shard_real.data(), &o, &s);\n    sumsq += s;",
