@@ -130,6 +130,7 @@ struct zero_layout {
 
   int grid_reduce = 0, grid_update = 0, grid_copy = 0;
   int grid_spec = 0;  // speculative single pass (set by zero_state_bind_alternate)
+  int chunk_reduce = 0;  // the pipelined reduce's elements per stage (set at bind)
   int chunk_spec = 0;  // its elements per pipeline stage
   // 1 (default): shared-memory pipelines fed by cp.async.bulk; 0: the
   // register-staged kernels, kept as the comparison baseline (environment
@@ -309,7 +310,7 @@ int launch_step(zero_layout* L, const GradSrc& src, void* const* allreduce_out,
   }
   ra.part_sumsq = L->d_part;
   ra.part_ovf = L->d_ovf;
-  ra.chunk = reduce_chunk(W, L->cfg.grad_dtype);
+  ra.chunk = L->chunk_reduce;
   ra.error = &L->d_state->error;
   ra.state = L->d_state;
   ra.guarded = guarded;
@@ -425,7 +426,7 @@ int launch_step_per_tensor(zero_layout* L, const GradSrc& src, void* const* allr
   } else {
     ra.out.base[0] = L->scratch;
   }
-  ra.chunk = reduce_chunk(W, L->cfg.grad_dtype);
+  ra.chunk = L->chunk_reduce;
   ra.error = &L->d_state->error;
   ra.state = L->d_state;
   ra.guarded = 0;
@@ -710,8 +711,19 @@ int zero_state_bind(zero_layout_t* L, void* master, void* m, void* v, void* para
     const int n_tiles = (int)L->tiles.size();
     if (const char* v = std::getenv("ZERO_REDUCE_VARIANT")) L->reduce_variant = std::atoi(v) == 0 ? 0 : 1;
     if (const char* v = std::getenv("ZERO_UPDATE_VARIANT")) L->update_variant = std::atoi(v) == 0 ? 0 : 1;
-    const int bps_r = reduce_blocks_per_sm(L->cfg.grad_dtype, L->comm_dtype, L->world(), L->cfg.stage,
-                                           L->reduce_variant);
+    // Launch-shape knobs of the pipelined reduce, read here like the variants:
+    // ZERO_REDUCE_STAGE_BYTES (bytes per stage, 3 stages) and
+    // ZERO_REDUCE_BLOCKS_PER_SM (a cap on resident blocks).
+    int red_stage_bytes = kRedStageBytes, red_bps_cap = 0;
+    if (const char* v = std::getenv("ZERO_REDUCE_STAGE_BYTES")) {
+      const int b = std::atoi(v);
+      if (b >= 4096 && b <= 73728) red_stage_bytes = b;
+    }
+    if (const char* v = std::getenv("ZERO_REDUCE_BLOCKS_PER_SM")) red_bps_cap = std::atoi(v);
+    L->chunk_reduce = reduce_chunk(L->world(), L->cfg.grad_dtype, red_stage_bytes);
+    int bps_r = reduce_blocks_per_sm(L->cfg.grad_dtype, L->comm_dtype, L->world(), L->cfg.stage,
+                                     L->reduce_variant, L->chunk_reduce);
+    if (red_bps_cap > 0 && bps_r > red_bps_cap) bps_r = red_bps_cap;
     const int bps_u = update_blocks_per_sm(L->comm_dtype, L->cfg.param_dtype, L->update_variant);
     if (bps_r <= 0 || bps_u <= 0)
       return fail(ZERO_ERR_CUDA, "kernel occupancy query failed (no sm_103a image for this GPU?)");

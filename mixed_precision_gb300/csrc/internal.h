@@ -130,9 +130,11 @@ struct UpdateArgs {
 constexpr int kRedStages = 3;
 constexpr int kRedStageBytes = 32768;
 constexpr int kRedConsumers = 8;  // consumer warps of the warp-specialised reduce
-int reduce_chunk(int world, int grad_dtype);  // elements per stage of the pipelined variant
+// elements per stage of the pipelined variant (stage_bytes: kRedStageBytes by default)
+int reduce_chunk(int world, int grad_dtype, int stage_bytes);
 cudaError_t launch_reduce(const ReduceArgs& a, int grid, int variant, cudaStream_t s);
-int reduce_blocks_per_sm(int grad_dtype, int comm_dtype, int world, int stage, int variant);
+int reduce_blocks_per_sm(int grad_dtype, int comm_dtype, int world, int stage, int variant,
+                         int chunk);
 cudaError_t launch_finalize(const double* part_sumsq, const unsigned* part_ovf, int n_part,
                             int world, const Hparams& hp, DevState* st, int guarded, cudaStream_t s);
 cudaError_t launch_update(const UpdateArgs& a, int grid, int variant, cudaStream_t s);

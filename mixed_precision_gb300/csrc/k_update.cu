@@ -21,19 +21,19 @@ static const void* reduce_kernel(int grad_dtype, int comm_dtype, int world, int 
 
 // Elements per stage of the pipelined reduce: the W ranks' slices of one chunk
 // fill about kRedStageBytes; a multiple of 128 elements, at least 128.
-int reduce_chunk(int world, int grad_dtype) {
+int reduce_chunk(int world, int grad_dtype, int stage_bytes) {
   const int g = grad_dtype == kF32 ? 4 : 2;
-  int c = kRedStageBytes / (world * g);
+  int c = stage_bytes / (world * g);
   c &= ~127;
   return c < 128 ? 128 : c;
 }
 
 static int reduce_threads(int variant) { return variant == 1 ? (kRedConsumers + 1) * 32 : kThreads; }
 
-static int reduce_smem(int world, int grad_dtype, int variant) {
+static int reduce_smem(int world, int grad_dtype, int variant, int chunk) {
   if (variant == 0) return 0;
   const int g = grad_dtype == kF32 ? 4 : 2;
-  return kRedStages * world * reduce_chunk(world, grad_dtype) * g;
+  return kRedStages * world * chunk * g;
 }
 
 cudaError_t launch_reduce(const ReduceArgs& a, int grid, int variant, cudaStream_t s) {
@@ -41,13 +41,14 @@ cudaError_t launch_reduce(const ReduceArgs& a, int grid, int variant, cudaStream
   if (f == nullptr) return cudaErrorInvalidValue;
   void* args[] = {const_cast<ReduceArgs*>(&a)};
   return cudaLaunchKernel(f, dim3(grid), dim3(reduce_threads(variant)), args,
-                          reduce_smem(a.world, a.grad_dtype, variant), s);
+                          reduce_smem(a.world, a.grad_dtype, variant, a.chunk), s);
 }
 
-int reduce_blocks_per_sm(int grad_dtype, int comm_dtype, int world, int stage, int variant) {
+int reduce_blocks_per_sm(int grad_dtype, int comm_dtype, int world, int stage, int variant,
+                         int chunk) {
   const void* f = reduce_kernel(grad_dtype, comm_dtype, world, stage, variant);
   if (f == nullptr) return 0;
-  const int smem = reduce_smem(world, grad_dtype, variant);
+  const int smem = reduce_smem(world, grad_dtype, variant, chunk);
   if (smem > 0 && cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
                       cudaSuccess)
     return 0;
