@@ -83,6 +83,9 @@ class SampledOracle:
                                     growth_interval=growth_interval)
         L = oracle.layout(numel, z.world, z.cfg.bucket_bytes, wl.ELEM_BYTES[z.grad_dtype])
         assert L.np_total == z.np
+        # the tests lay their inputs out at the library's offsets: the oracle's own
+        # layout must agree (it is also checked bit for bit on the host)
+        assert list(z.offsets) == [int(o) for o in L.param_offset]
         self.L = L
 
     def global_reduce(self, grads_gpu):

@@ -48,8 +48,12 @@ class Pair:
         self.last_mode = None
         self.L = oracle.layout(self.numel, world, bucket_bytes, wl.ELEM_BYTES[grad_dtype])
         assert self.z.np == self.L.np_total
+        # Inputs are laid out with the oracle's own offsets; the library's
+        # must be the same (they are tested bit for bit on the host as well).
+        self.offsets = [int(o) for o in self.L.param_offset]
+        assert list(self.z.offsets) == self.offsets
         self.np = self.L.np_total
-        master0 = wl.master_init(self.z.offsets, self.numel, self.np, master_sigma,
+        master0 = wl.master_init(self.offsets, self.numel, self.np, master_sigma,
                                  wl.master_seed(index))
         m0 = master0.cuda() if self.np else torch.zeros(8, device="cuda")
         self.z.init(m0, init_scale=init_scale, dynamic=dynamic,
@@ -75,7 +79,7 @@ class Pair:
         """Seeded flat gradients (CPU) for this step; inject = [(rank, flat_index, bits)]."""
         out = []
         for r in range(self.W):
-            g = wl.flat_grads(self.z.offsets, self.numel, self.np, sigma,
+            g = wl.flat_grads(self.offsets, self.numel, self.np, sigma,
                               wl.grad_seed(self.index, r, step), self.gdt,
                               zero_params=zero_params)
             out.append(g)
@@ -95,7 +99,7 @@ class Pair:
             per = []
             for r in range(self.W):
                 row = []
-                for p, (off, n) in enumerate(zip(self.z.offsets, self.numel)):
+                for p, (off, n) in enumerate(zip(self.offsets, self.numel)):
                     t = grads_cpu[r][off:off + n]
                     row.append(None if (n == 0 or not t.any()) else t.clone().cuda())
                 per.append(row)
@@ -108,7 +112,7 @@ class Pair:
             per = []
             for r in range(self.W):
                 row = []
-                for off, n in zip(self.z.offsets, self.numel):
+                for off, n in zip(self.offsets, self.numel):
                     t = grads_cpu[r][off:off + n]
                     row.append(None if (n == 0 or not t.any()) else t.clone().cuda())
                 per.append(row)
@@ -197,7 +201,7 @@ class Pair:
                           oracle.decode(p, self.pdt), bound, self.pdt == wl.BF16)
         bad = np.nonzero(~ok & self.mask_flat)[0]
         if len(bad):
-            offs = np.array(self.z.offsets)
+            offs = np.array(self.offsets)
             pid = np.searchsorted(offs, bad, side="right") - 1
             raise AssertionError(
                 f"{len(bad)} params beyond tolerance; first flat {bad[:6].tolist()} params "
