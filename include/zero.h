@@ -292,7 +292,8 @@ int zero_step_per_tensor_launch(zero_layout_t* layout, const void* const* grads,
 /* The same step in one pass over memory when it can be: the reduce, the norm
  * partials and the AdamW update with clip coefficient 1 run in one kernel,
  * which reads the current state set and writes the other one (and the
- * parameters) without knowing the global norm yet. Its finalize then
+ * parameters) without knowing the global norm yet. Its last block to finish
+ * runs the finalize, which then
  *   - commits (no overflow, clip coefficient exactly 1): the other set
  *     becomes current; results are bit-identical to zero_step;
  *   - skips (overflow, [ND] FP16 dynamic loss scaling): state unchanged, the
@@ -304,8 +305,8 @@ int zero_step_per_tensor_launch(zero_layout_t* layout, const void* const* grads,
  * and those not taken return at once, so the call never synchronises.
  * While the last finalized step clipped, the single pass is predicted to
  * fall back and returns at once: the step then costs what zero_step costs
- * plus two empty launches, and only the step on which clipping switches on
- * pays for both passes.
+ * plus two near-empty launches, and only the step on which clipping switches
+ * on pays for both passes.
  * The commit decision uses the single pass's own norm, summed in another
  * grouping than zero_step's (both within the parity tolerance of the exact
  * norm); only a norm within that rounding of the clip threshold could make
