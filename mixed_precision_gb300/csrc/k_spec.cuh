@@ -11,13 +11,14 @@
 //   - apply AdamW with clip 1 to the CURRENT state set and write the result
 //     to the OTHER set (the current one stays intact), and the cast
 //     parameters in place.
-// k_finalize_spec then commits (flips DevState::cur), skips (overflow: the
-// parameters are recast from the untouched master), or asks for the ordinary
-// two-pass step (clipping active), whose kernels run guarded on that flag.
+// The last block to finish then runs finalize_spec_state (finalize.cuh): it
+// commits (flips DevState::cur), skips (overflow: the parameters are recast
+// from the untouched master), or asks for the ordinary two-pass step
+// (clipping active), whose kernels run guarded on that flag.
 // A committed step is bit-identical to the two-pass step: same reduced
 // values, same scalars (derive_adam_scalars with clip 1), same update.
 // While the last finalized step clipped, the pass returns at once (the
-// finalize's predictor, k_update.cu) and costs one empty launch.
+// finalize's one-bit predictor) and costs one near-empty launch.
 // Bytes per element when it commits: 2W (grads) + 24 (state) + 2 (params).
 #pragma once
 
