@@ -289,7 +289,8 @@ BlockPlan plan_block(const zero_layout* L) {
   return b;
 }
 
-// The two-pass step: reduce, finalize, update. `guarded` (the speculative
+// The two-pass step: reduce (its last block runs the finalize, or the
+// finalize kernel follows), then the update. `guarded` (the speculative
 // step's fallback): each kernel runs only if the speculative finalize asked.
 int launch_step(zero_layout* L, const GradSrc& src, void* const* allreduce_out,
                 const zero_hparams* hp, cudaStream_t s, int guarded = 0) {

@@ -14,8 +14,10 @@
 // reduce-scatter output). Stage 1 writes r into all W flat outputs (the
 // all-reduce). Every thread accumulates sum(r^2) (fp32 over 8 elements, then
 // a compensated fp32 running sum, fp64 for huge groups) and an "any non-finite
-// r" flag; each block writes one fp64 partial and one flag. The grid is persistent (a multiple of the SM count) and walks the
-// tile list with a fixed stride, so the partials are deterministic.
+// r" flag; each block writes one fp64 partial and one flag. The grid is
+// persistent (a multiple of the SM count) and walks the tile list with a
+// fixed stride, so the partials are deterministic. In the pipelined kernel,
+// the last block to finish then runs the finalize (finalize.cuh).
 #pragma once
 
 #include "bulk.cuh"
@@ -184,8 +186,11 @@ __global__ void __launch_bounds__(kThreads, 4) k_reduce_norm(const __grid_consta
 // block's norm partial is assembled without a block barrier: each consumer
 // warp leaves its partial in a shared slot and the last warp to finish (a
 // shared-memory counter) adds the slots in warp order, so the result is the
-// same on every run. A warp whose bounded wait gives up records
-// kErrWaitTimeout and leaves; the block then writes no partial.
+// same on every run. With fuse_finalize, that warp then counts its block in
+// on a device counter, and the warp of the last block to do so sums all the
+// partials and runs finalize_state. A warp whose bounded wait gives up
+// records kErrWaitTimeout and leaves; the block then writes no partial (and
+// the step's finalize does not run: the error is reported instead).
 // ---------------------------------------------------------------------------
 template <typename GT, typename CT, int WT, bool STAGE1, int NC>
 __global__ void __launch_bounds__((NC + 1) * 32)

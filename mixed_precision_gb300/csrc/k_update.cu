@@ -1,5 +1,6 @@
-// K2 (finalize) and K3 (fused unscale / clip / AdamW / cast-out), plus the
-// launch dispatch of K1.
+// K2 (the one-block finalize, for the paths that do not fuse it into K1), K3
+// (fused unscale / clip / AdamW / cast-out), the launch dispatch of K1, and
+// the speculative pass's launch.
 #include "bulk.cuh"
 #include "finalize.cuh"
 #include "vec.cuh"
