@@ -57,7 +57,7 @@ __device__ inline void finalize_state(double sumsq, unsigned any, int world, con
   st->beta2_pow_of = hp.beta2;
   const AdamScalars a = derive_adam_scalars(hp, inv, c, b1t, b2t);
   st->gscale = a.gs;
-  st->decay = a.decay;
+  st->lr_wd = a.lr_wd;
   st->step_size = a.step;
   st->inv_sqrt_bc2 = a.isb2;
   st->beta1 = a.b1;
@@ -125,7 +125,7 @@ __device__ inline void finalize_spec_state(double sumsq, unsigned any, int world
   st->fast_path = 1;
   const AdamScalars a = derive_adam_scalars(hp, inv, 1.0, b1t, b2t);
   st->gscale = a.gs;
-  st->decay = a.decay;
+  st->lr_wd = a.lr_wd;
   st->step_size = a.step;
   st->inv_sqrt_bc2 = a.isb2;
   st->beta1 = a.b1;

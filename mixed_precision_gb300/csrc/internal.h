@@ -48,7 +48,7 @@ struct DevState {
   double grad_norm, clip_coef, norm_sq_raw;
   // per-step values for the update kernel (fp32, derived in fp64)
   float gscale;        // clip / (S * D)
-  float decay;         // 1 - lr * wd
+  float lr_wd;         // lr * wd (decoupled decay: p <- p - lr_wd * p)
   float step_size;     // lr / (1 - beta1^t)
   float inv_sqrt_bc2;  // 1 / sqrt(1 - beta2^t)
   float beta1, one_minus_beta1, beta2, one_minus_beta2, eps;

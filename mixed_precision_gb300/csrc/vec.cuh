@@ -161,13 +161,13 @@ __device__ __forceinline__ void store4_raw(T* p, const T (&e)[4]) {
 // One fixed sequence of correctly rounded fp32 operations (explicit
 // intrinsics, so no kernel's compiler contracts it differently): every
 // update kernel produces the same bits for the same inputs and scalars.
-//   g = r * gscale;  p *= decay;  m = b1 m + (1-b1) g;  v = b2 v + (1-b2) g^2;
+//   g = r * gscale;  p -= lr_wd * p;  m = b1 m + (1-b1) g;  v = b2 v + (1-b2) g^2;
 //   p -= step * m / (sqrt(v) * inv_sqrt_bc2 + eps)
 struct AdamScalars {
-  float gs, decay, step, isb2, eps, b1, omb1, b2, omb2;
+  float gs, lr_wd, step, isb2, eps, b1, omb1, b2, omb2;
 
   __device__ static AdamScalars from(const DevState* st) {
-    return AdamScalars{st->gscale, st->decay, st->step_size, st->inv_sqrt_bc2, st->eps,
+    return AdamScalars{st->gscale, st->lr_wd, st->step_size, st->inv_sqrt_bc2, st->eps,
                        st->beta1, st->one_minus_beta1, st->beta2, st->one_minus_beta2};
   }
 
@@ -178,7 +178,10 @@ struct AdamScalars {
   // are much slower on such operands than on ordinary ones.
   __device__ __forceinline__ void apply(float r, float& p, float& m, float& v) const {
     const float g = __fmul_rn(r, gs);
-    p = __fmul_rn(p, decay);
+    // decoupled decay as p - (lr*wd)*p in one rounding: 1 - lr*wd rounded to
+    // fp32 keeps only a few digits of lr*wd (fp32 resolves 1.2e-7 near 1), a
+    // bias that would repeat every step
+    p = __fmaf_rn(-lr_wd, p, p);
     m = __fmaf_rn(b1, m, __fmul_rn(omb1, g));
     v = __fmaf_rn(b2, v, __fmul_rn(omb2, __fmul_rn(g, g)));
     const bool vz = v == 0.0f, mz = m == 0.0f;  // v >= +0 always
@@ -217,7 +220,7 @@ __device__ __forceinline__ AdamScalars derive_adam_scalars(const Hparams& hp, do
   const double bc2 = 1.0 - b2t;
   AdamScalars s;
   s.gs = (float)(inv * c);
-  s.decay = (float)(1.0 - hp.lr * hp.weight_decay);
+  s.lr_wd = (float)(hp.lr * hp.weight_decay);
   s.step = (float)(hp.lr / bc1);
   s.isb2 = (float)(1.0 / sqrt(bc2));
   s.eps = (float)hp.eps;

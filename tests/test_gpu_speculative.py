@@ -375,3 +375,42 @@ def test_no_write_outside_buffers(stage):
     bad = [i for i, g in enumerate(bufs) if not g.intact()]
     assert not bad, bad
     z.close()
+
+
+def test_long_run_mixed_entry_points():
+    """300 steps against the oracle, rotating through every step entry point
+    (flat, per-tensor, speculative flat and per-tensor, host copies), with
+    seeded overflows and clipping switching on and off: the scaler stays
+    exact and the state within the parity bar widened by the fp32 constants'
+    bias (about 5e-8 per step measured, 1.2e-7 allowed), all the way (the
+    running beta powers, the state-set flips and the predictor included)."""
+    import numpy as np
+    shapes = small_qwen_shapes()
+    W = 3
+    pr = Pair(shapes, W, 2, 60_000, wl.F16, wl.F16, init_scale=2.0 ** 12, dynamic=True,
+              growth_interval=7, index=360, speculative=True)
+    rng = np.random.default_rng(360)
+    modes = ["flat", "speculative", "tensors", "speculative_tensors", "host"]
+    rank, idx = wl.inject_position(pr.numel, pr.z.offsets, W, seed=361)
+    fast = 0
+    for step in range(300):
+        mode = modes[step % len(modes)]
+        clip = bool(rng.random() < 0.25)
+        inf = bool(rng.random() < 0.05)
+        # the scale grows over the run and shrinks the unscaled norm: 1e-9
+        # clips at any scale reached here, 1.0 never does
+        hp = Hparams(lr=1e-3, weight_decay=0.01, max_grad_norm=1e-9 if clip else 1.0)
+        g = pr.grads(step, 1e-3, inject=[(rank, idx, INF_BITS[wl.F16])] if inf else None)
+        st, info, gc = pr.step(g, hp, mode=mode)
+        if step % 10 == 0 or inf or step == 299:
+            # The per-step bar (1e-5) plus a bias that grows with t: the fp32
+            # path rounds each hyper-parameter constant of the update (beta1,
+            # beta2, 1-beta, bias corrections, lr*wd) once, and applies the same
+            # rounded value every step, while the oracle works in fp64. Allow
+            # two fp32 roundings' worth (2^-23) per applied step.
+            pr.check(st, info, gc, rtol=1e-5 + st["t"] * 2.0 ** -23)
+        assert st["overflow"] == info.overflow
+        assert (st["scale"], st["counter"], st["t"]) == (pr.o_scaler.scale, pr.o_scaler.counter,
+                                                         pr.o_scaler.t)
+        fast += st["fast_path"]
+    assert 20 < fast < 120  # commits happened, and not on every speculative step
