@@ -120,8 +120,8 @@ cudaError_t launch_state_init(const ScalerCfg& cfg, DevState* st, cudaStream_t s
 // "Distributed optimizer": each rank updates its FP32 master slice and
 // moments, then the all-gather rebuilds the BF16 parameter buffer -- here the
 // cast result is written straight into the flat parameter buffer.
-//   g = r * gscale;  p -= lr_wd * p;  m = b1 m + (1-b1) g;  v = b2 v + (1-b2) g^2;
-//   p -= step_size * m / (sqrt(v) * inv_sqrt_bc2 + eps);  param = RNE(p).
+//   g = r * gscale;  m = b1 m + (1-b1) g;  v = b2 v + (1-b2) g^2;
+//   p -= lr_wd * p + step_size * m / (sqrt(v) * inv_sqrt_bc2 + eps);  param = RNE(p).
 // Element math in fp32. A skipped step returns before touching memory.
 // ---------------------------------------------------------------------------
 template <typename CT, typename PT>

@@ -161,8 +161,8 @@ __device__ __forceinline__ void store4_raw(T* p, const T (&e)[4]) {
 // One fixed sequence of correctly rounded fp32 operations (explicit
 // intrinsics, so no kernel's compiler contracts it differently): every
 // update kernel produces the same bits for the same inputs and scalars.
-//   g = r * gscale;  p -= lr_wd * p;  m = b1 m + (1-b1) g;  v = b2 v + (1-b2) g^2;
-//   p -= step * m / (sqrt(v) * inv_sqrt_bc2 + eps)
+//   g = r * gscale;  m = b1 m + (1-b1) g;  v = b2 v + (1-b2) g^2;
+//   p -= lr_wd * p + step * m / (sqrt(v) * inv_sqrt_bc2 + eps)
 struct AdamScalars {
   float gs, lr_wd, step, isb2, eps, b1, omb1, b2, omb2;
 
@@ -178,17 +178,21 @@ struct AdamScalars {
   // are much slower on such operands than on ordinary ones.
   __device__ __forceinline__ void apply(float r, float& p, float& m, float& v) const {
     const float g = __fmul_rn(r, gs);
-    // decoupled decay as p - (lr*wd)*p in one rounding: 1 - lr*wd rounded to
-    // fp32 keeps only a few digits of lr*wd (fp32 resolves 1.2e-7 near 1), a
-    // bias that would repeat every step
-    p = __fmaf_rn(-lr_wd, p, p);
-    m = __fmaf_rn(b1, m, __fmul_rn(omb1, g));
-    v = __fmaf_rn(b2, v, __fmul_rn(omb2, __fmul_rn(g, g)));
+    // moments as interpolations m + (1-b1)(g - m) and v + (1-b2)(g^2 - v):
+    // the implied beta is exactly 1 - (1-beta) in fp32, where b*x + (1-b)*y
+    // with b and 1-b rounded separately would not sum to one (0.999f +
+    // 0.001f exceeds 1 by 1.3e-8, a bias v's long memory accumulates)
+    m = __fmaf_rn(omb1, __fsub_rn(g, m), m);
+    v = __fmaf_rn(omb2, __fsub_rn(__fmul_rn(g, g), v), v);
     const bool vz = v == 0.0f, mz = m == 0.0f;  // v >= +0 always
     const float sv = __fsqrt_rn(vz ? 1.0f : v);
     const float denom = __fmaf_rn(vz ? 0.0f : sv, isb2, eps);
-    const float q = __fdiv_rn(mz ? 1.0f : m, denom);
-    p = __fmaf_rn(-step, mz ? m : q, p);
+    const float q = mz ? m : __fdiv_rn(mz ? 1.0f : m, denom);
+    // The step's whole change to p, decoupled decay included, formed at its
+    // own scale (far below p's) and subtracted with one rounding: rounding p
+    // twice per step (after the decay, then after the update) makes the fp32
+    // state walk away from an exact update by up to half an ulp a step.
+    p = __fsub_rn(p, __fmaf_rn(lr_wd, p, __fmul_rn(step, q)));
   }
 };
 

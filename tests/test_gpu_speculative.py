@@ -381,9 +381,11 @@ def test_long_run_mixed_entry_points():
     """300 steps against the oracle, rotating through every step entry point
     (flat, per-tensor, speculative flat and per-tensor, host copies), with
     seeded overflows and clipping switching on and off: the scaler stays
-    exact and the state within the parity bar widened by the fp32 constants'
-    bias (about 5e-8 per step measured, 1.2e-7 allowed), all the way (the
-    running beta powers, the state-set flips and the predictor included)."""
+    exact and the state within the per-step parity bar all the way (the
+    running beta powers, the state-set flips and the predictor included).
+    The update rounds each stored value once a step, as the oracle's fp32
+    state is rounded once a step from fp64, so the error does not grow with
+    t (about 1.3e-6 on the master weights and 4.8e-7 on v, flat, measured)."""
     import numpy as np
     shapes = small_qwen_shapes()
     W = 3
@@ -403,12 +405,7 @@ def test_long_run_mixed_entry_points():
         g = pr.grads(step, 1e-3, inject=[(rank, idx, INF_BITS[wl.F16])] if inf else None)
         st, info, gc = pr.step(g, hp, mode=mode)
         if step % 10 == 0 or inf or step == 299:
-            # The per-step bar (1e-5) plus a bias that grows with t: the fp32
-            # path rounds each hyper-parameter constant of the update (beta1,
-            # beta2, 1-beta, bias corrections, lr*wd) once, and applies the same
-            # rounded value every step, while the oracle works in fp64. Allow
-            # two fp32 roundings' worth (2^-23) per applied step.
-            pr.check(st, info, gc, rtol=1e-5 + st["t"] * 2.0 ** -23)
+            pr.check(st, info, gc, rtol=1e-5)
         assert st["overflow"] == info.overflow
         assert (st["scale"], st["counter"], st["t"]) == (pr.o_scaler.scale, pr.o_scaler.counter,
                                                          pr.o_scaler.t)
