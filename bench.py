@@ -37,12 +37,12 @@ L2_BYTES = 129 * 1000 * 1000
 # (dram__bytes_read.sum + dram__bytes_write.sum / elements), with the capture
 # it comes from; None until a capture of the current kernel exists.
 NCU_TRAFFIC_PER_ELEM = {
-    # profiles/k_adamw_cast_ws_qwen3_layers8.md: (1.7628 + 1.7003) GB / 125,847,552 elements
+    # profiles/k_adamw_cast_ws_qwen3_layers8.md: (1.7628 + 1.7005) GB / 125,847,552 elements
     "k_adamw_cast": 27.52,
     # profiles/k_reduce_norm_ws_qwen3_layers8.md: (504.1 + 204.9) MB / 125,847,552 elements
     "k_reduce_norm": 5.634,
-    # profiles/k_spec_step_qwen3_layers8.md: (2.0147 + 1.7143) GB / 125,847,552 elements
-    "k_spec_step": 29.63,
+    # profiles/k_spec_step_qwen3_layers8.md: (2.0232 + 1.7131) GB / 125,847,552 elements
+    "k_spec_step": 29.69,
 }
 
 
