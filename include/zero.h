@@ -258,8 +258,11 @@ int zero_state_init(zero_layout_t* layout, const float* master_init_flat,
  * Enqueues two kernels on `stream` (three with the register-staged reduce):
  *   reduce + overflow/norm partials, whose last block to finish runs the
  *   finalize (norm, clip, scaler, t); then the fused unscale/clip/AdamW/
- *   cast-out (returns at once on a skipped step). After ZERO_ERR_TIMEOUT the
- *   state must be initialised again (zero_state_init).
+ *   cast-out (returns at once on a skipped step). After a kernel's bounded
+ *   wait gives up (reported as ZERO_ERR_TIMEOUT by the next state read),
+ *   every kernel of every step entry point returns at once: master, m, v,
+ *   the parameters and the scaler stay as they were until zero_state_init
+ *   initialises the state again.
  * Reduced value r = RNE_comm(g_0 + ... + g_{W-1}) (fp32 adds in rank order);
  * overflow = any non-finite r over real elements; on overflow the update is
  * skipped, S is multiplied by backoff (dynamic mode, floored at min_scale)
@@ -429,6 +432,14 @@ int zero_reduce_norm_noalloc(const void* const* grads, int world, int64_t n, int
  * CUDA failure. Synchronises `stream`; the context stays usable. No
  * counterpart on the pages: it tests failure detection without a GPU fault. */
 int zero_selftest_wait_timeout(uint32_t spin_limit, void* stream);
+
+/* The same self-test bound to a layout: the wait's timeout is OR-ed into the
+ * layout's device error word, exactly as a step kernel records one. Requires
+ * zero_state_init. Synchronises `stream` and returns what the next state
+ * read reports: ZERO_ERR_TIMEOUT when the wait gave up (the expected
+ * outcome). From then on the layout's step kernels return at once, until
+ * zero_state_init. */
+int zero_selftest_layout_timeout(zero_layout_t* layout, uint32_t spin_limit, void* stream);
 
 /* ------------------------------------------------------------------------ */
 /* Gradient accumulation into fp32 main-gradient buffers ([DO] "BF16 model   */

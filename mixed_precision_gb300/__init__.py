@@ -7,6 +7,7 @@ exists: without the built library every call raises.
 """
 from ._abi import (ZERO_BF16, ZERO_STATE_BLOB_BYTES, zero_accumulate, zero_gather_bucket,
                    zero_loss_scale_state_async, zero_state_blob_decode, zero_scaler_restore, zero_selftest_wait_timeout,
+                   zero_selftest_layout_timeout,
                    zero_state_export_params, zero_state_import_params, ZERO_F16, ZERO_F32, ZeroError, zero_bucket_range, zero_config,
                    zero_gather_params, zero_hparams, zero_last_error, zero_layout_create,
                    zero_layout_destroy, zero_layout_info, zero_layout_query,

@@ -107,6 +107,7 @@ def lib() -> ctypes.CDLL:
             "zero_set_step_events": [P, PP],
             "zero_reduce_norm_noalloc": [PP, I, I64, I, I, P, P, P, P],
             "zero_selftest_wait_timeout": [ctypes.c_uint32, P],
+            "zero_selftest_layout_timeout": [P, ctypes.c_uint32, P],
             "zero_accumulate": [P, PP, I, PP, I, P],
             "zero_state_export_params": [P, P, P, P, P],
             "zero_state_import_params": [P, P, P, P, P],
@@ -264,6 +265,10 @@ def zero_reduce_norm_noalloc(grads, n: int, grad_dtype: int, comm_dtype: int, re
 
 def zero_selftest_wait_timeout(spin_limit: int, stream: int) -> None:
     _check(lib().zero_selftest_wait_timeout(spin_limit, stream or None))
+
+
+def zero_selftest_layout_timeout(layout: int, spin_limit: int, stream: int) -> None:
+    _check(lib().zero_selftest_layout_timeout(layout, spin_limit, stream or None))
 
 
 def zero_accumulate(layout: int, micro, micro_dtype: int, main, first: bool, stream: int) -> None:

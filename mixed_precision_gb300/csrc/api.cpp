@@ -1157,6 +1157,19 @@ int zero_scaler_restore(zero_layout_t* L, const zero_scaler_state* st, void* str
   return ZERO_OK;
 }
 
+int zero_selftest_layout_timeout(zero_layout_t* L, uint32_t spin_limit, void* stream) {
+  if (int rc = check_ready(L, true)) return rc;
+  if (spin_limit < 1 || spin_limit > kSpinLimit)
+    return fail(ZERO_ERR_INVALID, "spin_limit outside 1..2^22");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_selftest_wait(spin_limit, &L->d_state->error, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "self-test");
+  // the layout's own error word decides, as for any step
+  zero_scaler_state out;
+  return zero_loss_scale_state(L, stream, &out);
+}
+
 int zero_state_export(zero_layout_t* L, float* master_flat, float* m_flat, float* v_flat,
                       void* stream) {
   if (int rc = check_ready(L, true)) return rc;

@@ -7,10 +7,9 @@
 
 #include <cstdint>
 
-namespace zg {
+#include "internal.h"  // kSpinLimit, kErrWaitTimeout
 
-constexpr uint32_t kSpinLimit = 1u << 22;  // try_wait retries before giving up
-constexpr unsigned kErrWaitTimeout = 1u;  // DevState::error bit: a bounded wait gave up
+namespace zg {
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));

@@ -15,6 +15,8 @@ constexpr int kTileElems = 8192;      // longest work unit (multiple of kParamAl
 constexpr int kThreads = 256;         // threads per block of the streaming kernels
 constexpr int kMaxBlocksPerSm = 8;    // 2048 threads / kThreads
 constexpr int kFinalizeThreads = 256;
+constexpr uint32_t kSpinLimit = 1u << 22;  // mbarrier try_wait retries before giving up
+constexpr unsigned kErrWaitTimeout = 1u;  // DevState::error bit: a bounded wait gave up
 
 enum Dtype : int { kF32 = 0, kF16 = 1, kBF16 = 2 };
 
@@ -52,7 +54,8 @@ struct DevState {
   float step_size;     // lr / (1 - beta1^t)
   float inv_sqrt_bc2;  // 1 / sqrt(1 - beta2^t)
   float beta1, one_minus_beta1, beta2, one_minus_beta2, eps;
-  unsigned error;  // bit 0: a kernel's bounded wait gave up (reported as ZERO_ERR_TIMEOUT)
+  unsigned error;  // bit 0: a kernel's bounded wait gave up (reported as ZERO_ERR_TIMEOUT);
+                   // while set, every kernel of the step returns at once
   int cur;             // which bound state set holds the current master/m/v (0 or 1)
   int need_fallback;   // speculative step: the two-pass step must run
   int restore_params;  // speculative step overflowed: recast params from the master
@@ -157,6 +160,9 @@ struct AccArgs {
   int n_tiles;
 };
 cudaError_t launch_accumulate(const AccArgs& a, int grid, cudaStream_t s);
+// The bounded-wait self-test; err (optional): a device error word to OR the
+// timeout into.
+cudaError_t launch_selftest_wait(uint32_t limit, unsigned* err, cudaStream_t s);
 
 // The speculative single-pass step (k_spec.cuh).
 struct SpecArgs {  // arguments of k_spec_step

@@ -186,7 +186,7 @@ __global__ void __launch_bounds__(kThreads)
     k_recast(const Tile* __restrict__ tiles, int n_tiles, const float* master0,
              const float* master1, PT* __restrict__ params, int params_by_shard,
              const DevState* __restrict__ st, int guarded) {
-  if (guarded && !st->restore_params) return;
+  if (guarded && (!st->restore_params || st->error)) return;
   const float* master = st->cur ? master1 : master0;
   for (int t = blockIdx.x; t < n_tiles; t += gridDim.x) {
     const Tile tl = tiles[t];

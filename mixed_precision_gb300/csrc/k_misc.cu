@@ -55,18 +55,26 @@ cudaError_t launch_accumulate(const AccArgs& a, int grid, cudaStream_t s) {
 }
 
 // Self-test: an mbarrier armed for 16 bytes that never arrive; the bounded
-// wait must give up and record the timeout. Nothing is copied, so nothing is
-// in flight when the block exits.
+// wait must give up and record the timeout, in the module's own word or (err
+// not NULL) OR-ed into a layout's device error word as the step kernels do.
+// Nothing is copied, so nothing is in flight when the block exits.
 static __device__ unsigned g_selftest_error;
 
-__global__ void k_selftest_wait(uint32_t limit) {
+__global__ void k_selftest_wait(uint32_t limit, unsigned* err) {
   __shared__ __align__(8) uint64_t bar;
   if (threadIdx.x == 0) {
     mbar_init(&bar, 1);
     mbar_init_fence();
     mbar_arrive_expect_tx(&bar, 16);
-    g_selftest_error = mbar_wait(&bar, 0, limit) ? 0u : kErrWaitTimeout;
+    const unsigned code = mbar_wait(&bar, 0, limit) ? 0u : kErrWaitTimeout;
+    g_selftest_error = code;
+    if (err != nullptr && code != 0u) atomicOr(err, code);
   }
+}
+
+cudaError_t launch_selftest_wait(uint32_t limit, unsigned* err, cudaStream_t s) {
+  k_selftest_wait<<<1, 32, 0, s>>>(limit, err);
+  return cudaGetLastError();
 }
 
 }  // namespace zg
@@ -78,8 +86,7 @@ extern "C" int zero_selftest_wait_timeout(uint32_t spin_limit, void* stream) {
     return zero_internal_fail(ZERO_ERR_INVALID, "spin_limit outside 1..2^22");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   unsigned err = 0;
-  k_selftest_wait<<<1, 32, 0, s>>>(spin_limit);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_selftest_wait(spin_limit, nullptr, s);
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);
   if (e == cudaSuccess) e = cudaMemcpyFromSymbol(&err, g_selftest_error, sizeof(err));
   if (e != cudaSuccess) return zero_internal_fail(ZERO_ERR_CUDA, cudaGetErrorString(e));

@@ -87,7 +87,7 @@ __device__ __forceinline__ void add_group(float ss, float& hi, float& lo, double
 
 template <typename GT, typename CT, int WT, bool STAGE1>
 __global__ void __launch_bounds__(kThreads, 4) k_reduce_norm(const __grid_constant__ ReduceArgs a) {
-  if (a.guarded && !a.state->need_fallback) return;
+  if (a.state->error || (a.guarded && !a.state->need_fallback)) return;
   // Vectors in flight per thread: keep up to eight 16-byte gradient loads
   // outstanding (at most four vectors, to stay within 64 registers).
   constexpr int U = (WT == 0 || WT >= 8) ? 1 : (8 / WT > 4 ? 4 : 8 / WT);
@@ -195,7 +195,7 @@ __global__ void __launch_bounds__(kThreads, 4) k_reduce_norm(const __grid_consta
 template <typename GT, typename CT, int WT, bool STAGE1, int NC>
 __global__ void __launch_bounds__((NC + 1) * 32)
     k_reduce_norm_ws(const __grid_constant__ ReduceArgs a) {
-  if (a.guarded && !a.state->need_fallback) return;
+  if (a.state->error || (a.guarded && !a.state->need_fallback)) return;
   constexpr int S = kRedStages;
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ __align__(8) uint64_t full[S];

@@ -56,6 +56,7 @@ __global__ void __launch_bounds__((NC + 1) * 32) k_spec_step(const __grid_consta
   const int kStage = kGrad + 12 * C;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const DevState* st = a.state;
+  if (st->error) return;
   if (st->predict_fallback) {  // predicted to clip: the two-pass kernels run instead
     if (a.fuse_finalize && blockIdx.x == 0 && threadIdx.x == 0) spec_predicted_state(a.state_rw);
     return;

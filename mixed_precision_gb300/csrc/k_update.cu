@@ -71,7 +71,7 @@ int reduce_blocks_per_sm(int grad_dtype, int comm_dtype, int world, int stage, i
 __global__ void __launch_bounds__(kFinalizeThreads)
     k_finalize(const double* __restrict__ part_sumsq, const unsigned* __restrict__ part_ovf,
                int n_part, int world, const Hparams hp, DevState* __restrict__ st, int guarded) {
-  if (guarded && !st->need_fallback) return;
+  if (st->error || (guarded && !st->need_fallback)) return;
   __shared__ double s_red[kFinalizeThreads / 32];
   __shared__ unsigned s_or[kFinalizeThreads / 32];
   double acc = 0.0;
@@ -127,7 +127,7 @@ cudaError_t launch_state_init(const ScalerCfg& cfg, DevState* st, cudaStream_t s
 template <typename CT, typename PT>
 __global__ void __launch_bounds__(kThreads) k_adamw_cast(const __grid_constant__ UpdateArgs a) {
   const DevState* st = a.state;
-  if (st->skip) return;
+  if (st->skip || st->error) return;
   const AdamScalars sc = AdamScalars::from(st);
   auto adam = [&](float r, float& p, float& m, float& v) { sc.apply(r, p, m, v); };
   const int cs = st->cur;
@@ -209,7 +209,7 @@ __global__ void __launch_bounds__((NC + 1) * 32)
   constexpr int kStage = UpdStage<CT>::bytes(C);
 
   const DevState* st = a.state;
-  if (st->skip) return;
+  if (st->skip || st->error) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int cs = st->cur;
   float* const s_master = a.master[cs];

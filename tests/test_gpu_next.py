@@ -26,6 +26,81 @@ def test_bounded_wait_times_out_and_context_survives():
     pr.check(st, info, gc)
 
 
+def test_layout_timeout_freezes_every_step_until_init():
+    """A bounded wait that gives up inside a layout (the self-test records it
+    in the layout's device error word, as a step kernel does) is reported as
+    ZERO_ERR_TIMEOUT by the next state read. Every step entry point then
+    leaves master, m, v, the parameters and the scaler as they were, and
+    zero_state_init makes the layout usable again: its next step matches a
+    fresh layout's bit for bit."""
+    from mixed_precision_gb300.engine import ZeroStep
+    shapes = [(3000,), (129,), (40000,), (1,)]
+    W = 2
+    hp = Hparams()
+    stream = torch.cuda.current_stream().cuda_stream
+
+    def fresh():
+        z = ZeroStep(shapes, W, 2, 100_000, wl.BF16, wl.BF16)
+        z.allocate(speculative=True)
+        z.init(wl.master_init(z.offsets, z.numels, z.np, 0.02, wl.master_seed(140), device="cuda"))
+        return z
+
+    def grads(z, step):
+        return [wl.flat_grads(z.offsets, z.numels, z.np, 1e-3, wl.grad_seed(140, r, step), wl.BF16,
+                              device="cuda") for r in range(W)]
+
+    def snapshot(z):  # both state sets (no state read: it would report the error)
+        return [t.clone() for t in (z.master, z.m, z.v, z.master2, z.m2, z.v2, z.params_flat)]
+
+    z = fresh()
+    z.step(grads(z, 0), hp)
+    st0 = z.scaler_state()
+    assert st0["t"] == 1
+    before = snapshot(z)
+    with pytest.raises(ZeroError) as e:
+        abi.zero_selftest_layout_timeout(z.handle, 2000, stream)
+    assert e.value.code == abi.ZERO_ERR_TIMEOUT
+    g = grads(z, 1)
+    per_tensor = [[z.param_view(g[w], p) for p in range(len(shapes))] for w in range(W)]
+    host = [t.cpu().pin_memory() for t in g]
+    dev = z.new_grad_buffers()
+    z.step(g, hp)
+    z.step_speculative(g, hp)
+    z.step_tensors(per_tensor, hp)
+    z.step_speculative_tensors(per_tensor, hp)
+    z.step_per_tensor_launch(g, hp)
+    z.step_host(host, dev, hp)
+    torch.cuda.synchronize()
+    with pytest.raises(ZeroError) as e:
+        z.scaler_state()
+    assert e.value.code == abi.ZERO_ERR_TIMEOUT
+    for a, b in zip(before, snapshot(z)):
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    # initialised again: the error is gone and the layout steps like a new one
+    z.init(wl.master_init(z.offsets, z.numels, z.np, 0.02, wl.master_seed(140), device="cuda"))
+    ref = fresh()
+    for k in range(2):
+        gk = grads(z, k)
+        z.step(gk, hp)
+        ref.step(gk, hp)
+    torch.cuda.synchronize()
+    sa, sb = z.scaler_state(), ref.scaler_state()
+    assert sa["t"] == sb["t"] == 2 and sa["scale"] == sb["scale"]
+    mask = torch.zeros(z.np, dtype=torch.bool, device="cuda")
+    for b in range(z.info.n_buckets):
+        for r in range(W):
+            f0, s0, ln = abi.zero_shard_range(z.handle, b, r)
+            for off, n in zip(z.offsets, z.numels):
+                lo, hi = max(off, f0), min(off + n, f0 + ln)
+                if lo < hi:
+                    mask[s0 + lo - f0:s0 + hi - f0] = True
+    for a, b in zip(z.current_state(), ref.current_state()):
+        assert torch.equal(a[:z.np][mask].view(torch.int32), b[:z.np][mask].view(torch.int32))
+    assert torch.equal(z.params_flat.view(torch.int16), ref.params_flat.view(torch.int16))
+    z.close()
+    ref.close()
+
+
 @pytest.mark.parametrize("micro_dtype,comm", [(wl.BF16, wl.BF16), (wl.F16, wl.F32)])
 def test_accumulate_then_boundary_step(micro_dtype, comm):
     """Three bf16/fp16 micro-steps accumulated into fp32 main gradients (bit
