@@ -125,6 +125,18 @@ class SampledOracle:
 
     def step(self, grads_gpu, hp):
         ovf, sumsq, red_at = self.global_reduce(grads_gpu)
+        self.last_reduce = (ovf, sumsq, red_at)
+        return self._apply(ovf, sumsq, red_at, hp)
+
+    def step_repeat(self, hp, ovf=None, sumsq=None):
+        """A step on the same gradients as the last `step` (its global reduce
+        reused), optionally with another overflow flag and sum of squares: an
+        injected non-finite value changes those and, on a skipped step,
+        nothing else."""
+        o, sq, red_at = self.last_reduce
+        return self._apply(o if ovf is None else ovf, sq if sumsq is None else sumsq, red_at, hp)
+
+    def _apply(self, ovf, sumsq, red_at, hp):
         o_hp = oracle.Hparams(hp.lr, hp.beta1, hp.beta2, hp.eps, hp.weight_decay, hp.max_grad_norm,
                               hp.grad_divisor)
         info = oracle.finalize(sumsq, ovf, self.z.world, o_hp, self.scaler)

@@ -88,11 +88,11 @@ def test_fullsize_qwen3_fp16_w8_stages_and_trajectory():
     z1.close()
     # 199 more steps on the same gradients, +inf at 1-indexed steps 50/100/150/200
     rank, idx = wl.inject_position(numel, z2.offsets, w.world, seed=3)
-    clean_ovf = info.overflow
     bits = INF_BITS[wl.F16]
     vals = [to_np(g[r][idx:idx + 1]) for r in range(w.world)]
     vals[rank] = np.array([bits], np.uint16)
-    inj_ovf, _ = oracle.overflow_sumsq(oracle.reduce(vals, wl.F16, wl.F16), wl.F16)
+    # the injected element's reduced value is +inf, so is the step's sum of squares
+    inj_ovf, inj_sq = oracle.overflow_sumsq(oracle.reduce(vals, wl.F16, wl.F16), wl.F16)
     saved = g[rank][idx].clone()
     for step in range(2, 201):
         inject = step % 50 == 0
@@ -102,13 +102,17 @@ def test_fullsize_qwen3_fp16_w8_stages_and_trajectory():
         st = z2.scaler_state()
         if inject:
             g[rank][idx] = saved
-        # the oracle's scaler on the oracle's flags (norm irrelevant to the trajectory)
-        o_info = oracle.finalize(1.0, inj_ovf if inject else clean_ovf, w.world,
-                                 oracle.Hparams(), so.scaler)
+        # the sampled oracle steps on the same gradients: the first step's
+        # global reduce, with the injected step's overflow flag
+        o_info, red_at = so.step_repeat(hp, *((inj_ovf, inj_sq) if inject else ()))
         assert (st["overflow"], st["skipped"]) == (o_info.overflow, o_info.skipped)
         assert (st["scale"], st["counter"], st["t"]) == (so.scaler.scale, so.scaler.counter,
                                                          so.scaler.t)
+        if step == 199:  # the last clean step: the sampled state after 196 updates
+            so.check(st, o_info, red_at)
     assert so.scaler.scale == 2.0 ** 12 and so.scaler.t == 196
+    # the skipped step 200 left the state as step 199 did
+    so.check(st, o_info, red_at, reduced=False)
     z2.close()
 
 
