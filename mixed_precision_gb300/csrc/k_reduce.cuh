@@ -340,36 +340,13 @@ __global__ void __launch_bounds__((NC + 1) * 32)
       ct += gridDim.x;
     }
   }
-  // warp partial (fixed shuffle tree), then the last warp adds the slots in order
-  double x = (double)hi + (double)lo + big;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) x += __shfl_down_sync(0xffffffffu, x, o);
-  const unsigned any = __any_sync(0xffffffffu, bad != 0u) ? 1u : 0u;
-  unsigned last = 0u;
-  if (lane == 0) {
-    s_part[warp] = x;
-    s_flag[warp] = any;
-    __threadfence_block();
-    if (atomicAdd(&s_done, 1u) == NC - 1) {
-      __threadfence_block();
-      double total = 0.0;
-      unsigned f = 0u;
-      for (int w = 0; w < NC; ++w) {
-        total += *reinterpret_cast<volatile double*>(&s_part[w]);
-        f |= *reinterpret_cast<volatile unsigned*>(&s_flag[w]);
-      }
-      a.part_sumsq[blockIdx.x] = total;
-      a.part_ovf[blockIdx.x] = f;
-      if (a.fuse_finalize) {  // publish the partial, then count this block in
-        __threadfence();
-        last = atomicInc(&a.state_rw->blocks_done, gridDim.x - 1) == gridDim.x - 1 ? 1u : 0u;
-      }
-    }
-  }
+  const bool last = publish_block_partial<NC>((double)hi + (double)lo + big, bad, s_part, s_flag,
+                                              &s_done, a.part_sumsq, a.part_ovf,
+                                              a.fuse_finalize ? &a.state_rw->blocks_done : nullptr);
   // The last block to finish (every other block has written its partial and
   // is past its reads of the state) finishes the step: the global sums and
   // finalize_state, by the warp that counted it in.
-  if (a.fuse_finalize && __shfl_sync(0xffffffffu, last, 0)) {
+  if (last) {
     __threadfence();
     double sumsq;
     unsigned ovf;
