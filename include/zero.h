@@ -62,12 +62,14 @@ extern "C" {
 
 #define ZERO_ABI_VERSION 1
 #define ZERO_MAX_WORLD 64
+/* Most elements of all parameters together (2^36: more than one GPU holds). */
+#define ZERO_MAX_ELEMS (((long long)1) << 36)
 
 typedef enum {
   ZERO_OK = 0,
   ZERO_ERR_INVALID = 1, /* bad argument: null, size, alignment, dtype, stage, world */
   ZERO_ERR_CUDA = 2,    /* a CUDA runtime call failed; the message names it */
-  ZERO_ERR_OOM = 3,     /* the library's own small device allocation failed */
+  ZERO_ERR_OOM = 3,     /* the library's own small device allocation, or a host allocation, failed */
   ZERO_ERR_TIMEOUT = 4, /* reserved: a bounded device wait gave up */
   ZERO_ERR_STATE = 5    /* call out of order (e.g. step before bind/init) */
 } zero_status;
@@ -185,7 +187,10 @@ typedef struct {
  * already holds a parameter (a parameter is never split); each bucket is
  * padded to a multiple of W*128 elements; rank r owns
  * [start + r*len/W, start + (r+1)*len/W) of every bucket.
- * *out receives a host object freed by zero_layout_destroy. Host only. */
+ * *out receives a host object freed by zero_layout_destroy. Host only.
+ * ZERO_ERR_INVALID when the parameters hold more than ZERO_MAX_ELEMS
+ * elements in all; ZERO_ERR_OOM when host memory runs out (*out stays NULL
+ * in both cases). */
 int zero_layout_create(const int64_t* const* shapes, const int* ndims, int n_params,
                        const zero_config* cfg, zero_layout_t** out);
 

@@ -5,7 +5,7 @@ hand-written CUDA for sm_103a). ``_abi`` binds its entry points one for one;
 ``engine.ZeroStep`` owns the device buffers of one layout. No CPU fallback
 exists: without the built library every call raises.
 """
-from ._abi import (ZERO_BF16, ZERO_STATE_BLOB_BYTES, zero_accumulate, zero_gather_bucket,
+from ._abi import (ZERO_BF16, ZERO_MAX_ELEMS, ZERO_STATE_BLOB_BYTES, zero_accumulate, zero_gather_bucket,
                    zero_loss_scale_state_async, zero_state_blob_decode, zero_scaler_restore, zero_selftest_wait_timeout,
                    zero_selftest_layout_timeout,
                    zero_state_export_params, zero_state_import_params, ZERO_F16, ZERO_F32, ZeroError, zero_bucket_range, zero_config,

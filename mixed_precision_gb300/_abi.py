@@ -18,6 +18,7 @@ LIB_PATH = os.path.join(_HERE, "libzero_gb300.so")
 ZERO_OK, ZERO_ERR_INVALID, ZERO_ERR_CUDA, ZERO_ERR_OOM, ZERO_ERR_TIMEOUT, ZERO_ERR_STATE = range(6)
 ZERO_F32, ZERO_F16, ZERO_BF16 = 0, 1, 2
 ZERO_MAX_WORLD = 64
+ZERO_MAX_ELEMS = 1 << 36
 ZERO_STATE_BLOB_BYTES = 256
 STATUS_NAME = {0: "ZERO_OK", 1: "ZERO_ERR_INVALID", 2: "ZERO_ERR_CUDA", 3: "ZERO_ERR_OOM",
                4: "ZERO_ERR_TIMEOUT", 5: "ZERO_ERR_STATE"}

@@ -9,6 +9,7 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <memory>
 #include <new>
 #include <string>
 #include <vector>
@@ -497,6 +498,19 @@ int check_allreduce(const zero_layout* L, void* const* allreduce_out) {
 
 }  // namespace
 
+// No C++ exception crosses the C ABI: the entry points that allocate host
+// memory run their bodies through this.
+template <typename F>
+int guarded(F&& body) {
+  try {
+    return body();
+  } catch (const std::bad_alloc&) {
+    return fail(ZERO_ERR_OOM, "host allocation failed");
+  } catch (...) {
+    return fail(ZERO_ERR_INVALID, "unexpected host error");
+  }
+}
+
 extern "C" {
 
 const char* zero_last_error(void) { return g_last_error.c_str(); }
@@ -515,8 +529,8 @@ int zero_set_step_events(zero_layout_t* L, void* const* events) {
   return ZERO_OK;
 }
 
-int zero_layout_create(const int64_t* const* shapes, const int* ndims, int n_params,
-                       const zero_config* cfg, zero_layout_t** out) {
+static int layout_create(const int64_t* const* shapes, const int* ndims, int n_params,
+                         const zero_config* cfg, zero_layout_t** out) {
   if (out == nullptr || cfg == nullptr) return fail(ZERO_ERR_INVALID, "NULL argument");
   *out = nullptr;
   if (n_params <= 0) return fail(ZERO_ERR_INVALID, "n_params must be positive");
@@ -533,35 +547,34 @@ int zero_layout_create(const int64_t* const* shapes, const int* ndims, int n_par
   if (cfg->bucket_bytes / dtype_bytes(cfg->grad_dtype) < 1)
     return fail(ZERO_ERR_INVALID, "bucket_bytes smaller than one gradient element");
 
-  zero_layout* L = new (std::nothrow) zero_layout();
-  if (L == nullptr) return fail(ZERO_ERR_OOM, "host allocation failed");
+  std::unique_ptr<zero_layout> L(new zero_layout());
   L->cfg = *cfg;
   L->comm_dtype = comm;
   L->numel.resize(n_params);
   for (int p = 0; p < n_params; ++p) {
-    if (ndims[p] < 0 || ndims[p] > 8 || (ndims[p] > 0 && shapes[p] == nullptr)) {
-      delete L;
+    if (ndims[p] < 0 || ndims[p] > 8 || (ndims[p] > 0 && shapes[p] == nullptr))
       return fail(ZERO_ERR_INVALID, "parameter %d: bad ndims/shape", p);
-    }
     int64_t n = 1;
     for (int d = 0; d < ndims[p]; ++d) {
       const int64_t k = shapes[p][d];
-      if (k < 0 || (k > 0 && n > (int64_t(1) << 46) / k)) {
-        delete L;
+      if (k < 0 || (k > 0 && n > ZERO_MAX_ELEMS / k))
         return fail(ZERO_ERR_INVALID, "parameter %d: negative or oversized dimension", p);
-      }
       n *= k;
     }
+    if (n > ZERO_MAX_ELEMS - L->n_real)
+      return fail(ZERO_ERR_INVALID, "more than %lld elements in all", (long long)ZERO_MAX_ELEMS);
     L->numel[p] = n;
     L->n_real += n;
   }
-  build_layout(L);
-  if (L->tiles.size() > (size_t)INT32_MAX) {
-    delete L;
-    return fail(ZERO_ERR_INVALID, "model too large for the tile table");
-  }
-  *out = L;
+  build_layout(L.get());
+  if (L->tiles.size() > (size_t)INT32_MAX) return fail(ZERO_ERR_INVALID, "model too large for the tile table");
+  *out = L.release();
   return ZERO_OK;
+}
+
+int zero_layout_create(const int64_t* const* shapes, const int* ndims, int n_params,
+                       const zero_config* cfg, zero_layout_t** out) {
+  return guarded([&] { return layout_create(shapes, ndims, n_params, cfg, out); });
 }
 
 int zero_layout_destroy(zero_layout_t* L) {
@@ -652,8 +665,8 @@ int zero_shard_range(const zero_layout_t* L, int bucket, int rank, int64_t* flat
   return ZERO_OK;
 }
 
-int zero_state_bind(zero_layout_t* L, void* master, void* m, void* v, void* params_flat,
-                    void* scratch) {
+static int state_bind(zero_layout_t* L, void* master, void* m, void* v, void* params_flat,
+                      void* scratch) {
   if (int rc = check_layout(L)) return rc;
   if (master == nullptr || m == nullptr || v == nullptr || params_flat == nullptr)
     return fail(ZERO_ERR_INVALID, "master/m/v/params_flat must not be NULL");
@@ -742,6 +755,11 @@ int zero_state_bind(zero_layout_t* L, void* master, void* m, void* v, void* para
   L->bound = true;
   L->initialized = false;
   return ZERO_OK;
+}
+
+int zero_state_bind(zero_layout_t* L, void* master, void* m, void* v, void* params_flat,
+                    void* scratch) {
+  return guarded([&] { return state_bind(L, master, m, v, params_flat, scratch); });
 }
 
 int zero_state_bind_alternate(zero_layout_t* L, void* master2, void* m2, void* v2) {
@@ -899,8 +917,8 @@ int zero_step_tensors(zero_layout_t* L, const void* const* grad_ptrs, void* cons
   return launch_step(L, src, allreduce_out, hp, s);
 }
 
-int zero_step_host(zero_layout_t* L, const void* const* host_grads, void* const* dev_grads,
-                   void* const* allreduce_out, const zero_hparams* hp, void* stream) {
+static int step_host(zero_layout_t* L, const void* const* host_grads, void* const* dev_grads,
+                     void* const* allreduce_out, const zero_hparams* hp, void* stream) {
   Range r_entry("zero_step_host");
   if (int rc = check_ready(L, true)) return rc;
   if (host_grads == nullptr || dev_grads == nullptr)
@@ -974,6 +992,11 @@ int zero_step_host(zero_layout_t* L, const void* const* host_grads, void* const*
   hs->recorded = L->k1_recorded;
   L->k1_done = nullptr;
   return rc;
+}
+
+int zero_step_host(zero_layout_t* L, const void* const* host_grads, void* const* dev_grads,
+                   void* const* allreduce_out, const zero_hparams* hp, void* stream) {
+  return guarded([&] { return step_host(L, host_grads, dev_grads, allreduce_out, hp, stream); });
 }
 
 int zero_accumulate(zero_layout_t* L, const void* const* micro, int micro_dtype, float* const* main,

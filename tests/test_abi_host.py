@@ -165,6 +165,42 @@ def test_invalid_arguments(zlib):
     zlib.zero_layout_destroy(h)
 
 
+def test_size_limits(zlib):
+    """The parameters' total is capped at ZERO_MAX_ELEMS (2^36) elements, per
+    parameter and in all; below the cap, element offsets past 2^32 are exact."""
+    cap = zlib.ZERO_MAX_ELEMS
+    assert cap == 1 << 36
+    for shapes in ([(cap + 1,)], [(1 << 20, (1 << 16) + 1)], [(cap // 2 + 1,), (cap // 2 + 1,)],
+                   [(1 << 40, 1 << 40)]):
+        with pytest.raises(zlib.ZeroError) as e:
+            zlib.zero_layout_create(shapes, _cfg(zlib, 2))
+        assert e.value.code == 1
+    # 5 parameters, three of them past 2^31 elements and ending past 2^33
+    big = [(3,), ((1 << 31) + 5,), (1 << 31, 3), (7,), ((1 << 31) + 64,)]
+    h = zlib.zero_layout_create(big, _cfg(zlib, 2, bucket=1 << 33))
+    info = zlib.zero_layout_query(h)
+    n = [3, (1 << 31) + 5, 3 << 31, 7, (1 << 31) + 64]
+    assert info.n_real == sum(n)
+    # offsets: each parameter starts on the next multiple of 64 (one bucket
+    # of 2^32 bf16 elements holds p0..p1; p2 opens the next, and so on)
+    offs = [zlib.zero_param_offset(h, p) for p in range(5)]
+    assert offs[0] == 0 and offs[1] == 64
+    for p in range(1, 5):
+        assert offs[p] % 64 == 0 and offs[p] >= offs[p - 1] + n[p - 1]
+    assert offs[4] > 1 << 33
+    # every rank's slice of every bucket is equal and tiles the bucket
+    total = 0
+    for b in range(info.n_buckets):
+        b0, bl = zlib.zero_bucket_range(h, b)
+        assert b0 == total and bl % (2 * 128) == 0
+        for r in range(2):
+            f0, s0, ln = zlib.zero_shard_range(h, b, r)
+            assert (f0, ln) == (b0 + r * bl // 2, bl // 2)
+        total += bl
+    assert total == info.n_padded
+    zlib.zero_layout_destroy(h)
+
+
 def test_allocator_failure_is_oom(zlib):
     from mixed_precision_gb300 import _abi
     calls = []

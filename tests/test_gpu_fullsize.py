@@ -174,3 +174,52 @@ def test_fullsize_speculative(name, plan):
             assert st["clip_coef"] < 1.0
         del g
     z.close()
+
+
+def test_tensor_past_2_31_elements():
+    """One parameter of 2^31 + 200 elements between two small ones, W=2,
+    ZeRO-2, bf16: offsets inside that parameter pass 2^31 in the per-tensor
+    pointer mode and in the per-tensor gather. The flat and per-tensor entry
+    points agree bit for bit, the sampled oracle agrees (the samples include
+    the parameter's last element), and the gathered tensors equal the flat
+    parameters."""
+    shapes = [(300,), ((1 << 31) + 200,), (77,)]
+    W = 2
+
+    def setup():
+        z = ZeroStep(shapes, W, 2, 1 << 30, wl.BF16, wl.BF16)
+        z.allocate()
+        m0 = wl.master_init(z.offsets, numel, z.np, 0.02, wl.master_seed(150), device="cuda")
+        z.init(m0)
+        return z, m0
+
+    numel = wl.numels(shapes)
+    za, master0 = setup()
+    zb, m0b = setup()
+    del m0b
+    assert za.offsets[1] + numel[1] > 1 << 31
+    so = SampledOracle(za, numel, master0, sample_indices(za, numel, 20_000, 5), 1.0, False, 1000)
+    del master0
+    g = [wl.flat_grads(za.offsets, numel, za.np, 1e-4, wl.grad_seed(150, r, 0), wl.BF16,
+                       device="cuda") for r in range(W)]
+    hp = Hparams()
+    za.step(g, hp)
+    zb.step_tensors([[zb.param_view(g[r], p) for p in range(len(shapes))] for r in range(W)], hp)
+    torch.cuda.synchronize()
+    st = za.scaler_state()
+    assert st == zb.scaler_state()
+    for a, b in ((za.master, zb.master), (za.m, zb.m), (za.v, zb.v)):
+        assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+    assert torch.equal(za.params_flat.view(torch.int16), zb.params_flat.view(torch.int16))
+    zb.close()
+    del zb
+    info, red_at = so.step(g, hp)
+    so.check(st, info, red_at)
+    del g
+    dst = [[torch.empty(n, dtype=torch.bfloat16, device="cuda") for n in numel]]
+    za.gather(dst)
+    torch.cuda.synchronize()
+    for p in range(len(shapes)):
+        assert torch.equal(dst[0][p].view(torch.int16),
+                           za.param_view(za.params_flat, p).view(torch.int16))
+    za.close()
