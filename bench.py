@@ -33,16 +33,17 @@ if ROOT not in sys.path:
 METRIC = "ZeRO step params updated/s and achieved HBM GB/s (% of GB300 step roofline)"
 DEFAULT_WORKLOAD = "qwen3_0.6b_bf16_w2"
 L2_BYTES = 129 * 1000 * 1000
-# DRAM bytes per real element of the update kernel from one ncu capture
+# DRAM bytes per real element of each dominant kernel from one ncu capture
 # (dram__bytes_read.sum + dram__bytes_write.sum / elements), with the capture
 # it comes from; None until a capture of the current kernel exists.
 NCU_TRAFFIC_PER_ELEM = {
-    # profiles/k_adamw_cast_ws_qwen3_layers8.md: (1.7628 + 1.7005) GB / 125,847,552 elements
-    "k_adamw_cast": 27.52,
-    # profiles/k_reduce_norm_ws_qwen3_layers8.md: (504.1 + 204.9) MB / 125,847,552 elements
-    "k_reduce_norm": 5.634,
-    # profiles/k_spec_step_qwen3_layers8.md: (2.0232 + 1.7131) GB / 125,847,552 elements
-    "k_spec_step": 29.69,
+    # profiles/dram_bytes_qwen3_0.6b_bf16_w2.md, one full-size launch:
+    # (8.350264 + 8.280116) GB / 596,049,920 elements
+    "k_adamw_cast": 27.901,
+    # the same capture: (2.387917 + 1.156840) GB / 596,049,920 elements
+    "k_reduce_norm": 5.947,
+    # profiles/k_spec_step_qwen3_layers8.md: (2.0236 + 1.7146) GB / 125,847,552 elements
+    "k_spec_step": 29.70,
 }
 
 
