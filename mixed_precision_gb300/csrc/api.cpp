@@ -68,7 +68,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 int dtype_bytes(int d) { return d == ZERO_F32 ? 4 : 2; }
 bool valid_dtype(int d) { return d == ZERO_F32 || d == ZERO_F16 || d == ZERO_BF16; }
 
-constexpr int kMaxPartials = 4096;  // upper bound on the reduce grid (SMs x blocks/SM)
+constexpr int kMaxPartials = 8192;  // upper bound on the reduce and single-pass grids
 constexpr int kMaxPerTensorGrid = 1024;  // per-tensor launches: blocks per launch at most
 
 void* default_alloc(size_t n, void*) {
@@ -665,6 +665,24 @@ int zero_shard_range(const zero_layout_t* L, int bucket, int rank, int64_t* flat
   return ZERO_OK;
 }
 
+// Grid sizes of the streaming kernels, as multiples of the blocks that fit on
+// the GPU at once. Every kernel walks its tiles grid-stride, so any grid is
+// correct; launching several times the resident blocks, so that blocks
+// finish and new ones start throughout the pass, moved more bytes per second
+// than a grid of exactly the resident blocks (measured on GB300: the update
+// 2.65 -> 2.42 ms, the reduce 0.570 -> 0.547 ms, the single pass 2.84 ->
+// 2.63 ms on the 596M-element workload). The environment variable `name`,
+// read at bind, overrides the default (1..64).
+constexpr int kReduceGridMult = 4;
+constexpr int kUpdateGridMult = 32;
+constexpr int kSpecGridMult = 13;
+constexpr int kCopyGridMult = 32;
+static int grid_mult(const char* name, int dflt) {
+  const char* v = std::getenv(name);
+  const int m = v ? std::atoi(v) : dflt;
+  return m < 1 ? 1 : (m > 64 ? 64 : m);
+}
+
 static int state_bind(zero_layout_t* L, void* master, void* m, void* v, void* params_flat,
                       void* scratch) {
   if (int rc = check_layout(L)) return rc;
@@ -741,9 +759,10 @@ static int state_bind(zero_layout_t* L, void* master, void* m, void* v, void* pa
     const int bps_u = update_blocks_per_sm(L->comm_dtype, L->cfg.param_dtype, L->update_variant);
     if (bps_r <= 0 || bps_u <= 0)
       return fail(ZERO_ERR_CUDA, "kernel occupancy query failed (no sm_103a image for this GPU?)");
-    L->grid_reduce = std::max(1, std::min({n_tiles, sms * bps_r, kMaxPartials}));
-    L->grid_update = std::max(1, std::min(n_tiles, sms * bps_u));
-    L->grid_copy = std::max(1, std::min(n_tiles, sms * 4));
+    L->grid_reduce =
+        std::max(1, std::min({n_tiles, sms * bps_r * grid_mult("ZERO_REDUCE_GRID_MULT", kReduceGridMult), kMaxPartials}));
+    L->grid_update = std::max(1, std::min(n_tiles, sms * bps_u * grid_mult("ZERO_UPDATE_GRID_MULT", kUpdateGridMult)));
+    L->grid_copy = std::max(1, std::min(n_tiles, sms * 4 * grid_mult("ZERO_COPY_GRID_MULT", kCopyGridMult)));
   }
   L->master = static_cast<float*>(master);
   L->m = static_cast<float*>(m);
@@ -789,7 +808,8 @@ int zero_state_bind_alternate(zero_layout_t* L, void* master2, void* m2, void* v
   L->chunk_spec = chunk;
   int sms = 0;
   ZERO_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, L->device));
-  L->grid_spec = std::max(1, std::min({(int)L->tiles.size(), sms * bps, kMaxPartials}));
+  L->grid_spec = std::max(
+      1, std::min({(int)L->tiles.size(), sms * bps * grid_mult("ZERO_SPEC_GRID_MULT", kSpecGridMult), kMaxPartials}));
   L->master2 = static_cast<float*>(master2);
   L->m2 = static_cast<float*>(m2);
   L->v2 = static_cast<float*>(v2);

@@ -176,9 +176,9 @@ __device__ inline void warp_sum_partials(const double* part, const unsigned* ovf
   const int lane = threadIdx.x & 31;
   double acc = 0.0;
   unsigned o = 0u;
-  // Eight independent loads in flight per lane, then the adds in index order
-  // (lane, lane + 32, ...): one L2 round trip per eight partials.
-  constexpr int U = 8;
+  // Sixteen independent loads in flight per lane, then the adds in index
+  // order (lane, lane + 32, ...): one L2 round trip per sixteen partials.
+  constexpr int U = 16;
   for (int base = lane; base < n; base += 32 * U) {
     double v[U];
     unsigned f[U];
