@@ -22,6 +22,8 @@
 // Bytes per element when it commits: 2W (grads) + 24 (state) + 2 (params).
 #pragma once
 
+#include <type_traits>
+
 #include "k_reduce.cuh"
 
 namespace zg {
@@ -166,13 +168,18 @@ __global__ void __launch_bounds__((NC + 1) * 32) k_spec_step(const __grid_consta
     // load (8 or 16 bytes per lane) and global store then covers contiguous
     // bytes across the warp: no bank conflicts, fully coalesced stores.
     const int w1 = min(nb, (warp + 1) * per);
+    // The warp's slice of the stage. Instantiated twice: without NULL-rank
+    // tests (flat buffers, or a tile every rank has a gradient for) and with
+    // them, so the common case carries no per-rank branch.
+    auto slice = [&](auto with_nulls) {
+      constexpr bool kNulls = decltype(with_nulls)::value;
     for (int base = warp * per; base < w1; base += 256) {
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const int e = base + 128 * h + 4 * lane;
         if (e >= w1) continue;
         float acc[4];
-        if (nulls & 1ull) {
+        if (kNulls && (nulls & 1ull)) {
 #pragma unroll
           for (int j = 0; j < 4; ++j) acc[j] = 0.0f;
         } else {
@@ -181,7 +188,7 @@ __global__ void __launch_bounds__((NC + 1) * 32) k_spec_step(const __grid_consta
 #pragma unroll(WT ? WT : 1)
         for (int w = 1; w < W; ++w) {
           float x[4];
-          if ((nulls >> w) & 1ull) {
+          if (kNulls && ((nulls >> w) & 1ull)) {
 #pragma unroll
             for (int j = 0; j < 4; ++j) x[j] = 0.0f;
           } else {
@@ -216,6 +223,12 @@ __global__ void __launch_bounds__((NC + 1) * 32) k_spec_step(const __grid_consta
         store4_f32(dst_v + so + e, v);
         store4_raw(pp + e, q);
       }
+    }
+    };
+    if (nulls == 0ull) {
+      slice(std::false_type{});
+    } else {
+      slice(std::true_type{});
     }
     if (warp == 0 && lane < clen - nb) {  // ragged tail, from global memory
       const int e = nb + lane;
