@@ -37,9 +37,13 @@ L2_BYTES = 129 * 1000 * 1000
 # (dram__bytes_read.sum + dram__bytes_write.sum / elements), with the capture
 # it comes from; None until a capture of the current kernel exists.
 NCU_TRAFFIC_PER_ELEM = {
-    "k_adamw_cast": None,
-    "k_reduce_norm": None,
-    "k_spec_step": None,
+    # profiles/dram_bytes_qwen3_0.6b_bf16_w2.md, one full-size launch each:
+    # (8.348124 + 8.280789) GB / 596,049,920 elements
+    "k_adamw_cast": 27.898,
+    # (2.387236 + 1.155004) GB / 596,049,920 elements
+    "k_reduce_norm": 5.943,
+    # (9.540655 + 8.295674) GB / 596,049,920 elements
+    "k_spec_step": 29.924,
 }
 
 
