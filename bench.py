@@ -42,8 +42,8 @@ NCU_TRAFFIC_PER_ELEM = {
     "k_adamw_cast": 27.898,
     # (2.387236 + 1.155004) GB / 596,049,920 elements
     "k_reduce_norm": 5.943,
-    # (9.540655 + 8.295674) GB / 596,049,920 elements
-    "k_spec_step": 29.924,
+    # (9.540289 + 8.295399) GB / 596,049,920 elements (7904 blocks)
+    "k_spec_step": 29.923,
 }
 
 

@@ -671,12 +671,15 @@ int zero_shard_range(const zero_layout_t* L, int bucket, int rank, int64_t* flat
 // finish and new ones start throughout the pass, moved more bytes per second
 // than a grid of exactly the resident blocks (measured on GB300: the update
 // 2.65 -> 2.42 ms, the reduce 0.570 -> 0.547 ms, the single pass 2.84 ->
-// 2.63 ms on the 596M-element workload). The environment variable `name`,
+// 2.60 ms on the 596M-element workload). The environment variable `name`,
 // read at bind, overrides the default (1..64).
 constexpr int kReduceGridMult = 4;
 constexpr int kUpdateGridMult = 32;
-constexpr int kSpecGridMult = 13;
 constexpr int kCopyGridMult = 32;
+// The single pass: 26x up to W = 4, 13x above (at W = 8 its consumers do
+// more work per byte and 26x was 1.6 % slower than 13x; at W = 2 and 4, 26x
+// was 0.6-0.9 % faster).
+static int spec_grid_mult_default(int world) { return world <= 4 ? 26 : 13; }
 static int grid_mult(const char* name, int dflt) {
   const char* v = std::getenv(name);
   const int m = v ? std::atoi(v) : dflt;
@@ -809,7 +812,7 @@ int zero_state_bind_alternate(zero_layout_t* L, void* master2, void* m2, void* v
   int sms = 0;
   ZERO_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, L->device));
   L->grid_spec = std::max(
-      1, std::min({(int)L->tiles.size(), sms * bps * grid_mult("ZERO_SPEC_GRID_MULT", kSpecGridMult), kMaxPartials}));
+      1, std::min({(int)L->tiles.size(), sms * bps * grid_mult("ZERO_SPEC_GRID_MULT", spec_grid_mult_default(L->world())), kMaxPartials}));
   L->master2 = static_cast<float*>(master2);
   L->m2 = static_cast<float*>(m2);
   L->v2 = static_cast<float*>(v2);
