@@ -130,6 +130,9 @@ struct zero_layout {
   size_t gather_cap = 0;
 
   int grid_reduce = 0, grid_update = 0, grid_copy = 0;
+  // the speculative step's guarded update and parameter restore: no-ops on
+  // committed steps, so their grids stay small (each block still starts)
+  int grid_update_guarded = 0, grid_copy_guarded = 0;
   int grid_spec = 0;  // speculative single pass (set by zero_state_bind_alternate)
   int chunk_reduce = 0;  // the pipelined reduce's elements per stage (set at bind)
   int chunk_spec = 0;  // its elements per pipeline stage
@@ -358,7 +361,7 @@ int launch_step(zero_layout* L, const GradSrc& src, void* const* allreduce_out,
     ua.state = L->d_state;
     ua.error = &L->d_state->error;
     Range r("K3 unscale+clip+AdamW+cast");
-    e = launch_update(ua, L->grid_update, L->update_variant, s);
+    e = launch_update(ua, guarded ? L->grid_update_guarded : L->grid_update, L->update_variant, s);
     if (e != cudaSuccess) return cuda_fail(e, "update kernel launch");
   }
   if (L->timing) ZERO_CUDA(cudaEventRecord(L->events[3], s));
@@ -404,7 +407,7 @@ int launch_step_spec(zero_layout* L, const GradSrc& src, const zero_hparams* hp,
   L->timing = timing;
   if (rc != ZERO_OK) return rc;
   e = launch_recast(L->d_tiles, n_tiles, sa.master, L->params, L->cfg.param_dtype, L->cfg.stage == 3,
-                    L->d_state, /*guarded=*/1, L->grid_copy, s);
+                    L->d_state, /*guarded=*/1, L->grid_copy_guarded, s);
   if (e != cudaSuccess) return cuda_fail(e, "parameter restore launch");
   if (L->timing) ZERO_CUDA(cudaEventRecord(L->events[3], s));
   return ZERO_OK;
@@ -670,12 +673,17 @@ int zero_shard_range(const zero_layout_t* L, int bucket, int rank, int64_t* flat
 // correct; launching several times the resident blocks, so that blocks
 // finish and new ones start throughout the pass, moved more bytes per second
 // than a grid of exactly the resident blocks (measured on GB300: the update
-// 2.65 -> 2.42 ms, the reduce 0.570 -> 0.547 ms, the single pass 2.84 ->
-// 2.60 ms on the 596M-element workload). The environment variable `name`,
-// read at bind, overrides the default (1..64).
+// 2.65 -> 2.42 ms at 32x and 2.37 ms at one block per tile, the reduce
+// 0.570 -> 0.547 ms, the single pass 2.84 -> 2.60 ms on the 596M-element
+// workload). The update's gain grew with the grid up to one block per tile
+// (blocks start in index order, so the tiles in flight are consecutive); the
+// reduce and the single pass keep one norm partial per block and stop at 4x
+// and 13-26x.
+// The environment variable `name`, read at bind, overrides the default
+// (1..2048).
 constexpr int kReduceGridMult = 4;
-constexpr int kUpdateGridMult = 32;
-constexpr int kCopyGridMult = 32;
+constexpr int kCopyGridMult = 128;
+constexpr int kGuardedGridMult = 32;
 // The single pass: 26x up to W = 4, 13x above (at W = 8 its consumers do
 // more work per byte and 26x was 1.6 % slower than 13x; at W = 2 and 4, 26x
 // was 0.6-0.9 % faster).
@@ -683,7 +691,7 @@ static int spec_grid_mult_default(int world) { return world <= 4 ? 26 : 13; }
 static int grid_mult(const char* name, int dflt) {
   const char* v = std::getenv(name);
   const int m = v ? std::atoi(v) : dflt;
-  return m < 1 ? 1 : (m > 64 ? 64 : m);
+  return m < 1 ? 1 : (m > 2048 ? 2048 : m);
 }
 
 static int state_bind(zero_layout_t* L, void* master, void* m, void* v, void* params_flat,
@@ -769,8 +777,15 @@ static int state_bind(zero_layout_t* L, void* master, void* m, void* v, void* pa
       return fail(ZERO_ERR_CUDA, "kernel occupancy query failed (no sm_103a image for this GPU?)");
     L->grid_reduce =
         std::max(1, std::min({n_tiles, sms * bps_r * grid_mult("ZERO_REDUCE_GRID_MULT", kReduceGridMult), kMaxPartials}));
-    L->grid_update = std::max(1, std::min(n_tiles, sms * bps_u * grid_mult("ZERO_UPDATE_GRID_MULT", kUpdateGridMult)));
+    // The update: one block per tile unless ZERO_UPDATE_GRID_MULT asks for a
+    // multiple of the resident blocks.
+    L->grid_update = std::getenv("ZERO_UPDATE_GRID_MULT") == nullptr
+                         ? std::max(1, n_tiles)
+                         : std::max(1, std::min(n_tiles, sms * bps_u * grid_mult("ZERO_UPDATE_GRID_MULT", 1)));
     L->grid_copy = std::max(1, std::min(n_tiles, sms * 4 * grid_mult("ZERO_COPY_GRID_MULT", kCopyGridMult)));
+    const int gm = grid_mult("ZERO_GUARDED_GRID_MULT", kGuardedGridMult);
+    L->grid_update_guarded = std::max(1, std::min(n_tiles, sms * bps_u * gm));
+    L->grid_copy_guarded = std::max(1, std::min(n_tiles, sms * 4 * gm));
   }
   L->master = static_cast<float*>(master);
   L->m = static_cast<float*>(m);
