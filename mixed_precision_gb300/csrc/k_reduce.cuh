@@ -14,9 +14,10 @@
 // reduce-scatter output). Stage 1 writes r into all W flat outputs (the
 // all-reduce). Every thread accumulates sum(r^2) (fp32 over 8 elements, then
 // a compensated fp32 running sum, fp64 for huge groups) and an "any non-finite
-// r" flag; each block writes one fp64 partial and one flag. The grid is
-// persistent (a multiple of the SM count) and walks the tile list with a
-// fixed stride, so the partials are deterministic. In the pipelined kernel,
+// r" flag; each block writes one fp64 partial and one flag. The grid (a
+// multiple of the blocks the GPU holds at once, fixed at bind) walks the tile
+// list with a fixed stride, so for a given grid the partials are
+// deterministic. In the pipelined kernel,
 // the last block to finish then runs the finalize (finalize.cuh).
 #pragma once
 
