@@ -173,57 +173,57 @@ __global__ void __launch_bounds__((NC + 1) * 32) k_spec_step(const __grid_consta
     // them, so the common case carries no per-rank branch.
     auto slice = [&](auto with_nulls) {
       constexpr bool kNulls = decltype(with_nulls)::value;
-    for (int base = warp * per; base < w1; base += 256) {
+      for (int base = warp * per; base < w1; base += 256) {
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int e = base + 128 * h + 4 * lane;
-        if (e >= w1) continue;
-        float acc[4];
-        if (kNulls && (nulls & 1ull)) {
+        for (int h = 0; h < 2; ++h) {
+          const int e = base + 128 * h + 4 * lane;
+          if (e >= w1) continue;
+          float acc[4];
+          if (kNulls && (nulls & 1ull)) {
 #pragma unroll
-          for (int j = 0; j < 4; ++j) acc[j] = 0.0f;
-        } else {
-          load4_smem(sg + e, acc);
-        }
-#pragma unroll(WT ? WT : 1)
-        for (int w = 1; w < W; ++w) {
-          float x[4];
-          if (kNulls && ((nulls >> w) & 1ull)) {
-#pragma unroll
-            for (int j = 0; j < 4; ++j) x[j] = 0.0f;
+            for (int j = 0; j < 4; ++j) acc[j] = 0.0f;
           } else {
-            load4_smem(sg + w * C + e, x);
+            load4_smem(sg + e, acc);
           }
+#pragma unroll(WT ? WT : 1)
+          for (int w = 1; w < W; ++w) {
+            float x[4];
+            if (kNulls && ((nulls >> w) & 1ull)) {
 #pragma unroll
-          for (int j = 0; j < 4; ++j) acc[j] = __fadd_rn(acc[j], x[j]);
-        }
-        float rf[4], p[4], m[4], v[4];
-        float ss = 0.0f;
-        bool fin = true;
+              for (int j = 0; j < 4; ++j) x[j] = 0.0f;
+            } else {
+              load4_smem(sg + w * C + e, x);
+            }
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const CT rc = DT<CT>::from_f32(acc[j]);
-          rf[j] = DT<CT>::to_f32(rc);
-          fin = fin && DT<CT>::finite_bits(rc);
-          ss = __fmaf_rn(rf[j], rf[j], ss);
-        }
-        if (!fin) bad = 1u;
-        add_group(ss, hi, lo, big, rf);
-        load4_smem(sp + e, p);
-        load4_smem(sm + e, m);
-        load4_smem(sv + e, v);
-        PT q[4];
+            for (int j = 0; j < 4; ++j) acc[j] = __fadd_rn(acc[j], x[j]);
+          }
+          float rf[4], p[4], m[4], v[4];
+          float ss = 0.0f;
+          bool fin = true;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          sc.apply(rf[j], p[j], m[j], v[j]);
-          q[j] = DT<PT>::from_f32(p[j]);
+          for (int j = 0; j < 4; ++j) {
+            const CT rc = DT<CT>::from_f32(acc[j]);
+            rf[j] = DT<CT>::to_f32(rc);
+            fin = fin && DT<CT>::finite_bits(rc);
+            ss = __fmaf_rn(rf[j], rf[j], ss);
+          }
+          if (!fin) bad = 1u;
+          add_group(ss, hi, lo, big, rf);
+          load4_smem(sp + e, p);
+          load4_smem(sm + e, m);
+          load4_smem(sv + e, v);
+          PT q[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            sc.apply(rf[j], p[j], m[j], v[j]);
+            q[j] = DT<PT>::from_f32(p[j]);
+          }
+          store4_f32(dst_master + so + e, p);
+          store4_f32(dst_m + so + e, m);
+          store4_f32(dst_v + so + e, v);
+          store4_raw(pp + e, q);
         }
-        store4_f32(dst_master + so + e, p);
-        store4_f32(dst_m + so + e, m);
-        store4_f32(dst_v + so + e, v);
-        store4_raw(pp + e, q);
       }
-    }
     };
     if (nulls == 0ull) {
       slice(std::false_type{});
