@@ -18,7 +18,7 @@ import torch
 import oracle
 import workloads as wl
 from _parity import to_np
-from _util import params_close, rel_err, scaled_err
+from _util import params_close, plain_param_stats, plain_state_stats, rel_err, scaled_err
 from mixed_precision_gb300 import _abi as abi
 
 
@@ -166,15 +166,18 @@ class SampledOracle:
                 assert np.array_equal(to_np(out[fl]), red_at)
         worst = 0.0
         cur = z.current_state() if hasattr(z, "master2") else (z.master, z.m, z.v)
-        for t, ref, h in zip(cur, (self.master, self.m, self.v), self.hist):
+        for name, t, ref, h in zip(("master", "m", "v"), cur, (self.master, self.m, self.v),
+                                   self.hist):
             got = t[sh].cpu().numpy()
             e = scaled_err(got, ref, h)
             worst = max(worst, float(e.max()))
             bad = rel_err(got, ref) > rtol
             assert np.all(np.abs(ref[bad]) < 0.1 * h[bad])
+            plain_state_stats("fullsize", name, got, ref, rtol)
         assert worst <= rtol, worst
         p = to_np(z.params_flat[fl])
         exp = oracle.encode(self.master, z.param_dtype)
+        plain_param_stats("fullsize", p, exp)
         ok = params_close(p, exp, oracle.decode(exp, z.param_dtype), oracle.decode(p, z.param_dtype),
                           rtol * self.hist[0].astype(np.float64), z.param_dtype == wl.BF16)
         assert ok.all(), int((~ok).sum())

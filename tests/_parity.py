@@ -12,7 +12,7 @@ import torch
 
 import oracle
 import workloads as wl
-from _util import params_close, rel_err, scaled_err, ulp_diff16
+from _util import params_close, plain_param_stats, plain_state_stats, rel_err, scaled_err, ulp_diff16
 from mixed_precision_gb300.engine import Hparams, ZeroStep
 
 INF_BITS = {wl.BF16: 0x7F80, wl.F16: 0x7C00}
@@ -188,6 +188,7 @@ class Pair:
             plain = rel_err(got, r)
             bad = plain > rtol
             assert np.all(np.abs(r[bad]) < 0.1 * h[bad]), f"{name}: mismatch away from a cancellation"
+            plain_state_stats("parity", name, got, r, rtol)
         assert worst <= rtol, worst
         p = to_np(self.z.params_flat)[:self.np]
         if self.stage == 3:  # sharded parameters: put them back in flat order
@@ -199,6 +200,7 @@ class Pair:
         bound[self.perm] = rtol * self.hist[0].astype(np.float64)
         ok = params_close(p, self.o_params, oracle.decode(self.o_params, self.pdt),
                           oracle.decode(p, self.pdt), bound, self.pdt == wl.BF16)
+        plain_param_stats("parity", p, self.o_params, self.mask_flat)
         bad = np.nonzero(~ok & self.mask_flat)[0]
         if len(bad):
             offs = np.array(self.offsets)
