@@ -12,8 +12,13 @@
 //
 // The caller passes all inputs and outputs. Host code must not hand the
 // array's name to a kernel: on the host that name is only a stand-in, not a
-// device address. The device address is looked up once per device with
-// cudaGetSymbolAddress, on the first call made with that device current.
+// device address. The device address belongs to one CUDA context (each
+// context loads its own copy of the module), so it is looked up with
+// cudaGetSymbolAddress on the first call made in each context and cached
+// under that context's unique ID (cuCtxGetId): a context created after
+// cudaDeviceReset, or one the caller made current through the driver API,
+// gets its own lookup instead of a stale address.
+#include <cuda.h>  // CUcontext / CUresult types; the two driver calls are resolved at run time
 #include <mutex>
 
 #include "k_reduce.cuh"
@@ -137,14 +142,57 @@ static const void* na_kernel(int grad_dtype, int comm_dtype) {
   }
 }
 
-// Per-device set-up: the array's device address and the SM count.
-struct NaDevice {
+// Per-context set-up: the array's device address in that context and the
+// device's SM count, keyed by the context's process-unique ID. The table is
+// small and reused round-robin; IDs are never reused, so an entry of a
+// destroyed context can never be matched again.
+struct NaContext {
+  unsigned long long ctx_id = 0;  // 0: empty slot
   unsigned char* scratch = nullptr;
   int sms = 0;
 };
-constexpr int kNaMaxDevices = 64;
-static NaDevice g_na_devices[kNaMaxDevices];
+constexpr int kNaMaxContexts = 64;
+static NaContext g_na_ctx[kNaMaxContexts];
+static int g_na_next = 0;
 static std::mutex g_na_mutex;
+
+typedef CUresult (*NaCtxGetCurrent)(CUcontext*);
+typedef CUresult (*NaCtxGetId)(CUcontext, unsigned long long*);
+static NaCtxGetCurrent g_get_current = nullptr;
+static NaCtxGetId g_get_id = nullptr;
+
+// The unique ID of the context current on this thread (caller holds
+// g_na_mutex). A thread on which the runtime has not yet made a context
+// current gets the device's primary context first, as any runtime call would.
+static int na_current_context(unsigned long long* id) {
+  if (g_get_current == nullptr || g_get_id == nullptr) {
+    cudaDriverEntryPointQueryResult q1, q2;
+    void* f1 = nullptr;
+    void* f2 = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f1, 12000, cudaEnableDefault, &q1) !=
+            cudaSuccess ||
+        q1 != cudaDriverEntryPointSuccess ||
+        cudaGetDriverEntryPointByVersion("cuCtxGetId", &f2, 12000, cudaEnableDefault, &q2) !=
+            cudaSuccess ||
+        q2 != cudaDriverEntryPointSuccess)
+      return zero_internal_fail(ZERO_ERR_CUDA, "cuCtxGetCurrent / cuCtxGetId not available");
+    g_get_current = reinterpret_cast<NaCtxGetCurrent>(f1);
+    g_get_id = reinterpret_cast<NaCtxGetId>(f2);
+  }
+  CUcontext c = nullptr;
+  if (g_get_current(&c) != CUDA_SUCCESS)
+    return zero_internal_fail(ZERO_ERR_CUDA, "cuCtxGetCurrent failed");
+  if (c == nullptr) {  // no context yet: let the runtime bind the primary one
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return zero_internal_fail(ZERO_ERR_CUDA, cudaGetErrorString(e));
+    if (g_get_current(&c) != CUDA_SUCCESS || c == nullptr)
+      return zero_internal_fail(ZERO_ERR_CUDA, "no CUDA context is current");
+  }
+  if (g_get_id(c, id) != CUDA_SUCCESS || *id == 0)
+    return zero_internal_fail(ZERO_ERR_CUDA, "cuCtxGetId failed");
+  return ZERO_OK;
+}
 
 }  // namespace zg
 
@@ -178,20 +226,29 @@ extern "C" int zero_reduce_norm_noalloc(const void* const* grads, int world, int
   int dev = -1;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return zero_internal_fail(ZERO_ERR_CUDA, cudaGetErrorString(e));
-  if (dev < 0 || dev >= kNaMaxDevices) return zero_internal_fail(ZERO_ERR_CUDA, "device ordinal too large");
-  NaDevice d;
+  NaContext d;
   {
     std::lock_guard<std::mutex> lock(g_na_mutex);
-    NaDevice& slot = g_na_devices[dev];
-    if (slot.scratch == nullptr) {
+    unsigned long long id = 0;
+    const int rc = na_current_context(&id);
+    if (rc != ZERO_OK) return rc;
+    int hit = -1;
+    for (int i = 0; i < kNaMaxContexts; ++i)
+      if (g_na_ctx[i].ctx_id == id) hit = i;
+    if (hit < 0) {  // first call in this context: look the array up here
+      NaContext c;
       void* p = nullptr;
       e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
       if (e != cudaSuccess) return zero_internal_fail(ZERO_ERR_CUDA, cudaGetErrorString(e));
-      e = cudaDeviceGetAttribute(&slot.sms, cudaDevAttrMultiProcessorCount, dev);
+      e = cudaDeviceGetAttribute(&c.sms, cudaDevAttrMultiProcessorCount, dev);
       if (e != cudaSuccess) return zero_internal_fail(ZERO_ERR_CUDA, cudaGetErrorString(e));
-      slot.scratch = static_cast<unsigned char*>(p);
+      c.ctx_id = id;
+      c.scratch = static_cast<unsigned char*>(p);
+      hit = g_na_next;
+      g_na_next = (g_na_next + 1) % kNaMaxContexts;
+      g_na_ctx[hit] = c;
     }
-    d = slot;
+    d = g_na_ctx[hit];
   }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (n == 0) {
