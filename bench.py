@@ -57,6 +57,9 @@ def parse_args(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=10,
                     help="end-to-end steps through the host-buffer entry point (0: skip)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--per-config-steps", type=int, default=20,
+                    help="timed steps of each other named workload after the default line "
+                         "(the MoE ~3.9B list; fp16 W=8 at stages 1 and 2); 0: skip")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="target CPU time of the oracle sample")
     ap.add_argument("--world", type=int, default=None, help="override the simulated world size")
@@ -75,6 +78,11 @@ def parse_args(argv=None):
                     help="launch the step tensor by tensor (the hook-style baseline)")
     ap.add_argument("--tensors", action="store_true",
                     help="step from per-tensor gradient pointers (NULL for all-zero gradients)")
+    ap.add_argument("--sharded", action="store_true",
+                    help="one rank per GPU (torchrun, NCCL): the workload's world is the number "
+                         "of GPUs, each GPU holds its own gradients and its shard of the state; "
+                         "reduce-scatter, norm all-reduce and all-gather between the local "
+                         "kernels (stages 2 and 3)")
     return ap.parse_args(argv)
 
 
@@ -332,6 +340,54 @@ def time_oracle_threads(w, target_elems: int, seconds: float, threads: int):
                                      f"{total} full oracle steps in all")
 
 
+def timed_steps(z, do_step, K: int, W: int, local: int, dist=None, device=None,
+                profile_range: bool = False) -> dict:
+    """W untimed warm-up steps, then K steps bracketed by a barrier and
+    synchronize() on both sides and timed with CUDA events on the launching
+    stream. The library records four events around its own launches in every
+    timed step (zero_set_step_events). Returns the timed region (max over
+    ranks), per-step durations, the per-kernel intervals and the clocks
+    sampled meanwhile."""
+    import torch
+
+    from mixed_precision_gb300 import _abi as abi
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    for row in ev:  # events are created on first record
+        for e in row:
+            e.record()
+    for _ in range(W):
+        do_step()
+    torch.cuda.synchronize()
+    barrier(dist, device)
+
+    sampler = ClockSampler(local).start()
+    time.sleep(0.3)
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    if profile_range:
+        torch.cuda.cudart().cudaProfilerStart()
+    t_start.record()
+    for k in range(K):
+        abi.zero_set_step_events(z.handle, [e.cuda_event for e in ev[k]])
+        do_step()
+    t_end.record()
+    if profile_range:
+        torch.cuda.cudart().cudaProfilerStop()
+    torch.cuda.synchronize()
+    abi.zero_set_step_events(z.handle, None)
+    clocks = sampler.stop()
+    barrier(dist, device)
+    local_ms = t_start.elapsed_time(t_end)
+    return {"total_ms": max_over_ranks(dist, local_ms, device),
+            "steps_ms": sorted(ev[k][0].elapsed_time(ev[k][3]) for k in range(K)),
+            "k1": [ev[k][0].elapsed_time(ev[k][1]) for k in range(K)],
+            "k2": [ev[k][1].elapsed_time(ev[k][2]) for k in range(K)],
+            "k3": [ev[k][2].elapsed_time(ev[k][3]) for k in range(K)],
+            "clocks": clocks}
+
+
 # ---------------------------------------------------------------------------
 # Our arm: the CUDA library through its C ABI
 # ---------------------------------------------------------------------------
@@ -390,44 +446,13 @@ def run_ours(args) -> dict | None:
     hp = Hparams(lr=w.lr, beta1=w.beta1, beta2=w.beta2, eps=w.eps, weight_decay=w.weight_decay,
                  max_grad_norm=w.max_grad_norm)
 
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
-    for row in ev:  # events are created on first record
-        for e in row:
-            e.record()
-    for _ in range(W):
-        do_step()
-    torch.cuda.synchronize()
-    barrier(dist, device)
-
-    sampler = ClockSampler(local).start()
-    time.sleep(0.3)
-    t_start = torch.cuda.Event(enable_timing=True)
-    t_end = torch.cuda.Event(enable_timing=True)
-    torch.cuda.synchronize()
-    if args.profile_range:
-        torch.cuda.cudart().cudaProfilerStart()
-    t_start.record()
-    for k in range(K):
-        abi.zero_set_step_events(z.handle, [e.cuda_event for e in ev[k]])
-        do_step()
-    t_end.record()
-    if args.profile_range:
-        torch.cuda.cudart().cudaProfilerStop()
-    torch.cuda.synchronize()
-    abi.zero_set_step_events(z.handle, None)
-    clocks = sampler.stop()
-    barrier(dist, device)
-    local_ms = t_start.elapsed_time(t_end)
-    total_ms = max_over_ranks(dist, local_ms, device)
+    tm = timed_steps(z, do_step, K, W, local, dist, device, args.profile_range)
+    total_ms, steps_ms, k1, k2, k3, clocks = (tm["total_ms"], tm["steps_ms"], tm["k1"], tm["k2"],
+                                              tm["k3"], tm["clocks"])
     st = z.scaler_state()
     assert st["overflow"] == 0 and st["steps"] == K + W, st
     # the speculative step commits on the fast path unless clipping is active
     fast_path = st["fast_path"] if args.speculative else None
-
-    steps_ms = sorted(ev[k][0].elapsed_time(ev[k][3]) for k in range(K))
-    k1 = [ev[k][0].elapsed_time(ev[k][1]) for k in range(K)]
-    k2 = [ev[k][1].elapsed_time(ev[k][2]) for k in range(K)]
-    k3 = [ev[k][2].elapsed_time(ev[k][3]) for k in range(K)]
 
     # The same step captured once into a CUDA graph and replayed K times.
     graph = None
@@ -621,9 +646,10 @@ def run_ours(args) -> dict | None:
                    "k_adamw_cast_gbs": k3_bytes / (k3_ms / 1e3) / 1e9}
     achieved = dom[1] / (dom[2] / 1e3) / 1e9
     tr = NCU_TRAFFIC_PER_ELEM.get(dom[0])
-    step_gbs = info.step_bytes_per_elem * N / step_s / 1e9
-    impl_bytes = info.step_bytes_per_elem if args.speculative else \
-        info.step_bytes_per_elem + (w.world * C if w.stage == 1 else C) + C
+    sb = stage_bytes(w)
+    # the stage's own bytes: the ledger, plus the all-reduce writes in stage 1
+    step_gbs = sb["own"] * N / step_s / 1e9
+    impl_bytes = sb["own"] if args.speculative else sb["impl"]
     out = {
         "metric": METRIC,
         "value": job_value(N, world, step_s),
@@ -646,12 +672,12 @@ def run_ours(args) -> dict | None:
                                                    "two-pass host entry point"
                                                    if args.speculative else None))),
         "hbm_gbs_step": step_gbs,
-        "step_roofline": {"bytes_per_param": info.step_bytes_per_elem, "peak_gbs": peak,
-                          "frac": step_gbs / peak, "peak_source": peak_src,
-                          # bytes the kernels must move per param: the ledger, plus
+        "step_roofline": {"bytes_per_param": sb["own"], "ledger_bytes_per_param": sb["ledger"],
+                          "peak_gbs": peak, "frac": step_gbs / peak, "peak_source": peak_src,
+                          # bytes the kernels must move per param: the stage's own, plus
                           # (two-pass) the reduced gradient written and read back
                           "impl_bytes_per_param": impl_bytes,
-                          "impl_ceiling": info.step_bytes_per_elem / impl_bytes},
+                          "impl_ceiling": sb["own"] / impl_bytes},
         "roofline": {"bound": "hbm", "kernel": dom[0], "achieved": achieved, "peak": peak,
                      "unit": "GB/s", "frac": achieved / peak,
                      "traffic": (tr * N if tr is not None else None),
@@ -675,6 +701,230 @@ def run_ours(args) -> dict | None:
     if dist is not None:
         dist.destroy_process_group()
     return out if rank == 0 else None
+
+
+# The other named workloads the step is quoted on, timed after the default
+# line in the same run: the ~3.9B MoE list (W=4, ZeRO-2) and the Qwen3 list
+# with fp16 dynamic scaling at W=8, ZeRO-1 against ZeRO-2.
+PER_CONFIG = [
+    ("moe_3.9b_bf16_w4", {"stage": 2}),
+    ("qwen3_0.6b_fp16_w8", {"stage": 1}),
+    ("qwen3_0.6b_fp16_w8", {"stage": 2}),
+]
+
+
+def stage_bytes(w) -> dict:
+    """Bytes per real element of one step of workload w.
+
+    ledger: the step's byte roofline, W*G gradient reads + 24 B of fp32
+    master/m/v read and written + P B of parameter writes. own: what the
+    stage itself must move -- stage 1 also writes the all-reduce result into
+    all W outputs (W*C more). impl: what the two-pass kernels move -- the
+    reduced gradient is stored (C, or W*C in stage 1) and read back (C).
+    """
+    import workloads as wl
+    G, C, P = (wl.ELEM_BYTES[w.grad_dtype], wl.ELEM_BYTES[w.comm_dtype],
+               wl.ELEM_BYTES[w.param_dtype])
+    ledger = w.world * G + 24 + P
+    own = ledger + (w.world * C if w.stage == 1 else 0)
+    impl = ledger + (w.world * C if w.stage == 1 else C) + C
+    return {"ledger": ledger, "own": own, "impl": impl,
+            "k1": w.world * G + (w.world * C if w.stage == 1 else C), "k3": C + 24 + P}
+
+
+def time_config(name: str, over: dict, steps: int, warmup: int, local: int) -> dict:
+    """One named workload through zero_step: its own buffers, seeded inputs,
+    warm-up, K timed steps with per-kernel events and sampled clocks. Frees
+    every buffer before it returns."""
+    import torch
+
+    import workloads as wl
+    from mixed_precision_gb300.engine import Hparams, ZeroStep
+
+    device = torch.device("cuda", local)
+    w = wl.workload(name, **over)
+    z = ZeroStep(w.shapes, w.world, w.stage, w.bucket_bytes, w.grad_dtype, w.param_dtype,
+                 w.comm_dtype)
+    z.allocate()
+    numel = wl.numels(w.shapes)
+    master0 = wl.master_init(z.offsets, numel, z.np, w.master_sigma, wl.master_seed(w.index),
+                             device=device)
+    z.init(master0, init_scale=w.init_scale, dynamic=w.dynamic, growth_interval=w.growth_interval)
+    torch.cuda.synchronize()
+    del master0
+    grads = [wl.flat_grads(z.offsets, numel, z.np, w.grad_sigma, wl.grad_seed(w.index, r),
+                           w.grad_dtype, device=device, zero_params=wl.zero_params(w, r))
+             for r in range(w.world)]
+    hp = Hparams(lr=w.lr, beta1=w.beta1, beta2=w.beta2, eps=w.eps, weight_decay=w.weight_decay,
+                 max_grad_norm=w.max_grad_norm)
+    tm = timed_steps(z, lambda: z.step(grads, hp), steps, warmup, local)
+    st = z.scaler_state()
+    assert st["overflow"] == 0 and st["steps"] == steps + warmup, st
+    N = w.n_real
+    peak, peak_src = hbm_peak()
+    b = stage_bytes(w)
+    step_s = tm["total_ms"] / 1e3 / steps
+    k1_ms, k3_ms = statistics.mean(tm["k1"]), statistics.mean(tm["k3"])
+    out = {
+        "config": config_of(w),
+        "steps": steps, "warmup": warmup,
+        "ms_per_step": tm["total_ms"] / steps,
+        "step_ms_median": tm["steps_ms"][steps // 2],
+        "value": N / step_s, "unit": "params/s",
+        "step_roofline": {"bytes_per_param": b["own"], "ledger_bytes_per_param": b["ledger"],
+                          "hbm_gbs": b["own"] * N / step_s / 1e9, "peak_gbs": peak,
+                          "frac": b["own"] * N / step_s / 1e9 / peak, "peak_source": peak_src,
+                          "impl_bytes_per_param": b["impl"],
+                          "impl_ceiling": b["own"] / b["impl"]},
+        "kernels_ms": {"k_reduce_norm": k1_ms, "k_finalize": statistics.mean(tm["k2"]),
+                       "k_adamw_cast": k3_ms,
+                       "k_reduce_norm_gbs": b["k1"] * N / (k1_ms / 1e3) / 1e9,
+                       "k_adamw_cast_gbs": b["k3"] * N / (k3_ms / 1e3) / 1e9},
+        "clip_coef_last": st["clip_coef"],
+        "scale": st["scale"],
+        "clocks": tm["clocks"],
+    }
+    z.close()
+    del grads, z
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return out
+
+
+def per_config(steps: int, warmup: int, local: int) -> dict:
+    """Every workload of PER_CONFIG, one after the other."""
+    out = {}
+    for name, over in PER_CONFIG:
+        key = name + "".join(f"_{k}{v}" for k, v in over.items())
+        out[key] = time_config(name, over, steps, warmup, local)
+    return out
+
+
+def run_sharded(args) -> dict | None:
+    """The sharded step across N GPUs (one process each): the workload's
+    parameter list with W = N, each rank's own seeded gradients, timed over
+    the whole step (collectives included) with CUDA events on the launching
+    stream, max over ranks. The model is fixed, so its shards shrink as N
+    grows: strong scaling."""
+    import socket
+
+    import torch
+    import torch.distributed as tdist
+
+    import workloads as wl
+    from mixed_precision_gb300.engine import Hparams
+    from mixed_precision_gb300.sharded import ShardedZeroStep
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if not tdist.is_initialized():
+        if "MASTER_PORT" not in os.environ:  # a single process without torchrun
+            with socket.socket() as s:
+                s.bind(("127.0.0.1", 0))
+                os.environ["MASTER_PORT"] = str(s.getsockname()[1])
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        tdist.init_process_group("nccl", rank=rank, world_size=world, device_id=device)
+    w = dataclasses_replace(workload_of(args), world=world)
+    if w.stage == 1:
+        raise SystemExit("--sharded times stages 2 and 3 (stage 1 all-reduces the gradients in place)")
+    K, Wm = args.steps, args.warmup
+    if Wm < 3:
+        raise SystemExit("--warmup must be at least 3")
+    z = ShardedZeroStep(w.shapes, w.stage, w.bucket_bytes, w.grad_dtype, w.param_dtype,
+                        device=device)
+    numel = wl.numels(w.shapes)
+    master0 = wl.master_init(z.offsets, numel, z.np, w.master_sigma, wl.master_seed(w.index),
+                             device=device)
+    z.init(master0, init_scale=w.init_scale, dynamic=w.dynamic, growth_interval=w.growth_interval)
+    del master0
+    grads = wl.flat_grads(z.offsets, numel, z.np, w.grad_sigma, wl.grad_seed(w.index, rank),
+                          w.grad_dtype, device=device, zero_params=wl.zero_params(w, rank))
+    hp = Hparams(lr=w.lr, beta1=w.beta1, beta2=w.beta2, eps=w.eps, weight_decay=w.weight_decay,
+                 max_grad_norm=w.max_grad_norm)
+    for _ in range(Wm):
+        z.step(grads, hp)
+    torch.cuda.synchronize()
+    barrier(tdist if world > 1 else None, device)
+    sampler = ClockSampler(local).start()
+    time.sleep(0.3)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    t0.record()
+    for _ in range(K):
+        z.step(grads, hp)
+    t1.record()
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    dist = tdist if world > 1 else None
+    barrier(dist, device)
+    total_ms = max_over_ranks(dist, t0.elapsed_time(t1), device)
+    st = z.scaler_state()
+    assert st["overflow"] == 0 and st["steps"] == K + Wm, st
+
+    # this rank's update kernel alone (the dominant local kernel)
+    u0, u1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    u0.record()
+    for _ in range(10):
+        z.local.update(None)
+    u1.record()
+    torch.cuda.synchronize()
+    upd_ms = u0.elapsed_time(u1) / 10
+    # end to end: each step's gradients copied in from pinned host memory, the
+    # scaler state read back after the loop
+    from mixed_precision_gb300 import _abi as abi
+    host = grads.cpu().pin_memory()
+    E = max(1, min(args.e2e_steps, 10))
+    blobs = torch.zeros((E, abi.ZERO_STATE_BLOB_BYTES), dtype=torch.uint8).pin_memory()
+    stream = torch.cuda.current_stream().cuda_stream
+    torch.cuda.synchronize()
+    barrier(dist, device)
+    e0 = time.perf_counter()
+    for k in range(E):
+        grads.copy_(host, non_blocking=True)
+        z.step(grads, hp)
+        abi.zero_loss_scale_state_async(z.handle, blobs[k].data_ptr(), stream)
+    torch.cuda.synchronize()
+    e2e_s = max_over_ranks(dist, time.perf_counter() - e0, device)
+    assert all(abi.zero_state_blob_decode(blobs[k].data_ptr()).overflow == 0 for k in range(E))
+
+    N = w.n_real
+    G, C, P = (wl.ELEM_BYTES[w.grad_dtype], wl.ELEM_BYTES[w.comm_dtype],
+               wl.ELEM_BYTES[w.param_dtype])
+    peak, peak_src = hbm_peak()
+    upd_bytes = (C + 24 + P) * z.info.n_real / world
+    achieved = upd_bytes / (upd_ms / 1e3) / 1e9
+    step_s = total_ms / 1e3 / K
+    out = {
+        "metric": METRIC, "value": N / step_s, "unit": "params/s", "n_gpus": world, "steps": K,
+        "warmup": Wm, "ms_per_step": total_ms / K, "higher_is_better": True, "scaling": "strong",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": dict(config_of(w), parallelism=f"zero{w.stage}_dp{world}",
+                       note="one rank per GPU: per-bucket reduce-scatter, 16-byte norm "
+                            "all-reduce and per-bucket all-gather (NCCL) around the local "
+                            "kernels"),
+        "roofline": {"bound": "hbm", "kernel": "k_adamw_cast (this rank's shard)",
+                     "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": None, "algorithmic_bytes_per_launch": upd_bytes,
+                     "peak_source": peak_src},
+        "e2e": {"value": N / (e2e_s / E), "unit": "params/s",
+                "h2d_bytes_per_step": z.np * G, "d2h_bytes_per_step": int(z.info.state_blob_used),
+                "note": "per rank: its gradients copied in from pinned host memory each step, "
+                        "the step's scaler state read back asynchronously"},
+        # per step: the shard norm, the finalize and the update (the collectives
+        # are NCCL's kernels)
+        "gpu_launches": K * 3,
+        "clocks": clocks,
+    }
+    z.close()
+    if world > 1:
+        tdist.destroy_process_group()
+    return out if rank == 0 else None
+
+
+def dataclasses_replace(w, **kw):
+    import dataclasses
+    return dataclasses.replace(w, **kw)
 
 
 # ---------------------------------------------------------------------------
@@ -716,9 +966,13 @@ def main(argv=None):
     args = parse_args(argv)
     if args.impl == "reference":
         out = run_reference(args)
+    elif args.sharded:
+        out = run_sharded(args)
     else:
         out = run_ours(args)
-        rank, world, _ = dist_env()
+        rank, world, local = dist_env()
+        if out is not None and world == 1 and args.per_config_steps > 0:
+            out["per_config"] = per_config(args.per_config_steps, max(3, args.warmup), local)
         if out is not None and world == 1 and not args.no_cpu_baseline:
             import workloads as wl
             out["cpu_baseline"] = cpu_baseline(workload_of(args), args.cpu_seconds)

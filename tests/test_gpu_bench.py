@@ -14,7 +14,8 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 def test_our_line_keys():
     res = subprocess.run([sys.executable, "bench.py", "--steps", "5", "--warmup", "3",
-                          "--e2e-steps", "2", "--cpu-seconds", "1"], cwd=ROOT,
+                          "--e2e-steps", "2", "--cpu-seconds", "1", "--per-config-steps", "3"],
+                         cwd=ROOT,
                          capture_output=True, text=True, timeout=900)
     assert res.returncode == 0, res.stderr[-2000:]
     lines = [l for l in res.stdout.strip().splitlines() if l.startswith("{")]
@@ -37,3 +38,14 @@ def test_our_line_keys():
     assert d["e2e"]["h2d_bytes_per_step"] > 0 and d["e2e"]["d2h_bytes_per_step"] > 0
     for k in ("sm_mhz", "sm_max_mhz", "reasons"):
         assert k in d["clocks"], k
+    # the other named workloads, each with its own bytes per step
+    pc = d["per_config"]
+    assert set(pc) == {"moe_3.9b_bf16_w4_stage2", "qwen3_0.6b_fp16_w8_stage1",
+                       "qwen3_0.6b_fp16_w8_stage2"}
+    for name, c in pc.items():
+        assert c["steps"] == 3 and c["ms_per_step"] > 0 and 0 < c["step_roofline"]["frac"] < 1.5
+        assert c["config"]["workload"] == name.rsplit("_stage", 1)[0]
+        for k in ("sm_mhz", "sm_max_mhz", "reasons"):
+            assert k in c["clocks"], k
+    s1 = pc["qwen3_0.6b_fp16_w8_stage1"]["step_roofline"]
+    assert s1["bytes_per_param"] == s1["ledger_bytes_per_param"] + 8 * 2  # the W*C all-reduce writes

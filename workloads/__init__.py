@@ -132,6 +132,12 @@ def workload(name: str, **over) -> Workload:
         # 2.5 GB on the device; a profiling-sized case of the same kernels.
         w = Workload(name, qwen3_0_6b_shapes(layers=8)[1:-1], 2, 2, BF16, BF16, BF16, 500 * MB,
                      1e-4, index=6)
+    elif name == "moe_layers2_bf16_w4":
+        # 2 layers of the MoE list (attention, router, 16 experts each), no
+        # embedding or head: 235M elements, about 5.6 GB on the device; a
+        # profiling-sized case of the same kernels with the same expert mix.
+        w = Workload(name, moe_3_9b_shapes(layers=2)[0][1:-1], 4, 2, BF16, BF16, BF16, 500 * MB,
+                     1e-4, index=7)
     elif name == "moe_3.9b_bf16_w4":
         w = Workload(name, moe_3_9b_shapes()[0], 4, 2, BF16, BF16, BF16, 500 * MB, 1e-4, index=4)
     elif name == "ragged_2000":
@@ -219,6 +225,9 @@ def zero_params(w: Workload, rank: int):
     workload, the experts that rank's tokens did not route to (14 of 16 per
     layer); none otherwise."""
     if w.name.startswith("moe_"):
-        _, tags = moe_3_9b_shapes()
+        layers = 2 if w.name == "moe_layers2_bf16_w4" else 32
+        _, tags = moe_3_9b_shapes(layers=layers)
+        if layers == 2:
+            tags = tags[1:-1]
         return moe_zero_experts(tags, rank, grad_seed(w.index, 0))
     return []
