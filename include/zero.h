@@ -418,13 +418,16 @@ int zero_set_step_events(zero_layout_t* layout, void* const* events);
  *   norm_sq_out   device double; overflow_out: device int32.
  * Scratch: a fixed array inside the library (about 768 KB on every GPU that
  * loads it, held until the process exits) for one partial per 65,536
- * elements; n above 2^32 is rejected with ZERO_ERR_INVALID. The first call
- * made with a device current looks up that array's device address for the
- * device (cudaGetSymbolAddress); make that first call before any stream
- * capture. Every call shares the one array: calls whose work overlaps on the
- * GPU (different streams, no ordering between them) race and give wrong
- * results. Allocates nothing: no cudaMalloc, cudaFree or allocating library
- * call. Enqueued on `stream`. */
+ * elements; n above 2^32 is rejected with ZERO_ERR_INVALID. Each CUDA
+ * context holds its own copy of the array, so the first call made in each
+ * context looks up that copy's device address (cudaGetSymbolAddress) and
+ * caches it under the context's unique ID: the device's primary context, a
+ * context the caller made current through the driver API, and the new
+ * primary context after cudaDeviceReset are looked up separately. Make the
+ * first call in each context before any stream capture. Every call shares
+ * the one array: calls whose work overlaps on the GPU (different streams, no
+ * ordering between them) race and give wrong results. Allocates nothing: no
+ * cudaMalloc, cudaFree or allocating library call. Enqueued on `stream`. */
 int zero_reduce_norm_noalloc(const void* const* grads, int world, int64_t n, int grad_dtype,
                              int comm_dtype, void* reduced_out, double* norm_sq_out,
                              int32_t* overflow_out, void* stream);
@@ -488,6 +491,59 @@ int zero_state_import_params(zero_layout_t* layout, const float* master_pm, cons
  * saved zero_scaler_state); the other fields of `st` are ignored. Enqueued
  * on `stream`. */
 int zero_scaler_restore(zero_layout_t* layout, const zero_scaler_state* st, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Sharded step: one process per GPU ([DO] "Distributed optimizer: trade      */
+/* replicated state for collectives": reduce-scatter of each bucket, local   */
+/* FP32 update of the rank's master slice and moments, all-gather of the     */
+/* parameters). The caller's communication library (NCCL, through its own    */
+/* bindings) runs the collectives between these calls; the library computes  */
+/* everything between them. The layout's world is the number of GPUs.        */
+/* ------------------------------------------------------------------------ */
+
+/* Make this layout rank `rank`'s (0..W-1) of a W-GPU job. Call after
+ * zero_layout_create and before zero_state_bind; the layout then holds only
+ * this rank's shard, and the buffers bound later are:
+ *   master, m, v, scratch  Np/W elements: this rank's slice of bucket 0, then
+ *                          bucket 1, ... (bucket b's slice starts at
+ *                          shard_offset - rank*Np/W of zero_shard_range);
+ *   params_flat            stages 1/2: Np elements, flat layout (the step
+ *                          writes this rank's slices; the caller's all-gather
+ *                          of each bucket fills the rest); stage 3: Np/W
+ *                          elements, this rank's slices.
+ * zero_state_init then initialises this rank's slices only (master_init_flat
+ * is still the whole flat buffer): all-gather the parameters once after it.
+ * Requires comm_dtype == grad_dtype (the collectives reduce in the gradient
+ * dtype). ZERO_ERR_STATE if called twice or after bind; every entry point
+ * that steps all W ranks in one process (zero_step*, accumulation, gathers,
+ * exports, imports) then returns ZERO_ERR_STATE. Host only. */
+int zero_dist_set_rank(zero_layout_t* layout, int rank);
+
+/* This rank's share of the global norm and overflow check: enqueues a kernel
+ * that writes norm_pair[0] = sum of r^2 over this rank's real elements (fp64
+ * partials, a fixed order for a given device) and norm_pair[1] = 1.0 if any
+ * of them is non-finite, else 0.0. The caller then sums the pair over ranks
+ * (one 16-byte all-reduce) and passes the result to zero_dist_finalize.
+ *   allreduced  stages 2/3: NULL (the bound scratch holds this rank's
+ *               reduce-scatter output); stage 1: device, Np elements of
+ *               comm_dtype, flat layout, this rank's all-reduced gradient.
+ *   norm_pair   device, 2 doubles, 8-byte aligned. */
+int zero_dist_shard_norm(zero_layout_t* layout, const void* allreduced, double* norm_pair,
+                         void* stream);
+
+/* The finalize from the all-reduced pair (device, 2 doubles: global sum of
+ * squares, > 0 when any rank overflowed): norm, clip coefficient, loss-scale
+ * state machine and t, exactly as zero_step's finalize with world W. Every
+ * rank gets the same pair, so every rank takes the same decision. */
+int zero_dist_finalize(zero_layout_t* layout, const double* norm_pair, const zero_hparams* hp,
+                       void* stream);
+
+/* Unscale + clip + AdamW on this rank's fp32 slice and cast-out of its
+ * parameters (stages 1/2: into params_flat at flat offsets; stage 3: into
+ * its own slices). Returns at once on the device after an overflow (the step
+ * is skipped). allreduced as for zero_dist_shard_norm. Then the caller
+ * all-gathers each bucket of params_flat (stages 1/2). */
+int zero_dist_update(zero_layout_t* layout, const void* allreduced, void* stream);
 
 /* Message for the last failing call on this thread ("" if none). The pointer
  * stays valid until the next failing call on this thread. */

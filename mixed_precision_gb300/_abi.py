@@ -116,6 +116,10 @@ def lib() -> ctypes.CDLL:
             "zero_gather_bucket": [P, I, P, P],
             "zero_loss_scale_state_async": [P, P, P],
             "zero_state_blob_decode": [P, ctypes.POINTER(zero_scaler_state)],
+            "zero_dist_set_rank": [P, I],
+            "zero_dist_shard_norm": [P, P, P, P],
+            "zero_dist_finalize": [P, P, ctypes.POINTER(zero_hparams), P],
+            "zero_dist_update": [P, P, P],
         }
         for name, args in sig.items():
             fn = getattr(L, name)
@@ -303,3 +307,19 @@ def zero_state_blob_decode(blob: int) -> zero_scaler_state:
     st = zero_scaler_state()
     _check(lib().zero_state_blob_decode(blob, ctypes.byref(st)))
     return st
+
+
+def zero_dist_set_rank(layout: int, rank: int) -> None:
+    _check(lib().zero_dist_set_rank(layout, rank))
+
+
+def zero_dist_shard_norm(layout: int, allreduced: int, norm_pair: int, stream: int) -> None:
+    _check(lib().zero_dist_shard_norm(layout, allreduced or None, norm_pair, stream or None))
+
+
+def zero_dist_finalize(layout: int, norm_pair: int, hp: zero_hparams, stream: int) -> None:
+    _check(lib().zero_dist_finalize(layout, norm_pair, ctypes.byref(hp), stream or None))
+
+
+def zero_dist_update(layout: int, allreduced: int, stream: int) -> None:
+    _check(lib().zero_dist_update(layout, allreduced or None, stream or None))

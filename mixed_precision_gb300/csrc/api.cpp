@@ -140,6 +140,10 @@ struct zero_layout {
   // register-staged kernels, kept as the comparison baseline (environment
   // ZERO_REDUCE_VARIANT / ZERO_UPDATE_VARIANT = 0 at bind selects them)
   int reduce_variant = 1, update_variant = 1;
+  // the pipelined update's tile schedule: 1 (default) = a device counter
+  // hands out tiles to a grid of the resident blocks; 0 = block b takes tiles
+  // b, b + grid, ... (environment ZERO_UPDATE_SCHED=static at bind)
+  int update_sched = 1;
   cudaEvent_t events[4] = {nullptr, nullptr, nullptr, nullptr};
   bool timing = false;
 
@@ -166,8 +170,17 @@ struct zero_layout {
   cudaEvent_t k1_done = nullptr;  // set only while zero_step_host runs its step: recorded after K1
   bool k1_recorded = false;
 
+  // Sharded mode (zero_dist_set_rank): this process holds rank `local_rank`'s
+  // shard only; -1 = every simulated rank in this process (the default).
+  int local_rank = -1;
+  int sms = 0;
+
   int world() const { return cfg.world; }
   int n_params() const { return (int)numel.size(); }
+  bool sharded() const { return local_rank >= 0; }
+  // elements of the bound master/m/v (and scratch) buffers, and of params
+  int64_t state_elems() const { return sharded() ? np / cfg.world : np; }
+  int64_t param_elems() const { return sharded() && cfg.stage == 3 ? np / cfg.world : np; }
 };
 
 namespace {
@@ -360,6 +373,7 @@ int launch_step(zero_layout* L, const GradSrc& src, void* const* allreduce_out,
     ua.params_flat = L->params;
     ua.state = L->d_state;
     ua.error = &L->d_state->error;
+    ua.tile_next = L->update_sched ? &L->d_state->tiles_next : nullptr;
     Range r("K3 unscale+clip+AdamW+cast");
     e = launch_update(ua, guarded ? L->grid_update_guarded : L->grid_update, L->update_variant, s);
     if (e != cudaSuccess) return cuda_fail(e, "update kernel launch");
@@ -464,6 +478,7 @@ int launch_step_per_tensor(zero_layout* L, const GradSrc& src, void* const* allr
   ua.params_flat = L->params;
   ua.state = L->d_state;
   ua.error = &L->d_state->error;
+  ua.tile_next = L->update_sched ? &L->d_state->tiles_next : nullptr;
   for (int p = 0; p < P; ++p) {
     const int n = L->pt_begin[p + 1] - L->pt_begin[p];
     if (n == 0) continue;
@@ -473,6 +488,15 @@ int launch_step_per_tensor(zero_layout* L, const GradSrc& src, void* const* allr
     if (e != cudaSuccess) return cuda_fail(e, "update kernel launch");
   }
   if (L->timing) ZERO_CUDA(cudaEventRecord(L->events[3], s));
+  return ZERO_OK;
+}
+
+// Entry points that step or copy every simulated rank's data in one process
+// have no meaning for a layout that holds one rank's shard.
+int check_not_sharded(const zero_layout* L, const char* what) {
+  if (L->sharded())
+    return fail(ZERO_ERR_STATE, "%s runs every rank in one process; this layout holds rank %d's "
+                "shard only (zero_dist_set_rank): use the zero_dist_* calls", what, L->local_rank);
   return ZERO_OK;
 }
 
@@ -751,6 +775,7 @@ static int state_bind(zero_layout_t* L, void* master, void* m, void* v, void* pa
     ZERO_CUDA(cudaGetDevice(&dev));
     ZERO_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
     L->device = dev;
+    L->sms = sms;
     const int n_tiles = (int)L->tiles.size();
     if (const char* v = std::getenv("ZERO_REDUCE_VARIANT")) L->reduce_variant = std::atoi(v) == 0 ? 0 : 1;
     if (const char* v = std::getenv("ZERO_UPDATE_VARIANT")) L->update_variant = std::atoi(v) == 0 ? 0 : 1;
@@ -777,15 +802,29 @@ static int state_bind(zero_layout_t* L, void* master, void* m, void* v, void* pa
       return fail(ZERO_ERR_CUDA, "kernel occupancy query failed (no sm_103a image for this GPU?)");
     L->grid_reduce =
         std::max(1, std::min({n_tiles, sms * bps_r * grid_mult("ZERO_REDUCE_GRID_MULT", kReduceGridMult), kMaxPartials}));
-    // The update: one block per tile unless ZERO_UPDATE_GRID_MULT asks for a
-    // multiple of the resident blocks.
-    L->grid_update = std::getenv("ZERO_UPDATE_GRID_MULT") == nullptr
-                         ? std::max(1, n_tiles)
-                         : std::max(1, std::min(n_tiles, sms * bps_u * grid_mult("ZERO_UPDATE_GRID_MULT", 1)));
-    L->grid_copy = std::max(1, std::min(n_tiles, sms * 4 * grid_mult("ZERO_COPY_GRID_MULT", kCopyGridMult)));
+    // The update: with the device tile counter (the default), a grid of the
+    // resident blocks times ZERO_UPDATE_GRID_MULT (default 1), the guarded
+    // update of the speculative step included; with the static schedule
+    // (ZERO_UPDATE_SCHED=static, register-staged variant too), one block per
+    // tile unless ZERO_UPDATE_GRID_MULT asks for a multiple of the resident
+    // blocks, and the guarded update at ZERO_GUARDED_GRID_MULT.
+    if (const char* v = std::getenv("ZERO_UPDATE_SCHED")) L->update_sched = std::strcmp(v, "static") != 0;
+    if (L->update_variant == 0) L->update_sched = 0;
     const int gm = grid_mult("ZERO_GUARDED_GRID_MULT", kGuardedGridMult);
-    L->grid_update_guarded = std::max(1, std::min(n_tiles, sms * bps_u * gm));
-    L->grid_copy_guarded = std::max(1, std::min(n_tiles, sms * 4 * gm));
+    if (L->update_sched) {
+      L->grid_update = std::max(1, std::min(n_tiles, sms * bps_u * grid_mult("ZERO_UPDATE_GRID_MULT", 1)));
+      L->grid_update_guarded = L->grid_update;
+    } else {
+      L->grid_update = std::getenv("ZERO_UPDATE_GRID_MULT") == nullptr
+                           ? std::max(1, n_tiles)
+                           : std::max(1, std::min(n_tiles, sms * bps_u * grid_mult("ZERO_UPDATE_GRID_MULT", 1)));
+      L->grid_update_guarded = std::max(1, std::min(n_tiles, sms * bps_u * gm));
+    }
+    L->grid_copy = std::max(1, std::min(n_tiles, sms * 4 * grid_mult("ZERO_COPY_GRID_MULT", kCopyGridMult)));
+    // the guarded parameter restore is a no-op on every step that did not
+    // overflow: one wave of resident blocks unless ZERO_GUARDED_GRID_MULT asks
+    L->grid_copy_guarded = std::max(
+        1, std::min(n_tiles, std::getenv("ZERO_GUARDED_GRID_MULT") ? sms * 4 * gm : sms * kMaxBlocksPerSm));
   }
   L->master = static_cast<float*>(master);
   L->m = static_cast<float*>(m);
@@ -806,6 +845,7 @@ int zero_state_bind(zero_layout_t* L, void* master, void* m, void* v, void* para
 
 int zero_state_bind_alternate(zero_layout_t* L, void* master2, void* m2, void* v2) {
   if (int rc = check_ready(L, false)) return rc;
+  if (int rc = check_not_sharded(L, "zero_state_bind_alternate")) return rc;
   if (L->cfg.stage == 1) return fail(ZERO_ERR_INVALID, "the speculative step needs stage 2 or 3");
   if (master2 == nullptr || m2 == nullptr || v2 == nullptr)
     return fail(ZERO_ERR_INVALID, "master2/m2/v2 must not be NULL");
@@ -849,11 +889,12 @@ int zero_state_init(zero_layout_t* L, const float* master_init_flat, const zero_
       !(cfg->backoff_factor > 0.0 && cfg->backoff_factor <= 1.0) || !(cfg->min_scale > 0.0))
     return fail(ZERO_ERR_INVALID, "scaler config out of range");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const size_t nbytes = (size_t)L->np * 4;
+  const size_t nbytes = (size_t)L->state_elems() * 4;
   ZERO_CUDA(cudaMemsetAsync(L->master, 0, nbytes, s));
   ZERO_CUDA(cudaMemsetAsync(L->m, 0, nbytes, s));
   ZERO_CUDA(cudaMemsetAsync(L->v, 0, nbytes, s));
-  ZERO_CUDA(cudaMemsetAsync(L->params, 0, (size_t)L->np * dtype_bytes(L->cfg.param_dtype), s));
+  ZERO_CUDA(cudaMemsetAsync(L->params, 0,
+                            (size_t)L->param_elems() * dtype_bytes(L->cfg.param_dtype), s));
   ScalerCfg sc{cfg->init_scale, cfg->dynamic ? 1 : 0, cfg->growth_interval, cfg->growth_factor,
                cfg->backoff_factor, cfg->min_scale};
   cudaError_t e = launch_state_init(sc, L->d_state, s);
@@ -871,6 +912,7 @@ int zero_step(zero_layout_t* L, const void* const* grads, void* const* allreduce
               const zero_hparams* hp, void* stream) {
   Range r_entry("zero_step");
   if (int rc = check_ready(L, true)) return rc;
+  if (int rc = check_not_sharded(L, "zero_step")) return rc;
   if (int rc = check_hparams(hp)) return rc;
   if (int rc = check_allreduce(L, allreduce_out)) return rc;
   if (grads == nullptr) return fail(ZERO_ERR_INVALID, "grads is NULL");
@@ -886,6 +928,7 @@ int zero_step(zero_layout_t* L, const void* const* grads, void* const* allreduce
 int zero_step_speculative(zero_layout_t* L, const void* const* grads, const zero_hparams* hp,
                           void* stream) {
   if (int rc = check_ready(L, true)) return rc;
+  if (int rc = check_not_sharded(L, "zero_step_speculative")) return rc;
   if (int rc = check_hparams(hp)) return rc;
   if (L->master2 == nullptr) return fail(ZERO_ERR_STATE, "zero_state_bind_alternate has not been called");
   if (grads == nullptr) return fail(ZERO_ERR_INVALID, "grads is NULL");
@@ -902,6 +945,7 @@ int zero_step_speculative_tensors(zero_layout_t* L, const void* const* grad_ptrs
                                   const zero_hparams* hp, void* stream) {
   Range r_entry("zero_step_speculative_tensors");
   if (int rc = check_ready(L, true)) return rc;
+  if (int rc = check_not_sharded(L, "zero_step_speculative_tensors")) return rc;
   if (int rc = check_hparams(hp)) return rc;
   if (L->master2 == nullptr) return fail(ZERO_ERR_STATE, "zero_state_bind_alternate has not been called");
   if (grad_ptrs == nullptr) return fail(ZERO_ERR_INVALID, "grad_ptrs is NULL");
@@ -925,6 +969,7 @@ int zero_step_per_tensor_launch(zero_layout_t* L, const void* const* grads,
                                 void* const* allreduce_out, const zero_hparams* hp, void* stream) {
   Range r_entry("zero_step_per_tensor_launch");
   if (int rc = check_ready(L, true)) return rc;
+  if (int rc = check_not_sharded(L, "zero_step_per_tensor_launch")) return rc;
   if (int rc = check_hparams(hp)) return rc;
   if (int rc = check_allreduce(L, allreduce_out)) return rc;
   if (grads == nullptr) return fail(ZERO_ERR_INVALID, "grads is NULL");
@@ -941,6 +986,7 @@ int zero_step_tensors(zero_layout_t* L, const void* const* grad_ptrs, void* cons
                       const zero_hparams* hp, void* stream) {
   Range r_entry("zero_step_tensors");
   if (int rc = check_ready(L, true)) return rc;
+  if (int rc = check_not_sharded(L, "zero_step_tensors")) return rc;
   if (int rc = check_hparams(hp)) return rc;
   if (int rc = check_allreduce(L, allreduce_out)) return rc;
   if (grad_ptrs == nullptr) return fail(ZERO_ERR_INVALID, "grad_ptrs is NULL");
@@ -964,6 +1010,7 @@ static int step_host(zero_layout_t* L, const void* const* host_grads, void* cons
                      void* const* allreduce_out, const zero_hparams* hp, void* stream) {
   Range r_entry("zero_step_host");
   if (int rc = check_ready(L, true)) return rc;
+  if (int rc = check_not_sharded(L, "zero_step_host")) return rc;
   if (host_grads == nullptr || dev_grads == nullptr)
     return fail(ZERO_ERR_INVALID, "host_grads/dev_grads is NULL");
   const size_t bytes = (size_t)L->np * dtype_bytes(L->cfg.grad_dtype);
@@ -1046,6 +1093,7 @@ int zero_accumulate(zero_layout_t* L, const void* const* micro, int micro_dtype,
                     int first, void* stream) {
   Range r_entry("zero_accumulate");
   if (int rc = check_ready(L, false)) return rc;
+  if (int rc = check_not_sharded(L, "zero_accumulate")) return rc;
   if (micro == nullptr || main == nullptr) return fail(ZERO_ERR_INVALID, "micro/main is NULL");
   if (!valid_dtype(micro_dtype)) return fail(ZERO_ERR_INVALID, "bad micro_dtype");
   AccArgs a{};
@@ -1108,6 +1156,7 @@ int zero_loss_scale_state(zero_layout_t* L, void* stream, zero_scaler_state* out
 
 int zero_gather_params(zero_layout_t* L, void* const* dst, int n_replicas, void* stream) {
   if (int rc = check_ready(L, true)) return rc;
+  if (int rc = check_not_sharded(L, "zero_gather_params")) return rc;
   if (dst == nullptr || n_replicas < 1) return fail(ZERO_ERR_INVALID, "dst NULL or n_replicas < 1");
   const int64_t n = (int64_t)n_replicas * L->n_params();
   for (int64_t i = 0; i < n; ++i) {
@@ -1138,6 +1187,7 @@ int zero_gather_params(zero_layout_t* L, void* const* dst, int n_replicas, void*
 int zero_gather_bucket(zero_layout_t* L, int bucket, void* dst, void* stream) {
   Range r_entry("zero_gather_bucket");
   if (int rc = check_ready(L, true)) return rc;
+  if (int rc = check_not_sharded(L, "zero_gather_bucket")) return rc;
   if (L->cfg.stage != 3)
     return fail(ZERO_ERR_STATE, "zero_gather_bucket is for stage 3 (parameters sharded)");
   if (bucket < 0 || bucket >= (int)L->bstart.size()) return fail(ZERO_ERR_INVALID, "bucket out of range");
@@ -1191,12 +1241,14 @@ static int state_pm_copy(zero_layout_t* L, float* a, float* b, float* c, int dir
 int zero_state_export_params(zero_layout_t* L, float* master_pm, float* m_pm, float* v_pm,
                              void* stream) {
   if (int rc = check_ready(L, true)) return rc;
+  if (int rc = check_not_sharded(L, "zero_state_export_params")) return rc;
   return state_pm_copy(L, master_pm, m_pm, v_pm, 0, stream);
 }
 
 int zero_state_import_params(zero_layout_t* L, const float* master_pm, const float* m_pm,
                              const float* v_pm, void* stream) {
   if (int rc = check_ready(L, true)) return rc;
+  if (int rc = check_not_sharded(L, "zero_state_import_params")) return rc;
   if (master_pm == nullptr) return fail(ZERO_ERR_INVALID, "master_pm is required");
   if (int rc = state_pm_copy(L, const_cast<float*>(master_pm), const_cast<float*>(m_pm),
                              const_cast<float*>(v_pm), 1, stream))
@@ -1239,14 +1291,142 @@ int zero_selftest_layout_timeout(zero_layout_t* L, uint32_t spin_limit, void* st
 int zero_state_export(zero_layout_t* L, float* master_flat, float* m_flat, float* v_flat,
                       void* stream) {
   if (int rc = check_ready(L, true)) return rc;
+  if (int rc = check_not_sharded(L, "zero_state_export")) return rc;
   return state_copy(L, master_flat, m_flat, v_flat, 0, stream);
 }
 
 int zero_state_import(zero_layout_t* L, const float* master_flat, const float* m_flat,
                       const float* v_flat, void* stream) {
   if (int rc = check_ready(L, true)) return rc;
+  if (int rc = check_not_sharded(L, "zero_state_import")) return rc;
   return state_copy(L, const_cast<float*>(master_flat), const_cast<float*>(m_flat),
                     const_cast<float*>(v_flat), 1, stream);
+}
+
+// ---------------------------------------------------------------------------
+// Sharded mode: one process per GPU, this layout holds one rank's shard.
+// leetllm "Deep dive: Megatron", "Distributed optimizer: trade replicated
+// state for collectives": reduce-scatter of each bucket, local fp32 update of
+// the rank's master slice and moments, all-gather of the parameters. The
+// caller's communication library runs the collectives between these calls.
+// ---------------------------------------------------------------------------
+
+static int dist_set_rank(zero_layout_t* L, int rank) {
+  if (int rc = check_layout(L)) return rc;
+  if (rank < 0 || rank >= L->world())
+    return fail(ZERO_ERR_INVALID, "rank %d outside 0..%d", rank, L->world() - 1);
+  if (L->sharded()) return fail(ZERO_ERR_STATE, "zero_dist_set_rank was already called");
+  if (L->dblock != nullptr) return fail(ZERO_ERR_STATE, "zero_dist_set_rank must come before zero_state_bind");
+  if (L->comm_dtype != L->cfg.grad_dtype)
+    return fail(ZERO_ERR_INVALID, "the sharded step needs comm_dtype == grad_dtype (the "
+                "collectives reduce the gradients in their own dtype)");
+  // This rank's tiles, in the same order, with shard offsets relative to the
+  // start of its own slice of the rank-major buffers.
+  const int64_t base = (int64_t)rank * (L->np / L->world());
+  std::vector<Tile> mine;
+  std::vector<int> begin;
+  for (size_t b = 0; b + 1 < L->bucket_tile_begin.size(); ++b) {
+    begin.push_back((int)mine.size());
+    for (int t = L->bucket_tile_begin[b]; t < L->bucket_tile_begin[b + 1]; ++t) {
+      Tile x = L->tiles[t];
+      if (x.rank != rank) continue;
+      x.shard -= base;
+      mine.push_back(x);
+    }
+  }
+  begin.push_back((int)mine.size());
+  L->tiles.swap(mine);
+  L->bucket_tile_begin.swap(begin);
+  L->tiles_pt = L->tiles;
+  std::stable_sort(L->tiles_pt.begin(), L->tiles_pt.end(),
+                   [](const Tile& a, const Tile& b) { return a.param < b.param; });
+  const int P = L->n_params();
+  L->pt_begin.assign(P + 1, 0);
+  for (const Tile& t : L->tiles_pt) L->pt_begin[t.param + 1] += 1;
+  for (int p = 0; p < P; ++p) L->pt_begin[p + 1] += L->pt_begin[p];
+  L->pt_partials = 0;
+  for (int p = 0; p < P; ++p)
+    L->pt_partials += std::min(L->pt_begin[p + 1] - L->pt_begin[p], kMaxPerTensorGrid);
+  L->local_rank = rank;
+  return ZERO_OK;
+}
+
+int zero_dist_set_rank(zero_layout_t* L, int rank) {
+  return guarded([&] { return dist_set_rank(L, rank); });
+}
+
+static int check_dist(zero_layout_t* L, const void* allreduced) {
+  if (int rc = check_ready(L, true)) return rc;
+  if (!L->sharded()) return fail(ZERO_ERR_STATE, "zero_dist_set_rank has not been called");
+  if (L->cfg.stage == 1) {
+    if (allreduced == nullptr || !aligned16(allreduced))
+      return fail(ZERO_ERR_INVALID, "stage 1 needs the all-reduced gradient (16-byte aligned)");
+  } else if (allreduced != nullptr) {
+    return fail(ZERO_ERR_INVALID, "stages 2/3 read the bound scratch: allreduced must be NULL");
+  }
+  return ZERO_OK;
+}
+
+int zero_dist_shard_norm(zero_layout_t* L, const void* allreduced, double* norm_pair, void* stream) {
+  Range r_entry("zero_dist_shard_norm");
+  if (int rc = check_dist(L, allreduced)) return rc;
+  if (norm_pair == nullptr || (reinterpret_cast<uintptr_t>(norm_pair) & 7u) != 0)
+    return fail(ZERO_ERR_INVALID, "norm_pair is NULL or not 8-byte aligned");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int n_tiles = (int)L->tiles.size();
+  if (n_tiles == 0) {  // this rank owns no real element
+    ZERO_CUDA(cudaMemsetAsync(norm_pair, 0, 2 * sizeof(double), s));
+    return ZERO_OK;
+  }
+  const bool s1 = L->cfg.stage == 1;
+  const int grid = std::max(1, std::min({n_tiles, L->sms * kMaxBlocksPerSm * 2, kMaxPartials}));
+  cudaError_t e = launch_shard_norm(L->d_tiles, n_tiles, s1 ? allreduced : L->scratch, L->comm_dtype,
+                                    s1 ? 1 : 0, L->d_part, L->d_ovf, L->d_state, norm_pair, grid, s);
+  if (e != cudaSuccess) return cuda_fail(e, "shard norm launch");
+  return ZERO_OK;
+}
+
+int zero_dist_finalize(zero_layout_t* L, const double* norm_pair, const zero_hparams* hp,
+                       void* stream) {
+  Range r_entry("zero_dist_finalize");
+  if (int rc = check_ready(L, true)) return rc;
+  if (!L->sharded()) return fail(ZERO_ERR_STATE, "zero_dist_set_rank has not been called");
+  if (int rc = check_hparams(hp)) return rc;
+  if (norm_pair == nullptr || (reinterpret_cast<uintptr_t>(norm_pair) & 7u) != 0)
+    return fail(ZERO_ERR_INVALID, "norm_pair is NULL or not 8-byte aligned");
+  Hparams h{hp->lr, hp->beta1, hp->beta2, hp->eps, hp->weight_decay, hp->max_grad_norm,
+            hp->grad_divisor};
+  cudaError_t e = launch_dist_finalize(norm_pair, L->world(), h, L->d_state,
+                                       static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "finalize launch");
+  return ZERO_OK;
+}
+
+int zero_dist_update(zero_layout_t* L, const void* allreduced, void* stream) {
+  Range r_entry("zero_dist_update");
+  if (int rc = check_dist(L, allreduced)) return rc;
+  const int n_tiles = (int)L->tiles.size();
+  if (n_tiles == 0) return ZERO_OK;
+  UpdateArgs ua{};
+  ua.tiles = L->d_tiles;
+  ua.n_tiles = n_tiles;
+  ua.stage = L->cfg.stage;
+  ua.comm_dtype = L->comm_dtype;
+  ua.param_dtype = L->cfg.param_dtype;
+  if (L->cfg.stage == 1)
+    ua.red.base[L->local_rank] = const_cast<void*>(allreduced);  // read at each tile's flat offset
+  else
+    ua.red.base[0] = L->scratch;
+  state_sets(L, ua.master, ua.m, ua.v);
+  ua.params_flat = L->params;
+  ua.state = L->d_state;
+  ua.error = &L->d_state->error;
+  ua.tile_next = L->update_sched ? &L->d_state->tiles_next : nullptr;
+  Range r("K3 unscale+clip+AdamW+cast (this rank)");
+  cudaError_t e = launch_update(ua, std::min(n_tiles, L->grid_update), L->update_variant,
+                                static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "update kernel launch");
+  return ZERO_OK;
 }
 
 }  // extern "C"

@@ -66,6 +66,7 @@ struct DevState {
                          // written their partial (wraps to 0 after the last one)
   double beta1_pow, beta2_pow;        // beta1^t and beta2^t as running products ...
   double beta1_pow_of, beta2_pow_of;  // ... of these betas (NaN: not valid, use pow)
+  unsigned tiles_next;  // the update kernel's tile counter (0 between launches)
 };
 
 struct Hparams {  // mirror of zero_hparams
@@ -125,6 +126,8 @@ struct UpdateArgs {
   void* params_flat;
   const DevState* state;
   unsigned* error;  // &state->error
+  unsigned* tile_next;  // the pipelined kernel's tile counter (&state->tiles_next), or
+                        // nullptr: block b takes tiles b, b + grid, ...
 };
 
 // Kernel launchers. Each returns the launch's cudaError_t.
@@ -207,6 +210,15 @@ cudaError_t launch_gather_bucket(const Tile* tiles, int n_tiles, const void* sha
                                  int grid, cudaStream_t s);
 cudaError_t launch_scaler_restore(DevState* st, double scale, long long counter, long long t,
                                   cudaStream_t s);
+// The sharded step's local kernels (k_dist.cu): the sum of squares and
+// non-finite flag of this rank's reduced values as the pair {sum, 1.0 | 0.0}
+// (by_flat: read red at each tile's flat offset, else at its shard offset),
+// and the finalize from that pair summed over ranks.
+cudaError_t launch_shard_norm(const Tile* tiles, int n_tiles, const void* red, int comm_dtype,
+                              int by_flat, double* part, unsigned* part_ovf, DevState* st,
+                              double* pair, int grid, cudaStream_t s);
+cudaError_t launch_dist_finalize(const double* pair, int world, const Hparams& hp, DevState* st,
+                                 cudaStream_t s);
 cudaError_t launch_gather(const Tile* tiles, int n_tiles, const void* params_flat,
                           void* const* dst_table, int n_params, int n_replicas, int elem_bytes,
                           int src_by_shard, int grid, cudaStream_t s);

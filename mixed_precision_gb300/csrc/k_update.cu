@@ -189,15 +189,37 @@ struct UpdStage {
 // mbarrier. One thread moving them in four bulk requests replaces seven
 // 16-byte loads per thread, which kept the load/store queues full; a chunk's
 // last (len mod 8) elements are not bulk-copied (16-byte rule) and come from
-// global memory directly. One producer warp (its lane 0) issues the
-// bulk copies of each chunk into the next free stage; NC consumer warps each
-// update a fixed slice of every chunk and release the stage by arriving on
-// its "empty" mbarrier. No block-wide barrier in the loop: consumer warps
-// never wait for one another, only for data. Bounded, warp-uniform waits: a
-// consumer warp that times out records kErrWaitTimeout and leaves; the
-// producer then times out on the stage that warp never releases, records
-// the error, waits (bounded) for its copies in flight and leaves.
+// global memory directly. One producer warp (its lane 0) issues the bulk
+// copies of each chunk into the next free stage and leaves the chunk's
+// offsets in a descriptor beside it; NC consumer warps each update a fixed
+// slice of every chunk and release the stage by arriving on its "empty"
+// mbarrier. No block-wide barrier in the loop: consumer warps never wait for
+// one another, only for data.
+//
+// Tile scheduling. With a.tile_next (the default), the producer takes its
+// next tile from a device counter (atomicInc, one tile ahead of the one it
+// is copying), so a grid of the blocks the GPU holds at once works through
+// the tiles in order, lowest first, and no block waits behind a long tile.
+// The counter wraps at n_tiles + gridDim.x - 1: every producer stops after
+// its first fetch past the end, so after the launch's last fetch the counter
+// is 0 again, ready for the next launch. Without a.tile_next, block b takes
+// tiles b, b + grid, ... The producer ends the work with a descriptor of
+// length -1.
+//
+// Bounded, warp-uniform waits: a consumer warp that times out records
+// kErrWaitTimeout and leaves; the producer then times out on the stage that
+// warp never releases, records the error, waits (bounded) for its copies in
+// flight and leaves (the counter is then not back at 0: the layout's steps
+// stay frozen until zero_state_init resets the device state).
 // ---------------------------------------------------------------------------
+struct ChunkDesc {
+  int64_t so;    // shard offset of the chunk (master, m, v)
+  int64_t po;    // parameter offset (flat; stage 3: shard)
+  int64_t ro;    // reduced-gradient offset (stage 1: flat; else shard)
+  int32_t rb;    // reduced-gradient buffer (stage 1: the tile's rank; else 0)
+  int32_t clen;  // elements in the chunk; -1: no more work
+};
+
 template <typename CT, typename PT, int C, int S, int NC>
 __global__ void __launch_bounds__((NC + 1) * 32)
     k_adamw_cast_ws(const __grid_constant__ UpdateArgs a) {
@@ -206,6 +228,7 @@ __global__ void __launch_bounds__((NC + 1) * 32)
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ __align__(8) uint64_t full[S];
   __shared__ __align__(8) uint64_t empty[S];
+  __shared__ ChunkDesc desc[S];
   constexpr int kStage = UpdStage<CT>::bytes(C);
 
   const DevState* st = a.state;
@@ -224,41 +247,74 @@ __global__ void __launch_bounds__((NC + 1) * 32)
   }
   __syncthreads();
 
-  auto red_ptr = [&](const Tile& tl) -> const CT* {
-    return a.stage == 1 ? static_cast<const CT*>(a.red.base[tl.rank]) + tl.flat
-                        : static_cast<const CT*>(a.red.base[0]) + tl.shard;
-  };
-
   if (warp == NC) {  // producer
     if (lane != 0) return;
-    int pt = blockIdx.x, pc = 0;
+    const int n_tiles = a.n_tiles;
+    const unsigned wrap = (unsigned)n_tiles + gridDim.x - 1u;
+    // the tile after `t` for this block (-1: none left)
+    auto next_tile = [&](int t) -> int {
+      if (a.tile_next != nullptr) {
+        const unsigned x = atomicInc(a.tile_next, wrap);
+        return x < (unsigned)n_tiles ? (int)x : -1;
+      }
+      const int x = t < 0 ? (int)blockIdx.x : t + (int)gridDim.x;
+      return x < n_tiles ? x : -1;
+    };
+    int pt = next_tile(-1);
+    Tile tl = a.tiles[pt >= 0 ? pt : 0];
+    // The next tile is claimed one tile ahead, and its descriptor is loaded
+    // after the first chunk of the current tile is issued: neither the
+    // counter's round trip nor the descriptor load stalls a tile boundary.
+    int pn = pt >= 0 ? next_tile(pt) : -1;
+    Tile tn = tl;
+    bool tn_loaded = false;
+    int pc = 0;
     unsigned k = 0;
     bool ok = true;
-    while (pt < a.n_tiles) {
+    while (true) {
       const int s = (int)(k % S);
       if (k >= (unsigned)S && !mbar_wait(&empty[s], ((k / S) - 1) & 1u)) {
         ok = false;
         break;
       }
-      const Tile tl = a.tiles[pt];
+      ChunkDesc& d = desc[s];
+      if (pt < 0) {  // no more work: the consumers stop at this stage
+        d.clen = -1;
+        mbar_arrive(&full[s]);
+        break;
+      }
       const int clen = min(C, tl.len - pc);
       const int nb = clen & ~7;
+      d.so = tl.shard + pc;
+      d.po = (a.stage == 3 ? tl.shard : tl.flat) + pc;
+      d.ro = (a.stage == 1 ? tl.flat : tl.shard) + pc;
+      d.rb = a.stage == 1 ? tl.rank : 0;
+      d.clen = clen;
       unsigned char* base = smem + s * kStage;
       if (nb > 0) {
         mbar_arrive_expect_tx(&full[s], (uint32_t)nb * (12u + (uint32_t)sizeof(CT)));
-        const int64_t so = tl.shard + pc;
-        bulk_g2s(base, s_master + so, nb * 4, &full[s]);
-        bulk_g2s(base + C * 4, s_m + so, nb * 4, &full[s]);
-        bulk_g2s(base + C * 8, s_v + so, nb * 4, &full[s]);
-        bulk_g2s(base + C * 12, red_ptr(tl) + pc, nb * (int)sizeof(CT), &full[s]);
+        bulk_g2s(base, s_master + d.so, nb * 4, &full[s]);
+        bulk_g2s(base + C * 4, s_m + d.so, nb * 4, &full[s]);
+        bulk_g2s(base + C * 8, s_v + d.so, nb * 4, &full[s]);
+        bulk_g2s(base + C * 12, static_cast<const CT*>(a.red.base[d.rb]) + d.ro,
+                 nb * (int)sizeof(CT), &full[s]);
       } else {
         mbar_arrive(&full[s]);
       }
       ++k;
       pc += C;
+      if (!tn_loaded && pn >= 0) {
+        tn = a.tiles[pn];
+        tn_loaded = true;
+      }
       if (pc >= tl.len) {
         pc = 0;
-        pt += gridDim.x;
+        pt = pn;
+        if (pt >= 0) {
+          tl = tn;
+          tn_loaded = false;
+          pn = next_tile(pt);
+        }
       }
     }
     if (!ok) {
@@ -271,25 +327,23 @@ __global__ void __launch_bounds__((NC + 1) * 32)
   const AdamScalars sc = AdamScalars::from(st);
   auto adam = [&](float r, float& p, float& m, float& v) { sc.apply(r, p, m, v); };
 
-  int ct = blockIdx.x, cc = 0;
   unsigned k = 0;
-  // The current tile's descriptor stays in registers for all its chunks.
-  Tile tl = a.tiles[ct < a.n_tiles ? ct : 0];
-  while (ct < a.n_tiles) {
+  while (true) {
     const int s = (int)(k % S);
-    const int clen = min(C, tl.len - cc);
-    const int nb = clen & ~7;
     if (!__all_sync(0xffffffffu, mbar_wait(&full[s], (k / S) & 1u))) {
       if (lane == 0) atomicOr(a.error, kErrWaitTimeout);
       return;
     }
+    const ChunkDesc d = desc[s];
+    if (d.clen < 0) break;
+    const int nb = d.clen & ~7;
     const unsigned char* base = smem + s * kStage;
     const float* sp = reinterpret_cast<const float*>(base);
     const float* sm = reinterpret_cast<const float*>(base + C * 4);
     const float* sv = reinterpret_cast<const float*>(base + C * 8);
     const CT* sr = reinterpret_cast<const CT*>(base + C * 12);
-    const int64_t so = tl.shard + cc, fo = tl.flat + cc;
-    PT* pp = static_cast<PT*>(a.params_flat) + (a.stage == 3 ? so : fo);
+    const int64_t so = d.so;
+    PT* pp = static_cast<PT*>(a.params_flat) + d.po;
     const int e_end = min(nb, (warp + 1) * kPerWarp);
 #pragma unroll 2
     for (int e = warp * kPerWarp + 4 * lane; e < e_end; e += 128) {
@@ -309,10 +363,10 @@ __global__ void __launch_bounds__((NC + 1) * 32)
                  DT<PT>::from_f32(p.w)};
       __stcs(reinterpret_cast<uint2*>(pp + e), *reinterpret_cast<const uint2*>(q));
     }
-    if (warp == 0 && lane < clen - nb) {
+    if (warp == 0 && lane < d.clen - nb) {
       const int e = nb + lane;
       float p = s_master[so + e], m = s_m[so + e], v = s_v[so + e];
-      adam(DT<CT>::to_f32(red_ptr(tl)[cc + e]), p, m, v);
+      adam(DT<CT>::to_f32(static_cast<const CT*>(a.red.base[d.rb])[d.ro + e]), p, m, v);
       s_master[so + e] = p;
       s_m[so + e] = m;
       s_v[so + e] = v;
@@ -321,12 +375,6 @@ __global__ void __launch_bounds__((NC + 1) * 32)
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[s]);
     ++k;
-    cc += C;
-    if (cc >= tl.len) {
-      cc = 0;
-      ct += gridDim.x;
-      if (ct < a.n_tiles) tl = a.tiles[ct];
-    }
   }
 }
 

@@ -226,3 +226,36 @@ def test_last_error_is_set(zlib):
     with pytest.raises(zlib.ZeroError):
         zlib.zero_layout_create([(10,)], _cfg(zlib, 0))
     assert "world" in zlib.zero_last_error()
+
+
+def test_dist_set_rank_partitions_the_tiles(zlib):
+    """zero_dist_set_rank keeps exactly rank r's tiles: over all ranks the
+    tables partition the full table. Rank out of range, a second call and a
+    communication dtype other than the gradient dtype are refused."""
+    from mixed_precision_gb300 import _abi
+    shapes = [(1000,), (77,), (300, 41), (8200,), (0,), (5,), (20000,)]
+    for W in (1, 2, 3, 5):
+        full = zlib.zero_layout_create(shapes, _cfg(zlib, W, 2, 40_000))
+        total = zlib.zero_layout_query(full).n_tiles
+        zlib.zero_layout_destroy(full)
+        per = []
+        for r in range(W):
+            h = zlib.zero_layout_create(shapes, _cfg(zlib, W, 2, 40_000))
+            _abi.zero_dist_set_rank(h, r)
+            per.append(zlib.zero_layout_query(h).n_tiles)
+            with pytest.raises(zlib.ZeroError) as e:
+                _abi.zero_dist_set_rank(h, r)
+            assert e.value.code == _abi.ZERO_ERR_STATE
+            zlib.zero_layout_destroy(h)
+        assert sum(per) == total and all(n > 0 for n in per)
+    h = zlib.zero_layout_create(shapes, _cfg(zlib, 2))
+    for bad in (-1, 2):
+        with pytest.raises(zlib.ZeroError) as e:
+            _abi.zero_dist_set_rank(h, bad)
+        assert e.value.code == _abi.ZERO_ERR_INVALID
+    zlib.zero_layout_destroy(h)
+    h = zlib.zero_layout_create(shapes, _cfg(zlib, 2, c=wl.F32))
+    with pytest.raises(zlib.ZeroError) as e:
+        _abi.zero_dist_set_rank(h, 0)
+    assert e.value.code == _abi.ZERO_ERR_INVALID
+    zlib.zero_layout_destroy(h)

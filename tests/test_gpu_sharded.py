@@ -1,0 +1,205 @@
+"""The sharded step on the GPU: R ranks of one job as threads of one process.
+
+Each thread is one rank: its own layout made rank r's with
+zero_dist_set_rank, its own shard buffers, and the library's kernels for the
+local steps (ShardedZeroStep with LibraryShard). The collectives are carried
+out on the host between the ranks' kernels (ThreadComm): every rank
+synchronises its GPU work, the ranks meet at a barrier, and each takes its
+result from all ranks' snapshots -- the sum in rank order in fp32, rounded
+once to the buffer's dtype (the reading the oracle takes of the
+reduce-scatter), fp64 for the norm pair. No kernel waits for another rank's
+kernel: the only waits are host barriers with a timeout.
+
+Every rank's master/m/v shard, parameters and scaler are compared with the
+oracle's partitioned step (orc_zero_step) on all ranks' gradients, at the
+tolerances of the other parity tests.
+"""
+import concurrent.futures
+import threading
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as wl
+from _parity import to_np
+from _util import params_close, rel_err, scaled_err
+from mixed_precision_gb300.engine import Hparams
+from mixed_precision_gb300.sharded import ShardedZeroStep
+
+pytestmark = pytest.mark.gpu
+
+
+class _Shared:
+    def __init__(self, world):
+        self.world = world
+        self.slots = [None] * world
+        self.barrier = threading.Barrier(world, timeout=120)
+
+
+class ThreadComm:
+    """The three collectives among R threads of one process (see above)."""
+
+    def __init__(self, shared: _Shared, rank: int):
+        self.shared, self.rank, self.world = shared, rank, shared.world
+
+    def _gather(self, t):
+        torch.cuda.synchronize()
+        self.shared.slots[self.rank] = t.clone()
+        self.shared.barrier.wait()
+        snaps = list(self.shared.slots)
+        self.shared.barrier.wait()  # every rank holds the snapshots before any slot changes
+        return snaps
+
+    @staticmethod
+    def _sum(parts):
+        acc_t = torch.float64 if parts[0].dtype == torch.float64 else torch.float32
+        acc = parts[0].to(acc_t)
+        for x in parts[1:]:
+            acc = acc + x.to(acc_t)
+        return acc.to(parts[0].dtype)
+
+    def reduce_scatter(self, out, inp):
+        snaps = self._gather(inp)
+        n = out.numel()
+        out.copy_(self._sum([s[self.rank * n:(self.rank + 1) * n] for s in snaps]))
+        torch.cuda.synchronize()
+
+    def all_reduce(self, t):
+        t.copy_(self._sum(self._gather(t)))
+        torch.cuda.synchronize()
+
+    def all_gather(self, out, inp):
+        out.copy_(torch.cat(self._gather(inp)))
+        torch.cuda.synchronize()
+
+
+SHAPES = [(96, 40), (7,), (300, 33), (1,), (64, 64), (1000,), (0,), (129, 3), (8200,)]
+
+
+def _run_rank(rank, shared, stage, gdt, bucket, steps, hp):
+    torch.cuda.set_device(0)
+    pdt = wl.F16 if gdt == wl.F16 else wl.BF16
+    dynamic = gdt == wl.F16
+    scale0 = 2.0 ** 10 if dynamic else 1.0
+    z = ShardedZeroStep(SHAPES, stage, bucket, gdt, pdt, comm=ThreadComm(shared, rank))
+    numel = wl.numels(SHAPES)
+    master0 = wl.master_init(z.offsets, numel, z.np, 0.02, wl.master_seed(50)).cuda()
+    z.init(master0, init_scale=scale0, dynamic=dynamic, growth_interval=3)
+    out = []
+    for step in range(steps):
+        g = _grads(z, numel, shared.world, step, gdt, scale0)[rank].cuda()
+        z.step(g, hp)
+        torch.cuda.synchronize()
+        out.append((z.scaler_state(), [to_np(t) for t in (z.local.master, z.local.m, z.local.v)],
+                    to_np(z.local.params)))
+    z.close()
+    return out
+
+
+def _grads(z, numel, world, step, gdt, scale0):
+    g = [wl.flat_grads(z.offsets, numel, z.np, 1e-3 * scale0, wl.grad_seed(51, w, step), gdt)
+         for w in range(world)]
+    if step == 2:  # one non-finite value on the last rank: every rank skips
+        g[world - 1][z.offsets[2] + 5] = float("inf")
+    return g
+
+
+@pytest.mark.parametrize("world,stage,gdt", [(2, 2, wl.BF16), (3, 2, wl.F16), (4, 1, wl.BF16),
+                                             (2, 3, wl.F16), (4, 3, wl.BF16), (1, 2, wl.BF16)])
+def test_sharded_ranks_match_oracle(world, stage, gdt):
+    bucket, steps = 24_000, 5
+    hp = Hparams(max_grad_norm=0.05 if world == 4 else 1.0)  # clipping active at W = 4
+    shared = _Shared(world)
+    with concurrent.futures.ThreadPoolExecutor(world) as ex:
+        futs = [ex.submit(_run_rank, r, shared, stage, gdt, bucket, steps, hp) for r in range(world)]
+        per_rank = [f.result(timeout=600) for f in futs]
+
+    # the oracle's partitioned step on every rank's gradients
+    pdt = wl.F16 if gdt == wl.F16 else wl.BF16
+    dynamic = gdt == wl.F16
+    scale0 = 2.0 ** 10 if dynamic else 1.0
+    numel = wl.numels(SHAPES)
+    L = oracle.layout(numel, world, bucket, wl.ELEM_BYTES[gdt])
+    n, npad = L.shard_total, L.np_total
+    perm = L.flat_of_shard()
+    real_shard = L.real_mask().astype(bool)[perm]
+    offs = [int(o) for o in L.param_offset]
+    master0 = wl.master_init(offs, numel, npad, 0.02, wl.master_seed(50)).numpy()
+    ms, mm, vv = master0[perm].copy(), np.zeros(npad, np.float32), np.zeros(npad, np.float32)
+    hist = [np.abs(ms), np.zeros(npad, np.float32), np.zeros(npad, np.float32)]
+    params = oracle.encode(master0, pdt)
+    params[~L.real_mask().astype(bool)] = 0
+    sc = oracle.Scaler(scale=scale0, dynamic=dynamic, growth_interval=3)
+    o_hp = oracle.Hparams(hp.lr, hp.beta1, hp.beta2, hp.eps, hp.weight_decay, hp.max_grad_norm,
+                          hp.grad_divisor)
+
+    class _Z:  # what _grads needs of a step object
+        offsets = offs
+        np = npad
+
+    for step in range(steps):
+        g = [to_np(x) for x in _grads(_Z, numel, world, step, gdt, scale0)]
+        outs = [np.zeros(npad, oracle.storage_dtype(gdt)) for _ in range(world)] if stage == 1 else None
+        info = oracle.zero_step(numel, world, min(stage, 2), bucket, gdt, gdt, pdt, g, ms, mm, vv,
+                                params, o_hp, sc, allreduce_out=outs)
+        for h, x in zip(hist, (ms, mm, vv)):
+            np.maximum(h, np.abs(x), out=h)
+        for r in range(world):
+            st, state, p = per_rank[r][step]
+            assert (st["scale"], st["counter"], st["t"]) == (sc.scale, sc.counter, sc.t), (r, step)
+            assert st["overflow"] == info.overflow and st["skipped"] == info.skipped
+            if np.isfinite(info.grad_norm):
+                assert abs(st["grad_norm"] - info.grad_norm) <= 1e-6 * info.grad_norm
+            sl = slice(r * n, (r + 1) * n)
+            real = real_shard[sl]
+            for got, ref, h in zip(state, (ms, mm, vv), hist):
+                got, ref, h = got[:n][real], ref[sl][real], h[sl][real]
+                assert scaled_err(got, ref, h).max(initial=0.0) <= 1e-5, (r, step)
+                bad = rel_err(got, ref) > 1e-5
+                assert np.all(np.abs(ref[bad]) < 0.1 * h[bad])
+            bound = 1e-5 * hist[0][sl].astype(np.float64)
+            if stage == 3:
+                exp = params[perm[sl]]
+                ok = params_close(p[:n], exp, oracle.decode(exp, pdt), oracle.decode(p[:n], pdt),
+                                  bound, pdt == wl.BF16)
+                assert ok[real].all(), (r, step)
+            else:
+                b_flat = np.zeros(npad)
+                b_flat[perm] = 1e-5 * hist[0].astype(np.float64)
+                ok = params_close(p[:npad], params, oracle.decode(params, pdt),
+                                  oracle.decode(p[:npad], pdt), b_flat, pdt == wl.BF16)
+                assert ok[L.real_mask().astype(bool)].all(), (r, step)
+                assert np.all(p[:npad][~L.real_mask().astype(bool)] == 0)
+
+
+def test_sharded_layout_refuses_single_process_steps():
+    """A layout that holds one rank's shard refuses the entry points that
+    step all W ranks in one process, and the sharded calls need a sharded
+    layout."""
+    from mixed_precision_gb300 import ZeroError
+    from mixed_precision_gb300 import _abi as abi
+    from mixed_precision_gb300.engine import ZeroStep
+
+    shared = _Shared(1)
+    z = ShardedZeroStep(SHAPES, 2, 24_000, wl.BF16, wl.BF16, comm=ThreadComm(shared, 0))
+    master0 = torch.zeros(z.np, dtype=torch.float32, device="cuda")
+    z.init(master0)
+    g = torch.zeros(z.np, dtype=torch.bfloat16, device="cuda")
+    stream = torch.cuda.current_stream().cuda_stream
+    with pytest.raises(ZeroError) as e:
+        abi.zero_step(z.handle, [g.data_ptr()], None, Hparams().c(), stream)
+    assert e.value.code == abi.ZERO_ERR_STATE
+    with pytest.raises(ZeroError) as e:  # stages 2/3 read the bound scratch
+        abi.zero_dist_update(z.handle, g.data_ptr(), stream)
+    assert e.value.code == abi.ZERO_ERR_INVALID
+    z.close()
+    plain = ZeroStep(SHAPES, 1, 2, 24_000, wl.BF16, wl.BF16)
+    plain.allocate()
+    plain.init(master0)
+    pair = torch.zeros(2, dtype=torch.float64, device="cuda")
+    with pytest.raises(ZeroError) as e:
+        abi.zero_dist_shard_norm(plain.handle, 0, pair.data_ptr(), stream)
+    assert e.value.code == abi.ZERO_ERR_STATE
+    plain.close()

@@ -1,0 +1,116 @@
+"""The sharded step's schedule across processes, on CPU (gloo, world size 2).
+
+ShardedZeroStep (mixed_precision_gb300/sharded.py) runs one rank per process:
+per bucket a reduce-scatter (stages 2/3) or an all-reduce (stage 1), this
+rank's share of the norm and overflow flag, one all-reduce of that pair, the
+finalize, the update of this rank's shard, and the per-bucket all-gather of
+the parameters. Here the local steps are the oracle's (tests/_oracle_shard.py)
+and the collectives are gloo's, so the test checks the schedule itself: which
+slices travel, in which buffers they land, and that the global decisions come
+out the same on every rank. Each rank compares its shard of master/m/v, its
+parameter buffer and its scaler with the oracle's own partitioned step
+(orc_zero_step) run on every rank's gradients, bit for bit. At W = 2 a
+two-term sum has one order, so the collectives' sums are the oracle's (leetllm
+"Deep dive: Megatron", "Distributed optimizer": the reduce-scatter sums each
+rank's slice; the all-gather rebuilds the parameter buffer).
+"""
+import os
+import socket
+import traceback
+
+import numpy as np
+import pytest
+import torch.multiprocessing as mp
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+SHAPES = [(96, 40), (7,), (300, 33), (1,), (64, 64), (1000,), (0,), (129, 3)]
+
+
+def _worker(rank, world, port, stage, gdt, q):
+    try:
+        os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+        import torch
+        import torch.distributed as dist
+        dist.init_process_group("gloo", rank=rank, world_size=world)
+        import oracle
+        import workloads as wl
+        from _oracle_shard import OracleShard, bits
+        from mixed_precision_gb300.engine import Hparams
+        from mixed_precision_gb300.sharded import ShardedZeroStep
+
+        pdt = wl.F16 if gdt == wl.F16 else wl.BF16
+        dynamic = gdt == wl.F16
+        scale0 = 2.0 ** 10 if dynamic else 1.0
+        bucket = 24_000  # several buckets, parameters of several sizes in each
+        z = ShardedZeroStep(SHAPES, stage, bucket, gdt, pdt, local=OracleShard)
+        numel = wl.numels(SHAPES)
+        L = oracle.layout(numel, world, bucket, wl.ELEM_BYTES[gdt])
+        assert z.np == L.np_total and len(z.buckets) == len(L.bucket_start) > 1
+        assert z.offsets == [int(o) for o in L.param_offset]
+        master0 = wl.master_init(z.offsets, numel, z.np, 0.02, wl.master_seed(40))
+        z.init(master0, init_scale=scale0, dynamic=dynamic, growth_interval=3)
+
+        n = z.shard_elems
+        ref_master = bits(master0)[L.flat_of_shard()].copy()
+        ref_m, ref_v = np.zeros_like(ref_master), np.zeros_like(ref_master)
+        ref_params = oracle.encode(bits(master0), pdt)
+        ref_params[~L.real_mask().astype(bool)] = 0
+        sc = oracle.Scaler(scale=scale0, dynamic=dynamic, growth_interval=3)
+        hp = Hparams(max_grad_norm=1.0 if stage != 3 else 0.05)
+        o_hp = oracle.Hparams(hp.lr, hp.beta1, hp.beta2, hp.eps, hp.weight_decay, hp.max_grad_norm,
+                              hp.grad_divisor)
+        shard_flat = L.flat_of_shard()[rank * n:(rank + 1) * n]
+        for step in range(6):
+            sigma = 1e-3 * (scale0 if dynamic else 1.0)
+            g_all = [wl.flat_grads(z.offsets, numel, z.np, sigma, wl.grad_seed(41, w, step), gdt)
+                     for w in range(world)]
+            if step == 2:  # one non-finite value on one rank: every rank skips
+                g_all[1][z.offsets[2] + 5] = float("inf")
+            outs = ([np.zeros(z.np, oracle.storage_dtype(gdt)) for _ in range(world)]
+                    if stage == 1 else None)
+            info = oracle.zero_step(numel, world, min(stage, 2), bucket, gdt, gdt, pdt,
+                                    [bits(g) for g in g_all], ref_master, ref_m, ref_v, ref_params,
+                                    o_hp, sc, allreduce_out=outs)
+            mine = g_all[rank].clone()
+            z.step(mine, hp)
+            st = z.scaler_state()
+            assert (st["scale"], st["counter"], st["t"]) == (sc.scale, sc.counter, sc.t), (step, st)
+            assert st["skipped"] == info.skipped == (1 if step == 2 else 0)
+            for got, ref in ((z.local.master, ref_master), (z.local.m, ref_m), (z.local.v, ref_v)):
+                assert np.array_equal(bits(got)[:n].view(np.uint32),
+                                      ref[rank * n:(rank + 1) * n].view(np.uint32)), step
+            p = bits(z.local.params)
+            if stage == 3:
+                assert np.array_equal(p[:n], ref_params[shard_flat]), step
+            else:
+                assert np.array_equal(p[:z.np], ref_params), step
+        dist.barrier()
+        dist.destroy_process_group()
+        q.put((rank, "ok"))
+    except Exception:
+        q.put((rank, traceback.format_exc()))
+
+
+@pytest.mark.parametrize("stage,gdt", [(2, 2), (2, 1), (1, 2), (3, 2), (3, 1)])
+def test_sharded_schedule_matches_oracle_two_ranks(stage, gdt):
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, stage, gdt, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = {}
+    for _ in range(2):
+        r, msg = q.get(timeout=300)
+        res[r] = msg
+    for p in procs:
+        p.join(timeout=60)
+    for r in range(2):
+        assert res[r] == "ok", f"rank {r}:\n{res[r]}"
+    assert all(p.exitcode == 0 for p in procs)
