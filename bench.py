@@ -33,17 +33,25 @@ if ROOT not in sys.path:
 METRIC = "ZeRO step params updated/s and achieved HBM GB/s (% of GB300 step roofline)"
 DEFAULT_WORKLOAD = "qwen3_0.6b_bf16_w2"
 L2_BYTES = 129 * 1000 * 1000
-# DRAM bytes per real element of each dominant kernel from one ncu capture
-# (dram__bytes_read.sum + dram__bytes_write.sum / elements), with the capture
-# it comes from; None until a capture of the current kernel exists.
+# DRAM bytes per real element of each dominant kernel, from one ncu capture
+# (dram__bytes_read.sum + dram__bytes_write.sum, one launch, one pass) on a
+# profiling-sized slice of the workload, at the kernel's current grid; the
+# bench line scales them by the workload's elements. Keyed by (kernel,
+# workload); a workload without a capture of its kernel reports null.
 NCU_TRAFFIC_PER_ELEM = {
-    # profiles/dram_bytes_qwen3_0.6b_bf16_w2.md, one full-size launch each:
-    # (8.348124 + 8.280789) GB / 596,049,920 elements
-    "k_adamw_cast": 27.898,
-    # (2.387236 + 1.155004) GB / 596,049,920 elements
-    "k_reduce_norm": 5.943,
-    # (9.540289 + 8.295399) GB / 596,049,920 elements (7904 blocks)
-    "k_spec_step": 29.923,
+    # update kernel, one block per tile (15,392 blocks), 8 Qwen3 layers,
+    # 125,847,552 elements: (1.762525 + 1.701564) GB
+    ("k_adamw_cast", "qwen3_0.6b_bf16_w2"): 27.526,
+    # reduce kernel, W=2, 1,216 blocks, the same slice: (0.504079 + 0.214487) GB
+    ("k_reduce_norm", "qwen3_0.6b_bf16_w2"): 5.710,
+    # update kernel, one block per tile (28,680 blocks), 2 MoE layers,
+    # 234,946,560 elements: (3.290662 + 3.229782) GB
+    ("k_adamw_cast", "moe_3.9b_bf16_w4"): 27.753,
+    # reduce kernel, W=4, 1,216 blocks, the same slice: (1.880804 + 0.448031) GB
+    ("k_reduce_norm", "moe_3.9b_bf16_w4"): 9.912,
+    # speculative single pass, W=2, 3,952 blocks, 8 Qwen3 layers:
+    # (2.0143 + 1.7090) GB / 125,847,552 elements
+    ("k_spec_step", "qwen3_0.6b_bf16_w2"): 29.59,
 }
 
 
@@ -629,7 +637,7 @@ def run_ours(args) -> dict | None:
     k1_bytes = N * (w.world * G + (w.world * C if w.stage == 1 else C))
     k3_bytes = N * (C + 24 + P)
     k1_ms, k2_ms, k3_ms = statistics.mean(k1), statistics.mean(k2), statistics.mean(k3)
-    if args.speculative:
+    if args.speculative and fast_path:
         # events: [single pass] [its finalize] [guarded fallback kernels + restore]
         spec_bytes = N * info.step_bytes_per_elem
         dom = ("k_spec_step", spec_bytes, k1_ms)
@@ -640,16 +648,18 @@ def run_ours(args) -> dict | None:
             ("k_reduce_norm", k1_bytes, k1_ms)
         # "k_finalize": the interval between the reduce and the update (the
         # finalize runs inside the reduce's last block, or as its own kernel
-        # with the register-staged reduce and per-tensor launches)
+        # with the register-staged reduce and per-tensor launches). A
+        # speculative step whose last finalize predicted clipping launches
+        # these two kernels itself, and the events bracket them the same way.
         kernels = {"k_reduce_norm": k1_ms, "k_finalize": k2_ms, "k_adamw_cast": k3_ms,
                    "k_reduce_norm_gbs": k1_bytes / (k1_ms / 1e3) / 1e9,
                    "k_adamw_cast_gbs": k3_bytes / (k3_ms / 1e3) / 1e9}
     achieved = dom[1] / (dom[2] / 1e3) / 1e9
-    tr = NCU_TRAFFIC_PER_ELEM.get(dom[0])
+    tr = NCU_TRAFFIC_PER_ELEM.get((dom[0], w.name))
     sb = stage_bytes(w)
     # the stage's own bytes: the ledger, plus the all-reduce writes in stage 1
     step_gbs = sb["own"] * N / step_s / 1e9
-    impl_bytes = sb["own"] if args.speculative else sb["impl"]
+    impl_bytes = sb["own"] if (args.speculative and fast_path) else sb["impl"]
     out = {
         "metric": METRIC,
         "value": job_value(N, world, step_s),
@@ -692,9 +702,10 @@ def run_ours(args) -> dict | None:
         "checkpoint": checkpoint,
         "e2e": e2e,
         # two-pass: reduce (its last block finalizes) + update; speculative:
-        # single pass (finalizes) + guarded reduce + update + guarded restore
+        # single pass (finalizes) + guarded reduce + update + guarded restore,
+        # or, once the device has predicted clipping, the two-pass launches
         "gpu_launches": K * ((2 * sum(1 for n in numel if n > 0) + 1) if args.per_tensor_launch
-                             else (4 if args.speculative else 2)),
+                             else (4 if (args.speculative and fast_path) else 2)),
         "clocks": clocks,
     }
     z.close()
@@ -784,6 +795,14 @@ def time_config(name: str, over: dict, steps: int, warmup: int, local: int) -> d
         "scale": st["scale"],
         "clocks": tm["clocks"],
     }
+    dom, dom_ms, dom_b = (("k_adamw_cast", k3_ms, b["k3"]) if k3_ms >= k1_ms
+                          else ("k_reduce_norm", k1_ms, b["k1"]))
+    achieved = dom_b * N / (dom_ms / 1e3) / 1e9
+    tr = NCU_TRAFFIC_PER_ELEM.get((dom, w.name))
+    out["roofline"] = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak,
+                       "unit": "GB/s", "frac": achieved / peak,
+                       "traffic": tr * N if tr is not None else None,
+                       "algorithmic_bytes_per_launch": dom_b * N, "peak_source": peak_src}
     z.close()
     del grads, z
     torch.cuda.synchronize()

@@ -312,9 +312,16 @@ int zero_step_per_tensor_launch(zero_layout_t* layout, const void* const* grads,
  * The decision is taken on the device; every branch's kernels are enqueued
  * and those not taken return at once, so the call never synchronises.
  * While the last finalized step clipped, the single pass is predicted to
- * fall back and returns at once: the step then costs what zero_step costs
- * plus two near-empty launches, and only the step on which clipping switches
- * on pays for both passes.
+ * fall back. Every finalize writes that prediction into a mapped pinned host
+ * word (allocated by zero_state_bind_alternate); when the latest value
+ * written says "clipped", the call launches the reduce / finalize / update
+ * kernels directly, unguarded, and costs what zero_step costs. The word may
+ * lag the GPU by the steps still queued: it only chooses which kernels run,
+ * and both choices compute the same step. While the stream is being
+ * captured, the word is not read (the graph keeps the device-guarded
+ * sequence, whose single pass then returns at once when predicted).
+ * ZERO_SPEC_HINT=0 in the environment at bind_alternate turns the word off.
+ * Only the step on which clipping switches on pays for both passes.
  * The commit decision uses the single pass's own norm, summed in another
  * grouping than zero_step's (both within the parity tolerance of the exact
  * norm); only a norm within that rounding of the clip threshold could make

@@ -140,10 +140,13 @@ struct zero_layout {
   // register-staged kernels, kept as the comparison baseline (environment
   // ZERO_REDUCE_VARIANT / ZERO_UPDATE_VARIANT = 0 at bind selects them)
   int reduce_variant = 1, update_variant = 1;
-  // the pipelined update's tile schedule: 1 (default) = a device counter
-  // hands out tiles to a grid of the resident blocks; 0 = block b takes tiles
-  // b, b + grid, ... (environment ZERO_UPDATE_SCHED=static at bind)
-  int update_sched = 1;
+  // The pipelined update's tile schedule. The step's own update: 0 (default)
+  // = block b takes tiles b, b + grid, ... with one block per tile; 1 =
+  // a device counter hands out tiles to a grid of the resident blocks
+  // (environment ZERO_UPDATE_SCHED=dynamic at bind). The speculative step's
+  // guarded update always takes the counter: as a no-op (committed steps) it
+  // then costs one wave of resident blocks, not one block per tile.
+  int update_sched = 0;
   cudaEvent_t events[4] = {nullptr, nullptr, nullptr, nullptr};
   bool timing = false;
 
@@ -174,6 +177,16 @@ struct zero_layout {
   // shard only; -1 = every simulated rank in this process (the default).
   int local_rank = -1;
   int sms = 0;
+
+  // The speculative step's clip prediction, written by every finalize into a
+  // mapped pinned host word (allocated by zero_state_bind_alternate). When
+  // the latest written prediction says the last finalized step clipped, the
+  // next speculative call launches the two-pass kernels directly instead of
+  // an empty single pass and guarded kernels (the same step either way).
+  // ZERO_SPEC_HINT=0 at bind_alternate leaves every decision to the device.
+  int* hint_host = nullptr;
+  int* hint_dev = nullptr;
+  bool use_hint = true;
 
   int world() const { return cfg.world; }
   int n_params() const { return (int)numel.size(); }
@@ -373,7 +386,8 @@ int launch_step(zero_layout* L, const GradSrc& src, void* const* allreduce_out,
     ua.params_flat = L->params;
     ua.state = L->d_state;
     ua.error = &L->d_state->error;
-    ua.tile_next = L->update_sched ? &L->d_state->tiles_next : nullptr;
+    const bool counter = L->update_variant == 1 && (guarded || L->update_sched);
+    ua.tile_next = counter ? &L->d_state->tiles_next : nullptr;
     Range r("K3 unscale+clip+AdamW+cast");
     e = launch_update(ua, guarded ? L->grid_update_guarded : L->grid_update, L->update_variant, s);
     if (e != cudaSuccess) return cuda_fail(e, "update kernel launch");
@@ -390,6 +404,17 @@ int launch_step(zero_layout* L, const GradSrc& src, void* const* allreduce_out,
 int launch_step_spec(zero_layout* L, const GradSrc& src, const zero_hparams* hp, cudaStream_t s) {
   const int n_tiles = (int)L->tiles.size();
   if (n_tiles == 0) return launch_step(L, src, nullptr, hp, s);
+  // The latest finalize predicted clipping: the two-pass kernels, unguarded.
+  // Not while the stream is being captured: a graph keeps the device-guarded
+  // sequence, which decides on every replay.
+  if (L->use_hint && L->hint_host != nullptr && *reinterpret_cast<volatile int*>(L->hint_host) != 0) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    ZERO_CUDA(cudaStreamIsCapturing(s, &cs));
+    if (cs == cudaStreamCaptureStatusNone) {
+      Range r_hint("speculative step: predicted clipping, two-pass kernels");
+      return launch_step(L, src, nullptr, hp, s);
+    }
+  }
   SpecArgs sa{};
   sa.tiles = L->d_tiles;
   sa.n_tiles = n_tiles;
@@ -616,6 +641,7 @@ int zero_layout_destroy(zero_layout_t* L) {
   }
   if (L->dblock) L->free_fn(L->dblock, L->alloc_ctx);
   if (L->d_gather) L->free_fn(L->d_gather, L->alloc_ctx);
+  if (L->hint_host) cudaFreeHost(L->hint_host);
   delete L;
   return ZERO_OK;
 }
@@ -808,18 +834,21 @@ static int state_bind(zero_layout_t* L, void* master, void* m, void* v, void* pa
     // (ZERO_UPDATE_SCHED=static, register-staged variant too), one block per
     // tile unless ZERO_UPDATE_GRID_MULT asks for a multiple of the resident
     // blocks, and the guarded update at ZERO_GUARDED_GRID_MULT.
-    if (const char* v = std::getenv("ZERO_UPDATE_SCHED")) L->update_sched = std::strcmp(v, "static") != 0;
+    if (const char* v = std::getenv("ZERO_UPDATE_SCHED")) L->update_sched = std::strcmp(v, "dynamic") == 0;
     if (L->update_variant == 0) L->update_sched = 0;
     const int gm = grid_mult("ZERO_GUARDED_GRID_MULT", kGuardedGridMult);
+    const int resident_u = std::max(1, std::min(n_tiles, sms * bps_u));
     if (L->update_sched) {
       L->grid_update = std::max(1, std::min(n_tiles, sms * bps_u * grid_mult("ZERO_UPDATE_GRID_MULT", 1)));
-      L->grid_update_guarded = L->grid_update;
     } else {
       L->grid_update = std::getenv("ZERO_UPDATE_GRID_MULT") == nullptr
                            ? std::max(1, n_tiles)
                            : std::max(1, std::min(n_tiles, sms * bps_u * grid_mult("ZERO_UPDATE_GRID_MULT", 1)));
-      L->grid_update_guarded = std::max(1, std::min(n_tiles, sms * bps_u * gm));
     }
+    // the guarded update: the counter and one wave of resident blocks (the
+    // register-staged variant has no counter: ZERO_GUARDED_GRID_MULT waves)
+    L->grid_update_guarded =
+        L->update_variant == 1 ? resident_u : std::max(1, std::min(n_tiles, sms * bps_u * gm));
     L->grid_copy = std::max(1, std::min(n_tiles, sms * 4 * grid_mult("ZERO_COPY_GRID_MULT", kCopyGridMult)));
     // the guarded parameter restore is a no-op on every step that did not
     // overflow: one wave of resident blocks unless ZERO_GUARDED_GRID_MULT asks
@@ -873,6 +902,16 @@ int zero_state_bind_alternate(zero_layout_t* L, void* master2, void* m2, void* v
   ZERO_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, L->device));
   L->grid_spec = std::max(
       1, std::min({(int)L->tiles.size(), sms * bps * grid_mult("ZERO_SPEC_GRID_MULT", spec_grid_mult_default(L->world())), kMaxPartials}));
+  if (L->hint_host == nullptr) {
+    void* h = nullptr;
+    ZERO_CUDA(cudaHostAlloc(&h, sizeof(int), cudaHostAllocMapped));
+    L->hint_host = static_cast<int*>(h);
+    *L->hint_host = 0;
+    void* d = nullptr;
+    ZERO_CUDA(cudaHostGetDevicePointer(&d, h, 0));
+    L->hint_dev = static_cast<int*>(d);
+  }
+  if (const char* v = std::getenv("ZERO_SPEC_HINT")) L->use_hint = std::atoi(v) != 0;
   L->master2 = static_cast<float*>(master2);
   L->m2 = static_cast<float*>(m2);
   L->v2 = static_cast<float*>(v2);
@@ -897,7 +936,7 @@ int zero_state_init(zero_layout_t* L, const float* master_init_flat, const zero_
                             (size_t)L->param_elems() * dtype_bytes(L->cfg.param_dtype), s));
   ScalerCfg sc{cfg->init_scale, cfg->dynamic ? 1 : 0, cfg->growth_interval, cfg->growth_factor,
                cfg->backoff_factor, cfg->min_scale};
-  cudaError_t e = launch_state_init(sc, L->d_state, s);
+  cudaError_t e = launch_state_init(sc, L->d_state, L->master2 ? L->hint_dev : nullptr, s);
   if (e != cudaSuccess) return cuda_fail(e, "state init launch");
   if (!L->tiles.empty()) {
     e = launch_init_from_flat(L->d_tiles, (int)L->tiles.size(), master_init_flat, L->master,

@@ -79,6 +79,13 @@ __device__ inline void apply_step(const Hparams& hp, double inv, double c, DevSt
   }
 }
 
+// The clip predictor, copied to the host word the library reads before the
+// next speculative step (a hint for which kernels to launch; every path
+// computes the same step).
+__device__ inline void publish_prediction(const DevState* st) {
+  if (st->hint != nullptr) *reinterpret_cast<volatile int*>(st->hint) = st->predict_fallback;
+}
+
 // The scaler state machine and the update's scalars from the global sum of
 // squares and overflow flag (one thread).
 __device__ inline void finalize_state(double sumsq, unsigned any, int world, const Hparams& hp,
@@ -91,6 +98,7 @@ __device__ inline void finalize_state(double sumsq, unsigned any, int world, con
   const double c = clip_coef(hp, st);
   st->skip = 0;
   st->predict_fallback = c < 1.0 ? 1 : 0;
+  publish_prediction(st);
   apply_step(hp, inv, c, st);
 }
 
@@ -109,6 +117,7 @@ __device__ inline void finalize_spec_state(double sumsq, unsigned any, int world
     st->need_fallback = 1;
     st->skip = 1;
     st->predict_fallback = 1;
+    publish_prediction(st);
     return;
   }
   st->skip = 1;  // the update already happened

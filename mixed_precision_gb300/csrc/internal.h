@@ -67,6 +67,9 @@ struct DevState {
   double beta1_pow, beta2_pow;        // beta1^t and beta2^t as running products ...
   double beta1_pow_of, beta2_pow_of;  // ... of these betas (NaN: not valid, use pow)
   unsigned tiles_next;  // the update kernel's tile counter (0 between launches)
+  int* hint;  // device address of a mapped pinned host word, or null: every
+              // finalize copies predict_fallback there, so the host can read
+              // the latest prediction without synchronising
 };
 
 struct Hparams {  // mirror of zero_hparams
@@ -145,7 +148,7 @@ cudaError_t launch_finalize(const double* part_sumsq, const unsigned* part_ovf, 
                             int world, const Hparams& hp, DevState* st, int guarded, cudaStream_t s);
 cudaError_t launch_update(const UpdateArgs& a, int grid, int variant, cudaStream_t s);
 int update_blocks_per_sm(int comm_dtype, int param_dtype, int variant);
-cudaError_t launch_state_init(const ScalerCfg& cfg, DevState* st, cudaStream_t s);
+cudaError_t launch_state_init(const ScalerCfg& cfg, DevState* st, int* hint, cudaStream_t s);
 cudaError_t launch_init_from_flat(const Tile* tiles, int n_tiles, const float* master_flat,
                                   float* master, void* params_flat, int param_dtype,
                                   int params_by_shard, int grid, cudaStream_t s);

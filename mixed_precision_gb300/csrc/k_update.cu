@@ -93,8 +93,10 @@ cudaError_t launch_finalize(const double* part_sumsq, const unsigned* part_ovf, 
   return cudaGetLastError();
 }
 
-__global__ void k_state_init(const ScalerCfg cfg, DevState* st) {
+__global__ void k_state_init(const ScalerCfg cfg, DevState* st, int* hint) {
   DevState z = {};
+  z.hint = hint;
+  if (hint != nullptr) *reinterpret_cast<volatile int*>(hint) = 0;
   z.scale = cfg.init_scale;
   z.dynamic = cfg.dynamic;
   z.growth_interval = cfg.growth_interval;
@@ -107,8 +109,8 @@ __global__ void k_state_init(const ScalerCfg cfg, DevState* st) {
   *st = z;
 }
 
-cudaError_t launch_state_init(const ScalerCfg& cfg, DevState* st, cudaStream_t s) {
-  k_state_init<<<1, 1, 0, s>>>(cfg, st);
+cudaError_t launch_state_init(const ScalerCfg& cfg, DevState* st, int* hint, cudaStream_t s) {
+  k_state_init<<<1, 1, 0, s>>>(cfg, st, hint);
   return cudaGetLastError();
 }
 

@@ -89,3 +89,41 @@ def test_grid_size_does_not_change_the_step(monkeypatch, spec, W, gdt):
         assert torch.equal(small.params_flat.view(torch.int16), large.params_flat.view(torch.int16))
     small.close()
     large.close()
+
+
+@pytest.mark.parametrize("W,gdt", [(2, wl.BF16), (8, wl.F16)])
+def test_update_tile_schedules_agree(monkeypatch, W, gdt):
+    """The update kernel's two tile schedules -- one block per tile, and a
+    device counter handing tiles to a grid of the resident blocks -- write
+    bit-identical state and parameters over clean, clipped and skipped steps.
+    The counter wraps back to 0 after every launch: were it left anywhere
+    else, the next step's update would skip tiles and the states would part."""
+    def layout(sched):
+        monkeypatch.setenv("ZERO_UPDATE_SCHED", sched)
+        z = ZeroStep(_shapes(), W, 2, 8_000_000, gdt, gdt)
+        z.allocate()
+        master0 = wl.master_init(z.offsets, z.numels, z.np, 0.02, wl.master_seed(92), device="cuda")
+        z.init(master0, init_scale=2.0 ** 12, dynamic=True, growth_interval=1000)
+        return z
+
+    per_tile, counter = layout("static"), layout("dynamic")
+    mask = _real_shard_mask(per_tile)
+    rank, idx = wl.inject_position(per_tile.numels, per_tile.offsets, W, seed=18)
+    for step, kind in enumerate(["clean", "clip", "inf", "clean", "clip", "clean"]):
+        g = [wl.flat_grads(per_tile.offsets, per_tile.numels, per_tile.np, 1e-3,
+                           wl.grad_seed(901, r, step), gdt, device="cuda") for r in range(W)]
+        if kind == "inf":
+            g[rank][idx] = float("inf")
+        hp = Hparams(max_grad_norm=1e-5 if kind == "clip" else 1e9)
+        for z in (per_tile, counter):
+            z.step(g, hp)
+        torch.cuda.synchronize()
+        sa, sb = per_tile.scaler_state(), counter.scaler_state()
+        for k in KEYS + ("grad_norm",):
+            assert sa[k] == sb[k], (step, k)
+        assert (sa["clip_coef"] < 1.0) == (kind == "clip") or kind == "inf"
+        for x, y in zip((per_tile.master, per_tile.m, per_tile.v), (counter.master, counter.m, counter.v)):
+            assert torch.equal(x[mask].view(torch.int32), y[mask].view(torch.int32)), step
+        assert torch.equal(per_tile.params_flat.view(torch.int16), counter.params_flat.view(torch.int16))
+    per_tile.close()
+    counter.close()

@@ -44,6 +44,7 @@ def ragged_shapes(seed):
     return [(s,) for s in sizes]
 
 
+@pytest.mark.parametrize("hint", ["1", "0"])
 @pytest.mark.parametrize("W,stage,gdt,cdt,pdt,bucket", [
     (2, 2, wl.BF16, -1, wl.BF16, 64_000),
     (2, 3, wl.BF16, -1, wl.BF16, 64_000),
@@ -53,8 +54,13 @@ def ragged_shapes(seed):
     (5, 2, wl.F32, wl.BF16, wl.BF16, 100_000),
     (1, 2, wl.F16, -1, wl.F16, 50_000),
 ])
-def test_every_branch_matches_oracle(W, stage, gdt, cdt, pdt, bucket):
-    """Commit, overflow skip, clip fallback, and commits again, against the oracle."""
+def test_every_branch_matches_oracle(monkeypatch, W, stage, gdt, cdt, pdt, bucket, hint):
+    """Commit, overflow skip, clip fallback, and commits again, against the oracle.
+    hint "1": after a step that clipped, the host reads the device's
+    prediction and launches the two-pass kernels itself; "0": every decision
+    stays on the device (the single pass returns at once, the guarded kernels
+    run). Both must give the oracle's step."""
+    monkeypatch.setenv("ZERO_SPEC_HINT", hint)
     pr = Pair(small_qwen_shapes(), W, stage, bucket, gdt, pdt, cdt, init_scale=8.0, dynamic=True,
               growth_interval=3, index=300 + W, speculative=True)
     rank, idx = wl.inject_position(pr.numel, pr.z.offsets, W, seed=W)
