@@ -111,9 +111,12 @@ typedef struct {
   int64_t n_buckets;
   int64_t n_tiles;         /* work units the kernels iterate over */
   int64_t grad_bytes;      /* bytes of ONE rank's flat gradient buffer (Np * size(grad)) */
-  int64_t state_bytes;     /* bytes of ONE of master/m/v (Np * 4, all ranks' shards) */
-  int64_t params_bytes;    /* bytes of the flat parameter buffer (Np * size(param)) */
-  int64_t scratch_bytes;   /* stage 2: reduced shards (Np * size(comm)); stage 1: 0 */
+  int64_t state_bytes;     /* bytes of ONE of master/m/v (Np * 4, all ranks' shards;
+                              after zero_dist_set_rank: Np/W * 4, this rank's) */
+  int64_t params_bytes;    /* bytes of the parameter buffer (Np * size(param); after
+                              zero_dist_set_rank in stage 3: Np/W * size(param)) */
+  int64_t scratch_bytes;   /* stages 2/3: reduced shards (Np * size(comm); after
+                              zero_dist_set_rank: Np/W * size(comm)); stage 1: 0 */
   int64_t allreduce_bytes; /* stage 1: bytes of ONE rank's all-reduce output; stage 2: 0 */
   int64_t device_bytes_owned; /* device bytes the library allocates at bind */
   double ledger_bytes_per_param; /* [DO] per-rank persistent bytes per parameter:

@@ -388,6 +388,7 @@ int launch_step(zero_layout* L, const GradSrc& src, void* const* allreduce_out,
     ua.error = &L->d_state->error;
     const bool counter = L->update_variant == 1 && (guarded || L->update_sched);
     ua.tile_next = counter ? &L->d_state->tiles_next : nullptr;
+    ua.restore = guarded && L->update_variant == 1 ? 1 : 0;  // the parameter restore rides along
     Range r("K3 unscale+clip+AdamW+cast");
     e = launch_update(ua, guarded ? L->grid_update_guarded : L->grid_update, L->update_variant, s);
     if (e != cudaSuccess) return cuda_fail(e, "update kernel launch");
@@ -398,9 +399,9 @@ int launch_step(zero_layout* L, const GradSrc& src, void* const* allreduce_out,
 
 // The speculative step: the single pass and its finalize; then the two-pass
 // kernels guarded on DevState::need_fallback (they return at once unless
-// clipping turned out active), the update (skipped unless the fallback
-// finalize cleared DevState::skip) and the parameter restore after an
-// overflow (guarded on DevState::restore_params).
+// clipping turned out active): the reduce, and the update (skipped unless the
+// fallback finalize cleared DevState::skip), which instead recasts the
+// parameters after an overflow (DevState::restore_params).
 int launch_step_spec(zero_layout* L, const GradSrc& src, const zero_hparams* hp, cudaStream_t s) {
   const int n_tiles = (int)L->tiles.size();
   if (n_tiles == 0) return launch_step(L, src, nullptr, hp, s);
@@ -445,9 +446,13 @@ int launch_step_spec(zero_layout* L, const GradSrc& src, const zero_hparams* hp,
   int rc = launch_step(L, src, nullptr, hp, s, /*guarded=*/1);
   L->timing = timing;
   if (rc != ZERO_OK) return rc;
-  e = launch_recast(L->d_tiles, n_tiles, sa.master, L->params, L->cfg.param_dtype, L->cfg.stage == 3,
-                    L->d_state, /*guarded=*/1, L->grid_copy_guarded, s);
-  if (e != cudaSuccess) return cuda_fail(e, "parameter restore launch");
+  // The parameter restore after an overflow: inside the guarded update (the
+  // pipelined kernel), else a guarded launch of its own.
+  if (L->update_variant != 1) {
+    e = launch_recast(L->d_tiles, n_tiles, sa.master, L->params, L->cfg.param_dtype,
+                      L->cfg.stage == 3, L->d_state, /*guarded=*/1, L->grid_copy_guarded, s);
+    if (e != cudaSuccess) return cuda_fail(e, "parameter restore launch");
+  }
   if (L->timing) ZERO_CUDA(cudaEventRecord(L->events[3], s));
   return ZERO_OK;
 }
@@ -672,9 +677,9 @@ int zero_layout_query(const zero_layout_t* L, zero_layout_info* o) {
   o->n_buckets = (int64_t)L->bstart.size();
   o->n_tiles = (int64_t)L->tiles.size();
   o->grad_bytes = L->np * (int64_t)G;
-  o->state_bytes = L->np * 4;
-  o->params_bytes = L->np * (int64_t)P;
-  o->scratch_bytes = L->cfg.stage != 1 ? L->np * C : 0;
+  o->state_bytes = L->state_elems() * 4;
+  o->params_bytes = L->param_elems() * (int64_t)P;
+  o->scratch_bytes = L->cfg.stage != 1 ? L->state_elems() * C : 0;
   o->allreduce_bytes = L->cfg.stage == 1 ? L->np * C : 0;
   o->device_bytes_owned = (int64_t)plan_block(L).total;
   o->ledger_bytes_per_param = L->cfg.stage == 1   ? P + G + 12.0 / W
@@ -903,13 +908,19 @@ int zero_state_bind_alternate(zero_layout_t* L, void* master2, void* m2, void* v
   L->grid_spec = std::max(
       1, std::min({(int)L->tiles.size(), sms * bps * grid_mult("ZERO_SPEC_GRID_MULT", spec_grid_mult_default(L->world())), kMaxPartials}));
   if (L->hint_host == nullptr) {
+    // Without mapped pinned memory the step still runs, every decision on
+    // the device: the word is an optimisation only.
     void* h = nullptr;
-    ZERO_CUDA(cudaHostAlloc(&h, sizeof(int), cudaHostAllocMapped));
-    L->hint_host = static_cast<int*>(h);
-    *L->hint_host = 0;
     void* d = nullptr;
-    ZERO_CUDA(cudaHostGetDevicePointer(&d, h, 0));
-    L->hint_dev = static_cast<int*>(d);
+    if (cudaHostAlloc(&h, sizeof(int), cudaHostAllocMapped) == cudaSuccess &&
+        cudaHostGetDevicePointer(&d, h, 0) == cudaSuccess) {
+      L->hint_host = static_cast<int*>(h);
+      *L->hint_host = 0;
+      L->hint_dev = static_cast<int*>(d);
+    } else {
+      if (h != nullptr) cudaFreeHost(h);
+      (void)cudaGetLastError();  // clear the failure: it is not the caller's
+    }
   }
   if (const char* v = std::getenv("ZERO_SPEC_HINT")) L->use_hint = std::atoi(v) != 0;
   L->master2 = static_cast<float*>(master2);

@@ -131,6 +131,9 @@ struct UpdateArgs {
   unsigned* error;  // &state->error
   unsigned* tile_next;  // the pipelined kernel's tile counter (&state->tiles_next), or
                         // nullptr: block b takes tiles b, b + grid, ...
+  int restore;  // 1 (the speculative step's guarded update): when the state asks
+                // for the parameters back after an overflow, recast them from
+                // the current master instead (pipelined kernel only)
 };
 
 // Kernel launchers. Each returns the launch's cudaError_t.

@@ -234,6 +234,28 @@ __global__ void __launch_bounds__((NC + 1) * 32)
   constexpr int kStage = UpdStage<CT>::bytes(C);
 
   const DevState* st = a.state;
+  if (a.restore && st->restore_params && !st->error) {
+    // The speculative step overflowed: its single pass wrote the parameters,
+    // the state stays as it was, so the parameters are recast from the
+    // current master (every block, tiles b, b + grid, ...).
+    const float* mp = a.master[st->cur];
+    for (int t = blockIdx.x; t < a.n_tiles; t += gridDim.x) {
+      const Tile tl = a.tiles[t];
+      const float* src = mp + tl.shard;
+      PT* dst = static_cast<PT*>(a.params_flat) + (a.stage == 3 ? tl.shard : tl.flat);
+      const int ng = tl.len >> 3;
+      for (int g = threadIdx.x; g < ng; g += blockDim.x) {
+        float x[8];
+        load8_f32(src + (int64_t)g * 8, x);
+        Pack8<PT> q;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) q.e[j] = DT<PT>::from_f32(x[j]);
+        store8_raw(dst + (int64_t)g * 8, q);
+      }
+      for (int i = ng * 8 + threadIdx.x; i < tl.len; i += blockDim.x) dst[i] = DT<PT>::from_f32(src[i]);
+    }
+    return;
+  }
   if (st->skip || st->error) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int cs = st->cur;

@@ -242,7 +242,12 @@ def test_dist_set_rank_partitions_the_tiles(zlib):
         for r in range(W):
             h = zlib.zero_layout_create(shapes, _cfg(zlib, W, 2, 40_000))
             _abi.zero_dist_set_rank(h, r)
-            per.append(zlib.zero_layout_query(h).n_tiles)
+            info = zlib.zero_layout_query(h)
+            per.append(info.n_tiles)
+            # the buffers of one rank's shard
+            assert info.state_bytes == info.shard_elems * 4
+            assert info.scratch_bytes == info.shard_elems * 2
+            assert info.params_bytes == info.n_padded * 2  # stage 2: the all-gathered buffer
             with pytest.raises(zlib.ZeroError) as e:
                 _abi.zero_dist_set_rank(h, r)
             assert e.value.code == _abi.ZERO_ERR_STATE
