@@ -525,8 +525,13 @@ int zero_scaler_restore(zero_layout_t* layout, const zero_scaler_state* st, void
  * is still the whole flat buffer): all-gather the parameters once after it.
  * Requires comm_dtype == grad_dtype (the collectives reduce in the gradient
  * dtype). ZERO_ERR_STATE if called twice or after bind; every entry point
- * that steps all W ranks in one process (zero_step*, accumulation, gathers,
- * exports, imports) then returns ZERO_ERR_STATE. Host only. */
+ * that steps all W ranks in one process (zero_step*, accumulation, gathers)
+ * then returns ZERO_ERR_STATE. zero_state_export / import and
+ * zero_state_export_params / import_params move this rank's elements only:
+ * an export writes them and zero-fills the rest of the destination (so the
+ * ranks' exports, summed as 32-bit integers, give the whole buffer, -0.0
+ * included); an import reads them from a whole buffer, which may come from a
+ * job of any W, stage or bucket size. Host only. */
 int zero_dist_set_rank(zero_layout_t* layout, int rank);
 
 /* This rank's share of the global norm and overflow check: enqueues a kernel

@@ -1279,8 +1279,11 @@ static int state_pm_copy(zero_layout_t* L, float* a, float* b, float* c, int dir
   state_sets(L, sm, sv1, sv2);
   float* const* shard[3] = {sm, sv1, sv2};
   for (int k = 0; k < 3; ++k) {
-    if (pm[k] == nullptr || L->tiles.empty()) continue;
+    if (pm[k] == nullptr) continue;
     if (!aligned16(pm[k])) return fail(ZERO_ERR_INVALID, "state buffer not 16-byte aligned");
+    // a sharded layout exports its own elements only: the rest reads as zero
+    if (dir == 0 && L->sharded()) ZERO_CUDA(cudaMemsetAsync(pm[k], 0, (size_t)L->n_real * 4, s));
+    if (L->tiles.empty()) continue;
     cudaError_t e = launch_state_pm(L->d_tiles, (int)L->tiles.size(), L->d_pm_delta, shard[k], pm[k],
                                     dir, L->d_state, L->grid_copy, s);
     if (e != cudaSuccess) return cuda_fail(e, "state copy launch");
@@ -1291,14 +1294,12 @@ static int state_pm_copy(zero_layout_t* L, float* a, float* b, float* c, int dir
 int zero_state_export_params(zero_layout_t* L, float* master_pm, float* m_pm, float* v_pm,
                              void* stream) {
   if (int rc = check_ready(L, true)) return rc;
-  if (int rc = check_not_sharded(L, "zero_state_export_params")) return rc;
   return state_pm_copy(L, master_pm, m_pm, v_pm, 0, stream);
 }
 
 int zero_state_import_params(zero_layout_t* L, const float* master_pm, const float* m_pm,
                              const float* v_pm, void* stream) {
   if (int rc = check_ready(L, true)) return rc;
-  if (int rc = check_not_sharded(L, "zero_state_import_params")) return rc;
   if (master_pm == nullptr) return fail(ZERO_ERR_INVALID, "master_pm is required");
   if (int rc = state_pm_copy(L, const_cast<float*>(master_pm), const_cast<float*>(m_pm),
                              const_cast<float*>(v_pm), 1, stream))
@@ -1341,14 +1342,12 @@ int zero_selftest_layout_timeout(zero_layout_t* L, uint32_t spin_limit, void* st
 int zero_state_export(zero_layout_t* L, float* master_flat, float* m_flat, float* v_flat,
                       void* stream) {
   if (int rc = check_ready(L, true)) return rc;
-  if (int rc = check_not_sharded(L, "zero_state_export")) return rc;
   return state_copy(L, master_flat, m_flat, v_flat, 0, stream);
 }
 
 int zero_state_import(zero_layout_t* L, const float* master_flat, const float* m_flat,
                       const float* v_flat, void* stream) {
   if (int rc = check_ready(L, true)) return rc;
-  if (int rc = check_not_sharded(L, "zero_state_import")) return rc;
   return state_copy(L, const_cast<float*>(master_flat), const_cast<float*>(m_flat),
                     const_cast<float*>(v_flat), 1, stream);
 }

@@ -100,6 +100,22 @@ class LibraryShard:
         st = abi.zero_loss_scale_state(self.z.handle, self._stream())
         return {f: getattr(st, f) for f, _ in abi.zero_scaler_state._fields_}
 
+    def export_params(self, master_pm, m_pm, v_pm) -> None:
+        """This rank's fp32 state into parameter-major buffers (N elements
+        each); the other ranks' elements are written as zero."""
+        abi.zero_state_export_params(self.z.handle, master_pm.data_ptr(), m_pm.data_ptr(),
+                                     v_pm.data_ptr(), self._stream())
+
+    def import_params(self, master_pm, m_pm, v_pm) -> None:
+        """This rank's elements from whole parameter-major buffers; its
+        parameter slices are recast."""
+        abi.zero_state_import_params(self.z.handle, master_pm.data_ptr(), m_pm.data_ptr(),
+                                     v_pm.data_ptr(), self._stream())
+
+    def scaler_restore(self, st: dict) -> None:
+        abi.zero_scaler_restore(self.z.handle, abi.zero_scaler_state(
+            st["scale"], st["counter"], st["t"], 0, 0, 0.0, 0.0, 0.0, 0, 0, 0), self._stream())
+
 
 class ShardedZeroStep:
     """Rank `rank` of a W-GPU data-parallel ZeRO-1/2/3 optimizer.
@@ -185,6 +201,39 @@ class ShardedZeroStep:
             n = b.slice_len(W)
             mine = p[b.start + self.rank * n:b.start + (self.rank + 1) * n]
             self.comm.all_gather(p[b.start:b.start + b.length], mine)
+
+    def gather_bucket(self, b: int, out: torch.Tensor) -> None:
+        """Stage 3: bucket b's parameters from every rank's slice into `out`
+        (its padded length, flat order) -- what a forward pass fetches
+        bucket by bucket."""
+        n = self.buckets[b].slice_len(self.world)
+        loc = self.buckets[b].local
+        self.comm.all_gather(out[:self.buckets[b].length], self.local.params[loc:loc + n])
+
+    # ---- checkpoints independent of W -------------------------------------
+    def export_params(self):
+        """(master, m, v) in parameter-major order -- N fp32 elements each, the
+        same for any W, stage or bucket size -- whole on every rank. Each
+        rank exports its own elements (zeros elsewhere); one all-reduce per
+        tensor sums their 32-bit patterns, exactly one rank contributing
+        each element."""
+        n = max(self.info.n_real, 1)
+        dev = self.local.master.device
+        out = [torch.empty(n, dtype=torch.float32, device=dev) for _ in range(3)]
+        self.local.export_params(*out)
+        for t in out:
+            self.comm.all_reduce(t.view(torch.int32))
+        return out
+
+    def import_params(self, master_pm, m_pm, v_pm, scaler: dict | None = None) -> None:
+        """This rank's elements from whole parameter-major buffers (exported by
+        a job of any W, stage or bucket size), its parameters recast and
+        all-gathered; `scaler` (scale, counter, t) restores the loss scaler.
+        Call after init (which sets the scaler's configuration)."""
+        self.local.import_params(master_pm, m_pm, v_pm)
+        if scaler is not None:
+            self.local.scaler_restore(scaler)
+        self.all_gather_params()
 
     def close(self) -> None:
         if self.handle:

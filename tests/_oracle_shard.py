@@ -97,6 +97,34 @@ class OracleShard:
         else:
             p[self.flat] = enc
 
+    def _pm_index(self):
+        """Parameter-major index of every real element of this rank's shard."""
+        if not hasattr(self, "_pm"):
+            offs = np.asarray(self.z.offsets, np.int64)
+            nums = np.asarray(self.z.numels, np.int64)
+            starts = np.concatenate([[0], np.cumsum(nums)[:-1]])
+            f = self.flat[self.real]
+            p = np.searchsorted(offs, f, side="right") - 1
+            self._pm = starts[p] + (f - offs[p])
+        return self._pm
+
+    def export_params(self, master_pm, m_pm, v_pm) -> None:
+        n = self.z.shard_elems
+        for src, dst in zip((self.master, self.m, self.v), (master_pm, m_pm, v_pm)):
+            d = bits(dst)
+            d[:] = 0
+            d[self._pm_index()] = bits(src)[:n][self.real]
+
+    def import_params(self, master_pm, m_pm, v_pm) -> None:
+        n = self.z.shard_elems
+        for dst, src in zip((self.master, self.m, self.v), (master_pm, m_pm, v_pm)):
+            d = bits(dst)[:n]
+            d[self.real] = bits(src)[self._pm_index()]
+        self._cast_params()
+
+    def scaler_restore(self, st: dict) -> None:
+        self.scaler.scale, self.scaler.counter, self.scaler.t = st["scale"], st["counter"], st["t"]
+
     def scaler_state(self) -> dict:
         info = self.info
         return {"scale": self.scaler.scale, "counter": self.scaler.counter, "t": self.scaler.t,

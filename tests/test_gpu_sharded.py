@@ -54,11 +54,13 @@ class ThreadComm:
 
     @staticmethod
     def _sum(parts):
-        acc_t = torch.float64 if parts[0].dtype == torch.float64 else torch.float32
+        dt = parts[0].dtype
+        acc_t = (torch.int64 if not dt.is_floating_point else
+                 torch.float64 if dt == torch.float64 else torch.float32)
         acc = parts[0].to(acc_t)
         for x in parts[1:]:
             acc = acc + x.to(acc_t)
-        return acc.to(parts[0].dtype)
+        return acc.to(dt)
 
     def reduce_scatter(self, out, inp):
         snaps = self._gather(inp)
@@ -94,8 +96,14 @@ def _run_rank(rank, shared, stage, gdt, bucket, steps, hp):
         torch.cuda.synchronize()
         out.append((z.scaler_state(), [to_np(t) for t in (z.local.master, z.local.m, z.local.v)],
                     to_np(z.local.params)))
+    gathered = []
+    if stage == 3:  # every bucket's parameters, all-gathered from the ranks' slices
+        for b, bk in enumerate(z.buckets):
+            buf = torch.empty(bk.length, dtype=z.local.params.dtype, device="cuda")
+            z.gather_bucket(b, buf)
+            gathered.append((bk.start, to_np(buf)))
     z.close()
-    return out
+    return out, gathered
 
 
 def _grads(z, numel, world, step, gdt, scale0):
@@ -114,7 +122,8 @@ def test_sharded_ranks_match_oracle(world, stage, gdt):
     shared = _Shared(world)
     with concurrent.futures.ThreadPoolExecutor(world) as ex:
         futs = [ex.submit(_run_rank, r, shared, stage, gdt, bucket, steps, hp) for r in range(world)]
-        per_rank = [f.result(timeout=600) for f in futs]
+        results = [f.result(timeout=600) for f in futs]
+    per_rank = [r[0] for r in results]
 
     # the oracle's partitioned step on every rank's gradients
     pdt = wl.F16 if gdt == wl.F16 else wl.BF16
@@ -172,6 +181,18 @@ def test_sharded_ranks_match_oracle(world, stage, gdt):
                                   oracle.decode(p[:npad], pdt), b_flat, pdt == wl.BF16)
                 assert ok[L.real_mask().astype(bool)].all(), (r, step)
                 assert np.all(p[:npad][~L.real_mask().astype(bool)] == 0)
+    if stage == 3:  # the gathered buckets: the flat parameters, on every rank alike
+        b_flat = np.zeros(npad)
+        b_flat[perm] = 1e-5 * hist[0].astype(np.float64)
+        real_flat = L.real_mask().astype(bool)
+        for r in range(world):
+            assert len(results[r][1]) == len(L.bucket_start)
+            for (b0, got), bl in zip(results[r][1], L.bucket_len):
+                sl = slice(b0, b0 + int(bl))
+                ok = params_close(got, params[sl], oracle.decode(params[sl], pdt),
+                                  oracle.decode(got, pdt), b_flat[sl], pdt == wl.BF16)
+                assert ok[real_flat[sl]].all(), (r, b0)
+                assert np.array_equal(got, results[0][1][[x[0] for x in results[0][1]].index(b0)][1])
 
 
 def test_sharded_layout_refuses_single_process_steps():
@@ -203,3 +224,94 @@ def test_sharded_layout_refuses_single_process_steps():
         abi.zero_dist_shard_norm(plain.handle, 0, pair.data_ptr(), stream)
     assert e.value.code == abi.ZERO_ERR_STATE
     plain.close()
+
+
+def _run_ranks(world, fn):
+    shared = _Shared(world)
+    with concurrent.futures.ThreadPoolExecutor(world) as ex:
+        futs = [ex.submit(fn, r, ThreadComm(shared, r)) for r in range(world)]
+        return [f.result(timeout=600) for f in futs]
+
+
+def test_checkpoint_across_gpu_counts():
+    """A 2-rank job (bucket 24 KB) steps, then assembles a parameter-major
+    checkpoint: each rank exports its elements, the all-reduce of the 32-bit
+    patterns joins them. A 4-rank job with 60 KB buckets imports it (and the
+    scaler); its own export is the same checkpoint bit for bit, and its next
+    step matches the oracle restarted from that state on its layout."""
+    gdt = pdt = wl.BF16
+    numel = wl.numels(SHAPES)
+    hp = Hparams()
+
+    def job_a(rank, comm):
+        torch.cuda.set_device(0)
+        z = ShardedZeroStep(SHAPES, 2, 24_000, gdt, pdt, comm=comm)
+        z.init(wl.master_init(z.offsets, numel, z.np, 0.02, wl.master_seed(52)).cuda())
+        for step in range(3):
+            g = wl.flat_grads(z.offsets, numel, z.np, 1e-3, wl.grad_seed(53, rank, step), gdt).cuda()
+            z.step(g, hp)
+        ex = z.export_params()
+        st = z.scaler_state()
+        torch.cuda.synchronize()
+        z.close()
+        return [t.clone() for t in ex], st
+
+    res_a = _run_ranks(2, job_a)
+    ex, st = res_a[0]
+    for other, _ in res_a[1:]:  # every rank holds the same whole checkpoint
+        for x, y in zip(ex, other):
+            assert torch.equal(x.view(torch.int32), y.view(torch.int32))
+    assert st["t"] == 3
+
+    def job_b(rank, comm):
+        torch.cuda.set_device(0)
+        z = ShardedZeroStep(SHAPES, 2, 60_000, gdt, pdt, comm=comm)
+        z.init(torch.zeros(max(z.np, 8), device="cuda"))
+        z.import_params(*ex, scaler=st)
+        again = [t.clone() for t in z.export_params()]
+        g = wl.flat_grads(z.offsets, numel, z.np, 1e-3, wl.grad_seed(53, rank, 3), gdt).cuda()
+        z.step(g, hp)
+        torch.cuda.synchronize()
+        out = (again, z.scaler_state(), [to_np(t) for t in (z.local.master, z.local.m, z.local.v)],
+               to_np(z.local.params))
+        z.close()
+        return out
+
+    res_b = _run_ranks(4, job_b)
+    for again, _, _, _ in res_b:
+        for x, y in zip(ex, again):
+            assert torch.equal(x.view(torch.int32), y.view(torch.int32))
+
+    # the oracle restarted from the checkpoint on the 4-rank layout
+    L = oracle.layout(numel, 4, 60_000, 2)
+    n, npad = L.shard_total, L.np_total
+    perm = L.flat_of_shard()
+    flats = []
+    for t in ex:
+        pm, flat, at = t.cpu().numpy(), np.zeros(npad, np.float32), 0
+        for o, k in zip(L.param_offset, numel):
+            flat[o:o + k] = pm[at:at + k]
+            at += k
+        flats.append(flat)
+    ms, mm, vv = (f[perm].copy() for f in flats)
+    hist = [np.maximum(np.abs(ms), 0), np.abs(mm), np.abs(vv)]
+    params = oracle.encode(flats[0], pdt)
+    params[~L.real_mask().astype(bool)] = 0
+    sc = oracle.Scaler(scale=st["scale"], counter=st["counter"], t=st["t"])
+    offs = [int(o) for o in L.param_offset]
+    g = [to_np(wl.flat_grads(offs, numel, npad, 1e-3, wl.grad_seed(53, r, 3), gdt)) for r in range(4)]
+    oracle.zero_step(numel, 4, 2, 60_000, gdt, gdt, pdt, g, ms, mm, vv, params, oracle.Hparams(), sc)
+    for h, x in zip(hist, (ms, mm, vv)):
+        np.maximum(h, np.abs(x), out=h)
+    real_shard = L.real_mask().astype(bool)[perm]
+    for r, (_, st_b, state, p) in enumerate(res_b):
+        assert (st_b["scale"], st_b["counter"], st_b["t"]) == (sc.scale, sc.counter, sc.t)
+        sl = slice(r * n, (r + 1) * n)
+        real = real_shard[sl]
+        for got, ref, h in zip(state, (ms, mm, vv), hist):
+            assert scaled_err(got[:n][real], ref[sl][real], h[sl][real]).max(initial=0.0) <= 1e-5
+        b_flat = np.zeros(npad)
+        b_flat[perm] = 1e-5 * hist[0].astype(np.float64)
+        ok = params_close(p[:npad], params, oracle.decode(params, pdt), oracle.decode(p[:npad], pdt),
+                          b_flat, True)
+        assert ok[L.real_mask().astype(bool)].all()

@@ -12,7 +12,11 @@ parameter buffer and its scaler with the oracle's own partitioned step
 (orc_zero_step) run on every rank's gradients, bit for bit. At W = 2 a
 two-term sum has one order, so the collectives' sums are the oracle's (leetllm
 "Deep dive: Megatron", "Distributed optimizer": the reduce-scatter sums each
-rank's slice; the all-gather rebuilds the parameter buffer).
+rank's slice; the all-gather rebuilds the parameter buffer). Then the ranks
+assemble a parameter-major checkpoint (each exports its own elements, an
+all-reduce of the 32-bit patterns joins them), which must equal the oracle's
+state, and restart a job with another bucket size from it, which must keep
+stepping like the oracle.
 """
 import os
 import socket
@@ -40,7 +44,7 @@ def _worker(rank, world, port, stage, gdt, q):
         dist.init_process_group("gloo", rank=rank, world_size=world)
         import oracle
         import workloads as wl
-        from _oracle_shard import OracleShard, bits
+        from _oracle_shard import TORCH_DTYPE, OracleShard, bits
         from mixed_precision_gb300.engine import Hparams
         from mixed_precision_gb300.sharded import ShardedZeroStep
 
@@ -90,6 +94,65 @@ def _worker(rank, world, port, stage, gdt, q):
                 assert np.array_equal(p[:n], ref_params[shard_flat]), step
             else:
                 assert np.array_equal(p[:z.np], ref_params), step
+
+        if stage == 3:  # every bucket's parameters, all-gathered from the ranks' slices
+            for b, (b0, bl) in enumerate(zip(L.bucket_start, L.bucket_len)):
+                out = torch.empty(int(bl), dtype=TORCH_DTYPE[pdt])
+                z.gather_bucket(b, out)
+                assert np.array_equal(bits(out), ref_params[int(b0):int(b0) + int(bl)]), b
+
+        # A checkpoint independent of W: every rank exports its elements, the
+        # all-reduce of their bit patterns assembles the whole buffer, equal to
+        # the oracle's state in parameter-major order.
+        def shards_to_pm(x, lay):
+            flat = np.zeros(lay.np_total, np.float32)
+            flat[lay.flat_of_shard()] = x
+            return np.concatenate([flat[o:o + k] for o, k in zip(lay.param_offset, numel)])
+
+        def pm_to_shards(pm, lay):
+            flat = np.zeros(lay.np_total, np.float32)
+            at = 0
+            for o, k in zip(lay.param_offset, numel):
+                flat[o:o + k] = pm[at:at + k]
+                at += k
+            return flat[lay.flat_of_shard()].copy(), flat
+
+        ex = z.export_params()
+        for got, ref in zip(ex, (ref_master, ref_m, ref_v)):
+            assert np.array_equal(bits(got).view(np.uint32), shards_to_pm(ref, L).view(np.uint32))
+        # ... and restarts a job with another bucket size, which then steps
+        # like the oracle restarted from the same state
+        bucket2 = 50_000
+        z2 = ShardedZeroStep(SHAPES, stage, bucket2, gdt, pdt, local=OracleShard)
+        z2.init(torch.zeros(z2.np), init_scale=scale0, dynamic=dynamic, growth_interval=3)
+        z2.import_params(*ex, scaler=z.scaler_state())
+        L2 = oracle.layout(numel, world, bucket2, wl.ELEM_BYTES[gdt])
+        n2 = z2.shard_elems
+        ref_master, mflat = pm_to_shards(bits(ex[0]), L2)
+        ref_m, _ = pm_to_shards(bits(ex[1]), L2)
+        ref_v, _ = pm_to_shards(bits(ex[2]), L2)
+        ref_params = oracle.encode(mflat, pdt)
+        ref_params[~L2.real_mask().astype(bool)] = 0
+        shard_flat2 = L2.flat_of_shard()[rank * n2:(rank + 1) * n2]
+        for step in range(6, 8):
+            g_all = [wl.flat_grads(z2.offsets, numel, z2.np, 1e-3 * scale0, wl.grad_seed(41, w, step),
+                                   gdt) for w in range(world)]
+            outs = ([np.zeros(z2.np, oracle.storage_dtype(gdt)) for _ in range(world)]
+                    if stage == 1 else None)
+            oracle.zero_step(numel, world, min(stage, 2), bucket2, gdt, gdt, pdt,
+                             [bits(g) for g in g_all], ref_master, ref_m, ref_v, ref_params, o_hp, sc,
+                             allreduce_out=outs)
+            z2.step(g_all[rank].clone(), hp)
+            st = z2.scaler_state()
+            assert (st["scale"], st["counter"], st["t"]) == (sc.scale, sc.counter, sc.t), (step, st)
+            for got, ref in ((z2.local.master, ref_master), (z2.local.m, ref_m), (z2.local.v, ref_v)):
+                assert np.array_equal(bits(got)[:n2].view(np.uint32),
+                                      ref[rank * n2:(rank + 1) * n2].view(np.uint32)), step
+            p = bits(z2.local.params)
+            if stage == 3:
+                assert np.array_equal(p[:n2], ref_params[shard_flat2]), step
+            else:
+                assert np.array_equal(p[:z2.np], ref_params), step
         dist.barrier()
         dist.destroy_process_group()
         q.put((rank, "ok"))
