@@ -49,3 +49,21 @@ def test_our_line_keys():
             assert k in c["clocks"], k
     s1 = pc["qwen3_0.6b_fp16_w8_stage1"]["step_roofline"]
     assert s1["bytes_per_param"] == s1["ledger_bytes_per_param"] + 8 * 2  # the W*C all-reduce writes
+
+
+def test_sharded_line_keys():
+    """bench.py --sharded, one process on one GPU (NCCL with one rank): the
+    whole sharded step, collectives included, prints a complete line."""
+    res = subprocess.run([sys.executable, "bench.py", "--sharded", "--steps", "3", "--warmup", "3",
+                          "--e2e-steps", "2"], cwd=ROOT, capture_output=True, text=True, timeout=900)
+    assert res.returncode == 0, res.stderr[-2000:]
+    lines = [l for l in res.stdout.strip().splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for k in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+              "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config", "roofline",
+              "e2e", "gpu_launches", "clocks"):
+        assert k in d, k
+    assert d["n_gpus"] == 1 and d["steps"] == 3 and d["value"] > 0 and d["scaling"] == "strong"
+    assert d["config"]["parallelism"] == "zero2_dp1" and d["gpu_launches"] == 3 * 3
+    assert d["e2e"]["h2d_bytes_per_step"] > 0 and d["e2e"]["d2h_bytes_per_step"] > 0

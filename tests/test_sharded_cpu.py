@@ -177,3 +177,57 @@ def test_sharded_schedule_matches_oracle_two_ranks(stage, gdt):
     for r in range(2):
         assert res[r] == "ok", f"rank {r}:\n{res[r]}"
     assert all(p.exitcode == 0 for p in procs)
+
+
+def _worker_leaves(rank, world, port, q):
+    """Both ranks step once; rank 1 then leaves between steps (its process
+    ends, nothing of it in flight). Rank 0's next step must end with an
+    error from its first collective, within the process group's timeout,
+    not hang."""
+    import time
+    from datetime import timedelta
+    try:
+        os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+        import torch.distributed as dist
+        dist.init_process_group("gloo", rank=rank, world_size=world, timeout=timedelta(seconds=10))
+        import workloads as wl
+        from _oracle_shard import OracleShard
+        from mixed_precision_gb300.engine import Hparams
+        from mixed_precision_gb300.sharded import ShardedZeroStep
+
+        z = ShardedZeroStep(SHAPES, 2, 24_000, wl.BF16, wl.BF16, local=OracleShard)
+        numel = wl.numels(SHAPES)
+        z.init(wl.master_init(z.offsets, numel, z.np, 0.02, wl.master_seed(42)))
+        g = wl.flat_grads(z.offsets, numel, z.np, 1e-3, wl.grad_seed(43, rank), wl.BF16)
+        z.step(g.clone(), Hparams())
+        if rank == 1:
+            q.put((rank, "left"))
+            q.close()
+            q.join_thread()  # the message is sent before the process ends
+            os._exit(0)  # leaves between steps, no collective in flight
+        t0 = time.monotonic()
+        try:
+            z.step(g.clone(), Hparams())
+            q.put((rank, "no error"))
+        except Exception as e:  # the collective reports the missing peer
+            q.put((rank, f"error after {time.monotonic() - t0:.1f} s: {type(e).__name__}"))
+        q.close()
+        q.join_thread()
+        os._exit(0)
+    except Exception:
+        q.put((rank, traceback.format_exc()))
+
+
+def test_rank_leaving_ends_the_next_collective_with_an_error():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker_leaves, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = dict(q.get(timeout=120) for _ in range(2))
+    for p in procs:
+        p.join(timeout=60)
+    assert res[1] == "left", res
+    assert res[0].startswith("error after"), res
+    assert float(res[0].split()[2]) < 30.0, res
