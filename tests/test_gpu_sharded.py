@@ -315,3 +315,56 @@ def test_checkpoint_across_gpu_counts():
         ok = params_close(p[:npad], params, oracle.decode(params, pdt), oracle.decode(p[:npad], pdt),
                           b_flat, True)
         assert ok[L.real_mask().astype(bool)].all()
+
+
+def test_fullsize_two_ranks_equal_the_single_process_step():
+    """The full Qwen3-0.6B-shaped list (596M parameters), W = 2, ZeRO-2,
+    bf16: two sharded ranks (threads, host-barrier collectives) against the
+    library's single-process step on the same gradients. With clipping off
+    the clip coefficient is exactly 1 on both sides and a two-term sum has
+    one order, so every rank's master/m/v slice and the gathered parameters
+    equal the single-process step's bit for bit over two steps (the second
+    with every element's moments non-zero); the norms agree within 1e-6
+    (their partial sums are grouped differently)."""
+    from mixed_precision_gb300 import _abi as abi
+    from mixed_precision_gb300.engine import ZeroStep
+
+    w = wl.workload("qwen3_0.6b_bf16_w2", max_grad_norm=0.0)
+    numel = wl.numels(w.shapes)
+    hp = Hparams(max_grad_norm=0.0)
+    ref = ZeroStep(w.shapes, 2, 2, w.bucket_bytes, w.grad_dtype, w.param_dtype)
+    ref.allocate()
+    m0 = wl.master_init(ref.offsets, numel, ref.np, w.master_sigma, wl.master_seed(w.index),
+                        device="cuda")
+    ref.init(m0)
+    grads = [[wl.flat_grads(ref.offsets, numel, ref.np, w.grad_sigma, wl.grad_seed(w.index, r, s),
+                            w.grad_dtype, device="cuda") for r in range(2)] for s in range(2)]
+    for s in range(2):
+        ref.step(grads[s], hp)
+    torch.cuda.synchronize()
+    ref_st = ref.scaler_state()
+
+    def rank_job(rank, comm):
+        torch.cuda.set_device(0)
+        z = ShardedZeroStep(w.shapes, 2, w.bucket_bytes, w.grad_dtype, w.param_dtype, comm=comm)
+        z.init(m0)
+        for s in range(2):
+            z.step(grads[s][rank].clone(), hp)
+        torch.cuda.synchronize()
+        n = z.shard_elems
+        lo = rank * n
+        same = [torch.equal(mine[:n].view(torch.int32), full[lo:lo + n].view(torch.int32))
+                for mine, full in zip((z.local.master, z.local.m, z.local.v),
+                                      (ref.master, ref.m, ref.v))]
+        params_same = torch.equal(z.local.params[:z.np].view(torch.int16),
+                                  ref.params_flat[:ref.np].view(torch.int16))
+        st = z.scaler_state()
+        z.close()
+        return same, params_same, st
+
+    for same, params_same, st in _run_ranks(2, rank_job):
+        assert all(same) and params_same
+        assert st["t"] == ref_st["t"] == 2 and st["overflow"] == 0
+        assert abs(st["grad_norm"] - ref_st["grad_norm"]) <= 1e-6 * ref_st["grad_norm"]
+    assert abi.zero_layout_query(ref.handle).n_real == 596_049_920
+    ref.close()
