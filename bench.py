@@ -721,6 +721,10 @@ PER_CONFIG = [
     ("moe_3.9b_bf16_w4", {"stage": 2}),
     ("qwen3_0.6b_fp16_w8", {"stage": 1}),
     ("qwen3_0.6b_fp16_w8", {"stage": 2}),
+    # the speculative step where clipping stays off: one pass, the step's
+    # whole ledger (the default line's workload clips every step)
+    ("qwen3_0.6b_bf16_w2", {"max_grad_norm": 0.0, "speculative": True}),
+    ("moe_3.9b_bf16_w4", {"max_grad_norm": 0.0, "speculative": True}),
 ]
 
 
@@ -744,19 +748,22 @@ def stage_bytes(w) -> dict:
 
 
 def time_config(name: str, over: dict, steps: int, warmup: int, local: int) -> dict:
-    """One named workload through zero_step: its own buffers, seeded inputs,
-    warm-up, K timed steps with per-kernel events and sampled clocks. Frees
-    every buffer before it returns."""
+    """One named workload through zero_step (or, with over["speculative"],
+    zero_step_speculative): its own buffers, seeded inputs, warm-up, K timed
+    steps with per-kernel events and sampled clocks. Frees every buffer
+    before it returns."""
     import torch
 
     import workloads as wl
     from mixed_precision_gb300.engine import Hparams, ZeroStep
 
     device = torch.device("cuda", local)
+    over = dict(over)
+    speculative = over.pop("speculative", False)
     w = wl.workload(name, **over)
     z = ZeroStep(w.shapes, w.world, w.stage, w.bucket_bytes, w.grad_dtype, w.param_dtype,
                  w.comm_dtype)
-    z.allocate()
+    z.allocate(speculative=speculative)
     numel = wl.numels(w.shapes)
     master0 = wl.master_init(z.offsets, numel, z.np, w.master_sigma, wl.master_seed(w.index),
                              device=device)
@@ -768,7 +775,8 @@ def time_config(name: str, over: dict, steps: int, warmup: int, local: int) -> d
              for r in range(w.world)]
     hp = Hparams(lr=w.lr, beta1=w.beta1, beta2=w.beta2, eps=w.eps, weight_decay=w.weight_decay,
                  max_grad_norm=w.max_grad_norm)
-    tm = timed_steps(z, lambda: z.step(grads, hp), steps, warmup, local)
+    step = (lambda: z.step_speculative(grads, hp)) if speculative else (lambda: z.step(grads, hp))
+    tm = timed_steps(z, step, steps, warmup, local)
     st = z.scaler_state()
     assert st["overflow"] == 0 and st["steps"] == steps + warmup, st
     N = w.n_real
@@ -776,6 +784,38 @@ def time_config(name: str, over: dict, steps: int, warmup: int, local: int) -> d
     b = stage_bytes(w)
     step_s = tm["total_ms"] / 1e3 / steps
     k1_ms, k3_ms = statistics.mean(tm["k1"]), statistics.mean(tm["k3"])
+    if speculative:
+        # events: [single pass, its finalize in its last block] [between]
+        # [guarded fallback kernels: no-ops when the step committed]
+        assert st["fast_path"] == 1, st
+        one_pass = b["ledger"]
+        out = {
+            "config": config_of(w, "speculative single pass, clipping off"),
+            "steps": steps, "warmup": warmup,
+            "ms_per_step": tm["total_ms"] / steps,
+            "step_ms_median": tm["steps_ms"][steps // 2],
+            "value": N / step_s, "unit": "params/s",
+            "step_roofline": {"bytes_per_param": b["own"], "ledger_bytes_per_param": b["ledger"],
+                              "hbm_gbs": b["own"] * N / step_s / 1e9, "peak_gbs": peak,
+                              "frac": b["own"] * N / step_s / 1e9 / peak, "peak_source": peak_src,
+                              "impl_bytes_per_param": one_pass, "impl_ceiling": 1.0},
+            "kernels_ms": {"k_spec_step": k1_ms, "between": statistics.mean(tm["k2"]),
+                           "guarded_fallback": k3_ms,
+                           "k_spec_step_gbs": one_pass * N / (k1_ms / 1e3) / 1e9},
+            "fast_path": st["fast_path"],
+            "clocks": tm["clocks"],
+        }
+        achieved = one_pass * N / (k1_ms / 1e3) / 1e9
+        tr = NCU_TRAFFIC_PER_ELEM.get(("k_spec_step", w.name))
+        out["roofline"] = {"bound": "hbm", "kernel": "k_spec_step", "achieved": achieved,
+                           "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                           "traffic": tr * N if tr is not None else None,
+                           "algorithmic_bytes_per_launch": one_pass * N, "peak_source": peak_src}
+        z.close()
+        del grads, z
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+        return out
     out = {
         "config": config_of(w),
         "steps": steps, "warmup": warmup,
@@ -814,7 +854,10 @@ def per_config(steps: int, warmup: int, local: int) -> dict:
     """Every workload of PER_CONFIG, one after the other."""
     out = {}
     for name, over in PER_CONFIG:
-        key = name + "".join(f"_{k}{v}" for k, v in over.items())
+        if over.get("speculative"):
+            key = name + "_speculative_clip0"
+        else:
+            key = name + "".join(f"_{k}{v}" for k, v in over.items())
         out[key] = time_config(name, over, steps, warmup, local)
     return out
 

@@ -41,10 +41,14 @@ def test_our_line_keys():
     # the other named workloads, each with its own bytes per step
     pc = d["per_config"]
     assert set(pc) == {"moe_3.9b_bf16_w4_stage2", "qwen3_0.6b_fp16_w8_stage1",
-                       "qwen3_0.6b_fp16_w8_stage2"}
+                       "qwen3_0.6b_fp16_w8_stage2", "qwen3_0.6b_bf16_w2_speculative_clip0",
+                       "moe_3.9b_bf16_w4_speculative_clip0"}
     for name, c in pc.items():
         assert c["steps"] == 3 and c["ms_per_step"] > 0 and 0 < c["step_roofline"]["frac"] < 1.5
-        assert c["config"]["workload"] == name.rsplit("_stage", 1)[0]
+        assert c["config"]["workload"] == name.rsplit("_stage", 1)[0].split("_speculative")[0]
+        assert "roofline" in c
+    for name in ("qwen3_0.6b_bf16_w2_speculative_clip0", "moe_3.9b_bf16_w4_speculative_clip0"):
+        assert pc[name]["fast_path"] == 1 and pc[name]["config"]["clip"] == 0.0
         for k in ("sm_mhz", "sm_max_mhz", "reasons"):
             assert k in c["clocks"], k
     s1 = pc["qwen3_0.6b_fp16_w8_stage1"]["step_roofline"]
