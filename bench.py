@@ -352,10 +352,12 @@ def timed_steps(z, do_step, K: int, W: int, local: int, dist=None, device=None,
                 profile_range: bool = False) -> dict:
     """W untimed warm-up steps, then K steps bracketed by a barrier and
     synchronize() on both sides and timed with CUDA events on the launching
-    stream. The library records four events around its own launches in every
-    timed step (zero_set_step_events). Returns the timed region (max over
-    ranks), per-step durations, the per-kernel intervals and the clocks
-    sampled meanwhile."""
+    stream, with nothing else enqueued between the steps' kernels (an event
+    between two kernels would keep the second from starting while the first
+    finishes). Then K more steps in which the library records four events
+    around its own launches (zero_set_step_events), for the per-kernel
+    times. Returns the first region (max over ranks), per-step durations and
+    per-kernel intervals from the second, and the clocks sampled over both."""
     import torch
 
     from mixed_precision_gb300 import _abi as abi
@@ -378,16 +380,19 @@ def timed_steps(z, do_step, K: int, W: int, local: int, dist=None, device=None,
         torch.cuda.cudart().cudaProfilerStart()
     t_start.record()
     for k in range(K):
-        abi.zero_set_step_events(z.handle, [e.cuda_event for e in ev[k]])
         do_step()
     t_end.record()
     if profile_range:
         torch.cuda.cudart().cudaProfilerStop()
     torch.cuda.synchronize()
+    local_ms = t_start.elapsed_time(t_end)
+    for k in range(K):  # the per-kernel times
+        abi.zero_set_step_events(z.handle, [e.cuda_event for e in ev[k]])
+        do_step()
+    torch.cuda.synchronize()
     abi.zero_set_step_events(z.handle, None)
     clocks = sampler.stop()
     barrier(dist, device)
-    local_ms = t_start.elapsed_time(t_end)
     return {"total_ms": max_over_ranks(dist, local_ms, device),
             "steps_ms": sorted(ev[k][0].elapsed_time(ev[k][3]) for k in range(K)),
             "k1": [ev[k][0].elapsed_time(ev[k][1]) for k in range(K)],
@@ -458,7 +463,7 @@ def run_ours(args) -> dict | None:
     total_ms, steps_ms, k1, k2, k3, clocks = (tm["total_ms"], tm["steps_ms"], tm["k1"], tm["k2"],
                                               tm["k3"], tm["clocks"])
     st = z.scaler_state()
-    assert st["overflow"] == 0 and st["steps"] == K + W, st
+    assert st["overflow"] == 0 and st["steps"] == 2 * K + W, st  # timed, then kernel-timed
     # the speculative step commits on the fast path unless clipping is active
     fast_path = st["fast_path"] if args.speculative else None
 
@@ -482,7 +487,7 @@ def run_ours(args) -> dict | None:
         r1.record()
         torch.cuda.synchronize()
         st_g = z.scaler_state()
-        assert st_g["overflow"] == 0 and st_g["steps"] == K + W + 3 + K, st_g
+        assert st_g["overflow"] == 0 and st_g["steps"] == 2 * K + W + 3 + K, st_g
         graph = {"ms_per_step": r0.elapsed_time(r1) / K, "steps": K,
                  "value": job_value(info.n_real, world, r0.elapsed_time(r1) / 1e3 / K)}
         del g
@@ -778,7 +783,7 @@ def time_config(name: str, over: dict, steps: int, warmup: int, local: int) -> d
     step = (lambda: z.step_speculative(grads, hp)) if speculative else (lambda: z.step(grads, hp))
     tm = timed_steps(z, step, steps, warmup, local)
     st = z.scaler_state()
-    assert st["overflow"] == 0 and st["steps"] == steps + warmup, st
+    assert st["overflow"] == 0 and st["steps"] == 2 * steps + warmup, st
     N = w.n_real
     peak, peak_src = hbm_peak()
     b = stage_bytes(w)

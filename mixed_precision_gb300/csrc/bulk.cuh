@@ -68,4 +68,18 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
   return false;
 }
 
+// Programmatic dependent launch (sm_90+). A kernel launched with the
+// programmatic-stream-serialization attribute may start before the kernel
+// ahead of it in the stream has finished; griddep_wait() then blocks until
+// that kernel has completed and its memory is visible, exactly the ordering
+// of a plain launch. Every step kernel calls it before its first global
+// access, then griddep_trigger(): once every block of this kernel has
+// started, the next kernel's blocks may be scheduled (into the slots this
+// kernel's finishing blocks free) and run up to their own wait. Without the
+// attribute both instructions do nothing.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 }  // namespace zg

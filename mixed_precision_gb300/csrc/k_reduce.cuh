@@ -88,6 +88,8 @@ __device__ __forceinline__ void add_group(float ss, float& hi, float& lo, double
 
 template <typename GT, typename CT, int WT, bool STAGE1>
 __global__ void __launch_bounds__(kThreads, 4) k_reduce_norm(const __grid_constant__ ReduceArgs a) {
+  griddep_wait();
+  griddep_trigger();
   if (a.state->error || (a.guarded && !a.state->need_fallback)) return;
   // Vectors in flight per thread: keep up to eight 16-byte gradient loads
   // outstanding (at most four vectors, to stay within 64 registers).
@@ -196,6 +198,8 @@ __global__ void __launch_bounds__(kThreads, 4) k_reduce_norm(const __grid_consta
 template <typename GT, typename CT, int WT, bool STAGE1, int NC>
 __global__ void __launch_bounds__((NC + 1) * 32)
     k_reduce_norm_ws(const __grid_constant__ ReduceArgs a) {
+  griddep_wait();
+  griddep_trigger();
   if (a.state->error || (a.guarded && !a.state->need_fallback)) return;
   constexpr int S = kRedStages;
   extern __shared__ __align__(128) unsigned char smem[];

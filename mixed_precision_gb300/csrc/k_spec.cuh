@@ -57,6 +57,8 @@ __global__ void __launch_bounds__((NC + 1) * 32) k_spec_step(const __grid_consta
   const int kGrad = W * C * (int)sizeof(GT);
   const int kStage = kGrad + 12 * C;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  griddep_wait();
+  griddep_trigger();
   const DevState* st = a.state;
   if (st->error) return;
   if (st->predict_fallback) {  // predicted to clip: the two-pass kernels run instead

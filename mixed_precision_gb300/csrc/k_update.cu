@@ -1,11 +1,43 @@
 // K2 (the one-block finalize, for the paths that do not fuse it into K1), K3
 // (fused unscale / clip / AdamW / cast-out), the launch dispatch of K1, and
 // the speculative pass's launch.
+#include <cstdlib>
+
 #include "bulk.cuh"
 #include "finalize.cuh"
 #include "vec.cuh"
 
 namespace zg {
+
+// Launches of the step kernels: with programmatic dependent launch (the
+// default; ZERO_PDL=0 in the environment turns it off) a kernel's blocks may
+// be scheduled while the kernel ahead of it finishes; each kernel waits for
+// that kernel's completion before touching memory (griddep_wait), so results
+// are those of plain stream order.
+static bool pdl_on() {
+  static const bool on = [] {
+    const char* v = std::getenv("ZERO_PDL");
+    return v == nullptr || std::atoi(v) != 0;
+  }();
+  return on;
+}
+
+cudaError_t launch_step_kernel(const void* f, int grid, int threads, void** args, int smem,
+                               cudaStream_t s) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = (size_t)smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  if (pdl_on()) {
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  return cudaLaunchKernelExC(&cfg, f, args);
+}
 
 const void* reduce_kernel_f32(int comm_dtype, int world, int stage, int variant);
 const void* reduce_kernel_f16(int comm_dtype, int world, int stage, int variant);
@@ -41,8 +73,8 @@ cudaError_t launch_reduce(const ReduceArgs& a, int grid, int variant, cudaStream
   const void* f = reduce_kernel(a.grad_dtype, a.comm_dtype, a.world, a.stage, variant);
   if (f == nullptr) return cudaErrorInvalidValue;
   void* args[] = {const_cast<ReduceArgs*>(&a)};
-  return cudaLaunchKernel(f, dim3(grid), dim3(reduce_threads(variant)), args,
-                          reduce_smem(a.world, a.grad_dtype, variant, a.chunk), s);
+  return launch_step_kernel(f, grid, reduce_threads(variant), args,
+                            reduce_smem(a.world, a.grad_dtype, variant, a.chunk), s);
 }
 
 int reduce_blocks_per_sm(int grad_dtype, int comm_dtype, int world, int stage, int variant,
@@ -128,6 +160,8 @@ cudaError_t launch_state_init(const ScalerCfg& cfg, DevState* st, int* hint, cud
 // ---------------------------------------------------------------------------
 template <typename CT, typename PT>
 __global__ void __launch_bounds__(kThreads) k_adamw_cast(const __grid_constant__ UpdateArgs a) {
+  griddep_wait();
+  griddep_trigger();
   const DevState* st = a.state;
   if (st->skip || st->error) return;
   const AdamScalars sc = AdamScalars::from(st);
@@ -233,6 +267,8 @@ __global__ void __launch_bounds__((NC + 1) * 32)
   __shared__ ChunkDesc desc[S];
   constexpr int kStage = UpdStage<CT>::bytes(C);
 
+  griddep_wait();
+  griddep_trigger();
   const DevState* st = a.state;
   if (a.restore && st->restore_params && !st->error) {
     // The speculative step overflowed: its single pass wrote the parameters,
@@ -443,8 +479,8 @@ cudaError_t launch_update(const UpdateArgs& a, int grid, int variant, cudaStream
   const void* f = update_kernel(a.comm_dtype, a.param_dtype, variant);
   if (f == nullptr) return cudaErrorInvalidValue;
   void* args[] = {const_cast<UpdateArgs*>(&a)};
-  return cudaLaunchKernel(f, dim3(grid), dim3(update_threads(variant)), args,
-                          update_smem(a.comm_dtype, variant), s);
+  return launch_step_kernel(f, grid, update_threads(variant), args,
+                            update_smem(a.comm_dtype, variant), s);
 }
 
 int update_blocks_per_sm(int comm_dtype, int param_dtype, int variant) {
@@ -501,8 +537,8 @@ cudaError_t launch_spec(const SpecArgs* args, int grad_dtype, int comm_dtype, in
   const void* f = spec_kernel(grad_dtype, comm_dtype, param_dtype, world);
   if (f == nullptr) return cudaErrorInvalidValue;
   void* a[] = {const_cast<SpecArgs*>(args)};
-  return cudaLaunchKernel(f, dim3(grid), dim3((kRedConsumers + 1) * 32), a,
-                          spec_smem(world, grad_dtype, args->chunk), s);
+  return launch_step_kernel(f, grid, (kRedConsumers + 1) * 32, a,
+                            spec_smem(world, grad_dtype, args->chunk), s);
 }
 
 int spec_blocks_per_sm(int grad_dtype, int comm_dtype, int param_dtype, int world, int chunk) {
