@@ -523,8 +523,9 @@ int zero_scaler_restore(zero_layout_t* layout, const zero_scaler_state* st, void
  *                          elements, this rank's slices.
  * zero_state_init then initialises this rank's slices only (master_init_flat
  * is still the whole flat buffer): all-gather the parameters once after it.
- * Requires comm_dtype == grad_dtype (the collectives reduce in the gradient
- * dtype). ZERO_ERR_STATE if called twice or after bind; every entry point
+ * Requires comm_dtype == grad_dtype, or ZERO_F32 with 16-bit gradients (the
+ * collectives reduce in the communication dtype; zero_dist_widen gives the
+ * fp32 copy to reduce). ZERO_ERR_STATE if called twice or after bind; every entry point
  * that steps all W ranks in one process (zero_step*, accumulation, gathers)
  * then returns ZERO_ERR_STATE. zero_state_export / import and
  * zero_state_export_params / import_params move this rank's elements only:
@@ -533,6 +534,13 @@ int zero_scaler_restore(zero_layout_t* layout, const zero_scaler_state* st, void
  * included); an import reads them from a whole buffer, which may come from a
  * job of any W, stage or bucket size. Host only. */
 int zero_dist_set_rank(zero_layout_t* layout, int rank);
+
+/* With an fp32 comm_dtype and 16-bit gradients ([ND] "9. Experimental
+ * Results": communication_data_type): out[i] = fp32(grads[i]) for the whole
+ * flat buffer, i < Np (exact), the buffer this rank then reduce-scatters (or,
+ * stage 1, all-reduces) in fp32. grads: device, Np elements of grad_dtype;
+ * out: device, Np floats; both 16-byte aligned. */
+int zero_dist_widen(zero_layout_t* layout, const void* grads, float* out, void* stream);
 
 /* This rank's share of the global norm and overflow check: enqueues a kernel
  * that writes norm_pair[0] = sum of r^2 over this rank's real elements (fp64

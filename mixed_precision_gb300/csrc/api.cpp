@@ -1366,9 +1366,9 @@ static int dist_set_rank(zero_layout_t* L, int rank) {
     return fail(ZERO_ERR_INVALID, "rank %d outside 0..%d", rank, L->world() - 1);
   if (L->sharded()) return fail(ZERO_ERR_STATE, "zero_dist_set_rank was already called");
   if (L->dblock != nullptr) return fail(ZERO_ERR_STATE, "zero_dist_set_rank must come before zero_state_bind");
-  if (L->comm_dtype != L->cfg.grad_dtype)
-    return fail(ZERO_ERR_INVALID, "the sharded step needs comm_dtype == grad_dtype (the "
-                "collectives reduce the gradients in their own dtype)");
+  if (L->comm_dtype != L->cfg.grad_dtype && L->comm_dtype != ZERO_F32)
+    return fail(ZERO_ERR_INVALID, "the sharded step needs comm_dtype == grad_dtype or ZERO_F32 "
+                "(the collectives reduce in the communication dtype; widening to fp32 is exact)");
   // This rank's tiles, in the same order, with shard offsets relative to the
   // start of its own slice of the rank-major buffers.
   const int64_t base = (int64_t)rank * (L->np / L->world());
@@ -1413,6 +1413,23 @@ static int check_dist(zero_layout_t* L, const void* allreduced) {
   } else if (allreduced != nullptr) {
     return fail(ZERO_ERR_INVALID, "stages 2/3 read the bound scratch: allreduced must be NULL");
   }
+  return ZERO_OK;
+}
+
+int zero_dist_widen(zero_layout_t* L, const void* grads, float* out, void* stream) {
+  Range r_entry("zero_dist_widen");
+  if (int rc = check_ready(L, false)) return rc;
+  if (!L->sharded()) return fail(ZERO_ERR_STATE, "zero_dist_set_rank has not been called");
+  if (L->cfg.grad_dtype == ZERO_F32 || L->comm_dtype != ZERO_F32)
+    return fail(ZERO_ERR_INVALID, "zero_dist_widen is for 16-bit gradients and an fp32 comm_dtype");
+  if (grads == nullptr || out == nullptr || !aligned16(grads) || !aligned16(out))
+    return fail(ZERO_ERR_INVALID, "grads/out NULL or not 16-byte aligned");
+  if (L->np == 0) return ZERO_OK;
+  const int grid = (int)std::max<int64_t>(
+      1, std::min<int64_t>((L->np / 8 + kThreads - 1) / kThreads, (int64_t)L->sms * kMaxBlocksPerSm * 4));
+  cudaError_t e = launch_widen(grads, L->cfg.grad_dtype, out, L->np, grid,
+                               static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "widen launch");
   return ZERO_OK;
 }
 

@@ -225,6 +225,9 @@ cudaError_t launch_shard_norm(const Tile* tiles, int n_tiles, const void* red, i
                               double* pair, int grid, cudaStream_t s);
 cudaError_t launch_dist_finalize(const double* pair, int world, const Hparams& hp, DevState* st,
                                  cudaStream_t s);
+// out[i] = fp32(g[i]), i < n (16-bit gradients widened for an fp32 collective).
+cudaError_t launch_widen(const void* g, int grad_dtype, float* out, int64_t n, int grid,
+                         cudaStream_t s);
 cudaError_t launch_gather(const Tile* tiles, int n_tiles, const void* params_flat,
                           void* const* dst_table, int n_params, int n_replicas, int elem_bytes,
                           int src_by_shard, int grid, cudaStream_t s);

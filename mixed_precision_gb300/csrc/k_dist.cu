@@ -91,6 +91,34 @@ __global__ void k_dist_finalize(const double* __restrict__ pair, int world, cons
   finalize_state(pair[0], pair[1] != 0.0 ? 1u : 0u, world, hp, st);
 }
 
+// out[i] = fp32(g[i]) over a plain range (exact: every bf16 and fp16 value is
+// an fp32 value). 16-byte vectors of 8 elements, then the tail.
+template <typename GT>
+__global__ void __launch_bounds__(kThreads)
+    k_widen(const GT* __restrict__ g, float* __restrict__ out, int64_t n) {
+  const int64_t nvec = n >> 3;
+  for (int64_t v = (int64_t)blockIdx.x * kThreads + threadIdx.x; v < nvec;
+       v += (int64_t)gridDim.x * kThreads) {
+    float x[8];
+    load8(g + v * 8, x);
+    store8_f32(out + v * 8, x);
+  }
+  for (int64_t i = nvec * 8 + (int64_t)blockIdx.x * kThreads + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * kThreads)
+    out[i] = DT<GT>::to_f32(g[i]);
+}
+
+cudaError_t launch_widen(const void* g, int grad_dtype, float* out, int64_t n, int grid,
+                         cudaStream_t s) {
+  if (grad_dtype == kF16)
+    k_widen<__half><<<grid, kThreads, 0, s>>>(static_cast<const __half*>(g), out, n);
+  else if (grad_dtype == kBF16)
+    k_widen<__nv_bfloat16><<<grid, kThreads, 0, s>>>(static_cast<const __nv_bfloat16*>(g), out, n);
+  else
+    return cudaErrorInvalidValue;
+  return cudaGetLastError();
+}
+
 cudaError_t launch_shard_norm(const Tile* tiles, int n_tiles, const void* red, int comm_dtype,
                               int by_flat, double* part, unsigned* part_ovf, DevState* st,
                               double* pair, int grid, cudaStream_t s) {

@@ -71,8 +71,11 @@ class LibraryShard:
         self.v = torch.empty(n_shard, dtype=torch.float32, device=dev)
         n_params = n_shard if z.stage == 3 else max(z.np, 8)
         self.params = torch.empty(n_params, dtype=TORCH_DTYPE[z.param_dtype], device=dev)
-        self.scratch = (torch.empty(n_shard, dtype=TORCH_DTYPE[z.grad_dtype], device=dev)
+        self.scratch = (torch.empty(n_shard, dtype=TORCH_DTYPE[z.comm_dtype], device=dev)
                         if z.stage != 1 else None)
+        # an fp32 collective of 16-bit gradients: this rank's widened copy
+        self.comm_buf = (torch.empty(max(z.np, 8), dtype=torch.float32, device=dev)
+                         if z.comm_dtype != z.grad_dtype else None)
         self.norm_pair = torch.zeros(2, dtype=torch.float64, device=dev)
         abi.zero_state_bind(z.handle, self.master.data_ptr(), self.m.data_ptr(), self.v.data_ptr(),
                             self.params.data_ptr(),
@@ -84,6 +87,14 @@ class LibraryShard:
 
     def init(self, master_init_flat: torch.Tensor, cfg: abi.zero_scaler_cfg) -> None:
         abi.zero_state_init(self.z.handle, master_init_flat.data_ptr(), cfg, self._stream())
+
+    def to_comm(self, grads: torch.Tensor) -> torch.Tensor:
+        """The buffer the collectives reduce: the gradients themselves, or
+        their exact fp32 widening when the communication dtype is fp32."""
+        if self.comm_buf is None:
+            return grads
+        abi.zero_dist_widen(self.z.handle, grads.data_ptr(), self.comm_buf.data_ptr(), self._stream())
+        return self.comm_buf
 
     def shard_norm(self, allreduced) -> None:
         abi.zero_dist_shard_norm(self.z.handle, allreduced.data_ptr() if allreduced is not None else 0,
@@ -129,13 +140,16 @@ class ShardedZeroStep:
 
     def __init__(self, shapes, stage: int = 2, bucket_bytes: int = 500_000_000,
                  grad_dtype: int = abi.ZERO_BF16, param_dtype: int = abi.ZERO_BF16, comm=None,
-                 local=None, device="cuda"):
+                 local=None, device="cuda", comm_dtype: int = -1):
         self.comm = comm if comm is not None else TorchComm()
         self.rank, self.world = self.comm.rank, self.comm.world
         self.shapes = [tuple(int(d) for d in s) for s in shapes]
         self.stage, self.grad_dtype, self.param_dtype = stage, grad_dtype, param_dtype
+        # the collectives' dtype: the gradients' own, or fp32 (abi.ZERO_F32)
+        self.comm_dtype = grad_dtype if comm_dtype < 0 else comm_dtype
         self.bucket_bytes = int(bucket_bytes)
-        cfg = abi.zero_config(self.world, stage, int(bucket_bytes), grad_dtype, param_dtype, -1, 0)
+        cfg = abi.zero_config(self.world, stage, int(bucket_bytes), grad_dtype, param_dtype,
+                              self.comm_dtype, 0)
         self.handle = abi.zero_layout_create(self.shapes, cfg)
         abi.zero_dist_set_rank(self.handle, self.rank)
         self.info = abi.zero_layout_query(self.handle)
@@ -169,21 +183,23 @@ class ShardedZeroStep:
     def step(self, grads: torch.Tensor, hp: Hparams) -> None:
         """One step from this rank's gradients (flat layout, Np elements of the
         gradient dtype). Stages 2/3: reduce-scatter bucket by bucket into this
-        rank's scratch. Stage 1: all-reduce bucket by bucket, in place on
-        `grads` (they hold the summed gradient afterwards). Then this rank's
+        rank's scratch. Stage 1: all-reduce bucket by bucket, in place (on
+        `grads`, which then hold the summed gradient, or on the fp32 copy
+        with an fp32 communication dtype). Then this rank's
         norm share, its all-reduce, the finalize, the local update, and the
         all-gather of the parameters (stages 1/2)."""
         W = self.world
         allreduced = None
+        src = self.local.to_comm(grads)
         for b in self.buckets:
-            g = grads[b.start:b.start + b.length]
+            g = src[b.start:b.start + b.length]
             if self.stage == 1:
                 self.comm.all_reduce(g)
             else:
                 n = b.slice_len(W)
                 self.comm.reduce_scatter(self.local.scratch[b.local:b.local + n], g)
         if self.stage == 1:
-            allreduced = grads
+            allreduced = src
         self.local.shard_norm(allreduced)
         self.comm.all_reduce(self.local.norm_pair)
         self.local.finalize(hp)

@@ -34,7 +34,7 @@ class OracleShard:
         self.v = torch.zeros_like(self.master)
         n_params = n_shard if z.stage == 3 else z.np
         self.params = torch.zeros(max(n_params, 8), dtype=TORCH_DTYPE[z.param_dtype])
-        self.scratch = (torch.zeros(max(n_shard, 8), dtype=TORCH_DTYPE[z.grad_dtype])
+        self.scratch = (torch.zeros(max(n_shard, 8), dtype=TORCH_DTYPE[z.comm_dtype])
                         if z.stage != 1 else None)
         self.norm_pair = torch.zeros(2, dtype=torch.float64)
         # flat index of every position of this rank's shard, and which are real
@@ -59,6 +59,13 @@ class OracleShard:
                                     growth_factor=cfg.growth_factor,
                                     backoff_factor=cfg.backoff_factor, min_scale=cfg.min_scale)
 
+    def to_comm(self, grads):
+        """The buffer the collectives reduce (fp32 comm: the exact widening,
+        by the oracle's own decode)."""
+        if self.z.comm_dtype == self.z.grad_dtype:
+            return grads
+        return torch.from_numpy(oracle.decode(bits(grads.contiguous()), self.z.grad_dtype))
+
     def _local_reduced(self, allreduced) -> np.ndarray:
         """This rank's reduced values in shard order; padding read as zero."""
         src = bits(allreduced)[self.flat] if allreduced is not None else \
@@ -68,7 +75,7 @@ class OracleShard:
 
     def shard_norm(self, allreduced) -> None:
         r = self._local_reduced(allreduced)
-        o, s = oracle.overflow_sumsq(r, self.z.grad_dtype, self.real.astype(np.uint8))
+        o, s = oracle.overflow_sumsq(r, self.z.comm_dtype, self.real.astype(np.uint8))
         self.norm_pair[0] = s
         self.norm_pair[1] = 1.0 if o else 0.0
 
@@ -84,7 +91,7 @@ class OracleShard:
         n = self.z.shard_elems
         r = self._local_reduced(allreduced)
         ms, mm, vv = (bits(t)[:n] for t in (self.master, self.m, self.v))
-        oracle.adamw(r, self.z.grad_dtype, self.hp, self.info, ms, mm, vv)
+        oracle.adamw(r, self.z.comm_dtype, self.hp, self.info, ms, mm, vv)
         self._cast_params()
 
     def _cast_params(self) -> None:

@@ -231,7 +231,7 @@ def test_last_error_is_set(zlib):
 def test_dist_set_rank_partitions_the_tiles(zlib):
     """zero_dist_set_rank keeps exactly rank r's tiles: over all ranks the
     tables partition the full table. Rank out of range, a second call and a
-    communication dtype other than the gradient dtype are refused."""
+    16-bit communication dtype other than the gradients' are refused."""
     from mixed_precision_gb300 import _abi
     shapes = [(1000,), (77,), (300, 41), (8200,), (0,), (5,), (20000,)]
     for W in (1, 2, 3, 5):
@@ -259,8 +259,13 @@ def test_dist_set_rank_partitions_the_tiles(zlib):
             _abi.zero_dist_set_rank(h, bad)
         assert e.value.code == _abi.ZERO_ERR_INVALID
     zlib.zero_layout_destroy(h)
-    h = zlib.zero_layout_create(shapes, _cfg(zlib, 2, c=wl.F32))
+    # a 16-bit communication dtype other than the gradients' is refused; fp32 is not
+    h = zlib.zero_layout_create(shapes, _cfg(zlib, 2, c=wl.F16))
     with pytest.raises(zlib.ZeroError) as e:
         _abi.zero_dist_set_rank(h, 0)
     assert e.value.code == _abi.ZERO_ERR_INVALID
+    zlib.zero_layout_destroy(h)
+    h = zlib.zero_layout_create(shapes, _cfg(zlib, 2, c=wl.F32))
+    _abi.zero_dist_set_rank(h, 0)
+    assert zlib.zero_layout_query(h).scratch_bytes == zlib.zero_layout_query(h).shard_elems * 4
     zlib.zero_layout_destroy(h)

@@ -80,12 +80,13 @@ class ThreadComm:
 SHAPES = [(96, 40), (7,), (300, 33), (1,), (64, 64), (1000,), (0,), (129, 3), (8200,)]
 
 
-def _run_rank(rank, shared, stage, gdt, bucket, steps, hp):
+def _run_rank(rank, shared, stage, gdt, bucket, steps, hp, cdt=-1):
     torch.cuda.set_device(0)
     pdt = wl.F16 if gdt == wl.F16 else wl.BF16
     dynamic = gdt == wl.F16
     scale0 = 2.0 ** 10 if dynamic else 1.0
-    z = ShardedZeroStep(SHAPES, stage, bucket, gdt, pdt, comm=ThreadComm(shared, rank))
+    z = ShardedZeroStep(SHAPES, stage, bucket, gdt, pdt, comm=ThreadComm(shared, rank),
+                        comm_dtype=cdt)
     numel = wl.numels(SHAPES)
     master0 = wl.master_init(z.offsets, numel, z.np, 0.02, wl.master_seed(50)).cuda()
     z.init(master0, init_scale=scale0, dynamic=dynamic, growth_interval=3)
@@ -114,14 +115,18 @@ def _grads(z, numel, world, step, gdt, scale0):
     return g
 
 
-@pytest.mark.parametrize("world,stage,gdt", [(2, 2, wl.BF16), (3, 2, wl.F16), (4, 1, wl.BF16),
-                                             (2, 3, wl.F16), (4, 3, wl.BF16), (1, 2, wl.BF16)])
-def test_sharded_ranks_match_oracle(world, stage, gdt):
+@pytest.mark.parametrize("world,stage,gdt,cdt", [(2, 2, wl.BF16, -1), (3, 2, wl.F16, -1),
+                                                 (4, 1, wl.BF16, -1), (2, 3, wl.F16, -1),
+                                                 (4, 3, wl.BF16, -1), (1, 2, wl.BF16, -1),
+                                                 (3, 2, wl.BF16, wl.F32), (4, 1, wl.F16, wl.F32)])
+def test_sharded_ranks_match_oracle(world, stage, gdt, cdt):
+    """cdt F32: fp32 collectives of the widened 16-bit gradients."""
     bucket, steps = 24_000, 5
     hp = Hparams(max_grad_norm=0.05 if world == 4 else 1.0)  # clipping active at W = 4
     shared = _Shared(world)
     with concurrent.futures.ThreadPoolExecutor(world) as ex:
-        futs = [ex.submit(_run_rank, r, shared, stage, gdt, bucket, steps, hp) for r in range(world)]
+        futs = [ex.submit(_run_rank, r, shared, stage, gdt, bucket, steps, hp, cdt)
+                for r in range(world)]
         results = [f.result(timeout=600) for f in futs]
     per_rank = [r[0] for r in results]
 
@@ -150,8 +155,9 @@ def test_sharded_ranks_match_oracle(world, stage, gdt):
 
     for step in range(steps):
         g = [to_np(x) for x in _grads(_Z, numel, world, step, gdt, scale0)]
-        outs = [np.zeros(npad, oracle.storage_dtype(gdt)) for _ in range(world)] if stage == 1 else None
-        info = oracle.zero_step(numel, world, min(stage, 2), bucket, gdt, gdt, pdt, g, ms, mm, vv,
+        c_eff = gdt if cdt < 0 else cdt
+        outs = [np.zeros(npad, oracle.storage_dtype(c_eff)) for _ in range(world)] if stage == 1 else None
+        info = oracle.zero_step(numel, world, min(stage, 2), bucket, gdt, c_eff, pdt, g, ms, mm, vv,
                                 params, o_hp, sc, allreduce_out=outs)
         for h, x in zip(hist, (ms, mm, vv)):
             np.maximum(h, np.abs(x), out=h)

@@ -36,7 +36,7 @@ def _free_port():
 SHAPES = [(96, 40), (7,), (300, 33), (1,), (64, 64), (1000,), (0,), (129, 3)]
 
 
-def _worker(rank, world, port, stage, gdt, q):
+def _worker(rank, world, port, stage, gdt, q, cdt=-1):
     try:
         os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
         import torch
@@ -52,7 +52,8 @@ def _worker(rank, world, port, stage, gdt, q):
         dynamic = gdt == wl.F16
         scale0 = 2.0 ** 10 if dynamic else 1.0
         bucket = 24_000  # several buckets, parameters of several sizes in each
-        z = ShardedZeroStep(SHAPES, stage, bucket, gdt, pdt, local=OracleShard)
+        z = ShardedZeroStep(SHAPES, stage, bucket, gdt, pdt, local=OracleShard, comm_dtype=cdt)
+        cdt = z.comm_dtype
         numel = wl.numels(SHAPES)
         L = oracle.layout(numel, world, bucket, wl.ELEM_BYTES[gdt])
         assert z.np == L.np_total and len(z.buckets) == len(L.bucket_start) > 1
@@ -76,9 +77,9 @@ def _worker(rank, world, port, stage, gdt, q):
                      for w in range(world)]
             if step == 2:  # one non-finite value on one rank: every rank skips
                 g_all[1][z.offsets[2] + 5] = float("inf")
-            outs = ([np.zeros(z.np, oracle.storage_dtype(gdt)) for _ in range(world)]
+            outs = ([np.zeros(z.np, oracle.storage_dtype(cdt)) for _ in range(world)]
                     if stage == 1 else None)
-            info = oracle.zero_step(numel, world, min(stage, 2), bucket, gdt, gdt, pdt,
+            info = oracle.zero_step(numel, world, min(stage, 2), bucket, gdt, cdt, pdt,
                                     [bits(g) for g in g_all], ref_master, ref_m, ref_v, ref_params,
                                     o_hp, sc, allreduce_out=outs)
             mine = g_all[rank].clone()
@@ -123,7 +124,7 @@ def _worker(rank, world, port, stage, gdt, q):
         # ... and restarts a job with another bucket size, which then steps
         # like the oracle restarted from the same state
         bucket2 = 50_000
-        z2 = ShardedZeroStep(SHAPES, stage, bucket2, gdt, pdt, local=OracleShard)
+        z2 = ShardedZeroStep(SHAPES, stage, bucket2, gdt, pdt, local=OracleShard, comm_dtype=cdt)
         z2.init(torch.zeros(z2.np), init_scale=scale0, dynamic=dynamic, growth_interval=3)
         z2.import_params(*ex, scaler=z.scaler_state())
         L2 = oracle.layout(numel, world, bucket2, wl.ELEM_BYTES[gdt])
@@ -137,9 +138,9 @@ def _worker(rank, world, port, stage, gdt, q):
         for step in range(6, 8):
             g_all = [wl.flat_grads(z2.offsets, numel, z2.np, 1e-3 * scale0, wl.grad_seed(41, w, step),
                                    gdt) for w in range(world)]
-            outs = ([np.zeros(z2.np, oracle.storage_dtype(gdt)) for _ in range(world)]
+            outs = ([np.zeros(z2.np, oracle.storage_dtype(cdt)) for _ in range(world)]
                     if stage == 1 else None)
-            oracle.zero_step(numel, world, min(stage, 2), bucket2, gdt, gdt, pdt,
+            oracle.zero_step(numel, world, min(stage, 2), bucket2, gdt, cdt, pdt,
                              [bits(g) for g in g_all], ref_master, ref_m, ref_v, ref_params, o_hp, sc,
                              allreduce_out=outs)
             z2.step(g_all[rank].clone(), hp)
@@ -160,12 +161,15 @@ def _worker(rank, world, port, stage, gdt, q):
         q.put((rank, traceback.format_exc()))
 
 
-@pytest.mark.parametrize("stage,gdt", [(2, 2), (2, 1), (1, 2), (3, 2), (3, 1)])
-def test_sharded_schedule_matches_oracle_two_ranks(stage, gdt):
+@pytest.mark.parametrize("stage,gdt,cdt", [(2, 2, -1), (2, 1, -1), (1, 2, -1), (3, 2, -1), (3, 1, -1),
+                                           (2, 2, 0), (1, 1, 0)])
+def test_sharded_schedule_matches_oracle_two_ranks(stage, gdt, cdt):
+    """cdt 0: fp32 collectives of 16-bit gradients (each rank widens its
+    gradients, exactly, and the reduce-scatter or all-reduce runs in fp32)."""
     ctx = mp.get_context("spawn")
     q = ctx.Queue()
     port = _free_port()
-    procs = [ctx.Process(target=_worker, args=(r, 2, port, stage, gdt, q)) for r in range(2)]
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, stage, gdt, q, cdt)) for r in range(2)]
     for p in procs:
         p.start()
     res = {}
