@@ -707,10 +707,11 @@ def run_ours(args) -> dict | None:
         "checkpoint": checkpoint,
         "e2e": e2e,
         # two-pass: reduce (its last block finalizes) + update; speculative:
-        # single pass (finalizes) + guarded reduce + update + guarded restore,
-        # or, once the device has predicted clipping, the two-pass launches
+        # single pass (finalizes) + guarded reduce + guarded update (which also
+        # carries the parameter restore), or, once the device has predicted
+        # clipping, the two-pass launches
         "gpu_launches": K * ((2 * sum(1 for n in numel if n > 0) + 1) if args.per_tensor_launch
-                             else (4 if (args.speculative and fast_path) else 2)),
+                             else (3 if (args.speculative and fast_path) else 2)),
         "clocks": clocks,
     }
     z.close()
