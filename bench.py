@@ -40,18 +40,21 @@ L2_BYTES = 129 * 1000 * 1000
 # workload); a workload without a capture of its kernel reports null.
 NCU_TRAFFIC_PER_ELEM = {
     # update kernel, one block per tile (15,392 blocks), 8 Qwen3 layers,
-    # 125,847,552 elements: (1.762525 + 1.701564) GB
-    ("k_adamw_cast", "qwen3_0.6b_bf16_w2"): 27.526,
-    # reduce kernel, W=2, 1,216 blocks, the same slice: (0.504079 + 0.214487) GB
-    ("k_reduce_norm", "qwen3_0.6b_bf16_w2"): 5.710,
+    # 125,847,552 elements: (1.762588 + 1.701842) GB
+    ("k_adamw_cast", "qwen3_0.6b_bf16_w2"): 27.529,
+    # reduce kernel, W=2, 1,216 blocks, the same slice: (0.504079 + 0.214297) GB
+    ("k_reduce_norm", "qwen3_0.6b_bf16_w2"): 5.708,
     # update kernel, one block per tile (28,680 blocks), 2 MoE layers,
-    # 234,946,560 elements: (3.290662 + 3.229782) GB
-    ("k_adamw_cast", "moe_3.9b_bf16_w4"): 27.753,
-    # reduce kernel, W=4, 1,216 blocks, the same slice: (1.880804 + 0.448031) GB
+    # 234,946,560 elements: (3.290513 + 3.229704) GB
+    ("k_adamw_cast", "moe_3.9b_bf16_w4"): 27.752,
+    # reduce kernel, W=4, 1,216 blocks, the same slice: (1.880805 + 0.448101) GB
     ("k_reduce_norm", "moe_3.9b_bf16_w4"): 9.912,
-    # speculative single pass, W=2, 3,952 blocks, 8 Qwen3 layers:
-    # (2.0143 + 1.7090) GB / 125,847,552 elements
-    ("k_spec_step", "qwen3_0.6b_bf16_w2"): 29.59,
+    # speculative single pass, W=2, 26 blocks per SM and resident block,
+    # 8 Qwen3 layers: (2.014366 + 1.708428) GB
+    ("k_spec_step", "qwen3_0.6b_bf16_w2"): 29.582,
+    # speculative single pass, W=4, the same grid rule, 2 MoE layers:
+    # (4.700327 + 3.243320) GB
+    ("k_spec_step", "moe_3.9b_bf16_w4"): 33.810,
 }
 
 
@@ -731,6 +734,11 @@ PER_CONFIG = [
     # whole ledger (the default line's workload clips every step)
     ("qwen3_0.6b_bf16_w2", {"max_grad_norm": 0.0, "speculative": True}),
     ("moe_3.9b_bf16_w4", {"max_grad_norm": 0.0, "speculative": True}),
+    # the layout sweep's 2000 ragged tensors (1.69G elements): the flat step at
+    # W = 2 and 8, and at W = 8 the same step launched tensor by tensor
+    ("ragged_2000", {"world": 2}),
+    ("ragged_2000", {"world": 8}),
+    ("ragged_2000", {"world": 8, "per_tensor_launch": True}),
 ]
 
 
@@ -766,6 +774,7 @@ def time_config(name: str, over: dict, steps: int, warmup: int, local: int) -> d
     device = torch.device("cuda", local)
     over = dict(over)
     speculative = over.pop("speculative", False)
+    per_tensor_launch = over.pop("per_tensor_launch", False)
     w = wl.workload(name, **over)
     z = ZeroStep(w.shapes, w.world, w.stage, w.bucket_bytes, w.grad_dtype, w.param_dtype,
                  w.comm_dtype)
@@ -781,7 +790,12 @@ def time_config(name: str, over: dict, steps: int, warmup: int, local: int) -> d
              for r in range(w.world)]
     hp = Hparams(lr=w.lr, beta1=w.beta1, beta2=w.beta2, eps=w.eps, weight_decay=w.weight_decay,
                  max_grad_norm=w.max_grad_norm)
-    step = (lambda: z.step_speculative(grads, hp)) if speculative else (lambda: z.step(grads, hp))
+    if speculative:
+        step = lambda: z.step_speculative(grads, hp)  # noqa: E731
+    elif per_tensor_launch:
+        step = lambda: z.step_per_tensor_launch(grads, hp)  # noqa: E731
+    else:
+        step = lambda: z.step(grads, hp)  # noqa: E731
     tm = timed_steps(z, step, steps, warmup, local)
     st = z.scaler_state()
     assert st["overflow"] == 0 and st["steps"] == 2 * steps + warmup, st
@@ -823,7 +837,8 @@ def time_config(name: str, over: dict, steps: int, warmup: int, local: int) -> d
         torch.cuda.empty_cache()
         return out
     out = {
-        "config": config_of(w),
+        "config": config_of(w, "per-tensor launches: two kernels per parameter and the finalize"
+                            if per_tensor_launch else None),
         "steps": steps, "warmup": warmup,
         "ms_per_step": tm["total_ms"] / steps,
         "step_ms_median": tm["steps_ms"][steps // 2],
@@ -862,6 +877,9 @@ def per_config(steps: int, warmup: int, local: int) -> dict:
     for name, over in PER_CONFIG:
         if over.get("speculative"):
             key = name + "_speculative_clip0"
+        elif name == "ragged_2000":
+            key = f"{name}_w{over['world']}" + ("_per_tensor_launch" if over.get("per_tensor_launch")
+                                                 else "")
         else:
             key = name + "".join(f"_{k}{v}" for k, v in over.items())
         out[key] = time_config(name, over, steps, warmup, local)

@@ -8,6 +8,9 @@ benchmark times, on sampled outputs (see _fullsize.py).
 - MoE ~3.9B, W=4, bf16, 14 of 16 experts' gradients zero per rank and layer:
   sampled parity, and the per-tensor entry point (NULL for the zero experts)
   bit-identical to the flat one.
+- The layout sweep's 2000 ragged tensors (1.69G elements; 1 MB buckets at
+  W=2, 1 GB buckets at W=8): sampled parity of the flat step and of the step
+  launched tensor by tensor, which must also store the same reduced values.
 - The speculative step at full size, in the launch configuration
   `bench.py --speculative` times: fp16 W=8 (clipping inactive) commits, skips
   on +inf and commits again; Qwen3 bf16 W=2 at clip 1.0 (clipping active)
@@ -145,6 +148,40 @@ def test_fullsize_moe_w4_flat_and_tensors():
     assert torch.equal(z.params_flat.view(torch.int16), zt.params_flat.view(torch.int16))
     zt.close()
     z.close()
+
+
+@pytest.mark.parametrize("world,bucket", [(2, 1 << 20), (8, 1 << 30)])
+def test_fullsize_ragged_2000_flat_and_per_tensor_launch(world, bucket):
+    w = wl.workload("ragged_2000", world=world, bucket_bytes=bucket)
+    z, numel, master0 = _setup(w)
+    # the greedy packing: 955 buckets of 1 MB (a tensor larger than the bucket
+    # gets one of its own), or 4 of 1 GB
+    assert z.info.n_buckets == (955 if bucket == 1 << 20 else 4)
+    idx = sample_indices(z, numel, 100_000, 5)
+    so = SampledOracle(z, numel, master0, idx, w.init_scale, w.dynamic, w.growth_interval)
+    del master0
+    g = _grads(z, w, numel, 0)
+    hp = _hp(w)
+    z.step(g, hp)
+    torch.cuda.synchronize()
+    st = z.scaler_state()
+    info, red_at = so.step(g, hp)
+    assert info.clip_coef < 1.0  # clip 1.0 is active on this workload
+    so.check(st, info, red_at)
+    z.close()
+    del z
+    # the same step with two kernel launches per parameter: the same oracle
+    # step from the same initial state (its global reduce reused)
+    zt, _, master0 = _setup(w)
+    sot = SampledOracle(zt, numel, master0, idx, w.init_scale, w.dynamic, w.growth_interval)
+    del master0
+    zt.step_per_tensor_launch(g, hp)
+    torch.cuda.synchronize()
+    stt = zt.scaler_state()
+    sot.last_reduce = so.last_reduce
+    info_t, _ = sot.step_repeat(hp)
+    sot.check(stt, info_t, red_at)
+    zt.close()
 
 
 @pytest.mark.parametrize("name,plan", [
