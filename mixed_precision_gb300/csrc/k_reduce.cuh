@@ -194,10 +194,21 @@ __global__ void __launch_bounds__(kThreads, 4) k_reduce_norm(const __grid_consta
 // partials and runs finalize_state. A warp whose bounded wait gives up
 // records kErrWaitTimeout and leaves; the block then writes no partial (and
 // the step's finalize does not run: the error is reported instead).
+//
+// TABLE (per-tensor pointers, NULL entries allowed): the pointer table is
+// read once per tile, and a tile with NULL ranks is cut into longer chunks.
+// Its live ranks' slices share the stage's W * C elements, one after the
+// other in rank order, so a chunk is floor(W / live) * C elements (a tile
+// whose ranks are mostly idle moves more bytes per pipeline round trip). The
+// length depends on the tile alone, so the producer and the consumers cut
+// every tile alike. The consumers take a chunk of k * C elements as k
+// C-element stretches in order, with the warp slices of a C-element chunk,
+// so every thread adds the same groups to its norm partial in the same order
+// as in flat mode: the two modes give the same bits. The flat instance is
+// the same code with those branches compiled out.
 // ---------------------------------------------------------------------------
-template <typename GT, typename CT, int WT, bool STAGE1, int NC>
-__global__ void __launch_bounds__((NC + 1) * 32)
-    k_reduce_norm_ws(const __grid_constant__ ReduceArgs a) {
+template <typename GT, typename CT, int WT, bool STAGE1, int NC, bool TABLE>
+__device__ __forceinline__ void reduce_ws_body(const ReduceArgs& a) {
   griddep_wait();
   griddep_trigger();
   if (a.state->error || (a.guarded && !a.state->need_fallback)) return;
@@ -223,11 +234,26 @@ __global__ void __launch_bounds__((NC + 1) * 32)
   }
   __syncthreads();
 
+  // table mode: the ranks whose gradient for a tile is NULL, and the tile's
+  // chunk length
+  auto null_mask = [&](const Tile& t) -> uint64_t {
+    uint64_t mk = 0ull;
+    for (int w = 0; w < W; ++w)
+      if (grad_ptr<GT>(a, t, w) == nullptr) mk |= 1ull << w;
+    return mk;
+  };
+  auto chunk_len = [&](uint64_t nulls) -> int {
+    const int live = W - __popcll(nulls);
+    return live >= W ? C : C * (W / max(live, 1));
+  };
+
   if (warp == NC) {  // producer
     if (lane != 0) return;
     int pt = blockIdx.x, pc = 0;
     unsigned k = 0;
     bool ok = true;
+    uint64_t nulls = 0ull;
+    int tc = C;  // the current tile's chunk length
     while (pt < a.n_tiles) {
       const int s = (int)(k % S);
       if (k >= (unsigned)S && !mbar_wait(&empty[s], ((k / S) - 1) & 1u)) {
@@ -235,23 +261,44 @@ __global__ void __launch_bounds__((NC + 1) * 32)
         break;
       }
       const Tile tl = a.tiles[pt];
-      const int clen = min(C, tl.len - pc);
+      if constexpr (TABLE) {
+        if (pc == 0) {
+          nulls = null_mask(tl);
+          tc = chunk_len(nulls);
+        }
+      }
+      const int clen = min(tc, tl.len - pc);
       const int nb = clen & ~7;
       GT* base = reinterpret_cast<GT*>(smem + s * kStage);
-      uint32_t bytes = 0;
-      for (int w = 0; w < W; ++w)
-        if (nb > 0 && grad_ptr<GT>(a, tl, w) != nullptr) bytes += nb * (uint32_t)sizeof(GT);
-      if (bytes > 0) {
-        mbar_arrive_expect_tx(&full[s], bytes);
-        for (int w = 0; w < W; ++w) {
-          const GT* g = grad_ptr<GT>(a, tl, w);
-          if (g != nullptr) bulk_g2s(base + w * C, g + pc, nb * (int)sizeof(GT), &full[s]);
+      if constexpr (TABLE) {
+        const uint32_t bytes = (uint32_t)((W - __popcll(nulls)) * nb) * (uint32_t)sizeof(GT);
+        if (bytes > 0) {
+          mbar_arrive_expect_tx(&full[s], bytes);
+          GT* dst = base;
+          for (int w = 0; w < W; ++w) {
+            if ((nulls >> w) & 1ull) continue;
+            bulk_g2s(dst, grad_ptr<GT>(a, tl, w) + pc, nb * (int)sizeof(GT), &full[s]);
+            dst += tc;
+          }
+        } else {
+          mbar_arrive(&full[s]);
         }
       } else {
-        mbar_arrive(&full[s]);
+        uint32_t bytes = 0;
+        for (int w = 0; w < W; ++w)
+          if (nb > 0 && grad_ptr<GT>(a, tl, w) != nullptr) bytes += nb * (uint32_t)sizeof(GT);
+        if (bytes > 0) {
+          mbar_arrive_expect_tx(&full[s], bytes);
+          for (int w = 0; w < W; ++w) {
+            const GT* g = grad_ptr<GT>(a, tl, w);
+            if (g != nullptr) bulk_g2s(base + w * C, g + pc, nb * (int)sizeof(GT), &full[s]);
+          }
+        } else {
+          mbar_arrive(&full[s]);
+        }
       }
       ++k;
-      pc += C;
+      pc += tc;
       if (pc >= tl.len) {
         pc = 0;
         pt += gridDim.x;
@@ -271,55 +318,113 @@ __global__ void __launch_bounds__((NC + 1) * 32)
   unsigned bad = 0u;
   int ct = blockIdx.x, cc = 0;
   unsigned k = 0;
+  uint64_t nulls = 0ull;
+  int tc = C;
   while (ct < a.n_tiles) {
     const int s = (int)(k % S);
     const Tile tl = a.tiles[ct];
-    const int clen = min(C, tl.len - cc);
+    if constexpr (TABLE) {
+      if (cc == 0) {
+        nulls = null_mask(tl);
+        tc = chunk_len(nulls);
+      }
+    }
+    const int clen = min(tc, tl.len - cc);
     const int nb = clen & ~7;
     if (!__all_sync(0xffffffffu, mbar_wait(&full[s], (k / S) & 1u))) {
       if (lane == 0) atomicOr(a.error, kErrWaitTimeout);
       return;
     }
     const GT* base = reinterpret_cast<const GT*>(smem + s * kStage);
-    const int e_end = min(nb, (warp + 1) * per);
-    for (int e = warp * per + 8 * lane; e < e_end; e += 256) {
-      float acc[8];
-      if (grad_ptr<GT>(a, tl, 0) != nullptr) {
-        load8_smem(base + e, acc);
-      } else {
+    if constexpr (TABLE) {
+      for (int v0 = 0; v0 < nb; v0 += C) {
+        const int e_end = min(nb, v0 + (warp + 1) * per);
+        for (int e = v0 + warp * per + 8 * lane; e < e_end; e += 256) {
+          float acc[8];
+          const GT* src = base;  // the next live rank's slice; a NULL rank adds +0.0
+          if (!(nulls & 1ull)) {
+            load8_smem(src + e, acc);
+            src += tc;
+          } else {
 #pragma unroll
-        for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
-      }
+            for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
+          }
 #pragma unroll(WT ? WT : 1)
-      for (int w = 1; w < W; ++w) {
-        float x[8];
-        if (grad_ptr<GT>(a, tl, w) != nullptr) {
-          load8_smem(base + w * C + e, x);
+          for (int w = 1; w < W; ++w) {
+            float x[8];
+            if (!((nulls >> w) & 1ull)) {
+              load8_smem(src + e, x);
+              src += tc;
+            } else {
+#pragma unroll
+              for (int j = 0; j < 8; ++j) x[j] = 0.0f;
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) acc[j] = __fadd_rn(acc[j], x[j]);
+          }
+          // from here as in flat mode
+          Pack8<CT> rc;
+          float rf[8];
+          float ss = 0.0f;
+          bool fin = true;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            rc.e[j] = DT<CT>::from_f32(acc[j]);
+            rf[j] = DT<CT>::to_f32(rc.e[j]);
+            fin = fin && DT<CT>::finite_bits(rc.e[j]);
+            ss = __fmaf_rn(rf[j], rf[j], ss);
+          }
+          if (!fin) bad = 1u;
+          add_group(ss, hi, lo, big, rf);
+          if constexpr (STAGE1) {
+            for (int w = 0; w < W; ++w)
+              store8_raw(static_cast<CT*>(a.out.base[w]) + tl.flat + cc + e, rc);
+          } else {
+            store8_raw(static_cast<CT*>(a.out.base[0]) + tl.shard + cc + e, rc);
+          }
+        }
+      }
+    } else {
+      const int e_end = min(nb, (warp + 1) * per);
+      for (int e = warp * per + 8 * lane; e < e_end; e += 256) {
+        float acc[8];
+        if (grad_ptr<GT>(a, tl, 0) != nullptr) {
+          load8_smem(base + e, acc);
         } else {
 #pragma unroll
-          for (int j = 0; j < 8; ++j) x[j] = 0.0f;
+          for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
         }
+#pragma unroll(WT ? WT : 1)
+        for (int w = 1; w < W; ++w) {
+          float x[8];
+          if (grad_ptr<GT>(a, tl, w) != nullptr) {
+            load8_smem(base + w * C + e, x);
+          } else {
 #pragma unroll
-        for (int j = 0; j < 8; ++j) acc[j] = __fadd_rn(acc[j], x[j]);
-      }
-      Pack8<CT> rc;
-      float rf[8];
-      float ss = 0.0f;
-      bool fin = true;
+            for (int j = 0; j < 8; ++j) x[j] = 0.0f;
+          }
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        rc.e[j] = DT<CT>::from_f32(acc[j]);
-        rf[j] = DT<CT>::to_f32(rc.e[j]);
-        fin = fin && DT<CT>::finite_bits(rc.e[j]);
-        ss = __fmaf_rn(rf[j], rf[j], ss);
-      }
-      if (!fin) bad = 1u;
-      add_group(ss, hi, lo, big, rf);
-      if constexpr (STAGE1) {
-        for (int w = 0; w < W; ++w)
-          store8_raw(static_cast<CT*>(a.out.base[w]) + tl.flat + cc + e, rc);
-      } else {
-        store8_raw(static_cast<CT*>(a.out.base[0]) + tl.shard + cc + e, rc);
+          for (int j = 0; j < 8; ++j) acc[j] = __fadd_rn(acc[j], x[j]);
+        }
+        Pack8<CT> rc;
+        float rf[8];
+        float ss = 0.0f;
+        bool fin = true;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          rc.e[j] = DT<CT>::from_f32(acc[j]);
+          rf[j] = DT<CT>::to_f32(rc.e[j]);
+          fin = fin && DT<CT>::finite_bits(rc.e[j]);
+          ss = __fmaf_rn(rf[j], rf[j], ss);
+        }
+        if (!fin) bad = 1u;
+        add_group(ss, hi, lo, big, rf);
+        if constexpr (STAGE1) {
+          for (int w = 0; w < W; ++w)
+            store8_raw(static_cast<CT*>(a.out.base[w]) + tl.flat + cc + e, rc);
+        } else {
+          store8_raw(static_cast<CT*>(a.out.base[0]) + tl.shard + cc + e, rc);
+        }
       }
     }
     if (warp == 0 && lane < clen - nb) {
@@ -339,7 +444,7 @@ __global__ void __launch_bounds__((NC + 1) * 32)
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[s]);
     ++k;
-    cc += C;
+    cc += tc;
     if (cc >= tl.len) {
       cc = 0;
       ct += gridDim.x;
@@ -360,8 +465,32 @@ __global__ void __launch_bounds__((NC + 1) * 32)
   }
 }
 
+// Resident blocks per SM that the default stages allow (three stages of 24 KB
+// where the W ranks' gradients take at most 4 bytes per element, else of
+// 32 KB): the table instance's register budget is sized for that many.
+template <typename GT, int WT>
+constexpr int red_min_blocks() {
+  return (WT > 0 && WT * (int)sizeof(GT) <= 4) ? 3 : 2;
+}
+
+template <typename GT, typename CT, int WT, bool STAGE1, int NC>
+__global__ void __launch_bounds__((NC + 1) * 32)
+    k_reduce_norm_ws(const __grid_constant__ ReduceArgs a) {
+  reduce_ws_body<GT, CT, WT, STAGE1, NC, false>(a);
+}
+
+template <typename GT, typename CT, int WT, bool STAGE1, int NC>
+__global__ void __launch_bounds__((NC + 1) * 32, red_min_blocks<GT, WT>())
+    k_reduce_norm_ws_table(const __grid_constant__ ReduceArgs a) {
+  reduce_ws_body<GT, CT, WT, STAGE1, NC, true>(a);
+}
+
+// variant 0: register-staged; 1: pipelined over flat buffers; 2: pipelined
+// over a per-tensor pointer table (NULL entries allowed).
 template <typename GT, typename CT, int WT, bool S1>
 const void* reduce_kernel_v(int variant) {
+  if (variant == 2)
+    return reinterpret_cast<const void*>(&k_reduce_norm_ws_table<GT, CT, WT, S1, kRedConsumers>);
   if (variant == 1)
     return reinterpret_cast<const void*>(&k_reduce_norm_ws<GT, CT, WT, S1, kRedConsumers>);
   return reinterpret_cast<const void*>(&k_reduce_norm<GT, CT, WT, S1>);

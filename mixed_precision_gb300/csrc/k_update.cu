@@ -61,7 +61,7 @@ int reduce_chunk(int world, int grad_dtype, int stage_bytes) {
   return c < 128 ? 128 : c;
 }
 
-static int reduce_threads(int variant) { return variant == 1 ? (kRedConsumers + 1) * 32 : kThreads; }
+static int reduce_threads(int variant) { return variant != 0 ? (kRedConsumers + 1) * 32 : kThreads; }
 
 static int reduce_smem(int world, int grad_dtype, int variant, int chunk) {
   if (variant == 0) return 0;
@@ -70,6 +70,8 @@ static int reduce_smem(int world, int grad_dtype, int variant, int chunk) {
 }
 
 cudaError_t launch_reduce(const ReduceArgs& a, int grid, int variant, cudaStream_t s) {
+  // the pipelined kernel has an instance of its own for per-tensor pointers
+  if (variant == 1 && a.src.table_mode) variant = 2;
   const void* f = reduce_kernel(a.grad_dtype, a.comm_dtype, a.world, a.stage, variant);
   if (f == nullptr) return cudaErrorInvalidValue;
   void* args[] = {const_cast<ReduceArgs*>(&a)};
@@ -85,6 +87,12 @@ int reduce_blocks_per_sm(int grad_dtype, int comm_dtype, int world, int stage, i
   if (smem > 0 && cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
                       cudaSuccess)
     return 0;
+  if (variant == 1) {  // the per-tensor pointer instance launches with the same shared memory
+    const void* ft = reduce_kernel(grad_dtype, comm_dtype, world, stage, 2);
+    if (ft == nullptr ||
+        cudaFuncSetAttribute(ft, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+      return 0;
+  }
   int n = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, f, reduce_threads(variant), smem) !=
       cudaSuccess)

@@ -107,6 +107,44 @@ def test_pointer_table_mode_matches_flat():
         assert np.array_equal(a, b)
 
 
+@pytest.mark.parametrize("W,gdt,cdt,stage", [(3, wl.BF16, wl.BF16, 2), (4, wl.BF16, wl.BF16, 2),
+                                             (8, wl.F16, wl.F16, 2), (4, wl.BF16, wl.F32, 2),
+                                             (5, wl.F32, wl.F32, 2), (4, wl.BF16, wl.BF16, 1)])
+def test_pointer_table_partial_nulls_match_flat_and_oracle(W, gdt, cdt, stage):
+    """Gradients that are NULL on some ranks only (the routed-experts
+    pattern): a tile's live ranks take longer chunks in the reduce's stages.
+    Every live count from 0 to W occurs (each rank drops about half of the
+    parameters); tensors span several tiles, with ragged tails. The result
+    matches the oracle and equals the flat step's, norm included, bit for
+    bit."""
+    rng = np.random.default_rng(300 + W)
+    sizes = [int(x) for x in rng.integers(1, 40_000, size=30)] + [8192, 8193, 24_577, 7, 1]
+    shapes = [(n,) for n in sizes]
+    P = len(shapes)
+    # parameter 0 dropped everywhere, parameter 1 nowhere
+    dropped = [(set(int(p) for p in rng.choice(P, size=P // 2, replace=False)) | {0}) - {1}
+               for _ in range(W)]
+    live = [sum(p not in d for d in dropped) for p in range(P)]
+    assert 0 in live and W in live and any(0 < c < W for c in live)
+    pdt = wl.F16 if gdt == wl.F16 else wl.BF16
+    outs = []
+    for mode in ("flat", "tensors"):
+        pr = Pair(shapes, W, stage, 150_000, gdt, pdt, comm_dtype=cdt, index=60 + W)
+        for step in range(2):
+            g = pr.grads(step, 1e-3)
+            for r in range(W):
+                for p in dropped[r]:
+                    g[r][pr.offsets[p]:pr.offsets[p] + sizes[p]] = 0
+            st, info, gc = pr.step(g, Hparams(max_grad_norm=0.05), mode=mode)
+            pr.check(st, info, gc)
+        assert info.clip_coef < 1.0
+        outs.append([to_np(t) for t in (pr.z.master, pr.z.m, pr.z.v, pr.z.params_flat)]
+                    + [st["grad_norm"], st["norm_sq_raw"]])
+    for a, b in zip(outs[0][:4], outs[1][:4]):
+        assert np.array_equal(a, b)
+    assert outs[0][4:] == outs[1][4:]
+
+
 @pytest.mark.parametrize("stage", [1, 2])
 def test_per_tensor_launch_matches_oracle(stage):
     """The tensor-by-tensor launch sequence (the hook-style baseline) computes
