@@ -739,6 +739,9 @@ PER_CONFIG = [
     ("ragged_2000", {"world": 2}),
     ("ragged_2000", {"world": 8}),
     ("ragged_2000", {"world": 8, "per_tensor_launch": True}),
+    # the MoE list as its gradients arrive: each rank's idle experts (14 of 16
+    # per layer) passed as NULL pointers
+    ("moe_3.9b_bf16_w4", {"stage": 2, "tensors": True}),
 ]
 
 
@@ -775,6 +778,7 @@ def time_config(name: str, over: dict, steps: int, warmup: int, local: int) -> d
     over = dict(over)
     speculative = over.pop("speculative", False)
     per_tensor_launch = over.pop("per_tensor_launch", False)
+    tensors = over.pop("tensors", False)
     w = wl.workload(name, **over)
     z = ZeroStep(w.shapes, w.world, w.stage, w.bucket_bytes, w.grad_dtype, w.param_dtype,
                  w.comm_dtype)
@@ -790,7 +794,19 @@ def time_config(name: str, over: dict, steps: int, warmup: int, local: int) -> d
              for r in range(w.world)]
     hp = Hparams(lr=w.lr, beta1=w.beta1, beta2=w.beta2, eps=w.eps, weight_decay=w.weight_decay,
                  max_grad_norm=w.max_grad_norm)
-    if speculative:
+    sparse_read = None
+    if tensors:
+        # per-tensor pointers, NULL for a rank's all-zero gradients (the
+        # experts its tokens did not reach): those reads are skipped
+        per, live_elems = [], 0
+        for r in range(w.world):
+            zero = set(wl.zero_params(w, r))
+            per.append([None if p in zero else grads[r][off:off + n]
+                        for p, (off, n) in enumerate(zip(z.offsets, numel))])
+            live_elems += sum(n for p, n in enumerate(numel) if p not in zero)
+        sparse_read = live_elems * wl.ELEM_BYTES[w.grad_dtype] / w.n_real  # B/param read
+        step = lambda: z.step_tensors(per, hp)  # noqa: E731
+    elif speculative:
         step = lambda: z.step_speculative(grads, hp)  # noqa: E731
     elif per_tensor_launch:
         step = lambda: z.step_per_tensor_launch(grads, hp)  # noqa: E731
@@ -836,9 +852,14 @@ def time_config(name: str, over: dict, steps: int, warmup: int, local: int) -> d
         torch.cuda.synchronize()
         torch.cuda.empty_cache()
         return out
+    note = None
+    if per_tensor_launch:
+        note = "per-tensor launches: two kernels per parameter and the finalize"
+    elif tensors:
+        note = ("per-tensor gradient pointers, NULL where a rank's gradient is all zero; the "
+                "ledger counts those reads, sparse_bytes_per_param does not")
     out = {
-        "config": config_of(w, "per-tensor launches: two kernels per parameter and the finalize"
-                            if per_tensor_launch else None),
+        "config": config_of(w, note),
         "steps": steps, "warmup": warmup,
         "ms_per_step": tm["total_ms"] / steps,
         "step_ms_median": tm["steps_ms"][steps // 2],
@@ -856,6 +877,13 @@ def time_config(name: str, over: dict, steps: int, warmup: int, local: int) -> d
         "scale": st["scale"],
         "clocks": tm["clocks"],
     }
+    if sparse_read is not None:
+        # the bytes the step must move when the NULL gradients are not read
+        sb = sparse_read + (b["own"] - w.world * wl.ELEM_BYTES[w.grad_dtype])
+        out["step_roofline"]["sparse_bytes_per_param"] = sb
+        out["step_roofline"]["sparse_frac"] = sb * N / step_s / 1e9 / peak
+        out["kernels_ms"]["k_reduce_norm_sparse_gbs"] = (
+            (sparse_read + b["k1"] - w.world * wl.ELEM_BYTES[w.grad_dtype]) * N / (k1_ms / 1e3) / 1e9)
     dom, dom_ms, dom_b = (("k_adamw_cast", k3_ms, b["k3"]) if k3_ms >= k1_ms
                           else ("k_reduce_norm", k1_ms, b["k1"]))
     achieved = dom_b * N / (dom_ms / 1e3) / 1e9
@@ -877,6 +905,8 @@ def per_config(steps: int, warmup: int, local: int) -> dict:
     for name, over in PER_CONFIG:
         if over.get("speculative"):
             key = name + "_speculative_clip0"
+        elif over.get("tensors"):
+            key = name + "_tensors_idle_experts_null"
         elif name == "ragged_2000":
             key = f"{name}_w{over['world']}" + ("_per_tensor_launch" if over.get("per_tensor_launch")
                                                  else "")

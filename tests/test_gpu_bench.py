@@ -43,10 +43,10 @@ def test_our_line_keys():
     assert set(pc) == {"moe_3.9b_bf16_w4_stage2", "qwen3_0.6b_fp16_w8_stage1",
                        "qwen3_0.6b_fp16_w8_stage2", "qwen3_0.6b_bf16_w2_speculative_clip0",
                        "moe_3.9b_bf16_w4_speculative_clip0", "ragged_2000_w2", "ragged_2000_w8",
-                       "ragged_2000_w8_per_tensor_launch"}
+                       "ragged_2000_w8_per_tensor_launch", "moe_3.9b_bf16_w4_tensors_idle_experts_null"}
     for name, c in pc.items():
         assert c["steps"] == 3 and c["ms_per_step"] > 0 and 0 < c["step_roofline"]["frac"] < 1.5
-        base = name.rsplit("_stage", 1)[0].split("_speculative")[0]
+        base = name.rsplit("_stage", 1)[0].split("_speculative")[0].split("_tensors")[0]
         if name.startswith("ragged_2000"):
             base = "ragged_2000"
             assert c["config"]["world_simulated"] == int(name.split("_w")[1][0])
@@ -59,6 +59,9 @@ def test_our_line_keys():
     # the flat step against launching it tensor by tensor, same bytes
     assert "per-tensor" in pc["ragged_2000_w8_per_tensor_launch"]["config"]["note"]
     assert "note" not in pc["ragged_2000_w8"]["config"]
+    # the MoE list with each rank's idle experts passed as NULL: fewer bytes to move
+    sp = pc["moe_3.9b_bf16_w4_tensors_idle_experts_null"]["step_roofline"]
+    assert sp["sparse_bytes_per_param"] < sp["bytes_per_param"] and 0 < sp["sparse_frac"] < 1.5
     s1 = pc["qwen3_0.6b_fp16_w8_stage1"]["step_roofline"]
     assert s1["bytes_per_param"] == s1["ledger_bytes_per_param"] + 8 * 2  # the W*C all-reduce writes
 
