@@ -337,50 +337,75 @@ __device__ __forceinline__ void reduce_ws_body(const ReduceArgs& a) {
     }
     const GT* base = reinterpret_cast<const GT*>(smem + s * kStage);
     if constexpr (TABLE) {
-      for (int v0 = 0; v0 < nb; v0 += C) {
-        const int e_end = min(nb, v0 + (warp + 1) * per);
-        for (int e = v0 + warp * per + 8 * lane; e < e_end; e += 256) {
-          float acc[8];
-          const GT* src = base;  // the next live rank's slice; a NULL rank adds +0.0
-          if (!(nulls & 1ull)) {
-            load8_smem(src + e, acc);
-            src += tc;
-          } else {
+      if (__popcll(nulls) == W) {
+        // Every rank's gradient is NULL: each reduced value is +0.0. The
+        // same groups still go through add_group, with the +0.0 sum the
+        // general path would compute, so the norm partial keeps its bits.
+        Pack8<CT> rc;
+        float rf[8];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
+        for (int j = 0; j < 8; ++j) {
+          rc.e[j] = DT<CT>::from_f32(0.0f);
+          rf[j] = 0.0f;
+        }
+        for (int v0 = 0; v0 < nb; v0 += C) {
+          const int e_end = min(nb, v0 + (warp + 1) * per);
+          for (int e = v0 + warp * per + 8 * lane; e < e_end; e += 256) {
+            add_group(0.0f, hi, lo, big, rf);
+            if constexpr (STAGE1) {
+              for (int w = 0; w < W; ++w)
+                store8_raw(static_cast<CT*>(a.out.base[w]) + tl.flat + cc + e, rc);
+            } else {
+              store8_raw(static_cast<CT*>(a.out.base[0]) + tl.shard + cc + e, rc);
+            }
           }
-#pragma unroll(WT ? WT : 1)
-          for (int w = 1; w < W; ++w) {
-            float x[8];
-            if (!((nulls >> w) & 1ull)) {
-              load8_smem(src + e, x);
+        }
+      } else {
+        for (int v0 = 0; v0 < nb; v0 += C) {
+          const int e_end = min(nb, v0 + (warp + 1) * per);
+          for (int e = v0 + warp * per + 8 * lane; e < e_end; e += 256) {
+            float acc[8];
+            const GT* src = base;  // the next live rank's slice; a NULL rank adds +0.0
+            if (!(nulls & 1ull)) {
+              load8_smem(src + e, acc);
               src += tc;
             } else {
 #pragma unroll
-              for (int j = 0; j < 8; ++j) x[j] = 0.0f;
+              for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
             }
+#pragma unroll(WT ? WT : 1)
+            for (int w = 1; w < W; ++w) {
+              float x[8];
+              if (!((nulls >> w) & 1ull)) {
+                load8_smem(src + e, x);
+                src += tc;
+              } else {
 #pragma unroll
-            for (int j = 0; j < 8; ++j) acc[j] = __fadd_rn(acc[j], x[j]);
-          }
-          // from here as in flat mode
-          Pack8<CT> rc;
-          float rf[8];
-          float ss = 0.0f;
-          bool fin = true;
+                for (int j = 0; j < 8; ++j) x[j] = 0.0f;
+              }
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            rc.e[j] = DT<CT>::from_f32(acc[j]);
-            rf[j] = DT<CT>::to_f32(rc.e[j]);
-            fin = fin && DT<CT>::finite_bits(rc.e[j]);
-            ss = __fmaf_rn(rf[j], rf[j], ss);
-          }
-          if (!fin) bad = 1u;
-          add_group(ss, hi, lo, big, rf);
-          if constexpr (STAGE1) {
-            for (int w = 0; w < W; ++w)
-              store8_raw(static_cast<CT*>(a.out.base[w]) + tl.flat + cc + e, rc);
-          } else {
-            store8_raw(static_cast<CT*>(a.out.base[0]) + tl.shard + cc + e, rc);
+              for (int j = 0; j < 8; ++j) acc[j] = __fadd_rn(acc[j], x[j]);
+            }
+            // from here as in flat mode
+            Pack8<CT> rc;
+            float rf[8];
+            float ss = 0.0f;
+            bool fin = true;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              rc.e[j] = DT<CT>::from_f32(acc[j]);
+              rf[j] = DT<CT>::to_f32(rc.e[j]);
+              fin = fin && DT<CT>::finite_bits(rc.e[j]);
+              ss = __fmaf_rn(rf[j], rf[j], ss);
+            }
+            if (!fin) bad = 1u;
+            add_group(ss, hi, lo, big, rf);
+            if constexpr (STAGE1) {
+              for (int w = 0; w < W; ++w)
+                store8_raw(static_cast<CT*>(a.out.base[w]) + tl.flat + cc + e, rc);
+            } else {
+              store8_raw(static_cast<CT*>(a.out.base[0]) + tl.shard + cc + e, rc);
+            }
           }
         }
       }
