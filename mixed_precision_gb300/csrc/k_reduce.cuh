@@ -504,6 +504,15 @@ __global__ void __launch_bounds__((NC + 1) * 32)
   reduce_ws_body<GT, CT, WT, STAGE1, NC, false>(a);
 }
 
+// Flat buffers, W known only at run time (W not 1, 2, 4 or 8): two resident
+// blocks of 32 KB stages, the registers budgeted for that (without the
+// bound ptxas spilled these instances).
+template <typename GT, typename CT, bool STAGE1, int NC>
+__global__ void __launch_bounds__((NC + 1) * 32, 2)
+    k_reduce_norm_ws_anyw(const __grid_constant__ ReduceArgs a) {
+  reduce_ws_body<GT, CT, 0, STAGE1, NC, false>(a);
+}
+
 template <typename GT, typename CT, int WT, bool STAGE1, int NC>
 __global__ void __launch_bounds__((NC + 1) * 32, red_min_blocks<GT, WT>())
     k_reduce_norm_ws_table(const __grid_constant__ ReduceArgs a) {
@@ -516,8 +525,12 @@ template <typename GT, typename CT, int WT, bool S1>
 const void* reduce_kernel_v(int variant) {
   if (variant == 2)
     return reinterpret_cast<const void*>(&k_reduce_norm_ws_table<GT, CT, WT, S1, kRedConsumers>);
-  if (variant == 1)
-    return reinterpret_cast<const void*>(&k_reduce_norm_ws<GT, CT, WT, S1, kRedConsumers>);
+  if (variant == 1) {
+    if constexpr (WT == 0)
+      return reinterpret_cast<const void*>(&k_reduce_norm_ws_anyw<GT, CT, S1, kRedConsumers>);
+    else
+      return reinterpret_cast<const void*>(&k_reduce_norm_ws<GT, CT, WT, S1, kRedConsumers>);
+  }
   return reinterpret_cast<const void*>(&k_reduce_norm<GT, CT, WT, S1>);
 }
 
