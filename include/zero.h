@@ -286,6 +286,11 @@ int zero_step(zero_layout_t* layout, const void* const* grads, void* const* allr
  *              (grad_ptrs[w * n_params + p]); each points at parameter p's
  *              numel elements of grad_dtype, 16-byte aligned; NULL means an
  *              all-zero gradient (not read at all).
+ * The results are those of zero_step on flat buffers holding the same
+ * values, bit for bit (norm included). The pointer table is read once per
+ * tile; where some ranks' pointers are NULL, the other ranks' slices of a
+ * tile move in longer chunks, and a tile whose ranks are all NULL is stored
+ * as zeros without being summed.
  * Everything else as zero_step. */
 int zero_step_tensors(zero_layout_t* layout, const void* const* grad_ptrs,
                       void* const* allreduce_out, const zero_hparams* hp, void* stream);
