@@ -389,6 +389,11 @@ int launch_step(zero_layout* L, const GradSrc& src, void* const* allreduce_out,
     const bool counter = L->update_variant == 1 && (guarded || L->update_sched);
     ua.tile_next = counter ? &L->d_state->tiles_next : nullptr;
     ua.restore = guarded && L->update_variant == 1 ? 1 : 0;  // the parameter restore rides along
+    if (src.table_mode) {
+      ua.table = src.table;
+      ua.n_params = src.n_params;
+      ua.world = W;
+    }
     Range r("K3 unscale+clip+AdamW+cast");
     e = launch_update(ua, guarded ? L->grid_update_guarded : L->grid_update, L->update_variant, s);
     if (e != cudaSuccess) return cuda_fail(e, "update kernel launch");

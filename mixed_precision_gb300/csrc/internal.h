@@ -134,6 +134,14 @@ struct UpdateArgs {
   int restore;  // 1 (the speculative step's guarded update): when the state asks
                 // for the parameters back after an overflow, recast them from
                 // the current master instead (pipelined kernel only)
+  // The step's per-tensor gradient pointers (device array [world * n_params],
+  // NULL = all-zero gradient), or nullptr for flat buffers. With a table the
+  // pipelined kernel's table instance runs: a tile whose ranks are all NULL
+  // has a reduced gradient of +0.0 (the reduce stored exactly that), so it
+  // is not read back.
+  const void* const* table;
+  int n_params;
+  int world;
 };
 
 // Kernel launchers. Each returns the launch's cudaError_t.

@@ -264,9 +264,8 @@ struct ChunkDesc {
   int32_t clen;  // elements in the chunk; -1: no more work
 };
 
-template <typename CT, typename PT, int C, int S, int NC>
-__global__ void __launch_bounds__((NC + 1) * 32)
-    k_adamw_cast_ws(const __grid_constant__ UpdateArgs a) {
+template <typename CT, typename PT, int C, int S, int NC, bool TABLE>
+__device__ __forceinline__ void update_ws_body(const UpdateArgs& a) {
   constexpr int kPerWarp = C / NC;
   static_assert(kPerWarp % 128 == 0, "a warp's slice must be whole 4-element groups per lane");
   extern __shared__ __align__(128) unsigned char smem[];
@@ -339,6 +338,7 @@ __global__ void __launch_bounds__((NC + 1) * 32)
     int pc = 0;
     unsigned k = 0;
     bool ok = true;
+    bool zero_tile = false;  // table mode: every rank's gradient for the tile is NULL
     while (true) {
       const int s = (int)(k % S);
       if (k >= (unsigned)S && !mbar_wait(&empty[s], ((k / S) - 1) & 1u)) {
@@ -351,21 +351,31 @@ __global__ void __launch_bounds__((NC + 1) * 32)
         mbar_arrive(&full[s]);
         break;
       }
+      if constexpr (TABLE) {
+        if (pc == 0) {
+          zero_tile = true;
+          for (int w = 0; w < a.world; ++w)
+            if (a.table[(int64_t)w * a.n_params + tl.param] != nullptr) zero_tile = false;
+        }
+      }
       const int clen = min(C, tl.len - pc);
       const int nb = clen & ~7;
       d.so = tl.shard + pc;
       d.po = (a.stage == 3 ? tl.shard : tl.flat) + pc;
       d.ro = (a.stage == 1 ? tl.flat : tl.shard) + pc;
       d.rb = a.stage == 1 ? tl.rank : 0;
+      if (TABLE && zero_tile) d.rb = -1;  // the consumers take +0.0 for the gradient
       d.clen = clen;
       unsigned char* base = smem + s * kStage;
       if (nb > 0) {
-        mbar_arrive_expect_tx(&full[s], (uint32_t)nb * (12u + (uint32_t)sizeof(CT)));
+        const bool grad = !(TABLE && zero_tile);
+        mbar_arrive_expect_tx(&full[s], (uint32_t)nb * (12u + (grad ? (uint32_t)sizeof(CT) : 0u)));
         bulk_g2s(base, s_master + d.so, nb * 4, &full[s]);
         bulk_g2s(base + C * 4, s_m + d.so, nb * 4, &full[s]);
         bulk_g2s(base + C * 8, s_v + d.so, nb * 4, &full[s]);
-        bulk_g2s(base + C * 12, static_cast<const CT*>(a.red.base[d.rb]) + d.ro,
-                 nb * (int)sizeof(CT), &full[s]);
+        if (grad)
+          bulk_g2s(base + C * 12, static_cast<const CT*>(a.red.base[d.rb]) + d.ro,
+                   nb * (int)sizeof(CT), &full[s]);
       } else {
         mbar_arrive(&full[s]);
       }
@@ -419,7 +429,15 @@ __global__ void __launch_bounds__((NC + 1) * 32)
       float4 m = *reinterpret_cast<const float4*>(sm + e);
       float4 v = *reinterpret_cast<const float4*>(sv + e);
       float r[4];
-      load4_smem(sr + e, r);
+      if constexpr (TABLE) {
+        if (d.rb >= 0) {
+          load4_smem(sr + e, r);
+        } else {
+          r[0] = r[1] = r[2] = r[3] = 0.0f;
+        }
+      } else {
+        load4_smem(sr + e, r);
+      }
       adam(r[0], p.x, m.x, v.x);
       adam(r[1], p.y, m.y, v.y);
       adam(r[2], p.z, m.z, v.z);
@@ -434,7 +452,9 @@ __global__ void __launch_bounds__((NC + 1) * 32)
     if (warp == 0 && lane < d.clen - nb) {
       const int e = nb + lane;
       float p = s_master[so + e], m = s_m[so + e], v = s_v[so + e];
-      adam(DT<CT>::to_f32(static_cast<const CT*>(a.red.base[d.rb])[d.ro + e]), p, m, v);
+      float r = 0.0f;
+      if (!TABLE || d.rb >= 0) r = DT<CT>::to_f32(static_cast<const CT*>(a.red.base[d.rb])[d.ro + e]);
+      adam(r, p, m, v);
       s_master[so + e] = p;
       s_m[so + e] = m;
       s_v[so + e] = v;
@@ -446,12 +466,29 @@ __global__ void __launch_bounds__((NC + 1) * 32)
   }
 }
 
+template <typename CT, typename PT, int C, int S, int NC>
+__global__ void __launch_bounds__((NC + 1) * 32)
+    k_adamw_cast_ws(const __grid_constant__ UpdateArgs a) {
+  update_ws_body<CT, PT, C, S, NC, false>(a);
+}
+
+// The step from per-tensor gradient pointers (UpdateArgs::table).
+template <typename CT, typename PT, int C, int S, int NC>
+__global__ void __launch_bounds__((NC + 1) * 32)
+    k_adamw_cast_ws_table(const __grid_constant__ UpdateArgs a) {
+  update_ws_body<CT, PT, C, S, NC, true>(a);
+}
+
 constexpr int kWsChunk = 2048;
 constexpr int kWsStages = 4;
 constexpr int kWsConsumers = 8;
 
+// variant 0: register-staged; 1: pipelined; 2: pipelined, per-tensor pointers
 template <typename CT, typename PT>
 static const void* update_kernel_cp(int variant) {
+  if (variant == 2)
+    return reinterpret_cast<const void*>(
+        &k_adamw_cast_ws_table<CT, PT, kWsChunk, kWsStages, kWsConsumers>);
   if (variant == 1)
     return reinterpret_cast<const void*>(
         &k_adamw_cast_ws<CT, PT, kWsChunk, kWsStages, kWsConsumers>);
@@ -478,12 +515,13 @@ static const void* update_kernel(int comm_dtype, int param_dtype, int variant) {
 
 static int update_smem(int comm_dtype, int variant) {
   const int cb = comm_dtype == kF32 ? 4 : 2;
-  return variant == 1 ? kWsStages * kWsChunk * (12 + cb) : 0;
+  return variant != 0 ? kWsStages * kWsChunk * (12 + cb) : 0;
 }
 
-static int update_threads(int variant) { return variant == 1 ? (kWsConsumers + 1) * 32 : kThreads; }
+static int update_threads(int variant) { return variant != 0 ? (kWsConsumers + 1) * 32 : kThreads; }
 
 cudaError_t launch_update(const UpdateArgs& a, int grid, int variant, cudaStream_t s) {
+  if (variant == 1 && a.table != nullptr) variant = 2;
   const void* f = update_kernel(a.comm_dtype, a.param_dtype, variant);
   if (f == nullptr) return cudaErrorInvalidValue;
   void* args[] = {const_cast<UpdateArgs*>(&a)};
@@ -498,6 +536,12 @@ int update_blocks_per_sm(int comm_dtype, int param_dtype, int variant) {
   if (smem > 0 && cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
                       cudaSuccess)
     return 0;
+  if (variant == 1) {  // the per-tensor pointer instance launches with the same shared memory
+    const void* ft = update_kernel(comm_dtype, param_dtype, 2);
+    if (ft == nullptr ||
+        cudaFuncSetAttribute(ft, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+      return 0;
+  }
   int n = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, f, update_threads(variant), smem) !=
       cudaSuccess)
