@@ -290,7 +290,7 @@ int zero_step(zero_layout_t* layout, const void* const* grads, void* const* allr
  * values, bit for bit (norm included). The pointer table is read once per
  * tile; where some ranks' pointers are NULL, the other ranks' slices of a
  * tile move in longer chunks, and a tile whose ranks are all NULL is stored
- * as zeros without being summed.
+ * as zeros without being summed and is not read back by the update.
  * Everything else as zero_step. */
 int zero_step_tensors(zero_layout_t* layout, const void* const* grad_ptrs,
                       void* const* allreduce_out, const zero_hparams* hp, void* stream);
