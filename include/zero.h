@@ -291,6 +291,9 @@ int zero_step(zero_layout_t* layout, const void* const* grads, void* const* allr
  * tile; where some ranks' pointers are NULL, the other ranks' slices of a
  * tile move in longer chunks, and a tile whose ranks are all NULL is stored
  * as zeros without being summed and is not read back by the update.
+ * The table is copied to the device on `stream` before the call returns, so
+ * the call cannot be captured into a CUDA graph: on a capturing stream it
+ * returns ZERO_ERR_INVALID and enqueues nothing.
  * Everything else as zero_step. */
 int zero_step_tensors(zero_layout_t* layout, const void* const* grad_ptrs,
                       void* const* allreduce_out, const zero_hparams* hp, void* stream);
@@ -348,7 +351,8 @@ int zero_step_speculative(zero_layout_t* layout, const void* const* grads, const
  * gradient, which is never read. Results are those of zero_step_speculative
  * on flat buffers holding zeros there, bit for bit. The table is copied to
  * the device on `stream` before the call returns, so it is not capturable
- * into a CUDA graph. Errors as zero_step_tensors. */
+ * into a CUDA graph (ZERO_ERR_INVALID on a capturing stream, nothing
+ * enqueued). Errors as zero_step_tensors. */
 int zero_step_speculative_tensors(zero_layout_t* layout, const void* const* grad_ptrs,
                                   const zero_hparams* hp, void* stream);
 

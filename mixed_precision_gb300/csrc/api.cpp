@@ -526,6 +526,21 @@ int launch_step_per_tensor(zero_layout* L, const GradSrc& src, void* const* allr
   return ZERO_OK;
 }
 
+// The per-tensor entry points copy the caller's host pointer array to the
+// device on the stream. A graph would keep that copy of host memory the
+// caller may since have changed or freed, so a capturing stream is refused
+// before anything is enqueued.
+static int check_not_capturing(cudaStream_t s, const char* what) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  ZERO_CUDA(cudaStreamIsCapturing(s, &cs));
+  if (cs != cudaStreamCaptureStatusNone)
+    return fail(ZERO_ERR_INVALID,
+                "%s copies its host pointer table on the stream and cannot be captured into a "
+                "graph; capture zero_step or zero_step_speculative over flat buffers instead",
+                what);
+  return ZERO_OK;
+}
+
 // Entry points that step or copy every simulated rank's data in one process
 // have no meaning for a layout that holds one rank's shard.
 int check_not_sharded(const zero_layout* L, const char* what) {
@@ -1010,6 +1025,7 @@ int zero_step_speculative_tensors(zero_layout_t* L, const void* const* grad_ptrs
       return fail(ZERO_ERR_INVALID, "grad_ptrs[%lld] is not 16-byte aligned", (long long)i);
   }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (int rc = check_not_capturing(s, "zero_step_speculative_tensors")) return rc;
   // The host array is staged by the runtime before this call returns.
   ZERO_CUDA(cudaMemcpyAsync(L->d_table, grad_ptrs, (size_t)n * sizeof(void*),
                             cudaMemcpyHostToDevice, s));
@@ -1051,6 +1067,7 @@ int zero_step_tensors(zero_layout_t* L, const void* const* grad_ptrs, void* cons
       return fail(ZERO_ERR_INVALID, "grad_ptrs[%lld] is not 16-byte aligned", (long long)i);
   }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (int rc = check_not_capturing(s, "zero_step_tensors")) return rc;
   // The host array is staged by the runtime before this call returns.
   ZERO_CUDA(cudaMemcpyAsync(L->d_table, grad_ptrs, (size_t)n * sizeof(void*),
                             cudaMemcpyHostToDevice, s));

@@ -134,3 +134,41 @@ def test_captured_step_replays_like_eager(spec, stage, gdt):
     del graph
     g_layout.close()
     eager.close()
+
+
+@pytest.mark.filterwarnings("ignore:The CUDA Graph is empty")
+def test_per_tensor_entry_points_refuse_capture():
+    """zero_step_tensors and zero_step_speculative_tensors copy the caller's
+    host pointer table on the stream, which a graph cannot keep: on a
+    capturing stream they return ZERO_ERR_INVALID and enqueue nothing, so the
+    capture stays valid and the state is untouched."""
+    from mixed_precision_gb300 import ZeroError
+    shapes = small_qwen_shapes()
+    z = _layout(shapes, 2, 2, wl.BF16, wl.BF16, True, 71)
+    g = [wl.flat_grads(z.offsets, z.numels, z.np, 1e-3, wl.grad_seed(71, r), wl.BF16,
+                       device="cuda") for r in range(2)]
+    per = [[g[r][off:off + n] for off, n in zip(z.offsets, z.numels)] for r in range(2)]
+    torch.cuda.synchronize()
+    before = z.scaler_state()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    codes = []
+    with torch.cuda.stream(side):
+        graph.capture_begin()
+        for call in (lambda: z.step_tensors(per, Hparams(), stream=side),
+                     lambda: z.step_speculative_tensors(per, Hparams(), stream=side)):
+            with pytest.raises(ZeroError) as e:
+                call()
+            codes.append(e.value.code)
+            assert "cannot be captured" in str(e.value)
+        graph.capture_end()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    assert codes == [abi.ZERO_ERR_INVALID] * 2
+    assert z.scaler_state() == before
+    # outside a capture the same calls step as usual
+    z.step_tensors(per, Hparams())
+    torch.cuda.synchronize()
+    assert z.scaler_state()["t"] == before["t"] + 1
+    z.close()
