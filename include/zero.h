@@ -47,8 +47,10 @@
  *     zero_set_step_events is active), and every decision of the step is
  *     taken on the device, so both can be captured into a CUDA graph and
  *     replayed on new gradients written into the captured buffers. The
- *     hyper-parameters are captured by value. zero_step_host is not
- *     capturable (its copy streams wait on events of earlier calls).
+ *     hyper-parameters are captured by value. zero_step_host and the
+ *     per-tensor step calls copy from host memory and are not capturable:
+ *     on a capturing stream they return ZERO_ERR_INVALID and enqueue
+ *     nothing.
  */
 #ifndef ZERO_GB300_H
 #define ZERO_GB300_H

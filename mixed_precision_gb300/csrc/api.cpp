@@ -527,16 +527,17 @@ int launch_step_per_tensor(zero_layout* L, const GradSrc& src, void* const* allr
 }
 
 // The per-tensor entry points copy the caller's host pointer array to the
-// device on the stream. A graph would keep that copy of host memory the
-// caller may since have changed or freed, so a capturing stream is refused
-// before anything is enqueued.
+// device on the stream, and the host-gradient entry point copies on streams
+// of its own ordered by events of earlier calls. A graph would keep copies
+// of host memory the caller may since have changed or freed, so a capturing
+// stream is refused before anything is enqueued.
 static int check_not_capturing(cudaStream_t s, const char* what) {
   cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
   ZERO_CUDA(cudaStreamIsCapturing(s, &cs));
   if (cs != cudaStreamCaptureStatusNone)
     return fail(ZERO_ERR_INVALID,
-                "%s copies its host pointer table on the stream and cannot be captured into a "
-                "graph; capture zero_step or zero_step_speculative over flat buffers instead",
+                "%s copies from host memory on its own and cannot be captured into a graph; "
+                "capture zero_step or zero_step_speculative over device buffers instead",
                 what);
   return ZERO_OK;
 }
@@ -1093,6 +1094,7 @@ static int step_host(zero_layout_t* L, const void* const* host_grads, void* cons
   }
   if (int rc = check_hparams(hp)) return rc;
   if (int rc = check_allreduce(L, allreduce_out)) return rc;
+  if (int rc = check_not_capturing(s, "zero_step_host")) return rc;
   if (!L->copy_ready) {
     if (const char* v = std::getenv("ZERO_H2D_STREAMS")) {
       const int n = std::atoi(v);

@@ -139,7 +139,8 @@ def test_captured_step_replays_like_eager(spec, stage, gdt):
 @pytest.mark.filterwarnings("ignore:The CUDA Graph is empty")
 def test_per_tensor_entry_points_refuse_capture():
     """zero_step_tensors and zero_step_speculative_tensors copy the caller's
-    host pointer table on the stream, which a graph cannot keep: on a
+    host pointer table on the stream, and zero_step_host copies host
+    gradients on streams of its own: none of it can live in a graph. On a
     capturing stream they return ZERO_ERR_INVALID and enqueue nothing, so the
     capture stays valid and the state is untouched."""
     from mixed_precision_gb300 import ZeroError
@@ -148,6 +149,7 @@ def test_per_tensor_entry_points_refuse_capture():
     g = [wl.flat_grads(z.offsets, z.numels, z.np, 1e-3, wl.grad_seed(71, r), wl.BF16,
                        device="cuda") for r in range(2)]
     per = [[g[r][off:off + n] for off, n in zip(z.offsets, z.numels)] for r in range(2)]
+    pinned = [t.cpu().pin_memory() for t in g]
     torch.cuda.synchronize()
     before = z.scaler_state()
     side = torch.cuda.Stream()
@@ -157,7 +159,8 @@ def test_per_tensor_entry_points_refuse_capture():
     with torch.cuda.stream(side):
         graph.capture_begin()
         for call in (lambda: z.step_tensors(per, Hparams(), stream=side),
-                     lambda: z.step_speculative_tensors(per, Hparams(), stream=side)):
+                     lambda: z.step_speculative_tensors(per, Hparams(), stream=side),
+                     lambda: z.step_host(pinned, g, Hparams(), stream=side)):
             with pytest.raises(ZeroError) as e:
                 call()
             codes.append(e.value.code)
@@ -165,7 +168,7 @@ def test_per_tensor_entry_points_refuse_capture():
         graph.capture_end()
     torch.cuda.current_stream().wait_stream(side)
     torch.cuda.synchronize()
-    assert codes == [abi.ZERO_ERR_INVALID] * 2
+    assert codes == [abi.ZERO_ERR_INVALID] * 3
     assert z.scaler_state() == before
     # outside a capture the same calls step as usual
     z.step_tensors(per, Hparams())
