@@ -55,6 +55,9 @@ NCU_TRAFFIC_PER_ELEM = {
     # speculative single pass, W=4, the same grid rule, 2 MoE layers:
     # (4.700327 + 3.243320) GB
     ("k_spec_step", "moe_3.9b_bf16_w4"): 33.810,
+    # update kernel's per-tensor pointer instance, 2 MoE layers with each
+    # rank's idle experts NULL: (3.051415 + 3.230056) GB
+    ("k_adamw_cast_table", "moe_3.9b_bf16_w4"): 26.736,
 }
 
 
@@ -887,7 +890,7 @@ def time_config(name: str, over: dict, steps: int, warmup: int, local: int) -> d
     dom, dom_ms, dom_b = (("k_adamw_cast", k3_ms, b["k3"]) if k3_ms >= k1_ms
                           else ("k_reduce_norm", k1_ms, b["k1"]))
     achieved = dom_b * N / (dom_ms / 1e3) / 1e9
-    tr = NCU_TRAFFIC_PER_ELEM.get((dom, w.name))
+    tr = NCU_TRAFFIC_PER_ELEM.get((dom + ("_table" if tensors else ""), w.name))
     out["roofline"] = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak,
                        "unit": "GB/s", "frac": achieved / peak,
                        "traffic": tr * N if tr is not None else None,
