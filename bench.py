@@ -808,6 +808,10 @@ def time_config(name: str, over: dict, steps: int, warmup: int, local: int) -> d
                         for p, (off, n) in enumerate(zip(z.offsets, numel))])
             live_elems += sum(n for p, n in enumerate(numel) if p not in zero)
         sparse_read = live_elems * wl.ELEM_BYTES[w.grad_dtype] / w.n_real  # B/param read
+        # parameters NULL on every rank: the update does not read their
+        # reduced gradient back (it is +0.0)
+        idle = set.intersection(*[set(wl.zero_params(w, r)) for r in range(w.world)])
+        idle_frac = sum(numel[p] for p in idle) / w.n_real
         step = lambda: z.step_tensors(per, hp)  # noqa: E731
     elif speculative:
         step = lambda: z.step_speculative(grads, hp)  # noqa: E731
@@ -887,7 +891,11 @@ def time_config(name: str, over: dict, steps: int, warmup: int, local: int) -> d
         out["step_roofline"]["sparse_frac"] = sb * N / step_s / 1e9 / peak
         out["kernels_ms"]["k_reduce_norm_sparse_gbs"] = (
             (sparse_read + b["k1"] - w.world * wl.ELEM_BYTES[w.grad_dtype]) * N / (k1_ms / 1e3) / 1e9)
-    dom, dom_ms, dom_b = (("k_adamw_cast", k3_ms, b["k3"]) if k3_ms >= k1_ms
+    k3_b = b["k3"]
+    if tensors:  # the update's per-tensor instance skips the idle tiles' gradient reads
+        k3_b -= wl.ELEM_BYTES[w.comm_dtype] * idle_frac
+        out["kernels_ms"]["k_adamw_cast_gbs"] = k3_b * N / (k3_ms / 1e3) / 1e9
+    dom, dom_ms, dom_b = (("k_adamw_cast", k3_ms, k3_b) if k3_ms >= k1_ms
                           else ("k_reduce_norm", k1_ms, b["k1"]))
     achieved = dom_b * N / (dom_ms / 1e3) / 1e9
     tr = NCU_TRAFFIC_PER_ELEM.get((dom + ("_table" if tensors else ""), w.name))
