@@ -927,6 +927,18 @@ def per_config(steps: int, warmup: int, local: int) -> dict:
     return out
 
 
+def local_buckets(z, rank: int) -> int:
+    """Buckets whose slice for `rank` holds a real element (each is one
+    update launch of the sharded step)."""
+    from mixed_precision_gb300 import _abi as abi
+    n = 0
+    for b in range(z.info.n_buckets):
+        f0, _, ln = abi.zero_shard_range(z.handle, b, rank)
+        if any(min(o + k, f0 + ln) > max(o, f0) for o, k in zip(z.offsets, z.numels) if k > 0):
+            n += 1
+    return n
+
+
 def run_sharded(args) -> dict | None:
     """The sharded step across N GPUs (one process each): the workload's
     parameter list with W = N, each rank's own seeded gradients, timed over
@@ -1038,9 +1050,11 @@ def run_sharded(args) -> dict | None:
                 "h2d_bytes_per_step": z.np * G, "d2h_bytes_per_step": int(z.info.state_blob_used),
                 "note": "per rank: its gradients copied in from pinned host memory each step, "
                         "the step's scaler state read back asynchronously"},
-        # per step: the shard norm, the finalize and the update (the collectives
+        # per step: the shard norm, the finalize and the update -- one launch
+        # per bucket that holds some of this rank's elements when the
+        # all-gathers overlap it (stages 1/2), one in stage 3 (the collectives
         # are NCCL's kernels)
-        "gpu_launches": K * 3,
+        "gpu_launches": K * (2 + (1 if w.stage == 3 else local_buckets(z, rank))),
         "clocks": clocks,
     }
     z.close()

@@ -579,6 +579,16 @@ int zero_dist_finalize(zero_layout_t* layout, const double* norm_pair, const zer
  * all-gathers each bucket of params_flat (stages 1/2). */
 int zero_dist_update(zero_layout_t* layout, const void* allreduced, void* stream);
 
+/* zero_dist_update restricted to buckets [first_bucket, first_bucket +
+ * n_buckets): this rank's tiles of those buckets only. Updating bucket by
+ * bucket lets the caller start each bucket's all-gather while the next
+ * bucket is being updated ([DO] "Distributed optimizer": the parameters come
+ * back bucket by bucket). The union of the ranges over a step must be every
+ * bucket once, after zero_dist_finalize. ZERO_ERR_INVALID for a range
+ * outside the layout's buckets; an empty range enqueues nothing. */
+int zero_dist_update_buckets(zero_layout_t* layout, const void* allreduced, int first_bucket,
+                             int n_buckets, void* stream);
+
 /* Message for the last failing call on this thread ("" if none). The pointer
  * stays valid until the next failing call on this thread. */
 const char* zero_last_error(void);

@@ -120,6 +120,7 @@ def lib() -> ctypes.CDLL:
             "zero_dist_shard_norm": [P, P, P, P],
             "zero_dist_finalize": [P, P, ctypes.POINTER(zero_hparams), P],
             "zero_dist_update": [P, P, P],
+            "zero_dist_update_buckets": [P, P, I, I, P],
             "zero_dist_widen": [P, P, P, P],
         }
         for name, args in sig.items():
@@ -324,6 +325,12 @@ def zero_dist_finalize(layout: int, norm_pair: int, hp: zero_hparams, stream: in
 
 def zero_dist_update(layout: int, allreduced: int, stream: int) -> None:
     _check(lib().zero_dist_update(layout, allreduced or None, stream or None))
+
+
+def zero_dist_update_buckets(layout: int, allreduced: int, first_bucket: int, n_buckets: int,
+                             stream: int) -> None:
+    _check(lib().zero_dist_update_buckets(layout, allreduced or None, first_bucket, n_buckets,
+                                          stream or None))
 
 
 def zero_dist_widen(layout: int, grads: int, out: int, stream: int) -> None:

@@ -1492,13 +1492,19 @@ int zero_dist_finalize(zero_layout_t* L, const double* norm_pair, const zero_hpa
   return ZERO_OK;
 }
 
-int zero_dist_update(zero_layout_t* L, const void* allreduced, void* stream) {
-  Range r_entry("zero_dist_update");
+int zero_dist_update_buckets(zero_layout_t* L, const void* allreduced, int first_bucket,
+                             int n_buckets, void* stream) {
+  Range r_entry("zero_dist_update_buckets");
   if (int rc = check_dist(L, allreduced)) return rc;
-  const int n_tiles = (int)L->tiles.size();
-  if (n_tiles == 0) return ZERO_OK;
+  const int nb = (int)L->bucket_tile_begin.size() - 1;
+  if (first_bucket < 0 || n_buckets < 0 || first_bucket + n_buckets > nb)
+    return fail(ZERO_ERR_INVALID, "buckets [%d, %d) outside the layout's %d", first_bucket,
+                first_bucket + n_buckets, nb);
+  const int t0 = L->bucket_tile_begin[first_bucket];
+  const int n_tiles = L->bucket_tile_begin[first_bucket + n_buckets] - t0;
+  if (n_tiles == 0) return ZERO_OK;  // this rank owns no real element there
   UpdateArgs ua{};
-  ua.tiles = L->d_tiles;
+  ua.tiles = L->d_tiles + t0;
   ua.n_tiles = n_tiles;
   ua.stage = L->cfg.stage;
   ua.comm_dtype = L->comm_dtype;
@@ -1511,12 +1517,18 @@ int zero_dist_update(zero_layout_t* L, const void* allreduced, void* stream) {
   ua.params_flat = L->params;
   ua.state = L->d_state;
   ua.error = &L->d_state->error;
+  // the counter wraps back to 0 at the end of every launch, whatever its tiles
   ua.tile_next = L->update_sched ? &L->d_state->tiles_next : nullptr;
   Range r("K3 unscale+clip+AdamW+cast (this rank)");
   cudaError_t e = launch_update(ua, std::min(n_tiles, L->grid_update), L->update_variant,
                                 static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "update kernel launch");
   return ZERO_OK;
+}
+
+int zero_dist_update(zero_layout_t* L, const void* allreduced, void* stream) {
+  if (int rc = check_dist(L, allreduced)) return rc;
+  return zero_dist_update_buckets(L, allreduced, 0, (int)L->bucket_tile_begin.size() - 1, stream);
 }
 
 }  // extern "C"

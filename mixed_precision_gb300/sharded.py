@@ -47,6 +47,11 @@ class TorchComm:
         """out (len) <- every rank's inp (len/W), in rank order."""
         self.dist.all_gather_into_tensor(out, inp, group=self.group)
 
+    def all_gather_async(self, out: torch.Tensor, inp: torch.Tensor):
+        """The same, started after the work already on the current stream and
+        running beside what is enqueued next; .wait() joins it."""
+        return self.dist.all_gather_into_tensor(out, inp, group=self.group, async_op=True)
+
 
 @dataclasses.dataclass
 class Bucket:
@@ -106,6 +111,11 @@ class LibraryShard:
     def update(self, allreduced) -> None:
         abi.zero_dist_update(self.z.handle, allreduced.data_ptr() if allreduced is not None else 0,
                              self._stream())
+
+    def update_buckets(self, first: int, count: int, allreduced) -> None:
+        abi.zero_dist_update_buckets(self.z.handle,
+                                     allreduced.data_ptr() if allreduced is not None else 0,
+                                     first, count, self._stream())
 
     def scaler_state(self) -> dict:
         st = abi.zero_loss_scale_state(self.z.handle, self._stream())
@@ -187,7 +197,9 @@ class ShardedZeroStep:
         `grads`, which then hold the summed gradient, or on the fp32 copy
         with an fp32 communication dtype). Then this rank's
         norm share, its all-reduce, the finalize, the local update, and the
-        all-gather of the parameters (stages 1/2)."""
+        all-gather of the parameters (stages 1/2), bucket by bucket with each
+        bucket's all-gather beside the next bucket's update when the
+        communicator can start one asynchronously."""
         W = self.world
         allreduced = None
         src = self.local.to_comm(grads)
@@ -203,8 +215,22 @@ class ShardedZeroStep:
         self.local.shard_norm(allreduced)
         self.comm.all_reduce(self.local.norm_pair)
         self.local.finalize(hp)
-        self.local.update(allreduced)
-        self.all_gather_params()
+        gather_async = getattr(self.comm, "all_gather_async", None)
+        if self.stage == 3 or gather_async is None:
+            self.local.update(allreduced)
+            self.all_gather_params()
+            return
+        # Bucket by bucket: bucket b's all-gather starts once its update is
+        # done and runs while bucket b + 1 is updated.
+        works = []
+        for i, b in enumerate(self.buckets):
+            self.local.update_buckets(i, 1, allreduced)
+            n = b.slice_len(W)
+            p = self.local.params
+            works.append(gather_async(p[b.start:b.start + b.length],
+                                      p[b.start + self.rank * n:b.start + (self.rank + 1) * n]))
+        for w in works:
+            w.wait()
 
     def all_gather_params(self) -> None:
         """Every rank's updated parameter slices into every rank's flat

@@ -94,6 +94,26 @@ class OracleShard:
         oracle.adamw(r, self.z.comm_dtype, self.hp, self.info, ms, mm, vv)
         self._cast_params()
 
+    def update_buckets(self, first: int, count: int, allreduced) -> None:
+        """The update of this rank's slices of buckets [first, first + count)
+        only (element-wise, so the same numbers as one whole update); only
+        their parameters are recast."""
+        if self.info.skipped or count == 0:
+            return
+        bs = self.z.buckets
+        lo = bs[first].local
+        hi = bs[first + count - 1].local + bs[first + count - 1].slice_len(self.z.world)
+        r = self._local_reduced(allreduced)[lo:hi]
+        ms, mm, vv = (bits(t)[lo:hi] for t in (self.master, self.m, self.v))
+        oracle.adamw(np.ascontiguousarray(r), self.z.comm_dtype, self.hp, self.info, ms, mm, vv)
+        enc = oracle.encode(bits(self.master)[lo:hi], self.z.param_dtype)
+        enc[~self.real[lo:hi]] = 0
+        p = bits(self.params)
+        if self.z.stage == 3:
+            p[lo:hi] = enc
+        else:
+            p[self.flat[lo:hi]] = enc
+
     def _cast_params(self) -> None:
         n = self.z.shard_elems
         enc = oracle.encode(bits(self.master)[:n], self.z.param_dtype)

@@ -80,5 +80,7 @@ def test_sharded_line_keys():
               "e2e", "gpu_launches", "clocks"):
         assert k in d, k
     assert d["n_gpus"] == 1 and d["steps"] == 3 and d["value"] > 0 and d["scaling"] == "strong"
-    assert d["config"]["parallelism"] == "zero2_dp1" and d["gpu_launches"] == 3 * 3
+    # per step: the shard norm, the finalize and one update per bucket (3 buckets
+    # of the Qwen3 list at 500 MB), each bucket's all-gather beside the next update
+    assert d["config"]["parallelism"] == "zero2_dp1" and d["gpu_launches"] == 3 * (2 + 3)
     assert d["e2e"]["h2d_bytes_per_step"] > 0 and d["e2e"]["d2h_bytes_per_step"] > 0
