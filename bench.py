@@ -42,7 +42,7 @@ NCU_TRAFFIC_PER_ELEM = {
     # update kernel, one block per tile (15,392 blocks), 8 Qwen3 layers,
     # 125,847,552 elements: (1.762588 + 1.701842) GB
     ("k_adamw_cast", "qwen3_0.6b_bf16_w2"): 27.529,
-    # reduce kernel, W=2, 1,216 blocks, the same slice: (0.504079 + 0.214297) GB
+    # reduce kernel, W=2, 1,824 blocks, the same slice: (0.504079 + 0.214297) GB
     ("k_reduce_norm", "qwen3_0.6b_bf16_w2"): 5.708,
     # update kernel, one block per tile (28,680 blocks), 2 MoE layers,
     # 234,946,560 elements: (3.290513 + 3.229704) GB
