@@ -429,8 +429,6 @@ def run_ours(args) -> dict | None:
 
     z = ZeroStep(w.shapes, w.world, w.stage, w.bucket_bytes, w.grad_dtype, w.param_dtype,
                  w.comm_dtype)
-    if args.speculative and w.stage == 1:
-        raise SystemExit("--speculative needs stage 2 or 3")
     z.allocate(speculative=args.speculative)
     info = z.info
     numel = wl.numels(w.shapes)
@@ -649,8 +647,9 @@ def run_ours(args) -> dict | None:
     k3_bytes = N * (C + 24 + P)
     k1_ms, k2_ms, k3_ms = statistics.mean(k1), statistics.mean(k2), statistics.mean(k3)
     if args.speculative and fast_path:
-        # events: [single pass] [its finalize] [guarded fallback kernels + restore]
-        spec_bytes = N * info.step_bytes_per_elem
+        # events: [single pass] [its finalize] [guarded fallback kernels + restore];
+        # in stage 1 the pass also writes the W all-reduce outputs
+        spec_bytes = N * (info.step_bytes_per_elem + (w.world * C if w.stage == 1 else 0))
         dom = ("k_spec_step", spec_bytes, k1_ms)
         kernels = {"k_spec_step": k1_ms, "between": k2_ms, "guarded_fallback": k3_ms,
                    "k_spec_step_gbs": spec_bytes / (k1_ms / 1e3) / 1e9}
@@ -737,6 +736,9 @@ PER_CONFIG = [
     # whole ledger (the default line's workload clips every step)
     ("qwen3_0.6b_bf16_w2", {"max_grad_norm": 0.0, "speculative": True}),
     ("moe_3.9b_bf16_w4", {"max_grad_norm": 0.0, "speculative": True}),
+    # ZeRO-1 at fp16 W=8, clip 1.0 (inactive there): the single pass also
+    # writes the W all-reduce outputs
+    ("qwen3_0.6b_fp16_w8", {"stage": 1, "speculative": True}),
     # the layout sweep's 2000 ragged tensors (1.69G elements): the flat step at
     # W = 2 and 8, and at W = 8 the same step launched tensor by tensor
     ("ragged_2000", {"world": 2}),
@@ -831,9 +833,10 @@ def time_config(name: str, over: dict, steps: int, warmup: int, local: int) -> d
         # events: [single pass, its finalize in its last block] [between]
         # [guarded fallback kernels: no-ops when the step committed]
         assert st["fast_path"] == 1, st
-        one_pass = b["ledger"]
+        one_pass = b["own"]  # the ledger, and in stage 1 the W all-reduce writes
         out = {
-            "config": config_of(w, "speculative single pass, clipping off"),
+            "config": config_of(w, "speculative single pass; clipping inactive, so every step "
+                                   "commits in one pass"),
             "steps": steps, "warmup": warmup,
             "ms_per_step": tm["total_ms"] / steps,
             "step_ms_median": tm["steps_ms"][steps // 2],
@@ -914,7 +917,9 @@ def per_config(steps: int, warmup: int, local: int) -> dict:
     """Every workload of PER_CONFIG, one after the other."""
     out = {}
     for name, over in PER_CONFIG:
-        if over.get("speculative"):
+        if over.get("speculative") and over.get("stage") == 1:
+            key = name + "_stage1_speculative"
+        elif over.get("speculative"):
             key = name + "_speculative_clip0"
         elif over.get("tensors"):
             key = name + "_tensors_idle_experts_null"

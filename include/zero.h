@@ -238,7 +238,7 @@ int zero_state_bind(zero_layout_t* layout, void* master, void* m, void* v, void*
  * which writes its result into whichever set is not current and then makes
  * that set current. zero_scaler_state.state_set tells which set holds the
  * current state; every other call (steps, export/import, gathers) follows it.
- * Stages 2 and 3 only. Call after zero_state_bind and before zero_state_init
+ * Any stage. Call after zero_state_bind and before zero_state_init
  * (the layout counts as not initialised afterwards; init makes set 0
  * current). Rebinding with zero_state_bind drops the alternate set.
  * Synchronous (queries the kernel's occupancy). */
@@ -342,19 +342,32 @@ int zero_step_per_tensor_launch(zero_layout_t* layout, const void* const* grads,
  * A committed step moves W*size(grad) + 24 + size(param) bytes per element,
  * the whole step's ledger; the reduced gradients are never stored, so the
  * scratch buffer's contents are unspecified afterwards.
- *   grads  flat gradients as for zero_step. Stages 2 and 3 only; needs
+ *   grads  flat gradients as for zero_step. Stages 2 and 3 (stage 1 through
+ *          zero_step_speculative_allreduce); needs
  *          zero_state_bind_alternate. Errors as zero_step. */
 int zero_step_speculative(zero_layout_t* layout, const void* const* grads, const zero_hparams* hp,
                           void* stream);
+
+/* The speculative step in any stage. allreduce_out as zero_step's: stage 1
+ * (ZeRO-1) takes W device pointers, Np elements of comm_dtype each, flat
+ * layout, and the single pass writes every rank's copy of the reduced
+ * gradient there on every step (committed, skipped or falling back), the
+ * values zero_step writes; stages 2 and 3 take NULL and behave as
+ * zero_step_speculative. A committed stage-1 step moves W*size(grad) + 24 +
+ * size(param) + W*size(comm) bytes per element. Errors as zero_step. */
+int zero_step_speculative_allreduce(zero_layout_t* layout, const void* const* grads,
+                                    void* const* allreduce_out, const zero_hparams* hp,
+                                    void* stream);
 
 /* The speculative step with gradients given per tensor, as zero_step_tensors
  * takes them: grad_ptrs is a host array of W * n_params device pointers
  * (grad_ptrs[w * n_params + p]), 16-byte aligned, NULL for an all-zero
  * gradient, which is never read. Results are those of zero_step_speculative
- * on flat buffers holding zeros there, bit for bit. The table is copied to
- * the device on `stream` before the call returns, so it is not capturable
- * into a CUDA graph (ZERO_ERR_INVALID on a capturing stream, nothing
- * enqueued). Errors as zero_step_tensors. */
+ * on flat buffers holding zeros there, bit for bit. Stages 2 and 3 (stage 1
+ * is refused: its all-reduce outputs are written from flat gradients). The
+ * table is copied to the device on `stream` before the call returns, so it
+ * is not capturable into a CUDA graph (ZERO_ERR_INVALID on a capturing
+ * stream, nothing enqueued). Errors as zero_step_tensors. */
 int zero_step_speculative_tensors(zero_layout_t* layout, const void* const* grad_ptrs,
                                   const zero_hparams* hp, void* stream);
 

@@ -95,6 +95,7 @@ def lib() -> ctypes.CDLL:
             "zero_state_init": [P, P, ctypes.POINTER(zero_scaler_cfg), P],
             "zero_state_bind_alternate": [P, P, P, P],
             "zero_step_speculative": [P, PP, ctypes.POINTER(zero_hparams), P],
+            "zero_step_speculative_allreduce": [P, PP, PP, ctypes.POINTER(zero_hparams), P],
             "zero_step_speculative_tensors": [P, PP, ctypes.POINTER(zero_hparams), P],
             "zero_step": [P, PP, PP, ctypes.POINTER(zero_hparams), P],
             "zero_step_tensors": [P, PP, PP, ctypes.POINTER(zero_hparams), P],
@@ -205,6 +206,13 @@ def zero_state_bind_alternate(layout: int, master2: int, m2: int, v2: int) -> No
 
 def zero_step_speculative(layout: int, grads, hp: zero_hparams, stream: int) -> None:
     _check(lib().zero_step_speculative(layout, _ptrs(grads), ctypes.byref(hp), stream or None))
+
+
+def zero_step_speculative_allreduce(layout: int, grads, allreduce_out, hp: zero_hparams,
+                                    stream: int) -> None:
+    _check(lib().zero_step_speculative_allreduce(
+        layout, _ptrs(grads), _ptrs(allreduce_out) if allreduce_out is not None else None,
+        ctypes.byref(hp), stream or None))
 
 
 def zero_step_speculative_tensors(layout: int, grad_ptrs, hp: zero_hparams, stream: int) -> None:

@@ -407,9 +407,10 @@ int launch_step(zero_layout* L, const GradSrc& src, void* const* allreduce_out,
 // clipping turned out active): the reduce, and the update (skipped unless the
 // fallback finalize cleared DevState::skip), which instead recasts the
 // parameters after an overflow (DevState::restore_params).
-int launch_step_spec(zero_layout* L, const GradSrc& src, const zero_hparams* hp, cudaStream_t s) {
+int launch_step_spec(zero_layout* L, const GradSrc& src, void* const* allreduce_out,
+                     const zero_hparams* hp, cudaStream_t s) {
   const int n_tiles = (int)L->tiles.size();
-  if (n_tiles == 0) return launch_step(L, src, nullptr, hp, s);
+  if (n_tiles == 0) return launch_step(L, src, allreduce_out, hp, s);
   // The latest finalize predicted clipping: the two-pass kernels, unguarded.
   // Not while the stream is being captured: a graph keeps the device-guarded
   // sequence, which decides on every replay.
@@ -418,7 +419,7 @@ int launch_step_spec(zero_layout* L, const GradSrc& src, const zero_hparams* hp,
     ZERO_CUDA(cudaStreamIsCapturing(s, &cs));
     if (cs == cudaStreamCaptureStatusNone) {
       Range r_hint("speculative step: predicted clipping, two-pass kernels");
-      return launch_step(L, src, nullptr, hp, s);
+      return launch_step(L, src, allreduce_out, hp, s);
     }
   }
   SpecArgs sa{};
@@ -427,6 +428,8 @@ int launch_step_spec(zero_layout* L, const GradSrc& src, const zero_hparams* hp,
   sa.world = L->world();
   sa.stage = L->cfg.stage;
   sa.src = src;
+  if (L->cfg.stage == 1)
+    for (int w = 0; w < L->world(); ++w) sa.out.base[w] = allreduce_out[w];
   state_sets(L, sa.master, sa.m, sa.v);
   sa.params = L->params;
   sa.state = L->d_state;
@@ -448,7 +451,7 @@ int launch_step_spec(zero_layout* L, const GradSrc& src, const zero_hparams* hp,
   const bool timing = L->timing;
   L->timing = false;
   Range r_fb("guarded two-pass fallback and restore");
-  int rc = launch_step(L, src, nullptr, hp, s, /*guarded=*/1);
+  int rc = launch_step(L, src, allreduce_out, hp, s, /*guarded=*/1);
   L->timing = timing;
   if (rc != ZERO_OK) return rc;
   // The parameter restore after an overflow: inside the guarded update (the
@@ -901,7 +904,6 @@ int zero_state_bind(zero_layout_t* L, void* master, void* m, void* v, void* para
 int zero_state_bind_alternate(zero_layout_t* L, void* master2, void* m2, void* v2) {
   if (int rc = check_ready(L, false)) return rc;
   if (int rc = check_not_sharded(L, "zero_state_bind_alternate")) return rc;
-  if (L->cfg.stage == 1) return fail(ZERO_ERR_INVALID, "the speculative step needs stage 2 or 3");
   if (master2 == nullptr || m2 == nullptr || v2 == nullptr)
     return fail(ZERO_ERR_INVALID, "master2/m2/v2 must not be NULL");
   if (!aligned16(master2) || !aligned16(m2) || !aligned16(v2))
@@ -920,7 +922,8 @@ int zero_state_bind_alternate(zero_layout_t* L, void* master2, void* m2, void* v
   }
   if (const char* v = std::getenv("ZERO_SPEC_BLOCKS_PER_SM")) bps_cap = std::atoi(v);
   const int chunk = spec_chunk(L->world(), L->cfg.grad_dtype, stage_bytes);
-  int bps = spec_blocks_per_sm(L->cfg.grad_dtype, L->comm_dtype, L->cfg.param_dtype, L->world(), chunk);
+  int bps = spec_blocks_per_sm(L->cfg.grad_dtype, L->comm_dtype, L->cfg.param_dtype, L->world(), chunk,
+                               L->cfg.stage == 1);
   if (bps <= 0) return fail(ZERO_ERR_CUDA, "speculative kernel occupancy query failed");
   if (bps_cap > 0) bps = std::min(bps, bps_cap);
   L->chunk_spec = chunk;
@@ -996,12 +999,14 @@ int zero_step(zero_layout_t* L, const void* const* grads, void* const* allreduce
   return launch_step(L, src, allreduce_out, hp, static_cast<cudaStream_t>(stream));
 }
 
-int zero_step_speculative(zero_layout_t* L, const void* const* grads, const zero_hparams* hp,
-                          void* stream) {
+int zero_step_speculative_allreduce(zero_layout_t* L, const void* const* grads,
+                                    void* const* allreduce_out, const zero_hparams* hp,
+                                    void* stream) {
   if (int rc = check_ready(L, true)) return rc;
   if (int rc = check_not_sharded(L, "zero_step_speculative")) return rc;
   if (int rc = check_hparams(hp)) return rc;
   if (L->master2 == nullptr) return fail(ZERO_ERR_STATE, "zero_state_bind_alternate has not been called");
+  if (int rc = check_allreduce(L, allreduce_out)) return rc;
   if (grads == nullptr) return fail(ZERO_ERR_INVALID, "grads is NULL");
   GradSrc src{};
   for (int w = 0; w < L->world(); ++w) {
@@ -1009,7 +1014,12 @@ int zero_step_speculative(zero_layout_t* L, const void* const* grads, const zero
       return fail(ZERO_ERR_INVALID, "grads[%d] is NULL or not 16-byte aligned", w);
     src.base[w] = grads[w];
   }
-  return launch_step_spec(L, src, hp, static_cast<cudaStream_t>(stream));
+  return launch_step_spec(L, src, allreduce_out, hp, static_cast<cudaStream_t>(stream));
+}
+
+int zero_step_speculative(zero_layout_t* L, const void* const* grads, const zero_hparams* hp,
+                          void* stream) {
+  return zero_step_speculative_allreduce(L, grads, nullptr, hp, stream);
 }
 
 int zero_step_speculative_tensors(zero_layout_t* L, const void* const* grad_ptrs,
@@ -1019,6 +1029,9 @@ int zero_step_speculative_tensors(zero_layout_t* L, const void* const* grad_ptrs
   if (int rc = check_not_sharded(L, "zero_step_speculative_tensors")) return rc;
   if (int rc = check_hparams(hp)) return rc;
   if (L->master2 == nullptr) return fail(ZERO_ERR_STATE, "zero_state_bind_alternate has not been called");
+  if (L->cfg.stage == 1)
+    return fail(ZERO_ERR_INVALID, "stage 1 writes the all-reduce outputs: use "
+                "zero_step_speculative_allreduce with flat gradients");
   if (grad_ptrs == nullptr) return fail(ZERO_ERR_INVALID, "grad_ptrs is NULL");
   const int64_t n = (int64_t)L->world() * L->n_params();
   for (int64_t i = 0; i < n; ++i) {
@@ -1034,7 +1047,7 @@ int zero_step_speculative_tensors(zero_layout_t* L, const void* const* grad_ptrs
   src.table = L->d_table;
   src.n_params = L->n_params();
   src.table_mode = 1;
-  return launch_step_spec(L, src, hp, s);
+  return launch_step_spec(L, src, nullptr, hp, s);
 }
 
 int zero_step_per_tensor_launch(zero_layout_t* L, const void* const* grads,

@@ -186,8 +186,9 @@ struct SpecArgs {  // arguments of k_spec_step
   const Tile* tiles;
   int n_tiles;
   int world;
-  int stage;  // 2 or 3 (3: parameters sharded)
+  int stage;  // 1, 2 or 3 (3: parameters sharded)
   GradSrc src;
+  RedBufs out;  // stage 1: the W all-reduce outputs (flat layout), written every step
   float* master[2];
   float* m[2];
   float* v[2];
@@ -207,7 +208,8 @@ constexpr int kSpecStageBytesHost = 32768;  // default bytes per pipeline stage
 int spec_chunk(int world, int grad_dtype, int stage_bytes);
 cudaError_t launch_spec(const SpecArgs* args, int grad_dtype, int comm_dtype, int param_dtype, int world,
                         int grid, cudaStream_t s);
-int spec_blocks_per_sm(int grad_dtype, int comm_dtype, int param_dtype, int world, int chunk);
+int spec_blocks_per_sm(int grad_dtype, int comm_dtype, int param_dtype, int world, int chunk,
+                       bool stage1);
 
 // Record a failure message for zero_last_error() and return `code` (for entry
 // points defined outside api.cpp).

@@ -42,8 +42,11 @@ __device__ __forceinline__ const GT* spec_grad_ptr(const GradSrc& src, const Til
 
 constexpr int kSpecStages = kSpecStagesHost;
 
-template <typename GT, typename CT, typename PT, int WT, int NC>
-__global__ void __launch_bounds__((NC + 1) * 32) k_spec_step(const __grid_constant__ SpecArgs a) {
+// S1: stage 1 (ZeRO-1), where the pass also writes every rank's copy of the
+// reduced gradient into the W all-reduce outputs (a.out), as the two-pass
+// reduce does.
+template <typename GT, typename CT, typename PT, int WT, int NC, bool S1>
+__device__ __forceinline__ void spec_body(const SpecArgs& a) {
   constexpr int S = kSpecStages;
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ __align__(8) uint64_t full[S];
@@ -211,6 +214,18 @@ __global__ void __launch_bounds__((NC + 1) * 32) k_spec_step(const __grid_consta
           }
           if (!fin) bad = 1u;
           add_group(ss, hi, lo, big, rf);
+          if constexpr (S1) {  // every rank's copy of the reduced gradient
+            if constexpr (sizeof(CT) == 4) {  // fp32: the reduced value is rf itself
+              for (int w = 0; w < W; ++w)
+                store4_f32(static_cast<float*>(a.out.base[w]) + tl.flat + cc + e, rf);
+            } else {
+              CT rq[4];
+#pragma unroll
+              for (int j = 0; j < 4; ++j) rq[j] = DT<CT>::from_f32(rf[j]);
+              for (int w = 0; w < W; ++w)
+                store4_raw(static_cast<CT*>(a.out.base[w]) + tl.flat + cc + e, rq);
+            }
+          }
           load4_smem(sp + e, p);
           load4_smem(sm + e, m);
           load4_smem(sv + e, v);
@@ -244,6 +259,8 @@ __global__ void __launch_bounds__((NC + 1) * 32) k_spec_step(const __grid_consta
       const float rf = DT<CT>::to_f32(rc);
       if (!DT<CT>::finite_bits(rc)) bad = 1u;
       big += (double)rf * (double)rf;
+      if constexpr (S1)
+        for (int w = 0; w < W; ++w) static_cast<CT*>(a.out.base[w])[tl.flat + cc + e] = rc;
       float p = src_master[so + e], m = src_m[so + e], v = src_v[so + e];
       sc.apply(rf, p, m, v);
       dst_master[so + e] = p;
@@ -278,29 +295,50 @@ __global__ void __launch_bounds__((NC + 1) * 32) k_spec_step(const __grid_consta
   }
 }
 
-template <typename GT, typename CT, typename PT>
+template <typename GT, typename CT, typename PT, int WT, int NC>
+__global__ void __launch_bounds__((NC + 1) * 32) k_spec_step(const __grid_constant__ SpecArgs a) {
+  spec_body<GT, CT, PT, WT, NC, false>(a);
+}
+
+// Stage 1: the all-reduce stores need registers of their own; two resident
+// blocks (what the 96 KB of stages allow) get the budget for them.
+template <typename GT, typename CT, typename PT, int WT, int NC>
+__global__ void __launch_bounds__((NC + 1) * 32, 2) k_spec_step_s1(const __grid_constant__ SpecArgs a) {
+  spec_body<GT, CT, PT, WT, NC, true>(a);
+}
+
+template <typename GT, typename CT, typename PT, int WT, bool S1>
+const void* spec_kernel_one() {
+  if constexpr (S1)
+    return reinterpret_cast<const void*>(&k_spec_step_s1<GT, CT, PT, WT, kRedConsumers>);
+  else
+    return reinterpret_cast<const void*>(&k_spec_step<GT, CT, PT, WT, kRedConsumers>);
+}
+
+template <typename GT, typename CT, typename PT, bool S1>
 const void* spec_kernel_w(int world) {
   switch (world) {
-    case 2: return reinterpret_cast<const void*>(&k_spec_step<GT, CT, PT, 2, kRedConsumers>);
-    case 4: return reinterpret_cast<const void*>(&k_spec_step<GT, CT, PT, 4, kRedConsumers>);
-    case 8: return reinterpret_cast<const void*>(&k_spec_step<GT, CT, PT, 8, kRedConsumers>);
-    default: return reinterpret_cast<const void*>(&k_spec_step<GT, CT, PT, 0, kRedConsumers>);
+    case 2: return spec_kernel_one<GT, CT, PT, 2, S1>();
+    case 4: return spec_kernel_one<GT, CT, PT, 4, S1>();
+    case 8: return spec_kernel_one<GT, CT, PT, 8, S1>();
+    default: return spec_kernel_one<GT, CT, PT, 0, S1>();
   }
 }
 
-template <typename GT, typename CT>
+template <typename GT, typename CT, bool S1>
 const void* spec_kernel_p(int param_dtype, int world) {
-  return param_dtype == kF16 ? spec_kernel_w<GT, CT, __half>(world)
-                             : spec_kernel_w<GT, CT, __nv_bfloat16>(world);
+  return param_dtype == kF16 ? spec_kernel_w<GT, CT, __half, S1>(world)
+                             : spec_kernel_w<GT, CT, __nv_bfloat16, S1>(world);
 }
 
-// The kernel instance for (grad dtype GT, comm dtype, param dtype, world).
-template <typename GT>
+// The kernel instance for (grad dtype GT, comm dtype, param dtype, world;
+// S1: stage 1).
+template <typename GT, bool S1>
 const void* spec_kernel_for(int comm_dtype, int param_dtype, int world) {
   switch (comm_dtype) {
-    case kF32: return spec_kernel_p<GT, float>(param_dtype, world);
-    case kF16: return spec_kernel_p<GT, __half>(param_dtype, world);
-    case kBF16: return spec_kernel_p<GT, __nv_bfloat16>(param_dtype, world);
+    case kF32: return spec_kernel_p<GT, float, S1>(param_dtype, world);
+    case kF16: return spec_kernel_p<GT, __half, S1>(param_dtype, world);
+    case kBF16: return spec_kernel_p<GT, __nv_bfloat16, S1>(param_dtype, world);
     default: return nullptr;
   }
 }

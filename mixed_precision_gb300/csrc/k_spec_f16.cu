@@ -3,6 +3,6 @@
 
 namespace zg {
 const void* spec_kernel_f16(int comm_dtype, int param_dtype, int world) {
-  return spec_kernel_for<__half>(comm_dtype, param_dtype, world);
+  return spec_kernel_for<__half, false>(comm_dtype, param_dtype, world);
 }
 }  // namespace zg

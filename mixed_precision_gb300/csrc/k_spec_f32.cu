@@ -3,6 +3,6 @@
 
 namespace zg {
 const void* spec_kernel_f32(int comm_dtype, int param_dtype, int world) {
-  return spec_kernel_for<float>(comm_dtype, param_dtype, world);
+  return spec_kernel_for<float, false>(comm_dtype, param_dtype, world);
 }
 }  // namespace zg

@@ -1,0 +1,10 @@
+// Speculative single-pass instances for __nv_bfloat16 gradients in stage 1 (ZeRO-1),
+// which also write the W all-reduce outputs (compiled apart from the other
+// stages' instances so that the build runs them in parallel).
+#include "k_spec.cuh"
+
+namespace zg {
+const void* spec_kernel_s1_bf16(int comm_dtype, int param_dtype, int world) {
+  return spec_kernel_for<__nv_bfloat16, true>(comm_dtype, param_dtype, world);
+}
+}  // namespace zg

@@ -560,12 +560,23 @@ namespace zg {
 const void* spec_kernel_f32(int comm_dtype, int param_dtype, int world);
 const void* spec_kernel_f16(int comm_dtype, int param_dtype, int world);
 const void* spec_kernel_bf16(int comm_dtype, int param_dtype, int world);
+const void* spec_kernel_s1_f32(int comm_dtype, int param_dtype, int world);
+const void* spec_kernel_s1_f16(int comm_dtype, int param_dtype, int world);
+const void* spec_kernel_s1_bf16(int comm_dtype, int param_dtype, int world);
 
-static const void* spec_kernel(int grad_dtype, int comm_dtype, int param_dtype, int world) {
+// stage1: the instance that also writes the W all-reduce outputs
+static const void* spec_kernel(int grad_dtype, int comm_dtype, int param_dtype, int world,
+                               bool stage1) {
   switch (grad_dtype) {
-    case kF32: return spec_kernel_f32(comm_dtype, param_dtype, world);
-    case kF16: return spec_kernel_f16(comm_dtype, param_dtype, world);
-    case kBF16: return spec_kernel_bf16(comm_dtype, param_dtype, world);
+    case kF32:
+      return stage1 ? spec_kernel_s1_f32(comm_dtype, param_dtype, world)
+                    : spec_kernel_f32(comm_dtype, param_dtype, world);
+    case kF16:
+      return stage1 ? spec_kernel_s1_f16(comm_dtype, param_dtype, world)
+                    : spec_kernel_f16(comm_dtype, param_dtype, world);
+    case kBF16:
+      return stage1 ? spec_kernel_s1_bf16(comm_dtype, param_dtype, world)
+                    : spec_kernel_bf16(comm_dtype, param_dtype, world);
     default: return nullptr;
   }
 }
@@ -586,15 +597,16 @@ static int spec_smem(int world, int grad_dtype, int chunk) {
 
 cudaError_t launch_spec(const SpecArgs* args, int grad_dtype, int comm_dtype, int param_dtype, int world,
                         int grid, cudaStream_t s) {
-  const void* f = spec_kernel(grad_dtype, comm_dtype, param_dtype, world);
+  const void* f = spec_kernel(grad_dtype, comm_dtype, param_dtype, world, args->stage == 1);
   if (f == nullptr) return cudaErrorInvalidValue;
   void* a[] = {const_cast<SpecArgs*>(args)};
   return launch_step_kernel(f, grid, (kRedConsumers + 1) * 32, a,
                             spec_smem(world, grad_dtype, args->chunk), s);
 }
 
-int spec_blocks_per_sm(int grad_dtype, int comm_dtype, int param_dtype, int world, int chunk) {
-  const void* f = spec_kernel(grad_dtype, comm_dtype, param_dtype, world);
+int spec_blocks_per_sm(int grad_dtype, int comm_dtype, int param_dtype, int world, int chunk,
+                       bool stage1) {
+  const void* f = spec_kernel(grad_dtype, comm_dtype, param_dtype, world, stage1);
   if (f == nullptr) return 0;
   const int smem = spec_smem(world, grad_dtype, chunk);
   if (cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)

@@ -62,7 +62,7 @@ class ZeroStep:
     def allocate(self, speculative: bool = False) -> None:
         """Allocate master/m/v, the flat params, the stage-2 scratch or the
         stage-1 all-reduce outputs, and bind them; with `speculative`, also a
-        second master/m/v set for step_speculative (stages 2 and 3)."""
+        second master/m/v set for step_speculative."""
         dev = self.device
         n = max(self.np, 8)  # an empty model still gets non-NULL buffers
         self.master = torch.empty(n, dtype=torch.float32, device=dev)
@@ -127,9 +127,15 @@ class ZeroStep:
 
     def step_speculative(self, grads, hp: Hparams, stream=None) -> None:
         """The step as one pass when clipping stays inactive and nothing
-        overflows (bit-identical to step); otherwise skip or two-pass fallback."""
-        abi.zero_step_speculative(self.handle, [g.data_ptr() for g in grads], hp.c(),
-                                  _stream_handle(stream))
+        overflows (bit-identical to step); otherwise skip or two-pass fallback.
+        Stage 1 also writes the all-reduce outputs, as step does."""
+        if self.stage == 1:
+            abi.zero_step_speculative_allreduce(self.handle, [g.data_ptr() for g in grads],
+                                                [t.data_ptr() for t in self.allreduce_out],
+                                                hp.c(), _stream_handle(stream))
+        else:
+            abi.zero_step_speculative(self.handle, [g.data_ptr() for g in grads], hp.c(),
+                                      _stream_handle(stream))
 
     def step_speculative_tensors(self, grads_per_rank, hp: Hparams, stream=None) -> None:
         """step_speculative from per-tensor gradients: grads_per_rank[w][p] is

@@ -157,9 +157,10 @@ class Pair:
         if not info.skipped:
             assert abs(gpu_state["clip_coef"] - info.clip_coef) <= 1e-6 * info.clip_coef
         # reduced values: bit-exact (a committed or skipped speculative step
-        # never stores them; its fallback does)
+        # never stores them in stages 2/3; its fallback does; in stage 1 the
+        # single pass writes the all-reduce outputs every step)
         spec_no_reduce = (self.last_mode or "").startswith("speculative") and (
-            gpu_state["fast_path"] or gpu_state["skipped"])
+            gpu_state["fast_path"] or gpu_state["skipped"]) and self.stage != 1
         if spec_no_reduce:
             pass
         elif self.stage != 1:

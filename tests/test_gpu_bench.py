@@ -43,7 +43,8 @@ def test_our_line_keys():
     assert set(pc) == {"moe_3.9b_bf16_w4_stage2", "qwen3_0.6b_fp16_w8_stage1",
                        "qwen3_0.6b_fp16_w8_stage2", "qwen3_0.6b_bf16_w2_speculative_clip0",
                        "moe_3.9b_bf16_w4_speculative_clip0", "ragged_2000_w2", "ragged_2000_w8",
-                       "ragged_2000_w8_per_tensor_launch", "moe_3.9b_bf16_w4_tensors_idle_experts_null"}
+                       "ragged_2000_w8_per_tensor_launch", "moe_3.9b_bf16_w4_tensors_idle_experts_null",
+                       "qwen3_0.6b_fp16_w8_stage1_speculative"}
     for name, c in pc.items():
         assert c["steps"] == 3 and c["ms_per_step"] > 0 and 0 < c["step_roofline"]["frac"] < 1.5
         base = name.rsplit("_stage", 1)[0].split("_speculative")[0].split("_tensors")[0]
@@ -56,6 +57,12 @@ def test_our_line_keys():
             assert k in c["clocks"], k
     for name in ("qwen3_0.6b_bf16_w2_speculative_clip0", "moe_3.9b_bf16_w4_speculative_clip0"):
         assert pc[name]["fast_path"] == 1 and pc[name]["config"]["clip"] == 0.0
+    # ZeRO-1 through the single pass: clip 1.0 stays inactive, every step commits,
+    # and its bytes count the all-reduce writes
+    s1s = pc["qwen3_0.6b_fp16_w8_stage1_speculative"]
+    assert s1s["fast_path"] == 1 and s1s["config"]["zero_stage"] == 1
+    assert s1s["step_roofline"]["bytes_per_param"] == \
+        pc["qwen3_0.6b_fp16_w8_stage1"]["step_roofline"]["bytes_per_param"]
     # the flat step against launching it tensor by tensor, same bytes
     assert "per-tensor" in pc["ragged_2000_w8_per_tensor_launch"]["config"]["note"]
     assert "note" not in pc["ragged_2000_w8"]["config"]

@@ -45,9 +45,9 @@ def draw(i: int) -> dict:
     clip = float(rng.choice([0.0, 1e-3, 1.0]))
     hp = Hparams(lr=float(rng.choice([1e-4, 1e-3])), weight_decay=float(rng.choice([0.0, 0.1])),
                  max_grad_norm=clip)
-    modes = ["flat", "tensors", "per_tensor_launch", "host"]
+    modes = ["flat", "tensors", "per_tensor_launch", "host", "speculative"]
     if stage != 1:
-        modes += ["speculative", "speculative_tensors"]
+        modes += ["speculative_tensors"]
     plan = [str(rng.choice(modes)) for _ in range(3)]
     inject = [bool(rng.random() < 0.25) for _ in range(3)]
     zero_params = [int(p) for p in rng.choice(n_t, size=n_t // 4, replace=False)]

@@ -53,6 +53,9 @@ def ragged_shapes(seed):
     (3, 2, wl.BF16, -1, wl.F16, 30_000),
     (5, 2, wl.F32, wl.BF16, wl.BF16, 100_000),
     (1, 2, wl.F16, -1, wl.F16, 50_000),
+    (2, 1, wl.BF16, -1, wl.BF16, 64_000),   # stage 1: the pass writes the all-reduce outputs
+    (8, 1, wl.F16, -1, wl.F16, 500_000_000),
+    (3, 1, wl.F16, wl.F32, wl.F16, 30_000),
 ])
 def test_every_branch_matches_oracle(monkeypatch, W, stage, gdt, cdt, pdt, bucket, hint):
     """Commit, overflow skip, clip fallback, and commits again, against the oracle.
@@ -196,7 +199,20 @@ def _assert_same(a, b, mask):
     for x, y in zip(a.current_state(), b.current_state()):
         assert torch.equal(x[mask].view(torch.int32), y[mask].view(torch.int32))
     assert torch.equal(a.params_flat.view(torch.int16), b.params_flat.view(torch.int16))
+    if a.stage == 1:  # every rank's all-reduce output, padding excluded
+        flat = _real_flat_mask(a)
+        for x, y in zip(a.allreduce_out, b.allreduce_out):
+            xi = x.view(torch.int32) if x.dtype == torch.float32 else x.view(torch.int16)
+            yi = y.view(torch.int32) if y.dtype == torch.float32 else y.view(torch.int16)
+            assert torch.equal(xi[flat], yi[flat])
     return sa
+
+
+def _real_flat_mask(z):
+    mask = torch.zeros(max(z.np, 8), dtype=torch.bool, device="cuda")
+    for off, n in zip(z.offsets, z.numels):
+        mask[off:off + n] = True
+    return mask
 
 
 @pytest.mark.parametrize("W,stage,gdt,pdt,cdt,shapes", [
@@ -207,6 +223,9 @@ def _assert_same(a, b, mask):
     (16, 2, wl.BF16, wl.BF16, -1, "ragged"),
     (64, 2, wl.BF16, wl.BF16, -1, "ragged"),
     (4, 2, wl.F32, wl.BF16, wl.BF16, "ragged"),
+    (8, 1, wl.F16, wl.F16, -1, "qwen"),
+    (3, 1, wl.BF16, wl.BF16, -1, "ragged"),
+    (2, 1, wl.F32, wl.BF16, wl.F32, "ragged"),
 ])
 def test_bit_identical_to_two_pass(W, stage, gdt, pdt, cdt, shapes):
     """The same inputs through both entry points, speculative steps
@@ -328,11 +347,18 @@ def test_needs_alternate_set_and_stage():
                          torch.empty_like(z.v))
     assert e.value.code == abi.ZERO_ERR_INVALID
     z.close()
+    # stage 1: the all-reduce outputs are required, and per-tensor pointers refused
     z1 = ZeroStep(shapes, 2, 1, 1 << 20, wl.BF16, wl.BF16)
-    z1.allocate()
+    z1.allocate(speculative=True)
+    z1.init(torch.zeros(max(z1.np, 8), device="cuda"))
+    g1 = z1.new_grad_buffers()
     with pytest.raises(ZeroError) as e:
-        z1.bind_alternate(*[torch.empty(max(z1.np, 8), device="cuda") for _ in range(3)])
+        abi.zero_step_speculative(z1.handle, [t.data_ptr() for t in g1], Hparams().c(), 0)
     assert e.value.code == abi.ZERO_ERR_INVALID
+    with pytest.raises(ZeroError) as e:
+        z1.step_speculative_tensors([[g[o:o + n] for o, n in zip(z1.offsets, z1.numels)]
+                                     for g in g1], Hparams())
+    assert e.value.code == abi.ZERO_ERR_INVALID and "stage 1" in str(e.value)
     z1.close()
 
 
@@ -353,19 +379,22 @@ class Guarded:
             bool((self.raw[GUARD + self.nbytes:] == PATTERN).all())
 
 
-@pytest.mark.parametrize("stage", [2, 3])
+@pytest.mark.parametrize("stage", [1, 2, 3])
 def test_no_write_outside_buffers(stage):
-    """Guard bands around both state sets, the parameters and the scratch
-    through commits, an overflow skip and a clip fallback."""
+    """Guard bands around both state sets, the parameters, the scratch and
+    (stage 1) the all-reduce outputs through commits, an overflow skip and a
+    clip fallback."""
     rng = np.random.default_rng(stage + 10)
     shapes = [(int(x),) for x in rng.integers(1, 20000, size=12)] + [(3,), (0,), (8191,), (8193,)]
     W = 3
     z = ZeroStep(shapes, W, stage, 40_000, wl.BF16, wl.BF16)
     n = z.np
     bufs = [Guarded(n, torch.float32) for _ in range(6)] + [Guarded(n, torch.bfloat16)
-                                                            for _ in range(2)]
-    z.bind(bufs[0].t, bufs[1].t, bufs[2].t, bufs[6].t, bufs[7].t)
+                                                            for _ in range(2 + W)]
+    z.bind(bufs[0].t, bufs[1].t, bufs[2].t, bufs[6].t, bufs[7].t if stage != 1 else None)
     z.bind_alternate(bufs[3].t, bufs[4].t, bufs[5].t)
+    if stage == 1:
+        z.allreduce_out = [g.t for g in bufs[8:8 + W]]
     numel = wl.numels(shapes)
     z.init(wl.master_init(z.offsets, numel, n, 0.02, 3, device="cuda"), init_scale=8.0, dynamic=True)
     rank, idx = wl.inject_position(numel, z.offsets, W, seed=3)
