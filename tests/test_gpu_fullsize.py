@@ -13,7 +13,8 @@ benchmark times, on sampled outputs (see _fullsize.py).
   launched tensor by tensor, which must also store the same reduced values.
 - The speculative step at full size, in the launch configuration
   `bench.py --speculative` times: fp16 W=8 (clipping inactive) commits, skips
-  on +inf and commits again; Qwen3 bf16 W=2 at clip 1.0 (clipping active)
+  on +inf and commits again, in stage 2 and in stage 1 (where the single pass
+  also writes the all-reduce outputs); Qwen3 bf16 W=2 at clip 1.0 (clipping active)
   falls back, then is predicted to. Sampled parity on every step.
 """
 import numpy as np
@@ -184,13 +185,14 @@ def test_fullsize_ragged_2000_flat_and_per_tensor_launch(world, bucket):
     zt.close()
 
 
-@pytest.mark.parametrize("name,plan", [
-    ("qwen3_0.6b_fp16_w8", ["commit", "skip", "commit"]),
-    ("qwen3_0.6b_bf16_w2", ["fallback", "predicted"]),
+@pytest.mark.parametrize("name,stage,plan", [
+    ("qwen3_0.6b_fp16_w8", 2, ["commit", "skip", "commit"]),
+    ("qwen3_0.6b_fp16_w8", 1, ["commit", "skip", "commit"]),  # also writes the all-reduce outputs
+    ("qwen3_0.6b_bf16_w2", 2, ["fallback", "predicted"]),
 ])
-def test_fullsize_speculative(name, plan):
+def test_fullsize_speculative(name, stage, plan):
     w = wl.workload(name)
-    z, numel, master0 = _setup(w, speculative=True)
+    z, numel, master0 = _setup(w, stage=stage, speculative=True)
     so = SampledOracle(z, numel, master0, sample_indices(z, numel, 100_000, 4), w.init_scale,
                        w.dynamic, w.growth_interval)
     del master0
@@ -206,7 +208,7 @@ def test_fullsize_speculative(name, plan):
         assert st["fast_path"] == (kind == "commit")
         assert st["skipped"] == (kind == "skip")
         info, red_at = so.step(g, hp)
-        so.check(st, info, red_at, reduced=kind in ("fallback", "predicted"))
+        so.check(st, info, red_at, reduced=stage == 1 or kind in ("fallback", "predicted"))
         if kind in ("fallback", "predicted"):
             assert st["clip_coef"] < 1.0
         del g
