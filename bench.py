@@ -58,6 +58,9 @@ NCU_TRAFFIC_PER_ELEM = {
     # update kernel's per-tensor pointer instance, 2 MoE layers with each
     # rank's idle experts NULL: (3.051415 + 3.230056) GB
     ("k_adamw_cast_table", "moe_3.9b_bf16_w4"): 26.736,
+    # the stage-1 single pass (all-reduce writes included), W=8, 2-byte
+    # gradients, 8 Qwen3 layers: (3.524556 + 3.723003) GB
+    ("k_spec_step_s1", "qwen3_0.6b_fp16_w8"): 57.590,
 }
 
 
@@ -665,7 +668,14 @@ def run_ours(args) -> dict | None:
                    "k_reduce_norm_gbs": k1_bytes / (k1_ms / 1e3) / 1e9,
                    "k_adamw_cast_gbs": k3_bytes / (k3_ms / 1e3) / 1e9}
     achieved = dom[1] / (dom[2] / 1e3) / 1e9
-    tr = NCU_TRAFFIC_PER_ELEM.get((dom[0], w.name))
+    # the capture of the instance that ran: the stage-1 single pass, or the
+    # per-tensor pointer update, has a key of its own
+    kname = dom[0]
+    if dom[0] == "k_spec_step" and w.stage == 1:
+        kname += "_s1"
+    elif dom[0] == "k_adamw_cast" and args.tensors:
+        kname += "_table"
+    tr = NCU_TRAFFIC_PER_ELEM.get((kname, w.name))
     sb = stage_bytes(w)
     # the stage's own bytes: the ledger, plus the all-reduce writes in stage 1
     step_gbs = sb["own"] * N / step_s / 1e9
@@ -852,7 +862,7 @@ def time_config(name: str, over: dict, steps: int, warmup: int, local: int) -> d
             "clocks": tm["clocks"],
         }
         achieved = one_pass * N / (k1_ms / 1e3) / 1e9
-        tr = NCU_TRAFFIC_PER_ELEM.get(("k_spec_step", w.name))
+        tr = NCU_TRAFFIC_PER_ELEM.get(("k_spec_step" + ("_s1" if w.stage == 1 else ""), w.name))
         out["roofline"] = {"bound": "hbm", "kernel": "k_spec_step", "achieved": achieved,
                            "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                            "traffic": tr * N if tr is not None else None,
