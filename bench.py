@@ -648,6 +648,9 @@ def run_ours(args) -> dict | None:
     P = wl.ELEM_BYTES[w.param_dtype]
     k1_bytes = N * (w.world * G + (w.world * C if w.stage == 1 else C))
     k3_bytes = N * (C + 24 + P)
+    if args.tensors:  # the update's per-tensor instance skips the idle tiles' gradient reads
+        idle = set.intersection(*[set(wl.zero_params(w, r)) for r in range(w.world)])
+        k3_bytes -= C * sum(wl.numels(w.shapes)[p] for p in idle)
     k1_ms, k2_ms, k3_ms = statistics.mean(k1), statistics.mean(k2), statistics.mean(k3)
     if args.speculative and fast_path:
         # events: [single pass] [its finalize] [guarded fallback kernels + restore];
