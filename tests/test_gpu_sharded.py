@@ -232,6 +232,12 @@ def test_sharded_layout_refuses_single_process_steps():
     with pytest.raises(ZeroError) as e:  # stages 2/3 read the bound scratch
         abi.zero_dist_update(z.handle, g.data_ptr(), stream)
     assert e.value.code == abi.ZERO_ERR_INVALID
+    nb = len(z.buckets)
+    for first, count in ((-1, 1), (0, nb + 1), (nb, 1), (1, -1)):  # outside the layout's buckets
+        with pytest.raises(ZeroError) as e:
+            abi.zero_dist_update_buckets(z.handle, 0, first, count, stream)
+        assert e.value.code == abi.ZERO_ERR_INVALID, (first, count)
+    abi.zero_dist_update_buckets(z.handle, 0, nb, 0, stream)  # an empty range enqueues nothing
     z.close()
     plain = ZeroStep(SHAPES, 1, 2, 24_000, wl.BF16, wl.BF16)
     plain.allocate()
