@@ -353,8 +353,11 @@ int zero_step_speculative(zero_layout_t* layout, const void* const* grads, const
  * layout, and the single pass writes every rank's copy of the reduced
  * gradient there on every step (committed, skipped or falling back), the
  * values zero_step writes; stages 2 and 3 take NULL and behave as
- * zero_step_speculative. A committed stage-1 step moves W*size(grad) + 24 +
- * size(param) + W*size(comm) bytes per element. Errors as zero_step. */
+ * zero_step_speculative. Unlike zero_step's, the outputs must not overlap
+ * the gradient buffers (ZERO_ERR_INVALID): a step that falls back reduces
+ * the gradients again after the single pass has written the outputs. A
+ * committed stage-1 step moves W*size(grad) + 24 + size(param) +
+ * W*size(comm) bytes per element. Errors as zero_step. */
 int zero_step_speculative_allreduce(zero_layout_t* layout, const void* const* grads,
                                     void* const* allreduce_out, const zero_hparams* hp,
                                     void* stream);

@@ -1014,6 +1014,21 @@ int zero_step_speculative_allreduce(zero_layout_t* L, const void* const* grads,
       return fail(ZERO_ERR_INVALID, "grads[%d] is NULL or not 16-byte aligned", w);
     src.base[w] = grads[w];
   }
+  if (L->cfg.stage == 1) {
+    // The single pass writes the outputs before the step's decision; a
+    // fallback then reduces the gradients again, so they must still hold
+    // every rank's own values: no output may overlap a gradient buffer.
+    const uintptr_t gb = (uintptr_t)L->np * dtype_bytes(L->cfg.grad_dtype);
+    const uintptr_t ob = (uintptr_t)L->np * dtype_bytes(L->comm_dtype);
+    for (int w = 0; w < L->world(); ++w)
+      for (int v = 0; v < L->world(); ++v) {
+        const uintptr_t o = reinterpret_cast<uintptr_t>(allreduce_out[w]);
+        const uintptr_t g = reinterpret_cast<uintptr_t>(grads[v]);
+        if (o < g + gb && g < o + ob)
+          return fail(ZERO_ERR_INVALID, "allreduce_out[%d] overlaps grads[%d]: the speculative "
+                      "step reduces the gradients again when it falls back", w, v);
+      }
+  }
   return launch_step_spec(L, src, allreduce_out, hp, static_cast<cudaStream_t>(stream));
 }
 

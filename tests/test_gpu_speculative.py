@@ -359,6 +359,14 @@ def test_needs_alternate_set_and_stage():
         z1.step_speculative_tensors([[g[o:o + n] for o, n in zip(z1.offsets, z1.numels)]
                                      for g in g1], Hparams())
     assert e.value.code == abi.ZERO_ERR_INVALID and "stage 1" in str(e.value)
+    # outputs overlapping the gradients (zero_step's in-place all-reduce) are
+    # refused: a fallback reduces the gradients again
+    for outs in ([g1[0], z1.allreduce_out[1]], [z1.allreduce_out[0], g1[1][8:]]):
+        with pytest.raises(ZeroError) as e:
+            abi.zero_step_speculative_allreduce(z1.handle, [t.data_ptr() for t in g1],
+                                                [t.data_ptr() for t in outs], Hparams().c(), 0)
+        assert e.value.code == abi.ZERO_ERR_INVALID and "overlaps" in str(e.value)
+    assert z1.scaler_state()["steps"] == 0  # nothing ran
     z1.close()
 
 
