@@ -204,8 +204,11 @@ __global__ void __launch_bounds__(kThreads, 4) k_reduce_norm(const __grid_consta
 // every tile alike. The consumers take a chunk of k * C elements as k
 // C-element stretches in order, with the warp slices of a C-element chunk,
 // so every thread adds the same groups to its norm partial in the same order
-// as in flat mode: the two modes give the same bits. The flat instance is
-// the same code with those branches compiled out.
+// as in flat mode: the two modes give the same bits. A tile whose ranks are
+// all NULL is stored as +0.0 without the sum and conversion work, its groups
+// still passed to the norm sum as +0.0 (a zero addend can change the
+// compensated sum's bits). The flat instance is the same code with those
+// branches compiled out.
 // ---------------------------------------------------------------------------
 template <typename GT, typename CT, int WT, bool STAGE1, int NC, bool TABLE>
 __device__ __forceinline__ void reduce_ws_body(const ReduceArgs& a) {
