@@ -238,7 +238,9 @@ struct UpdStage {
 // offsets in a descriptor beside it; NC consumer warps each update a fixed
 // slice of every chunk and release the stage by arriving on its "empty"
 // mbarrier. No block-wide barrier in the loop: consumer warps never wait for
-// one another, only for data.
+// one another, only for data. The table instance (the step from per-tensor
+// pointers) checks each tile's W pointers; where all are NULL the reduced
+// gradient is +0.0 (what the reduce stored), so it is not copied in.
 //
 // Tile scheduling. With a.tile_next (the default), the producer takes its
 // next tile from a device counter (atomicInc, one tile ahead of the one it
@@ -260,7 +262,8 @@ struct ChunkDesc {
   int64_t so;    // shard offset of the chunk (master, m, v)
   int64_t po;    // parameter offset (flat; stage 3: shard)
   int64_t ro;    // reduced-gradient offset (stage 1: flat; else shard)
-  int32_t rb;    // reduced-gradient buffer (stage 1: the tile's rank; else 0)
+  int32_t rb;    // reduced-gradient buffer (stage 1: the tile's rank; else 0);
+                 // -1 (table instance): every rank's gradient is NULL, take +0.0
   int32_t clen;  // elements in the chunk; -1: no more work
 };
 
