@@ -55,6 +55,12 @@ def _same(a, b, mask):
     for x, y in zip(a.current_state(), b.current_state()):
         assert torch.equal(x[mask].view(torch.int32), y[mask].view(torch.int32))
     assert torch.equal(a.params_flat.view(torch.int16), b.params_flat.view(torch.int16))
+    if a.stage == 1:  # the all-reduce outputs over real elements
+        flat = torch.zeros(max(a.np, 8), dtype=torch.bool, device="cuda")
+        for off, n in zip(a.offsets, a.numels):
+            flat[off:off + n] = True
+        for x, y in zip(a.allreduce_out, b.allreduce_out):
+            assert torch.equal(x.view(torch.int16)[flat], y.view(torch.int16)[flat])
     return sa
 
 
@@ -67,7 +73,8 @@ def _grads(z, W, gdt, step, sigma=1e-3, inf_at=None):
 
 
 @pytest.mark.parametrize("spec,stage,gdt", [(False, 2, wl.F16), (False, 3, wl.BF16),
-                                            (True, 2, wl.BF16), (True, 3, wl.F16)])
+                                            (True, 2, wl.BF16), (True, 3, wl.F16),
+                                            (False, 1, wl.BF16), (True, 1, wl.F16)])
 def test_captured_step_replays_like_eager(spec, stage, gdt):
     """Replays with clean gradients, an overflow, clipping switching on and
     off (speculative: commit, skip, fallback, predicted fallback) and scale
