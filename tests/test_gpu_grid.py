@@ -31,10 +31,10 @@ def _shapes():
     return [(1024, 1024)] * 12 + [(1000,), (3000, 7), (129, 257)]
 
 
-def _layout(monkeypatch, mult, W, gdt, spec):
+def _layout(monkeypatch, mult, W, gdt, spec, stage=2):
     for k in KNOBS:
         monkeypatch.setenv(k, str(mult))
-    z = ZeroStep(_shapes(), W, 2, 8_000_000, gdt, gdt)
+    z = ZeroStep(_shapes(), W, stage, 8_000_000, gdt, gdt)
     z.allocate(speculative=spec)
     master0 = wl.master_init(z.offsets, z.numels, z.np, 0.02, wl.master_seed(91), device="cuda")
     z.init(master0, init_scale=2.0 ** 12, dynamic=True, growth_interval=1000)
@@ -53,11 +53,12 @@ def _real_shard_mask(z):
     return mask
 
 
-@pytest.mark.parametrize("spec,W,gdt", [(False, 2, wl.BF16), (False, 8, wl.F16), (True, 2, wl.BF16),
-                                        (True, 4, wl.F16)])
-def test_grid_size_does_not_change_the_step(monkeypatch, spec, W, gdt):
-    small = _layout(monkeypatch, 1, W, gdt, spec)
-    large = _layout(monkeypatch, 64, W, gdt, spec)
+@pytest.mark.parametrize("spec,W,gdt,stage", [(False, 2, wl.BF16, 2), (False, 8, wl.F16, 2),
+                                              (True, 2, wl.BF16, 2), (True, 4, wl.F16, 2),
+                                              (False, 4, wl.BF16, 1), (True, 8, wl.F16, 1)])
+def test_grid_size_does_not_change_the_step(monkeypatch, spec, W, gdt, stage):
+    small = _layout(monkeypatch, 1, W, gdt, spec, stage)
+    large = _layout(monkeypatch, 64, W, gdt, spec, stage)
     mask = _real_shard_mask(small)
     rank, idx = wl.inject_position(small.numels, small.offsets, W, seed=17)
     hp = Hparams(max_grad_norm=1e9)
@@ -81,7 +82,14 @@ def test_grid_size_does_not_change_the_step(monkeypatch, spec, W, gdt):
             assert abs(sa["grad_norm"] - sb["grad_norm"]) <= 1e-6 * sb["grad_norm"]
             if spec:
                 assert sa["fast_path"] == sb["fast_path"]
-        if not spec:
+        if stage == 1:
+            # every rank's all-reduce output (written by the single pass too)
+            flat = torch.zeros(max(small.np, 8), dtype=torch.bool, device="cuda")
+            for off, n in zip(small.offsets, small.numels):
+                flat[off:off + n] = True
+            for x, y in zip(small.allreduce_out, large.allreduce_out):
+                assert torch.equal(x.view(torch.int16)[flat], y.view(torch.int16)[flat])
+        elif not spec:
             # the reduced gradients, rank-major like the state
             assert torch.equal(small.scratch[mask].view(torch.int16), large.scratch[mask].view(torch.int16))
         for x, y in zip(small.current_state(), large.current_state()):
