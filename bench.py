@@ -61,6 +61,9 @@ NCU_TRAFFIC_PER_ELEM = {
     # the stage-1 single pass (all-reduce writes included), W=8, 2-byte
     # gradients, 8 Qwen3 layers: (3.524556 + 3.723003) GB
     ("k_spec_step_s1", "qwen3_0.6b_fp16_w8"): 57.590,
+    # update kernel, one block per tile (19,763 blocks), the first 200 of the
+    # 2000 ragged tensors, 160,922,893 elements: (2.254052 + 2.193213) GB
+    ("k_adamw_cast", "ragged_2000"): 27.636,
 }
 
 
