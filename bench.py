@@ -64,6 +64,11 @@ NCU_TRAFFIC_PER_ELEM = {
     # update kernel, one block per tile (19,763 blocks), the first 200 of the
     # 2000 ragged tensors, 160,922,893 elements: (2.254052 + 2.193213) GB
     ("k_adamw_cast", "ragged_2000"): 27.636,
+    # fp16 W=8, 8 Qwen3 layers: the update (15,392 blocks), (1.762527 +
+    # 1.701489) GB; the stage-1 reduce with its W all-reduce writes (1,216
+    # blocks), (2.014353 + 1.962679) GB
+    ("k_adamw_cast", "qwen3_0.6b_fp16_w8"): 27.526,
+    ("k_reduce_norm_s1", "qwen3_0.6b_fp16_w8"): 31.602,
 }
 
 
@@ -677,7 +682,7 @@ def run_ours(args) -> dict | None:
     # the capture of the instance that ran: the stage-1 single pass, or the
     # per-tensor pointer update, has a key of its own
     kname = dom[0]
-    if dom[0] == "k_spec_step" and w.stage == 1:
+    if dom[0] in ("k_spec_step", "k_reduce_norm") and w.stage == 1:
         kname += "_s1"
     elif dom[0] == "k_adamw_cast" and args.tensors:
         kname += "_table"
@@ -917,7 +922,8 @@ def time_config(name: str, over: dict, steps: int, warmup: int, local: int) -> d
     dom, dom_ms, dom_b = (("k_adamw_cast", k3_ms, k3_b) if k3_ms >= k1_ms
                           else ("k_reduce_norm", k1_ms, b["k1"]))
     achieved = dom_b * N / (dom_ms / 1e3) / 1e9
-    tr = NCU_TRAFFIC_PER_ELEM.get((dom + ("_table" if tensors else ""), w.name))
+    suffix = "_table" if tensors else ("_s1" if dom == "k_reduce_norm" and w.stage == 1 else "")
+    tr = NCU_TRAFFIC_PER_ELEM.get((dom + suffix, w.name))
     out["roofline"] = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak,
                        "unit": "GB/s", "frac": achieved / peak,
                        "traffic": tr * N if tr is not None else None,

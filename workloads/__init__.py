@@ -132,6 +132,10 @@ def workload(name: str, **over) -> Workload:
         # 2.5 GB on the device; a profiling-sized case of the same kernels.
         w = Workload(name, qwen3_0_6b_shapes(layers=8)[1:-1], 2, 2, BF16, BF16, BF16, 500 * MB,
                      1e-4, index=6)
+    elif name == "qwen3_layers8_fp16_w8":
+        # the same 8 layers with the fp16 W=8 list's dtypes and loss scaling
+        w = Workload(name, qwen3_0_6b_shapes(layers=8)[1:-1], 8, 2, F16, F16, F16, 500 * MB, 1e-4,
+                     init_scale=2.0 ** 16, dynamic=True, index=9)
     elif name == "moe_layers2_bf16_w4":
         # 2 layers of the MoE list (attention, router, 16 experts each), no
         # embedding or head: 235M elements, about 5.6 GB on the device; a
